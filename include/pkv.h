@@ -1,0 +1,174 @@
+/*
+ * pkv.h -- C ABI of libpkv: attention over a paged KV cache on NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow the subject's web pages (cited by page title and section):
+ *  [FAPA] "Flash Attention与Paged Attention如何共同优化大模型推理？" (ipipp.com)
+ *         s2: tiled attention with a running max m and running sum l, old output
+ *             rescaled by exp(m_old - m_new), final division by l; the library
+ *             call's causal flag.  s3: pages of block_size tokens, cache shape
+ *             [num_blocks, 2, num_heads, block_size, head_dim], per-sequence page
+ *             table, each page's valid-token count.
+ *  [CHUNK] "企业官网建设流程全解析" (cf-1.com) s2.1: logical block = i / block_size,
+ *             physical block = block_table[logical], offset = i % block_size;
+ *             s2.3: one launch for the whole batch instead of one per request.
+ *  [ON2]  "为什么Attention是O(n²)" (answer.freetools.me): softmax(QK^T/sqrt(d_k))V
+ *             (mathematics section); prefill writes every prompt token's K/V into
+ *             the cache, a decode step attends one query to all cached K/V and
+ *             appends the new token's K/V (prefill / decode section); grouped-query
+ *             attention, several query heads sharing one KV head (GQA section).
+ *  [BLK]  "从一次压测翻车说起：分块 attention ..." (pwwt.cn) s3.3, s5.3: parallelise
+ *             over batch x head and over key/value blocks (here: split-KV with a
+ *             log-sum-exp merge instead of atomics); s3.4, s5.4: FP32 accumulation.
+ *
+ * Conventions shared by every call
+ *  - All data pointers are DEVICE pointers owned by the caller; the library never
+ *    allocates, frees or keeps them.  Every pointer must be 16-byte aligned.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL is
+ *    the legacy default stream).  A returned PKV_OK means the launch was queued.
+ *  - Arguments are validated on the host before anything is launched; an invalid
+ *    call returns an error and launches nothing.
+ *  - Values that live on the device (page ids, lengths) are range-checked by the
+ *    kernels: a bad one never faults, the affected token or tile is skipped or
+ *    read from page 0, and a sticky device error word records the first such
+ *    event (read it with pkv_get_device_error).
+ *  - Cache layout (row-major): cache[pb][kv][h][off][d] over
+ *    [num_blocks, 2, num_kv_heads, block_size, head_dim]; kv = 0 is K, 1 is V;
+ *    element offset ((((pb*2 + kv)*Hkv + h)*bs + off)*D + d).
+ *  - Query head h reads KV head h / (Hq / Hkv).
+ *  - Block tables are int32 [batch, max_blocks_per_seq]; entry [b][i / bs] holds
+ *    the page of token i of sequence b.  Unused entries are never read.
+ *  - Arithmetic: fp16 / bf16 inputs, FP32 products, sums and softmax; the output is
+ *    rounded once (round-to-nearest-even) to out_dtype.
+ *  - lse outputs are natural-log log-sum-exp of the scaled scores, FP32
+ *    (-inf for an empty context).
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,   /* null / misaligned pointer, negative size, inconsistent shapes */
+    PKV_ERR_UNSUPPORTED = 2,   /* head_dim, block_size, dtype or head grouping outside the supported set */
+    PKV_ERR_WORKSPACE = 3,     /* workspace missing or smaller than pkv_decode_workspace_size() */
+    PKV_ERR_CUDA = 4,          /* a CUDA runtime call failed (launch, attribute, sync) */
+    PKV_ERR_DEVICE_RANGE = 5,  /* device error word: a page id, table slot or length was out of range */
+    PKV_ERR_TIMEOUT = 6        /* device error word: a bounded wait inside a kernel expired */
+} pkv_status;
+
+typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_F32 = 2 } pkv_dtype;
+
+/* The paged KV cache [num_blocks, 2, num_kv_heads, block_size, head_dim] ([FAPA] s3).
+ * dtype is PKV_F16 or PKV_BF16.  Supported: head_dim 64 or 128; block_size a power
+ * of two in [8, 512]. */
+typedef struct {
+    void *ptr;
+    int num_blocks;
+    int num_kv_heads;
+    int block_size;
+    int head_dim;
+    pkv_dtype dtype;
+} pkv_cache;
+
+/* kv_cache_append -- write new tokens' K and V into their pages ([ON2] prefill /
+ * decode; [CHUNK] s2.1 addressing).
+ *   k_new, v_new      [num_new_tokens, Hkv, D] in the cache dtype, packed by
+ *                     sequence: sequence b owns rows cu_new_lens[b] .. cu_new_lens[b+1]-1.
+ *   cu_new_lens       int32 [batch+1], cu_new_lens[0] = 0, non-decreasing,
+ *                     cu_new_lens[batch] = num_new_tokens.
+ *   ctx_before        int32 [batch]: tokens already cached; the j-th new token of
+ *                     sequence b goes to position ctx_before[b] + j.
+ *   block_tables      int32 [batch, max_blocks_per_seq]; pages for every written
+ *                     position must already be assigned.
+ * The copy is bit-exact.  Positions whose table slot is beyond max_blocks_per_seq,
+ * or whose page id is outside [0, num_blocks), are skipped and flag
+ * PKV_ERR_DEVICE_RANGE.  Nothing else in the cache is modified. */
+pkv_status pkv_kv_cache_append(pkv_cache cache, const void *k_new, const void *v_new,
+                               const int *cu_new_lens, const int *ctx_before,
+                               const int *block_tables, int batch, int max_blocks_per_seq,
+                               int num_new_tokens, void *stream);
+
+/* Bytes of workspace pkv_paged_attn_decode needs for these sizes (0 is possible).
+ * num_splits as passed to pkv_paged_attn_decode (0 = automatic). */
+size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int block_size, int max_blocks_per_seq, int num_splits);
+
+/* Tokens per split that pkv_paged_attn_decode uses for these sizes (a multiple of
+ * its 64-token tile); a context of L tokens is cut into ceil(L / chunk) splits. */
+int pkv_decode_split_tokens(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                            int block_size, int max_blocks_per_seq, int num_splits);
+
+/* paged_attn_decode -- one query per sequence against its whole paged context
+ * ([ON2] decode; [FAPA] s2 online softmax, s3 paging; [BLK] s5.3 split over
+ * key/value blocks).
+ *   q             [batch, Hq, D] in the cache dtype.
+ *   context_lens  int32 [batch]: cached tokens of each sequence (0 allowed: the
+ *                 output is 0 and lse is -inf); must not exceed
+ *                 max_blocks_per_seq * block_size (else flagged and clamped).
+ *   scale         multiplies q.k (1/sqrt(D) for the textbook definition).
+ *   num_splits    0 = automatic; else the context capacity
+ *                 max_blocks_per_seq * block_size is cut into this many splits.
+ *   workspace     device scratch of at least pkv_decode_workspace_size() bytes
+ *                 (FP32 partial outputs and their lse); contents need no init.
+ *   out           [batch, Hq, D] in out_dtype (the cache dtype or PKV_F32).
+ *   lse           FP32 [batch, Hq] or NULL.
+ * Launches the split kernel and, when some context spans several splits, the
+ * merge of pkv_attn_combine on the same stream. */
+pkv_status pkv_paged_attn_decode(pkv_cache cache, const void *q, int num_q_heads,
+                                 const int *block_tables, const int *context_lens, int batch,
+                                 int max_blocks_per_seq, float scale, int num_splits,
+                                 void *workspace, size_t workspace_bytes,
+                                 void *out, pkv_dtype out_dtype, float *lse, void *stream);
+
+/* paged_attn_prefill -- a chunk of queries per sequence against its paged context,
+ * causal or not ([ON2] prefill; [FAPA] s2 causal flag; [BLK] s2.2 chunked queries).
+ * "Append first, then attend": the chunk's own K/V must already be in the cache.
+ *   q             [total_q, Hq, D] in the cache dtype, packed by sequence:
+ *                 sequence b owns rows cu_q_lens[b] .. cu_q_lens[b+1]-1.
+ *   cu_q_lens     int32 [batch+1] (q_len_b = cu_q_lens[b+1] - cu_q_lens[b]).
+ *   context_lens  int32 [batch]: tokens in the cache INCLUDING the chunk, with
+ *                 q_len_b <= context_lens[b].
+ *   causal        non-zero: query r of sequence b sits at absolute position
+ *                 context_lens[b] - q_len_b + r and sees keys 0 .. that position
+ *                 (bottom-right alignment); zero: every query sees the whole context.
+ *   max_q_len     an upper bound of q_len_b over the batch (sizes the grid).
+ *   out           [total_q, Hq, D] in out_dtype; lse FP32 [total_q, Hq] or NULL. */
+pkv_status pkv_paged_attn_prefill(pkv_cache cache, const void *q, int num_q_heads,
+                                  const int *cu_q_lens, const int *context_lens,
+                                  const int *block_tables, int batch, int max_blocks_per_seq,
+                                  int total_q, int max_q_len, float scale, int causal,
+                                  void *out, pkv_dtype out_dtype, float *lse, void *stream);
+
+/* attn_combine -- log-sum-exp merge of split-KV partial results ([FAPA] s2: the
+ * same rescale-by-exp(m_old - m_new) identity applied to whole splits).
+ *   partial_o     FP32 [n_rows, num_splits, head_dim]: each split's output,
+ *                 already divided by that split's own softmax sum.
+ *   partial_lse   FP32 [n_rows, num_splits]: natural-log lse of each split's
+ *                 scaled scores; -inf marks an empty split (weight 0).
+ *   out           [n_rows, head_dim] in out_dtype; lse FP32 [n_rows] or NULL.
+ * A row whose splits are all empty gets output 0 and lse -inf. */
+pkv_status pkv_attn_combine(const float *partial_o, const float *partial_lse, int n_rows,
+                            int num_splits, int head_dim, void *out, pkv_dtype out_dtype,
+                            float *lse, void *stream);
+
+/* Synchronise `stream`, then read and clear the sticky device error word of the
+ * current device.  *code receives PKV_OK, PKV_ERR_DEVICE_RANGE or PKV_ERR_TIMEOUT.
+ * Returns PKV_ERR_CUDA if the synchronisation or the read fails. */
+pkv_status pkv_get_device_error(void *stream, int *code);
+
+/* Human-readable name of a status code (static storage). */
+const char *pkv_status_string(pkv_status status);
+
+/* Library ABI version (major * 100 + minor). */
+int pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

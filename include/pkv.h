@@ -47,6 +47,13 @@
 
 #include <stddef.h>
 
+/* Exported symbols (the library is built with hidden visibility by default). */
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -88,19 +95,19 @@ typedef struct {
  * The copy is bit-exact.  Positions whose table slot is beyond max_blocks_per_seq,
  * or whose page id is outside [0, num_blocks), are skipped and flag
  * PKV_ERR_DEVICE_RANGE.  Nothing else in the cache is modified. */
-pkv_status pkv_kv_cache_append(pkv_cache cache, const void *k_new, const void *v_new,
+PKV_API pkv_status pkv_kv_cache_append(pkv_cache cache, const void *k_new, const void *v_new,
                                const int *cu_new_lens, const int *ctx_before,
                                const int *block_tables, int batch, int max_blocks_per_seq,
                                int num_new_tokens, void *stream);
 
 /* Bytes of workspace pkv_paged_attn_decode needs for these sizes (0 is possible).
  * num_splits as passed to pkv_paged_attn_decode (0 = automatic). */
-size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+PKV_API size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim,
                                  int block_size, int max_blocks_per_seq, int num_splits);
 
 /* Tokens per split that pkv_paged_attn_decode uses for these sizes (a multiple of
  * its 64-token tile); a context of L tokens is cut into ceil(L / chunk) splits. */
-int pkv_decode_split_tokens(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+PKV_API int pkv_decode_split_tokens(int batch, int num_q_heads, int num_kv_heads, int head_dim,
                             int block_size, int max_blocks_per_seq, int num_splits);
 
 /* paged_attn_decode -- one query per sequence against its whole paged context
@@ -119,7 +126,7 @@ int pkv_decode_split_tokens(int batch, int num_q_heads, int num_kv_heads, int he
  *   lse           FP32 [batch, Hq] or NULL.
  * Launches the split kernel and, when some context spans several splits, the
  * merge of pkv_attn_combine on the same stream. */
-pkv_status pkv_paged_attn_decode(pkv_cache cache, const void *q, int num_q_heads,
+PKV_API pkv_status pkv_paged_attn_decode(pkv_cache cache, const void *q, int num_q_heads,
                                  const int *block_tables, const int *context_lens, int batch,
                                  int max_blocks_per_seq, float scale, int num_splits,
                                  void *workspace, size_t workspace_bytes,
@@ -138,7 +145,7 @@ pkv_status pkv_paged_attn_decode(pkv_cache cache, const void *q, int num_q_heads
  *                 (bottom-right alignment); zero: every query sees the whole context.
  *   max_q_len     an upper bound of q_len_b over the batch (sizes the grid).
  *   out           [total_q, Hq, D] in out_dtype; lse FP32 [total_q, Hq] or NULL. */
-pkv_status pkv_paged_attn_prefill(pkv_cache cache, const void *q, int num_q_heads,
+PKV_API pkv_status pkv_paged_attn_prefill(pkv_cache cache, const void *q, int num_q_heads,
                                   const int *cu_q_lens, const int *context_lens,
                                   const int *block_tables, int batch, int max_blocks_per_seq,
                                   int total_q, int max_q_len, float scale, int causal,
@@ -152,20 +159,20 @@ pkv_status pkv_paged_attn_prefill(pkv_cache cache, const void *q, int num_q_head
  *                 scaled scores; -inf marks an empty split (weight 0).
  *   out           [n_rows, head_dim] in out_dtype; lse FP32 [n_rows] or NULL.
  * A row whose splits are all empty gets output 0 and lse -inf. */
-pkv_status pkv_attn_combine(const float *partial_o, const float *partial_lse, int n_rows,
+PKV_API pkv_status pkv_attn_combine(const float *partial_o, const float *partial_lse, int n_rows,
                             int num_splits, int head_dim, void *out, pkv_dtype out_dtype,
                             float *lse, void *stream);
 
 /* Synchronise `stream`, then read and clear the sticky device error word of the
  * current device.  *code receives PKV_OK, PKV_ERR_DEVICE_RANGE or PKV_ERR_TIMEOUT.
  * Returns PKV_ERR_CUDA if the synchronisation or the read fails. */
-pkv_status pkv_get_device_error(void *stream, int *code);
+PKV_API pkv_status pkv_get_device_error(void *stream, int *code);
 
 /* Human-readable name of a status code (static storage). */
-const char *pkv_status_string(pkv_status status);
+PKV_API const char *pkv_status_string(pkv_status status);
 
 /* Library ABI version (major * 100 + minor). */
-int pkv_version(void);
+PKV_API int pkv_version(void);
 
 #ifdef __cplusplus
 }

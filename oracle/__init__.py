@@ -84,12 +84,12 @@ def _u16(a) -> np.ndarray:
         return np.ascontiguousarray(a)
     import torch
     assert a.dtype in (torch.float16, torch.bfloat16, torch.int16, torch.uint16)
-    return np.ascontiguousarray(a.contiguous().view(torch.int16).numpy().view(np.uint16))
+    return np.ascontiguousarray(a.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
 
 
 def _i32(a) -> np.ndarray:
     if not isinstance(a, np.ndarray):
-        a = a.numpy()
+        a = a.detach().cpu().numpy()
     return np.ascontiguousarray(a, dtype=np.int32)
 
 

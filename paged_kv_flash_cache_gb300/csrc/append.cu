@@ -1,0 +1,108 @@
+// append.cu -- kv_cache_append: scatter new tokens' K and V rows into their pages.
+//
+// A decode step appends the new token's K and V to the cache and prefill stores every
+// prompt token's K and V ("为什么Attention是O(n²)", prefill / decode section); token i of a
+// sequence lives in page block_table[i / block_size] at offset i % block_size
+// ("企业官网建设流程全解析", section 2.1) of the cache [num_blocks, 2, num_heads, block_size,
+// head_dim] ("Flash Attention与Paged Attention如何共同优化大模型推理？", section 3).
+//
+// One warp per new token: the warp resolves (sequence, position, page) once, then moves the
+// token's Hkv x D K row-set and V row-set as 16-byte vectors.  Reads of k_new / v_new are
+// contiguous; each destination head row (D elements) is a contiguous 128 / 256-byte run.
+// Pure bandwidth: 2 reads + 2 writes of Hkv * D * 2 bytes per token.
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kAppendThreads = 256;
+constexpr int kUnroll = 4;
+
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kAppendThreads) append_kernel(AppendArgs a) {
+    constexpr int kVecPerRow = D / 8;  // 16-byte vectors per head row
+    const int lane = threadIdx.x & 31;
+    const int warps_total = gridDim.x * (kAppendThreads / 32);
+    const int hkv = a.num_kv_heads;
+    const int vec_per_token = hkv * kVecPerRow;
+    const uint4 *kn = static_cast<const uint4 *>(a.k_new);
+    const uint4 *vn = static_cast<const uint4 *>(a.v_new);
+    uint4 *cache = static_cast<uint4 *>(a.cache);
+    // vectors between consecutive heads / between K and V of one page
+    const size_t head_stride = (size_t)a.block_size * kVecPerRow;
+    const size_t kv_stride = (size_t)hkv * head_stride;
+
+    for (int t = blockIdx.x * (kAppendThreads / 32) + (threadIdx.x >> 5); t < a.num_new_tokens; t += warps_total) {
+        // sequence of token t: last b with cu_new_lens[b] <= t
+        int lo = 0, hi = a.batch;  // answer in [lo, hi)
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (__ldg(a.cu_new_lens + mid) <= t) lo = mid; else hi = mid;
+        }
+        const int b = lo;
+        const long long pos = (long long)__ldg(a.ctx_before + b) + (t - __ldg(a.cu_new_lens + b));
+        const long long logical = pos >> a.log2_block_size;
+        if (pos < 0 || logical >= a.max_blocks_per_seq) {
+            if (lane == 0) set_error(a.err, kErrDeviceRange);
+            continue;
+        }
+        const int pb = __ldg(a.block_tables + (size_t)b * a.max_blocks_per_seq + logical);
+        if (pb < 0 || pb >= a.num_blocks) {
+            if (lane == 0) set_error(a.err, kErrDeviceRange);
+            continue;
+        }
+        const int off = (int)(pos & (a.block_size - 1));
+        const size_t page_base = (size_t)pb * 2 * kv_stride + (size_t)off * kVecPerRow;
+        const uint4 *ks = kn + (size_t)t * vec_per_token;
+        const uint4 *vs = vn + (size_t)t * vec_per_token;
+        for (int c0 = lane; c0 < vec_per_token; c0 += 32 * kUnroll) {
+            uint4 kv[kUnroll], vv[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int c = c0 + u * 32;
+                if (c < vec_per_token) {
+                    kv[u] = ld_stream(ks + c);
+                    vv[u] = ld_stream(vs + c);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int c = c0 + u * 32;
+                if (c < vec_per_token) {
+                    const int h = c / kVecPerRow;
+                    const int e = c - h * kVecPerRow;
+                    const size_t dst = page_base + (size_t)h * head_stride + e;
+                    cache[dst] = kv[u];
+                    cache[dst + kv_stride] = vv[u];
+                }
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_append(const AppendArgs &a, cudaStream_t s) {
+    if (a.num_new_tokens == 0 || a.batch == 0) return cudaSuccess;
+    const int warps_per_cta = kAppendThreads / 32;
+    const int want = (a.num_new_tokens + warps_per_cta - 1) / warps_per_cta;
+    const int cap = device_info().num_sms * 8;
+    const int grid = want < cap ? want : cap;
+    if (a.head_dim == 128) {
+        append_kernel<128><<<grid, kAppendThreads, 0, s>>>(a);
+    } else {
+        append_kernel<64><<<grid, kAppendThreads, 0, s>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

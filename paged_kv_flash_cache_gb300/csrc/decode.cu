@@ -1,0 +1,493 @@
+// decode.cu -- paged_attn_decode (split-KV, online softmax) and the split merge.
+//
+// What it computes: for each sequence b and query head h, softmax(q.K^T * scale) V over the
+// sequence's cached tokens ("为什么Attention是O(n²)", mathematics section), reading K/V
+// through the block table ("企业官网建设流程全解析", section 2.1; cache layout of
+// "Flash Attention与Paged Attention如何共同优化大模型推理？", section 3) with the running-max /
+// running-sum update of that page's section 2: new max m', old sum and output scaled by
+// exp(m - m'), final division by the sum.  Contexts are cut into splits of `chunk` tokens so a
+// small batch still fills every SM (parallelism over key/value blocks, "从一次压测翻车说起",
+// sections 3.3 and 5.3); split results are merged by their log-sum-exp instead of atomics.
+//
+// Kernel structure (one persistent CTA per SM slot):
+//   * work unit = (sequence, KV head, split); units are numbered in a prologue from the
+//     context lengths (block-wide scan) and dealt round-robin to the CTAs;
+//   * warp 4 (producer) streams each unit's tokens in 64-token tiles into a ring of
+//     shared-memory stages with bulk copies (TMA engine, one copy per page slice of K and of
+//     V -- pages are contiguous [block_size, D] rows), completion on an mbarrier;
+//   * warps 0-3 (consumers) each take 16 tokens of a tile: lanes split D into 16-byte
+//     chunks, q.k partial sums are reduced with xor shuffles, and every lane keeps running
+//     (m, l, acc) for all query heads of the GQA group, so each K/V byte is read from HBM
+//     exactly once per KV head;
+//   * at the end of a unit the states are merged (shuffles within a warp, shared memory
+//     across warps): a single-split context writes the final output, otherwise the split's
+//     normalised output and lse go to the workspace for the merge kernel.
+#include <type_traits>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
+constexpr int kStages = 4;
+constexpr int kMaxBatch = 2048;  // context lengths + unit prefix kept in shared memory
+
+template <int D, int G>
+struct DecodeLayout {
+    static constexpr int kTile = kDecodeTile;
+    static constexpr int kTokPerWarp = kTile / kConsumerWarps;      // 16
+    static constexpr int kLanesPerTok = D / 8;                      // 16 (D=128) or 8 (D=64)
+    static constexpr int kTokPerStep = 32 / kLanesPerTok;           // 2 or 4
+    static constexpr int kSteps = kTokPerWarp / kTokPerStep;        // 8 or 4
+    static constexpr int kStepsPerBatch = (kSteps * G <= 32) ? kSteps : (32 / G);  // bounds registers
+    static constexpr size_t kKBytes = (size_t)kTile * D * 2;
+    static constexpr size_t kQBytes = (size_t)G * D * 2;
+    static constexpr size_t kStageBytes = ((2 * kKBytes + kQBytes) + 127) / 128 * 128;
+    static constexpr size_t kMergeFloats = (size_t)kConsumerWarps * G * (D + 2);
+    static constexpr size_t kBarOffset = kStages * kStageBytes;
+    static constexpr size_t kMergeOffset = kBarOffset + 2 * kStages * 8 + 16;  // + abort flag
+    static constexpr size_t kIntsOffset = kMergeOffset + kMergeFloats * 4;
+    static size_t smem_bytes(int batch) { return kIntsOffset + (size_t)(2 * batch + 2 + 64) * 4; }
+};
+
+struct UnitCursor {
+    int b, kvh, split, t0, t1;
+};
+
+// Unit u -> (b, kv head, split); prefix[b] = units of sequences < b, units ordered with the KV
+// head fastest so consecutive CTAs share block-table rows.
+__device__ __forceinline__ UnitCursor unit_of(int u, const int *prefix, const int *lens, int batch, int hkv,
+                                              int chunk) {
+    int lo = 0, hi = batch;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (prefix[mid] <= u) lo = mid; else hi = mid;
+    }
+    UnitCursor c;
+    c.b = lo;
+    const int r = u - prefix[lo];
+    c.kvh = r % hkv;
+    c.split = r / hkv;
+    c.t0 = c.split * chunk;
+    const int end = c.t0 + chunk;
+    c.t1 = end < lens[lo] ? end : lens[lo];
+    return c;
+}
+
+template <typename Tag, int D, int G>
+__global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeArgs a) {
+    using L = DecodeLayout<D, G>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kBarOffset);
+    uint64_t *empty = full + kStages;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + kStages);
+    float *merge = reinterpret_cast<float *>(smem + L::kMergeOffset);
+    int *lens = reinterpret_cast<int *>(smem + L::kIntsOffset);
+    int *prefix = lens + a.batch;          // [batch + 1]
+    int *scan_tmp = prefix + a.batch + 1;  // [kDecodeThreads / 32]
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int hkv = a.cache.num_kv_heads, bs = a.cache.block_size, chunk = a.chunk;
+    const int cap = a.max_blocks_per_seq * bs;
+
+    if (tid == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kConsumerWarps);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    // ---- prologue: clamp lengths, units per sequence, exclusive scan (all threads) ----
+    const int per = (a.batch + kDecodeThreads - 1) / kDecodeThreads;
+    const int i0 = tid * per;
+    int local = 0;
+    for (int i = i0; i < i0 + per && i < a.batch; ++i) {
+        int len = __ldg(a.context_lens + i);
+        if (len < 0 || len > cap) {
+            set_error(a.err, kErrDeviceRange);
+            len = len < 0 ? 0 : cap;
+        }
+        lens[i] = len;
+        local += ((len + chunk - 1) / chunk) * hkv;
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) scan_tmp[warp] = incl;
+    __syncthreads();
+    int warp_base = 0;
+    for (int w = 0; w < warp; ++w) warp_base += scan_tmp[w];
+    int run = warp_base + incl - local;
+    for (int i = i0; i < i0 + per && i < a.batch; ++i) {
+        prefix[i] = run;
+        run += ((lens[i] + chunk - 1) / chunk) * hkv;
+    }
+    if (tid == kDecodeThreads - 1) prefix[a.batch] = warp_base + incl;
+    __syncthreads();
+    const int num_units = prefix[a.batch];
+
+    if (warp == kConsumerWarps) {
+        // ================================ producer warp ================================
+        const uint64_t pol = l2_policy_evict_first();
+        const uint16_t *cache = static_cast<const uint16_t *>(a.cache.ptr);
+        const uint16_t *qg = static_cast<const uint16_t *>(a.q);
+        const size_t head_elems = (size_t)bs * D;
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued_mask = 0;  // stages with copies issued (bit i), for the abort drain
+        uint32_t issued_parity = 0;
+        for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+            const UnitCursor c = unit_of(u, prefix, lens, a.batch, hkv, chunk);
+            const int *bt = a.block_tables + (size_t)c.b * a.max_blocks_per_seq;
+            for (int ts = c.t0; ts < c.t1; ts += L::kTile) {
+                const int n = min(L::kTile, c.t1 - ts);
+                const int first_page = ts >> a.cache.log2_block_size;
+                const int last_page = (ts + n - 1) >> a.cache.log2_block_size;
+                const int npages = last_page - first_page + 1;  // <= 64/bs, or 1
+                // page id of this lane's slice, fetched before waiting for the stage
+                int pb = 0;
+                if (lane < npages) {
+                    pb = __ldg(bt + first_page + lane);
+                    if (pb < 0 || pb >= a.cache.num_blocks) {
+                        set_error(a.err, kErrDeviceRange);
+                        pb = 0;
+                    }
+                }
+                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.err)) {
+                    // Stop issuing; let copies already in flight land before the CTA exits
+                    // (each wait is bounded again).
+                    for (int i = 0; i < kStages; ++i) {
+                        if (issued_mask & (1u << i)) {
+                            volatile int no_abort = 0;
+                            mbar_wait(&full[i], (issued_parity >> i) & 1u, &no_abort, nullptr);
+                        }
+                    }
+                    return;
+                }
+                uint8_t *st = smem + (size_t)stage * L::kStageBytes;
+                const bool first_tile = (ts == c.t0);
+                if (lane == 0) {
+                    const uint32_t bytes = (uint32_t)n * D * 2 * 2 + (first_tile ? (uint32_t)L::kQBytes : 0u);
+                    mbar_arrive_expect_tx(&full[stage], bytes);
+                }
+                __syncwarp();
+                if (lane < npages) {
+                    const int lp = first_page + lane;
+                    const int tok_lo = max(ts, lp * bs);
+                    const int tok_hi = min(ts + n, (lp + 1) * bs);
+                    const int off = tok_lo - lp * bs;
+                    const uint32_t bytes = (uint32_t)(tok_hi - tok_lo) * D * 2;
+                    const size_t kbase = (((size_t)pb * 2) * hkv + c.kvh) * head_elems + (size_t)off * D;
+                    const size_t vbase = kbase + (size_t)hkv * head_elems;
+                    uint8_t *dk = st + (size_t)(tok_lo - ts) * D * 2;
+                    bulk_g2s(dk, cache + kbase, bytes, &full[stage], pol);
+                    bulk_g2s(dk + L::kKBytes, cache + vbase, bytes, &full[stage], pol);
+                }
+                if (first_tile && lane == 0) {
+                    const uint16_t *qsrc = qg + ((size_t)c.b * a.num_q_heads + (size_t)c.kvh * G) * D;
+                    bulk_g2s(st + 2 * L::kKBytes, qsrc, (uint32_t)L::kQBytes, &full[stage], pol);
+                }
+                issued_mask |= 1u << stage;
+                issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        return;
+    }
+
+    // ================================ consumer warps ================================
+    const int slot = lane / L::kLanesPerTok;   // token slot within a step
+    const int chk = lane % L::kLanesPerTok;    // this lane's 8-element chunk of D
+    const float qscale = a.scale * kLog2e;     // scores in log2 units
+    float qf[G][8];
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+        const UnitCursor c = unit_of(u, prefix, lens, a.batch, hkv, chunk);
+        float m[G], l[G], acc[G][8];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            m[g] = -INFINITY;
+            l[g] = 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[g][j] = 0.f;
+        }
+        for (int ts = c.t0; ts < c.t1; ts += L::kTile) {
+            const int n = min(L::kTile, c.t1 - ts);
+            if (!mbar_wait(&full[stage], phase, abort_flag, a.err)) return;
+            const uint8_t *st = smem + (size_t)stage * L::kStageBytes;
+            if (ts == c.t0) {
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(st + 2 * L::kKBytes + ((size_t)g * D + chk * 8) * 2);
+                    unpack8(raw, qf[g], Tag());
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) qf[g][j] *= qscale;
+                }
+            }
+            const uint8_t *sk = st;
+            const uint8_t *sv = st + L::kKBytes;
+#pragma unroll
+            for (int b0 = 0; b0 < L::kSteps; b0 += L::kStepsPerBatch) {
+                float s[L::kStepsPerBatch][G];
+                bool valid[L::kStepsPerBatch];
+#pragma unroll
+                for (int i = 0; i < L::kStepsPerBatch; ++i) {
+                    const int t = warp * L::kTokPerWarp + (b0 + i) * L::kTokPerStep + slot;
+                    valid[i] = t < n;
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(sk + ((size_t)t * D + chk * 8) * 2);
+                    float kf[8];
+                    unpack8(raw, kf, Tag());
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        float part = 0.f;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) part = fmaf(qf[g][j], kf[j], part);
+#pragma unroll
+                        for (int o = L::kLanesPerTok / 2; o > 0; o >>= 1)
+                            part += __shfl_xor_sync(0xffffffffu, part, o);
+                        s[i][g] = valid[i] ? part : -INFINITY;
+                    }
+                }
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float mt = s[0][g];
+#pragma unroll
+                    for (int i = 1; i < L::kStepsPerBatch; ++i) mt = fmaxf(mt, s[i][g]);
+                    const float m_new = fmaxf(m[g], mt);
+                    if (m_new != -INFINITY) {
+                        const float alpha = exp2f(m[g] - m_new);  // 0 when m[g] = -inf
+                        l[g] *= alpha;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) acc[g][j] *= alpha;
+                        m[g] = m_new;
+                    }
+#pragma unroll
+                    for (int i = 0; i < L::kStepsPerBatch; ++i) {
+                        s[i][g] = valid[i] ? exp2f(s[i][g] - m[g]) : 0.f;
+                        l[g] += s[i][g];
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < L::kStepsPerBatch; ++i) {
+                    if (!valid[i]) continue;
+                    const int t = warp * L::kTokPerWarp + (b0 + i) * L::kTokPerStep + slot;
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(sv + ((size_t)t * D + chk * 8) * 2);
+                    float vf[8];
+                    unpack8(raw, vf, Tag());
+#pragma unroll
+                    for (int g = 0; g < G; ++g)
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) acc[g][j] = fmaf(s[i][g], vf[j], acc[g][j]);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[stage]);
+            if (++stage == kStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        // ---- merge the token slots of this warp (lanes with the same chunk) ----
+#pragma unroll
+        for (int o = L::kLanesPerTok; o < 32; o <<= 1) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float mo = __shfl_xor_sync(0xffffffffu, m[g], o);
+                const float lo = __shfl_xor_sync(0xffffffffu, l[g], o);
+                const float mn = fmaxf(m[g], mo);
+                const float wa = (m[g] == -INFINITY) ? 0.f : exp2f(m[g] - mn);
+                const float wb = (mo == -INFINITY) ? 0.f : exp2f(mo - mn);
+                l[g] = l[g] * wa + lo * wb;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float ao = __shfl_xor_sync(0xffffffffu, acc[g][j], o);
+                    acc[g][j] = acc[g][j] * wa + ao * wb;
+                }
+                m[g] = mn;
+            }
+        }
+        // ---- merge across the consumer warps through shared memory ----
+        if (slot == 0) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float *row = merge + ((size_t)warp * G + g) * (D + 2);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) row[chk * 8 + j] = acc[g][j];
+                if (chk == 0) {
+                    row[D] = m[g];
+                    row[D + 1] = l[g];
+                }
+            }
+        }
+        named_barrier(1, kConsumerWarps * 32);
+        const int splits = (lens[c.b] + chunk - 1) / chunk;
+        for (int idx = tid; idx < G * D; idx += kConsumerWarps * 32) {
+            const int g = idx / D, d = idx - (idx / D) * D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, merge[((size_t)w * G + g) * (D + 2) + D]);
+            float lsum = 0.f, o = 0.f;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float *row = merge + ((size_t)w * G + g) * (D + 2);
+                const float mw = row[D];
+                const float wgt = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+                lsum += row[D + 1] * wgt;
+                o += row[d] * wgt;
+            }
+            const float res = lsum > 0.f ? o / lsum : 0.f;
+            const float lse_v = lsum > 0.f ? (M + log2f(lsum)) * kLn2 : -INFINITY;
+            const int h = c.kvh * G + g;
+            const size_t row_id = (size_t)c.b * a.num_q_heads + h;
+            if (splits == 1) {
+                store_out(a.out, row_id * D + d, res, a.out_dtype);
+                if (d == 0 && a.lse) a.lse[row_id] = lse_v;
+            } else {
+                const size_t pr = row_id * a.s_max + c.split;
+                a.part_o[pr * D + d] = res;
+                if (d == 0) a.part_lse[pr] = lse_v;
+            }
+        }
+        named_barrier(1, kConsumerWarps * 32);
+    }
+}
+
+// ---- split merge: one warp per output row --------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
+    constexpr int kPer = D / 32;  // elements per lane
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= a.n_rows) return;
+    int S = a.num_splits;
+    if (a.context_lens) {
+        const int b = row / a.rows_per_seq;
+        int len = __ldg(a.context_lens + b);
+        len = len < 0 ? 0 : len;
+        S = (len + a.chunk - 1) / a.chunk;
+        if (S > a.num_splits) S = a.num_splits;
+        if (S == 1) return;  // finished by the split kernel
+    }
+    const float *pl = a.part_lse + (size_t)row * a.num_splits;
+    const float *po = a.part_o + (size_t)row * a.num_splits * D;
+    float M = -INFINITY;
+    for (int s = lane; s < S; s += 32) M = fmaxf(M, pl[s]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float o_acc[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) o_acc[j] = 0.f;
+    float wsum = 0.f;
+    if (M != -INFINITY) {
+        for (int s = 0; s < S; ++s) {
+            const float ls = pl[s];
+            if (ls == -INFINITY) continue;
+            const float w = exp2f((ls - M) * kLog2e);
+            wsum += w;
+#pragma unroll
+            for (int j = 0; j < kPer; ++j) o_acc[j] = fmaf(w, po[(size_t)s * D + lane * kPer + j], o_acc[j]);
+        }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) store_out(a.out, (size_t)row * D + lane * kPer + j, o_acc[j] * inv, a.out_dtype);
+    if (lane == 0 && a.lse) a.lse[row] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
+}
+
+template <typename Tag, int D, int G>
+cudaError_t launch_decode_t(const DecodeArgs &a, int grid, cudaStream_t s) {
+    const size_t smem = DecodeLayout<D, G>::smem_bytes(a.batch);
+    auto kern = decode_split_kernel<Tag, D, G>;
+    // opt in to the largest size this kernel can ask for, once per device
+    static unsigned int configured = 0;
+    const int dev = device_info().device;
+    if (dev < 32 && !(configured & (1u << dev))) {
+        const int max_smem = (int)DecodeLayout<D, G>::smem_bytes(kMaxBatch);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+        if (e != cudaSuccess) return e;
+        configured |= 1u << dev;
+    } else if (dev >= 32) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    kern<<<grid, kDecodeThreads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename Tag, int D>
+cudaError_t dispatch_group(const DecodeArgs &a, int grid, cudaStream_t s) {
+    switch (a.num_q_heads / a.cache.num_kv_heads) {
+        case 1: return launch_decode_t<Tag, D, 1>(a, grid, s);
+        case 2: return launch_decode_t<Tag, D, 2>(a, grid, s);
+        case 4: return launch_decode_t<Tag, D, 4>(a, grid, s);
+        case 8: return launch_decode_t<Tag, D, 8>(a, grid, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+int decode_max_batch() { return kMaxBatch; }
+
+size_t decode_smem_bytes(int head_dim, int group, int batch) {
+    auto pick = [&](auto d_tag, auto g_tag) {
+        return DecodeLayout<decltype(d_tag)::value, decltype(g_tag)::value>::smem_bytes(batch);
+    };
+    using I64 = std::integral_constant<int, 64>;
+    using I128 = std::integral_constant<int, 128>;
+    using G1 = std::integral_constant<int, 1>;
+    using G2 = std::integral_constant<int, 2>;
+    using G4 = std::integral_constant<int, 4>;
+    using G8 = std::integral_constant<int, 8>;
+    if (head_dim == 64) {
+        switch (group) {
+            case 1: return pick(I64(), G1());
+            case 2: return pick(I64(), G2());
+            case 4: return pick(I64(), G4());
+            default: return pick(I64(), G8());
+        }
+    }
+    switch (group) {
+        case 1: return pick(I128(), G1());
+        case 2: return pick(I128(), G2());
+        case 4: return pick(I128(), G4());
+        default: return pick(I128(), G8());
+    }
+}
+
+int decode_ctas_per_sm(int head_dim, int group, int dtype) {
+    (void)head_dim; (void)group; (void)dtype;
+    return 1;  // __launch_bounds__(.., 1) and ~130 KB of stages: one resident CTA per SM
+}
+
+cudaError_t launch_decode(const DecodeArgs &a, int grid, cudaStream_t s) {
+    if (a.batch == 0) return cudaSuccess;
+    if (a.cache.dtype == 1) {
+        return a.cache.head_dim == 128 ? dispatch_group<BF16Tag, 128>(a, grid, s) : dispatch_group<BF16Tag, 64>(a, grid, s);
+    }
+    return a.cache.head_dim == 128 ? dispatch_group<F16Tag, 128>(a, grid, s) : dispatch_group<F16Tag, 64>(a, grid, s);
+}
+
+cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s) {
+    if (a.n_rows == 0) return cudaSuccess;
+    const int grid = (a.n_rows + 7) / 8;
+    if (a.head_dim == 128) {
+        combine_kernel<128><<<grid, 256, 0, s>>>(a);
+    } else {
+        combine_kernel<64><<<grid, 256, 0, s>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

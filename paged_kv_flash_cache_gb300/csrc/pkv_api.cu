@@ -1,0 +1,315 @@
+// pkv_api.cu -- the C ABI of libpkv (declared in include/pkv.h): argument validation,
+// launch configuration, workspace sizing, status codes and the device error word.
+// No call here allocates device memory.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+
+// Sticky device error word (first range / timeout event wins); one per device context.
+__device__ int g_device_error;
+
+namespace {
+
+struct DeviceSlot {
+    bool ready = false;
+    DeviceInfo info{};
+    int *err_ptr = nullptr;
+};
+constexpr int kMaxDevices = 64;
+DeviceSlot g_slots[kMaxDevices];
+std::mutex g_slot_lock;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int ilog2(int x) {
+    int r = 0;
+    while ((1 << r) < x) ++r;
+    return r;
+}
+
+DeviceSlot &slot() {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= kMaxDevices) dev = 0;
+    DeviceSlot &s = g_slots[dev];
+    if (!s.ready) {
+        std::lock_guard<std::mutex> g(g_slot_lock);
+        if (!s.ready) {
+            s.info.device = dev;
+            int sms = 0;
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            s.info.num_sms = sms > 0 ? sms : 1;
+            s.info.decode_ctas_per_sm = 1;
+            void *p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_device_error) == cudaSuccess) s.err_ptr = static_cast<int *>(p);
+            s.ready = true;
+        }
+    }
+    return s;
+}
+
+pkv_status check_cache(const pkv_cache &c) {
+    if (!c.ptr || !aligned16(c.ptr)) return PKV_ERR_INVALID_ARG;
+    if (c.num_blocks < 0 || c.num_kv_heads <= 0 || c.block_size <= 0 || c.head_dim <= 0) return PKV_ERR_INVALID_ARG;
+    if (c.dtype != PKV_F16 && c.dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+    if (c.head_dim != 64 && c.head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (!is_pow2(c.block_size) || c.block_size < 8 || c.block_size > 512) return PKV_ERR_UNSUPPORTED;
+    return PKV_OK;
+}
+
+pkv_status check_out_dtype(pkv_dtype out_dtype, pkv_dtype cache_dtype) {
+    if (out_dtype != cache_dtype && out_dtype != PKV_F32) return PKV_ERR_UNSUPPORTED;
+    return PKV_OK;
+}
+
+CacheView view_of(const pkv_cache &c) {
+    CacheView v;
+    v.ptr = c.ptr;
+    v.num_blocks = c.num_blocks;
+    v.num_kv_heads = c.num_kv_heads;
+    v.block_size = c.block_size;
+    v.log2_block_size = ilog2(c.block_size);
+    v.head_dim = c.head_dim;
+    v.dtype = (int)c.dtype;
+    return v;
+}
+
+// Tokens per decode split.  Automatic: enough (sequence, KV head, split) units for about
+// eight per CTA at full capacity, in [128, 512] tokens; explicit: capacity / num_splits
+// rounded up to the tile.
+int split_tokens(int batch, int num_kv_heads, int block_size, int max_blocks_per_seq, int num_splits) {
+    const long long cap = (long long)max_blocks_per_seq * block_size;
+    const int tile = kDecodeTile;
+    if (num_splits > 0) {
+        long long c = (cap + num_splits - 1) / num_splits;
+        c = (c + tile - 1) / tile * tile;
+        return (int)(c < tile ? tile : c);
+    }
+    const DeviceInfo &d = slot().info;
+    const long long ctas = (long long)d.num_sms * d.decode_ctas_per_sm;
+    const long long want = (long long)batch * num_kv_heads * cap / (ctas * 8 > 0 ? ctas * 8 : 1);
+    int c = 512;
+    while (c > 128 && c > want) c >>= 1;
+    return c;
+}
+
+}  // namespace
+
+const DeviceInfo &device_info() { return slot().info; }
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+int pkv_version(void) { return 100; }
+
+const char *pkv_status_string(pkv_status s) {
+    switch (s) {
+        case PKV_OK: return "PKV_OK";
+        case PKV_ERR_INVALID_ARG: return "PKV_ERR_INVALID_ARG";
+        case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
+        case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE";
+        case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
+        case PKV_ERR_DEVICE_RANGE: return "PKV_ERR_DEVICE_RANGE";
+        case PKV_ERR_TIMEOUT: return "PKV_ERR_TIMEOUT";
+    }
+    return "PKV_ERR_UNKNOWN";
+}
+
+pkv_status pkv_kv_cache_append(pkv_cache cache, const void *k_new, const void *v_new, const int *cu_new_lens,
+                               const int *ctx_before, const int *block_tables, int batch, int max_blocks_per_seq,
+                               int num_new_tokens, void *stream) {
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK) return st;
+    if (batch < 0 || num_new_tokens < 0 || max_blocks_per_seq <= 0) return PKV_ERR_INVALID_ARG;
+    if (batch == 0 || num_new_tokens == 0) return PKV_OK;
+    if (!k_new || !v_new || !cu_new_lens || !ctx_before || !block_tables) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new)) return PKV_ERR_INVALID_ARG;
+    DeviceSlot &s = slot();
+    AppendArgs a;
+    a.cache = cache.ptr;
+    a.num_blocks = cache.num_blocks;
+    a.num_kv_heads = cache.num_kv_heads;
+    a.block_size = cache.block_size;
+    a.log2_block_size = ilog2(cache.block_size);
+    a.head_dim = cache.head_dim;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.cu_new_lens = cu_new_lens;
+    a.ctx_before = ctx_before;
+    a.block_tables = block_tables;
+    a.batch = batch;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_new_tokens = num_new_tokens;
+    a.err = s.err_ptr;
+    return launch_append(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int pkv_decode_split_tokens(int batch, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                            int max_blocks_per_seq, int num_splits) {
+    (void)num_q_heads;
+    (void)head_dim;
+    if (batch <= 0 || num_kv_heads <= 0 || block_size <= 0 || max_blocks_per_seq <= 0) return kDecodeTile;
+    return split_tokens(batch, num_kv_heads, block_size, max_blocks_per_seq, num_splits);
+}
+
+size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                 int max_blocks_per_seq, int num_splits) {
+    if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        max_blocks_per_seq <= 0)
+        return 0;
+    const long long cap = (long long)max_blocks_per_seq * block_size;
+    const int chunk = split_tokens(batch, num_kv_heads, block_size, max_blocks_per_seq, num_splits);
+    const long long s_max = (cap + chunk - 1) / chunk;
+    if (s_max <= 1) return 0;
+    return (size_t)batch * num_q_heads * s_max * (head_dim + 1) * sizeof(float);
+}
+
+pkv_status pkv_paged_attn_decode(pkv_cache cache, const void *q, int num_q_heads, const int *block_tables,
+                                 const int *context_lens, int batch, int max_blocks_per_seq, float scale,
+                                 int num_splits, void *workspace, size_t workspace_bytes, void *out,
+                                 pkv_dtype out_dtype, float *lse, void *stream) {
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK) return st;
+    if ((st = check_out_dtype(out_dtype, cache.dtype)) != PKV_OK) return st;
+    if (batch < 0 || max_blocks_per_seq <= 0 || num_q_heads <= 0 || num_splits < 0) return PKV_ERR_INVALID_ARG;
+    if (num_q_heads % cache.num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+    const int group = num_q_heads / cache.num_kv_heads;
+    if (group != 1 && group != 2 && group != 4 && group != 8) return PKV_ERR_UNSUPPORTED;
+    if (batch > decode_max_batch()) return PKV_ERR_UNSUPPORTED;
+    if (batch == 0) return PKV_OK;
+    if (!q || !block_tables || !context_lens || !out) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(out) || (lse && !aligned16(lse))) return PKV_ERR_INVALID_ARG;
+    const long long cap = (long long)max_blocks_per_seq * cache.block_size;
+    if (cap > (1ll << 30)) return PKV_ERR_UNSUPPORTED;
+    DeviceSlot &s = slot();
+    const int chunk = split_tokens(batch, cache.num_kv_heads, cache.block_size, max_blocks_per_seq, num_splits);
+    const int s_max = (int)((cap + chunk - 1) / chunk);
+    const size_t need = pkv_decode_workspace_size(batch, num_q_heads, cache.num_kv_heads, cache.head_dim,
+                                                  cache.block_size, max_blocks_per_seq, num_splits);
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return PKV_ERR_WORKSPACE;
+    DecodeArgs a;
+    a.cache = view_of(cache);
+    a.q = q;
+    a.num_q_heads = num_q_heads;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.batch = batch;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.scale = scale;
+    a.chunk = chunk;
+    a.s_max = s_max;
+    a.part_o = static_cast<float *>(workspace);
+    a.part_lse = need > 0 ? a.part_o + (size_t)batch * num_q_heads * s_max * cache.head_dim : nullptr;
+    a.out = out;
+    a.out_dtype = (int)out_dtype;
+    a.lse = lse;
+    a.err = s.err_ptr;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const int grid = s.info.num_sms * s.info.decode_ctas_per_sm;
+    if (launch_decode(a, grid, cs) != cudaSuccess) return PKV_ERR_CUDA;
+    // Rows that span several splits (and empty rows) are finished by the merge.
+    CombineArgs c;
+    c.part_o = a.part_o;
+    c.part_lse = a.part_lse;
+    c.n_rows = batch * num_q_heads;
+    c.num_splits = s_max;
+    c.head_dim = cache.head_dim;
+    c.context_lens = context_lens;
+    c.rows_per_seq = num_q_heads;
+    c.chunk = chunk;
+    c.out = out;
+    c.out_dtype = (int)out_dtype;
+    c.lse = lse;
+    if (launch_combine(c, cs) != cudaSuccess) return PKV_ERR_CUDA;
+    return PKV_OK;
+}
+
+pkv_status pkv_attn_combine(const float *partial_o, const float *partial_lse, int n_rows, int num_splits,
+                            int head_dim, void *out, pkv_dtype out_dtype, float *lse, void *stream) {
+    if (n_rows < 0 || num_splits <= 0) return PKV_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (out_dtype != PKV_F16 && out_dtype != PKV_BF16 && out_dtype != PKV_F32) return PKV_ERR_UNSUPPORTED;
+    if (n_rows == 0) return PKV_OK;
+    if (!partial_o || !partial_lse || !out) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(partial_o) || !aligned16(out)) return PKV_ERR_INVALID_ARG;
+    slot();
+    CombineArgs c;
+    c.part_o = partial_o;
+    c.part_lse = partial_lse;
+    c.n_rows = n_rows;
+    c.num_splits = num_splits;
+    c.head_dim = head_dim;
+    c.context_lens = nullptr;
+    c.rows_per_seq = 1;
+    c.chunk = 1;
+    c.out = out;
+    c.out_dtype = (int)out_dtype;
+    c.lse = lse;
+    return launch_combine(c, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_paged_attn_prefill(pkv_cache cache, const void *q, int num_q_heads, const int *cu_q_lens,
+                                  const int *context_lens, const int *block_tables, int batch,
+                                  int max_blocks_per_seq, int total_q, int max_q_len, float scale, int causal,
+                                  void *out, pkv_dtype out_dtype, float *lse, void *stream) {
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK) return st;
+    if ((st = check_out_dtype(out_dtype, cache.dtype)) != PKV_OK) return st;
+    if (batch < 0 || max_blocks_per_seq <= 0 || num_q_heads <= 0 || total_q < 0 || max_q_len < 0)
+        return PKV_ERR_INVALID_ARG;
+    if (num_q_heads % cache.num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+    if (batch == 0 || total_q == 0) return PKV_OK;
+    if (!q || !cu_q_lens || !context_lens || !block_tables || !out) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(out) || (lse && !aligned16(lse))) return PKV_ERR_INVALID_ARG;
+    const long long cap = (long long)max_blocks_per_seq * cache.block_size;
+    if (cap > (1ll << 30)) return PKV_ERR_UNSUPPORTED;
+    DeviceSlot &s = slot();
+    PrefillArgs a;
+    a.cache = view_of(cache);
+    a.q = q;
+    a.num_q_heads = num_q_heads;
+    a.cu_q_lens = cu_q_lens;
+    a.context_lens = context_lens;
+    a.block_tables = block_tables;
+    a.batch = batch;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.total_q = total_q;
+    a.max_q_len = max_q_len;
+    a.scale = scale;
+    a.causal = causal ? 1 : 0;
+    a.out = out;
+    a.out_dtype = (int)out_dtype;
+    a.lse = lse;
+    a.err = s.err_ptr;
+    cudaError_t e = launch_prefill(a, static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_get_device_error(void *stream, int *code) {
+    if (!code) return PKV_ERR_INVALID_ARG;
+    *code = PKV_OK;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return PKV_ERR_CUDA;
+    DeviceSlot &s = slot();
+    if (!s.err_ptr) return PKV_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, s.err_ptr, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return PKV_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(s.err_ptr, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return PKV_ERR_CUDA;
+    }
+    *code = v;
+    return PKV_OK;
+}
+
+}  // extern "C"

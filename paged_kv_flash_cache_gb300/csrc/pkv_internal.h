@@ -1,0 +1,89 @@
+// pkv_internal.h -- host-side launcher interface between the C ABI (pkv_api.cu)
+// and the kernel translation units.  Arguments arrive here already validated.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/pkv.h"
+
+namespace pkv {
+
+struct CacheView {
+    const void *ptr;
+    int num_blocks, num_kv_heads, block_size, log2_block_size, head_dim;
+    int dtype;  // 0 fp16, 1 bf16
+};
+
+struct AppendArgs {
+    void *cache;
+    int num_blocks, num_kv_heads, block_size, log2_block_size, head_dim;
+    const void *k_new, *v_new;
+    const int *cu_new_lens, *ctx_before, *block_tables;
+    int batch, max_blocks_per_seq, num_new_tokens;
+    int *err;
+};
+
+struct DecodeArgs {
+    CacheView cache;
+    const void *q;
+    int num_q_heads;
+    const int *block_tables, *context_lens;
+    int batch, max_blocks_per_seq;
+    float scale;
+    int chunk;   // tokens per split (multiple of the decode tile)
+    int s_max;   // splits a full-capacity context uses: ceil(max_blocks_per_seq * block_size / chunk)
+    float *part_o;    // [batch, Hq, s_max, D]
+    float *part_lse;  // [batch, Hq, s_max]
+    void *out;
+    int out_dtype;
+    float *lse;
+    int *err;
+};
+
+struct CombineArgs {
+    const float *part_o, *part_lse;
+    int n_rows, num_splits, head_dim;
+    // When context_lens is set, row r = b * rows_per_seq + h uses ceil(len_b / chunk)
+    // splits; rows with exactly one split were finished by the decode kernel.
+    const int *context_lens;
+    int rows_per_seq, chunk;
+    void *out;
+    int out_dtype;
+    float *lse;
+};
+
+struct PrefillArgs {
+    CacheView cache;
+    const void *q;
+    int num_q_heads;
+    const int *cu_q_lens, *context_lens, *block_tables;
+    int batch, max_blocks_per_seq, total_q, max_q_len;
+    float scale;
+    int causal;
+    void *out;
+    int out_dtype;
+    float *lse;
+    int *err;
+};
+
+// Per-device facts cached on first use.
+struct DeviceInfo {
+    int device;
+    int num_sms;
+    int decode_ctas_per_sm;
+};
+const DeviceInfo &device_info();
+
+constexpr int kDecodeTile = 64;  // tokens per decode pipeline stage
+
+cudaError_t launch_append(const AppendArgs &a, cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs &a, int grid, cudaStream_t s);
+cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s);
+cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t s);
+int decode_ctas_per_sm(int head_dim, int group, int dtype);
+size_t decode_smem_bytes(int head_dim, int group, int batch);
+int decode_max_batch();
+
+}  // namespace pkv

@@ -87,7 +87,15 @@ def cu_lens(lens: Sequence[int]) -> torch.Tensor:
 
 
 def randn_t(gen: torch.Generator, shape, dtype: str) -> torch.Tensor:
-    return torch.randn(shape, generator=gen, dtype=torch.float32).to(TORCH_DTYPE[dtype])
+    """N(0, 1) draws in fp32 on the generator's device, rounded to fp16 / bf16."""
+    return torch.randn(shape, generator=gen, dtype=torch.float32, device=gen.device).to(TORCH_DTYPE[dtype])
+
+
+def data_generator(seed: int, device="cpu") -> torch.Generator:
+    """Generator for token data. Large workloads draw on the GPU (a CPU draw of a few GB takes
+    minutes); each problem instance is then self-consistent: the oracle reads the same tensors
+    after a copy to the host."""
+    return torch.Generator(device=device).manual_seed(seed)
 
 
 @dataclass
@@ -165,8 +173,9 @@ def make_problem(name: str, *, batch: int, num_q_heads: int, num_kv_heads: int, 
                  causal: bool, seed: int, num_blocks: Optional[int] = None,
                  free_order: Optional[Sequence[int]] = None, tables: Optional[List[List[int]]] = None,
                  max_blocks_per_seq: Optional[int] = None, pool_init: str = "noise",
-                 kv_data=None, scale: Optional[float] = None) -> PagedProblem:
+                 kv_data=None, scale: Optional[float] = None, device="cpu") -> PagedProblem:
     gen = torch.Generator().manual_seed(seed)
+    dgen = data_generator(seed, device)
     context_lens = [int(x) for x in context_lens]
     q_lens = [int(x) for x in q_lens]
     if tables is None:
@@ -186,13 +195,13 @@ def make_problem(name: str, *, batch: int, num_q_heads: int, num_kv_heads: int, 
     elif kv_data is not None:
         k_ctx, v_ctx = kv_data
     else:
-        k_ctx = randn_t(gen, (total, num_kv_heads, head_dim), dtype)
-        v_ctx = randn_t(gen, (total, num_kv_heads, head_dim), dtype)
-    q = randn_t(gen, (sum(q_lens), num_q_heads, head_dim), dtype)
+        k_ctx = randn_t(dgen, (total, num_kv_heads, head_dim), dtype)
+        v_ctx = randn_t(dgen, (total, num_kv_heads, head_dim), dtype)
+    q = randn_t(dgen, (sum(q_lens), num_q_heads, head_dim), dtype)
     if pool_init == "none":
         pool = None
     else:
-        pool = _pool_noise(gen, num_blocks, num_kv_heads, block_size, head_dim, dtype, pool_init == "cheap")
+        pool = _pool_noise(dgen, num_blocks, num_kv_heads, block_size, head_dim, dtype, pool_init == "cheap")
     return PagedProblem(
         name=name, dtype=dtype, batch=batch, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
         head_dim=head_dim, block_size=block_size, num_blocks=num_blocks,
@@ -232,7 +241,7 @@ def tiny(seed: int = 1235, chunk: int = 48):
 
 
 def decode_7b(seed: int = 1236, batch: int = 16, lo: int = 1024, hi: int = 8192, pool_init: str = "cheap",
-              block_size: int = 16, dtype: str = F16) -> PagedProblem:
+              block_size: int = 16, dtype: str = F16, device="cpu") -> PagedProblem:
     """7B-like decode: 32 heads x 128, contexts uniform in [lo, hi], pool 1.2x the pages needed,
     pages handed out in a seeded random order."""
     gen = torch.Generator().manual_seed(seed)
@@ -243,11 +252,11 @@ def decode_7b(seed: int = 1236, batch: int = 16, lo: int = 1024, hi: int = 8192,
     return make_problem("decode_7b", batch=batch, num_q_heads=32, num_kv_heads=32, head_dim=128,
                         block_size=block_size, context_lens=lens, q_lens=[1] * batch, dtype=dtype,
                         causal=False, seed=seed + 1, num_blocks=nb, free_order=order, pool_init=pool_init,
-                        max_blocks_per_seq=(hi + block_size - 1) // block_size)
+                        max_blocks_per_seq=(hi + block_size - 1) // block_size, device=device)
 
 
 def prefill_long(seed: int = 1237, batch: int = 4, seq: int = 8192, chunk: int = 512, heads: int = 32,
-                 head_dim: int = 128, block_size: int = 16, dtype: str = BF16) -> PagedProblem:
+                 head_dim: int = 128, block_size: int = 16, dtype: str = BF16, device="cpu") -> PagedProblem:
     """Long causal prefill: `batch` sequences of `seq` tokens in bf16, pages of 16 tokens
     spread by a seeded permutation over a pool of exactly the pages needed. The whole
     sequence is described once; `prefill_chunks` cuts it into `chunk`-token query calls."""
@@ -256,7 +265,7 @@ def prefill_long(seed: int = 1237, batch: int = 4, seq: int = 8192, chunk: int =
     order = torch.randperm(pages, generator=gen).tolist()
     p = make_problem("prefill_long", batch=batch, num_q_heads=heads, num_kv_heads=heads, head_dim=head_dim,
                      block_size=block_size, context_lens=[seq] * batch, q_lens=[seq] * batch, dtype=dtype,
-                     causal=True, seed=seed + 1, num_blocks=pages, free_order=order, pool_init="none")
+                     causal=True, seed=seed + 1, num_blocks=pages, free_order=order, pool_init="none", device=device)
     p.meta["chunk"] = chunk
     return p
 
@@ -279,7 +288,7 @@ def prefill_chunk_view(p: PagedProblem, c: int) -> dict:
 
 
 def bs_sweep(block_size: int, seed: int = 1238, batch: int = 32, ctx: int = 4096,
-             kv_data: Optional[tuple] = None, pool_init: str = "cheap") -> PagedProblem:
+             kv_data: Optional[tuple] = None, pool_init: str = "cheap", device="cpu") -> PagedProblem:
     """Block-size sweep: `batch` x `ctx` tokens, 32 heads x 128, fp16; the same K/V token data for
     every block size (pass kv_data from `bs_sweep_kv`); pool = exactly the pages needed, permuted."""
     gen = torch.Generator().manual_seed(seed * 1000 + block_size)
@@ -288,11 +297,11 @@ def bs_sweep(block_size: int, seed: int = 1238, batch: int = 32, ctx: int = 4096
     return make_problem("bs_sweep_%d" % block_size, batch=batch, num_q_heads=32, num_kv_heads=32, head_dim=128,
                         block_size=block_size, context_lens=[ctx] * batch, q_lens=[1] * batch, dtype=F16,
                         causal=False, seed=seed, num_blocks=pages, free_order=order, kv_data=kv_data,
-                        pool_init=pool_init)
+                        pool_init=pool_init, device=device)
 
 
-def bs_sweep_kv(seed: int = 1238, batch: int = 32, ctx: int = 4096) -> tuple:
-    gen = torch.Generator().manual_seed(seed + 7)
+def bs_sweep_kv(seed: int = 1238, batch: int = 32, ctx: int = 4096, device="cpu") -> tuple:
+    gen = data_generator(seed + 7, device)
     k = randn_t(gen, (batch * ctx, 32, 128), F16)
     v = randn_t(gen, (batch * ctx, 32, 128), F16)
     return k, v
@@ -307,7 +316,7 @@ def mixed_lens(seed: int, batch: int = 64, median: float = 2048.0, sigma: float 
 
 
 def mixed_serving(seed: int = 1239, batch: int = 64, block_size: int = 32, pool_init: str = "cheap",
-                  kv_data=None) -> PagedProblem:
+                  kv_data=None, device="cpu") -> PagedProblem:
     """Mixed serving batch: lognormal contexts (median 2048, sigma 1, clipped to [16, 32768]),
     32 Q heads sharing 8 KV heads, head_dim 128, bf16, block_size 32, fragmented pool.
 
@@ -333,7 +342,7 @@ def mixed_serving(seed: int = 1239, batch: int = 64, block_size: int = 32, pool_
     return make_problem("mixed_serving", batch=batch, num_q_heads=32, num_kv_heads=8, head_dim=128,
                         block_size=block_size, context_lens=lens, q_lens=[1] * batch, dtype=BF16,
                         causal=False, seed=seed + 1, num_blocks=nb, tables=tables, max_blocks_per_seq=mb,
-                        pool_init=pool_init, kv_data=kv_data)
+                        pool_init=pool_init, kv_data=kv_data, device=device)
 
 
 def append_step(p: PagedProblem, seed: int = 99) -> dict:

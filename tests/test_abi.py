@@ -1,0 +1,89 @@
+"""The C-ABI library builds, loads without a GPU and exports every symbol include/pkv.h
+declares; host-side validation rejects bad calls before anything is launched."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_flash_cache_gb300 as pkv
+from paged_kv_flash_cache_gb300 import build as pkv_build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "pkv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pkv_build.build()
+    return pkv.load_library()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_symbols() == sorted(pkv.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    assert lib.pkv_version() == 100
+    assert lib.pkv_status_string(0) == b"PKV_OK"
+    assert lib.pkv_status_string(3) == b"PKV_ERR_WORKSPACE"
+
+
+def test_only_c_abi_symbols_are_exported(lib):
+    """Internal C++ symbols stay hidden (-fvisibility=hidden); nm lists the dynamic exports."""
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", pkv.library_path()], capture_output=True, text=True).stdout
+    ours = sorted({l.split()[-1] for l in out.splitlines() if " T " in l and l.split()[-1].startswith("pkv_")})
+    assert ours == sorted(pkv.EXPORTS)
+
+
+def _cache(ptr=16, nb=4, hkv=2, bs=16, d=128, dt=0):
+    return pkv._Cache(ctypes.c_void_p(ptr), nb, hkv, bs, d, dt)
+
+
+def test_host_validation_without_gpu(lib):
+    P = ctypes.c_void_p
+    good = P(4096)
+    # null cache pointer
+    assert lib.pkv_kv_cache_append(_cache(ptr=0), good, good, good, good, good, 1, 4, 3, None) == 1
+    # misaligned cache pointer
+    assert lib.pkv_kv_cache_append(_cache(ptr=4098), good, good, good, good, good, 1, 4, 3, None) == 1
+    # unsupported head_dim / block_size / dtype
+    assert lib.pkv_kv_cache_append(_cache(d=96), good, good, good, good, good, 1, 4, 3, None) == 2
+    assert lib.pkv_kv_cache_append(_cache(bs=24), good, good, good, good, good, 1, 4, 3, None) == 2
+    assert lib.pkv_kv_cache_append(_cache(bs=1024), good, good, good, good, good, 1, 4, 3, None) == 2
+    assert lib.pkv_kv_cache_append(_cache(dt=2), good, good, good, good, good, 1, 4, 3, None) == 2
+    # negative sizes
+    assert lib.pkv_kv_cache_append(_cache(), good, good, good, good, good, -1, 4, 3, None) == 1
+    # nothing to do is fine and launches nothing
+    assert lib.pkv_kv_cache_append(_cache(), good, good, good, good, good, 1, 4, 0, None) == 0
+    # decode: Hq not a multiple of Hkv, unsupported group, out dtype
+    F = ctypes.c_float
+    args = lambda hq, out_dt=0: (_cache(), good, hq, good, good, 2, 4, F(0.1), 0, good, 1 << 20, good, out_dt, None,
+                                 None)
+    assert lib.pkv_paged_attn_decode(*args(3)) == 1
+    assert lib.pkv_paged_attn_decode(*args(6)) == 2      # group 3
+    assert lib.pkv_paged_attn_decode(*args(2, out_dt=1)) == 2   # bf16 out for an fp16 cache
+    # prefill: negative total_q
+    assert lib.pkv_paged_attn_prefill(_cache(), good, 2, good, good, good, 1, 4, -1, 4, F(0.1), 1, good, 0, None,
+                                      None) == 1
+    # combine: bad head_dim, bad split count
+    assert lib.pkv_attn_combine(good, good, 4, 2, 96, good, 2, None, None) == 2
+    assert lib.pkv_attn_combine(good, good, 4, 0, 128, good, 2, None, None) == 1
+
+
+def test_workspace_sizing_with_explicit_splits(lib):
+    # capacity 4 * 16 = 64 tokens in 1 split: no workspace
+    assert pkv.decode_workspace_size(2, 4, 4, 128, 16, 4, num_splits=1) == 0
+    # capacity 512 * 16 = 8192 tokens in 4 splits of 2048: B * Hq * 4 * (D + 1) floats
+    assert pkv.decode_split_tokens(16, 32, 32, 128, 16, 512, num_splits=4) == 2048
+    assert pkv.decode_workspace_size(16, 32, 32, 128, 16, 512, num_splits=4) == 16 * 32 * 4 * 129 * 4
+    # split size is rounded up to the 64-token tile
+    assert pkv.decode_split_tokens(1, 8, 8, 64, 16, 10, num_splits=3) == 64

@@ -1,0 +1,196 @@
+"""GPU parity: kv_cache_append (bit-exact) and paged_attn_decode (within the stated tolerances)
+against the CPU oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_flash_cache_gb300 as pkv
+from paged_kv_flash_cache_gb300 import workloads as W
+from tests.helpers import cache_bits, check_close, device_cache, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from paged_kv_flash_cache_gb300 import build
+    build.build()
+    oracle.build()
+    assert torch.cuda.is_available()
+
+
+def problem(*, lens, hq=8, hkv=8, d=128, bs=16, dtype=W.F16, seed=5, extra=7, mb=None):
+    pages = sum((L + bs - 1) // bs for L in lens)
+    nb = pages + extra
+    order = torch.randperm(nb, generator=torch.Generator().manual_seed(seed + 9)).tolist()
+    return W.make_problem("t", batch=len(lens), num_q_heads=hq, num_kv_heads=hkv, head_dim=d, block_size=bs,
+                          context_lens=lens, q_lens=[1] * len(lens), dtype=dtype, causal=False, seed=seed,
+                          num_blocks=nb, free_order=order, max_blocks_per_seq=mb)
+
+
+def run_decode(p, cache, num_splits=0, out_dtype=None, with_lse=True):
+    q = to_dev(p.q)
+    lse = torch.empty((p.batch, p.num_q_heads), dtype=torch.float32, device="cuda") if with_lse else None
+    out = pkv.paged_attn_decode(cache, q, to_dev(p.block_tables), to_dev(p.context_lens), scale=p.scale,
+                                num_splits=num_splits, out_dtype=out_dtype, lse=lse)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    return out, lse
+
+
+# ------------------------------------------------------------------------------------------------
+# append
+# ------------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("bs", [8, 16, 64, 512])
+@pytest.mark.parametrize("d,dtype", [(128, W.F16), (64, W.BF16)])
+def test_append_bit_exact(bs, d, dtype):
+    p = problem(lens=[1, 37, 100, 513], bs=bs, d=d, dtype=dtype, hq=4, hkv=4)
+    dev = device_cache(p)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    ref = oracle.build_cache(p)
+    assert np.array_equal(cache_bits(dev), ref)       # every pool element, untouched pages included
+
+
+def test_append_two_steps_and_decode_step_tokens():
+    """Context then a chunk (ctx_before > 0), then one decode-step token per sequence."""
+    dec, pre = W.tiny()
+    cu = pre.cu_ctx_lens.tolist()
+    first = [37, 100]
+    rows1 = torch.cat([torch.arange(cu[0], cu[0] + 37), torch.arange(cu[1], cu[1] + 100)])
+    rows2 = torch.cat([torch.arange(cu[0] + 37, cu[1]), torch.arange(cu[1] + 100, cu[2])])
+    dev = pre.pool_init.to("cuda")
+    ref = oracle.empty_cache_bits(pre)
+    bt = to_dev(pre.block_tables)
+    for rows, lens, before in ((rows1, first, [0, 0]), (rows2, [48, 48], first)):
+        k, v = pre.k_ctx[rows], pre.v_ctx[rows]
+        pkv.kv_cache_append(dev, to_dev(k), to_dev(v), to_dev(W.cu_lens(lens)),
+                            to_dev(torch.tensor(before, dtype=torch.int32)), bt)
+        oracle.kv_cache_append(ref, k, v, W.cu_lens(lens), torch.tensor(before, dtype=torch.int32),
+                               pre.block_tables)
+    torch.cuda.synchronize()
+    assert np.array_equal(cache_bits(dev), ref)
+    step = W.append_step(dec, seed=3)
+    pkv.kv_cache_append(dev, to_dev(step["k_new"]), to_dev(step["v_new"]), to_dev(step["cu_new_lens"]),
+                        to_dev(step["ctx_before"]), to_dev(step["block_tables"]))
+    oracle.kv_cache_append(ref, step["k_new"], step["v_new"], step["cu_new_lens"], step["ctx_before"],
+                           step["block_tables"])
+    torch.cuda.synchronize()
+    assert np.array_equal(cache_bits(dev), ref)
+    assert pkv.get_device_error() == 0
+
+
+def test_append_bad_page_is_flagged_not_faulted():
+    p = problem(lens=[40, 20], bs=16, hq=2, hkv=2)
+    bt = p.block_tables.clone()
+    bt[0, 1] = p.num_blocks + 5          # out of range: tokens 16..31 of sequence 0 must be skipped
+    dev = p.pool_init.to("cuda")
+    pkv.kv_cache_append(dev, to_dev(p.k_ctx), to_dev(p.v_ctx), to_dev(p.cu_ctx_lens),
+                        torch.zeros(2, dtype=torch.int32, device="cuda"), to_dev(bt))
+    assert pkv.get_device_error() == 5
+    assert pkv.get_device_error() == 0     # the word is cleared by the read
+    ref = oracle.empty_cache_bits(p)
+    assert oracle.kv_cache_append(ref, p.k_ctx, p.v_ctx, p.cu_ctx_lens, torch.zeros(2, dtype=torch.int32), bt) == -1
+    assert np.array_equal(cache_bits(dev), ref)
+
+
+# ------------------------------------------------------------------------------------------------
+# decode
+# ------------------------------------------------------------------------------------------------
+
+def test_tiny_decode_all_elements():
+    dec, _ = W.tiny()
+    cache = device_cache(dec)
+    out, lse = run_decode(dec, cache)
+    ref, ref_lse = oracle.attention_of(dec, cache_bits(cache))
+    check_close(out, ref, "f16", roundings=1, what="tiny decode")
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-5, atol=1e-5)
+
+
+LENS = [1, 63, 64, 65, 1000, 3001, 17, 4096]
+
+
+@pytest.mark.parametrize("bs", [8, 16, 32, 64, 128, 512])
+def test_decode_block_sizes(bs):
+    p = problem(lens=LENS, bs=bs, hq=4, hkv=4)
+    cache = device_cache(p)
+    out, lse = run_decode(p, cache)
+    ref, ref_lse = oracle.attention_of(p, cache_bits(cache))
+    check_close(out, ref, "f16", roundings=1, what="bs=%d" % bs)
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-5, atol=1e-5)
+
+
+@pytest.mark.parametrize("dtype", [W.F16, W.BF16])
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (16, 4), (16, 2)])
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_gqa_dtypes(dtype, hq, hkv, d):
+    p = problem(lens=[5, 700, 129, 2000], hq=hq, hkv=hkv, d=d, dtype=dtype, bs=32, seed=hq + hkv + d)
+    cache = device_cache(p)
+    out, lse = run_decode(p, cache)
+    ref, ref_lse = oracle.attention_of(p, cache_bits(cache))
+    check_close(out, ref, dtype, roundings=1, what="%s hq=%d hkv=%d d=%d" % (dtype, hq, hkv, d))
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-5, atol=1e-5)
+
+
+@pytest.mark.parametrize("num_splits", [1, 2, 3, 7, 64])
+def test_decode_explicit_splits_and_fp32_output(num_splits):
+    p = problem(lens=[3000, 64, 1, 2500], hq=8, hkv=2, bs=16, dtype=W.BF16, mb=256)
+    cache = device_cache(p)
+    out, lse = run_decode(p, cache, num_splits=num_splits, out_dtype=torch.float32)
+    ref, ref_lse = oracle.attention_of(p, cache_bits(cache))
+    # FP32 output: no rounding to bf16 anywhere on the decode path -> the literal bounds
+    check_close(out, ref, "bf16", roundings=0, what="splits=%d fp32 out" % num_splits)
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-5, atol=1e-5)
+
+
+def test_decode_special_cases():
+    """Empty context -> 0 / -inf; one token -> V exactly; identical keys -> mean(V)."""
+    L = 300
+    gen = torch.Generator().manual_seed(4)
+    krow = torch.randn(1, 4, 128, generator=gen).to(torch.float16)
+    k = torch.cat([torch.randn(1, 4, 128, generator=gen).to(torch.float16), krow.expand(L, 4, 128)])
+    v = torch.randn(1 + L, 4, 128, generator=gen).to(torch.float16)
+    p = problem(lens=[0, 1, L], hq=4, hkv=4, bs=16)
+    p2 = W.make_problem("s", batch=3, num_q_heads=4, num_kv_heads=4, head_dim=128, block_size=16,
+                        context_lens=[0, 1, L], q_lens=[1, 1, 1], dtype=W.F16, causal=False, seed=5,
+                        num_blocks=p.num_blocks, free_order=list(range(p.num_blocks)), kv_data=(k, v))
+    cache = device_cache(p2)
+    out, lse = run_decode(p2, cache, out_dtype=torch.float32)
+    o = out.cpu()
+    assert torch.all(o[0] == 0) and torch.all(torch.isneginf(lse[0].cpu()))
+    assert torch.equal(o[1], v[0].to(torch.float32))                       # bit-exact V
+    mean_v = v[1:].to(torch.float64).mean(0)
+    assert torch.allclose(o[2].to(torch.float64), mean_v, atol=1e-5, rtol=0)
+
+
+def test_decode_bad_page_flags_error():
+    p = problem(lens=[200, 50], hq=4, hkv=4, bs=16)
+    cache = device_cache(p)
+    bt = p.block_tables.clone()
+    bt[0, 3] = -7
+    pkv.paged_attn_decode(cache, to_dev(p.q), to_dev(bt), to_dev(p.context_lens), scale=p.scale)
+    assert pkv.get_device_error() == 5
+    lens = p.context_lens.clone()
+    lens[1] = 10 ** 6                      # beyond the table's capacity: clamped and flagged
+    pkv.paged_attn_decode(cache, to_dev(p.q), to_dev(p.block_tables), to_dev(lens), scale=p.scale)
+    assert pkv.get_device_error() == 5
+    assert pkv.get_device_error() == 0
+
+
+def test_attn_combine_entry_point():
+    rng = np.random.default_rng(3)
+    po = rng.standard_normal((37, 5, 128))
+    pl = rng.standard_normal((37, 5)) * 3
+    pl[0, :] = -np.inf
+    pl[1, 2:] = -np.inf
+    ref, ref_lse = oracle.attn_combine(po, pl)
+    lse = torch.empty(37, dtype=torch.float32, device="cuda")
+    out = pkv.attn_combine(torch.tensor(po, dtype=torch.float32, device="cuda"),
+                           torch.tensor(pl, dtype=torch.float32, device="cuda"), lse=lse)
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(out.cpu().numpy(), ref, rtol=2e-6, atol=2e-6)
+    got_lse = lse.cpu().numpy()
+    assert np.isneginf(got_lse[0]) and np.all(out[0].cpu().numpy() == 0)
+    np.testing.assert_allclose(got_lse[1:], ref_lse[1:], rtol=1e-6, atol=1e-6)

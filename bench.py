@@ -1,0 +1,552 @@
+#!/usr/bin/env python
+"""Benchmark of attention over a paged KV cache on GB300.
+
+Headline: the 7B-like paged decode step (batch 16, 32 heads x head_dim 128, fp16,
+block_size 16, contexts uniform in [1024, 8192], pages shuffled over a pool 1.2x the
+pages needed). One step = attend one query per sequence to its whole paged context
+(split-KV kernel + merge) and append the new token's K/V. Reported metric: K/V bytes
+read per step / step time (GB/s), next to the decode call's roofline fraction.
+
+Secondary lines (in "extra"): the block-size sweep 8..512 (32 x 4096 tokens, fp16),
+the mixed serving batch (64 lognormal contexts, GQA 32/8, bf16, fragmented pool) and,
+when the prefill kernel is available, the long causal prefill (4 x 8192, bf16, 512-token
+chunks, append then attend).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 launch with torch.distributed.run; every rank is an independent replica with
+its own pool (the path has no exchange step), value = sum over ranks / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention KV-read GB/s (% of HBM peak); prefill attn TFLOP/s"
+L2_BYTES = 129 * 1024 * 1024
+PROFILES = os.path.join(ROOT, "profiles")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default="", help="comma list of extra workloads (bs_sweep,mixed,prefill)")
+    ap.add_argument("--profile", choices=["decode", "append", "prefill"], default=None,
+                    help="small case for ncu captures: W + K launches of one kernel, nothing else timed")
+    return ap.parse_args()
+
+
+def profile_case(args):
+    """A few GB at most on the device, a few launches: the case ncu --set full captures."""
+    import torch
+    from paged_kv_flash_cache_gb300 import build as pkv_build
+    pkv_build.build()
+    import paged_kv_flash_cache_gb300 as pkv
+    from paged_kv_flash_cache_gb300 import workloads as W
+    if args.profile in ("decode", "append"):
+        # 7B-like decode at batch 4: ~0.3 GB of K/V (above L2), same shapes otherwise
+        p = W.decode_7b(batch=4, pool_init="none", device="cuda")
+        cache = torch.zeros((p.num_blocks, 2, 32, 16, 128), dtype=torch.float16, device="cuda")
+        k, v, cu, bt = p.k_ctx.cuda(), p.v_ctx.cuda(), p.cu_ctx_lens.cuda(), p.block_tables.cuda()
+        zeros = torch.zeros(p.batch, dtype=torch.int32, device="cuda")
+        pkv.kv_cache_append(cache, k, v, cu, zeros, bt)
+        q, ctx = p.q.cuda(), p.context_lens.cuda()
+        out = torch.empty((p.batch, 32, 128), dtype=torch.float16, device="cuda")
+        for _ in range(args.warmup + args.steps):
+            if args.profile == "decode":
+                pkv.paged_attn_decode(cache, q, bt, ctx, scale=p.scale, out=out)
+            else:
+                pkv.kv_cache_append(cache, k, v, cu, zeros, bt)
+        torch.cuda.synchronize()
+        assert pkv.get_device_error() == 0
+    else:
+        p = W.prefill_long(batch=1, device="cuda")
+        shape = (p.num_blocks, 2, p.num_kv_heads, p.block_size, p.head_dim)
+        cache = torch.zeros(shape, dtype=p.q.dtype, device="cuda")
+        bt = p.block_tables.cuda()
+        pkv.kv_cache_append(cache, p.k_ctx.cuda(), p.v_ctx.cuda(), p.cu_ctx_lens.cuda(),
+                            torch.zeros(1, dtype=torch.int32, device="cuda"), bt)
+        v = W.prefill_chunk_view(p, 15)
+        q = p.q[v["rows"]].cuda()
+        cu, ctx = v["cu_q_lens"].cuda(), v["context_lens"].cuda()
+        for _ in range(args.warmup + args.steps):
+            pkv.paged_attn_prefill(cache, q, cu, ctx, bt, max_q_len=512, scale=p.scale, causal=True)
+        torch.cuda.synchronize()
+        assert pkv.get_device_error() == 0
+    print("profile case done:", args.profile)
+
+
+# ------------------------------------------------------------------------------------------------
+# distributed plumbing (barrier + max of the timing only; no data-path collective)
+# ------------------------------------------------------------------------------------------------
+
+class Dist:
+    def __init__(self):
+        import torch
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.torch = torch
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if torch.cuda.is_available():
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        t = self.torch.tensor([x], dtype=self.torch.float64,
+                              device="cuda" if self.torch.cuda.is_available() else "cpu")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, x: float) -> float:
+        if not self.pg:
+            return x
+        t = self.torch.tensor([x], dtype=self.torch.float64,
+                              device="cuda" if self.torch.cuda.is_available() else "cpu")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks: nvidia-smi sampled in the background, kept for the timed window
+# ------------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.QUERY,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [s for t, s in self.samples if t0 <= t <= t1]
+        window = "timed"
+        if not inside:
+            # timed region shorter than the sampling period: nearest samples around it
+            near = sorted(self.samples, key=lambda ts: min(abs(ts[0] - t0), abs(ts[0] - t1)))[:3]
+            inside = [s for _, s in near]
+            window = "nearest to timed region (region shorter than the 100 ms sampling period)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        mhz = [float(s[1]) for s in inside if s[1].replace(".", "").isdigit()]
+        mx = [float(s[2]) for s in inside if s[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in inside for i in range(4) if len(s) > 5 + i and s[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside), "window": window}
+
+
+# ------------------------------------------------------------------------------------------------
+# measured peaks and committed ncu traffic figures
+# ------------------------------------------------------------------------------------------------
+
+def peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def kernel_source_hash(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, "paged_kv_flash_cache_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(summary_name: str, files) -> float | None:
+    """Per-launch DRAM bytes from a committed ncu summary, if it was taken on the current source."""
+    p = os.path.join(PROFILES, summary_name)
+    if not os.path.exists(p):
+        return None
+    kv = {}
+    for line in open(p):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("source_sha256_16") != kernel_source_hash(files):
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------------------------------------
+# workloads on the device
+# ------------------------------------------------------------------------------------------------
+
+def device_problem(p, torch):
+    """Move a generated problem to the GPU: pool allocated, context appended by the library."""
+    import paged_kv_flash_cache_gb300 as pkv
+    shape = (p.num_blocks, 2, p.num_kv_heads, p.block_size, p.head_dim)
+    cache = torch.zeros(shape, dtype=p.k_ctx.dtype, device="cuda")
+    pkv.kv_cache_append(cache, p.k_ctx.cuda(), p.v_ctx.cuda(), p.cu_ctx_lens.cuda(),
+                        torch.zeros(p.batch, dtype=torch.int32, device="cuda"), p.block_tables.cuda())
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    return cache
+
+
+def decode_bytes(p) -> dict:
+    """Algorithmic bytes of one decode call: K/V of every cached token once per KV head, q in,
+    output out, the block-table entries and context lengths read."""
+    kv = p.kv_bytes_read()
+    qo = 2 * p.batch * p.num_q_heads * p.head_dim * 2
+    pages = sum((int(L) + p.block_size - 1) // p.block_size for L in p.context_lens.tolist())
+    table = pages * 4 + p.batch * 4
+    return {"kv": kv, "total": kv + qo + table}
+
+
+def time_loop(torch, fn, steps, stream, inner_events=None):
+    """K calls of fn between two events on `stream`; returns total ms."""
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        fn(i)
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end)
+
+
+def bench_decode(torch, p, steps, warmup, dist, want_clocks=True):
+    import paged_kv_flash_cache_gb300 as pkv
+    from paged_kv_flash_cache_gb300 import workloads as W
+    cache = device_problem(p, torch)
+    q = p.q.cuda()
+    ctx = p.context_lens.cuda()
+    step_in = W.append_step(p, seed=7)
+    bt = step_in["block_tables"].cuda()
+    k_new, v_new = step_in["k_new"].cuda(), step_in["v_new"].cuda()
+    cu_new, before = step_in["cu_new_lens"].cuda(), step_in["ctx_before"].cuda()
+    mb = bt.shape[1]
+    ws_bytes = pkv.decode_workspace_size(p.batch, p.num_q_heads, p.num_kv_heads, p.head_dim, p.block_size, mb)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
+    out = torch.empty((p.batch, p.num_q_heads, p.head_dim), dtype=q.dtype, device="cuda")
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+
+    def step(i, timed=False):
+        if timed:
+            ev[i][0].record(stream)
+        pkv.paged_attn_decode(cache, q, bt, ctx, scale=p.scale, workspace=ws, out=out)
+        if timed:
+            ev[i][1].record(stream)
+        pkv.kv_cache_append(cache, k_new, v_new, cu_new, before, bt)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    sampler = ClockSampler(torch.cuda.current_device()) if want_clocks else None
+    if sampler:
+        time.sleep(0.3)
+    dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    ms = time_loop(torch, lambda i: step(i, True), steps, stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    dist.barrier()
+    decode_ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+    clocks = None
+    if sampler:
+        time.sleep(0.25)
+        sampler.stop()
+        clocks = sampler.summary(t0, t1)
+    assert pkv.get_device_error() == 0
+    res = {"ms_total": ms, "ms_per_step": ms / steps, "decode_ms": decode_ms, "clocks": clocks,
+           "launches_per_step": 3, "bytes": decode_bytes(p)}
+    # end to end through the public API: inputs copied from pinned host memory every step,
+    # the step's output read back
+    h_q = p.q.cpu().pin_memory()
+    h_k, h_v = step_in["k_new"].pin_memory(), step_in["v_new"].pin_memory()
+    h_cu, h_before = step_in["cu_new_lens"].pin_memory(), step_in["ctx_before"].pin_memory()
+    h_bt, h_ctx = step_in["block_tables"].pin_memory(), p.context_lens.pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new)
+    d_cu, d_before, d_bt, d_ctx = (torch.empty_like(cu_new), torch.empty_like(before), torch.empty_like(bt),
+                                   torch.empty_like(ctx))
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_cu, h_before, h_bt, h_ctx))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step(i):
+        for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_cu, h_cu), (d_before, h_before), (d_bt, h_bt),
+                     (d_ctx, h_ctx)):
+            d.copy_(h, non_blocking=True)
+        pkv.paged_attn_decode(cache, d_q, d_bt, d_ctx, scale=p.scale, workspace=ws, out=out)
+        pkv.kv_cache_append(cache, d_k, d_v, d_cu, d_before, d_bt)
+        h_out.copy_(out, non_blocking=True)
+
+    for i in range(warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    dist.barrier()
+    e2e_ms = time_loop(torch, e2e_step, steps, stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    res.update(e2e_ms_per_step=e2e_ms / steps, h2d=h2d, d2h=d2h)
+    del cache
+    torch.cuda.empty_cache()
+    return res
+
+
+def cpu_baseline_decode(p, budget_s=8.0):
+    """The oracle as it stands, all host cores, on the same decode workload (whole batch,
+    repeated until `budget_s` of wall time is spent)."""
+    import oracle
+    oracle.build()
+    t_build = time.time()
+    cache = oracle.build_cache(p)
+    t_build = time.time() - t_build
+    cores = os.cpu_count() or 1
+    reps, t = 0, 0.0
+    while t < budget_s and reps < 50:
+        t0 = time.time()
+        oracle.attention_of(p, cache, nthreads=cores)
+        t += time.time() - t0
+        reps += 1
+    gbs = p.kv_bytes_read() * reps / t / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": "whole decode batch (%d sequences x %d heads, %d cached tokens), %d repetition(s), %.1f s; "
+                      "fp64 token walk + two-pass softmax; cache build %.1f s not timed"
+                      % (p.batch, p.num_q_heads, int(p.context_lens.sum()), reps, t, t_build)}
+
+
+def bench_bs_sweep(torch, steps, warmup):
+    import paged_kv_flash_cache_gb300 as pkv
+    from paged_kv_flash_cache_gb300 import workloads as W
+    kv = W.bs_sweep_kv(device="cuda")
+    out = {}
+    pk = peaks()
+    for bs in (8, 16, 32, 64, 128, 512):
+        p = W.bs_sweep(bs, kv_data=kv, pool_init="none", device="cuda")
+        cache = device_problem(p, torch)
+        q, bt, ctx = p.q.cuda(), p.block_tables.cuda(), p.context_lens.cuda()
+        ws = torch.empty(max(16, pkv.decode_workspace_size(p.batch, 32, 32, 128, bs, bt.shape[1])),
+                         dtype=torch.uint8, device="cuda")
+        o = torch.empty((p.batch, 32, 128), dtype=q.dtype, device="cuda")
+        fn = lambda i: pkv.paged_attn_decode(cache, q, bt, ctx, scale=p.scale, workspace=ws, out=o)
+        for i in range(warmup):
+            fn(i)
+        ms = time_loop(torch, fn, steps, torch.cuda.current_stream()) / steps
+        b = decode_bytes(p)
+        out[str(bs)] = {"ms": round(ms, 4), "kv_gbs": round(b["kv"] / ms / 1e6, 1),
+                        "frac_of_hbm": round(b["total"] / ms / 1e6 / pk["hbm_gbs"], 3)}
+        del cache
+        torch.cuda.empty_cache()
+    vals = [out[k]["kv_gbs"] for k in ("16", "32", "64", "128")]
+    return {"workload": "32 seqs x 4096 ctx, 32 heads x 128, fp16, identical K/V data per block size, "
+                        "pool = pages needed, randomly permuted", "per_block_size": out,
+            "flatness_16_128": round(min(vals) / max(vals), 3)}
+
+
+def bench_mixed(torch, steps, warmup):
+    import paged_kv_flash_cache_gb300 as pkv
+    from paged_kv_flash_cache_gb300 import workloads as W
+    p = W.mixed_serving(pool_init="none", device="cuda")
+    cache = device_problem(p, torch)
+    q, bt, ctx = p.q.cuda(), p.block_tables.cuda(), p.context_lens.cuda()
+    ws = torch.empty(max(16, pkv.decode_workspace_size(p.batch, 32, 8, 128, 32, bt.shape[1])), dtype=torch.uint8,
+                     device="cuda")
+    o = torch.empty((p.batch, 32, 128), dtype=q.dtype, device="cuda")
+    fn = lambda i: pkv.paged_attn_decode(cache, q, bt, ctx, scale=p.scale, workspace=ws, out=o)
+    for i in range(warmup):
+        fn(i)
+    ms = time_loop(torch, fn, steps, torch.cuda.current_stream()) / steps
+    b = decode_bytes(p)
+    del cache
+    torch.cuda.empty_cache()
+    return {"workload": "64 seqs, lognormal ctx (median 2048, sigma 1, [16, 32768]), GQA 32/8, 128, bf16, "
+                        "bs 32, fragmented pool 2x", "total_ctx_tokens": int(p.context_lens.sum()),
+            "ms": round(ms, 4), "kv_gbs": round(b["kv"] / ms / 1e6, 1),
+            "frac_of_hbm": round(b["total"] / ms / 1e6 / peaks()["hbm_gbs"], 3),
+            "tokens_per_s": round(p.batch / ms * 1e3, 1)}
+
+
+def bench_prefill(torch, steps, warmup):
+    import paged_kv_flash_cache_gb300 as pkv
+    from paged_kv_flash_cache_gb300 import workloads as W
+    p = W.prefill_long(device="cuda")
+    shape = (p.num_blocks, 2, p.num_kv_heads, p.block_size, p.head_dim)
+    cache = torch.zeros(shape, dtype=p.q.dtype, device="cuda")
+    bt = p.block_tables.cuda()
+    chunks = []
+    for c in range(8192 // p.meta["chunk"]):
+        v = W.prefill_chunk_view(p, c)
+        rows = v["rows"].cuda()
+        chunks.append(dict(q=p.q[rows].contiguous(), k=p.k_ctx[rows].contiguous(), v=p.v_ctx[rows].contiguous(),
+                           cu=v["cu_q_lens"].cuda(), ctx=v["context_lens"].cuda(), before=v["ctx_before"].cuda(),
+                           out=torch.empty_like(p.q[rows]), ql=int(v["q_lens"][0])))
+
+    def step(i):
+        for ch in chunks:
+            pkv.kv_cache_append(cache, ch["k"], ch["v"], ch["cu"], ch["before"], bt)
+            pkv.paged_attn_prefill(cache, ch["q"], ch["cu"], ch["ctx"], bt, max_q_len=ch["ql"], scale=p.scale,
+                                   causal=True, out=ch["out"])
+
+    step(0)
+    torch.cuda.synchronize()
+    for i in range(warmup):
+        step(i)
+    ms = time_loop(torch, step, steps, torch.cuda.current_stream()) / steps
+    flops = p.causal_flops()
+    del cache
+    torch.cuda.empty_cache()
+    return {"workload": "4 x 8192 causal prefill, 32 heads x 128, bf16, bs 16 pages, 16 chunks of 512 "
+                        "(append chunk, then attend)", "ms_per_pass": round(ms, 3),
+            "tflops": round(flops / ms / 1e9, 1), "frac_of_dense_bf16": round(flops / ms / 1e9 / peaks()["bf16_tflops"], 3),
+            "prompt_tokens_per_s": round(4 * 8192 / ms * 1e3, 1)}
+
+
+# ------------------------------------------------------------------------------------------------
+
+def main():
+    args = parse()
+    if args.profile:
+        profile_case(args)
+        return
+    import torch
+    dist = Dist()
+    workload_cfg = {"workload": "7B-like paged decode step: batch 16, 32 heads x head_dim 128, fp16, block_size 16, "
+                                "contexts uniform in [1024, 8192] (seeded), pages shuffled over a pool 1.2x the "
+                                "pages needed",
+                    "step": "paged_attn_decode (split-KV kernel + merge kernel) then kv_cache_append of the new "
+                            "token (16 tokens)",
+                    "l2": "inputs larger than L2: %.2f GB of K/V read per step vs 129 MB L2" % 0,
+                    "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
+    if args.impl == "reference":
+        # The oracle is the reference arm: rank 0 only, on the host cores.
+        if dist.rank != 0:
+            dist.close()
+            return
+        from paged_kv_flash_cache_gb300 import workloads as W
+        p = W.decode_7b(pool_init="none", device="cuda" if torch.cuda.is_available() else "cpu")
+        workload_cfg["l2"] = "n/a (CPU)"
+        import oracle
+        oracle.build()
+        cache = oracle.build_cache(p)
+        cores = os.cpu_count() or 1
+        for _ in range(args.warmup):
+            oracle.attention_of(p, cache, nthreads=cores)
+        t0 = time.time()
+        for _ in range(args.steps):
+            oracle.attention_of(p, cache, nthreads=cores)
+        dt = (time.time() - t0) / args.steps
+        v = p.kv_bytes_read() / dt / 1e9
+        line = {"metric": METRIC, "value": round(v, 3), "unit": "GB/s", "impl": "reference", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": workload_cfg,
+                "cpu_baseline": {"value": round(v, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                 "sample": "whole decode batch per step (16 seqs x 32 heads, %d cached tokens)"
+                                           % int(p.context_lens.sum())},
+                "e2e": {"value": round(v, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        dist.close()
+        return
+
+    from paged_kv_flash_cache_gb300 import build as pkv_build
+    pkv_build.build()
+    import paged_kv_flash_cache_gb300 as pkv
+    from paged_kv_flash_cache_gb300 import workloads as W
+    torch.cuda.set_device(dist.local)
+    pk = peaks()
+    p = W.decode_7b(seed=1236 + 100 * dist.rank, pool_init="none", device="cuda")
+    r = bench_decode(torch, p, args.steps, args.warmup, dist)
+    kv_gb = r["bytes"]["kv"] / 1e9
+    workload_cfg["l2"] = "inputs larger than L2: %.2f GB of K/V read per step vs 129 MB L2" % kv_gb
+    ms = dist.max(r["ms_per_step"])
+    total_kv = dist.sum(r["bytes"]["kv"])
+    value = total_kv / (ms * 1e-3) / 1e9
+    e2e_ms = dist.max(r["e2e_ms_per_step"])
+    achieved = r["bytes"]["total"] / (r["decode_ms"] * 1e-3) / 1e9
+    files = ["decode.cu", "pkv_device.cuh", "pkv_internal.h"]
+    roofline = {"bound": "hbm", "kernel": "paged_attn_decode call (decode_split_kernel + combine_kernel)",
+                "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / pk["hbm_gbs"], 3), "peak_source": pk["source"],
+                "traffic": ncu_traffic("decode_split_7b_ncu.txt", files),
+                "algorithmic_bytes_per_launch": r["bytes"]["total"], "avg_launch_ms": round(r["decode_ms"], 4)}
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16", "data": "synthetic", "config": workload_cfg,
+            "roofline": roofline,
+            "e2e": {"value": round(total_kv / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                    "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+            "gpu_launches": r["launches_per_step"] * args.steps, "clocks": r["clocks"],
+            "tokens_per_s": round(args.gpus * p.batch / (ms * 1e-3), 1)}
+    if dist.rank == 0 and not args.no_extra:
+        extra = {}
+        only = set(filter(None, args.only.split(",")))
+        for name, fn in (("bs_sweep", bench_bs_sweep), ("mixed", bench_mixed), ("prefill", bench_prefill)):
+            if only and name not in only:
+                continue
+            try:
+                extra[name] = fn(torch, max(3, args.steps // 4), 3)
+            except Exception as e:  # a secondary workload must not hide the headline line
+                extra[name] = {"error": "%s: %s" % (type(e).__name__, str(e)[:200])}
+        line["extra"] = extra
+    if dist.rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_decode(p)
+    if dist.rank == 0:
+        print(json.dumps(line))
+    dist.close()
+
+
+if __name__ == "__main__":
+    main()

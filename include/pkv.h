@@ -163,6 +163,31 @@ PKV_API pkv_status pkv_attn_combine(const float *partial_o, const float *partial
                             int num_splits, int head_dim, void *out, pkv_dtype out_dtype,
                             float *lse, void *stream);
 
+/* paged_attn_decode_noalloc -- the same computation and arguments as
+ * pkv_paged_attn_decode, for callers that cannot allocate device memory: a plugin
+ * that its host framework hands only input and output buffers (no workspace, no
+ * allocator), or a runtime that reserves all device memory in its own pool up front.
+ * The paper has no counterpart: this is a deployment convenience, not part of the
+ * method.
+ *   - Allocates nothing (no cudaMalloc, cudaFree or allocating library call).  The
+ *     split partials live in a fixed array of PKV_DECODE_NOALLOC_SCRATCH_BYTES that
+ *     the library keeps in device memory; every GPU that loads the library holds it
+ *     until the process exits.
+ *   - Sizes whose workspace (pkv_decode_workspace_size) exceeds that array are
+ *     rejected with PKV_ERR_WORKSPACE before anything is launched.
+ *   - The first call on each device (that device current) looks up the array's device
+ *     address with cudaGetSymbolAddress; make that first call before any stream
+ *     capture.
+ *   - All calls share the one array, which keeps the last call's contents.  Nothing
+ *     in it has to start at zero: each call writes every partial it later reads.
+ *     Calls that overlap on the GPU (concurrent streams, or several host threads)
+ *     race on the array: serialise them. */
+#define PKV_DECODE_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+PKV_API pkv_status pkv_paged_attn_decode_noalloc(pkv_cache cache, const void *q, int num_q_heads,
+                                         const int *block_tables, const int *context_lens, int batch,
+                                         int max_blocks_per_seq, float scale, int num_splits,
+                                         void *out, pkv_dtype out_dtype, float *lse, void *stream);
+
 /* Synchronise `stream`, then read and clear the sticky device error word of the
  * current device.  *code receives PKV_OK, PKV_ERR_DEVICE_RANGE or PKV_ERR_TIMEOUT.
  * Returns PKV_ERR_CUDA if the synchronisation or the read fails. */

@@ -23,6 +23,7 @@ from typing import Optional
 __all__ = [
     "PkvError", "library_path", "load_library", "kv_cache_append", "paged_attn_decode", "paged_attn_prefill",
     "attn_combine", "decode_workspace_size", "decode_split_tokens", "get_device_error", "STATUS",
+    "paged_attn_decode_noalloc",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -36,8 +37,9 @@ F16, BF16, F32 = 0, 1, 2
 
 # Every symbol include/pkv.h declares.
 EXPORTS = ("pkv_kv_cache_append", "pkv_decode_workspace_size", "pkv_decode_split_tokens", "pkv_paged_attn_decode",
-           "pkv_paged_attn_prefill", "pkv_attn_combine", "pkv_get_device_error", "pkv_status_string",
-           "pkv_version")
+           "pkv_paged_attn_decode_noalloc", "pkv_paged_attn_prefill", "pkv_attn_combine", "pkv_get_device_error",
+           "pkv_status_string", "pkv_version")
+DECODE_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024   # PKV_DECODE_NOALLOC_SCRATCH_BYTES in include/pkv.h
 
 
 class PkvError(RuntimeError):
@@ -74,6 +76,8 @@ def load_library():
         lib.pkv_decode_split_tokens.restype = I
         lib.pkv_paged_attn_decode.argtypes = [_Cache, P, I, P, P, I, I, F, I, P, Z, P, I, P, P]
         lib.pkv_paged_attn_decode.restype = I
+        lib.pkv_paged_attn_decode_noalloc.argtypes = [_Cache, P, I, P, P, I, I, F, I, P, I, P, P]
+        lib.pkv_paged_attn_decode_noalloc.restype = I
         lib.pkv_paged_attn_prefill.argtypes = [_Cache, P, I, P, P, P, I, I, I, I, F, I, P, I, P, P]
         lib.pkv_paged_attn_prefill.restype = I
         lib.pkv_attn_combine.argtypes = [P, P, I, I, I, P, I, P, P]
@@ -192,6 +196,28 @@ def paged_attn_decode(cache, q, block_tables, context_lens, scale: Optional[floa
                                      _dev(workspace, "workspace"), ws_bytes, _dev(out, "out"),
                                      _dtype_code(out.dtype), _dev(lse, "lse"), _stream(stream)),
            "pkv_paged_attn_decode")
+    return out
+
+
+def paged_attn_decode_noalloc(cache, q, block_tables, context_lens, scale: Optional[float] = None,
+                              num_splits: int = 0, out=None, out_dtype=None, lse=None, stream=None):
+    """paged_attn_decode without a workspace: for callers that cannot allocate device memory.
+    The split partials go to a fixed array the library holds on each device (see
+    include/pkv.h); sizes needing more than DECODE_NOALLOC_SCRATCH_BYTES raise PkvError
+    (PKV_ERR_WORKSPACE). Calls sharing a device must not overlap on the GPU. Returns `out`
+    (allocated here with PyTorch only when the caller passes none)."""
+    torch = _torch()
+    lib = load_library()
+    c = _cache_struct(cache)
+    batch, hq, d = q.shape
+    mb = block_tables.shape[1]
+    if out is None:
+        out = torch.empty((batch, hq, d), dtype=out_dtype or cache.dtype, device=q.device)
+    scale = (1.0 / math.sqrt(d)) if scale is None else float(scale)
+    _check(lib.pkv_paged_attn_decode_noalloc(c, _dev(q, "q"), hq, _i32(block_tables, "block_tables"),
+                                             _i32(context_lens, "context_lens"), batch, mb, scale, int(num_splits),
+                                             _dev(out, "out"), _dtype_code(out.dtype), _dev(lse, "lse"),
+                                             _stream(stream)), "pkv_paged_attn_decode_noalloc")
     return out
 
 

@@ -30,7 +30,7 @@
 namespace pkv {
 namespace {
 
-constexpr int kConsumerWarps = 4;
+constexpr int kConsumerWarps = 8;
 constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStages = 4;
 constexpr int kMaxBatch = 2048;  // context lengths + unit prefix kept in shared memory
@@ -38,11 +38,11 @@ constexpr int kMaxBatch = 2048;  // context lengths + unit prefix kept in shared
 template <int D, int G>
 struct DecodeLayout {
     static constexpr int kTile = kDecodeTile;
-    static constexpr int kTokPerWarp = kTile / kConsumerWarps;      // 16
+    static constexpr int kTokPerWarp = kTile / kConsumerWarps;      // 8
     static constexpr int kLanesPerTok = D / 8;                      // 16 (D=128) or 8 (D=64)
     static constexpr int kTokPerStep = 32 / kLanesPerTok;           // 2 or 4
-    static constexpr int kSteps = kTokPerWarp / kTokPerStep;        // 8 or 4
-    static constexpr int kStepsPerBatch = (kSteps * G <= 32) ? kSteps : (32 / G);  // bounds registers
+    static constexpr int kSteps = kTokPerWarp / kTokPerStep;        // 4 or 2
+    static constexpr int kStepsPerBatch = (kSteps * G <= 16) ? kSteps : (16 / G);  // bounds registers
     static constexpr size_t kKBytes = (size_t)kTile * D * 2;
     static constexpr size_t kQBytes = (size_t)G * D * 2;
     static constexpr size_t kStageBytes = ((2 * kKBytes + kQBytes) + 127) / 128 * 128;
@@ -209,30 +209,32 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
     const int slot = lane / L::kLanesPerTok;   // token slot within a step
     const int chk = lane % L::kLanesPerTok;    // this lane's 8-element chunk of D
     const float qscale = a.scale * kLog2e;     // scores in log2 units
-    float qf[G][8];
+    float2 qf[G][4];                           // q chunk, scaled, as fp32 pairs
     int stage = 0;
     uint32_t phase = 0;
     for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
         const UnitCursor c = unit_of(u, prefix, lens, a.batch, hkv, chunk);
-        float m[G], l[G], acc[G][8];
+        float m[G], l[G];
+        float2 acc[G][4];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
             m[g] = -INFINITY;
             l[g] = 0.f;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[g][j] = 0.f;
+            for (int j = 0; j < 4; ++j) acc[g][j] = make_float2(0.f, 0.f);
         }
         for (int ts = c.t0; ts < c.t1; ts += L::kTile) {
             const int n = min(L::kTile, c.t1 - ts);
             if (!mbar_wait(&full[stage], phase, abort_flag, a.err)) return;
             const uint8_t *st = smem + (size_t)stage * L::kStageBytes;
             if (ts == c.t0) {
+                const float2 qs2 = make_float2(qscale, qscale);
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
                     const uint4 raw = *reinterpret_cast<const uint4 *>(st + 2 * L::kKBytes + ((size_t)g * D + chk * 8) * 2);
-                    unpack8(raw, qf[g], Tag());
+                    unpack8x2(raw, qf[g], Tag());
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) qf[g][j] *= qscale;
+                    for (int j = 0; j < 4; ++j) qf[g][j] = fmul2(qf[g][j], qs2);
                 }
             }
             const uint8_t *sk = st;
@@ -246,13 +248,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
                     const int t = warp * L::kTokPerWarp + (b0 + i) * L::kTokPerStep + slot;
                     valid[i] = t < n;
                     const uint4 raw = *reinterpret_cast<const uint4 *>(sk + ((size_t)t * D + chk * 8) * 2);
-                    float kf[8];
-                    unpack8(raw, kf, Tag());
+                    float2 kf[4];
+                    unpack8x2(raw, kf, Tag());
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
-                        float part = 0.f;
+                        float2 pp = fmul2(qf[g][0], kf[0]);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) part = fmaf(qf[g][j], kf[j], part);
+                        for (int j = 1; j < 4; ++j) pp = ffma2(qf[g][j], kf[j], pp);
+                        float part = pp.x + pp.y;
 #pragma unroll
                         for (int o = L::kLanesPerTok / 2; o > 0; o >>= 1)
                             part += __shfl_xor_sync(0xffffffffu, part, o);
@@ -268,8 +271,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
                     if (m_new != -INFINITY) {
                         const float alpha = exp2f(m[g] - m_new);  // 0 when m[g] = -inf
                         l[g] *= alpha;
+                        const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) acc[g][j] *= alpha;
+                        for (int j = 0; j < 4; ++j) acc[g][j] = fmul2(acc[g][j], a2);
                         m[g] = m_new;
                     }
 #pragma unroll
@@ -283,12 +287,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
                     if (!valid[i]) continue;
                     const int t = warp * L::kTokPerWarp + (b0 + i) * L::kTokPerStep + slot;
                     const uint4 raw = *reinterpret_cast<const uint4 *>(sv + ((size_t)t * D + chk * 8) * 2);
-                    float vf[8];
-                    unpack8(raw, vf, Tag());
+                    float2 vf[4];
+                    unpack8x2(raw, vf, Tag());
 #pragma unroll
-                    for (int g = 0; g < G; ++g)
+                    for (int g = 0; g < G; ++g) {
+                        const float2 p2 = make_float2(s[i][g], s[i][g]);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) acc[g][j] = fmaf(s[i][g], vf[j], acc[g][j]);
+                        for (int j = 0; j < 4; ++j) acc[g][j] = ffma2(p2, vf[j], acc[g][j]);
+                    }
                 }
             }
             __syncwarp();
@@ -310,9 +316,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
                 const float wb = (mo == -INFINITY) ? 0.f : exp2f(mo - mn);
                 l[g] = l[g] * wa + lo * wb;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float ao = __shfl_xor_sync(0xffffffffu, acc[g][j], o);
-                    acc[g][j] = acc[g][j] * wa + ao * wb;
+                for (int j = 0; j < 4; ++j) {
+                    const float ax = __shfl_xor_sync(0xffffffffu, acc[g][j].x, o);
+                    const float ay = __shfl_xor_sync(0xffffffffu, acc[g][j].y, o);
+                    acc[g][j].x = acc[g][j].x * wa + ax * wb;
+                    acc[g][j].y = acc[g][j].y * wa + ay * wb;
                 }
                 m[g] = mn;
             }
@@ -323,7 +331,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
             for (int g = 0; g < G; ++g) {
                 float *row = merge + ((size_t)warp * G + g) * (D + 2);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) row[chk * 8 + j] = acc[g][j];
+                for (int j = 0; j < 4; ++j) {
+                    row[chk * 8 + 2 * j] = acc[g][j].x;
+                    row[chk * 8 + 2 * j + 1] = acc[g][j].y;
+                }
                 if (chk == 0) {
                     row[D] = m[g];
                     row[D + 1] = l[g];

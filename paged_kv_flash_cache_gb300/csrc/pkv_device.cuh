@@ -138,6 +138,50 @@ __device__ __forceinline__ void unpack8(const uint4 &raw, float (&f)[8], BF16Tag
     }
 }
 
+// Eight packed 16-bit values to four fp32 pairs (element 2i in .x, 2i+1 in .y).
+__device__ __forceinline__ void unpack8x2(const uint4 &raw, float2 (&f)[4], F16Tag) {
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __half2 h;
+        memcpy(&h, &w[i], 4);
+        f[i] = __half22float2(h);
+    }
+}
+
+__device__ __forceinline__ void unpack8x2(const uint4 &raw, float2 (&f)[4], BF16Tag) {
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+}
+
+// Paired FP32 arithmetic of sm_100-class GPUs (one instruction for two lanes of a float2).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rc, ra, rb, rc;\n\tmov.b64 {%0, %1}, rc;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 ra, ra, rb;\n\tmov.b64 {%0, %1}, ra;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // Output element store with a single round-to-nearest-even conversion.
 // out_dtype: 0 = fp16, 1 = bf16, 2 = fp32.
 __device__ __forceinline__ void store_out(void *out, size_t idx, float v, int out_dtype) {

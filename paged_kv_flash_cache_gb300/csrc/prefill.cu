@@ -9,20 +9,22 @@
 // flag of the library call quoted there.  Prefill is the matrix-matrix phase ("为什么Attention是
 // O(n²)", prefill / decode section): Q K^T and P V are dense contractions and run as tcgen05.mma.
 //
-// CTA = one query head x 128 query rows of one sequence (192 threads):
-//   warp 0     TMA producer: Q tile once (3-D tensor map over [total_q, Hq, D]); for each
-//              128-key tile, the pages it covers are looked up in the block table by the
-//              warp's lanes and each lane issues its page's K and V boxes (2-D tensor map over
-//              the cache viewed as rows of D elements), 128-byte swizzle, into a 2-stage ring;
-//   warp 1     TMEM owner and MMA issuer (one thread): S = Q K^T into TMEM columns [0, 128),
-//              then O += P V into columns [128, 128 + D); S of tile j+1 is issued as soon as the
-//              softmax has read S of tile j, so the tensor pipe works during the softmax;
-//   warps 2-5  softmax / epilogue, one query row per thread (TMEM lane = row): scale, causal and
-//              context masks, row max, exp2, row sum, P (input dtype) written to shared memory in
-//              the swizzled K-major layout the MMA reads; O is rescaled in TMEM only when the
-//              running max grows by more than 2^8 (the final O / l uses the same max, so the
-//              result is exact); the epilogue reads O from TMEM, divides by l, writes out / lse.
-// Every wait is bounded (a timeout sets the device error word and the CTA winds down).
+// CTA = one query head x 256 query rows of one sequence, as two 128-row tiles A and B that share
+// every K/V tile (384 threads, three warpgroups):
+//   warp 0     TMA producer: both Q tiles once (3-D tensor map over [total_q, Hq, D]); then for
+//              each 128-key tile j the K tile and the V tile, each into one slot of a 4-slot ring:
+//              the pages a tile covers are looked up in the block table by the warp's lanes and each
+//              lane issues its page's boxes (2-D tensor map over the cache viewed as rows of D
+//              elements, 128-byte swizzle);
+//   warp 1     TMEM owner and MMA issuer (one thread). TMEM columns: S [0,128) shared by the two
+//              tiles, P_A [128,192), P_B [192,256), O_A [256,256+D), O_B [384,384+D). Per key tile:
+//              S = Q_A K^T, S = Q_B K^T (each after the other tile's softmax has read S),
+//              O_A += P_A V, O_B += P_B V with P read from TMEM (only V comes from shared memory);
+//   WG 1, 2    softmax of tile A / tile B, one query row per thread (TMEM lane = row): scale,
+//              causal / context masks, running max (O rescaled in TMEM only when the max grows by
+//              more than 2^8; the final O / l uses the same max, so the result is exact), exp2, row
+//              sum, P in the input dtype written to TMEM; epilogue O / l -> out, lse.
+// Warpgroup 0 gives registers to the two softmax warpgroups (setmaxnreg).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -35,26 +37,25 @@
 namespace pkv {
 namespace {
 
-constexpr int kBM = 128;       // query rows per CTA
+constexpr int kBM = 128;       // query rows per tile
+constexpr int kRows = 256;     // query rows per CTA (tiles A and B)
 constexpr int kBN = 128;       // keys per KV tile
-constexpr int kStages = 2;     // KV ring depth
-constexpr int kThreads = 192;  // 6 warps
+constexpr int kRing = 4;       // K/V ring slots
+constexpr int kThreads = 384;  // 3 warpgroups
 constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by more than 2^8
+constexpr uint32_t kColS = 0, kColP = 128, kColO = 256;
 
 template <int D>
 struct PrefillLayout {
     static constexpr int kHalves = D / 64;                      // 128-byte swizzle atoms along D
     static constexpr uint32_t kTileHalf = 128 * 128;            // 128 rows x 128 bytes
-    static constexpr uint32_t kQBytes = kHalves * kTileHalf;
-    static constexpr uint32_t kKVBytes = kHalves * kTileHalf;   // one K (or V) tile
-    static constexpr uint32_t kPBytes = 2 * kTileHalf;          // 128 rows x 128 keys
+    static constexpr uint32_t kQBytes = kHalves * kTileHalf;    // one 128-row Q tile
+    static constexpr uint32_t kKVBytes = kHalves * kTileHalf;   // one K or V tile
     static constexpr uint32_t kQOff = 0;
-    static constexpr uint32_t kKVOff = kQOff + kQBytes;         // stage s: K at +2*s*kKVBytes, V after it
-    static constexpr uint32_t kPOff = kKVOff + kStages * 2 * kKVBytes;
-    static constexpr uint32_t kBarOff = kPOff + kPBytes;
-    static constexpr uint32_t kSmemBytes = kBarOff + 128 + 1024;  // barriers + alignment slack
-    static constexpr uint32_t kTmemCols = 256;                    // S: 128 columns, O: D columns
-    static constexpr uint32_t kOCol = 128;
+    static constexpr uint32_t kRingOff = 2 * kQBytes;
+    static constexpr uint32_t kBarOff = kRingOff + kRing * kKVBytes;
+    static constexpr uint32_t kSmemBytes = kBarOff + 256 + 1024;  // barriers + alignment slack
+    static constexpr uint32_t kTmemCols = 512;
 };
 
 struct PrefillParams {
@@ -92,47 +93,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 1024-byte alignment: the 128-byte swizzle pattern is a function of address bits 4-9.
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint8_t *sQ = smem + Lay::kQOff;
-    uint8_t *sP = smem + Lay::kPOff;
+    uint8_t *sRing = smem + Lay::kRingOff;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::kBarOff);
-    uint64_t *full = bars;        // [kStages] K/V tile landed
-    uint64_t *empty = bars + 2;   // [kStages] K/V stage free again
-    uint64_t *q_full = bars + 4;
-    uint64_t *s_full = bars + 5;  // S_j in TMEM
-    uint64_t *s_free = bars + 6;  // softmax has read S_j
-    uint64_t *p_full = bars + 7;  // P_j in shared memory (and O rescaled)
-    uint64_t *o_done = bars + 8;  // P_j V_j accumulated into O
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 9);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 10);
-    uint64_t *drain = bars + 11;  // every MMA issued has completed (before TMEM is freed)
+    uint64_t *kv_full = bars;            // [kRing]
+    uint64_t *kv_empty = bars + 4;       // [kRing]
+    uint64_t *q_full = bars + 8;
+    uint64_t *s_full = bars + 9;         // [2] S of tile A / B computed
+    uint64_t *s_free = bars + 11;        // [2] softmax A / B has read S
+    uint64_t *p_full = bars + 13;        // [2] P_A / P_B in TMEM (and O rescaled)
+    uint64_t *o_done = bars + 15;        // [2] P V accumulated into O_A / O_B
+    uint64_t *drain = bars + 17;         // every MMA issued has completed
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 18);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 19);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int mt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int q0 = __ldg(p.cu_q_lens + b);
     const int q_len = __ldg(p.cu_q_lens + b + 1) - q0;
-    const int m_start = mt * kBM;
+    const int m_start = mt * kRows;
     if (m_start >= q_len) return;  // uniform: nothing allocated yet
-    int L = __ldg(p.context_lens + b);
-    const int cap = p.mb * p.bs;
-    if (L > cap || q_len > L || L < 0) {
+    const int L = __ldg(p.context_lens + b);
+    if (L > p.mb * p.bs || q_len > L || L < 0) {
         if (threadIdx.x == 0) set_error(p.err, kErrDeviceRange);
         return;
     }
-    const int rows = min(kBM, q_len - m_start);
+    const int rows = min(kRows, q_len - m_start);
     const int qpos0 = L - q_len + m_start;                // absolute position of row 0
     const int kv_end = p.causal ? qpos0 + rows : L;       // keys [0, kv_end) are needed
     const int n_tiles = (kv_end + kBN - 1) / kBN;
     const int g = h / p.group;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+        for (int s = 0; s < kRing; ++s) {
+            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
         }
         mbar_init(q_full, 1);
-        mbar_init(s_full, 1);
-        mbar_init(s_free, 4);
-        mbar_init(p_full, 4);
-        mbar_init(o_done, 1);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&s_full[x], 1);
+            mbar_init(&s_free[x], 4);
+            mbar_init(&p_full[x], 4);
+            mbar_init(&o_done[x], 1);
+        }
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -146,224 +148,265 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        // ===================================== TMA producer =====================================
-        const int box_rows = p.bs < kBN ? p.bs : kBN;
-        uint32_t issued_mask = 0, issued_parity = 0;
-        if (lane == 0) {
-            tc::prefetch_tensormap(&tm_q);
-            tc::prefetch_tensormap(&tm_kv);
-            mbar_arrive_expect_tx(q_full, Lay::kQBytes);
+    if (warp < 4) {
+        tc::regs_dec<56>();
+        if (warp == 0) {
+            // ==================================== TMA producer ====================================
+            const int box_rows = p.bs < kBN ? p.bs : kBN;
+            uint32_t issued = 0;  // ring items issued (for the abort drain)
+            if (lane == 0) {
+                tc::prefetch_tensormap(&tm_q);
+                tc::prefetch_tensormap(&tm_kv);
+                mbar_arrive_expect_tx(q_full, 2 * Lay::kQBytes);
 #pragma unroll
-            for (int hf = 0; hf < Lay::kHalves; ++hf)
-                tc::tma_load_3d(sQ + hf * Lay::kTileHalf, &tm_q, hf * 64, h, q0 + m_start, q_full);
-        }
-        const int *bt = p.block_tables + (size_t)b * p.mb;
-        for (int j = 0; j < n_tiles; ++j) {
-            const int s = j % kStages;
-            const uint32_t ph = (uint32_t)(j / kStages) & 1u;
-            const int kv_start = j * kBN;
-            const int n_valid = min(kBN, L - kv_start);
-            const int page0 = kv_start >> p.log2_bs;
-            const int npages = p.bs < kBN ? (n_valid + p.bs - 1) / p.bs : 1;
-            const int off = p.bs < kBN ? 0 : (kv_start & (p.bs - 1));
-            int pb = 0;
-            if (lane < npages) {
-                pb = __ldg(bt + page0 + lane);
-                if (pb < 0 || pb >= p.num_blocks) {
-                    set_error(p.err, kErrDeviceRange);
-                    pb = 0;
-                }
+                for (int x = 0; x < 2; ++x)
+#pragma unroll
+                    for (int hf = 0; hf < Lay::kHalves; ++hf)
+                        tc::tma_load_3d(sQ + x * Lay::kQBytes + hf * Lay::kTileHalf, &tm_q, hf * 64, h,
+                                        q0 + m_start + x * kBM, q_full);
             }
-            if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.err)) {
-                for (int i = 0; i < kStages; ++i)
-                    if (issued_mask & (1u << i)) {
-                        volatile int no_abort = 0;
-                        mbar_wait(&full[i], (issued_parity >> i) & 1u, &no_abort, nullptr);
+            const int *bt = p.block_tables + (size_t)b * p.mb;
+            bool ok = true;
+            for (int j = 0; j < n_tiles && ok; ++j) {
+                const int kv_start = j * kBN;
+                const int n_valid = min(kBN, L - kv_start);
+                const int page0 = kv_start >> p.log2_bs;
+                const int npages = p.bs < kBN ? (n_valid + p.bs - 1) / p.bs : 1;
+                const int off = p.bs < kBN ? 0 : (kv_start & (p.bs - 1));
+                int pb = 0;
+                if (lane < npages) {
+                    pb = __ldg(bt + page0 + lane);
+                    if (pb < 0 || pb >= p.num_blocks) {
+                        set_error(p.err, kErrDeviceRange);
+                        pb = 0;
                     }
-                break;
+                }
+                for (int kv = 0; kv < 2; ++kv) {
+                    const uint32_t u = 2u * j + kv, slot = u % kRing, ph = (u / kRing) & 1u;
+                    if (!mbar_wait(&kv_empty[slot], ph ^ 1u, abort_flag, p.err)) { ok = false; break; }
+                    uint8_t *dst0 = sRing + slot * Lay::kKVBytes;
+                    if (lane == 0)
+                        mbar_arrive_expect_tx(&kv_full[slot], (uint32_t)npages * box_rows * 128u * Lay::kHalves);
+                    __syncwarp();
+                    if (lane < npages) {
+                        const int row = ((pb * 2 + kv) * p.num_kv_heads + g) * p.bs + off;
+                        const uint32_t dst = (uint32_t)lane * box_rows * 128u;
+#pragma unroll
+                        for (int hf = 0; hf < Lay::kHalves; ++hf)
+                            tc::tma_load_2d(dst0 + hf * Lay::kTileHalf + dst, &tm_kv, hf * 64, row, &kv_full[slot]);
+                    }
+                    ++issued;
+                }
             }
-            uint8_t *sK = smem + Lay::kKVOff + (uint32_t)s * 2 * Lay::kKVBytes;
-            uint8_t *sV = sK + Lay::kKVBytes;
-            if (lane == 0)
-                mbar_arrive_expect_tx(&full[s], (uint32_t)npages * box_rows * 128u * Lay::kHalves * 2u);
+            if (!ok) {
+                // let copies in flight land before the CTA exits (bounded)
+                const uint32_t first = issued > (uint32_t)kRing ? issued - kRing : 0u;
+                for (uint32_t u = first; u < issued; ++u) {
+                    volatile int no_abort = 0;
+                    mbar_wait(&kv_full[u % kRing], (u / kRing) & 1u, &no_abort, nullptr);
+                }
+            }
+        } else if (warp == 1) {
+            // ===================================== MMA issuer =====================================
+            if (lane == 0) {
+                const uint32_t id_qk = tc::idesc_f16(BF16, kBM, kBN, false);
+                const uint32_t id_pv = tc::idesc_f16(BF16, kBM, D, true);
+                const uint32_t aQ = smem_addr(sQ), aRing = smem_addr(sRing);
+                auto ring_wait = [&](uint32_t u) {
+                    return mbar_wait(&kv_full[u % kRing], (u / kRing) & 1u, abort_flag, p.err);
+                };
+                auto qk = [&](int x, uint32_t aK) {
+                    const uint32_t aQx = aQ + (uint32_t)x * Lay::kQBytes;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t o = (uint32_t)(kk >> 2) * Lay::kTileHalf + (uint32_t)(kk & 3) * 32u;
+                        tc::mma_f16_ss(tmem + kColS, tc::smem_desc(aQx + o, 16, 1024), tc::smem_desc(aK + o, 16, 1024),
+                                       id_qk, kk > 0 ? 1u : 0u);
+                    }
+                    tc::mma_commit(&s_full[x]);
+                };
+                auto pv = [&](int x, uint32_t aV, int j) {
+                    const uint32_t tP = tmem + kColP + 64u * x, tO = tmem + kColO + 128u * x;
+#pragma unroll
+                    for (int kk = 0; kk < kBN / 16; ++kk) {
+                        // V is [keys x D], D contiguous: MN-major B; 8-key groups 1024 B apart,
+                        // 64-column halves kTileHalf apart. P: 16 keys = 8 TMEM columns.
+                        tc::mma_f16_ts(tO, tP + 8u * kk, tc::smem_desc(aV + (uint32_t)kk * 2048u, Lay::kTileHalf, 1024),
+                                       id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc::mma_commit(&o_done[x]);
+                };
+                bool ok = mbar_wait(q_full, 0, abort_flag, p.err) && ring_wait(0);
+                if (ok) {
+                    tc::fence_after_sync();
+                    qk(0, aRing);
+                }
+                for (int j = 0; ok && j < n_tiles; ++j) {
+                    const uint32_t uK = 2u * j, uV = uK + 1;
+                    const uint32_t aK = aRing + (uK % kRing) * Lay::kKVBytes;
+                    const uint32_t aV = aRing + (uV % kRing) * Lay::kKVBytes;
+                    const uint32_t ph = (uint32_t)j & 1u;
+                    // S = Q_B K_j^T once softmax A has read S_A(j)
+                    if (!(ok = mbar_wait(&s_free[0], ph, abort_flag, p.err))) break;
+                    tc::fence_after_sync();
+                    qk(1, aK);
+                    tc::mma_commit(&kv_empty[uK % kRing]);
+                    // O_A += P_A V_j
+                    if (!(ok = ring_wait(uV) && mbar_wait(&p_full[0], ph, abort_flag, p.err))) break;
+                    tc::fence_after_sync();
+                    pv(0, aV, j);
+                    // S = Q_A K_{j+1}^T once softmax B has read S_B(j)
+                    if (j + 1 < n_tiles) {
+                        if (!(ok = mbar_wait(&s_free[1], ph, abort_flag, p.err) && ring_wait(uK + 2))) break;
+                        tc::fence_after_sync();
+                        qk(0, aRing + ((uK + 2) % kRing) * Lay::kKVBytes);
+                    }
+                    // O_B += P_B V_j
+                    if (!(ok = mbar_wait(&p_full[1], ph, abort_flag, p.err))) break;
+                    tc::fence_after_sync();
+                    pv(1, aV, j);
+                    tc::mma_commit(&kv_empty[uV % kRing]);
+                }
+                tc::mma_commit(drain);
+                volatile int no_abort = 0;
+                mbar_wait(drain, 0, &no_abort, p.err);
+            }
             __syncwarp();
-            if (lane < npages) {
-                const int rowK = ((pb * 2 + 0) * p.num_kv_heads + g) * p.bs + off;
-                const int rowV = rowK + p.num_kv_heads * p.bs;
-                const uint32_t dst = (uint32_t)lane * box_rows * 128u;
-#pragma unroll
-                for (int hf = 0; hf < Lay::kHalves; ++hf) {
-                    tc::tma_load_2d(sK + hf * Lay::kTileHalf + dst, &tm_kv, hf * 64, rowK, &full[s]);
-                    tc::tma_load_2d(sV + hf * Lay::kTileHalf + dst, &tm_kv, hf * 64, rowV, &full[s]);
-                }
-            }
-            issued_mask |= 1u << s;
-            issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
         }
-    } else if (warp == 1) {
-        // ====================================== MMA issuer ======================================
-        if (lane == 0) {
-            const uint32_t id_qk = tc::idesc_f16(BF16, kBM, kBN, false);
-            const uint32_t id_pv = tc::idesc_f16(BF16, kBM, D, true);
-            const uint32_t tS = tmem, tO = tmem + Lay::kOCol;
-            const uint32_t aQ = smem_addr(sQ), aP = smem_addr(sP);
-            const uint32_t aKV = smem_addr(smem + Lay::kKVOff);
-            bool ok = mbar_wait(q_full, 0, abort_flag, p.err);
-            auto issue_qk = [&](int j) -> bool {
-                const int s = j % kStages;
-                if (!mbar_wait(&full[s], (uint32_t)(j / kStages) & 1u, abort_flag, p.err)) return false;
-                tc::fence_after_sync();
-                const uint32_t aK = aKV + (uint32_t)s * 2 * Lay::kKVBytes;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t o = (uint32_t)(kk >> 2) * Lay::kTileHalf + (uint32_t)(kk & 3) * 32u;
-                    tc::mma_f16_ss(tS, tc::smem_desc(aQ + o, 16, 1024), tc::smem_desc(aK + o, 16, 1024), id_qk,
-                                   kk > 0 ? 1u : 0u);
-                }
-                tc::mma_commit(s_full);
-                return true;
-            };
-            if (ok) ok = issue_qk(0);
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                if (j + 1 < n_tiles) {
-                    // S is single-buffered: wait until the softmax has read S_j
-                    if (!mbar_wait(s_free, (uint32_t)j & 1u, abort_flag, p.err) || !issue_qk(j + 1)) break;
-                }
-                if (!mbar_wait(p_full, (uint32_t)j & 1u, abort_flag, p.err)) break;
-                tc::fence_after_sync();
-                const int s = j % kStages;
-                const uint32_t aV = aKV + (uint32_t)s * 2 * Lay::kKVBytes + Lay::kKVBytes;
-#pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    const uint32_t oP = (uint32_t)(kk >> 2) * Lay::kTileHalf + (uint32_t)(kk & 3) * 32u;
-                    // V is [keys x D] with D contiguous: MN-major B; 8-key groups 1024 B apart,
-                    // 64-column halves kTileHalf apart
-                    tc::mma_f16_ss(tO, tc::smem_desc(aP + oP, 16, 1024),
-                                   tc::smem_desc(aV + (uint32_t)kk * 2048u, Lay::kTileHalf, 1024), id_pv,
-                                   (j > 0 || kk > 0) ? 1u : 0u);
-                }
-                tc::mma_commit(o_done);
-                tc::mma_commit(&empty[s]);
-            }
-            tc::mma_commit(drain);
-            volatile int no_abort = 0;
-            mbar_wait(drain, 0, &no_abort, p.err);
-        }
-        __syncwarp();
     } else {
-        // ================================ softmax + epilogue ================================
+        tc::regs_inc<224>();
+        // ================================= softmax + epilogue =================================
+        const int x = (warp >> 2) - 1;                 // 0: tile A, 1: tile B
         const int quarter = warp & 3;                  // TMEM lanes 32*quarter .. +31
         const int r = quarter * 32 + lane;             // row within the tile
-        const bool row_ok = r < rows;
-        const int qpos = qpos0 + r;
+        const int row = x * kBM + r;                   // row within the CTA block
+        const bool row_ok = row < rows;
+        const int qpos = qpos0 + row;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-        const uint32_t tS = tmem + lane_base, tO = tmem + Lay::kOCol + lane_base;
+        const uint32_t tS = tmem + kColS + lane_base;
+        const uint32_t tP = tmem + kColP + 64u * x + lane_base;
+        const uint32_t tO = tmem + kColO + 128u * x + lane_base;
+        const float c = p.scale_log2;
         float m_use = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int j = 0; j < n_tiles && ok; ++j) {
+        for (int j = 0; j < n_tiles; ++j) {
             const int kv_start = j * kBN;
-            if (!mbar_wait(s_full, (uint32_t)j & 1u, abort_flag, p.err)) { ok = false; break; }
+            const uint32_t ph = (uint32_t)j & 1u;
+            if (!(ok = mbar_wait(&s_full[x], ph, abort_flag, p.err))) break;
             tc::fence_after_sync();
             float s[kBN];
 #pragma unroll
-            for (int c = 0; c < kBN / 32; ++c) tc::tmem_ld32(tS + c * 32, *reinterpret_cast<float(*)[32]>(&s[c * 32]));
+            for (int cc = 0; cc < kBN / 32; ++cc)
+                tc::tmem_ld32(tS + cc * 32, *reinterpret_cast<float(*)[32]>(&s[cc * 32]));
             tc::tmem_wait_ld();
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(s_free);
+            if (lane == 0) mbar_arrive(&s_free[x]);
             // last key index this row may see in this tile (-1: none)
             int lim = L - 1 - kv_start;
             if (p.causal) lim = min(lim, qpos - kv_start);
             if (!row_ok) lim = -1;
+            const bool masked = lim < kBN - 1;
             float mx = -INFINITY;
+            if (masked) {
 #pragma unroll
-            for (int i = 0; i < kBN; ++i) {
-                const float v = (i <= lim) ? s[i] * p.scale_log2 : -INFINITY;
-                s[i] = v;
-                mx = fmaxf(mx, v);
+                for (int i = 0; i < kBN; ++i) {
+                    s[i] = (i <= lim) ? s[i] : -INFINITY;
+                    mx = fmaxf(mx, s[i]);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < kBN; i += 2) mx = fmax3(mx, s[i], s[i + 1]);
             }
-            const float m_new = fmaxf(m_use, mx);
+            const float m_new = fmaxf(m_use, mx * c);
             const bool grow = m_new > m_use + kRescaleLog2;   // false when m_new = -inf
             const float alpha = grow ? fast_exp2(m_use - m_new) : 1.f;  // 0 when m_use = -inf
             if (grow) {
                 m_use = m_new;
                 l *= alpha;
             }
-            // O and P are touched only after P_{j-1} V_{j-1} is done
+            const float neg_m = -m_use;
+            uint32_t pk[kBN / 2];
+            float lsum = 0.f;
+            if (masked) {
+#pragma unroll
+                for (int i = 0; i < kBN; i += 2) {
+                    const float e0 = (i <= lim) ? fast_exp2(fmaf(s[i], c, neg_m)) : 0.f;
+                    const float e1 = (i + 1 <= lim) ? fast_exp2(fmaf(s[i + 1], c, neg_m)) : 0.f;
+                    lsum += e0 + e1;
+                    pk[i / 2] = pack2(e0, e1, BF16);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < kBN; i += 2) {
+                    const float e0 = fast_exp2(fmaf(s[i], c, neg_m));
+                    const float e1 = fast_exp2(fmaf(s[i + 1], c, neg_m));
+                    lsum += e0 + e1;
+                    pk[i / 2] = pack2(e0, e1, BF16);
+                }
+            }
+            l += lsum;
+            // P_x and O_x are touched only after P_x V_{j-1} is done
             if (j > 0) {
-                if (!mbar_wait(o_done, (uint32_t)(j - 1) & 1u, abort_flag, p.err)) { ok = false; break; }
+                if (!(ok = mbar_wait(&o_done[x], (uint32_t)(j - 1) & 1u, abort_flag, p.err))) break;
                 tc::fence_after_sync();
                 if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
+                    for (int cc = 0; cc < D / 32; ++cc) {
                         float o[32];
-                        tc::tmem_ld32(tO + c * 32, o);
+                        tc::tmem_ld32(tO + cc * 32, o);
                         tc::tmem_wait_ld();
 #pragma unroll
                         for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                        tc::tmem_st32(tO + c * 32, o);
+                        tc::tmem_st32(tO + cc * 32, o);
                     }
-                    tc::tmem_wait_st();
                 }
             }
-            float lsum = 0.f;
 #pragma unroll
-            for (int i = 0; i < kBN; ++i) {
-                const float e = (s[i] == -INFINITY) ? 0.f : fast_exp2(s[i] - m_use);
-                s[i] = e;
-                lsum += e;
-            }
-            l += lsum;
-            // P row -> shared memory, K-major, 128-byte swizzle (16-byte chunk c of row r at c ^ (r & 7))
-#pragma unroll
-            for (int c = 0; c < kBN / 8; ++c) {
-                uint4 v;
-                v.x = pack2(s[c * 8 + 0], s[c * 8 + 1], BF16);
-                v.y = pack2(s[c * 8 + 2], s[c * 8 + 3], BF16);
-                v.z = pack2(s[c * 8 + 4], s[c * 8 + 5], BF16);
-                v.w = pack2(s[c * 8 + 6], s[c * 8 + 7], BF16);
-                const uint32_t o = (uint32_t)(c >> 3) * Lay::kTileHalf + (uint32_t)r * 128u +
-                                   ((uint32_t)((c & 7) ^ (r & 7)) << 4);
-                *reinterpret_cast<uint4 *>(sP + o) = v;
-            }
-            // keys at or beyond the context end may hold unwritten cache bytes: zero those V rows
+            for (int cc = 0; cc < kBN / 32; ++cc)
+                tc::tmem_st16(tP + cc * 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[cc * 16]));
+            tc::tmem_wait_st();
+            // keys at or beyond the context end may hold unwritten cache bytes: tile A zeroes those V rows
             const int n_valid = L - kv_start;
-            if (n_valid < kBN && r >= n_valid) {
-                uint8_t *sV = smem + Lay::kKVOff + (uint32_t)(j % kStages) * 2 * Lay::kKVBytes + Lay::kKVBytes;
+            if (x == 0 && n_valid < kBN) {
+                const uint32_t uV = 2u * j + 1;
+                if (!(ok = mbar_wait(&kv_full[uV % kRing], (uV / kRing) & 1u, abort_flag, p.err))) break;
+                if (r >= n_valid) {
+                    uint8_t *sV = sRing + (uV % kRing) * Lay::kKVBytes;
 #pragma unroll
-                for (int hf = 0; hf < Lay::kHalves; ++hf)
+                    for (int hf = 0; hf < Lay::kHalves; ++hf)
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4 *>(sV + hf * Lay::kTileHalf + (uint32_t)r * 128u + c * 16) =
-                            make_uint4(0, 0, 0, 0);
+                        for (int cc = 0; cc < 8; ++cc)
+                            *reinterpret_cast<uint4 *>(sV + hf * Lay::kTileHalf + (uint32_t)r * 128u + cc * 16) =
+                                make_uint4(0, 0, 0, 0);
+                }
+                tc::fence_proxy_async_smem();
             }
-            tc::fence_proxy_async_smem();
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
+            if (lane == 0) mbar_arrive(&p_full[x]);
         }
         // ---- epilogue: O / l ----
-        if (ok && mbar_wait(o_done, (uint32_t)(n_tiles - 1) & 1u, abort_flag, p.err)) {
+        if (ok && mbar_wait(&o_done[x], (uint32_t)(n_tiles - 1) & 1u, abort_flag, p.err)) {
             tc::fence_after_sync();
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            const size_t row_g = (size_t)(q0 + m_start + r);
+            const size_t row_g = (size_t)(q0 + m_start + row);
             const size_t obase = (row_g * p.num_q_heads + h) * D;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int cc = 0; cc < D / 32; ++cc) {
                 float o[32];
-                tc::tmem_ld32(tO + c * 32, o);
+                tc::tmem_ld32(tO + cc * 32, o);
                 tc::tmem_wait_ld();
                 if (row_ok) {
                     if (p.out_dtype == 2) {
-                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + obase + c * 32);
+                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + obase + cc * 32);
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
                             dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
                                                  o[4 * i + 3] * inv);
                     } else {
                         const bool obf = p.out_dtype == 1;
-                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) + obase + c * 32);
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) + obase + cc * 32);
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             uint4 v;
@@ -463,7 +506,7 @@ cudaError_t launch_t(const PrefillArgs &a, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         if (dev < 64) configured[dev] = true;
     }
-    dim3 grid((a.max_q_len + kBM - 1) / kBM, a.num_q_heads, a.batch);
+    dim3 grid((a.max_q_len + kRows - 1) / kRows, a.num_q_heads, a.batch);
     kern<<<grid, kThreads, Lay::kSmemBytes, stream>>>(tm_q, tm_kv, p);
     return cudaGetLastError();
 }

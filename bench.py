@@ -46,7 +46,7 @@ def parse():
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="", help="comma list of extra workloads (bs_sweep,mixed,prefill)")
-    ap.add_argument("--profile", choices=["decode", "append", "prefill"], default=None,
+    ap.add_argument("--profile", choices=["decode", "append", "prefill", "decode_mixed"], default=None,
                     help="small case for ncu captures: W + K launches of one kernel, nothing else timed")
     return ap.parse_args()
 
@@ -72,6 +72,19 @@ def profile_case(args):
                 pkv.paged_attn_decode(cache, q, bt, ctx, scale=p.scale, out=out)
             else:
                 pkv.kv_cache_append(cache, k, v, cu, zeros, bt)
+        torch.cuda.synchronize()
+        assert pkv.get_device_error() == 0
+    elif args.profile == "decode_mixed":
+        # the mixed serving batch itself: 0.62 GB of K/V in a 1.2 GB pool
+        p = W.mixed_serving(pool_init="none", device="cuda")
+        cache = torch.zeros((p.num_blocks, 2, 8, 32, 128), dtype=torch.bfloat16, device="cuda")
+        bt = p.block_tables.cuda()
+        pkv.kv_cache_append(cache, p.k_ctx.cuda(), p.v_ctx.cuda(), p.cu_ctx_lens.cuda(),
+                            torch.zeros(p.batch, dtype=torch.int32, device="cuda"), bt)
+        q, ctx = p.q.cuda(), p.context_lens.cuda()
+        out = torch.empty((p.batch, 32, 128), dtype=torch.bfloat16, device="cuda")
+        for _ in range(args.warmup + args.steps):
+            pkv.paged_attn_decode(cache, q, bt, ctx, scale=p.scale, out=out)
         torch.cuda.synchronize()
         assert pkv.get_device_error() == 0
     else:

@@ -34,6 +34,13 @@ constexpr int kConsumerWarps = 8;
 constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStages = 4;
 constexpr int kMaxBatch = 2048;  // context lengths + unit prefix kept in shared memory
+constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (log2 units)
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 template <int D, int G>
 struct DecodeLayout {
@@ -267,18 +274,19 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
                     float mt = s[0][g];
 #pragma unroll
                     for (int i = 1; i < L::kStepsPerBatch; ++i) mt = fmaxf(mt, s[i][g]);
-                    const float m_new = fmaxf(m[g], mt);
-                    if (m_new != -INFINITY) {
-                        const float alpha = exp2f(m[g] - m_new);  // 0 when m[g] = -inf
+                    // Lazy rescale: the running max moves only when a score exceeds it by more
+                    // than 2^8; until then exp2(s - m) <= 256 and the final acc / l is unchanged.
+                    if (mt > m[g] + kRescaleLog2) {
+                        const float alpha = ex2_approx(m[g] - mt);  // 0 when m[g] = -inf
                         l[g] *= alpha;
                         const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
                         for (int j = 0; j < 4; ++j) acc[g][j] = fmul2(acc[g][j], a2);
-                        m[g] = m_new;
+                        m[g] = mt;
                     }
 #pragma unroll
                     for (int i = 0; i < L::kStepsPerBatch; ++i) {
-                        s[i][g] = valid[i] ? exp2f(s[i][g] - m[g]) : 0.f;
+                        s[i][g] = valid[i] ? ex2_approx(s[i][g] - m[g]) : 0.f;
                         l[g] += s[i][g];
                     }
                 }

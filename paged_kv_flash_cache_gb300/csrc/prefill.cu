@@ -17,9 +17,10 @@
 //              lane issues its page's boxes (2-D tensor map over the cache viewed as rows of D
 //              elements, 128-byte swizzle);
 //   warp 1     TMEM owner and MMA issuer (one thread). TMEM columns: S [0,128) shared by the two
-//              tiles, P_A [128,192), P_B [192,256), O_A [256,256+D), O_B [384,384+D). Per key tile:
-//              S = Q_A K^T, S = Q_B K^T (each after the other tile's softmax has read S),
-//              O_A += P_A V, O_B += P_B V with P read from TMEM (only V comes from shared memory);
+//              tiles, P_A [128,192), P_B [192,256), O_A [256,256+D), O_B [384,384+D). Issue order
+//              per key tile j: S = Q_A K_{j+1}^T, O_A += P_A V_j, S = Q_B K_{j+1}^T, O_B += P_B V_j,
+//              each S after the other tile's softmax has read S; P is read from TMEM, so only K and
+//              V come from shared memory;
 //   WG 1, 2    softmax of tile A / tile B, one query row per thread (TMEM lane = row): scale,
 //              causal / context masks, running max (O rescaled in TMEM only when the max grows by
 //              more than 2^8; the final O / l uses the same max, so the result is exact), exp2, row
@@ -74,6 +75,38 @@ __device__ __forceinline__ float fast_exp2(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+
+// exp2 on the FMA pipe for two values at once (the MUFU exp2 rate of an SM equals its bf16 tensor
+// rate per score element at head_dim 128, so a share of the exponentials is evaluated here).
+// Cody-Waite range reduction 2^x = 2^j 2^f, j = round(x) by the 1.5*2^23 magic-number addition,
+// f in [-1/2, 1/2]; 2^f by a minimax polynomial (relative error, Remez exchange, constant term
+// pinned to 1 so exp2(0) = 1 exactly; coefficients from csrc/exp2_poly.py): degree 3 (max
+// relative error 4.3e-4) when P is rounded to bf16, degree 4 (3.6e-6) when P is fp16; 2^j is
+// added to the exponent field. Inputs are clamped to >= -125 (2^-125 ~ 0 against the row sum).
+template <bool BF16>
+__device__ __forceinline__ float2 exp2_fma2(float2 x) {
+    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+    x.x = fmaxf(x.x, -125.f);
+    x.y = fmaxf(x.y, -125.f);
+    const float2 t = fadd2(x, make_float2(kMagic, kMagic));
+    const float2 f = fsub2(x, fsub2(t, make_float2(kMagic, kMagic)));
+    float2 p;
+    if (BF16) {
+        p = ffma2(make_float2(4.169875011e-02f, 4.169875011e-02f), f, make_float2(2.420305163e-01f, 2.420305163e-01f));
+        p = ffma2(p, f, make_float2(6.957668066e-01f, 6.957668066e-01f));
+    } else {
+        p = ffma2(make_float2(9.782912210e-03f, 9.782912210e-03f), f, make_float2(5.597688258e-02f, 5.597688258e-02f));
+        p = ffma2(p, f, make_float2(2.402071059e-01f, 2.402071059e-01f));
+        p = ffma2(p, f, make_float2(6.931136250e-01f, 6.931136250e-01f));
+    }
+    p = ffma2(p, f, make_float2(1.f, 1.f));
+    // t's low mantissa bits hold j (offset by the magic number, whose bits shift out)
+    return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(t.x) << 23)),
+                       __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23)));
+}
+
+// Pairs q of a 128-key row with (q % 8) < kEmuPerEight take exp2_fma2, the others MUFU ex2.
+constexpr int kEmuPerEight = 0;
 
 __device__ __forceinline__ uint32_t pack2(float a, float b, bool bf16) {
     if (bf16) {
@@ -239,27 +272,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool ok = mbar_wait(q_full, 0, abort_flag, p.err) && ring_wait(0);
                 if (ok) {
                     tc::fence_after_sync();
-                    qk(0, aRing);
+                    qk(0, aRing);  // S = Q_A K_0^T
+                    ok = mbar_wait(&s_free[0], 0, abort_flag, p.err);
+                    if (ok) {
+                        tc::fence_after_sync();
+                        qk(1, aRing);  // S = Q_B K_0^T once softmax A has read S_A(0)
+                        tc::mma_commit(&kv_empty[0]);
+                    }
                 }
+                // Steady state: the next S of a tile is issued as soon as the other tile's softmax
+                // has read S, ahead of this tile's P V, so each softmax finds its next S ready.
                 for (int j = 0; ok && j < n_tiles; ++j) {
-                    const uint32_t uK = 2u * j, uV = uK + 1;
-                    const uint32_t aK = aRing + (uK % kRing) * Lay::kKVBytes;
+                    const uint32_t uK = 2u * j, uV = uK + 1, uKn = uK + 2;
                     const uint32_t aV = aRing + (uV % kRing) * Lay::kKVBytes;
+                    const uint32_t aKn = aRing + (uKn % kRing) * Lay::kKVBytes;
                     const uint32_t ph = (uint32_t)j & 1u;
-                    // S = Q_B K_j^T once softmax A has read S_A(j)
-                    if (!(ok = mbar_wait(&s_free[0], ph, abort_flag, p.err))) break;
-                    tc::fence_after_sync();
-                    qk(1, aK);
-                    tc::mma_commit(&kv_empty[uK % kRing]);
+                    const bool more = j + 1 < n_tiles;
+                    // S = Q_A K_{j+1}^T once softmax B has read S_B(j)
+                    if (more) {
+                        if (!(ok = mbar_wait(&s_free[1], ph, abort_flag, p.err) && ring_wait(uKn))) break;
+                        tc::fence_after_sync();
+                        qk(0, aKn);
+                    }
                     // O_A += P_A V_j
                     if (!(ok = ring_wait(uV) && mbar_wait(&p_full[0], ph, abort_flag, p.err))) break;
                     tc::fence_after_sync();
                     pv(0, aV, j);
-                    // S = Q_A K_{j+1}^T once softmax B has read S_B(j)
-                    if (j + 1 < n_tiles) {
-                        if (!(ok = mbar_wait(&s_free[1], ph, abort_flag, p.err) && ring_wait(uK + 2))) break;
+                    // S = Q_B K_{j+1}^T once softmax A has read S_A(j+1)
+                    if (more) {
+                        if (!(ok = mbar_wait(&s_free[0], ph ^ 1u, abort_flag, p.err))) break;
                         tc::fence_after_sync();
-                        qk(0, aRing + ((uK + 2) % kRing) * Lay::kKVBytes);
+                        qk(1, aKn);
+                        tc::mma_commit(&kv_empty[uKn % kRing]);
                     }
                     // O_B += P_B V_j
                     if (!(ok = mbar_wait(&p_full[1], ph, abort_flag, p.err))) break;
@@ -307,17 +351,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (p.causal) lim = min(lim, qpos - kv_start);
             if (!row_ok) lim = -1;
             const bool masked = lim < kBN - 1;
-            float mx = -INFINITY;
             if (masked) {
 #pragma unroll
-                for (int i = 0; i < kBN; ++i) {
-                    s[i] = (i <= lim) ? s[i] : -INFINITY;
-                    mx = fmaxf(mx, s[i]);
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < kBN; i += 2) mx = fmax3(mx, s[i], s[i + 1]);
+                for (int i = 0; i < kBN; ++i) s[i] = (i <= lim) ? s[i] : -INFINITY;
             }
+            // row max as 8 independent chains (two warps per scheduler cannot hide a 64-deep chain)
+            float m8[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) m8[k] = fmax3(s[k], s[k + 8], s[k + 16]);
+#pragma unroll
+            for (int i = 24; i < kBN; i += 16)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) m8[k] = fmax3(m8[k], s[i + k], (i + 8 + k < kBN) ? s[i + 8 + k] : -INFINITY);
+            const float mx = fmaxf(fmax3(m8[0], m8[1], m8[2]), fmax3(fmax3(m8[3], m8[4], m8[5]), m8[6], m8[7]));
             const float m_new = fmaxf(m_use, mx * c);
             const bool grow = m_new > m_use + kRescaleLog2;   // false when m_new = -inf
             const float alpha = grow ? fast_exp2(m_use - m_new) : 1.f;  // 0 when m_use = -inf
@@ -325,26 +371,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_use = m_new;
                 l *= alpha;
             }
-            const float neg_m = -m_use;
+            // masked entries are -inf; m_use is finite for a row with a visible key, and a row
+            // without one (padding row) uses 0 so that exp2(-inf) = 0 instead of a NaN
+            const float neg_m = (m_use == -INFINITY) ? 0.f : -m_use;
             uint32_t pk[kBN / 2];
-            float lsum = 0.f;
+            float2 l4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            const float2 c2 = make_float2(c, c), nm2 = make_float2(neg_m, neg_m);
             if (masked) {
+                // boundary tiles: -inf entries, MUFU only (ex2(-inf) = 0)
 #pragma unroll
-                for (int i = 0; i < kBN; i += 2) {
-                    const float e0 = (i <= lim) ? fast_exp2(fmaf(s[i], c, neg_m)) : 0.f;
-                    const float e1 = (i + 1 <= lim) ? fast_exp2(fmaf(s[i + 1], c, neg_m)) : 0.f;
-                    lsum += e0 + e1;
-                    pk[i / 2] = pack2(e0, e1, BF16);
+                for (int q = 0; q < kBN / 2; ++q) {
+                    const float2 xq = ffma2(make_float2(s[2 * q], s[2 * q + 1]), c2, nm2);
+                    const float2 e = make_float2(fast_exp2(xq.x), fast_exp2(xq.y));
+                    l4[q & 3] = fadd2(l4[q & 3], e);
+                    pk[q] = pack2(e.x, e.y, BF16);
                 }
             } else {
 #pragma unroll
-                for (int i = 0; i < kBN; i += 2) {
-                    const float e0 = fast_exp2(fmaf(s[i], c, neg_m));
-                    const float e1 = fast_exp2(fmaf(s[i + 1], c, neg_m));
-                    lsum += e0 + e1;
-                    pk[i / 2] = pack2(e0, e1, BF16);
+                for (int q = 0; q < kBN / 2; ++q) {
+                    const float2 xq = ffma2(make_float2(s[2 * q], s[2 * q + 1]), c2, nm2);
+                    const float2 e = ((q & 7) < kEmuPerEight) ? exp2_fma2<BF16>(xq)
+                                                              : make_float2(fast_exp2(xq.x), fast_exp2(xq.y));
+                    l4[q & 3] = fadd2(l4[q & 3], e);
+                    pk[q] = pack2(e.x, e.y, BF16);
                 }
             }
+            const float2 l2 = fadd2(fadd2(l4[0], l4[1]), fadd2(l4[2], l4[3]));
+            const float lsum = l2.x + l2.y;
             l += lsum;
             // P_x and O_x are touched only after P_x V_{j-1} is done
             if (j > 0) {

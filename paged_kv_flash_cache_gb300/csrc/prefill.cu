@@ -16,11 +16,11 @@
 //              the pages a tile covers are looked up in the block table by the warp's lanes and each
 //              lane issues its page's boxes (2-D tensor map over the cache viewed as rows of D
 //              elements, 128-byte swizzle);
-//   warp 1     TMEM owner and MMA issuer (one thread). TMEM columns: S [0,128) shared by the two
-//              tiles, P_A [128,192), P_B [192,256), O_A [256,256+D), O_B [384,384+D). Issue order
-//              per key tile j: S = Q_A K_{j+1}^T, O_A += P_A V_j, S = Q_B K_{j+1}^T, O_B += P_B V_j,
-//              each S after the other tile's softmax has read S; P is read from TMEM, so only K and
-//              V come from shared memory;
+//   warp 1     TMEM owner and MMA issuer (one thread). TMEM columns: S_A [0,128), S_B [128,256),
+//              O_A [256,256+D), O_B [384,384+D); P_x is written over the first 64 columns of S_x.
+//              Ping-pong issue order per key tile j: O_A += P_A V_j, S_A = Q_A K_{j+1}^T,
+//              O_B += P_B V_j, S_B = Q_B K_{j+1}^T, so one tile's softmax overlaps the other tile's
+//              MMAs; P is the A operand straight from TMEM, so only K and V come from shared memory;
 //   WG 1, 2    softmax of tile A / tile B, one query row per thread (TMEM lane = row): scale,
 //              causal / context masks, running max (O rescaled in TMEM only when the max grows by
 //              more than 2^8; the final O / l uses the same max, so the result is exact), exp2, row
@@ -44,7 +44,9 @@ constexpr int kBN = 128;       // keys per KV tile
 constexpr int kRing = 4;       // K/V ring slots
 constexpr int kThreads = 384;  // 3 warpgroups
 constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by more than 2^8
-constexpr uint32_t kColS = 0, kColP = 128, kColO = 256;
+// TMEM columns: S_A (and P_A over its first 64 columns) [0,128), S_B / P_B [128,256),
+// O_A [256,384), O_B [384,512).
+constexpr uint32_t kColS = 0, kColO = 256;
 
 template <int D>
 struct PrefillLayout {
@@ -131,8 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *kv_full = bars;            // [kRing]
     uint64_t *kv_empty = bars + 4;       // [kRing]
     uint64_t *q_full = bars + 8;
-    uint64_t *s_full = bars + 9;         // [2] S of tile A / B computed
-    uint64_t *s_free = bars + 11;        // [2] softmax A / B has read S
+    uint64_t *s_full = bars + 9;         // [2] S_A / S_B computed
     uint64_t *p_full = bars + 13;        // [2] P_A / P_B in TMEM (and O rescaled)
     uint64_t *o_done = bars + 15;        // [2] P V accumulated into O_A / O_B
     uint64_t *drain = bars + 17;         // every MMA issued has completed
@@ -164,7 +165,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(q_full, 1);
         for (int x = 0; x < 2; ++x) {
             mbar_init(&s_full[x], 1);
-            mbar_init(&s_free[x], 4);
             mbar_init(&p_full[x], 4);
             mbar_init(&o_done[x], 1);
         }
@@ -253,13 +253,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t o = (uint32_t)(kk >> 2) * Lay::kTileHalf + (uint32_t)(kk & 3) * 32u;
-                        tc::mma_f16_ss(tmem + kColS, tc::smem_desc(aQx + o, 16, 1024), tc::smem_desc(aK + o, 16, 1024),
+                        tc::mma_f16_ss(tmem + kColS + 128u * x, tc::smem_desc(aQx + o, 16, 1024), tc::smem_desc(aK + o, 16, 1024),
                                        id_qk, kk > 0 ? 1u : 0u);
                     }
                     tc::mma_commit(&s_full[x]);
                 };
                 auto pv = [&](int x, uint32_t aV, int j) {
-                    const uint32_t tP = tmem + kColP + 64u * x, tO = tmem + kColO + 128u * x;
+                    const uint32_t tP = tmem + kColS + 128u * x, tO = tmem + kColO + 128u * x;
 #pragma unroll
                     for (int kk = 0; kk < kBN / 16; ++kk) {
                         // V is [keys x D], D contiguous: MN-major B; 8-key groups 1024 B apart,
@@ -272,44 +272,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool ok = mbar_wait(q_full, 0, abort_flag, p.err) && ring_wait(0);
                 if (ok) {
                     tc::fence_after_sync();
-                    qk(0, aRing);  // S = Q_A K_0^T
-                    ok = mbar_wait(&s_free[0], 0, abort_flag, p.err);
-                    if (ok) {
-                        tc::fence_after_sync();
-                        qk(1, aRing);  // S = Q_B K_0^T once softmax A has read S_A(0)
-                        tc::mma_commit(&kv_empty[0]);
-                    }
+                    qk(0, aRing);  // S_A = Q_A K_0^T
+                    qk(1, aRing);  // S_B = Q_B K_0^T
+                    tc::mma_commit(&kv_empty[0]);
                 }
-                // Steady state: the next S of a tile is issued as soon as the other tile's softmax
-                // has read S, ahead of this tile's P V, so each softmax finds its next S ready.
+                // Ping-pong: tile A's P V_j then its next S, then tile B's. P_x sits in S_x's columns;
+                // the tensor pipe runs the MMAs of this thread in issue order, so S_x(j+1) is
+                // written only after P_x(j) V_j has read P_x(j).
                 for (int j = 0; ok && j < n_tiles; ++j) {
                     const uint32_t uK = 2u * j, uV = uK + 1, uKn = uK + 2;
                     const uint32_t aV = aRing + (uV % kRing) * Lay::kKVBytes;
                     const uint32_t aKn = aRing + (uKn % kRing) * Lay::kKVBytes;
                     const uint32_t ph = (uint32_t)j & 1u;
                     const bool more = j + 1 < n_tiles;
-                    // S = Q_A K_{j+1}^T once softmax B has read S_B(j)
-                    if (more) {
-                        if (!(ok = mbar_wait(&s_free[1], ph, abort_flag, p.err) && ring_wait(uKn))) break;
-                        tc::fence_after_sync();
-                        qk(0, aKn);
-                    }
-                    // O_A += P_A V_j
                     if (!(ok = ring_wait(uV) && mbar_wait(&p_full[0], ph, abort_flag, p.err))) break;
                     tc::fence_after_sync();
                     pv(0, aV, j);
-                    // S = Q_B K_{j+1}^T once softmax A has read S_A(j+1)
                     if (more) {
-                        if (!(ok = mbar_wait(&s_free[0], ph ^ 1u, abort_flag, p.err))) break;
-                        tc::fence_after_sync();
-                        qk(1, aKn);
-                        tc::mma_commit(&kv_empty[uKn % kRing]);
+                        if (!(ok = ring_wait(uKn))) break;
+                        qk(0, aKn);
                     }
-                    // O_B += P_B V_j
                     if (!(ok = mbar_wait(&p_full[1], ph, abort_flag, p.err))) break;
                     tc::fence_after_sync();
                     pv(1, aV, j);
                     tc::mma_commit(&kv_empty[uV % kRing]);
+                    if (more) {
+                        qk(1, aKn);
+                        tc::mma_commit(&kv_empty[uKn % kRing]);
+                    }
                 }
                 tc::mma_commit(drain);
                 volatile int no_abort = 0;
@@ -327,8 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool row_ok = row < rows;
         const int qpos = qpos0 + row;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-        const uint32_t tS = tmem + kColS + lane_base;
-        const uint32_t tP = tmem + kColP + 64u * x + lane_base;
+        const uint32_t tS = tmem + kColS + 128u * x + lane_base;   // S_x, and P_x over its first 64 columns
         const uint32_t tO = tmem + kColO + 128u * x + lane_base;
         const float c = p.scale_log2;
         float m_use = -INFINITY, l = 0.f;
@@ -343,9 +332,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int cc = 0; cc < kBN / 32; ++cc)
                 tc::tmem_ld32(tS + cc * 32, *reinterpret_cast<float(*)[32]>(&s[cc * 32]));
             tc::tmem_wait_ld();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s_free[x]);
             // last key index this row may see in this tile (-1: none)
             int lim = L - 1 - kv_start;
             if (p.causal) lim = min(lim, qpos - kv_start);
@@ -417,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 #pragma unroll
             for (int cc = 0; cc < kBN / 32; ++cc)
-                tc::tmem_st16(tP + cc * 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[cc * 16]));
+                tc::tmem_st16(tS + cc * 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[cc * 16]));
             tc::tmem_wait_st();
             // keys at or beyond the context end may hold unwritten cache bytes: tile A zeroes those V rows
             const int n_valid = L - kv_start;

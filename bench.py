@@ -447,24 +447,49 @@ def bench_prefill(torch, steps, warmup):
                            cu=v["cu_q_lens"].cuda(), ctx=v["context_lens"].cuda(), before=v["ctx_before"].cuda(),
                            out=torch.empty_like(p.q[rows]), ql=int(v["q_lens"][0])))
 
-    def step(i):
-        for ch in chunks:
+    n_chunks = len(chunks)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_chunks)]
+    stream = torch.cuda.current_stream()
+
+    def step(i, timed=False):
+        for c, ch in enumerate(chunks):
+            if timed:
+                ev[c][0].record(stream)
             pkv.kv_cache_append(cache, ch["k"], ch["v"], ch["cu"], ch["before"], bt)
+            if timed:
+                ev[c][1].record(stream)
             pkv.paged_attn_prefill(cache, ch["q"], ch["cu"], ch["ctx"], bt, max_q_len=ch["ql"], scale=p.scale,
                                    causal=True, out=ch["out"])
+            if timed:
+                ev[c][2].record(stream)
 
     step(0)
     torch.cuda.synchronize()
     for i in range(warmup):
         step(i)
-    ms = time_loop(torch, step, steps, torch.cuda.current_stream()) / steps
+    app_ms = attn_ms = 0.0
+    total_ms = 0.0
+    for i in range(steps):
+        total_ms += time_loop(torch, lambda k: step(k, True), 1, stream)
+        app_ms += sum(e[0].elapsed_time(e[1]) for e in ev)
+        attn_ms += sum(e[1].elapsed_time(e[2]) for e in ev)
+    ms, app_ms, attn_ms = total_ms / steps, app_ms / steps, attn_ms / steps
     flops = p.causal_flops()
+    # append moves every prompt token's K and V row-set once in, once out
+    app_bytes = 2 * 2 * p.batch * 8192 * p.num_kv_heads * p.head_dim * 2
+    pk = peaks()
     del cache
     torch.cuda.empty_cache()
     return {"workload": "4 x 8192 causal prefill, 32 heads x 128, bf16, bs 16 pages, 16 chunks of 512 "
                         "(append chunk, then attend)", "ms_per_pass": round(ms, 3),
-            "tflops": round(flops / ms / 1e9, 1), "frac_of_dense_bf16": round(flops / ms / 1e9 / peaks()["bf16_tflops"], 3),
-            "prompt_tokens_per_s": round(4 * 8192 / ms * 1e3, 1)}
+            "tflops": round(flops / ms / 1e9, 1), "frac_of_dense_bf16": round(flops / ms / 1e9 / pk["bf16_tflops"], 3),
+            "attention_only": {"ms": round(attn_ms, 3), "tflops": round(flops / attn_ms / 1e9, 1),
+                               "frac_of_dense_bf16": round(flops / attn_ms / 1e9 / pk["bf16_tflops"], 3),
+                               "kernel": "prefill_kernel, 16 launches per pass", "launches": n_chunks},
+            "append": {"ms": round(app_ms, 3), "gbs": round(app_bytes / app_ms / 1e6, 1),
+                       "frac_of_hbm": round(app_bytes / app_ms / 1e6 / pk["hbm_gbs"], 3),
+                       "bytes": app_bytes, "launches": n_chunks},
+            "causal_flops": flops, "prompt_tokens_per_s": round(4 * 8192 / ms * 1e3, 1)}
 
 
 # ------------------------------------------------------------------------------------------------

@@ -56,7 +56,13 @@ struct DecodeLayout {
     static constexpr size_t kMergeFloats = (size_t)kConsumerWarps * G * (D + 2);
     static constexpr size_t kBarOffset = kStages * kStageBytes;
     static constexpr size_t kMergeOffset = kBarOffset + 2 * kStages * 8 + 16;  // + abort flag
-    static constexpr size_t kIntsOffset = kMergeOffset + kMergeFloats * 4;
+    // grouped heads (G > 1): a batch of kGqaSteps steps gives each lane of a token group one
+    // (token, head) score after a reduce-scatter, i.e. kGqaSteps * G <= kLanesPerTok values
+    static constexpr int kGqaSteps = (kSteps * G <= kLanesPerTok) ? kSteps : (kLanesPerTok / G);
+    static constexpr int kGqaN = kGqaSteps * G;
+    static constexpr size_t kPOffset = kMergeOffset + kMergeFloats * 4;     // per-warp p broadcast buffer
+    static constexpr size_t kPFloats = (size_t)kConsumerWarps * kTokPerStep * kGqaN;
+    static constexpr size_t kIntsOffset = kPOffset + kPFloats * 4;
     static size_t smem_bytes(int batch) { return kIntsOffset + (size_t)(2 * batch + 2 + 64) * 4; }
 };
 
@@ -217,10 +223,22 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
     const int chk = lane % L::kLanesPerTok;    // this lane's 8-element chunk of D
     const float qscale = a.scale * kLog2e;     // scores in log2 units
     float2 qf[G][4];                           // q chunk, scaled, as fp32 pairs
+    // grouped heads: after the reduce-scatter, lane (within its token group) owns value k_own =
+    // step * G + head; `shift` drops the low lane bits that only replicate it
+    constexpr int kLog2N = L::kGqaN >= 16 ? 4 : L::kGqaN >= 8 ? 3 : L::kGqaN >= 4 ? 2 : L::kGqaN >= 2 ? 1 : 0;
+    constexpr int kLog2R = L::kLanesPerTok == 16 ? 4 : 3;
+    constexpr int shift = kLog2R - kLog2N;
+    const int group_base = lane & ~(L::kLanesPerTok - 1);
+    const int k_own = (lane & (L::kLanesPerTok - 1)) >> shift;
+    const int g_own = k_own % G;
+    float *pbuf = reinterpret_cast<float *>(smem + L::kPOffset) + ((size_t)warp * L::kTokPerStep + slot) * L::kGqaN;
+    (void)group_base; (void)g_own; (void)pbuf;
     int stage = 0;
     uint32_t phase = 0;
     for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
         const UnitCursor c = unit_of(u, prefix, lens, a.batch, hkv, chunk);
+        float l_own = 0.f;                     // grouped heads: this lane's share of its head's sum
+        (void)l_own;
         float m[G], l[G];
         float2 acc[G][4];
 #pragma unroll
@@ -244,6 +262,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
                     for (int j = 0; j < 4; ++j) qf[g][j] = fmul2(qf[g][j], qs2);
                 }
             }
+            if constexpr (G == 1) {
             const uint8_t *sk = st;
             const uint8_t *sv = st + L::kKBytes;
 #pragma unroll
@@ -305,12 +324,117 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
                     }
                 }
             }
+            } else {
+            const uint8_t *sk = st;
+            const uint8_t *sv = st + L::kKBytes;
+#pragma unroll
+            for (int b0 = 0; b0 < L::kSteps; b0 += L::kGqaSteps) {
+                constexpr int S = L::kGqaSteps, N = L::kGqaN, R = L::kLanesPerTok;
+                // q.k partial sums for S tokens x G heads, value k = i * G + g
+                float v[N];
+#pragma unroll
+                for (int i = 0; i < S; ++i) {
+                    const int t = warp * L::kTokPerWarp + (b0 + i) * L::kTokPerStep + slot;
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(sk + ((size_t)t * D + chk * 8) * 2);
+                    float2 kf[4];
+                    unpack8x2(raw, kf, Tag());
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        float2 pp = fmul2(qf[g][0], kf[0]);
+#pragma unroll
+                        for (int j = 1; j < 4; ++j) pp = ffma2(qf[g][j], kf[j], pp);
+                        v[i * G + g] = pp.x + pp.y;
+                    }
+                }
+                // reduce-scatter over the R lanes of the token group: each level halves the values a
+                // lane keeps (upper or lower half by its lane bit) and adds the partner's other half;
+                // once one value is left the remaining levels all-reduce it
+#pragma unroll
+                for (int lev = 0; (R >> (lev + 1)) >= 1; ++lev) {
+                    const int o = R >> (lev + 1);
+                    const int cnt = N >> lev;
+                    if (cnt > 1) {
+                        const int half = cnt >> 1;
+                        const bool hi = (lane & o) != 0;
+#pragma unroll
+                        for (int q = 0; q < half; ++q) {
+                            const float send = hi ? v[q] : v[q + half];
+                            const float keep = hi ? v[q + half] : v[q];
+                            v[q] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                        }
+                    } else {
+                        v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+                    }
+                }
+                const int tok_own = warp * L::kTokPerWarp + (b0 + k_own / G) * L::kTokPerStep + slot;
+                const float s_own = (tok_own < n) ? v[0] : -INFINITY;
+                // batch max of this lane's head over the S steps (the first log2(S) lane bits)
+                float mb = s_own;
+#pragma unroll
+                for (int o = R >> 1; o > (R >> 1) / S; o >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+                float m_own = m[0];
+#pragma unroll
+                for (int g = 1; g < G; ++g) m_own = (g_own == g) ? m[g] : m_own;
+                if (__any_sync(0xffffffffu, mb > m_own + kRescaleLog2)) {
+                    // lazy rescale: every lane learns each head's batch max from a lane that owns it
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        const float Mg = __shfl_sync(0xffffffffu, mb, group_base | (g << shift));
+                        if (Mg > m[g] + kRescaleLog2) {
+                            const float alpha = ex2_approx(m[g] - Mg);  // 0 when m[g] = -inf
+                            const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) acc[g][j] = fmul2(acc[g][j], a2);
+                            if (g == g_own) l_own *= alpha;
+                            m[g] = Mg;
+                        }
+                    }
+#pragma unroll
+                    for (int g = 0; g < G; ++g) m_own = (g_own == g) ? m[g] : m_own;
+                }
+                const float p_own = (s_own == -INFINITY) ? 0.f : ex2_approx(s_own - m_own);
+                l_own += p_own;
+                // broadcast the N probabilities of this token group through shared memory
+                pbuf[k_own] = p_own;
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < S; ++i) {
+                    const int t = warp * L::kTokPerWarp + (b0 + i) * L::kTokPerStep + slot;
+                    if (t >= n) continue;
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(sv + ((size_t)t * D + chk * 8) * 2);
+                    float2 vf[4];
+                    unpack8x2(raw, vf, Tag());
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        const float pg = pbuf[i * G + g];
+                        const float2 p2 = make_float2(pg, pg);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) acc[g][j] = ffma2(p2, vf[j], acc[g][j]);
+                    }
+                }
+                __syncwarp();
+            }
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
             if (++stage == kStages) {
                 stage = 0;
                 phase ^= 1u;
             }
+        }
+        if constexpr (G > 1) {
+            // l[g] = sum of l_own over the lanes owning head g (all bits but the head bits),
+            // divided by the replication of each value, then handed to every lane
+            constexpr int R = L::kLanesPerTok, S = L::kGqaSteps;
+            float lt = l_own;
+#pragma unroll
+            for (int o = R >> 1; o >= 1; o >>= 1) {
+                const bool head_bit = (o <= (R >> 1) / S) && (o > ((R >> 1) / S) / G);
+                if (!head_bit) lt += __shfl_xor_sync(0xffffffffu, lt, o);
+            }
+            lt *= 1.f / (float)(1 << shift);
+#pragma unroll
+            for (int g = 0; g < G; ++g) l[g] = __shfl_sync(0xffffffffu, lt, group_base | (g << shift));
         }
         // ---- merge the token slots of this warp (lanes with the same chunk) ----
 #pragma unroll

@@ -504,24 +504,29 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
         }
         named_barrier(1, kConsumerWarps * 32);
     }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---- split merge: one warp per output row --------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
     constexpr int kPer = D / 32;  // elements per lane
+    // Launched as a programmatic dependent of the split kernel: everything above the wait may
+    // run while the split kernel drains; the wait returns once its writes are visible.
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    if (row >= a.n_rows) return;
     int S = a.num_splits;
-    if (a.context_lens) {
+    bool done_by_split = false;
+    if (row < a.n_rows && a.context_lens) {
         const int b = row / a.rows_per_seq;
         int len = __ldg(a.context_lens + b);
         len = len < 0 ? 0 : len;
         S = (len + a.chunk - 1) / a.chunk;
         if (S > a.num_splits) S = a.num_splits;
-        if (S == 1) return;  // finished by the split kernel
+        done_by_split = (S == 1);  // finished by the split kernel
     }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (row >= a.n_rows || done_by_split) return;
     const float *pl = a.part_lse + (size_t)row * a.num_splits;
     const float *po = a.part_o + (size_t)row * a.num_splits * D;
     float M = -INFINITY;
@@ -533,14 +538,24 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
     for (int j = 0; j < kPer; ++j) o_acc[j] = 0.f;
     float wsum = 0.f;
     if (M != -INFINITY) {
-        for (int s = 0; s < S; ++s) {
-            const float ls = pl[s];
-            if (ls == -INFINITY) continue;
-            const float w = exp2f((ls - M) * kLog2e);
-            wsum += w;
+        // 32 splits at a time: lane s holds split s's weight; partial rows are read with the
+        // loads of four splits in flight
+        for (int s0 = 0; s0 < S; s0 += 32) {
+            const int s_l = s0 + lane;
+            const float ls = s_l < S ? pl[s_l] : -INFINITY;
+            const float w_l = ls == -INFINITY ? 0.f : exp2f((ls - M) * kLog2e);
+            wsum += w_l;
+            const int n = min(32, S - s0);
+#pragma unroll 4
+            for (int k = 0; k < n; ++k) {
+                const float w = __shfl_sync(0xffffffffu, w_l, k);
+                const float *src = po + (size_t)(s0 + k) * D + lane * kPer;
 #pragma unroll
-            for (int j = 0; j < kPer; ++j) o_acc[j] = fmaf(w, po[(size_t)s * D + lane * kPer + j], o_acc[j]);
+                for (int j = 0; j < kPer; ++j) o_acc[j] = fmaf(w, src[j], o_acc[j]);
+            }
         }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
 #pragma unroll
@@ -624,13 +639,19 @@ cudaError_t launch_decode(const DecodeArgs &a, int grid, cudaStream_t s) {
 
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s) {
     if (a.n_rows == 0) return cudaSuccess;
-    const int grid = (a.n_rows + 7) / 8;
-    if (a.head_dim == 128) {
-        combine_kernel<128><<<grid, 256, 0, s>>>(a);
-    } else {
-        combine_kernel<64><<<grid, 256, 0, s>>>(a);
-    }
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((a.n_rows + 7) / 8);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    // programmatic dependent launch: may start while the preceding kernel on `s` finishes
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (a.head_dim == 128) return cudaLaunchKernelEx(&cfg, combine_kernel<128>, a);
+    return cudaLaunchKernelEx(&cfg, combine_kernel<64>, a);
 }
 
 }  // namespace pkv

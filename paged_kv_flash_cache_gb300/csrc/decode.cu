@@ -11,7 +11,7 @@
 //
 // Kernel structure (one persistent CTA per SM slot):
 //   * work unit = (sequence, KV head, split); units are numbered in a prologue from the
-//     context lengths (block-wide scan) and dealt round-robin to the CTAs;
+//     context lengths (block-wide scan) and claimed in order from a counter in the workspace;
 //   * warp 4 (producer) streams each unit's tokens in 64-token tiles into a ring of
 //     shared-memory stages with bulk copies (TMA engine, one copy per page slice of K and of
 //     V -- pages are contiguous [block_size, D] rows), completion on an mbarrier;
@@ -55,7 +55,7 @@ struct DecodeLayout {
     static constexpr size_t kStageBytes = ((2 * kKBytes + kQBytes) + 127) / 128 * 128;
     static constexpr size_t kMergeFloats = (size_t)kConsumerWarps * G * (D + 2);
     static constexpr size_t kBarOffset = kStages * kStageBytes;
-    static constexpr size_t kMergeOffset = kBarOffset + 2 * kStages * 8 + 16;  // + abort flag
+    static constexpr size_t kMergeOffset = kBarOffset + 2 * kStages * 8 + 32;  // + abort flag, unit ids
     // grouped heads (G > 1): a batch of kGqaSteps steps gives each lane of a token group one
     // (token, head) score after a reduce-scatter, i.e. kGqaSteps * G <= kLanesPerTok values
     static constexpr int kGqaSteps = (kSteps * G <= kLanesPerTok) ? kSteps : (kLanesPerTok / G);
@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kBarOffset);
     uint64_t *empty = full + kStages;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + kStages);
+    int *stage_unit = reinterpret_cast<int *>(empty + kStages) + 4;  // [kStages] unit of each filled stage, -1: end
     float *merge = reinterpret_cast<float *>(smem + L::kMergeOffset);
     int *lens = reinterpret_cast<int *>(smem + L::kIntsOffset);
     int *prefix = lens + a.batch;          // [batch + 1]
@@ -156,7 +157,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
         uint32_t phase = 0;
         uint32_t issued_mask = 0;  // stages with copies issued (bit i), for the abort drain
         uint32_t issued_parity = 0;
-        for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+        // Units are claimed from a counter in the workspace (cleared by the host before the launch):
+        // CTAs take them in order, so concurrent CTAs stream neighbouring head slices of the same
+        // pages, and a CTA that finishes early takes more. The next claim is made while the
+        // current unit's tiles are issued.
+        int u = 0;
+        if (lane == 0) u = atomicAdd(a.sched, 1);
+        u = __shfl_sync(0xffffffffu, u, 0);
+        while (u < num_units) {
+            int u_next = 0;
+            if (lane == 0) u_next = atomicAdd(a.sched, 1);
             const UnitCursor c = unit_of(u, prefix, lens, a.batch, hkv, chunk);
             const int *bt = a.block_tables + (size_t)c.b * a.max_blocks_per_seq;
             for (int ts = c.t0; ts < c.t1; ts += L::kTile) {
@@ -187,6 +197,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
                 uint8_t *st = smem + (size_t)stage * L::kStageBytes;
                 const bool first_tile = (ts == c.t0);
                 if (lane == 0) {
+                    stage_unit[stage] = u;
                     const uint32_t bytes = (uint32_t)n * D * 2 * 2 + (first_tile ? (uint32_t)L::kQBytes : 0u);
                     mbar_arrive_expect_tx(&full[stage], bytes);
                 }
@@ -214,6 +225,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
                     phase ^= 1u;
                 }
             }
+            u = __shfl_sync(0xffffffffu, u_next, 0);
+        }
+        // end marker: one more stage carrying unit id -1
+        if (mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.err) && lane == 0) {
+            stage_unit[stage] = -1;
+            mbar_arrive(&full[stage]);
         }
         return;
     }
@@ -235,7 +252,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
     (void)group_base; (void)g_own; (void)pbuf;
     int stage = 0;
     uint32_t phase = 0;
-    for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+    for (;;) {
+        // the unit of the next stage (or the end marker) is known once that stage is full
+        if (!mbar_wait(&full[stage], phase, abort_flag, a.err)) return;
+        const int u = stage_unit[stage];
+        if (u < 0) break;
         const UnitCursor c = unit_of(u, prefix, lens, a.batch, hkv, chunk);
         float l_own = 0.f;                     // grouped heads: this lane's share of its head's sum
         (void)l_own;
@@ -250,7 +271,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
         }
         for (int ts = c.t0; ts < c.t1; ts += L::kTile) {
             const int n = min(L::kTile, c.t1 - ts);
-            if (!mbar_wait(&full[stage], phase, abort_flag, a.err)) return;
+            if (ts != c.t0 && !mbar_wait(&full[stage], phase, abort_flag, a.err)) return;
             const uint8_t *st = smem + (size_t)stage * L::kStageBytes;
             if (ts == c.t0) {
                 const float2 qs2 = make_float2(qscale, qscale);

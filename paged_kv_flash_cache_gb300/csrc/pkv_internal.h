@@ -34,6 +34,7 @@ struct DecodeArgs {
     float scale;
     int chunk;   // tokens per split (multiple of the decode tile)
     int s_max;   // splits a full-capacity context uses: ceil(max_blocks_per_seq * block_size / chunk)
+    int *sched;       // unit claim counter (zero at launch)
     float *part_o;    // [batch, Hq, s_max, D]
     float *part_lse;  // [batch, Hq, s_max]
     void *out;

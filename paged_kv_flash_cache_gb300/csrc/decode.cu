@@ -24,6 +24,7 @@
 //     normalised output and lse go to the workspace for the merge kernel.
 #include <type_traits>
 
+#include "decode_common.cuh"
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
@@ -66,30 +67,6 @@ struct DecodeLayout {
     static size_t smem_bytes(int batch) { return kIntsOffset + (size_t)(2 * batch + 2 + 64) * 4; }
 };
 
-struct UnitCursor {
-    int b, kvh, split, t0, t1;
-};
-
-// Unit u -> (b, kv head, split); prefix[b] = units of sequences < b, units ordered with the KV
-// head fastest so consecutive CTAs share block-table rows.
-__device__ __forceinline__ UnitCursor unit_of(int u, const int *prefix, const int *lens, int batch, int hkv,
-                                              int chunk) {
-    int lo = 0, hi = batch;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (prefix[mid] <= u) lo = mid; else hi = mid;
-    }
-    UnitCursor c;
-    c.b = lo;
-    const int r = u - prefix[lo];
-    c.kvh = r % hkv;
-    c.split = r / hkv;
-    c.t0 = c.split * chunk;
-    const int end = c.t0 + chunk;
-    c.t1 = end < lens[lo] ? end : lens[lo];
-    return c;
-}
-
 template <typename Tag, int D, int G>
 __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeArgs a) {
     using L = DecodeLayout<D, G>;
@@ -116,35 +93,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
         fence_barrier_init();
     }
     // ---- prologue: clamp lengths, units per sequence, exclusive scan (all threads) ----
-    const int per = (a.batch + kDecodeThreads - 1) / kDecodeThreads;
-    const int i0 = tid * per;
-    int local = 0;
-    for (int i = i0; i < i0 + per && i < a.batch; ++i) {
-        int len = __ldg(a.context_lens + i);
-        if (len < 0 || len > cap) {
-            set_error(a.err, kErrDeviceRange);
-            len = len < 0 ? 0 : cap;
-        }
-        lens[i] = len;
-        local += ((len + chunk - 1) / chunk) * hkv;
-    }
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-    }
-    if (lane == 31) scan_tmp[warp] = incl;
-    __syncthreads();
-    int warp_base = 0;
-    for (int w = 0; w < warp; ++w) warp_base += scan_tmp[w];
-    int run = warp_base + incl - local;
-    for (int i = i0; i < i0 + per && i < a.batch; ++i) {
-        prefix[i] = run;
-        run += ((lens[i] + chunk - 1) / chunk) * hkv;
-    }
-    if (tid == kDecodeThreads - 1) prefix[a.batch] = warp_base + incl;
-    __syncthreads();
+    decode_scan_units<kDecodeThreads>(a, lens, prefix, scan_tmp);
     const int num_units = prefix[a.batch];
 
     if (warp == kConsumerWarps) {

@@ -1,0 +1,437 @@
+// decode_gqa.cu -- paged_attn_decode for grouped-query attention (four or more query heads per
+// KV head) with the group's q.K^T and P.V contractions on tensor cores.
+//
+// Same computation as decode.cu: for each sequence and query head, softmax(q.K^T * scale) V over
+// the cached tokens read through the block table ("企业官网建设流程全解析", section 2.1; layout of
+// "Flash Attention与Paged Attention如何共同优化大模型推理？", section 3), with the running max /
+// running sum of that page's section 2, split over key/value blocks and merged by log-sum-exp.
+// Under grouped-query attention ("为什么Attention是O(n²)", GQA section) the G query heads of a KV
+// head form a G x D matrix, so every K and V tile meets a dense product: S^T = K_tile Q_g^T
+// (tokens x heads) and O^T += V_tile^T P^T. On CUDA cores each K/V element would cost G FMAs plus
+// conversions and cross-lane sums; here one mma.sync m16n8k16 covers 16 tokens x 8 head slots x
+// 16 dims.
+//
+// Kernel structure (persistent, one CTA per SM, 5 warps):
+//   * units (sequence, KV head, split) are numbered from the context lengths and claimed in order
+//     from a counter in the workspace, as in decode.cu;
+//   * warp 4 streams each unit's 64-token tiles with TMA: the pages a tile covers are looked up by
+//     the warp's lanes and each lane issues its page's K and V boxes (64 columns x rows, 128-byte
+//     swizzle, through a 2-D tensor map over the cache), into a 4-stage ring; q comes in with the
+//     unit's first tile;
+//   * warps 0-3 each own 16 tokens of a tile: ldmatrix from the swizzled tile gives the A fragments
+//     of K (row) and of V (transposed); q, held as B fragments for the whole unit, has the group's
+//     heads in the N slots (padding slots are zero); the scores stay in the accumulator fragments:
+//     column max by shuffles, lazy rescale (threshold 2^8), exp2, and P moved into B-fragment
+//     layout with movmatrix; O^T accumulates in registers; at the end of a unit the warps merge
+//     through shared memory and write the output (single split) or the split partials.
+#include <cuda.h>
+
+#include "decode_common.cuh"
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+#include "tcgen05.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kWarps = 4;                         // consumer warps, 16 tokens each
+constexpr int kThreads = (kWarps + 1) * 32;
+constexpr int kTile = 64;                         // tokens per stage
+constexpr int kStagesG = 4;
+constexpr int kMaxBatchG = 2048;
+constexpr float kRescale = 8.0f;                  // lazy rescale threshold (log2 units)
+
+template <int D, int G>
+struct GqaLayout {
+    static constexpr int kHalves = D / 64;                          // 128-byte swizzle atoms along D
+    static constexpr uint32_t kHalfBytes = kTile * 128;             // 64 rows x 128 bytes
+    static constexpr uint32_t kKBytes = kHalves * kHalfBytes;       // one K (or V) tile
+    static constexpr uint32_t kQBytes = G * D * 2;
+    static constexpr uint32_t kStageBytes = (2 * kKBytes + kQBytes + 1023) / 1024 * 1024;
+    static constexpr uint32_t kBarOffset = kStagesG * kStageBytes;
+    static constexpr uint32_t kMergeOffset = kBarOffset + 2 * kStagesG * 8 + 32;  // + abort flag, unit ids
+    static constexpr uint32_t kMergeFloats = kWarps * G * (D + 2);
+    static constexpr uint32_t kIntsOffset = kMergeOffset + kMergeFloats * 4;
+    __host__ __device__ static size_t smem_bytes(int batch) {
+        return kIntsOffset + (size_t)(2 * batch + 2 + 64) * 4 + 1024;  // + 1024-byte alignment slack
+    }
+};
+
+__device__ __forceinline__ float ex2f(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+template <bool BF16>
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    if (BF16) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    } else {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+}
+
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack_pair(float a, float b) {
+    if (BF16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Shared-memory address of token row t, 16-byte chunk cc (0..7) of a 64-column half in the
+// 128-byte-swizzled layout TMA writes (chunk position cc ^ (t & 7)).
+__device__ __forceinline__ uint32_t swz(uint32_t half_base, int t, int cc) {
+    return half_base + (uint32_t)t * 128u + ((uint32_t)(cc ^ (t & 7)) << 4);
+}
+
+template <int D, int G, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_gqa_kernel(const __grid_constant__ CUtensorMap tm_kv, DecodeArgs a) {
+    using L = GqaLayout<D, G>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kBarOffset);
+    uint64_t *empty = full + kStagesG;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + kStagesG);
+    int *stage_unit = reinterpret_cast<int *>(empty + kStagesG) + 4;
+    float *merge = reinterpret_cast<float *>(smem + L::kMergeOffset);
+    int *lens = reinterpret_cast<int *>(smem + L::kIntsOffset);
+    int *prefix = lens + a.batch;
+    int *scan_tmp = prefix + a.batch + 1;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int hkv = a.cache.num_kv_heads, bs = a.cache.block_size, chunk = a.chunk;
+
+    if (tid == 0) {
+        for (int i = 0; i < kStagesG; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kWarps);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    decode_scan_units<kThreads>(a, lens, prefix, scan_tmp);
+    const int num_units = prefix[a.batch];
+
+    if (warp == kWarps) {
+        // ===================================== producer warp =====================================
+        const uint64_t pol = l2_policy_evict_first();
+        const uint16_t *qg = static_cast<const uint16_t *>(a.q);
+        const int box_rows = bs < kTile ? bs : kTile;
+        if (lane == 0) tc::prefetch_tensormap(&tm_kv);
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued_mask = 0, issued_parity = 0;
+        int u = 0;
+        if (lane == 0) u = atomicAdd(a.sched, 1);
+        u = __shfl_sync(0xffffffffu, u, 0);
+        while (u < num_units) {
+            int u_next = 0;
+            if (lane == 0) u_next = atomicAdd(a.sched, 1);
+            const UnitCursor c = unit_of(u, prefix, lens, a.batch, hkv, chunk);
+            const int *bt = a.block_tables + (size_t)c.b * a.max_blocks_per_seq;
+            for (int ts = c.t0; ts < c.t1; ts += kTile) {
+                const int n = min(kTile, c.t1 - ts);
+                const int page0 = ts >> a.cache.log2_block_size;
+                const int npages = bs < kTile ? (n + bs - 1) / bs : 1;
+                const int off = bs < kTile ? 0 : (ts & (bs - 1));
+                int pb = 0;
+                if (lane < npages) {
+                    pb = __ldg(bt + page0 + lane);
+                    if (pb < 0 || pb >= a.cache.num_blocks) {
+                        set_error(a.err, kErrDeviceRange);
+                        pb = 0;
+                    }
+                }
+                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.err)) {
+                    for (int i = 0; i < kStagesG; ++i)
+                        if (issued_mask & (1u << i)) {
+                            volatile int no_abort = 0;
+                            mbar_wait(&full[i], (issued_parity >> i) & 1u, &no_abort, nullptr);
+                        }
+                    return;
+                }
+                uint8_t *st = smem + (size_t)stage * L::kStageBytes;
+                const bool first_tile = (ts == c.t0);
+                if (lane == 0) {
+                    stage_unit[stage] = u;
+                    const uint32_t bytes = (uint32_t)npages * box_rows * 128u * L::kHalves * 2u +
+                                           (first_tile ? L::kQBytes : 0u);
+                    mbar_arrive_expect_tx(&full[stage], bytes);
+                }
+                __syncwarp();
+                if (lane < npages) {
+                    const int rowK = ((pb * 2 + 0) * hkv + c.kvh) * bs + off;
+                    const int rowV = rowK + hkv * bs;
+                    const uint32_t dst = (uint32_t)lane * box_rows * 128u;
+#pragma unroll
+                    for (int hf = 0; hf < L::kHalves; ++hf) {
+                        tc::tma_load_2d(st + hf * L::kHalfBytes + dst, &tm_kv, hf * 64, rowK, &full[stage]);
+                        tc::tma_load_2d(st + L::kKBytes + hf * L::kHalfBytes + dst, &tm_kv, hf * 64, rowV, &full[stage]);
+                    }
+                }
+                if (first_tile && lane == 0) {
+                    const uint16_t *qsrc = qg + ((size_t)c.b * a.num_q_heads + (size_t)c.kvh * G) * D;
+                    bulk_g2s(st + 2 * L::kKBytes, qsrc, L::kQBytes, &full[stage], pol);
+                }
+                issued_mask |= 1u << stage;
+                issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                if (++stage == kStagesG) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            u = __shfl_sync(0xffffffffu, u_next, 0);
+        }
+        if (mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.err) && lane == 0) {
+            stage_unit[stage] = -1;
+            mbar_arrive(&full[stage]);
+        }
+        return;
+    }
+
+    // ===================================== consumer warps =====================================
+    constexpr int kKSteps = D / 16;         // k-steps of q.K^T, m-tiles of O^T
+    const int gid = lane >> 2, tig = lane & 3;
+    const int g_lo = 2 * tig;               // this lane's two head slots (columns of S^T / O^T)
+    const float sl = a.scale * kLog2e;
+    uint32_t bq[kKSteps][2];                // q as B fragments (n = head slot, k = dims)
+    int stage = 0;
+    uint32_t phase = 0;
+    for (;;) {
+        if (!mbar_wait(&full[stage], phase, abort_flag, a.err)) return;
+        const int u = stage_unit[stage];
+        if (u < 0) break;
+        const UnitCursor c = unit_of(u, prefix, lens, a.batch, hkv, chunk);
+        float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+        float o[kKSteps][4];
+#pragma unroll
+        for (int mt = 0; mt < kKSteps; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+        for (int ts = c.t0; ts < c.t1; ts += kTile) {
+            const int n = min(kTile, c.t1 - ts);
+            if (ts != c.t0 && !mbar_wait(&full[stage], phase, abort_flag, a.err)) return;
+            uint8_t *st = smem + (size_t)stage * L::kStageBytes;
+            const uint32_t aK = smem_addr(st), aV = aK + L::kKBytes;
+            if (ts == c.t0) {
+                const uint16_t *sq = reinterpret_cast<const uint16_t *>(st + 2 * L::kKBytes);
+#pragma unroll
+                for (int kk = 0; kk < kKSteps; ++kk) {
+                    if (gid < G) {
+                        bq[kk][0] = *reinterpret_cast<const uint32_t *>(sq + gid * D + kk * 16 + 2 * tig);
+                        bq[kk][1] = *reinterpret_cast<const uint32_t *>(sq + gid * D + kk * 16 + 8 + 2 * tig);
+                    } else {
+                        bq[kk][0] = bq[kk][1] = 0u;
+                    }
+                }
+            }
+            const int t0w = warp * 16;      // this warp's tokens in the tile
+            if (t0w + 16 > n) {
+                // tokens at or beyond the context end may hold unwritten cache bytes (or stale
+                // tile data): zero this warp's V rows there so that 0 * garbage cannot reach O
+                for (int t = t0w + (lane >> 3); t < t0w + 16; t += 4) {
+                    if (t < n) continue;
+#pragma unroll
+                    for (int hf = 0; hf < L::kHalves; ++hf)
+                        *reinterpret_cast<uint4 *>(st + L::kKBytes + hf * L::kHalfBytes + t * 128 + (lane & 7) * 16) =
+                            make_uint4(0, 0, 0, 0);
+                }
+                __syncwarp();
+            }
+            // ---- S^T = K_w q^T: 16 tokens x 8 head slots ----
+            float s[4] = {0.f, 0.f, 0.f, 0.f};
+            {
+                const int mi = lane >> 3;
+                const int t = t0w + (lane & 7) + 8 * (mi & 1);
+#pragma unroll
+                for (int kk = 0; kk < kKSteps; ++kk) {
+                    uint32_t af[4];
+                    const int cc = 2 * (kk & 3) + (mi >> 1);
+                    ldsm_x4(swz(aK + (kk >> 2) * L::kHalfBytes, t, cc), af);
+                    mma16816<BF16>(s, af, bq[kk][0], bq[kk][1]);
+                }
+            }
+            const bool v0 = t0w + gid < n, v1 = t0w + gid + 8 < n;
+            s[0] = v0 ? s[0] : -INFINITY;
+            s[1] = v0 ? s[1] : -INFINITY;
+            s[2] = v1 ? s[2] : -INFINITY;
+            s[3] = v1 ? s[3] : -INFINITY;
+            // column max over the 16 tokens (lanes with the same tig)
+            float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+            for (int ofs = 4; ofs < 32; ofs <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, ofs));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, ofs));
+            }
+            mx0 *= sl;
+            mx1 *= sl;
+            // lazy rescale: the running max of a head moves only when a score exceeds it by > 2^8
+            if (mx0 > m[0] + kRescale) {
+                const float al = ex2f(m[0] - mx0);  // 0 when m = -inf
+                l[0] *= al;
+#pragma unroll
+                for (int mt = 0; mt < kKSteps; ++mt) {
+                    o[mt][0] *= al;
+                    o[mt][2] *= al;
+                }
+                m[0] = mx0;
+            }
+            if (mx1 > m[1] + kRescale) {
+                const float al = ex2f(m[1] - mx1);
+                l[1] *= al;
+#pragma unroll
+                for (int mt = 0; mt < kKSteps; ++mt) {
+                    o[mt][1] *= al;
+                    o[mt][3] *= al;
+                }
+                m[1] = mx1;
+            }
+            const float p0 = v0 ? ex2f(fmaf(s[0], sl, -m[0])) : 0.f;
+            const float p1 = v0 ? ex2f(fmaf(s[1], sl, -m[1])) : 0.f;
+            const float p2 = v1 ? ex2f(fmaf(s[2], sl, -m[0])) : 0.f;
+            const float p3 = v1 ? ex2f(fmaf(s[3], sl, -m[1])) : 0.f;
+            l[0] += p0 + p2;
+            l[1] += p1 + p3;
+            // P^T (tokens x head slots) in accumulator layout -> P as B fragments (k = tokens)
+            const uint32_t pb0 = movmatrix_t(pack_pair<BF16>(p0, p1));
+            const uint32_t pb1 = movmatrix_t(pack_pair<BF16>(p2, p3));
+            // ---- O^T += V_w^T P^T: D x 8 head slots ----
+            {
+                const int mi = lane >> 3;
+                const int t = t0w + (lane & 7) + 8 * (mi >> 1);
+#pragma unroll
+                for (int mt = 0; mt < kKSteps; ++mt) {
+                    uint32_t af[4];
+                    const int cc = 2 * (mt & 3) + (mi & 1);
+                    ldsm_x4_t(swz(aV + (mt >> 2) * L::kHalfBytes, t, cc), af);
+                    mma16816<BF16>(o[mt], af, pb0, pb1);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[stage]);
+            if (++stage == kStagesG) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        // ---- merge: sum l over the lanes of each head slot, then across the warps ----
+#pragma unroll
+        for (int ofs = 4; ofs < 32; ofs <<= 1) {
+            l[0] += __shfl_xor_sync(0xffffffffu, l[0], ofs);
+            l[1] += __shfl_xor_sync(0xffffffffu, l[1], ofs);
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int g = g_lo + j;
+            if (g < G) {
+                float *row = merge + ((size_t)warp * G + g) * (D + 2);
+#pragma unroll
+                for (int mt = 0; mt < kKSteps; ++mt) {
+                    row[mt * 16 + gid] = o[mt][j];
+                    row[mt * 16 + gid + 8] = o[mt][j + 2];
+                }
+                if (gid == 0) {
+                    row[D] = m[j];
+                    row[D + 1] = l[j];
+                }
+            }
+        }
+        named_barrier(1, kWarps * 32);
+        const int splits = (lens[c.b] + chunk - 1) / chunk;
+        for (int idx = tid; idx < G * D; idx += kWarps * 32) {
+            const int g = idx / D, d = idx - (idx / D) * D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, merge[((size_t)w * G + g) * (D + 2) + D]);
+            float lsum = 0.f, acc = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float *row = merge + ((size_t)w * G + g) * (D + 2);
+                const float mw = row[D];
+                const float wgt = (mw == -INFINITY) ? 0.f : ex2f(mw - M);
+                lsum += row[D + 1] * wgt;
+                acc += row[d] * wgt;
+            }
+            const float res = lsum > 0.f ? acc / lsum : 0.f;
+            const float lse_v = lsum > 0.f ? (M + log2f(lsum)) * kLn2 : -INFINITY;
+            const int h = c.kvh * G + g;
+            const size_t row_id = (size_t)c.b * a.num_q_heads + h;
+            if (splits == 1) {
+                store_out(a.out, row_id * D + d, res, a.out_dtype);
+                if (d == 0 && a.lse) a.lse[row_id] = lse_v;
+            } else {
+                const size_t pr = row_id * a.s_max + c.split;
+                a.part_o[pr * D + d] = res;
+                if (d == 0) a.part_lse[pr] = lse_v;
+            }
+        }
+        named_barrier(1, kWarps * 32);
+    }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <int D, int G, bool BF16>
+cudaError_t launch_gqa_t(const DecodeArgs &a, int grid, cudaStream_t s) {
+    CUtensorMap tm;
+    const int box_rows = a.cache.block_size < kTile ? a.cache.block_size : kTile;
+    cudaError_t e = encode_cache_map(a.cache, box_rows, &tm);
+    if (e != cudaSuccess) return e;
+    auto kern = decode_gqa_kernel<D, G, BF16>;
+    static bool configured[64] = {};
+    const int dev = device_info().device;
+    if (dev >= 64 || !configured[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)GqaLayout<D, G>::smem_bytes(kMaxBatchG));
+        if (e != cudaSuccess) return e;
+        if (dev < 64) configured[dev] = true;
+    }
+    kern<<<grid, kThreads, GqaLayout<D, G>::smem_bytes(a.batch), s>>>(tm, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_gqa(const DecodeArgs &a, int grid, cudaStream_t s) {
+    if (a.batch == 0) return cudaSuccess;
+    const int group = a.num_q_heads / a.cache.num_kv_heads;
+    const bool bf16 = a.cache.dtype == 1;
+    if (a.cache.head_dim == 128) {
+        if (group == 4) return bf16 ? launch_gqa_t<128, 4, true>(a, grid, s) : launch_gqa_t<128, 4, false>(a, grid, s);
+        if (group == 8) return bf16 ? launch_gqa_t<128, 8, true>(a, grid, s) : launch_gqa_t<128, 8, false>(a, grid, s);
+    } else {
+        if (group == 4) return bf16 ? launch_gqa_t<64, 4, true>(a, grid, s) : launch_gqa_t<64, 4, false>(a, grid, s);
+        if (group == 8) return bf16 ? launch_gqa_t<64, 8, true>(a, grid, s) : launch_gqa_t<64, 8, false>(a, grid, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pkv

@@ -222,7 +222,9 @@ pkv_status pkv_paged_attn_decode(pkv_cache cache, const void *q, int num_q_heads
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const int grid = s.info.num_sms * s.info.decode_ctas_per_sm;
     if (cudaMemsetAsync(a.sched, 0, sizeof(int), cs) != cudaSuccess) return PKV_ERR_CUDA;
-    if (launch_decode(a, grid, cs) != cudaSuccess) return PKV_ERR_CUDA;
+    // four or more query heads per KV head: the group's products run on tensor cores
+    const cudaError_t le = group >= 4 ? launch_decode_gqa(a, grid, cs) : launch_decode(a, grid, cs);
+    if (le != cudaSuccess) return PKV_ERR_CUDA;
     // Rows that span several splits (and empty rows) are finished by the merge.
     CombineArgs c;
     c.part_o = a.part_o;

@@ -2,6 +2,7 @@
 // and the kernel translation units.  Arguments arrive here already validated.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -80,6 +81,8 @@ const DeviceInfo &device_info();
 constexpr int kDecodeTile = 64;  // tokens per decode pipeline stage
 
 cudaError_t launch_append(const AppendArgs &a, cudaStream_t s);
+cudaError_t encode_cache_map(const CacheView &c, int box_rows, CUtensorMap *map);
+cudaError_t launch_decode_gqa(const DecodeArgs &a, int grid, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs &a, int grid, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t s);

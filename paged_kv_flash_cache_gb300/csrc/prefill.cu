@@ -488,6 +488,29 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+}  // namespace
+
+// 2-D tensor map over the cache viewed as rows of D elements (row ((pb*2 + kv)*Hkv + h)*bs + off),
+// boxes of 64 columns x box_rows rows, 128-byte swizzle.
+cudaError_t encode_cache_map(const CacheView &c, int box_rows, CUtensorMap *map) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const CUtensorMapDataType dt = c.dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const cuuint64_t nrows = (cuuint64_t)c.num_blocks * 2 * c.num_kv_heads * c.block_size;
+    if (nrows > 0x7fffffffull || nrows == 0) return cudaErrorNotSupported;  // TMA row coordinates are int32
+    cuuint64_t dims[2] = {(cuuint64_t)c.head_dim, nrows};
+    cuuint64_t strides[1] = {(cuuint64_t)c.head_dim * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(map, dt, 2, const_cast<void *>(c.ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+        CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    return cudaSuccess;
+}
+
+namespace {
+
 template <int D, bool BF16>
 cudaError_t launch_t(const PrefillArgs &a, cudaStream_t stream) {
     using Lay = PrefillLayout<D>;
@@ -507,17 +530,8 @@ cudaError_t launch_t(const PrefillArgs &a, cudaStream_t stream) {
             return cudaErrorInvalidValue;
     }
     {
-        // cache viewed as rows of D elements: row ((pb*2 + kv)*Hkv + h)*bs + off
-        const cuuint64_t nrows = (cuuint64_t)a.cache.num_blocks * 2 * a.cache.num_kv_heads * a.cache.block_size;
-        if (nrows > 0x7fffffffull) return cudaErrorNotSupported;  // TMA row coordinates are int32
-        cuuint64_t dims[2] = {(cuuint64_t)D, nrows};
-        cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-        cuuint32_t box[2] = {64, (cuuint32_t)(a.cache.block_size < kBN ? a.cache.block_size : kBN)};
-        cuuint32_t es[2] = {1, 1};
-        if (enc(&tm_kv, dt, 2, const_cast<void *>(a.cache.ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
+        const cudaError_t e = encode_cache_map(a.cache, a.cache.block_size < kBN ? a.cache.block_size : kBN, &tm_kv);
+        if (e != cudaSuccess) return e;
     }
     PrefillParams p;
     p.cu_q_lens = a.cu_q_lens;

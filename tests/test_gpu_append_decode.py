@@ -29,6 +29,12 @@ def problem(*, lens, hq=8, hkv=8, d=128, bs=16, dtype=W.F16, seed=5, extra=7, mb
                           num_blocks=nb, free_order=order, max_blocks_per_seq=mb)
 
 
+def p_roundings(p):
+    """Roundings to the input type on the decode path besides the output: with four or more query
+    heads per KV head the group's P.V contraction runs on tensor cores with P in the input type."""
+    return 1 if p.num_q_heads // p.num_kv_heads >= 4 else 0
+
+
 def run_decode(p, cache, num_splits=0, out_dtype=None, with_lse=True):
     q = to_dev(p.q)
     lse = torch.empty((p.batch, p.num_q_heads), dtype=torch.float32, device="cuda") if with_lse else None
@@ -130,7 +136,7 @@ def test_decode_gqa_dtypes(dtype, hq, hkv, d):
     cache = device_cache(p)
     out, lse = run_decode(p, cache)
     ref, ref_lse = oracle.attention_of(p, cache_bits(cache))
-    check_close(out, ref, dtype, roundings=1, what="%s hq=%d hkv=%d d=%d" % (dtype, hq, hkv, d))
+    check_close(out, ref, dtype, roundings=1 + p_roundings(p), what="%s hq=%d hkv=%d d=%d" % (dtype, hq, hkv, d))
     np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-5, atol=1e-5)
 
 
@@ -140,8 +146,18 @@ def test_decode_explicit_splits_and_fp32_output(num_splits):
     cache = device_cache(p)
     out, lse = run_decode(p, cache, num_splits=num_splits, out_dtype=torch.float32)
     ref, ref_lse = oracle.attention_of(p, cache_bits(cache))
-    # FP32 output: no rounding to bf16 anywhere on the decode path -> the literal bounds
-    check_close(out, ref, "bf16", roundings=0, what="splits=%d fp32 out" % num_splits)
+    # FP32 output: the only rounding left is P before the tensor-core P.V of a 4-head group
+    check_close(out, ref, "bf16", roundings=p_roundings(p), what="splits=%d fp32 out" % num_splits)
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-5, atol=1e-5)
+
+
+def test_decode_fp32_output_literal_bounds_mha():
+    """MHA decode keeps P in FP32: with an FP32 output nothing is rounded to bf16 -> literal bounds."""
+    p = problem(lens=[3000, 64, 1, 2500], hq=4, hkv=4, bs=16, dtype=W.BF16, mb=256)
+    cache = device_cache(p)
+    out, lse = run_decode(p, cache, num_splits=3, out_dtype=torch.float32)
+    ref, ref_lse = oracle.attention_of(p, cache_bits(cache))
+    check_close(out, ref, "bf16", roundings=0, what="mha fp32 out")
     np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-5, atol=1e-5)
 
 

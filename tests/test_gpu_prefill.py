@@ -98,10 +98,11 @@ def test_prefill_first_row_is_v0_and_q_len_one_is_decode():
     out_d = pkv.paged_attn_decode(cache_d, to_dev(d.q), to_dev(d.block_tables), to_dev(d.context_lens),
                                   scale=d.scale, out_dtype=torch.float32)
     torch.cuda.synchronize()
-    # both within their bounds of the oracle; the prefill also rounds P to bf16
+    # both within their bounds of the oracle; each rounds P to bf16 (the prefill always, the decode
+    # because this is a 4-head group on tensor cores)
     ref, _ = oracle.attention_of(d, cache_bits(cache_d))
     check_close(out_p, ref, "bf16", roundings=1, what="q_len 1 prefill")
-    check_close(out_d, ref, "bf16", roundings=0, what="decode")
+    check_close(out_d, ref, "bf16", roundings=1, what="decode")
 
 
 def test_prefill_bad_lengths_flag_error():

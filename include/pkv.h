@@ -100,9 +100,9 @@ PKV_API pkv_status pkv_kv_cache_append(pkv_cache cache, const void *k_new, const
                                const int *block_tables, int batch, int max_blocks_per_seq,
                                int num_new_tokens, void *stream);
 
-/* Bytes of workspace pkv_paged_attn_decode needs for these sizes: a 256-byte header
- * (a work counter) plus, when a context can span several splits, the FP32 split
- * partials.  num_splits as passed to pkv_paged_attn_decode (0 = automatic). */
+/* Bytes of workspace pkv_paged_attn_decode needs for these sizes: the FP32 split
+ * partials, or 0 when no context can span several splits.  num_splits as passed to
+ * pkv_paged_attn_decode (0 = automatic). */
 PKV_API size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim,
                                  int block_size, int max_blocks_per_seq, int num_splits);
 
@@ -122,8 +122,7 @@ PKV_API int pkv_decode_split_tokens(int batch, int num_q_heads, int num_kv_heads
  *   num_splits    0 = automatic; else the context capacity
  *                 max_blocks_per_seq * block_size is cut into this many splits.
  *   workspace     device scratch of at least pkv_decode_workspace_size() bytes
- *                 (work counter, FP32 partial outputs and their lse); contents need
- *                 no init: the call clears the counter on `stream` before its kernels.
+ *                 (FP32 partial outputs and their lse); contents need no init.
  *   out           [batch, Hq, D] in out_dtype (the cache dtype or PKV_F32).
  *   lse           FP32 [batch, Hq] or NULL.
  * Launches the split kernel and, when some context spans several splits, the
@@ -180,9 +179,8 @@ PKV_API pkv_status pkv_attn_combine(const float *partial_o, const float *partial
  *   - The first call on each device (that device current) looks up the array's device
  *     address with cudaGetSymbolAddress; make that first call before any stream
  *     capture.
- *   - All calls share the one array, which keeps the last call's contents.  Each
- *     call clears the work counter at its start and writes every partial it later
- *     reads, so nothing has to be zeroed by the caller.
+ *   - All calls share the one array, which keeps the last call's contents.  Nothing
+ *     in it has to start at zero: each call writes every partial it later reads.
  *     Calls that overlap on the GPU (concurrent streams, or several host threads)
  *     race on the array: serialise them. */
 #define PKV_DECODE_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)

@@ -187,8 +187,8 @@ def paged_attn_decode(cache, q, block_tables, context_lens, scale: Optional[floa
     if out is None:
         out = torch.empty((batch, hq, d), dtype=out_dtype or cache.dtype, device=q.device)
     need = decode_workspace_size(batch, hq, cache.shape[2], d, cache.shape[3], mb, num_splits)
-    if workspace is None:
-        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     scale = (1.0 / math.sqrt(d)) if scale is None else float(scale)
     _check(lib.pkv_paged_attn_decode(c, _dev(q, "q"), hq, _i32(block_tables, "block_tables"),

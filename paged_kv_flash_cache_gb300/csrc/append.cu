@@ -6,9 +6,10 @@
 // ("企业官网建设流程全解析", section 2.1) of the cache [num_blocks, 2, num_heads, block_size,
 // head_dim] ("Flash Attention与Paged Attention如何共同优化大模型推理？", section 3).
 //
-// One warp per new token: the warp resolves (sequence, position, page) once, then moves the
-// token's Hkv x D K row-set and V row-set as 16-byte vectors.  Reads of k_new / v_new are
-// contiguous; each destination head row (D elements) is a contiguous 128 / 256-byte run.
+// One warp per (new token, group of 8 heads): the warp resolves (sequence, position, page), then
+// moves those heads' K rows and V rows as 16-byte vectors. Reads of k_new / v_new are contiguous;
+// each destination head row (D elements) is a contiguous 128 / 256-byte run. Small items keep
+// every SM busy even when a call appends a few thousand tokens.
 // Pure bandwidth: 2 reads + 2 writes of Hkv * D * 2 bytes per token.
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
@@ -27,12 +28,16 @@ __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
     return v;
 }
 
+constexpr int kHeadsPerItem = 8;  // a work item is one token's K and V rows of up to 8 heads
+
 template <int D>
 __global__ void __launch_bounds__(kAppendThreads) append_kernel(AppendArgs a) {
     constexpr int kVecPerRow = D / 8;  // 16-byte vectors per head row
     const int lane = threadIdx.x & 31;
     const int warps_total = gridDim.x * (kAppendThreads / 32);
     const int hkv = a.num_kv_heads;
+    const int chunks = (hkv + kHeadsPerItem - 1) / kHeadsPerItem;
+    const long long items = (long long)a.num_new_tokens * chunks;
     const int vec_per_token = hkv * kVecPerRow;
     const uint4 *kn = static_cast<const uint4 *>(a.k_new);
     const uint4 *vn = static_cast<const uint4 *>(a.v_new);
@@ -41,7 +46,12 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(AppendArgs a) {
     const size_t head_stride = (size_t)a.block_size * kVecPerRow;
     const size_t kv_stride = (size_t)hkv * head_stride;
 
-    for (int t = blockIdx.x * (kAppendThreads / 32) + (threadIdx.x >> 5); t < a.num_new_tokens; t += warps_total) {
+    pdl_wait();  // the previous kernel may still read the pages this call writes
+    for (long long it = (long long)blockIdx.x * (kAppendThreads / 32) + (threadIdx.x >> 5); it < items;
+         it += warps_total) {
+        const int t = (int)(it / chunks);
+        const int h0 = (int)(it - (long long)t * chunks) * kHeadsPerItem;
+        const int nvec = min(kHeadsPerItem, hkv - h0) * kVecPerRow;
         // sequence of token t: last b with cu_new_lens[b] <= t
         int lo = 0, hi = a.batch;  // answer in [lo, hi)
         while (hi - lo > 1) {
@@ -62,14 +72,14 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(AppendArgs a) {
         }
         const int off = (int)(pos & (a.block_size - 1));
         const size_t page_base = (size_t)pb * 2 * kv_stride + (size_t)off * kVecPerRow;
-        const uint4 *ks = kn + (size_t)t * vec_per_token;
-        const uint4 *vs = vn + (size_t)t * vec_per_token;
-        for (int c0 = lane; c0 < vec_per_token; c0 += 32 * kUnroll) {
+        const uint4 *ks = kn + (size_t)t * vec_per_token + (size_t)h0 * kVecPerRow;
+        const uint4 *vs = vn + (size_t)t * vec_per_token + (size_t)h0 * kVecPerRow;
+        for (int c0 = lane; c0 < nvec; c0 += 32 * kUnroll) {
             uint4 kv[kUnroll], vv[kUnroll];
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 const int c = c0 + u * 32;
-                if (c < vec_per_token) {
+                if (c < nvec) {
                     kv[u] = ld_stream(ks + c);
                     vv[u] = ld_stream(vs + c);
                 }
@@ -77,9 +87,9 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(AppendArgs a) {
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 const int c = c0 + u * 32;
-                if (c < vec_per_token) {
-                    const int h = c / kVecPerRow;
-                    const int e = c - h * kVecPerRow;
+                if (c < nvec) {
+                    const int h = h0 + c / kVecPerRow;
+                    const int e = c % kVecPerRow;
                     const size_t dst = page_base + (size_t)h * head_stride + e;
                     cache[dst] = kv[u];
                     cache[dst + kv_stride] = vv[u];
@@ -87,6 +97,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(AppendArgs a) {
             }
         }
     }
+    pdl_launch_dependents();
 }
 
 }  // namespace
@@ -94,15 +105,12 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(AppendArgs a) {
 cudaError_t launch_append(const AppendArgs &a, cudaStream_t s) {
     if (a.num_new_tokens == 0 || a.batch == 0) return cudaSuccess;
     const int warps_per_cta = kAppendThreads / 32;
-    const int want = (a.num_new_tokens + warps_per_cta - 1) / warps_per_cta;
+    const long long items = (long long)a.num_new_tokens * ((a.num_kv_heads + kHeadsPerItem - 1) / kHeadsPerItem);
+    const long long want = (items + warps_per_cta - 1) / warps_per_cta;
     const int cap = device_info().num_sms * 8;
-    const int grid = want < cap ? want : cap;
-    if (a.head_dim == 128) {
-        append_kernel<128><<<grid, kAppendThreads, 0, s>>>(a);
-    } else {
-        append_kernel<64><<<grid, kAppendThreads, 0, s>>>(a);
-    }
-    return cudaGetLastError();
+    const int grid = want < cap ? (int)want : cap;
+    if (a.head_dim == 128) return launch_pdl(append_kernel<128>, dim3(grid), dim3(kAppendThreads), 0, s, a);
+    return launch_pdl(append_kernel<64>, dim3(grid), dim3(kAppendThreads), 0, s, a);
 }
 
 }  // namespace pkv

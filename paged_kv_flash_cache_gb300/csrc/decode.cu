@@ -11,7 +11,8 @@
 //
 // Kernel structure (one persistent CTA per SM slot):
 //   * work unit = (sequence, KV head, split); units are numbered in a prologue from the
-//     context lengths (block-wide scan) and claimed in order from a counter in the workspace;
+//     context lengths (block-wide scan) and dealt round-robin to the CTAs, so concurrent CTAs
+//     stream neighbouring head slices of the same pages;
 //   * warp 4 (producer) streams each unit's tokens in 64-token tiles into a ring of
 //     shared-memory stages with bulk copies (TMA engine, one copy per page slice of K and of
 //     V -- pages are contiguous [block_size, D] rows), completion on an mbarrier;
@@ -106,16 +107,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
         uint32_t phase = 0;
         uint32_t issued_mask = 0;  // stages with copies issued (bit i), for the abort drain
         uint32_t issued_parity = 0;
-        // Units are claimed from a counter in the workspace (cleared by the host before the launch):
-        // CTAs take them in order, so concurrent CTAs stream neighbouring head slices of the same
-        // pages, and a CTA that finishes early takes more. The next claim is made while the
-        // current unit's tiles are issued.
-        int u = 0;
-        if (lane == 0) u = atomicAdd(a.sched, 1);
-        u = __shfl_sync(0xffffffffu, u, 0);
-        while (u < num_units) {
-            int u_next = 0;
-            if (lane == 0) u_next = atomicAdd(a.sched, 1);
+        pdl_wait();  // the cache may have just been written by the previous kernel
+        for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
             const UnitCursor c = unit_of(u, prefix, lens, a.batch, hkv, chunk);
             const int *bt = a.block_tables + (size_t)c.b * a.max_blocks_per_seq;
             for (int ts = c.t0; ts < c.t1; ts += L::kTile) {
@@ -174,7 +167,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
                     phase ^= 1u;
                 }
             }
-            u = __shfl_sync(0xffffffffu, u_next, 0);
         }
         // end marker: one more stage carrying unit id -1
         if (mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.err) && lane == 0) {
@@ -474,7 +466,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
         }
         named_barrier(1, kConsumerWarps * 32);
     }
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    pdl_launch_dependents();
 }
 
 // ---- split merge: one warp per output row --------------------------------------------------
@@ -549,8 +541,7 @@ cudaError_t launch_decode_t(const DecodeArgs &a, int grid, cudaStream_t s) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    kern<<<grid, kDecodeThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kDecodeThreads), smem, s, a);
 }
 
 template <typename Tag, int D>

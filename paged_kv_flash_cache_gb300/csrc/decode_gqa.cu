@@ -12,8 +12,8 @@
 // 16 dims.
 //
 // Kernel structure (persistent, one CTA per SM, 5 warps):
-//   * units (sequence, KV head, split) are numbered from the context lengths and claimed in order
-//     from a counter in the workspace, as in decode.cu;
+//   * units (sequence, KV head, split) are numbered from the context lengths and dealt
+//     round-robin to the CTAs, as in decode.cu;
 //   * warp 4 streams each unit's 64-token tiles with TMA: the pages a tile covers are looked up by
 //     the warp's lanes and each lane issues its page's K and V boxes (64 columns x rows, 128-byte
 //     swizzle, through a 2-D tensor map over the cache), into a 4-stage ring; q comes in with the
@@ -152,12 +152,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int stage = 0;
         uint32_t phase = 0;
         uint32_t issued_mask = 0, issued_parity = 0;
-        int u = 0;
-        if (lane == 0) u = atomicAdd(a.sched, 1);
-        u = __shfl_sync(0xffffffffu, u, 0);
-        while (u < num_units) {
-            int u_next = 0;
-            if (lane == 0) u_next = atomicAdd(a.sched, 1);
+        pdl_wait();  // the cache may have just been written by the previous kernel
+        for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
             const UnitCursor c = unit_of(u, prefix, lens, a.batch, hkv, chunk);
             const int *bt = a.block_tables + (size_t)c.b * a.max_blocks_per_seq;
             for (int ts = c.t0; ts < c.t1; ts += kTile) {
@@ -211,7 +207,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     phase ^= 1u;
                 }
             }
-            u = __shfl_sync(0xffffffffu, u_next, 0);
         }
         if (mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.err) && lane == 0) {
             stage_unit[stage] = -1;
@@ -396,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         named_barrier(1, kWarps * 32);
     }
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    pdl_launch_dependents();
 }
 
 template <int D, int G, bool BF16>
@@ -414,8 +409,7 @@ cudaError_t launch_gqa_t(const DecodeArgs &a, int grid, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         if (dev < 64) configured[dev] = true;
     }
-    kern<<<grid, kThreads, GqaLayout<D, G>::smem_bytes(a.batch), s>>>(tm, a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), GqaLayout<D, G>::smem_bytes(a.batch), s, tm, a);
 }
 
 }  // namespace

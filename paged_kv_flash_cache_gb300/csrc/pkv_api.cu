@@ -28,8 +28,6 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
-// Decode workspace: a 256-byte header (the unit claim counter) before the split partials.
-constexpr size_t kWorkspaceHeader = 256;
 
 int ilog2(int x) {
     int r = 0;
@@ -173,9 +171,8 @@ size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads, i
     const long long cap = (long long)max_blocks_per_seq * block_size;
     const int chunk = split_tokens(batch, num_kv_heads, block_size, max_blocks_per_seq, num_splits);
     const long long s_max = (cap + chunk - 1) / chunk;
-    // the unit claim counter, then (when a context can span several splits) the partials
-    const size_t partials = s_max <= 1 ? 0 : (size_t)batch * num_q_heads * s_max * (head_dim + 1) * sizeof(float);
-    return kWorkspaceHeader + partials;
+    if (s_max <= 1) return 0;
+    return (size_t)batch * num_q_heads * s_max * (head_dim + 1) * sizeof(float);
 }
 
 pkv_status pkv_paged_attn_decode(pkv_cache cache, const void *q, int num_q_heads, const int *block_tables,
@@ -200,7 +197,7 @@ pkv_status pkv_paged_attn_decode(pkv_cache cache, const void *q, int num_q_heads
     const int s_max = (int)((cap + chunk - 1) / chunk);
     const size_t need = pkv_decode_workspace_size(batch, num_q_heads, cache.num_kv_heads, cache.head_dim,
                                                   cache.block_size, max_blocks_per_seq, num_splits);
-    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PKV_ERR_WORKSPACE;
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return PKV_ERR_WORKSPACE;
     DecodeArgs a;
     a.cache = view_of(cache);
     a.q = q;
@@ -212,16 +209,14 @@ pkv_status pkv_paged_attn_decode(pkv_cache cache, const void *q, int num_q_heads
     a.scale = scale;
     a.chunk = chunk;
     a.s_max = s_max;
-    a.sched = static_cast<int *>(workspace);
-    a.part_o = reinterpret_cast<float *>(static_cast<char *>(workspace) + kWorkspaceHeader);
-    a.part_lse = need > kWorkspaceHeader ? a.part_o + (size_t)batch * num_q_heads * s_max * cache.head_dim : nullptr;
+    a.part_o = static_cast<float *>(workspace);
+    a.part_lse = need > 0 ? a.part_o + (size_t)batch * num_q_heads * s_max * cache.head_dim : nullptr;
     a.out = out;
     a.out_dtype = (int)out_dtype;
     a.lse = lse;
     a.err = s.err_ptr;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const int grid = s.info.num_sms * s.info.decode_ctas_per_sm;
-    if (cudaMemsetAsync(a.sched, 0, sizeof(int), cs) != cudaSuccess) return PKV_ERR_CUDA;
     // four or more query heads per KV head: the group's products run on tensor cores
     const cudaError_t le = group >= 4 ? launch_decode_gqa(a, grid, cs) : launch_decode(a, grid, cs);
     if (le != cudaSuccess) return PKV_ERR_CUDA;

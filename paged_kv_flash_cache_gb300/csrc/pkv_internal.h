@@ -35,7 +35,6 @@ struct DecodeArgs {
     float scale;
     int chunk;   // tokens per split (multiple of the decode tile)
     int s_max;   // splits a full-capacity context uses: ceil(max_blocks_per_seq * block_size / chunk)
-    int *sched;       // unit claim counter (zero at launch)
     float *part_o;    // [batch, Hq, s_max, D]
     float *part_lse;  // [batch, Hq, s_max]
     void *out;
@@ -69,6 +68,24 @@ struct PrefillArgs {
     float *lse;
     int *err;
 };
+
+// Launch with programmatic stream serialization (the kernel calls pdl_wait() before touching
+// memory the previous kernel may write).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
 
 // Per-device facts cached on first use.
 struct DeviceInfo {

@@ -187,6 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ==================================== TMA producer ====================================
             const int box_rows = p.bs < kBN ? p.bs : kBN;
             uint32_t issued = 0;  // ring items issued (for the abort drain)
+            pdl_wait();  // the chunk's own K/V may have just been appended by the previous kernel
             if (lane == 0) {
                 tc::prefetch_tensormap(&tm_q);
                 tc::prefetch_tensormap(&tm_kv);
@@ -463,6 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc::fence_before_sync();
     __syncthreads();
+    pdl_launch_dependents();
     if (warp == 1) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, Lay::kTmemCols);
@@ -560,8 +562,7 @@ cudaError_t launch_t(const PrefillArgs &a, cudaStream_t stream) {
         if (dev < 64) configured[dev] = true;
     }
     dim3 grid((a.max_q_len + kRows - 1) / kRows, a.num_q_heads, a.batch);
-    kern<<<grid, kThreads, Lay::kSmemBytes, stream>>>(tm_q, tm_kv, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, dim3(kThreads), Lay::kSmemBytes, stream, tm_q, tm_kv, p);
 }
 
 }  // namespace

@@ -80,10 +80,10 @@ def test_host_validation_without_gpu(lib):
 
 
 def test_workspace_sizing_with_explicit_splits(lib):
-    # capacity 4 * 16 = 64 tokens in 1 split: only the 256-byte header (work counter)
-    assert pkv.decode_workspace_size(2, 4, 4, 128, 16, 4, num_splits=1) == 256
-    # capacity 512 * 16 = 8192 tokens in 4 splits of 2048: header + B * Hq * 4 * (D + 1) floats
+    # capacity 4 * 16 = 64 tokens in 1 split: no workspace
+    assert pkv.decode_workspace_size(2, 4, 4, 128, 16, 4, num_splits=1) == 0
+    # capacity 512 * 16 = 8192 tokens in 4 splits of 2048: B * Hq * 4 * (D + 1) floats
     assert pkv.decode_split_tokens(16, 32, 32, 128, 16, 512, num_splits=4) == 2048
-    assert pkv.decode_workspace_size(16, 32, 32, 128, 16, 512, num_splits=4) == 256 + 16 * 32 * 4 * 129 * 4
+    assert pkv.decode_workspace_size(16, 32, 32, 128, 16, 512, num_splits=4) == 16 * 32 * 4 * 129 * 4
     # split size is rounded up to the 64-token tile
     assert pkv.decode_split_tokens(1, 8, 8, 64, 16, 10, num_splits=3) == 64

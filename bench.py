@@ -556,7 +556,7 @@ def main():
     value = total_kv / (ms * 1e-3) / 1e9
     e2e_ms = dist.max(r["e2e_ms_per_step"])
     achieved = r["bytes"]["total"] / (r["decode_ms"] * 1e-3) / 1e9
-    files = ["decode.cu", "pkv_device.cuh", "pkv_internal.h"]
+    files = ["decode.cu", "decode_common.cuh", "pkv_device.cuh", "pkv_internal.h"]
     roofline = {"bound": "hbm", "kernel": "paged_attn_decode call (decode_split_kernel + combine_kernel)",
                 "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / pk["hbm_gbs"], 3), "peak_source": pk["source"],

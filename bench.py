@@ -45,7 +45,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", default="", help="comma list of extra workloads (bs_sweep,mixed,prefill)")
+    ap.add_argument("--only", default="", help="comma list of extra workloads (bs_sweep,mixed,prefix,prefill)")
     ap.add_argument("--profile", choices=["decode", "append", "prefill", "decode_mixed"], default=None,
                     help="small case for ncu captures: W + K launches of one kernel, nothing else timed")
     return ap.parse_args()
@@ -432,6 +432,51 @@ def bench_mixed(torch, steps, warmup):
             "tokens_per_s": round(p.batch / ms * 1e3, 1)}
 
 
+def bench_prefix(torch, steps, warmup):
+    """Decode over a batch whose block tables share a cached prompt's pages (prefix caching),
+    against the same contexts with private copies of those pages."""
+    import paged_kv_flash_cache_gb300 as pkv
+    from paged_kv_flash_cache_gb300 import workloads as W
+    p = W.prefix_shared(pool_init="none", device="cuda")
+    shape = (p.num_blocks, 2, p.num_kv_heads, p.block_size, p.head_dim)
+    cache = torch.zeros(shape, dtype=p.k_ctx.dtype, device="cuda")
+    for a in (W.shared_append(p), W.private_append(p)):
+        pkv.kv_cache_append(cache, a["k_new"].cuda(), a["v_new"].cuda(), a["cu_new_lens"].cuda(),
+                            a["ctx_before"].cuda(), a["block_tables"].cuda())
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    lens = p.context_lens.tolist()
+    flat = W.make_problem("prefix_unshared", batch=p.batch, num_q_heads=32, num_kv_heads=32, head_dim=128,
+                          block_size=16, context_lens=lens, q_lens=[1] * p.batch, dtype=p.dtype, causal=False,
+                          seed=5, pool_init="none", kv_data=(p.k_ctx, p.v_ctx), device="cuda")
+    res = {}
+    for name, prob, c in (("shared", p, cache), ("unshared", flat, None)):
+        if c is None:
+            c = device_problem(prob, torch)
+        q, bt, ctx = p.q.cuda(), prob.block_tables.cuda(), prob.context_lens.cuda()
+        ws = torch.empty(max(16, pkv.decode_workspace_size(p.batch, 32, 32, 128, 16, bt.shape[1])),
+                         dtype=torch.uint8, device="cuda")
+        o = torch.empty((p.batch, 32, 128), dtype=q.dtype, device="cuda")
+        fn = lambda i: pkv.paged_attn_decode(c, q, bt, ctx, scale=p.scale, workspace=ws, out=o)
+        for i in range(warmup):
+            fn(i)
+        res[name] = time_loop(torch, fn, steps, torch.cuda.current_stream()) / steps
+        del c
+    del cache
+    torch.cuda.empty_cache()
+    logical = p.kv_bytes_read()
+    s_tok = p.meta["shared_tokens"]
+    unique = (s_tok + sum(L - s_tok for L in lens)) * p.num_kv_heads * p.head_dim * 2 * 2
+    ms = res["shared"]
+    return {"workload": "16 requests sharing a 4096-token prompt (256 shared pages of 16) + 256..2048 own tokens "
+                        "each, 32 heads x 128, fp16; decode; same contexts with private pages for comparison",
+            "ms": round(ms, 4), "unshared_ms": round(res["unshared"], 4),
+            "logical_kv_gbs": round(logical / ms / 1e6, 1), "unique_kv_bytes": unique, "logical_kv_bytes": logical,
+            "unique_kv_gbs": round(unique / ms / 1e6, 1),
+            "unshared_frac_of_hbm": round(decode_bytes(flat)["total"] / res["unshared"] / 1e6 / peaks()["hbm_gbs"], 3),
+            "tokens_per_s": round(p.batch / ms * 1e3, 1)}
+
+
 def bench_prefill(torch, steps, warmup):
     import paged_kv_flash_cache_gb300 as pkv
     from paged_kv_flash_cache_gb300 import workloads as W
@@ -573,7 +618,8 @@ def main():
     if dist.rank == 0 and not args.no_extra:
         extra = {}
         only = set(filter(None, args.only.split(",")))
-        for name, fn in (("bs_sweep", bench_bs_sweep), ("mixed", bench_mixed), ("prefill", bench_prefill)):
+        for name, fn in (("bs_sweep", bench_bs_sweep), ("mixed", bench_mixed), ("prefix", bench_prefix),
+                         ("prefill", bench_prefill)):
             if only and name not in only:
                 continue
             try:

@@ -93,6 +93,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
         *abort_flag = 0;
         fence_barrier_init();
     }
+    // Everything below may read memory the previous kernel on the stream wrote (lengths, tables,
+    // q, the cache), so only the barrier set-up above overlaps that kernel's tail.
+    pdl_wait();
     // ---- prologue: clamp lengths, units per sequence, exclusive scan (all threads) ----
     decode_scan_units<kDecodeThreads>(a, lens, prefix, scan_tmp);
     const int num_units = prefix[a.batch];
@@ -107,7 +110,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
         uint32_t phase = 0;
         uint32_t issued_mask = 0;  // stages with copies issued (bit i), for the abort drain
         uint32_t issued_parity = 0;
-        pdl_wait();  // the cache may have just been written by the previous kernel
         for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
             const UnitCursor c = unit_of(u, prefix, lens, a.batch, hkv, chunk);
             const int *bt = a.block_tables + (size_t)c.b * a.max_blocks_per_seq;

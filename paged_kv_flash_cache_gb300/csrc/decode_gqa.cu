@@ -140,6 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         fence_barrier_init();
     }
+    pdl_wait();  // lengths, tables, q and the cache may come from the previous kernel
     decode_scan_units<kThreads>(a, lens, prefix, scan_tmp);
     const int num_units = prefix[a.batch];
 
@@ -152,7 +153,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         int stage = 0;
         uint32_t phase = 0;
         uint32_t issued_mask = 0, issued_parity = 0;
-        pdl_wait();  // the cache may have just been written by the previous kernel
         for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
             const UnitCursor c = unit_of(u, prefix, lens, a.batch, hkv, chunk);
             const int *bt = a.block_tables + (size_t)c.b * a.max_blocks_per_seq;

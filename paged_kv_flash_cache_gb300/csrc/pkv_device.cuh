@@ -103,10 +103,11 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
 }
 
 // Programmatic dependent launch. A kernel launched with programmatic stream serialization may
-// start while the previous kernel on its stream drains: before pdl_wait() it touches only
-// memory that no kernel of this library writes (lengths, block tables) and its own shared
-// memory; pdl_wait() returns once the previous kernel has completed and its writes are visible.
-// pdl_launch_dependents() lets the next such kernel start launching.
+// start while the previous kernel on its stream drains: before pdl_wait() it touches only its
+// kernel parameters and its own shared memory (any global input may have been written by the
+// previous kernel, the caller's included); pdl_wait() returns once the previous kernel has
+// completed and its writes are visible. pdl_launch_dependents() lets the next such kernel start
+// launching.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -142,6 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int mt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    pdl_wait();  // lengths, tables, q and the chunk's own K/V may come from the previous kernel
     const int q0 = __ldg(p.cu_q_lens + b);
     const int q_len = __ldg(p.cu_q_lens + b + 1) - q0;
     const int m_start = mt * kRows;
@@ -187,7 +188,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ==================================== TMA producer ====================================
             const int box_rows = p.bs < kBN ? p.bs : kBN;
             uint32_t issued = 0;  // ring items issued (for the abort drain)
-            pdl_wait();  // the chunk's own K/V may have just been appended by the previous kernel
             if (lane == 0) {
                 tc::prefetch_tensormap(&tm_q);
                 tc::prefetch_tensormap(&tm_kv);

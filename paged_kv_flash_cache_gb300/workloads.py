@@ -16,6 +16,8 @@ Sources (page titles from the subject's web pages):
     [num_blocks, 2, num_heads, block_size, head_dim].
   * "企业官网建设流程全解析" (cf-1.com), section 2.1: block table maps logical block
     i // block_size to a physical block.
+  * pwwt.cn write-up on chunked attention (a 7B model 70x slower), section 5.4: prefix
+    caching -- requests sharing a prompt reuse its cached K/V pages.
 Values follow the workloads of the pages' 7B-like cases (32 heads x head_dim
 128, contexts of 4k-8k tokens, batch 16, block sizes 8-512): Q/K/V ~ N(0, 1)
 cast to fp16 or bf16.
@@ -38,10 +40,15 @@ class OutOfBlocks(RuntimeError):
 
 
 class BlockAllocator:
-    """Free-list page allocator (ipipp.com page, section 3, `PagedKVCache`).
+    """Free-list page allocator (ipipp.com page, section 3, `PagedKVCache`), with a reference
+    count per block so that several block tables can hold the same pages (prefix caching,
+    pwwt.cn write-up on chunked attention, section 5.4: requests that open with the same prompt
+    reuse its cached K/V instead of recomputing it).
 
-    `free` starts as ``list(range(num_blocks))`` unless an explicit order is
-    given (a seeded permutation spreads a sequence's pages over the pool).
+    `free` starts as ``list(range(num_blocks))`` unless an explicit order is given (a seeded
+    permutation spreads a sequence's pages over the pool). `allocate` hands out blocks with one
+    reference each; `share` adds a reference to blocks already handed out; `release` drops one
+    reference per listed block and returns a block to the free list when its count reaches 0.
     """
 
     def __init__(self, num_blocks: int, block_size: int,
@@ -53,6 +60,7 @@ class BlockAllocator:
         self.free: List[int] = list(range(num_blocks)) if free_order is None else [int(x) for x in free_order]
         if sorted(self.free) != list(range(num_blocks)):
             raise ValueError("free_order must be a permutation of range(num_blocks)")
+        self.refs: List[int] = [0] * num_blocks
 
     def blocks_needed(self, num_tokens: int) -> int:
         return (num_tokens + self.block_size - 1) // self.block_size
@@ -61,10 +69,41 @@ class BlockAllocator:
         needed = self.blocks_needed(num_tokens)
         if len(self.free) < needed:
             raise OutOfBlocks("not enough free KV cache blocks: need %d, have %d" % (needed, len(self.free)))
-        return [self.free.pop() for _ in range(needed)]
+        out = [self.free.pop() for _ in range(needed)]
+        for b in out:
+            self.refs[b] = 1
+        return out
+
+    def _counts(self, blocks: Sequence[int]) -> dict:
+        counts: dict = {}
+        for b in blocks:
+            b = int(b)
+            if not 0 <= b < self.num_blocks:
+                raise ValueError("block %d is outside the pool" % b)
+            counts[b] = counts.get(b, 0) + 1
+        return counts
+
+    def share(self, blocks: Sequence[int]) -> List[int]:
+        """One more reference to each of `blocks` (all must be allocated); returns them, for the
+        new owner's block table."""
+        counts = self._counts(blocks)
+        for b in counts:
+            if self.refs[b] == 0:
+                raise ValueError("block %d is free: only allocated blocks can be shared" % b)
+        for b, n in counts.items():
+            self.refs[b] += n
+        return [int(b) for b in blocks]
 
     def release(self, blocks: Sequence[int]) -> None:
-        self.free.extend(int(b) for b in blocks)
+        counts = self._counts(blocks)
+        for b, n in counts.items():
+            if self.refs[b] < n:
+                raise ValueError("block %d released more often than it is held" % b)
+        for b in blocks:
+            b = int(b)
+            self.refs[b] -= 1
+            if self.refs[b] == 0:
+                self.free.append(b)
 
 
 def block_table_tensor(tables: Sequence[Sequence[int]], max_blocks_per_seq: int) -> torch.Tensor:
@@ -343,6 +382,71 @@ def mixed_serving(seed: int = 1239, batch: int = 64, block_size: int = 32, pool_
                         block_size=block_size, context_lens=lens, q_lens=[1] * batch, dtype=BF16,
                         causal=False, seed=seed + 1, num_blocks=nb, tables=tables, max_blocks_per_seq=mb,
                         pool_init=pool_init, kv_data=kv_data, device=device)
+
+
+def prefix_shared(seed: int = 1240, batch: int = 16, prefix: int = 4096, lo: int = 256, hi: int = 2048,
+                  block_size: int = 16, heads: int = 32, kv_heads: Optional[int] = None, head_dim: int = 128,
+                  dtype: str = F16, prefill: bool = False, pool_init: str = "cheap", device="cpu") -> PagedProblem:
+    """Prefix caching (pwwt.cn write-up on chunked attention, section 5.4): `batch` requests open
+    with the same `prefix`-token prompt, then carry their own tokens (uniform in [lo, hi]).
+
+    The pages filled by the prompt alone (prefix // block_size of them) are allocated once and
+    shared, through the allocator's reference counts, by every request's block table; the
+    prompt's partial last page (if any) and each request's own tokens go to private pages, since
+    a request writes into them; the prompt's pages keep one reference of their own (the prefix
+    cache's) besides one per request. The pool holds the shared pages, the private pages and 10%
+    spare, handed out in a seeded random order. k_ctx / v_ctx hold every request's whole context
+    (the prompt rows identical across requests). With `prefill`, each request's queries are its
+    tokens after the shared pages (the part a prefix-cache hit still has to compute, causal);
+    otherwise one decode query per request. `shared_append` and `private_append` split the
+    context's append into the prompt's shared pages (once) and each request's own rows."""
+    kv_heads = heads if kv_heads is None else kv_heads
+    gen = torch.Generator().manual_seed(seed)
+    own = torch.randint(lo, hi + 1, (batch,), generator=gen).tolist()
+    lens = [prefix + n for n in own]
+    n_shared = prefix // block_size
+    shared_tokens = n_shared * block_size
+    private = [(L + block_size - 1) // block_size - n_shared for L in lens]
+    nb = int(math.ceil(1.1 * (n_shared + sum(private))))
+    order = torch.randperm(nb, generator=gen).tolist()
+    alloc = BlockAllocator(nb, block_size, order)
+    shared = alloc.allocate(shared_tokens)
+    tables = [alloc.share(shared) + alloc.allocate(L - shared_tokens) for L in lens]
+    dgen = data_generator(seed + 5, device)
+    k_pre = randn_t(dgen, (prefix, kv_heads, head_dim), dtype)
+    v_pre = randn_t(dgen, (prefix, kv_heads, head_dim), dtype)
+    k_parts, v_parts = [], []
+    for n in own:
+        k_parts += [k_pre, randn_t(dgen, (n, kv_heads, head_dim), dtype)]
+        v_parts += [v_pre, randn_t(dgen, (n, kv_heads, head_dim), dtype)]
+    q_lens = [L - shared_tokens for L in lens] if prefill else [1] * batch
+    mb = max(len(t) for t in tables)
+    p = make_problem("prefix_shared", batch=batch, num_q_heads=heads, num_kv_heads=kv_heads, head_dim=head_dim,
+                     block_size=block_size, context_lens=lens, q_lens=q_lens, dtype=dtype, causal=prefill,
+                     seed=seed + 1, num_blocks=nb, tables=tables, max_blocks_per_seq=mb, pool_init=pool_init,
+                     kv_data=(torch.cat(k_parts), torch.cat(v_parts)), device=device)
+    p.meta.update(prefix=prefix, shared_tokens=shared_tokens, shared_blocks=shared, allocator=alloc)
+    return p
+
+
+def shared_append(p: PagedProblem) -> dict:
+    """Append arguments that write the shared prompt pages once (request 0's first rows)."""
+    s = p.meta["shared_tokens"]
+    return dict(k_new=p.k_ctx[:s], v_new=p.v_ctx[:s], cu_new_lens=cu_lens([s]),
+                ctx_before=torch.zeros(1, dtype=torch.int32), block_tables=p.block_tables[:1].clone())
+
+
+def private_append(p: PagedProblem) -> dict:
+    """Append arguments that write every request's rows after the shared pages."""
+    s = p.meta["shared_tokens"]
+    rows, start = [], 0
+    for L in p.context_lens.tolist():
+        rows.append(torch.arange(start + s, start + L))
+        start += L
+    rows = torch.cat(rows)
+    return dict(k_new=p.k_ctx[rows].contiguous(), v_new=p.v_ctx[rows].contiguous(),
+                cu_new_lens=cu_lens([L - s for L in p.context_lens.tolist()]),
+                ctx_before=torch.full((p.batch,), s, dtype=torch.int32), block_tables=p.block_tables.clone())
 
 
 def append_step(p: PagedProblem, seed: int = 99) -> dict:

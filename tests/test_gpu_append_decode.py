@@ -181,6 +181,32 @@ def test_decode_special_cases():
     assert torch.allclose(o[2].to(torch.float64), mean_v, atol=1e-5, rtol=0)
 
 
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 4)])
+def test_decode_inputs_written_by_the_previous_kernel(hq, hkv):
+    """Lengths, block table and q produced by device kernels queued just before the decode call
+    (no synchronisation in between), after a kernel that left other values there: the decode
+    kernels start early under programmatic launch, so they must still see the final inputs."""
+    p = problem(lens=[700, 1, 2049, 130], hq=hq, hkv=hkv, bs=16, dtype=W.F16, seed=hq)
+    cache = device_cache(p)
+    ref, _ = oracle.attention_of(p, cache_bits(cache))
+    lens_true, bt_true, q_true = to_dev(p.context_lens), to_dev(p.block_tables), to_dev(p.q)
+    lens, bt, q = torch.empty_like(lens_true), torch.empty_like(bt_true), torch.empty_like(q_true)
+    busy = torch.empty(1 << 26, dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    for _ in range(3):
+        lens.fill_(3)
+        bt.fill_(0)
+        q.fill_(0.5)
+        busy.fill_(1.0)                                   # a long kernel ahead of the writers
+        torch.add(lens_true, 0, out=lens)
+        torch.add(bt_true, 0, out=bt)
+        torch.mul(q_true, 1, out=q)
+        out = pkv.paged_attn_decode(cache, q, bt, lens, scale=p.scale)
+        torch.cuda.synchronize()
+        assert pkv.get_device_error() == 0
+        check_close(out, ref, "f16", roundings=1 + p_roundings(p), what="inputs from kernels hq=%d" % hq)
+
+
 def test_decode_bad_page_flags_error():
     p = problem(lens=[200, 50], hq=4, hkv=4, bs=16)
     cache = device_cache(p)

@@ -76,6 +76,31 @@ def test_prefill_dtypes_gqa_causality(dtype, causal, hq, hkv, d):
     check(p, cache, out, lse, roundings=2, what="%s causal=%s hq=%d hkv=%d d=%d" % (dtype, causal, hq, hkv, d))
 
 
+def test_prefill_inputs_written_by_the_previous_kernel():
+    """Query offsets, lengths, block table and q produced by device kernels queued just before
+    the prefill call, with no synchronisation in between (the kernel starts early under
+    programmatic launch and must still see them)."""
+    p = problem(lens=[520, 77, 1000], q_lens=[200, 77, 384], hq=8, hkv=8, bs=16, seed=21)
+    cache = device_cache(p)
+    ref, _ = oracle.attention_of(p, cache_bits(cache))
+    srcs = [to_dev(t) for t in (p.cu_q_lens, p.context_lens, p.block_tables, p.q)]
+    dsts = [torch.empty_like(t) for t in srcs]
+    busy = torch.empty(1 << 26, dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for t in dsts:
+            t.fill_(1)
+        busy.fill_(1.0)
+        for src, dst in zip(srcs, dsts):
+            torch.add(src, 0, out=dst)
+        cu, ctx, bt, q = dsts
+        out = pkv.paged_attn_prefill(cache, q, cu, ctx, bt, max_q_len=int(p.q_lens.max()), scale=p.scale,
+                                     causal=True)
+        torch.cuda.synchronize()
+        assert pkv.get_device_error() == 0
+        check_close(out, ref, p.dtype, roundings=2, what="prefill inputs from kernels")
+
+
 def test_prefill_fp32_output_single_rounding():
     p = problem(lens=[640, 333], q_lens=[512, 333], hq=4, hkv=4, dtype=W.BF16, bs=32, seed=3)
     cache = device_cache(p)

@@ -418,3 +418,75 @@ def test_mixed_serving_pool_is_fragmented_and_disjoint():
     m = (bt[:, 1:] >= 0) & (bt[:, :-1] >= 0)
     adj = ((bt[:, 1:] - bt[:, :-1]).abs() == 1) & m
     assert adj.sum().item() < 0.05 * m.sum().item()
+
+
+# ----------------------------------------------------------------------------------------------
+# prefix caching: reference-counted pages shared by several block tables (pwwt.cn write-up on
+# chunked attention, section 5.4)
+# ----------------------------------------------------------------------------------------------
+
+def test_allocator_reference_counts():
+    a = W.BlockAllocator(6, 16)
+    pre = a.allocate(32)                          # [5, 4], one reference each
+    t1 = a.share(pre) + a.allocate(10)
+    t2 = a.share(pre) + a.allocate(20)
+    assert t1[:2] == t2[:2] == pre and a.refs[5] == a.refs[4] == 3
+    a.release(t1)                                 # private page freed, shared pages still held
+    assert a.free == [0, t1[2]] and a.refs[5] == 2
+    a.release(pre)
+    a.release(t2)                                 # last holder: pages return in release order
+    assert sorted(a.free) == list(range(6)) and a.free[-4:] == t2 and a.refs == [0] * 6
+    with pytest.raises(ValueError):
+        a.release([3])                            # not held
+    with pytest.raises(ValueError):
+        a.share([3])                              # free blocks cannot be shared
+    b = a.allocate(16)
+    with pytest.raises(ValueError):
+        a.release(b + b)                          # released twice in one call, held once
+    assert a.refs[b[0]] == 1                      # a rejected release changes nothing
+
+
+def test_prefix_workload_tables_share_exactly_the_prompt_pages():
+    p = W.prefix_shared(batch=5, prefix=100, lo=3, hi=60, block_size=16, heads=2, head_dim=32, pool_init="none")
+    s = p.meta["shared_tokens"]
+    assert s == 96
+    shared = p.meta["shared_blocks"]
+    bt = p.block_tables
+    for b in range(p.batch):
+        assert bt[b, :6].tolist() == shared
+    private = [x for x in bt[:, 6:].flatten().tolist() if x >= 0]
+    assert len(set(private)) == len(private) and not set(private) & set(shared)
+    refs = p.meta["allocator"].refs
+    assert all(refs[x] == p.batch + 1 for x in shared) and all(refs[x] == 1 for x in private)
+    # the prompt's rows are identical in every request's context
+    cu = p.cu_ctx_lens.tolist()
+    for b in range(1, p.batch):
+        assert torch.equal(p.k_ctx[cu[b]:cu[b] + 100], p.k_ctx[:100])
+        assert torch.equal(p.v_ctx[cu[b]:cu[b] + 100], p.v_ctx[:100])
+
+
+def test_prefix_appends_once_equal_every_context_appended():
+    """Writing the shared pages once plus each request's own rows gives the pool that appending
+    every request's whole context gives (the shared pages then receive identical rows)."""
+    p = W.prefix_shared(batch=4, prefix=70, lo=1, hi=50, block_size=16, heads=2, head_dim=32)
+    whole = oracle.build_cache(p)
+    cache = oracle.empty_cache_bits(p)
+    for args in (W.shared_append(p), W.private_append(p)):
+        assert oracle.kv_cache_append(cache, **args) == 0
+    assert np.array_equal(cache, whole)
+
+
+@pytest.mark.parametrize("prefill", [False, True])
+def test_shared_pages_equal_private_copies_bit_identical(prefill):
+    """Attention over tables that alias the prompt's pages equals attention over tables that give
+    every request its own copy of them (the oracle reads a page by id; aliasing is invisible)."""
+    p = W.prefix_shared(batch=3, prefix=50, lo=1, hi=40, block_size=8, heads=4, kv_heads=2, head_dim=32,
+                        prefill=prefill)
+    got, got_lse = oracle.attention_of(p, oracle.build_cache(p))
+    lens = p.context_lens.tolist()
+    copy = W.make_problem("unshared", batch=p.batch, num_q_heads=4, num_kv_heads=2, head_dim=32, block_size=8,
+                          context_lens=lens, q_lens=p.q_lens.tolist(), dtype=p.dtype, causal=p.causal, seed=3,
+                          kv_data=(p.k_ctx, p.v_ctx))
+    ref, ref_lse = oracle.attention_of(copy, oracle.build_cache(copy), q=p.q)
+    assert copy.block_tables.unique().numel() > p.block_tables.unique().numel()
+    assert np.array_equal(got, ref) and np.array_equal(got_lse, ref_lse)

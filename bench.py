@@ -46,7 +46,7 @@ def parse():
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="", help="comma list of extra workloads (bs_sweep,mixed,prefix,prefill)")
-    ap.add_argument("--profile", choices=["decode", "append", "prefill", "decode_mixed"], default=None,
+    ap.add_argument("--profile", choices=["decode", "append", "prefill", "decode_mixed", "decode_prefix"], default=None,
                     help="small case for ncu captures: W + K launches of one kernel, nothing else timed")
     return ap.parse_args()
 
@@ -83,6 +83,19 @@ def profile_case(args):
                             torch.zeros(p.batch, dtype=torch.int32, device="cuda"), bt)
         q, ctx = p.q.cuda(), p.context_lens.cuda()
         out = torch.empty((p.batch, 32, 128), dtype=torch.bfloat16, device="cuda")
+        for _ in range(args.warmup + args.steps):
+            pkv.paged_attn_decode(cache, q, bt, ctx, scale=p.scale, out=out)
+        torch.cuda.synchronize()
+        assert pkv.get_device_error() == 0
+    elif args.profile == "decode_prefix":
+        # the shared-prompt decode batch itself: 0.37 GB of unique K/V, 1.38 GB read per call
+        p = W.prefix_shared(pool_init="none", device="cuda")
+        cache = torch.zeros((p.num_blocks, 2, 32, 16, 128), dtype=torch.float16, device="cuda")
+        for ap_ in (W.shared_append(p), W.private_append(p)):
+            pkv.kv_cache_append(cache, ap_["k_new"].cuda(), ap_["v_new"].cuda(), ap_["cu_new_lens"].cuda(),
+                                ap_["ctx_before"].cuda(), ap_["block_tables"].cuda())
+        q, ctx, bt = p.q.cuda(), p.context_lens.cuda(), p.block_tables.cuda()
+        out = torch.empty((p.batch, 32, 128), dtype=torch.float16, device="cuda")
         for _ in range(args.warmup + args.steps):
             pkv.paged_attn_decode(cache, q, bt, ctx, scale=p.scale, out=out)
         torch.cuda.synchronize()

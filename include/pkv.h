@@ -107,7 +107,8 @@ PKV_API size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_
                                  int block_size, int max_blocks_per_seq, int num_splits);
 
 /* Tokens per split that pkv_paged_attn_decode uses for these sizes (a multiple of
- * its 64-token tile); a context of L tokens is cut into ceil(L / chunk) splits. */
+ * its 64-token tile, and at least capacity / 2048 so that a context has at most 2048
+ * splits); a context of L tokens is cut into ceil(L / chunk) splits. */
 PKV_API int pkv_decode_split_tokens(int batch, int num_q_heads, int num_kv_heads, int head_dim,
                             int block_size, int max_blocks_per_seq, int num_splits);
 

@@ -9,20 +9,23 @@
 // small batch still fills every SM (parallelism over key/value blocks, "从一次压测翻车说起",
 // sections 3.3 and 5.3); split results are merged by their log-sum-exp instead of atomics.
 //
-// Kernel structure (one persistent CTA per SM slot):
+// Kernel structure (one persistent CTA per SM):
 //   * work unit = (sequence, KV head, split); units are numbered in a prologue from the
-//     context lengths (block-wide scan) and dealt round-robin to the CTAs, so concurrent CTAs
-//     stream neighbouring head slices of the same pages;
-//   * warp 4 (producer) streams each unit's tokens in 64-token tiles into a ring of
+//     context lengths (decode_common.cuh: split-major, all KV heads of a sequence together)
+//     and dealt round-robin to the CTAs;
+//   * warp 8 (producer) streams each unit's tokens in 64-token tiles into a ring of
 //     shared-memory stages with bulk copies (TMA engine, one copy per page slice of K and of
-//     V -- pages are contiguous [block_size, D] rows), completion on an mbarrier;
-//   * warps 0-3 (consumers) each take 16 tokens of a tile: lanes split D into 16-byte
+//     V -- pages are contiguous [block_size, D] rows), completion on an mbarrier; page ids
+//     are read one unit ahead;
+//   * warps 0-7 (consumers) each take 8 tokens of a tile: lanes split D into 16-byte
 //     chunks, q.k partial sums are reduced with xor shuffles, and every lane keeps running
-//     (m, l, acc) for all query heads of the GQA group, so each K/V byte is read from HBM
-//     exactly once per KV head;
-//   * at the end of a unit the states are merged (shuffles within a warp, shared memory
-//     across warps): a single-split context writes the final output, otherwise the split's
-//     normalised output and lse go to the workspace for the merge kernel.
+//     (m, l, acc) for the query heads of its KV head, so each K/V byte is read from HBM once
+//     per KV head;
+//   * at the end of a unit each consumer warp merges its token slots by shuffles and leaves
+//     its (m, l, acc) rows in one of two shared-memory merge buffers; warp 9 (merger) combines
+//     the eight warps' rows while the consumers go on with the next unit. A single-split
+//     context gets its final output there, otherwise the split's normalised output and lse go
+//     to the workspace for the merge kernel.
 #include <type_traits>
 
 #include "decode_common.cuh"
@@ -33,9 +36,11 @@ namespace pkv {
 namespace {
 
 constexpr int kConsumerWarps = 8;
-constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kMergeWarp = kConsumerWarps + 1;
+constexpr int kDecodeThreads = (kConsumerWarps + 2) * 32;
 constexpr int kStages = 4;
-constexpr int kMaxBatch = 2048;  // context lengths + unit prefix kept in shared memory
+constexpr int kMaxBatch = 2048;  // unit tables (lengths, order, split offsets) kept in shared memory
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (log2 units)
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -57,15 +62,17 @@ struct DecodeLayout {
     static constexpr size_t kStageBytes = ((2 * kKBytes + kQBytes) + 127) / 128 * 128;
     static constexpr size_t kMergeFloats = (size_t)kConsumerWarps * G * (D + 2);
     static constexpr size_t kBarOffset = kStages * kStageBytes;
-    static constexpr size_t kMergeOffset = kBarOffset + 2 * kStages * 8 + 32;  // + abort flag, unit ids
+    // barriers: full / empty per stage, merge full / empty per merge buffer; then the abort flag
+    // (padded to 16 bytes), the unit of each stage and the unit of each merge buffer
+    static constexpr size_t kMergeOffset = kBarOffset + (2 * kStages + 4) * 8 + 64;
     // grouped heads (G > 1): a batch of kGqaSteps steps gives each lane of a token group one
     // (token, head) score after a reduce-scatter, i.e. kGqaSteps * G <= kLanesPerTok values
     static constexpr int kGqaSteps = (kSteps * G <= kLanesPerTok) ? kSteps : (kLanesPerTok / G);
     static constexpr int kGqaN = kGqaSteps * G;
-    static constexpr size_t kPOffset = kMergeOffset + kMergeFloats * 4;     // per-warp p broadcast buffer
+    static constexpr size_t kPOffset = kMergeOffset + 2 * kMergeFloats * 4;  // per-warp p broadcast buffer
     static constexpr size_t kPFloats = (size_t)kConsumerWarps * kTokPerStep * kGqaN;
     static constexpr size_t kIntsOffset = kPOffset + kPFloats * 4;
-    static size_t smem_bytes(int batch) { return kIntsOffset + (size_t)(2 * batch + 2 + 64) * 4; }
+    static size_t smem_bytes(int batch, int s_max) { return kIntsOffset + unit_table_ints(batch, s_max) * 4; }
 };
 
 template <typename Tag, int D, int G>
@@ -74,21 +81,25 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kBarOffset);
     uint64_t *empty = full + kStages;
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + kStages);
-    int *stage_unit = reinterpret_cast<int *>(empty + kStages) + 4;  // [kStages] unit of each filled stage, -1: end
-    float *merge = reinterpret_cast<float *>(smem + L::kMergeOffset);
-    int *lens = reinterpret_cast<int *>(smem + L::kIntsOffset);
-    int *prefix = lens + a.batch;          // [batch + 1]
-    int *scan_tmp = prefix + a.batch + 1;  // [kDecodeThreads / 32]
+    uint64_t *mfull = empty + kStages;   // [2] the consumer warps' rows of a unit are in buffer i
+    uint64_t *mempty = mfull + 2;        // [2] the merger has read buffer i
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(mempty + 2);
+    int *stage_unit = reinterpret_cast<int *>(mempty + 2) + 4;  // [kStages] unit of each filled stage, -1: end
+    int *merge_unit = stage_unit + kStages;                     // [2] unit of each merge buffer, -1: end
+    float *merge = reinterpret_cast<float *>(smem + L::kMergeOffset);  // [2][kConsumerWarps][G][D + 2]
+    const UnitTable ut = unit_table(reinterpret_cast<int *>(smem + L::kIntsOffset), a.batch, a.s_max);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int hkv = a.cache.num_kv_heads, bs = a.cache.block_size, chunk = a.chunk;
-    const int cap = a.max_blocks_per_seq * bs;
 
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kConsumerWarps);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&mfull[i], kConsumerWarps);
+            mbar_init(&mempty[i], 1);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -97,10 +108,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
     // q, the cache), so only the barrier set-up above overlaps that kernel's tail.
     pdl_wait();
     // ---- prologue: clamp lengths, units per sequence, exclusive scan (all threads) ----
-    decode_scan_units<kDecodeThreads>(a, lens, prefix, scan_tmp);
-    const int num_units = prefix[a.batch];
+    const int num_units = decode_scan_units<kDecodeThreads>(a, ut);
 
-    if (warp == kConsumerWarps) {
+    if (warp == kProducerWarp) {
         // ================================ producer warp ================================
         const uint64_t pol = l2_policy_evict_first();
         const uint16_t *cache = static_cast<const uint16_t *>(a.cache.ptr);
@@ -110,18 +120,32 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
         uint32_t phase = 0;
         uint32_t issued_mask = 0;  // stages with copies issued (bit i), for the abort drain
         uint32_t issued_parity = 0;
+        UnitCursor c = {};
+        PageWindow win = {};
+        if ((int)blockIdx.x < num_units) {
+            c = unit_of(blockIdx.x, ut, a.s_max, hkv, chunk);
+            win = unit_pages(a, c, lane);
+        }
         for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
-            const UnitCursor c = unit_of(u, prefix, lens, a.batch, hkv, chunk);
+            // the next unit's cursor and page ids, loading while this unit's copies go out
+            UnitCursor cn = c;
+            PageWindow wn = win;
+            if (u + (int)gridDim.x < num_units) {
+                cn = unit_of(u + gridDim.x, ut, a.s_max, hkv, chunk);
+                wn = unit_pages(a, cn, lane);
+            }
             const int *bt = a.block_tables + (size_t)c.b * a.max_blocks_per_seq;
+            const int unit_last_page = (c.t1 - 1) >> a.cache.log2_block_size;
             for (int ts = c.t0; ts < c.t1; ts += L::kTile) {
                 const int n = min(L::kTile, c.t1 - ts);
                 const int first_page = ts >> a.cache.log2_block_size;
                 const int last_page = (ts + n - 1) >> a.cache.log2_block_size;
                 const int npages = last_page - first_page + 1;  // <= 64/bs, or 1
-                // page id of this lane's slice, fetched before waiting for the stage
-                int pb = 0;
+                if (last_page >= win.first + win.count)         // units of more than 64 pages
+                    win = load_pages(bt, first_page, unit_last_page - first_page + 1, lane);
+                // page id of this lane's slice
+                int pb = window_page(win, first_page + lane);
                 if (lane < npages) {
-                    pb = __ldg(bt + first_page + lane);
                     if (pb < 0 || pb >= a.cache.num_blocks) {
                         set_error(a.err, kErrDeviceRange);
                         pb = 0;
@@ -169,12 +193,76 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
                     phase ^= 1u;
                 }
             }
+            c = cn;
+            win = wn;
         }
         // end marker: one more stage carrying unit id -1
         if (mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.err) && lane == 0) {
             stage_unit[stage] = -1;
             mbar_arrive(&full[stage]);
         }
+        return;
+    }
+
+    if (warp == kMergeWarp) {
+        // ================================= merge warp =================================
+        // Combines the consumer warps' (m, l, acc) rows of a unit: lane w < 8 takes warp w's
+        // (m, l), M and the weighted sum of l are reduced over the whole warp, the weights
+        // exp2(m_w - M) go to every lane by shuffles, and lane j sums the rows' elements
+        // j, j + 32, ...
+        int mbuf = 0;
+        uint32_t mphase = 0;
+        for (;;) {
+            if (!mbar_wait(&mfull[mbuf], mphase, abort_flag, a.err)) return;
+            const int u = merge_unit[mbuf];
+            if (u < 0) break;
+            const UnitCursor c = unit_of(u, ut, a.s_max, hkv, chunk);
+            const float *rows = merge + (size_t)mbuf * L::kMergeFloats;
+            const int splits = (ut.lens[c.b] + chunk - 1) / chunk;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float *rg = rows + (size_t)g * (D + 2);  // warp w's row: rg + w * G * (D + 2)
+                const float mw = lane < kConsumerWarps ? rg[(size_t)lane * G * (D + 2) + D] : -INFINITY;
+                const float lw = lane < kConsumerWarps ? rg[(size_t)lane * G * (D + 2) + D + 1] : 0.f;
+                float M = mw;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+                const float wgt = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+                float lsum = lw * wgt;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+                float wv[kConsumerWarps];
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) wv[w] = __shfl_sync(0xffffffffu, wgt, w);
+                const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+                const int h = c.kvh * G + g;
+                const size_t row_id = (size_t)c.b * a.num_q_heads + h;
+#pragma unroll
+                for (int d = lane; d < D; d += 32) {
+                    float o = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kConsumerWarps; ++w) o += rg[(size_t)w * G * (D + 2) + d] * wv[w];
+                    const float res = o * inv;
+                    if (splits == 1) store_out(a.out, row_id * D + d, res, a.out_dtype);
+                    else a.part_o[(row_id * a.s_max + c.split) * D + d] = res;
+                }
+                if (lane == 0) {
+                    const float lse_v = lsum > 0.f ? (M + log2f(lsum)) * kLn2 : -INFINITY;
+                    if (splits == 1) {
+                        if (a.lse) a.lse[row_id] = lse_v;
+                    } else {
+                        a.part_lse[row_id * a.s_max + c.split] = lse_v;
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&mempty[mbuf]);
+            if (++mbuf == 2) {
+                mbuf = 0;
+                mphase ^= 1u;
+            }
+        }
+        pdl_launch_dependents();
         return;
     }
 
@@ -195,12 +283,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
     (void)group_base; (void)g_own; (void)pbuf;
     int stage = 0;
     uint32_t phase = 0;
+    int mbuf = 0;           // merge buffer of the next unit
+    uint32_t mphase = 0;
     for (;;) {
         // the unit of the next stage (or the end marker) is known once that stage is full
         if (!mbar_wait(&full[stage], phase, abort_flag, a.err)) return;
         const int u = stage_unit[stage];
         if (u < 0) break;
-        const UnitCursor c = unit_of(u, prefix, lens, a.batch, hkv, chunk);
+        const UnitCursor c = unit_of(u, ut, a.s_max, hkv, chunk);
         float l_own = 0.f;                     // grouped heads: this lane's share of its head's sum
         (void)l_own;
         float m[G], l[G];
@@ -421,11 +511,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
                 m[g] = mn;
             }
         }
-        // ---- merge across the consumer warps through shared memory ----
+        // ---- hand this warp's rows to the merge warp ----
+        if (!mbar_wait(&mempty[mbuf], mphase ^ 1u, abort_flag, a.err)) return;
+        float *rows = merge + (size_t)mbuf * L::kMergeFloats;
         if (slot == 0) {
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                float *row = merge + ((size_t)warp * G + g) * (D + 2);
+                float *row = rows + ((size_t)warp * G + g) * (D + 2);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     row[chk * 8 + 2 * j] = acc[g][j].x;
@@ -437,36 +529,19 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
                 }
             }
         }
-        named_barrier(1, kConsumerWarps * 32);
-        const int splits = (lens[c.b] + chunk - 1) / chunk;
-        for (int idx = tid; idx < G * D; idx += kConsumerWarps * 32) {
-            const int g = idx / D, d = idx - (idx / D) * D;
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, merge[((size_t)w * G + g) * (D + 2) + D]);
-            float lsum = 0.f, o = 0.f;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const float *row = merge + ((size_t)w * G + g) * (D + 2);
-                const float mw = row[D];
-                const float wgt = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
-                lsum += row[D + 1] * wgt;
-                o += row[d] * wgt;
-            }
-            const float res = lsum > 0.f ? o / lsum : 0.f;
-            const float lse_v = lsum > 0.f ? (M + log2f(lsum)) * kLn2 : -INFINITY;
-            const int h = c.kvh * G + g;
-            const size_t row_id = (size_t)c.b * a.num_q_heads + h;
-            if (splits == 1) {
-                store_out(a.out, row_id * D + d, res, a.out_dtype);
-                if (d == 0 && a.lse) a.lse[row_id] = lse_v;
-            } else {
-                const size_t pr = row_id * a.s_max + c.split;
-                a.part_o[pr * D + d] = res;
-                if (d == 0) a.part_lse[pr] = lse_v;
-            }
+        if (warp == 0 && lane == 0) merge_unit[mbuf] = u;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&mfull[mbuf]);
+        if (++mbuf == 2) {
+            mbuf = 0;
+            mphase ^= 1u;
         }
-        named_barrier(1, kConsumerWarps * 32);
+    }
+    // end marker for the merge warp
+    if (mbar_wait(&mempty[mbuf], mphase ^ 1u, abort_flag, a.err)) {
+        if (warp == 0 && lane == 0) merge_unit[mbuf] = -1;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&mfull[mbuf]);
     }
     pdl_launch_dependents();
 }
@@ -529,13 +604,13 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
 
 template <typename Tag, int D, int G>
 cudaError_t launch_decode_t(const DecodeArgs &a, int grid, cudaStream_t s) {
-    const size_t smem = DecodeLayout<D, G>::smem_bytes(a.batch);
+    const size_t smem = DecodeLayout<D, G>::smem_bytes(a.batch, a.s_max);
     auto kern = decode_split_kernel<Tag, D, G>;
     // opt in to the largest size this kernel can ask for, once per device
     static unsigned int configured = 0;
     const int dev = device_info().device;
     if (dev < 32 && !(configured & (1u << dev))) {
-        const int max_smem = (int)DecodeLayout<D, G>::smem_bytes(kMaxBatch);
+        const int max_smem = (int)DecodeLayout<D, G>::smem_bytes(kMaxBatch, kDecodeMaxSplits);
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
         if (e != cudaSuccess) return e;
         configured |= 1u << dev;
@@ -551,41 +626,13 @@ cudaError_t dispatch_group(const DecodeArgs &a, int grid, cudaStream_t s) {
     switch (a.num_q_heads / a.cache.num_kv_heads) {
         case 1: return launch_decode_t<Tag, D, 1>(a, grid, s);
         case 2: return launch_decode_t<Tag, D, 2>(a, grid, s);
-        case 4: return launch_decode_t<Tag, D, 4>(a, grid, s);
-        case 8: return launch_decode_t<Tag, D, 8>(a, grid, s);
-        default: return cudaErrorInvalidValue;
+        default: return cudaErrorInvalidValue;  // four or more heads per KV head: decode_gqa.cu
     }
 }
 
 }  // namespace
 
 int decode_max_batch() { return kMaxBatch; }
-
-size_t decode_smem_bytes(int head_dim, int group, int batch) {
-    auto pick = [&](auto d_tag, auto g_tag) {
-        return DecodeLayout<decltype(d_tag)::value, decltype(g_tag)::value>::smem_bytes(batch);
-    };
-    using I64 = std::integral_constant<int, 64>;
-    using I128 = std::integral_constant<int, 128>;
-    using G1 = std::integral_constant<int, 1>;
-    using G2 = std::integral_constant<int, 2>;
-    using G4 = std::integral_constant<int, 4>;
-    using G8 = std::integral_constant<int, 8>;
-    if (head_dim == 64) {
-        switch (group) {
-            case 1: return pick(I64(), G1());
-            case 2: return pick(I64(), G2());
-            case 4: return pick(I64(), G4());
-            default: return pick(I64(), G8());
-        }
-    }
-    switch (group) {
-        case 1: return pick(I128(), G1());
-        case 2: return pick(I128(), G2());
-        case 4: return pick(I128(), G4());
-        default: return pick(I128(), G8());
-    }
-}
 
 int decode_ctas_per_sm(int head_dim, int group, int dtype) {
     (void)head_dim; (void)group; (void)dtype;

@@ -1,5 +1,14 @@
-// decode_common.cuh -- pieces shared by the split-KV decode kernels: the work-unit cursor and
-// the prologue that numbers the units from the context lengths.
+// decode_common.cuh -- pieces shared by the split-KV decode kernels: the work-unit numbering
+// built in each CTA's prologue from the context lengths, and the cursor it gives for a unit.
+//
+// A unit is (sequence, KV head, split of `chunk` tokens). Units are numbered split-major: every
+// unit of split 0, then of split 1, ...; inside a split by sequence (in order of decreasing split
+// count, so split s is held by the first n_s sequences of that order, ties by index), then by KV
+// head. Units are dealt round-robin, so the CTAs running at one time read the same token range
+// of a few sequences, all KV heads of each: the heads of one page are one contiguous run of
+// memory, and where block tables share pages (requests that open with the same cached prompt)
+// the sequences read each shared page within a few microseconds of each other, the later reads
+// from L2. Every CTA builds the same numbering: no step of it depends on thread timing.
 #pragma once
 
 #include "pkv_device.cuh"
@@ -11,64 +20,146 @@ struct UnitCursor {
     int b, kvh, split, t0, t1;
 };
 
-// Unit u -> (b, kv head, split); prefix[b] = units of sequences < b, units ordered with the KV
-// head fastest so consecutive CTAs share block-table rows.
-__device__ __forceinline__ UnitCursor unit_of(int u, const int *prefix, const int *lens, int batch, int hkv,
-                                              int chunk) {
-    int lo = 0, hi = batch;
+// Shared-memory tables of the numbering (all int):
+//   lens  [batch]      context lengths clamped to the table's capacity
+//   ord   [batch]      sequences by decreasing split count, ties by index
+//   first [s_max + 1]  first[s] = sum over sequences of min(splits, s); split s's units start at
+//                      first[s] * hkv and number n_s * hkv, n_s = first[s + 1] - first[s]
+//   hist  [s_max + 1]  prologue scratch: sequences per split count, then a fill count
+struct UnitTable {
+    int *lens, *ord, *first, *hist;
+};
+
+__host__ __device__ constexpr size_t unit_table_ints(int batch, int s_max) {
+    return 2 * (size_t)batch + 2 * ((size_t)s_max + 1);
+}
+
+__device__ __forceinline__ UnitTable unit_table(int *ints, int batch, int s_max) {
+    UnitTable t;
+    t.lens = ints;
+    t.ord = ints + batch;
+    t.first = ints + 2 * batch;
+    t.hist = t.first + s_max + 1;
+    return t;
+}
+
+__device__ __forceinline__ UnitCursor unit_of(int u, const UnitTable &t, int s_max, int hkv, int chunk) {
+    int lo = 0, hi = s_max;  // the split: last s with first[s] * hkv <= u
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (prefix[mid] <= u) lo = mid; else hi = mid;
+        if (t.first[mid] * hkv <= u) lo = mid; else hi = mid;
     }
+    const int r = u - t.first[lo] * hkv;  // < n_lo * hkv
+    const int rank = r / hkv;
     UnitCursor c;
-    c.b = lo;
-    const int r = u - prefix[lo];
-    c.kvh = r % hkv;
-    c.split = r / hkv;
-    c.t0 = c.split * chunk;
+    c.split = lo;
+    c.kvh = r - rank * hkv;
+    c.b = t.ord[rank];
+    c.t0 = lo * chunk;
     const int end = c.t0 + chunk;
-    c.t1 = end < lens[lo] ? end : lens[lo];
+    const int len = t.lens[c.b];
+    c.t1 = end < len ? end : len;
     return c;
 }
 
-// Clamp the context lengths into shared memory (flagging out-of-range ones), and write the
-// exclusive prefix of units per sequence (ceil(len / chunk) splits x KV heads) to prefix[0..batch];
-// prefix[batch] is the total. All kThreads threads of the CTA take part; ends with __syncthreads.
+// Page ids of up to 64 consecutive logical pages of one block-table row, two per lane of the
+// producer warp (lane j holds pages first + j and first + 32 + j). The producer loads a unit's
+// window one unit ahead, so the table read's latency is not on the path that issues the unit's
+// copies; units of more than 64 pages load further windows as they go.
+struct PageWindow {
+    int first, count, p0, p1;
+};
+
+__device__ __forceinline__ PageWindow load_pages(const int *bt_row, int first, int count, int lane) {
+    PageWindow w;
+    w.first = first;
+    w.count = count < 64 ? count : 64;
+    w.p0 = lane < w.count ? __ldg(bt_row + first + lane) : 0;
+    w.p1 = lane + 32 < w.count ? __ldg(bt_row + first + 32 + lane) : 0;
+    return w;
+}
+
+// The first window of unit c (its pages from c.t0's page on).
+__device__ __forceinline__ PageWindow unit_pages(const DecodeArgs &a, const UnitCursor &c, int lane) {
+    const int *bt_row = a.block_tables + (size_t)c.b * a.max_blocks_per_seq;
+    const int f = c.t0 >> a.cache.log2_block_size;
+    const int l = (c.t1 - 1) >> a.cache.log2_block_size;
+    return load_pages(bt_row, f, l - f + 1, lane);
+}
+
+// Page id of logical page `page` (inside the window) for the calling lane; all 32 lanes call,
+// lanes whose page lies outside the window get an unspecified id they must not use.
+__device__ __forceinline__ int window_page(const PageWindow &w, int page) {
+    int rel = page - w.first;
+    rel = rel < 0 ? 0 : (rel > 63 ? 63 : rel);
+    const int lo = __shfl_sync(0xffffffffu, w.p0, rel & 31);
+    const int hi = __shfl_sync(0xffffffffu, w.p1, rel & 31);
+    return rel < 32 ? lo : hi;
+}
+
+// Prologue run by all kThreads threads of a CTA: clamp the lengths (flagging out-of-range ones)
+// and build the tables above. Returns the number of units; ends with __syncthreads.
 template <int kThreads>
-__device__ __forceinline__ void decode_scan_units(const DecodeArgs &a, int *lens, int *prefix, int *scan_tmp) {
-    constexpr int kDecodeThreads = kThreads;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int hkv = a.cache.num_kv_heads, chunk = a.chunk;
+__device__ __forceinline__ int decode_scan_units(const DecodeArgs &a, const UnitTable &t) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int chunk = a.chunk, S = a.s_max;
     const int cap = a.max_blocks_per_seq * a.cache.block_size;
-    const int per = (a.batch + kDecodeThreads - 1) / kDecodeThreads;
-    const int i0 = tid * per;
-    int local = 0;
-    for (int i = i0; i < i0 + per && i < a.batch; ++i) {
+    for (int s = tid; s <= S; s += kThreads) t.hist[s] = 0;
+    __syncthreads();
+    for (int i = tid; i < a.batch; i += kThreads) {
         int len = __ldg(a.context_lens + i);
         if (len < 0 || len > cap) {
             set_error(a.err, kErrDeviceRange);
             len = len < 0 ? 0 : cap;
         }
-        lens[i] = len;
-        local += ((len + chunk - 1) / chunk) * hkv;
+        t.lens[i] = len;
+        atomicAdd(&t.hist[(len + chunk - 1) / chunk], 1);  // split count <= S since len <= cap
     }
-    int incl = local;
+    __syncthreads();
+    if (tid < 32) {
+        // n_s = batch - (sequences with at most s splits); first[s + 1] = first[s] + n_s
+        int below = 0, run = 0;
+        for (int s0 = 0; s0 < S; s0 += 32) {
+            const int s = s0 + lane;
+            int h = s < S ? t.hist[s] : 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, h, o);
+                if (lane >= o) h += y;
+            }
+            int n = s < S ? a.batch - (below + h) : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, n, o);
+                if (lane >= o) n += y;
+            }
+            if (s < S) t.first[s + 1] = run + n;
+            below += __shfl_sync(0xffffffffu, h, 31);
+            run += __shfl_sync(0xffffffffu, n, 31);
+        }
+        if (lane == 0) t.first[0] = 0;
+        __syncwarp();
+        // Stable placement, 32 sequences at a time in index order: a sequence with k splits goes
+        // after the sequences with more than k splits and after those with k splits and a lower
+        // index (hist[k] now counts those already placed).
+        for (int s = lane; s <= S; s += 32) t.hist[s] = 0;
+        __syncwarp();
+        for (int i0 = 0; i0 < a.batch; i0 += 32) {
+            const int i = i0 + lane;
+            const int k = i < a.batch ? (t.lens[i] + chunk - 1) / chunk : -1;
+            const unsigned same = __match_any_sync(0xffffffffu, k);
+            const int rank = __popc(same & ((1u << lane) - 1u));
+            if (i < a.batch) {
+                const int above = k < S ? t.first[k + 1] - t.first[k] : 0;
+                t.ord[above + t.hist[k] + rank] = i;
+            }
+            __syncwarp();
+            if (i < a.batch && rank == __popc(same) - 1) t.hist[k] += __popc(same);
+            __syncwarp();
+        }
     }
-    if (lane == 31) scan_tmp[warp] = incl;
     __syncthreads();
-    int warp_base = 0;
-    for (int w = 0; w < warp; ++w) warp_base += scan_tmp[w];
-    int run = warp_base + incl - local;
-    for (int i = i0; i < i0 + per && i < a.batch; ++i) {
-        prefix[i] = run;
-        run += ((lens[i] + chunk - 1) / chunk) * hkv;
-    }
-    if (tid == kDecodeThreads - 1) prefix[a.batch] = warp_base + incl;
-    __syncthreads();
+    return t.first[S] * a.cache.num_kv_heads;
 }
 
 }  // namespace pkv

@@ -52,8 +52,8 @@ struct GqaLayout {
     static constexpr uint32_t kMergeOffset = kBarOffset + 2 * kStagesG * 8 + 32;  // + abort flag, unit ids
     static constexpr uint32_t kMergeFloats = kWarps * G * (D + 2);
     static constexpr uint32_t kIntsOffset = kMergeOffset + kMergeFloats * 4;
-    __host__ __device__ static size_t smem_bytes(int batch) {
-        return kIntsOffset + (size_t)(2 * batch + 2 + 64) * 4 + 1024;  // + 1024-byte alignment slack
+    __host__ __device__ static size_t smem_bytes(int batch, int s_max) {
+        return kIntsOffset + unit_table_ints(batch, s_max) * 4 + 1024;  // + 1024-byte alignment slack
     }
 };
 
@@ -125,9 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + kStagesG);
     int *stage_unit = reinterpret_cast<int *>(empty + kStagesG) + 4;
     float *merge = reinterpret_cast<float *>(smem + L::kMergeOffset);
-    int *lens = reinterpret_cast<int *>(smem + L::kIntsOffset);
-    int *prefix = lens + a.batch;
-    int *scan_tmp = prefix + a.batch + 1;
+    const UnitTable ut = unit_table(reinterpret_cast<int *>(smem + L::kIntsOffset), a.batch, a.s_max);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int hkv = a.cache.num_kv_heads, bs = a.cache.block_size, chunk = a.chunk;
@@ -141,8 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_barrier_init();
     }
     pdl_wait();  // lengths, tables, q and the cache may come from the previous kernel
-    decode_scan_units<kThreads>(a, lens, prefix, scan_tmp);
-    const int num_units = prefix[a.batch];
+    const int num_units = decode_scan_units<kThreads>(a, ut);
 
     if (warp == kWarps) {
         // ===================================== producer warp =====================================
@@ -153,17 +150,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         int stage = 0;
         uint32_t phase = 0;
         uint32_t issued_mask = 0, issued_parity = 0;
+        UnitCursor c = {};
+        PageWindow win = {};
+        if ((int)blockIdx.x < num_units) {
+            c = unit_of(blockIdx.x, ut, a.s_max, hkv, chunk);
+            win = unit_pages(a, c, lane);
+        }
         for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
-            const UnitCursor c = unit_of(u, prefix, lens, a.batch, hkv, chunk);
+            // the next unit's cursor and page ids, loading while this unit's copies go out
+            UnitCursor cn = c;
+            PageWindow wn = win;
+            if (u + (int)gridDim.x < num_units) {
+                cn = unit_of(u + gridDim.x, ut, a.s_max, hkv, chunk);
+                wn = unit_pages(a, cn, lane);
+            }
             const int *bt = a.block_tables + (size_t)c.b * a.max_blocks_per_seq;
+            const int unit_last_page = (c.t1 - 1) >> a.cache.log2_block_size;
             for (int ts = c.t0; ts < c.t1; ts += kTile) {
                 const int n = min(kTile, c.t1 - ts);
                 const int page0 = ts >> a.cache.log2_block_size;
                 const int npages = bs < kTile ? (n + bs - 1) / bs : 1;
                 const int off = bs < kTile ? 0 : (ts & (bs - 1));
-                int pb = 0;
+                if (page0 + npages > win.first + win.count)  // units of more than 64 pages
+                    win = load_pages(bt, page0, unit_last_page - page0 + 1, lane);
+                int pb = window_page(win, page0 + lane);
                 if (lane < npages) {
-                    pb = __ldg(bt + page0 + lane);
                     if (pb < 0 || pb >= a.cache.num_blocks) {
                         set_error(a.err, kErrDeviceRange);
                         pb = 0;
@@ -207,6 +218,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     phase ^= 1u;
                 }
             }
+            c = cn;
+            win = wn;
         }
         if (mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.err) && lane == 0) {
             stage_unit[stage] = -1;
@@ -227,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&full[stage], phase, abort_flag, a.err)) return;
         const int u = stage_unit[stage];
         if (u < 0) break;
-        const UnitCursor c = unit_of(u, prefix, lens, a.batch, hkv, chunk);
+        const UnitCursor c = unit_of(u, ut, a.s_max, hkv, chunk);
         float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
         float o[kKSteps][4];
 #pragma unroll
@@ -361,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         named_barrier(1, kWarps * 32);
-        const int splits = (lens[c.b] + chunk - 1) / chunk;
+        const int splits = (ut.lens[c.b] + chunk - 1) / chunk;
         for (int idx = tid; idx < G * D; idx += kWarps * 32) {
             const int g = idx / D, d = idx - (idx / D) * D;
             float M = -INFINITY;
@@ -405,11 +418,11 @@ cudaError_t launch_gqa_t(const DecodeArgs &a, int grid, cudaStream_t s) {
     const int dev = device_info().device;
     if (dev >= 64 || !configured[dev]) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)GqaLayout<D, G>::smem_bytes(kMaxBatchG));
+                                 (int)GqaLayout<D, G>::smem_bytes(kMaxBatchG, kDecodeMaxSplits));
         if (e != cudaSuccess) return e;
         if (dev < 64) configured[dev] = true;
     }
-    return launch_pdl(kern, dim3(grid), dim3(kThreads), GqaLayout<D, G>::smem_bytes(a.batch), s, tm, a);
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), GqaLayout<D, G>::smem_bytes(a.batch, a.s_max), s, tm, a);
 }
 
 }  // namespace

@@ -84,21 +84,25 @@ CacheView view_of(const pkv_cache &c) {
 
 // Tokens per decode split.  Automatic: enough (sequence, KV head, split) units for about
 // eight per CTA at full capacity, in [128, 512] tokens; explicit: capacity / num_splits
-// rounded up to the tile.
+// rounded up to the tile.  Either way at least capacity / kDecodeMaxSplits, rounded up to the
+// tile, so that a full context has at most kDecodeMaxSplits splits.
 int split_tokens(int batch, int num_kv_heads, int block_size, int max_blocks_per_seq, int num_splits) {
     const long long cap = (long long)max_blocks_per_seq * block_size;
-    const int tile = kDecodeTile;
+    const long long tile = kDecodeTile;
+    long long c;
     if (num_splits > 0) {
-        long long c = (cap + num_splits - 1) / num_splits;
-        c = (c + tile - 1) / tile * tile;
-        return (int)(c < tile ? tile : c);
+        c = (cap + num_splits - 1) / num_splits;
+    } else {
+        const DeviceInfo &d = slot().info;
+        const long long ctas = (long long)d.num_sms * d.decode_ctas_per_sm;
+        const long long want = (long long)batch * num_kv_heads * cap / (ctas * 8 > 0 ? ctas * 8 : 1);
+        c = 512;
+        while (c > 128 && c > want) c >>= 1;
     }
-    const DeviceInfo &d = slot().info;
-    const long long ctas = (long long)d.num_sms * d.decode_ctas_per_sm;
-    const long long want = (long long)batch * num_kv_heads * cap / (ctas * 8 > 0 ? ctas * 8 : 1);
-    int c = 512;
-    while (c > 128 && c > want) c >>= 1;
-    return c;
+    const long long floor_c = (cap + kDecodeMaxSplits - 1) / kDecodeMaxSplits;
+    if (c < floor_c) c = floor_c;
+    c = (c + tile - 1) / tile * tile;
+    return (int)(c < tile ? tile : c);
 }
 
 }  // namespace

@@ -95,7 +95,8 @@ struct DeviceInfo {
 };
 const DeviceInfo &device_info();
 
-constexpr int kDecodeTile = 64;  // tokens per decode pipeline stage
+constexpr int kDecodeTile = 64;         // tokens per decode pipeline stage
+constexpr int kDecodeMaxSplits = 2048;  // splits of one context (bounds the split size from below)
 
 cudaError_t launch_append(const AppendArgs &a, cudaStream_t s);
 cudaError_t encode_cache_map(const CacheView &c, int box_rows, CUtensorMap *map);
@@ -104,7 +105,6 @@ cudaError_t launch_decode(const DecodeArgs &a, int grid, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t s);
 int decode_ctas_per_sm(int head_dim, int group, int dtype);
-size_t decode_smem_bytes(int head_dim, int group, int batch);
 int decode_max_batch();
 
 }  // namespace pkv

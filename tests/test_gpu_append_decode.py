@@ -207,6 +207,22 @@ def test_decode_inputs_written_by_the_previous_kernel(hq, hkv):
         check_close(out, ref, "f16", roundings=1 + p_roundings(p), what="inputs from kernels hq=%d" % hq)
 
 
+@pytest.mark.parametrize("hq,hkv", [(2, 2), (8, 2)])
+def test_decode_large_batch_many_equal_lengths(hq, hkv):
+    """Hundreds of sequences, most sharing a handful of lengths: every CTA numbers the work
+    units from the lengths on its own, so the numbering must not depend on thread timing."""
+    gen = torch.Generator().manual_seed(17)
+    choices = torch.tensor([0, 1, 64, 65, 300, 1000, 1500])
+    lens = choices[torch.randint(0, len(choices), (600,), generator=gen)].tolist()
+    p = problem(lens=lens, hq=hq, hkv=hkv, d=64, bs=16, dtype=W.BF16, seed=hq, mb=128)
+    cache = device_cache(p)
+    ref, ref_lse = oracle.attention_of(p, cache_bits(cache))
+    for splits in (0, 5):
+        out, lse = run_decode(p, cache, num_splits=splits)
+        check_close(out, ref, W.BF16, roundings=1 + p_roundings(p), what="batch 600 splits=%d" % splits)
+        np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-5, atol=1e-5)
+
+
 def test_decode_bad_page_flags_error():
     p = problem(lens=[200, 50], hq=4, hkv=4, bs=16)
     cache = device_cache(p)

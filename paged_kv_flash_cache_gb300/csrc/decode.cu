@@ -206,62 +206,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
 
     if (warp == kMergeWarp) {
         // ================================= merge warp =================================
-        // Combines the consumer warps' (m, l, acc) rows of a unit: lane w < 8 takes warp w's
-        // (m, l), M and the weighted sum of l are reduced over the whole warp, the weights
-        // exp2(m_w - M) go to every lane by shuffles, and lane j sums the rows' elements
-        // j, j + 32, ...
-        int mbuf = 0;
-        uint32_t mphase = 0;
-        for (;;) {
-            if (!mbar_wait(&mfull[mbuf], mphase, abort_flag, a.err)) return;
-            const int u = merge_unit[mbuf];
-            if (u < 0) break;
-            const UnitCursor c = unit_of(u, ut, a.s_max, hkv, chunk);
-            const float *rows = merge + (size_t)mbuf * L::kMergeFloats;
-            const int splits = (ut.lens[c.b] + chunk - 1) / chunk;
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float *rg = rows + (size_t)g * (D + 2);  // warp w's row: rg + w * G * (D + 2)
-                const float mw = lane < kConsumerWarps ? rg[(size_t)lane * G * (D + 2) + D] : -INFINITY;
-                const float lw = lane < kConsumerWarps ? rg[(size_t)lane * G * (D + 2) + D + 1] : 0.f;
-                float M = mw;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-                const float wgt = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
-                float lsum = lw * wgt;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
-                float wv[kConsumerWarps];
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) wv[w] = __shfl_sync(0xffffffffu, wgt, w);
-                const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-                const int h = c.kvh * G + g;
-                const size_t row_id = (size_t)c.b * a.num_q_heads + h;
-#pragma unroll
-                for (int d = lane; d < D; d += 32) {
-                    float o = 0.f;
-#pragma unroll
-                    for (int w = 0; w < kConsumerWarps; ++w) o += rg[(size_t)w * G * (D + 2) + d] * wv[w];
-                    const float res = o * inv;
-                    if (splits == 1) store_out(a.out, row_id * D + d, res, a.out_dtype);
-                    else a.part_o[(row_id * a.s_max + c.split) * D + d] = res;
-                }
-                if (lane == 0) {
-                    const float lse_v = lsum > 0.f ? (M + log2f(lsum)) * kLn2 : -INFINITY;
-                    if (splits == 1) {
-                        if (a.lse) a.lse[row_id] = lse_v;
-                    } else {
-                        a.part_lse[row_id * a.s_max + c.split] = lse_v;
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&mempty[mbuf]);
-            if (++mbuf == 2) {
-                mbuf = 0;
-                mphase ^= 1u;
-            }
-        }
+        merge_warp_loop<D, G, kConsumerWarps>(a, ut, merge, L::kMergeFloats, mfull, mempty, merge_unit, abort_flag,
+                                              lane);
         pdl_launch_dependents();
         return;
     }

@@ -97,6 +97,72 @@ __device__ __forceinline__ int window_page(const PageWindow &w, int page) {
     return rel < 32 ? lo : hi;
 }
 
+// The merge warp of a decode CTA. At the end of a unit each of the W consumer warps leaves its
+// (acc[D], m, l) row per query head of the unit in merge buffer i ([W][G][D + 2] floats; m in
+// log2 units, acc and l relative to 2^m), writes the unit id (warp 0) and arrives on mfull[i]; this
+// loop combines the rows -- M = max m, weights 2^(m_w - M), out = sum w acc / sum w l, lse =
+// (M + log2 sum w l) ln 2 -- writes the final output of a single-split context or the split's
+// partial, and frees the buffer on mempty[i]. Buffers alternate; unit id -1 ends the loop.
+// Returns false if a wait gave up (the error word is set).
+template <int D, int G, int W>
+__device__ __forceinline__ bool merge_warp_loop(const DecodeArgs &a, const UnitTable &ut, const float *merge,
+                                                size_t buf_floats, uint64_t *mfull, uint64_t *mempty,
+                                                const int *merge_unit, volatile int *abort_flag, int lane) {
+    static_assert(W <= 32, "one lane per consumer warp");
+    const int hkv = a.cache.num_kv_heads, chunk = a.chunk;
+    int mbuf = 0;
+    uint32_t mphase = 0;
+    for (;;) {
+        if (!mbar_wait(&mfull[mbuf], mphase, abort_flag, a.err)) return false;
+        const int u = merge_unit[mbuf];
+        if (u < 0) return true;
+        const UnitCursor c = unit_of(u, ut, a.s_max, hkv, chunk);
+        const float *rows = merge + (size_t)mbuf * buf_floats;
+        const int splits = (ut.lens[c.b] + chunk - 1) / chunk;
+#pragma unroll 1
+        for (int g = 0; g < G; ++g) {
+            const float *rg = rows + (size_t)g * (D + 2);  // warp w's row: rg + w * G * (D + 2)
+            const float mw = lane < W ? rg[(size_t)lane * G * (D + 2) + D] : -INFINITY;
+            const float lw = lane < W ? rg[(size_t)lane * G * (D + 2) + D + 1] : 0.f;
+            float M = mw;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+            const float wgt = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+            float lsum = lw * wgt;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+            float wv[W];
+#pragma unroll
+            for (int w = 0; w < W; ++w) wv[w] = __shfl_sync(0xffffffffu, wgt, w);
+            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+            const size_t row_id = (size_t)c.b * a.num_q_heads + (size_t)c.kvh * G + g;
+#pragma unroll
+            for (int d = lane; d < D; d += 32) {
+                float o = 0.f;
+#pragma unroll
+                for (int w = 0; w < W; ++w) o += rg[(size_t)w * G * (D + 2) + d] * wv[w];
+                const float res = o * inv;
+                if (splits == 1) store_out(a.out, row_id * D + d, res, a.out_dtype);
+                else a.part_o[(row_id * a.s_max + c.split) * D + d] = res;
+            }
+            if (lane == 0) {
+                const float lse_v = lsum > 0.f ? (M + log2f(lsum)) * kLn2 : -INFINITY;
+                if (splits == 1) {
+                    if (a.lse) a.lse[row_id] = lse_v;
+                } else {
+                    a.part_lse[row_id * a.s_max + c.split] = lse_v;
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&mempty[mbuf]);
+        if (++mbuf == 2) {
+            mbuf = 0;
+            mphase ^= 1u;
+        }
+    }
+}
+
 // Prologue run by all kThreads threads of a CTA: clamp the lengths (flagging out-of-range ones)
 // and build the tables above. Returns the number of units; ends with __syncthreads.
 template <int kThreads>

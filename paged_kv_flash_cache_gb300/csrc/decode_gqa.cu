@@ -11,19 +11,21 @@
 // conversions and cross-lane sums; here one mma.sync m16n8k16 covers 16 tokens x 8 head slots x
 // 16 dims.
 //
-// Kernel structure (persistent, one CTA per SM, 5 warps):
+// Kernel structure (persistent, one CTA per SM, 6 warps):
 //   * units (sequence, KV head, split) are numbered from the context lengths and dealt
 //     round-robin to the CTAs, as in decode.cu;
-//   * warp 4 streams each unit's 64-token tiles with TMA: the pages a tile covers are looked up by
-//     the warp's lanes and each lane issues its page's K and V boxes (64 columns x rows, 128-byte
+//   * warp 4 streams each unit's 64-token tiles with TMA: the page ids of a unit are read one
+//     unit ahead, and each lane issues its page's K and V boxes (64 columns x rows, 128-byte
 //     swizzle, through a 2-D tensor map over the cache), into a 4-stage ring; q comes in with the
 //     unit's first tile;
 //   * warps 0-3 each own 16 tokens of a tile: ldmatrix from the swizzled tile gives the A fragments
 //     of K (row) and of V (transposed); q, held as B fragments for the whole unit, has the group's
 //     heads in the N slots (padding slots are zero); the scores stay in the accumulator fragments:
 //     column max by shuffles, lazy rescale (threshold 2^8), exp2, and P moved into B-fragment
-//     layout with movmatrix; O^T accumulates in registers; at the end of a unit the warps merge
-//     through shared memory and write the output (single split) or the split partials.
+//     layout with movmatrix; O^T accumulates in registers; at the end of a unit each warp leaves
+//     its rows in one of two shared-memory merge buffers and goes on with the next unit;
+//   * warp 5 merges the four warps' rows and writes the output (single split) or the split
+//     partials.
 #include <cuda.h>
 
 #include "decode_common.cuh"
@@ -35,7 +37,9 @@ namespace pkv {
 namespace {
 
 constexpr int kWarps = 4;                         // consumer warps, 16 tokens each
-constexpr int kThreads = (kWarps + 1) * 32;
+constexpr int kProducerWarp = kWarps;
+constexpr int kMergeWarp = kWarps + 1;
+constexpr int kThreads = (kWarps + 2) * 32;
 constexpr int kTile = 64;                         // tokens per stage
 constexpr int kStagesG = 4;
 constexpr int kMaxBatchG = 2048;
@@ -49,9 +53,11 @@ struct GqaLayout {
     static constexpr uint32_t kQBytes = G * D * 2;
     static constexpr uint32_t kStageBytes = (2 * kKBytes + kQBytes + 1023) / 1024 * 1024;
     static constexpr uint32_t kBarOffset = kStagesG * kStageBytes;
-    static constexpr uint32_t kMergeOffset = kBarOffset + 2 * kStagesG * 8 + 32;  // + abort flag, unit ids
-    static constexpr uint32_t kMergeFloats = kWarps * G * (D + 2);
-    static constexpr uint32_t kIntsOffset = kMergeOffset + kMergeFloats * 4;
+    // barriers: full / empty per stage, merge full / empty per merge buffer; then the abort flag
+    // (padded to 16 bytes), the unit of each stage and the unit of each merge buffer
+    static constexpr uint32_t kMergeOffset = kBarOffset + (2 * kStagesG + 4) * 8 + 64;
+    static constexpr uint32_t kMergeFloats = kWarps * G * (D + 2);  // one of two merge buffers
+    static constexpr uint32_t kIntsOffset = kMergeOffset + 2 * kMergeFloats * 4;
     __host__ __device__ static size_t smem_bytes(int batch, int s_max) {
         return kIntsOffset + unit_table_ints(batch, s_max) * 4 + 1024;  // + 1024-byte alignment slack
     }
@@ -122,9 +128,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kBarOffset);
     uint64_t *empty = full + kStagesG;
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + kStagesG);
-    int *stage_unit = reinterpret_cast<int *>(empty + kStagesG) + 4;
-    float *merge = reinterpret_cast<float *>(smem + L::kMergeOffset);
+    uint64_t *mfull = empty + kStagesG;  // [2] the consumer warps' rows of a unit are in buffer i
+    uint64_t *mempty = mfull + 2;        // [2] the merge warp has read buffer i
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(mempty + 2);
+    int *stage_unit = reinterpret_cast<int *>(mempty + 2) + 4;
+    int *merge_unit = stage_unit + kStagesG;  // [2] unit of each merge buffer, -1: end
+    float *merge = reinterpret_cast<float *>(smem + L::kMergeOffset);  // [2][kWarps][G][D + 2]
     const UnitTable ut = unit_table(reinterpret_cast<int *>(smem + L::kIntsOffset), a.batch, a.s_max);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -135,13 +144,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kWarps);
         }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&mfull[i], kWarps);
+            mbar_init(&mempty[i], 1);
+        }
         *abort_flag = 0;
         fence_barrier_init();
     }
     pdl_wait();  // lengths, tables, q and the cache may come from the previous kernel
     const int num_units = decode_scan_units<kThreads>(a, ut);
 
-    if (warp == kWarps) {
+    if (warp == kProducerWarp) {
         // ===================================== producer warp =====================================
         const uint64_t pol = l2_policy_evict_first();
         const uint16_t *qg = static_cast<const uint16_t *>(a.q);
@@ -228,6 +241,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         return;
     }
 
+    if (warp == kMergeWarp) {
+        // ====================================== merge warp ======================================
+        merge_warp_loop<D, G, kWarps>(a, ut, merge, L::kMergeFloats, mfull, mempty, merge_unit, abort_flag, lane);
+        pdl_launch_dependents();
+        return;
+    }
+
     // ===================================== consumer warps =====================================
     constexpr int kKSteps = D / 16;         // k-steps of q.K^T, m-tiles of O^T
     const int gid = lane >> 2, tig = lane & 3;
@@ -236,6 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t bq[kKSteps][2];                // q as B fragments (n = head slot, k = dims)
     int stage = 0;
     uint32_t phase = 0;
+    int mbuf = 0;  // merge buffer of the next unit
+    uint32_t mphase = 0;
     for (;;) {
         if (!mbar_wait(&full[stage], phase, abort_flag, a.err)) return;
         const int u = stage_unit[stage];
@@ -357,11 +379,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             l[0] += __shfl_xor_sync(0xffffffffu, l[0], ofs);
             l[1] += __shfl_xor_sync(0xffffffffu, l[1], ofs);
         }
+        // ---- hand this warp's rows to the merge warp ----
+        if (!mbar_wait(&mempty[mbuf], mphase ^ 1u, abort_flag, a.err)) return;
+        float *rows = merge + (size_t)mbuf * L::kMergeFloats;
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
             const int g = g_lo + j;
             if (g < G) {
-                float *row = merge + ((size_t)warp * G + g) * (D + 2);
+                float *row = rows + ((size_t)warp * G + g) * (D + 2);
 #pragma unroll
                 for (int mt = 0; mt < kKSteps; ++mt) {
                     row[mt * 16 + gid] = o[mt][j];
@@ -373,36 +398,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        named_barrier(1, kWarps * 32);
-        const int splits = (ut.lens[c.b] + chunk - 1) / chunk;
-        for (int idx = tid; idx < G * D; idx += kWarps * 32) {
-            const int g = idx / D, d = idx - (idx / D) * D;
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, merge[((size_t)w * G + g) * (D + 2) + D]);
-            float lsum = 0.f, acc = 0.f;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float *row = merge + ((size_t)w * G + g) * (D + 2);
-                const float mw = row[D];
-                const float wgt = (mw == -INFINITY) ? 0.f : ex2f(mw - M);
-                lsum += row[D + 1] * wgt;
-                acc += row[d] * wgt;
-            }
-            const float res = lsum > 0.f ? acc / lsum : 0.f;
-            const float lse_v = lsum > 0.f ? (M + log2f(lsum)) * kLn2 : -INFINITY;
-            const int h = c.kvh * G + g;
-            const size_t row_id = (size_t)c.b * a.num_q_heads + h;
-            if (splits == 1) {
-                store_out(a.out, row_id * D + d, res, a.out_dtype);
-                if (d == 0 && a.lse) a.lse[row_id] = lse_v;
-            } else {
-                const size_t pr = row_id * a.s_max + c.split;
-                a.part_o[pr * D + d] = res;
-                if (d == 0) a.part_lse[pr] = lse_v;
-            }
+        if (warp == 0 && lane == 0) merge_unit[mbuf] = u;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&mfull[mbuf]);
+        if (++mbuf == 2) {
+            mbuf = 0;
+            mphase ^= 1u;
         }
-        named_barrier(1, kWarps * 32);
+    }
+    // end marker for the merge warp
+    if (mbar_wait(&mempty[mbuf], mphase ^ 1u, abort_flag, a.err)) {
+        if (warp == 0 && lane == 0) merge_unit[mbuf] = -1;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&mfull[mbuf]);
     }
     pdl_launch_dependents();
 }

@@ -45,7 +45,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", default="", help="comma list of extra workloads (bs_sweep,mixed,prefix,prefill)")
+    ap.add_argument("--only", default="", help="comma list of extra workloads (bs_sweep,mixed,prefix,fp8,prefill)")
     ap.add_argument("--profile", choices=["decode", "append", "prefill", "decode_mixed", "decode_prefix"], default=None,
                     help="small case for ncu captures: W + K launches of one kernel, nothing else timed")
     return ap.parse_args()
@@ -490,6 +490,42 @@ def bench_prefix(torch, steps, warmup):
             "tokens_per_s": round(p.batch / ms * 1e3, 1)}
 
 
+def bench_fp8(torch, steps, warmup, fp16_ms=None):
+    """The 7B-like decode batch with the cache in FP8 (E4M3 codes + one FP32 scale per row)."""
+    import paged_kv_flash_cache_gb300 as pkv
+    from paged_kv_flash_cache_gb300 import workloads as W
+    p = W.decode_7b(pool_init="none", device="cuda", kv_format="fp8")
+    shape = (p.num_blocks, 2, p.num_kv_heads, p.block_size, p.head_dim)
+    codes = torch.zeros(shape, dtype=torch.uint8, device="cuda")
+    scales = torch.zeros(shape[:4], dtype=torch.float32, device="cuda")
+    pkv.kv_cache_append(codes, p.k_ctx, p.v_ctx, p.cu_ctx_lens.cuda(), torch.zeros(p.batch, dtype=torch.int32,
+                        device="cuda"), p.block_tables.cuda(), scales=scales)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    q, bt, ctx = p.q.cuda(), p.block_tables.cuda(), p.context_lens.cuda()
+    ws = torch.empty(max(16, pkv.decode_workspace_size(p.batch, 32, 32, 128, 16, bt.shape[1])), dtype=torch.uint8,
+                     device="cuda")
+    o = torch.empty((p.batch, 32, 128), dtype=q.dtype, device="cuda")
+    fn = lambda i: pkv.paged_attn_decode(codes, q, bt, ctx, scale=p.scale, workspace=ws, out=o, scales=scales)
+    for i in range(warmup):
+        fn(i)
+    ms = time_loop(torch, fn, steps, torch.cuda.current_stream()) / steps
+    tokens = int(p.context_lens.sum())
+    kv = tokens * p.num_kv_heads * 2 * (p.head_dim + 4)          # codes + one FP32 scale per row
+    qo = 2 * p.batch * p.num_q_heads * p.head_dim * 2
+    table = sum((int(L) + 15) // 16 for L in p.context_lens.tolist()) * 4 + p.batch * 4
+    del codes, scales
+    torch.cuda.empty_cache()
+    r = {"workload": "7B-like decode batch (16 x U[1024, 8192] contexts, 32 heads x 128, bs 16) with an FP8 "
+                     "E4M3 cache, one FP32 scale per (page, K/V, head, token) row; fp16 q and output",
+         "ms": round(ms, 4), "kv_bytes": kv, "kv_gbs": round(kv / ms / 1e6, 1),
+         "frac_of_hbm": round((kv + qo + table) / ms / 1e6 / peaks()["hbm_gbs"], 3),
+         "tokens_per_s": round(p.batch / ms * 1e3, 1)}
+    if fp16_ms:
+        r["speedup_vs_fp16_cache"] = round(fp16_ms / ms, 3)
+    return r
+
+
 def bench_prefill(torch, steps, warmup):
     import paged_kv_flash_cache_gb300 as pkv
     from paged_kv_flash_cache_gb300 import workloads as W
@@ -632,7 +668,7 @@ def main():
         extra = {}
         only = set(filter(None, args.only.split(",")))
         for name, fn in (("bs_sweep", bench_bs_sweep), ("mixed", bench_mixed), ("prefix", bench_prefix),
-                         ("prefill", bench_prefill)):
+                         ("fp8", lambda t, k, w: bench_fp8(t, k, w, r["decode_ms"])), ("prefill", bench_prefill)):
             if only and name not in only:
                 continue
             try:

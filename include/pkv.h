@@ -70,9 +70,27 @@ typedef enum {
 
 typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_F32 = 2 } pkv_dtype;
 
+/* How the cache stores K and V.
+ *  PKV_KV_NATIVE    ptr holds dtype elements (2 bytes each).
+ *  PKV_KV_FP8_E4M3  ptr holds one-byte OCP FP8 E4M3 codes (1 sign, 4 exponent bits
+ *                   with bias 7, 3 fraction bits; no infinities; largest finite
+ *                   448) and `scales` one FP32 scale per cached row, i.e. per
+ *                   (page, K/V, KV head, token): element = decode(code) * scale.
+ *                   A row is written by pkv_kv_cache_append as scale = amax / 448,
+ *                   code = round-to-nearest-even, saturating, of x * (448 / amax),
+ *                   in FP32 (amax = largest |x| of the row; an all-zero row stores
+ *                   scale 0 and zero codes).  The pages name KV-cache compression
+ *                   ([ON2]) without a scheme; this per-row scaling is the library's
+ *                   reading of it. */
+typedef enum { PKV_KV_NATIVE = 0, PKV_KV_FP8_E4M3 = 1 } pkv_kv_format;
+
 /* The paged KV cache [num_blocks, 2, num_kv_heads, block_size, head_dim] ([FAPA] s3).
- * dtype is PKV_F16 or PKV_BF16.  Supported: head_dim 64 or 128; block_size a power
- * of two in [8, 512]. */
+ * dtype (PKV_F16 or PKV_BF16) is the type of q, k_new and v_new, of the default
+ * output, and of the elements of a native cache.  Supported: head_dim 64 or 128;
+ * block_size a power of two in [8, 512].  format and scales are as above (scales
+ * [num_blocks, 2, num_kv_heads, block_size], 16-byte aligned; NULL for a native
+ * cache).  An FP8 cache is supported by append and decode; prefill over it returns
+ * PKV_ERR_UNSUPPORTED. */
 typedef struct {
     void *ptr;
     int num_blocks;
@@ -80,10 +98,13 @@ typedef struct {
     int block_size;
     int head_dim;
     pkv_dtype dtype;
+    pkv_kv_format format;
+    float *scales;
 } pkv_cache;
 
 /* kv_cache_append -- write new tokens' K and V into their pages ([ON2] prefill /
- * decode; [CHUNK] s2.1 addressing).
+ * decode; [CHUNK] s2.1 addressing); an FP8 cache receives each row's codes and
+ * scale, computed as described at pkv_kv_format.
  *   k_new, v_new      [num_new_tokens, Hkv, D] in the cache dtype, packed by
  *                     sequence: sequence b owns rows cu_new_lens[b] .. cu_new_lens[b+1]-1.
  *   cu_new_lens       int32 [batch+1], cu_new_lens[0] = 0, non-decreasing,
@@ -92,7 +113,7 @@ typedef struct {
  *                     sequence b goes to position ctx_before[b] + j.
  *   block_tables      int32 [batch, max_blocks_per_seq]; pages for every written
  *                     position must already be assigned.
- * The copy is bit-exact.  Positions whose table slot is beyond max_blocks_per_seq,
+ * A native cache receives a bit-exact copy.  Positions whose table slot is beyond max_blocks_per_seq,
  * or whose page id is outside [0, num_blocks), are skipped and flag
  * PKV_ERR_DEVICE_RANGE.  Nothing else in the cache is modified. */
 PKV_API pkv_status pkv_kv_cache_append(pkv_cache cache, const void *k_new, const void *v_new,
@@ -199,7 +220,7 @@ PKV_API pkv_status pkv_get_device_error(void *stream, int *code);
 PKV_API const char *pkv_status_string(pkv_status status);
 
 /* Library ABI version (major * 100 + minor). */
-PKV_API int pkv_version(void);
+PKV_API int pkv_version(void);  /* 101: pkv_cache carries format and scales */
 
 #ifdef __cplusplus
 }

@@ -20,6 +20,11 @@ Functions and the passages they follow (page titles of the subject's web pages):
   * attn_combine -- log-sum-exp merge of split partial results; the rescale
     identity is the one of the online-softmax update in section 2 of the
     ipipp.com page (old terms scaled by exp(m_old - m_new)).
+  * e4m3_encode / e4m3_decode, kv_cache_append_fp8, paged_attention_fp8 -- the
+    FP8 cache: the "KV cache compression" the answer.freetools.me page names
+    without a scheme, read as one FP32 scale per cached row (amax / 448) and OCP
+    FP8 E4M3 codes (round to nearest even, saturating); attention over the
+    exactly dequantised values.
 Pins (tests/test_oracle_pins.py) tie every function to closed forms,
 invariants and a library routine; none is "parity unpinned".
 """
@@ -29,6 +34,7 @@ import ctypes
 import os
 import subprocess
 import threading
+from typing import NamedTuple
 
 import numpy as np
 
@@ -69,6 +75,14 @@ def _load():
             lib.oracle_paged_attention.restype = I
             lib.oracle_attn_combine.argtypes = [P, P, L, I, I, P, P]
             lib.oracle_attn_combine.restype = I
+            lib.oracle_e4m3_encode.argtypes = [P, P, L]
+            lib.oracle_e4m3_encode.restype = None
+            lib.oracle_e4m3_decode.argtypes = [P, P, L]
+            lib.oracle_e4m3_decode.restype = None
+            lib.oracle_kv_cache_append_fp8.argtypes = [P, P, I, I, I, I, I, P, P, P, P, P, I, I]
+            lib.oracle_kv_cache_append_fp8.restype = I
+            lib.oracle_paged_attention_fp8.argtypes = [I, P, P, I, I, I, I, P, I, P, P, P, I, I, D, I, P, L, P, P, I]
+            lib.oracle_paged_attention_fp8.restype = I
             _lib = lib
     return _lib
 
@@ -151,9 +165,83 @@ def attn_combine(partial_o: np.ndarray, partial_lse: np.ndarray):
     return out, lse
 
 
+class Fp8Cache(NamedTuple):
+    """An FP8 cache on the host: E4M3 codes uint8 [NB, 2, Hkv, bs, D], scales float32 [NB, 2, Hkv, bs]."""
+    codes: np.ndarray
+    scales: np.ndarray
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """float32 values -> E4M3 codes (round to nearest even, saturating to +-448)."""
+    xf = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    out = np.zeros(xf.shape, dtype=np.uint8)
+    _load().oracle_e4m3_encode(_ptr(xf), _ptr(out), int(xf.size))
+    return out
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    c = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+    out = np.zeros(c.shape, dtype=np.float64)
+    _load().oracle_e4m3_decode(_ptr(c), _ptr(out), int(c.size))
+    return out
+
+
+def kv_cache_append_fp8(cache: Fp8Cache, dtype: str, k_new, v_new, cu_new_lens, ctx_before, block_tables) -> int:
+    """In-place quantising append into an Fp8Cache (k_new / v_new in `dtype`). Returns the C status."""
+    codes, scales = cache
+    assert codes.dtype == np.uint8 and codes.flags.c_contiguous and codes.ndim == 5
+    assert scales.dtype == np.float32 and scales.flags.c_contiguous and scales.shape == codes.shape[:4]
+    nb, two, hkv, bs, d = codes.shape
+    k = _u16(k_new)
+    v = _u16(v_new)
+    cu = _i32(cu_new_lens)
+    cb = _i32(ctx_before)
+    bt = _i32(block_tables)
+    batch, mb = bt.shape
+    assert k.shape == v.shape and k.size == int(cu[-1]) * hkv * d
+    return _load().oracle_kv_cache_append_fp8(_ptr(codes), _ptr(scales), nb, hkv, bs, d, DTYPE_CODE[dtype], _ptr(k),
+                                              _ptr(v), _ptr(cu), _ptr(cb), _ptr(bt), batch, mb)
+
+
+def paged_attention_fp8(dtype: str, cache: Fp8Cache, q, num_q_heads: int, cu_q_lens, context_lens, block_tables,
+                        scale: float, causal: bool, rows=None, nthreads: int = 0):
+    """paged_attention over an FP8 cache (q in `dtype`). Returns (out, lse) as float64."""
+    codes, scales = cache
+    nb, two, hkv, bs, d = codes.shape
+    qb = _u16(q)
+    cu = _i32(cu_q_lens)
+    cl = _i32(context_lens)
+    bt = _i32(block_tables)
+    batch, mb = bt.shape
+    sel = None
+    if rows is not None:
+        sel = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        n = int(sel.size)
+    else:
+        n = int(cu[-1])
+    out = np.zeros((n, num_q_heads, d), dtype=np.float64)
+    lse = np.zeros((n, num_q_heads), dtype=np.float64)
+    if nthreads <= 0:
+        nthreads = os.cpu_count() or 1
+    rc = _load().oracle_paged_attention_fp8(DTYPE_CODE[dtype], _ptr(np.ascontiguousarray(codes)),
+                                            _ptr(np.ascontiguousarray(scales)), nb, hkv, bs, d, _ptr(qb),
+                                            num_q_heads, _ptr(cu), _ptr(cl), _ptr(bt), batch, mb, float(scale),
+                                            1 if causal else 0, _ptr(sel), n, _ptr(out), _ptr(lse), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_paged_attention_fp8: status %d (bad page id, table slot or row)" % rc)
+    return out, lse
+
+
 def empty_cache_bits(problem) -> np.ndarray:
-    """The pool as uint16 bits, starting from the problem's seeded noise (or zeros)."""
+    """The pool as uint16 bits (an Fp8Cache for an FP8 problem), starting from the problem's
+    seeded noise (or zeros)."""
     shape = (problem.num_blocks, 2, problem.num_kv_heads, problem.block_size, problem.head_dim)
+    if getattr(problem, "kv_format", "native") == "fp8":
+        if problem.pool_init is None:
+            return Fp8Cache(np.zeros(shape, dtype=np.uint8), np.zeros(shape[:4], dtype=np.float32))
+        codes, scales = problem.pool_init
+        return Fp8Cache(np.ascontiguousarray(codes.cpu().numpy().reshape(shape)).copy(),
+                        np.ascontiguousarray(scales.cpu().numpy().reshape(shape[:4])).copy())
     if problem.pool_init is None:
         return np.zeros(shape, dtype=np.uint16)
     return _u16(problem.pool_init).reshape(shape).copy()
@@ -163,8 +251,12 @@ def build_cache(problem) -> np.ndarray:
     """Pool bits after appending every context token of `problem` (ctx_before = 0)."""
     import torch
     cache = empty_cache_bits(problem)
-    rc = kv_cache_append(cache, problem.k_ctx, problem.v_ctx, problem.cu_ctx_lens,
-                         torch.zeros(problem.batch, dtype=torch.int32), problem.block_tables)
+    if isinstance(cache, Fp8Cache):
+        rc = kv_cache_append_fp8(cache, problem.dtype, problem.k_ctx, problem.v_ctx, problem.cu_ctx_lens,
+                                 torch.zeros(problem.batch, dtype=torch.int32), problem.block_tables)
+    else:
+        rc = kv_cache_append(cache, problem.k_ctx, problem.v_ctx, problem.cu_ctx_lens,
+                             torch.zeros(problem.batch, dtype=torch.int32), problem.block_tables)
     if rc != 0:
         raise ValueError("oracle append failed: %d" % rc)
     return cache
@@ -173,6 +265,11 @@ def build_cache(problem) -> np.ndarray:
 def attention_of(problem, cache_bits: np.ndarray, rows=None, nthreads: int = 0, q=None, cu_q_lens=None,
                  context_lens=None):
     """paged_attention with a problem's own tensors (optionally overriding q / lengths)."""
+    if isinstance(cache_bits, Fp8Cache):
+        return paged_attention_fp8(problem.dtype, cache_bits, problem.q if q is None else q, problem.num_q_heads,
+                                   problem.cu_q_lens if cu_q_lens is None else cu_q_lens,
+                                   problem.context_lens if context_lens is None else context_lens,
+                                   problem.block_tables, problem.scale, problem.causal, rows=rows, nthreads=nthreads)
     return paged_attention(problem.dtype, cache_bits, problem.q if q is None else q, problem.num_q_heads,
                            problem.cu_q_lens if cu_q_lens is None else cu_q_lens,
                            problem.context_lens if context_lens is None else context_lens,

@@ -30,6 +30,14 @@
  * All fp16 / bf16 inputs are converted exactly to double.  The log-sum-exp of
  * the scaled scores (lse = M + ln sum exp(s_i - M)) is returned beside the
  * output; the split-KV merge is checked against it.
+ *
+ * FP8 cache (the "KV cache compression" the answer.freetools.me page names,
+ * with no scheme given; reading listed in the design notes): every cached row
+ * (one token's K or V of one KV head, head_dim values) is stored as OCP FP8
+ * E4M3 codes with one FP32 scale, scale = amax / 448 and code = round-to-
+ * nearest-even, saturating, of x * (448 / amax), all in binary32 arithmetic;
+ * an all-zero row stores scale 0 and zero codes.  The attention reads each
+ * element as decode(code) * scale, exactly, in double.
  */
 #include <math.h>
 #include <pthread.h>
@@ -67,6 +75,65 @@ static double to_double(int dtype, uint16_t h) {
     return dtype == ORACLE_BF16 ? bf16_bits_to_double(h) : half_bits_to_double(h);
 }
 
+/* OCP FP8 E4M3 ("FN" variant): 1 sign, 4 exponent (bias 7), 3 fraction bits;
+ * no infinities, S.1111.111 is NaN, largest finite (1 + 6/8) * 2^8 = 448;
+ * exponent field 0 holds the subnormals m * 2^-9. */
+static double e4m3_to_double(uint8_t c) {
+    int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) v = NAN;
+    else if (e == 0) v = ldexp((double)m, -9);
+    else v = ldexp((double)(8 + m), e - 10);   /* (1 + m/8) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+/* Nearest E4M3 value, ties to the even fraction, magnitudes beyond 448
+ * saturated to 448 (a finite input never gives NaN). */
+static uint8_t double_to_e4m3(double x) {
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs(x);
+    if (a >= 448.0) return sign | 0x7E;
+    if (a < ldexp(1.0, -6)) {                   /* subnormal spacing 2^-9 */
+        double q = rint(a * 512.0);             /* exact scaling; rint rounds ties to even */
+        return sign | (uint8_t)q;               /* q = 8 is the smallest normal, code 0x08 */
+    }
+    int e2;
+    frexp(a, &e2);                              /* a in [2^(e2-1), 2^e2) */
+    int e = e2 - 1;
+    double r = rint(ldexp(a, 3 - e)) - 8.0;     /* fraction in eighths, rounded */
+    if (r == 8.0) { r = 0.0; e += 1; }
+    if (e > 8 || (e == 8 && r > 6.0)) return sign | 0x7E;
+    return sign | (uint8_t)(((e + 7) << 3) | (int)r);
+}
+
+void oracle_e4m3_encode(const float *x, uint8_t *codes, long n) {
+    for (long i = 0; i < n; ++i) codes[i] = double_to_e4m3((double)x[i]);
+}
+
+void oracle_e4m3_decode(const uint8_t *codes, double *x, long n) {
+    for (long i = 0; i < n; ++i) x[i] = e4m3_to_double(codes[i]);
+}
+
+/* Quantise one row of d values (binary32 arithmetic throughout). */
+static float quantise_row(int dtype, const uint16_t *src, uint8_t *dst, int d) {
+    float amax = 0.0f;
+    for (int e = 0; e < d; ++e) {
+        float a = fabsf((float)to_double(dtype, src[e]));
+        if (a > amax) amax = a;
+    }
+    if (amax == 0.0f) {
+        for (int e = 0; e < d; ++e) dst[e] = 0;
+        return 0.0f;
+    }
+    float scale = amax / 448.0f;
+    float inv = 448.0f / amax;
+    for (int e = 0; e < d; ++e) {
+        float y = (float)to_double(dtype, src[e]) * inv;
+        dst[e] = double_to_e4m3((double)y);
+    }
+    return scale;
+}
+
 /* Element offset of cache[pb][kv][h][off][0]. */
 static size_t cache_row(int pb, int kv, int h, int off, int hkv, int bs, int d) {
     return ((((size_t)pb * 2 + kv) * hkv + h) * bs + off) * (size_t)d;
@@ -74,13 +141,13 @@ static size_t cache_row(int pb, int kv, int h, int off, int hkv, int bs, int d) 
 
 /* ------------------------------------------------------------------------- */
 /* Append: for token t of sequence b (t-th of its new tokens), position
- * pos = ctx_before[b] + t, page = table[b][pos / bs], offset pos % bs;
- * copy the 16-bit patterns of K and V.  Returns 0, or -1 on an out-of-range
- * page id / table slot (nothing is written for that token). */
-int oracle_kv_cache_append(uint16_t *cache, int nb, int hkv, int bs, int d,
-                           const uint16_t *k_new, const uint16_t *v_new,
-                           const int *cu_new_lens, const int *ctx_before,
-                           const int *block_tables, int batch, int mb) {
+ * pos = ctx_before[b] + t, page = table[b][pos / bs], offset pos % bs; `row`
+ * writes token t's K and V rows of every head there.  Returns 0, or -1 on an
+ * out-of-range page id / table slot (nothing is written for that token). */
+typedef void (*append_row_fn)(void *ctx, int t, int pb, int off);
+
+static int append_walk(int nb, int bs, const int *cu_new_lens, const int *ctx_before, const int *block_tables,
+                       int batch, int mb, append_row_fn row, void *ctx) {
     int rc = 0;
     for (int b = 0; b < batch; ++b) {
         for (int t = cu_new_lens[b]; t < cu_new_lens[b + 1]; ++t) {
@@ -89,23 +156,66 @@ int oracle_kv_cache_append(uint16_t *cache, int nb, int hkv, int bs, int d,
             if (logical < 0 || logical >= mb) { rc = -1; continue; }
             int pb = block_tables[(size_t)b * mb + logical];
             if (pb < 0 || pb >= nb) { rc = -1; continue; }
-            int off = (int)(pos % bs);
-            for (int h = 0; h < hkv; ++h) {
-                const uint16_t *ks = k_new + ((size_t)t * hkv + h) * d;
-                const uint16_t *vs = v_new + ((size_t)t * hkv + h) * d;
-                uint16_t *kd = cache + cache_row(pb, 0, h, off, hkv, bs, d);
-                uint16_t *vd = cache + cache_row(pb, 1, h, off, hkv, bs, d);
-                for (int e = 0; e < d; ++e) { kd[e] = ks[e]; vd[e] = vs[e]; }
-            }
+            row(ctx, t, pb, (int)(pos % bs));
         }
     }
     return rc;
+}
+
+typedef struct {
+    int hkv, bs, d, dtype;
+    const uint16_t *k_new, *v_new;
+    uint16_t *cache;                  /* native: 16-bit patterns copied */
+    uint8_t *codes; float *scales;    /* FP8: quantised */
+} append_job;
+
+/* Native cache: copy the 16-bit patterns of K and V. */
+static void copy_rows(void *ctx, int t, int pb, int off) {
+    append_job *A = (append_job *)ctx;
+    for (int h = 0; h < A->hkv; ++h) {
+        const uint16_t *ks = A->k_new + ((size_t)t * A->hkv + h) * A->d;
+        const uint16_t *vs = A->v_new + ((size_t)t * A->hkv + h) * A->d;
+        uint16_t *kd = A->cache + cache_row(pb, 0, h, off, A->hkv, A->bs, A->d);
+        uint16_t *vd = A->cache + cache_row(pb, 1, h, off, A->hkv, A->bs, A->d);
+        for (int e = 0; e < A->d; ++e) { kd[e] = ks[e]; vd[e] = vs[e]; }
+    }
+}
+
+/* FP8 cache: quantise each K and V row, store its codes and scale. */
+static void quantise_rows(void *ctx, int t, int pb, int off) {
+    append_job *A = (append_job *)ctx;
+    for (int h = 0; h < A->hkv; ++h) {
+        for (int kv = 0; kv < 2; ++kv) {
+            const uint16_t *src = (kv == 0 ? A->k_new : A->v_new) + ((size_t)t * A->hkv + h) * A->d;
+            size_t row = cache_row(pb, kv, h, off, A->hkv, A->bs, A->d);
+            A->scales[row / (size_t)A->d] = quantise_row(A->dtype, src, A->codes + row, A->d);
+        }
+    }
+}
+
+int oracle_kv_cache_append(uint16_t *cache, int nb, int hkv, int bs, int d,
+                           const uint16_t *k_new, const uint16_t *v_new,
+                           const int *cu_new_lens, const int *ctx_before,
+                           const int *block_tables, int batch, int mb) {
+    append_job A = {hkv, bs, d, 0, k_new, v_new, cache, NULL, NULL};
+    return append_walk(nb, bs, cu_new_lens, ctx_before, block_tables, batch, mb, copy_rows, &A);
+}
+
+/* The same walk into an FP8 cache: codes [NB, 2, Hkv, bs, D] bytes, scales
+ * [NB, 2, Hkv, bs] FP32; each new row is quantised as described above. */
+int oracle_kv_cache_append_fp8(uint8_t *codes, float *scales, int nb, int hkv, int bs, int d, int dtype,
+                               const uint16_t *k_new, const uint16_t *v_new,
+                               const int *cu_new_lens, const int *ctx_before,
+                               const int *block_tables, int batch, int mb) {
+    append_job A = {hkv, bs, d, dtype, k_new, v_new, NULL, codes, scales};
+    return append_walk(nb, bs, cu_new_lens, ctx_before, block_tables, batch, mb, quantise_rows, &A);
 }
 
 /* ------------------------------------------------------------------------- */
 typedef struct {
     int dtype;
     const uint16_t *cache; int nb, hkv, bs, d;
+    const uint8_t *codes; const float *scales;   /* FP8 cache (cache == NULL) */
     const uint16_t *q; int hq;
     const int *cu_q_lens, *context_lens, *block_tables; int batch, mb;
     double scale; int causal;
@@ -114,6 +224,12 @@ typedef struct {
     long next; pthread_mutex_t lock;      /* work counter over (row, head) */
     int status;
 } attn_job;
+
+/* Element e of the cached row starting at element offset `row`. */
+static double kv_elem(const attn_job *J, size_t row, int e) {
+    if (J->codes) return e4m3_to_double(J->codes[row + e]) * (double)J->scales[row / (size_t)J->d];
+    return to_double(J->dtype, J->cache[row + e]);
+}
 
 /* One (query row, query head): the definition written out. */
 static int attend_one(attn_job *J, long sel, int h, double *s, double *acc) {
@@ -141,9 +257,9 @@ static int attend_one(attn_job *J, long sel, int h, double *s, double *acc) {
         if (logical >= J->mb) return -1;
         int pb = J->block_tables[(size_t)b * J->mb + logical];
         if (pb < 0 || pb >= J->nb) return -1;
-        const uint16_t *kr = J->cache + cache_row(pb, 0, g, (int)(i % J->bs), J->hkv, J->bs, J->d);
+        size_t kr = cache_row(pb, 0, g, (int)(i % J->bs), J->hkv, J->bs, J->d);
         double dot = 0.0;
-        for (int e = 0; e < J->d; ++e) dot += to_double(J->dtype, qv[e]) * to_double(J->dtype, kr[e]);
+        for (int e = 0; e < J->d; ++e) dot += to_double(J->dtype, qv[e]) * kv_elem(J, kr, e);
         s[i] = J->scale * dot;
     }
     /* pass 2: max, exponentials, sum, weighted sum of V */
@@ -155,8 +271,8 @@ static int attend_one(attn_job *J, long sel, int h, double *s, double *acc) {
         double w = exp(s[i] - M);
         sum += w;
         int pb = J->block_tables[(size_t)b * J->mb + i / J->bs];
-        const uint16_t *vr = J->cache + cache_row(pb, 1, g, (int)(i % J->bs), J->hkv, J->bs, J->d);
-        for (int e = 0; e < J->d; ++e) acc[e] += w * to_double(J->dtype, vr[e]);
+        size_t vr = cache_row(pb, 1, g, (int)(i % J->bs), J->hkv, J->bs, J->d);
+        for (int e = 0; e < J->d; ++e) acc[e] += w * kv_elem(J, vr, e);
     }
     for (int e = 0; e < J->d; ++e) o[e] = acc[e] / sum;
     if (lse) *lse = M + log(sum);
@@ -192,16 +308,40 @@ static void *attn_worker(void *arg) {
  * sees the whole context).  rows == NULL selects all rows 0..n_rows-1.
  * Returns 0, -1 on an out-of-range page id / table slot / row, -2 on bad
  * arguments. */
+static int run_attention(attn_job *J, int nthreads);
+
 int oracle_paged_attention(int dtype, const uint16_t *cache, int nb, int hkv, int bs, int d,
                            const uint16_t *q, int hq, const int *cu_q_lens, const int *context_lens,
                            const int *block_tables, int batch, int mb, double scale, int causal,
                            const long *rows, long n_rows, double *out, double *lse, int nthreads) {
     if (hkv <= 0 || hq <= 0 || hq % hkv != 0 || d <= 0 || bs <= 0 || batch < 0) return -2;
     attn_job J;
-    J.dtype = dtype; J.cache = cache; J.nb = nb; J.hkv = hkv; J.bs = bs; J.d = d;
+    J.dtype = dtype; J.cache = cache; J.codes = NULL; J.scales = NULL;
+    J.nb = nb; J.hkv = hkv; J.bs = bs; J.d = d;
     J.q = q; J.hq = hq; J.cu_q_lens = cu_q_lens; J.context_lens = context_lens;
     J.block_tables = block_tables; J.batch = batch; J.mb = mb; J.scale = scale; J.causal = causal;
-    J.rows = rows; J.n_rows = n_rows; J.out = out; J.lse = lse; J.next = 0; J.status = 0;
+    J.rows = rows; J.n_rows = n_rows; J.out = out; J.lse = lse;
+    return run_attention(&J, nthreads);
+}
+
+/* The same attention over an FP8 cache (q in dtype). */
+int oracle_paged_attention_fp8(int dtype, const uint8_t *codes, const float *scales, int nb, int hkv, int bs,
+                               int d, const uint16_t *q, int hq, const int *cu_q_lens, const int *context_lens,
+                               const int *block_tables, int batch, int mb, double scale, int causal,
+                               const long *rows, long n_rows, double *out, double *lse, int nthreads) {
+    if (hkv <= 0 || hq <= 0 || hq % hkv != 0 || d <= 0 || bs <= 0 || batch < 0) return -2;
+    attn_job J;
+    J.dtype = dtype; J.cache = NULL; J.codes = codes; J.scales = scales;
+    J.nb = nb; J.hkv = hkv; J.bs = bs; J.d = d;
+    J.q = q; J.hq = hq; J.cu_q_lens = cu_q_lens; J.context_lens = context_lens;
+    J.block_tables = block_tables; J.batch = batch; J.mb = mb; J.scale = scale; J.causal = causal;
+    J.rows = rows; J.n_rows = n_rows; J.out = out; J.lse = lse;
+    return run_attention(&J, nthreads);
+}
+
+static int run_attention(attn_job *J0, int nthreads) {
+    attn_job J = *J0;
+    J.next = 0; J.status = 0;
     pthread_mutex_init(&J.lock, NULL);
     if (nthreads < 1) nthreads = 1;
     if (nthreads == 1) {

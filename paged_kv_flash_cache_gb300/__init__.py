@@ -10,7 +10,10 @@ Entry points (same names as the C ABI without the ``pkv_`` prefix):
   kv_cache_append, paged_attn_decode, paged_attn_prefill, attn_combine,
   decode_workspace_size, decode_split_tokens, get_device_error.
 Cache tensors have shape [num_blocks, 2, num_kv_heads, block_size, head_dim]
-(K at index 0, V at index 1) in float16 or bfloat16.
+(K at index 0, V at index 1) in float16 or bfloat16, or hold FP8 E4M3 codes
+(torch.float8_e4m3fn or uint8) with a float32 `scales` tensor
+[num_blocks, 2, num_kv_heads, block_size], one scale per cached row; q, k_new and
+v_new then stay float16 / bfloat16 (see pkv_kv_format in include/pkv.h).
 """
 from __future__ import annotations
 
@@ -34,6 +37,7 @@ _lib = None
 STATUS = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED", 3: "PKV_ERR_WORKSPACE",
           4: "PKV_ERR_CUDA", 5: "PKV_ERR_DEVICE_RANGE", 6: "PKV_ERR_TIMEOUT"}
 F16, BF16, F32 = 0, 1, 2
+KV_NATIVE, KV_FP8_E4M3 = 0, 1
 
 # Every symbol include/pkv.h declares.
 EXPORTS = ("pkv_kv_cache_append", "pkv_decode_workspace_size", "pkv_decode_split_tokens", "pkv_paged_attn_decode",
@@ -50,7 +54,8 @@ class PkvError(RuntimeError):
 
 class _Cache(ctypes.Structure):
     _fields_ = [("ptr", ctypes.c_void_p), ("num_blocks", ctypes.c_int), ("num_kv_heads", ctypes.c_int),
-                ("block_size", ctypes.c_int), ("head_dim", ctypes.c_int), ("dtype", ctypes.c_int)]
+                ("block_size", ctypes.c_int), ("head_dim", ctypes.c_int), ("dtype", ctypes.c_int),
+                ("format", ctypes.c_int), ("scales", ctypes.c_void_p)]
 
 
 def library_path() -> str:
@@ -136,11 +141,27 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
-def _cache_struct(cache) -> _Cache:
+def is_fp8_cache(cache) -> bool:
+    torch = _torch()
+    return cache.dtype == torch.uint8 or cache.dtype == getattr(torch, "float8_e4m3fn", None)
+
+
+def _cache_struct(cache, act_dtype, scales=None) -> _Cache:
+    """The C view of `cache`; act_dtype is the type of q / k_new / v_new."""
+    torch = _torch()
     if cache.dim() != 5 or cache.shape[1] != 2:
         raise ValueError("cache must be [num_blocks, 2, num_kv_heads, block_size, head_dim]")
     nb, _, hkv, bs, d = cache.shape
-    return _Cache(_dev(cache, "cache"), nb, hkv, bs, d, _dtype_code(cache.dtype))
+    if is_fp8_cache(cache):
+        if scales is None or scales.dtype != torch.float32 or tuple(scales.shape) != (nb, 2, hkv, bs):
+            raise ValueError("an FP8 cache needs float32 scales [num_blocks, 2, num_kv_heads, block_size]")
+        return _Cache(_dev(cache, "cache"), nb, hkv, bs, d, _dtype_code(act_dtype), KV_FP8_E4M3,
+                      _dev(scales, "scales"))
+    if scales is not None:
+        raise ValueError("scales are only for an FP8 cache")
+    if act_dtype != cache.dtype:
+        raise TypeError("q / k_new / v_new must have the cache dtype")
+    return _Cache(_dev(cache, "cache"), nb, hkv, bs, d, _dtype_code(cache.dtype), KV_NATIVE, None)
 
 
 def _check(status: int, where: str):
@@ -152,12 +173,13 @@ def _check(status: int, where: str):
 # entry points
 # ---------------------------------------------------------------------------------------------
 
-def kv_cache_append(cache, k_new, v_new, cu_new_lens, ctx_before, block_tables, stream=None) -> None:
-    """Scatter new tokens' K/V ([T_new, Hkv, D], packed by sequence) into their pages."""
+def kv_cache_append(cache, k_new, v_new, cu_new_lens, ctx_before, block_tables, stream=None, scales=None) -> None:
+    """Scatter new tokens' K/V ([T_new, Hkv, D], packed by sequence) into their pages (an FP8
+    cache: quantised, with their row scales written to `scales`)."""
     lib = load_library()
-    c = _cache_struct(cache)
-    if k_new.dtype != cache.dtype or v_new.dtype != cache.dtype or k_new.shape != v_new.shape:
-        raise TypeError("k_new / v_new must match each other and the cache dtype")
+    if k_new.dtype != v_new.dtype or k_new.shape != v_new.shape:
+        raise TypeError("k_new / v_new must match each other")
+    c = _cache_struct(cache, k_new.dtype, scales)
     batch, mb = block_tables.shape
     _check(lib.pkv_kv_cache_append(c, _dev(k_new, "k_new"), _dev(v_new, "v_new"), _i32(cu_new_lens, "cu_new_lens"),
                                    _i32(ctx_before, "ctx_before"), _i32(block_tables, "block_tables"), batch, mb,
@@ -177,15 +199,15 @@ def decode_split_tokens(batch, num_q_heads, num_kv_heads, head_dim, block_size, 
 
 
 def paged_attn_decode(cache, q, block_tables, context_lens, scale: Optional[float] = None, num_splits: int = 0,
-                      workspace=None, out=None, out_dtype=None, lse=None, stream=None):
+                      workspace=None, out=None, out_dtype=None, lse=None, stream=None, scales=None):
     """One query per sequence ([B, Hq, D]) against its paged context. Returns `out`."""
     torch = _torch()
     lib = load_library()
-    c = _cache_struct(cache)
+    c = _cache_struct(cache, q.dtype, scales)
     batch, hq, d = q.shape
     mb = block_tables.shape[1]
     if out is None:
-        out = torch.empty((batch, hq, d), dtype=out_dtype or cache.dtype, device=q.device)
+        out = torch.empty((batch, hq, d), dtype=out_dtype or q.dtype, device=q.device)
     need = decode_workspace_size(batch, hq, cache.shape[2], d, cache.shape[3], mb, num_splits)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -200,7 +222,7 @@ def paged_attn_decode(cache, q, block_tables, context_lens, scale: Optional[floa
 
 
 def paged_attn_decode_noalloc(cache, q, block_tables, context_lens, scale: Optional[float] = None,
-                              num_splits: int = 0, out=None, out_dtype=None, lse=None, stream=None):
+                              num_splits: int = 0, out=None, out_dtype=None, lse=None, stream=None, scales=None):
     """paged_attn_decode without a workspace: for callers that cannot allocate device memory.
     The split partials go to a fixed array the library holds on each device (see
     include/pkv.h); sizes needing more than DECODE_NOALLOC_SCRATCH_BYTES raise PkvError
@@ -208,11 +230,11 @@ def paged_attn_decode_noalloc(cache, q, block_tables, context_lens, scale: Optio
     (allocated here with PyTorch only when the caller passes none)."""
     torch = _torch()
     lib = load_library()
-    c = _cache_struct(cache)
+    c = _cache_struct(cache, q.dtype, scales)
     batch, hq, d = q.shape
     mb = block_tables.shape[1]
     if out is None:
-        out = torch.empty((batch, hq, d), dtype=out_dtype or cache.dtype, device=q.device)
+        out = torch.empty((batch, hq, d), dtype=out_dtype or q.dtype, device=q.device)
     scale = (1.0 / math.sqrt(d)) if scale is None else float(scale)
     _check(lib.pkv_paged_attn_decode_noalloc(c, _dev(q, "q"), hq, _i32(block_tables, "block_tables"),
                                              _i32(context_lens, "context_lens"), batch, mb, scale, int(num_splits),
@@ -223,16 +245,17 @@ def paged_attn_decode_noalloc(cache, q, block_tables, context_lens, scale: Optio
 
 def paged_attn_prefill(cache, q, cu_q_lens, context_lens, block_tables, max_q_len: int,
                        scale: Optional[float] = None, causal: bool = True, out=None, out_dtype=None, lse=None,
-                       stream=None):
+                       stream=None, scales=None):
     """A chunk of queries per sequence ([sum q_len, Hq, D]) against its paged context
-    (the chunk's own K/V already appended). Returns `out`."""
+    (the chunk's own K/V already appended). Returns `out`. An FP8 cache raises PkvError
+    (PKV_ERR_UNSUPPORTED)."""
     torch = _torch()
     lib = load_library()
-    c = _cache_struct(cache)
+    c = _cache_struct(cache, q.dtype, scales)
     total_q, hq, d = q.shape
     batch, mb = block_tables.shape
     if out is None:
-        out = torch.empty((total_q, hq, d), dtype=out_dtype or cache.dtype, device=q.device)
+        out = torch.empty((total_q, hq, d), dtype=out_dtype or q.dtype, device=q.device)
     scale = (1.0 / math.sqrt(d)) if scale is None else float(scale)
     _check(lib.pkv_paged_attn_prefill(c, _dev(q, "q"), hq, _i32(cu_q_lens, "cu_q_lens"),
                                       _i32(context_lens, "context_lens"), _i32(block_tables, "block_tables"), batch,

@@ -10,7 +10,8 @@
 // moves those heads' K rows and V rows as 16-byte vectors. Reads of k_new / v_new are contiguous;
 // each destination head row (D elements) is a contiguous 128 / 256-byte run. Small items keep
 // every SM busy even when a call appends a few thousand tokens.
-// Pure bandwidth: 2 reads + 2 writes of Hkv * D * 2 bytes per token.
+// Pure bandwidth: 2 reads + 2 writes of Hkv * D * 2 bytes per token (an FP8 cache: writes of
+// Hkv * (D + 4) bytes for each of K and V).
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
@@ -100,6 +101,82 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(AppendArgs a) {
     pdl_launch_dependents();
 }
 
+// FP8 cache: the warp's rows (up to 8 heads x K and V of one token) are quantised kRows at a
+// time; D / 8 lanes hold one row (8 elements each), find its largest magnitude by shuffles and
+// write 8 codes each, the row's first lane its scale. All arithmetic in FP32: scale = amax / 448,
+// code = E4M3(x * (448 / amax)) rounded to nearest even and saturated.
+template <int D, typename Tag>
+__global__ void __launch_bounds__(kAppendThreads) append_fp8_kernel(AppendArgs a) {
+    constexpr int kLanesPerRow = D / 8;
+    constexpr int kRows = 32 / kLanesPerRow;  // rows quantised per pass of the warp
+    const int lane = threadIdx.x & 31;
+    const int sub = lane / kLanesPerRow, chk = lane % kLanesPerRow;
+    const int warps_total = gridDim.x * (kAppendThreads / 32);
+    const int hkv = a.num_kv_heads;
+    const int chunks = (hkv + kHeadsPerItem - 1) / kHeadsPerItem;
+    const long long items = (long long)a.num_new_tokens * chunks;
+    const uint4 *kn = static_cast<const uint4 *>(a.k_new);
+    const uint4 *vn = static_cast<const uint4 *>(a.v_new);
+    uint8_t *codes = static_cast<uint8_t *>(a.cache);
+
+    pdl_wait();  // the previous kernel may still read the pages this call writes
+    for (long long it = (long long)blockIdx.x * (kAppendThreads / 32) + (threadIdx.x >> 5); it < items;
+         it += warps_total) {
+        const int t = (int)(it / chunks);
+        const int h0 = (int)(it - (long long)t * chunks) * kHeadsPerItem;
+        const int nh = min(kHeadsPerItem, hkv - h0);
+        int lo = 0, hi = a.batch;  // sequence of token t: last b with cu_new_lens[b] <= t
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (__ldg(a.cu_new_lens + mid) <= t) lo = mid; else hi = mid;
+        }
+        const int b = lo;
+        const long long pos = (long long)__ldg(a.ctx_before + b) + (t - __ldg(a.cu_new_lens + b));
+        const long long logical = pos >> a.log2_block_size;
+        if (pos < 0 || logical >= a.max_blocks_per_seq) {
+            if (lane == 0) set_error(a.err, kErrDeviceRange);
+            continue;
+        }
+        const int pb = __ldg(a.block_tables + (size_t)b * a.max_blocks_per_seq + logical);
+        if (pb < 0 || pb >= a.num_blocks) {
+            if (lane == 0) set_error(a.err, kErrDeviceRange);
+            continue;
+        }
+        const int off = (int)(pos & (a.block_size - 1));
+        for (int r0 = 0; r0 < 2 * nh; r0 += kRows) {
+            const int r = r0 + sub;  // row r: K (r < nh) or V of head h0 + r % nh
+            const bool active = r < 2 * nh;
+            const int kv = active && r >= nh ? 1 : 0;
+            const int h = h0 + (active ? r - kv * nh : 0);
+            float2 f[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                           make_float2(0.f, 0.f)};
+            if (active) {
+                const uint4 raw = ld_stream((kv ? vn : kn) + ((size_t)t * hkv + h) * kLanesPerRow + chk);
+                unpack8x2(raw, f, Tag());
+            }
+            float amax = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) amax = fmaxf(amax, fmaxf(fabsf(f[j].x), fabsf(f[j].y)));
+#pragma unroll
+            for (int o = kLanesPerRow / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            if (active) {
+                const size_t row = (((size_t)pb * 2 + kv) * hkv + h) * a.block_size + off;
+                uint2 c = make_uint2(0u, 0u);
+                float scale = 0.f;
+                if (amax > 0.f) {
+                    scale = amax / 448.0f;
+                    const float inv = 448.0f / amax;
+                    c.x = pack_e4m3x2(f[0].x * inv, f[0].y * inv) | (pack_e4m3x2(f[1].x * inv, f[1].y * inv) << 16);
+                    c.y = pack_e4m3x2(f[2].x * inv, f[2].y * inv) | (pack_e4m3x2(f[3].x * inv, f[3].y * inv) << 16);
+                }
+                *reinterpret_cast<uint2 *>(codes + row * D + chk * 8) = c;
+                if (chk == 0) a.scales[row] = scale;
+            }
+        }
+    }
+    pdl_launch_dependents();
+}
+
 }  // namespace
 
 cudaError_t launch_append(const AppendArgs &a, cudaStream_t s) {
@@ -109,6 +186,14 @@ cudaError_t launch_append(const AppendArgs &a, cudaStream_t s) {
     const long long want = (items + warps_per_cta - 1) / warps_per_cta;
     const int cap = device_info().num_sms * 8;
     const int grid = want < cap ? (int)want : cap;
+    if (a.fp8) {
+        if (a.dtype == 1) {
+            if (a.head_dim == 128) return launch_pdl(append_fp8_kernel<128, BF16Tag>, dim3(grid), dim3(kAppendThreads), 0, s, a);
+            return launch_pdl(append_fp8_kernel<64, BF16Tag>, dim3(grid), dim3(kAppendThreads), 0, s, a);
+        }
+        if (a.head_dim == 128) return launch_pdl(append_fp8_kernel<128, F16Tag>, dim3(grid), dim3(kAppendThreads), 0, s, a);
+        return launch_pdl(append_fp8_kernel<64, F16Tag>, dim3(grid), dim3(kAppendThreads), 0, s, a);
+    }
     if (a.head_dim == 128) return launch_pdl(append_kernel<128>, dim3(grid), dim3(kAppendThreads), 0, s, a);
     return launch_pdl(append_kernel<64>, dim3(grid), dim3(kAppendThreads), 0, s, a);
 }

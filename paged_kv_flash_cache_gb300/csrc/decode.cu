@@ -49,17 +49,19 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
-template <int D, int G>
+template <int D, int G, bool FP8>
 struct DecodeLayout {
     static constexpr int kTile = kDecodeTile;
+    static constexpr int kKB = FP8 ? 1 : 2;                        // bytes per cached element
     static constexpr int kTokPerWarp = kTile / kConsumerWarps;      // 8
     static constexpr int kLanesPerTok = D / 8;                      // 16 (D=128) or 8 (D=64)
     static constexpr int kTokPerStep = 32 / kLanesPerTok;           // 2 or 4
     static constexpr int kSteps = kTokPerWarp / kTokPerStep;        // 4 or 2
     static constexpr int kStepsPerBatch = (kSteps * G <= 16) ? kSteps : (16 / G);  // bounds registers
-    static constexpr size_t kKBytes = (size_t)kTile * D * 2;
+    static constexpr size_t kKBytes = (size_t)kTile * D * kKB;
     static constexpr size_t kQBytes = (size_t)G * D * 2;
-    static constexpr size_t kStageBytes = ((2 * kKBytes + kQBytes) + 127) / 128 * 128;
+    static constexpr size_t kSOffset = 2 * kKBytes + kQBytes;  // FP8: K row scales [kTile], V row scales [kTile]
+    static constexpr size_t kStageBytes = ((kSOffset + (FP8 ? 2 * kTile * 4 : 0)) + 127) / 128 * 128;
     static constexpr size_t kMergeFloats = (size_t)kConsumerWarps * G * (D + 2);
     static constexpr size_t kBarOffset = kStages * kStageBytes;
     // barriers: full / empty per stage, merge full / empty per merge buffer; then the abort flag
@@ -75,9 +77,26 @@ struct DecodeLayout {
     static size_t smem_bytes(int batch, int s_max) { return kIntsOffset + unit_table_ints(batch, s_max) * 4; }
 };
 
-template <typename Tag, int D, int G>
+// This lane's 8 elements (chunk chk) of row t of a stage's K or V tile, as fp32 pairs.
+template <typename Tag, int D, bool FP8>
+__device__ __forceinline__ void load_row8(const uint8_t *tile, int t, int chk, float2 (&f)[4]) {
+    if constexpr (FP8) {
+        unpack_e4m3x8(*reinterpret_cast<const uint2 *>(tile + (size_t)t * D + chk * 8), f);
+    } else {
+        unpack8x2(*reinterpret_cast<const uint4 *>(tile + ((size_t)t * D + chk * 8) * 2), f, Tag());
+    }
+}
+
+// Scale of row t of a tile (FP8 cache), 1 for a native cache.
+template <bool FP8>
+__device__ __forceinline__ float row_scale(const float *scales, int t) {
+    if constexpr (FP8) return scales[t];
+    else return 1.f;
+}
+
+template <typename Tag, int D, int G, bool FP8>
 __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeArgs a) {
-    using L = DecodeLayout<D, G>;
+    using L = DecodeLayout<D, G, FP8>;
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kBarOffset);
     uint64_t *empty = full + kStages;
@@ -113,9 +132,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
     if (warp == kProducerWarp) {
         // ================================ producer warp ================================
         const uint64_t pol = l2_policy_evict_first();
-        const uint16_t *cache = static_cast<const uint16_t *>(a.cache.ptr);
+        const uint8_t *cache = static_cast<const uint8_t *>(a.cache.ptr);
         const uint16_t *qg = static_cast<const uint16_t *>(a.q);
-        const size_t head_elems = (size_t)bs * D;
+        const size_t head_bytes = (size_t)bs * D * L::kKB;
         int stage = 0;
         uint32_t phase = 0;
         uint32_t issued_mask = 0;  // stages with copies issued (bit i), for the abort drain
@@ -166,7 +185,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
                 const bool first_tile = (ts == c.t0);
                 if (lane == 0) {
                     stage_unit[stage] = u;
-                    const uint32_t bytes = (uint32_t)n * D * 2 * 2 + (first_tile ? (uint32_t)L::kQBytes : 0u);
+                    uint32_t bytes = (uint32_t)n * D * L::kKB * 2 + (first_tile ? (uint32_t)L::kQBytes : 0u);
+                    if constexpr (FP8) {
+                        // row scales, each page slice's copy rounded up to 4 rows (16 bytes)
+                        for (int lp = first_page; lp <= last_page; ++lp) {
+                            const int m = min(ts + n, (lp + 1) * bs) - max(ts, lp * bs);
+                            bytes += 2u * (uint32_t)((m + 3) & ~3) * 4u;
+                        }
+                    }
                     mbar_arrive_expect_tx(&full[stage], bytes);
                 }
                 __syncwarp();
@@ -175,12 +201,21 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
                     const int tok_lo = max(ts, lp * bs);
                     const int tok_hi = min(ts + n, (lp + 1) * bs);
                     const int off = tok_lo - lp * bs;
-                    const uint32_t bytes = (uint32_t)(tok_hi - tok_lo) * D * 2;
-                    const size_t kbase = (((size_t)pb * 2) * hkv + c.kvh) * head_elems + (size_t)off * D;
-                    const size_t vbase = kbase + (size_t)hkv * head_elems;
-                    uint8_t *dk = st + (size_t)(tok_lo - ts) * D * 2;
+                    const uint32_t bytes = (uint32_t)(tok_hi - tok_lo) * D * L::kKB;
+                    const size_t kbase = (((size_t)pb * 2) * hkv + c.kvh) * head_bytes + (size_t)off * D * L::kKB;
+                    const size_t vbase = kbase + (size_t)hkv * head_bytes;
+                    uint8_t *dk = st + (size_t)(tok_lo - ts) * D * L::kKB;
                     bulk_g2s(dk, cache + kbase, bytes, &full[stage], pol);
                     bulk_g2s(dk + L::kKBytes, cache + vbase, bytes, &full[stage], pol);
+                    if constexpr (FP8) {
+                        // off and tok_lo - ts are multiples of 4 rows, and a page holds a multiple
+                        // of 4 rows, so the rounded-up copy stays inside the page's scale row
+                        const float *ksrc = a.cache.scales + (((size_t)pb * 2) * hkv + c.kvh) * bs + off;
+                        const uint32_t sbytes = (uint32_t)((tok_hi - tok_lo + 3) & ~3) * 4u;
+                        uint8_t *ds = st + L::kSOffset + (size_t)(tok_lo - ts) * 4;
+                        bulk_g2s(ds, ksrc, sbytes, &full[stage], pol);
+                        bulk_g2s(ds + L::kTile * 4, ksrc + (size_t)hkv * bs, sbytes, &full[stage], pol);
+                    }
                 }
                 if (first_tile && lane == 0) {
                     const uint16_t *qsrc = qg + ((size_t)c.b * a.num_q_heads + (size_t)c.kvh * G) * D;
@@ -265,6 +300,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
             if constexpr (G == 1) {
             const uint8_t *sk = st;
             const uint8_t *sv = st + L::kKBytes;
+            const float *ksc = reinterpret_cast<const float *>(st + L::kSOffset);  // FP8 row scales
+            const float *vsc = ksc + L::kTile;
+            (void)ksc; (void)vsc;
 #pragma unroll
             for (int b0 = 0; b0 < L::kSteps; b0 += L::kStepsPerBatch) {
                 float s[L::kStepsPerBatch][G];
@@ -273,9 +311,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
                 for (int i = 0; i < L::kStepsPerBatch; ++i) {
                     const int t = warp * L::kTokPerWarp + (b0 + i) * L::kTokPerStep + slot;
                     valid[i] = t < n;
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(sk + ((size_t)t * D + chk * 8) * 2);
                     float2 kf[4];
-                    unpack8x2(raw, kf, Tag());
+                    load_row8<Tag, D, FP8>(sk, t, chk, kf);
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
                         float2 pp = fmul2(qf[g][0], kf[0]);
@@ -285,7 +322,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
 #pragma unroll
                         for (int o = L::kLanesPerTok / 2; o > 0; o >>= 1)
                             part += __shfl_xor_sync(0xffffffffu, part, o);
-                        s[i][g] = valid[i] ? part : -INFINITY;
+                        s[i][g] = valid[i] ? part * row_scale<FP8>(ksc, t) : -INFINITY;
                     }
                 }
 #pragma unroll
@@ -313,12 +350,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
                 for (int i = 0; i < L::kStepsPerBatch; ++i) {
                     if (!valid[i]) continue;
                     const int t = warp * L::kTokPerWarp + (b0 + i) * L::kTokPerStep + slot;
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(sv + ((size_t)t * D + chk * 8) * 2);
                     float2 vf[4];
-                    unpack8x2(raw, vf, Tag());
+                    load_row8<Tag, D, FP8>(sv, t, chk, vf);
+                    const float vs = row_scale<FP8>(vsc, t);
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
-                        const float2 p2 = make_float2(s[i][g], s[i][g]);
+                        const float pv = s[i][g] * vs;
+                        const float2 p2 = make_float2(pv, pv);
 #pragma unroll
                         for (int j = 0; j < 4; ++j) acc[g][j] = ffma2(p2, vf[j], acc[g][j]);
                     }
@@ -327,6 +365,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
             } else {
             const uint8_t *sk = st;
             const uint8_t *sv = st + L::kKBytes;
+            const float *ksc = reinterpret_cast<const float *>(st + L::kSOffset);  // FP8 row scales
+            const float *vsc = ksc + L::kTile;
+            (void)ksc; (void)vsc;
 #pragma unroll
             for (int b0 = 0; b0 < L::kSteps; b0 += L::kGqaSteps) {
                 constexpr int S = L::kGqaSteps, N = L::kGqaN, R = L::kLanesPerTok;
@@ -335,9 +376,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
 #pragma unroll
                 for (int i = 0; i < S; ++i) {
                     const int t = warp * L::kTokPerWarp + (b0 + i) * L::kTokPerStep + slot;
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(sk + ((size_t)t * D + chk * 8) * 2);
                     float2 kf[4];
-                    unpack8x2(raw, kf, Tag());
+                    load_row8<Tag, D, FP8>(sk, t, chk, kf);
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
                         float2 pp = fmul2(qf[g][0], kf[0]);
@@ -367,7 +407,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
                     }
                 }
                 const int tok_own = warp * L::kTokPerWarp + (b0 + k_own / G) * L::kTokPerStep + slot;
-                const float s_own = (tok_own < n) ? v[0] : -INFINITY;
+                const float s_own = (tok_own < n) ? v[0] * row_scale<FP8>(ksc, tok_own) : -INFINITY;
                 // batch max of this lane's head over the S steps (the first log2(S) lane bits)
                 float mb = s_own;
 #pragma unroll
@@ -401,12 +441,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
                 for (int i = 0; i < S; ++i) {
                     const int t = warp * L::kTokPerWarp + (b0 + i) * L::kTokPerStep + slot;
                     if (t >= n) continue;
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(sv + ((size_t)t * D + chk * 8) * 2);
                     float2 vf[4];
-                    unpack8x2(raw, vf, Tag());
+                    load_row8<Tag, D, FP8>(sv, t, chk, vf);
+                    const float vs = row_scale<FP8>(vsc, t);
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
-                        const float pg = pbuf[i * G + g];
+                        const float pg = pbuf[i * G + g] * vs;
                         const float2 p2 = make_float2(pg, pg);
 #pragma unroll
                         for (int j = 0; j < 4; ++j) acc[g][j] = ffma2(p2, vf[j], acc[g][j]);
@@ -548,15 +588,15 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
     if (lane == 0 && a.lse) a.lse[row] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
 }
 
-template <typename Tag, int D, int G>
+template <typename Tag, int D, int G, bool FP8>
 cudaError_t launch_decode_t(const DecodeArgs &a, int grid, cudaStream_t s) {
-    const size_t smem = DecodeLayout<D, G>::smem_bytes(a.batch, a.s_max);
-    auto kern = decode_split_kernel<Tag, D, G>;
+    const size_t smem = DecodeLayout<D, G, FP8>::smem_bytes(a.batch, a.s_max);
+    auto kern = decode_split_kernel<Tag, D, G, FP8>;
     // opt in to the largest size this kernel can ask for, once per device
     static unsigned int configured = 0;
     const int dev = device_info().device;
     if (dev < 32 && !(configured & (1u << dev))) {
-        const int max_smem = (int)DecodeLayout<D, G>::smem_bytes(kMaxBatch, kDecodeMaxSplits);
+        const int max_smem = (int)DecodeLayout<D, G, FP8>::smem_bytes(kMaxBatch, kDecodeMaxSplits);
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
         if (e != cudaSuccess) return e;
         configured |= 1u << dev;
@@ -569,9 +609,18 @@ cudaError_t launch_decode_t(const DecodeArgs &a, int grid, cudaStream_t s) {
 
 template <typename Tag, int D>
 cudaError_t dispatch_group(const DecodeArgs &a, int grid, cudaStream_t s) {
+    if (a.cache.fp8) {
+        switch (a.num_q_heads / a.cache.num_kv_heads) {
+            case 1: return launch_decode_t<Tag, D, 1, true>(a, grid, s);
+            case 2: return launch_decode_t<Tag, D, 2, true>(a, grid, s);
+            case 4: return launch_decode_t<Tag, D, 4, true>(a, grid, s);
+            case 8: return launch_decode_t<Tag, D, 8, true>(a, grid, s);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     switch (a.num_q_heads / a.cache.num_kv_heads) {
-        case 1: return launch_decode_t<Tag, D, 1>(a, grid, s);
-        case 2: return launch_decode_t<Tag, D, 2>(a, grid, s);
+        case 1: return launch_decode_t<Tag, D, 1, false>(a, grid, s);
+        case 2: return launch_decode_t<Tag, D, 2, false>(a, grid, s);
         default: return cudaErrorInvalidValue;  // four or more heads per KV head: decode_gqa.cu
     }
 }

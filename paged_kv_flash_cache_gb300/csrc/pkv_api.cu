@@ -59,6 +59,8 @@ DeviceSlot &slot() {
 pkv_status check_cache(const pkv_cache &c) {
     if (!c.ptr || !aligned16(c.ptr)) return PKV_ERR_INVALID_ARG;
     if (c.num_blocks < 0 || c.num_kv_heads <= 0 || c.block_size <= 0 || c.head_dim <= 0) return PKV_ERR_INVALID_ARG;
+    if (c.format != PKV_KV_NATIVE && c.format != PKV_KV_FP8_E4M3) return PKV_ERR_UNSUPPORTED;
+    if (c.format == PKV_KV_FP8_E4M3 && (!c.scales || !aligned16(c.scales))) return PKV_ERR_INVALID_ARG;
     if (c.dtype != PKV_F16 && c.dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
     if (c.head_dim != 64 && c.head_dim != 128) return PKV_ERR_UNSUPPORTED;
     if (!is_pow2(c.block_size) || c.block_size < 8 || c.block_size > 512) return PKV_ERR_UNSUPPORTED;
@@ -79,6 +81,8 @@ CacheView view_of(const pkv_cache &c) {
     v.log2_block_size = ilog2(c.block_size);
     v.head_dim = c.head_dim;
     v.dtype = (int)c.dtype;
+    v.fp8 = c.format == PKV_KV_FP8_E4M3 ? 1 : 0;
+    v.scales = v.fp8 ? c.scales : nullptr;
     return v;
 }
 
@@ -115,7 +119,7 @@ using namespace pkv;
 
 extern "C" {
 
-int pkv_version(void) { return 100; }
+int pkv_version(void) { return 101; }
 
 const char *pkv_status_string(pkv_status s) {
     switch (s) {
@@ -147,6 +151,9 @@ pkv_status pkv_kv_cache_append(pkv_cache cache, const void *k_new, const void *v
     a.block_size = cache.block_size;
     a.log2_block_size = ilog2(cache.block_size);
     a.head_dim = cache.head_dim;
+    a.dtype = (int)cache.dtype;
+    a.fp8 = cache.format == PKV_KV_FP8_E4M3 ? 1 : 0;
+    a.scales = a.fp8 ? cache.scales : nullptr;
     a.k_new = k_new;
     a.v_new = v_new;
     a.cu_new_lens = cu_new_lens;
@@ -221,8 +228,10 @@ pkv_status pkv_paged_attn_decode(pkv_cache cache, const void *q, int num_q_heads
     a.err = s.err_ptr;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const int grid = s.info.num_sms * s.info.decode_ctas_per_sm;
-    // four or more query heads per KV head: the group's products run on tensor cores
-    const cudaError_t le = group >= 4 ? launch_decode_gqa(a, grid, cs) : launch_decode(a, grid, cs);
+    // four or more query heads per KV head of a native cache: the group kernel (tensor cores);
+    // an FP8 cache decodes on the CUDA-core kernel for every grouping
+    const cudaError_t le =
+        (group >= 4 && !a.cache.fp8) ? launch_decode_gqa(a, grid, cs) : launch_decode(a, grid, cs);
     if (le != cudaSuccess) return PKV_ERR_CUDA;
     // Rows that span several splits (and empty rows) are finished by the merge.
     CombineArgs c;
@@ -271,6 +280,7 @@ pkv_status pkv_paged_attn_prefill(pkv_cache cache, const void *q, int num_q_head
                                   void *out, pkv_dtype out_dtype, float *lse, void *stream) {
     pkv_status st = check_cache(cache);
     if (st != PKV_OK) return st;
+    if (cache.format != PKV_KV_NATIVE) return PKV_ERR_UNSUPPORTED;
     if ((st = check_out_dtype(out_dtype, cache.dtype)) != PKV_OK) return st;
     if (batch < 0 || max_blocks_per_seq <= 0 || num_q_heads <= 0 || total_q < 0 || max_q_len < 0)
         return PKV_ERR_INVALID_ARG;

@@ -166,6 +166,31 @@ __device__ __forceinline__ void unpack8x2(const uint4 &raw, float2 (&f)[4], BF16
     for (int i = 0; i < 4; ++i) f[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
 }
 
+// OCP FP8 E4M3 codes, one byte per element, in increasing element order. Eight codes (one
+// 8-byte load) to four fp32 pairs: every E4M3 value is exact in fp16, and fp16 in fp32.
+__device__ __forceinline__ void unpack_e4m3x8(const uint2 &raw, float2 (&f)[4]) {
+    const uint32_t w[2] = {raw.x, raw.y};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        uint32_t lo, hi;
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(lo) : "h"((unsigned short)(w[i] & 0xffffu)));
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hi) : "h"((unsigned short)(w[i] >> 16)));
+        __half2 h0, h1;
+        memcpy(&h0, &lo, 4);
+        memcpy(&h1, &hi, 4);
+        f[2 * i] = __half22float2(h0);
+        f[2 * i + 1] = __half22float2(h1);
+    }
+}
+
+// Two fp32 values to two E4M3 codes (round to nearest even, magnitudes beyond 448 saturated);
+// x0 goes to the low byte.
+__device__ __forceinline__ uint32_t pack_e4m3x2(float x0, float x1) {
+    unsigned short r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(x1), "f"(x0));
+    return r;
+}
+
 // Paired FP32 arithmetic of sm_100-class GPUs (one instruction for two lanes of a float2).
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
     float2 d;

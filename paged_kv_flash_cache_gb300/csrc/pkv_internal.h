@@ -14,12 +14,17 @@ namespace pkv {
 struct CacheView {
     const void *ptr;
     int num_blocks, num_kv_heads, block_size, log2_block_size, head_dim;
-    int dtype;  // 0 fp16, 1 bf16
+    int dtype;  // 0 fp16, 1 bf16: q / k_new / v_new, and the elements of a native cache
+    int fp8;    // 1: ptr holds E4M3 codes and `scales` one FP32 scale per row
+    const float *scales;
 };
 
 struct AppendArgs {
     void *cache;
     int num_blocks, num_kv_heads, block_size, log2_block_size, head_dim;
+    int dtype;      // type of k_new / v_new
+    int fp8;        // 1: quantise into E4M3 codes + per-row scales
+    float *scales;
     const void *k_new, *v_new;
     const int *cu_new_lens, *ctx_before, *block_tables;
     int batch, max_blocks_per_seq, num_new_tokens;

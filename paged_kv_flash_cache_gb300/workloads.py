@@ -145,7 +145,8 @@ class PagedProblem:
     sequence order; they are appended into the pool by `kv_cache_append` with
     ctx_before = 0. q holds [sum(q_len_b), Hq, D]; decode has q_len_b = 1.
     `pool_init` is the pool's content before any append (seeded noise, so a
-    wrong page read changes the result).
+    wrong page read changes the result); for an FP8 cache it is the pair
+    (codes uint8 [NB, 2, Hkv, bs, D], scales float32 [NB, 2, Hkv, bs]).
     """
     name: str
     dtype: str
@@ -165,6 +166,7 @@ class PagedProblem:
     causal: bool
     scale: float
     meta: dict = field(default_factory=dict)
+    kv_format: str = "native"           # "fp8": the cache holds E4M3 codes + per-row FP32 scales
 
     @property
     def max_blocks_per_seq(self) -> int:
@@ -207,12 +209,24 @@ def _pool_noise(gen: torch.Generator, nb: int, hkv: int, bs: int, d: int, dtype:
     return page.expand(nb, 2, hkv, bs, d).clone()
 
 
+def _pool_noise_fp8(gen: torch.Generator, nb: int, hkv: int, bs: int, d: int, cheap: bool):
+    """Noise for an FP8 pool: random E4M3 codes (the two NaN codes replaced by 0) and scales."""
+    n = 1 if cheap else nb
+    codes = torch.randint(0, 256, (n, 2, hkv, bs, d), generator=gen, dtype=torch.int32, device=gen.device)
+    codes = torch.where((codes & 0x7F) == 0x7F, torch.zeros_like(codes), codes).to(torch.uint8)
+    scales = (torch.rand((n, 2, hkv, bs), generator=gen, device=gen.device) * 0.05 + 1e-3).to(torch.float32)
+    if cheap:
+        codes = codes.expand(nb, 2, hkv, bs, d).clone()
+        scales = scales.expand(nb, 2, hkv, bs).clone()
+    return codes, scales
+
+
 def make_problem(name: str, *, batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
                  block_size: int, context_lens: Sequence[int], q_lens: Sequence[int], dtype: str,
                  causal: bool, seed: int, num_blocks: Optional[int] = None,
                  free_order: Optional[Sequence[int]] = None, tables: Optional[List[List[int]]] = None,
                  max_blocks_per_seq: Optional[int] = None, pool_init: str = "noise",
-                 kv_data=None, scale: Optional[float] = None, device="cpu") -> PagedProblem:
+                 kv_data=None, scale: Optional[float] = None, device="cpu", kv_format: str = "native") -> PagedProblem:
     gen = torch.Generator().manual_seed(seed)
     dgen = data_generator(seed, device)
     context_lens = [int(x) for x in context_lens]
@@ -237,8 +251,12 @@ def make_problem(name: str, *, batch: int, num_q_heads: int, num_kv_heads: int, 
         k_ctx = randn_t(dgen, (total, num_kv_heads, head_dim), dtype)
         v_ctx = randn_t(dgen, (total, num_kv_heads, head_dim), dtype)
     q = randn_t(dgen, (sum(q_lens), num_q_heads, head_dim), dtype)
+    if kv_format not in ("native", "fp8"):
+        raise ValueError("kv_format must be 'native' or 'fp8'")
     if pool_init == "none":
         pool = None
+    elif kv_format == "fp8":
+        pool = _pool_noise_fp8(dgen, num_blocks, num_kv_heads, block_size, head_dim, pool_init == "cheap")
     else:
         pool = _pool_noise(dgen, num_blocks, num_kv_heads, block_size, head_dim, dtype, pool_init == "cheap")
     return PagedProblem(
@@ -247,7 +265,7 @@ def make_problem(name: str, *, batch: int, num_q_heads: int, num_kv_heads: int, 
         context_lens=torch.tensor(context_lens, dtype=torch.int32),
         q_lens=torch.tensor(q_lens, dtype=torch.int32), block_tables=bt, k_ctx=k_ctx, v_ctx=v_ctx,
         q=q, pool_init=pool, causal=causal,
-        scale=(1.0 / math.sqrt(head_dim)) if scale is None else float(scale))
+        scale=(1.0 / math.sqrt(head_dim)) if scale is None else float(scale), kv_format=kv_format)
 
 
 # --------------------------------------------------------------------------------------
@@ -280,9 +298,9 @@ def tiny(seed: int = 1235, chunk: int = 48):
 
 
 def decode_7b(seed: int = 1236, batch: int = 16, lo: int = 1024, hi: int = 8192, pool_init: str = "cheap",
-              block_size: int = 16, dtype: str = F16, device="cpu") -> PagedProblem:
+              block_size: int = 16, dtype: str = F16, device="cpu", kv_format: str = "native") -> PagedProblem:
     """7B-like decode: 32 heads x 128, contexts uniform in [lo, hi], pool 1.2x the pages needed,
-    pages handed out in a seeded random order."""
+    pages handed out in a seeded random order (kv_format "fp8": the same tokens into an FP8 cache)."""
     gen = torch.Generator().manual_seed(seed)
     lens = torch.randint(lo, hi + 1, (batch,), generator=gen).tolist()
     pages = sum((L + block_size - 1) // block_size for L in lens)
@@ -291,7 +309,7 @@ def decode_7b(seed: int = 1236, batch: int = 16, lo: int = 1024, hi: int = 8192,
     return make_problem("decode_7b", batch=batch, num_q_heads=32, num_kv_heads=32, head_dim=128,
                         block_size=block_size, context_lens=lens, q_lens=[1] * batch, dtype=dtype,
                         causal=False, seed=seed + 1, num_blocks=nb, free_order=order, pool_init=pool_init,
-                        max_blocks_per_seq=(hi + block_size - 1) // block_size, device=device)
+                        max_blocks_per_seq=(hi + block_size - 1) // block_size, device=device, kv_format=kv_format)
 
 
 def prefill_long(seed: int = 1237, batch: int = 4, seq: int = 8192, chunk: int = 512, heads: int = 32,

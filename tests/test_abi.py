@@ -31,7 +31,7 @@ def test_header_declares_the_binding_exports():
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_symbols():
         assert hasattr(lib, name), name
-    assert lib.pkv_version() == 100
+    assert lib.pkv_version() == 101
     assert lib.pkv_status_string(0) == b"PKV_OK"
     assert lib.pkv_status_string(3) == b"PKV_ERR_WORKSPACE"
 
@@ -44,8 +44,8 @@ def test_only_c_abi_symbols_are_exported(lib):
     assert ours == sorted(pkv.EXPORTS)
 
 
-def _cache(ptr=16, nb=4, hkv=2, bs=16, d=128, dt=0):
-    return pkv._Cache(ctypes.c_void_p(ptr), nb, hkv, bs, d, dt)
+def _cache(ptr=16, nb=4, hkv=2, bs=16, d=128, dt=0, fmt=0, scales=None):
+    return pkv._Cache(ctypes.c_void_p(ptr), nb, hkv, bs, d, dt, fmt, None if scales is None else ctypes.c_void_p(scales))
 
 
 def test_host_validation_without_gpu(lib):
@@ -77,6 +77,24 @@ def test_host_validation_without_gpu(lib):
     # combine: bad head_dim, bad split count
     assert lib.pkv_attn_combine(good, good, 4, 2, 96, good, 2, None, None) == 2
     assert lib.pkv_attn_combine(good, good, 4, 0, 128, good, 2, None, None) == 1
+
+
+def test_fp8_cache_validation_without_gpu(lib):
+    P = ctypes.c_void_p
+    F = ctypes.c_float
+    good = P(4096)
+    # FP8 cache without scales, with misaligned scales, with an unknown format
+    assert lib.pkv_kv_cache_append(_cache(fmt=1), good, good, good, good, good, 1, 4, 3, None) == 1
+    assert lib.pkv_kv_cache_append(_cache(fmt=1, scales=4100), good, good, good, good, good, 1, 4, 3, None) == 1
+    assert lib.pkv_kv_cache_append(_cache(fmt=7, scales=4096), good, good, good, good, good, 1, 4, 3, None) == 2
+    # nothing to append: accepted, nothing launched
+    assert lib.pkv_kv_cache_append(_cache(fmt=1, scales=4096), good, good, good, good, good, 1, 4, 0, None) == 0
+    # prefill over an FP8 cache is not supported
+    assert lib.pkv_paged_attn_prefill(_cache(fmt=1, scales=4096), good, 2, good, good, good, 1, 4, 8, 4, F(0.1), 1,
+                                      good, 0, None, None) == 2
+    # decode: the activation dtype must still be fp16 / bf16
+    args = (_cache(fmt=1, scales=4096, dt=2), good, 2, good, good, 2, 4, F(0.1), 0, good, 1 << 20, good, 0, None, None)
+    assert lib.pkv_paged_attn_decode(*args) == 2
 
 
 def test_workspace_sizing_with_explicit_splits(lib):

@@ -1,0 +1,170 @@
+"""GPU parity for the FP8 cache (E4M3 codes with one FP32 scale per cached row) through the C ABI:
+the quantising append is bit-exact against the oracle (codes and scales, every pool element), and
+decode over the FP8 cache matches the oracle's attention over the exactly dequantised values
+within the stated tolerances, for every head grouping, block sizes 8..512, splits and FP32 output."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_flash_cache_gb300 as pkv
+from paged_kv_flash_cache_gb300 import workloads as W
+from tests.helpers import check_close, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from paged_kv_flash_cache_gb300 import build
+    build.build()
+    oracle.build()
+    assert torch.cuda.is_available()
+
+
+def problem(*, lens, hq=8, hkv=8, d=128, bs=16, dtype=W.BF16, seed=5, extra=7, mb=None, kv_data=None):
+    nb = sum((L + bs - 1) // bs for L in lens) + extra
+    order = torch.randperm(nb, generator=torch.Generator().manual_seed(seed + 9)).tolist()
+    return W.make_problem("f", batch=len(lens), num_q_heads=hq, num_kv_heads=hkv, head_dim=d, block_size=bs,
+                          context_lens=lens, q_lens=[1] * len(lens), dtype=dtype, causal=False, seed=seed,
+                          num_blocks=nb, free_order=order, max_blocks_per_seq=mb, kv_format="fp8", kv_data=kv_data)
+
+
+def device_fp8(p):
+    """Pool noise on the device, then every context token appended by the library."""
+    codes, scales = p.pool_init
+    codes, scales = codes.cuda().contiguous(), scales.cuda().contiguous()
+    pkv.kv_cache_append(codes, to_dev(p.k_ctx), to_dev(p.v_ctx), to_dev(p.cu_ctx_lens),
+                        torch.zeros(p.batch, dtype=torch.int32, device="cuda"), to_dev(p.block_tables),
+                        scales=scales)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    return codes, scales
+
+
+def host(codes, scales):
+    return oracle.Fp8Cache(codes.cpu().numpy().copy(), scales.cpu().numpy().copy())
+
+
+def decode(p, codes, scales, num_splits=0, out_dtype=None):
+    lse = torch.empty((p.batch, p.num_q_heads), dtype=torch.float32, device="cuda")
+    out = pkv.paged_attn_decode(codes, to_dev(p.q), to_dev(p.block_tables), to_dev(p.context_lens), scale=p.scale,
+                                num_splits=num_splits, out_dtype=out_dtype, lse=lse, scales=scales)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    return out, lse
+
+
+@pytest.mark.parametrize("bs", [8, 16, 128])
+@pytest.mark.parametrize("d,dtype", [(128, W.BF16), (64, W.F16)])
+def test_fp8_append_bit_exact(bs, d, dtype):
+    p = problem(lens=[1, 37, 100, 513], bs=bs, d=d, dtype=dtype, hq=4, hkv=4)
+    codes, scales = device_fp8(p)
+    ref = oracle.build_cache(p)
+    got = host(codes, scales)
+    assert np.array_equal(got.codes, ref.codes)
+    assert np.array_equal(got.scales.view(np.uint32), ref.scales.view(np.uint32))
+
+
+def test_fp8_append_special_rows():
+    """Zero rows, rows of +-0, huge and tiny magnitudes, ties of the scaled values."""
+    d, hkv = 128, 3
+    k = torch.randn(6, hkv, d, generator=torch.Generator().manual_seed(1))
+    k[0] = 0.0
+    k[1] = -0.0
+    k[2, 0] = 60000.0
+    k[3] = k[3] * 1e-6
+    k[4, 1, :8] = torch.tensor([448.0, 1.0625, 1.1875, -3.0, 2.0 ** -10, 0.0, -0.0, 7.0])
+    k = k.to(torch.float16)
+    v = torch.flip(k, dims=[0]).contiguous()
+    p = problem(lens=[6], hq=hkv, hkv=hkv, d=d, bs=8, dtype=W.F16, kv_data=(k, v))
+    codes, scales = device_fp8(p)
+    ref = oracle.build_cache(p)
+    got = host(codes, scales)
+    assert np.array_equal(got.codes, ref.codes)
+    assert np.array_equal(got.scales.view(np.uint32), ref.scales.view(np.uint32))
+
+
+LENS = [1, 63, 64, 65, 1000, 3001, 17, 4096]
+
+
+@pytest.mark.parametrize("bs", [8, 16, 32, 64, 128, 512])
+def test_fp8_decode_block_sizes(bs):
+    p = problem(lens=LENS, bs=bs, hq=4, hkv=4, dtype=W.F16, seed=bs)
+    codes, scales = device_fp8(p)
+    out, lse = decode(p, codes, scales)
+    ref, ref_lse = oracle.attention_of(p, host(codes, scales))
+    check_close(out, ref, W.F16, roundings=1, what="fp8 bs=%d" % bs)
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-5, atol=1e-5)
+
+
+@pytest.mark.parametrize("dtype", [W.F16, W.BF16])
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (16, 4), (32, 4)])
+@pytest.mark.parametrize("d", [64, 128])
+def test_fp8_decode_groupings(dtype, hq, hkv, d):
+    p = problem(lens=[5, 700, 129, 2000], hq=hq, hkv=hkv, d=d, dtype=dtype, bs=32, seed=hq + hkv + d)
+    codes, scales = device_fp8(p)
+    out, lse = decode(p, codes, scales)
+    ref, ref_lse = oracle.attention_of(p, host(codes, scales))
+    check_close(out, ref, dtype, roundings=1, what="fp8 %s hq=%d hkv=%d d=%d" % (dtype, hq, hkv, d))
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-5, atol=1e-5)
+
+
+@pytest.mark.parametrize("num_splits", [1, 3, 64])
+def test_fp8_decode_splits_fp32_output(num_splits):
+    """FP32 output: nothing on the path is rounded to 16 bits -> the literal bounds."""
+    p = problem(lens=[3000, 64, 1, 2500], hq=8, hkv=2, bs=16, dtype=W.BF16, mb=256)
+    codes, scales = device_fp8(p)
+    out, lse = decode(p, codes, scales, num_splits=num_splits, out_dtype=torch.float32)
+    ref, ref_lse = oracle.attention_of(p, host(codes, scales))
+    check_close(out, ref, W.BF16, roundings=0, what="fp8 splits=%d fp32 out" % num_splits)
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-5, atol=1e-5)
+
+
+def test_fp8_decode_step_append_then_decode():
+    """A decode step: one new token per sequence quantised into its page, then attention over it."""
+    p = problem(lens=[100, 31, 512, 7], hq=8, hkv=2, bs=16, dtype=W.BF16, extra=12, mb=40)
+    codes, scales = device_fp8(p)
+    step = W.append_step(p, seed=4)
+    pkv.kv_cache_append(codes, to_dev(step["k_new"]), to_dev(step["v_new"]), to_dev(step["cu_new_lens"]),
+                        to_dev(step["ctx_before"]), to_dev(step["block_tables"]), scales=scales)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    ref_cache = oracle.build_cache(p)
+    assert oracle.kv_cache_append_fp8(ref_cache, p.dtype, **step) == 0
+    got = host(codes, scales)
+    assert np.array_equal(got.codes, ref_cache.codes) and np.array_equal(got.scales, ref_cache.scales)
+    lens = p.context_lens + 1
+    out = pkv.paged_attn_decode(codes, to_dev(p.q), to_dev(step["block_tables"]), to_dev(lens), scale=p.scale,
+                                scales=scales)
+    torch.cuda.synchronize()
+    ref, _ = oracle.paged_attention_fp8(p.dtype, got, p.q, p.num_q_heads, p.cu_q_lens, lens, step["block_tables"],
+                                        p.scale, False)
+    check_close(out, ref, W.BF16, roundings=1, what="fp8 decode step")
+
+
+def test_fp8_prefill_is_refused():
+    p = problem(lens=[40], hq=4, hkv=4, bs=16)
+    codes, scales = device_fp8(p)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.paged_attn_prefill(codes, to_dev(p.q), to_dev(p.cu_q_lens), to_dev(p.context_lens),
+                               to_dev(p.block_tables), max_q_len=1, scale=p.scale, scales=scales)
+    assert e.value.status == 2
+
+
+def test_fp8_decode_full_7b_size_sampled():
+    """The 7B-like decode batch (16 x 1k-8k contexts, 32 heads x 128) on an FP8 cache, in the
+    launch configuration the benchmark times; every row against the oracle."""
+    p = W.decode_7b(pool_init="none", device="cuda", kv_format="fp8")
+    shape = (p.num_blocks, 2, 32, 16, 128)
+    codes = torch.zeros(shape, dtype=torch.uint8, device="cuda")
+    scales = torch.zeros(shape[:4], dtype=torch.float32, device="cuda")
+    pkv.kv_cache_append(codes, p.k_ctx, p.v_ctx, p.cu_ctx_lens.cuda(),
+                        torch.zeros(p.batch, dtype=torch.int32, device="cuda"), p.block_tables.cuda(), scales=scales)
+    out = pkv.paged_attn_decode(codes, p.q, p.block_tables.cuda(), p.context_lens.cuda(), scale=p.scale,
+                                scales=scales)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    p.q = p.q.cpu()
+    ref, _ = oracle.attention_of(p, host(codes, scales))
+    check_close(out, ref, W.F16, roundings=1, what="fp8 7B decode")

@@ -7,6 +7,7 @@ import shutil
 
 import pytest
 
+import tests.test_oracle_fp8 as fp8_pins
 import tests.test_oracle_pins as pins
 
 ORACLE_DIR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle")
@@ -20,8 +21,8 @@ MUTATIONS = [
     ("gqa_modulo", "int g = h / group;", "int g = h % J->hkv;"),
     ("causal_off_by_one", "(long)L - q_len + r + 1", "(long)L - q_len + r"),
     ("causal_top_left", "(long)L - q_len + r + 1", "r + 1"),
-    ("offset_xor", "const uint16_t *kr = J->cache + cache_row(pb, 0, g, (int)(i % J->bs)",
-     "const uint16_t *kr = J->cache + cache_row(pb, 0, g, (int)((i % J->bs) ^ 1)"),
+    ("offset_xor", "size_t kr = cache_row(pb, 0, g, (int)(i % J->bs)",
+     "size_t kr = cache_row(pb, 0, g, (int)((i % J->bs) ^ 1)"),
     ("last_key_dropped", "for (long i = 0; i < kmax; ++i) {\n        double w", "for (long i = 0; i + 1 < kmax; ++i) {\n        double w"),
     ("combine_weight_inverted", "double w = exp(ls[s] - M);", "double w = exp(M - ls[s]);"),
     ("append_ignores_ctx_before", "long pos = (long)ctx_before[b] + (t - cu_new_lens[b]);",
@@ -65,6 +66,42 @@ def test_some_pin_fails_on_planted_mistake(tmp_path, monkeypatch, name, old, new
     for fn, kw in PIN_TESTS:
         try:
             getattr(pins, fn)(**kw)
+        except (AssertionError, ValueError):
+            failed.append(fn)
+    assert failed, "no pin caught mutation %s" % name
+
+
+# The FP8 cache: the E4M3 conversion, the quantising append and the dequantising attention.
+FP8_MUTATIONS = [
+    ("e4m3_exponent_bias", "else v = ldexp((double)(8 + m), e - 10);", "else v = ldexp((double)(8 + m), e - 9);"),
+    ("e4m3_rounds_up", "double r = rint(ldexp(a, 3 - e)) - 8.0;", "double r = ceil(ldexp(a, 3 - e)) - 8.0;"),
+    ("e4m3_ties_away", "double r = rint(ldexp(a, 3 - e)) - 8.0;", "double r = round(ldexp(a, 3 - e)) - 8.0;"),
+    ("e4m3_subnormal_step", "double q = rint(a * 512.0);", "double q = rint(a * 256.0);"),
+    ("fp8_scale_inverted", "float scale = amax / 448.0f;", "float scale = 448.0f / amax;"),
+    ("fp8_codes_unscaled", "float y = (float)to_double(dtype, src[e]) * inv;",
+     "float y = (float)to_double(dtype, src[e]);"),
+    ("fp8_first_scale_only", "* (double)J->scales[row / (size_t)J->d];", "* (double)J->scales[0];"),
+    ("fp8_scale_dropped", "* (double)J->scales[row / (size_t)J->d];", ";"),
+]
+
+FP8_PIN_TESTS = [
+    ("test_decode_every_code_matches_torch", {}),
+    ("test_encode_matches_torch_in_range_including_ties", {}),
+    ("test_encode_ties_go_to_even_and_saturates", {}),
+    ("test_append_follows_the_definition", {}),
+    ("test_append_roundtrip_error_bound", {}),
+    ("test_attention_over_fp8_is_softmax_of_dequantised", dict(causal=False, q_lens=None)),
+]
+
+
+@pytest.mark.parametrize("name,old,new", FP8_MUTATIONS, ids=[m[0] for m in FP8_MUTATIONS])
+def test_some_fp8_pin_fails_on_planted_mistake(tmp_path, monkeypatch, name, old, new):
+    mutant = load_mutant(tmp_path, name, old, new)
+    monkeypatch.setattr(fp8_pins, "oracle", mutant)
+    failed = []
+    for fn, kw in FP8_PIN_TESTS:
+        try:
+            getattr(fp8_pins, fn)(**kw)
         except (AssertionError, ValueError):
             failed.append(fn)
     assert failed, "no pin caught mutation %s" % name

@@ -34,7 +34,7 @@ def device_problem(p):
 
 
 def call_noalloc(lib, cache, q, bt, ctx, scale, num_splits, out, lse):
-    c = pkv._cache_struct(cache)
+    c = pkv._cache_struct(cache, cache.dtype)
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     return lib.pkv_paged_attn_decode_noalloc(c, ctypes.c_void_p(q.data_ptr()), q.shape[1],
                                              ctypes.c_void_p(bt.data_ptr()), ctypes.c_void_p(ctx.data_ptr()),

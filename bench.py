@@ -46,7 +46,8 @@ def parse():
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="", help="comma list of extra workloads (bs_sweep,mixed,prefix,fp8,prefill)")
-    ap.add_argument("--profile", choices=["decode", "append", "prefill", "decode_mixed", "decode_prefix"], default=None,
+    ap.add_argument("--profile", choices=["decode", "append", "prefill", "decode_mixed", "decode_prefix", "decode_fp8"],
+                    default=None,
                     help="small case for ncu captures: W + K launches of one kernel, nothing else timed")
     return ap.parse_args()
 
@@ -85,6 +86,21 @@ def profile_case(args):
         out = torch.empty((p.batch, 32, 128), dtype=torch.bfloat16, device="cuda")
         for _ in range(args.warmup + args.steps):
             pkv.paged_attn_decode(cache, q, bt, ctx, scale=p.scale, out=out)
+        torch.cuda.synchronize()
+        assert pkv.get_device_error() == 0
+    elif args.profile == "decode_fp8":
+        # 7B-like decode at batch 4 on an FP8 cache: 0.2 GB of codes + scales (above L2)
+        p = W.decode_7b(batch=4, pool_init="none", device="cuda", kv_format="fp8")
+        shape = (p.num_blocks, 2, 32, 16, 128)
+        codes = torch.zeros(shape, dtype=torch.uint8, device="cuda")
+        scales = torch.zeros(shape[:4], dtype=torch.float32, device="cuda")
+        bt = p.block_tables.cuda()
+        pkv.kv_cache_append(codes, p.k_ctx, p.v_ctx, p.cu_ctx_lens.cuda(),
+                            torch.zeros(p.batch, dtype=torch.int32, device="cuda"), bt, scales=scales)
+        q, ctx = p.q.cuda(), p.context_lens.cuda()
+        out = torch.empty((p.batch, 32, 128), dtype=torch.float16, device="cuda")
+        for _ in range(args.warmup + args.steps):
+            pkv.paged_attn_decode(codes, q, bt, ctx, scale=p.scale, out=out, scales=scales)
         torch.cuda.synchronize()
         assert pkv.get_device_error() == 0
     elif args.profile == "decode_prefix":

@@ -228,10 +228,11 @@ pkv_status pkv_paged_attn_decode(pkv_cache cache, const void *q, int num_q_heads
     a.err = s.err_ptr;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const int grid = s.info.num_sms * s.info.decode_ctas_per_sm;
-    // four or more query heads per KV head of a native cache: the group kernel (tensor cores);
-    // an FP8 cache decodes on the CUDA-core kernel for every grouping
-    const cudaError_t le =
-        (group >= 4 && !a.cache.fp8) ? launch_decode_gqa(a, grid, cs) : launch_decode(a, grid, cs);
+    // tensor cores: four or more query heads per KV head of a native cache (the group kernel),
+    // and every grouping of an FP8 cache with head_dim 128; CUDA cores for the rest
+    cudaError_t le;
+    if (a.cache.fp8) le = cache.head_dim == 128 ? launch_decode_fp8(a, grid, cs) : launch_decode(a, grid, cs);
+    else le = group >= 4 ? launch_decode_gqa(a, grid, cs) : launch_decode(a, grid, cs);
     if (le != cudaSuccess) return PKV_ERR_CUDA;
     // Rows that span several splits (and empty rows) are finished by the merge.
     CombineArgs c;

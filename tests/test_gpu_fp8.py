@@ -42,6 +42,12 @@ def device_fp8(p):
     return codes, scales
 
 
+def roundings(p, fp32_out=False):
+    """Roundings to 16 bits on the path: the output (unless FP32) and, on the tensor-core path
+    (head_dim 128), the probabilities P in f16 before the P.V product."""
+    return (0 if fp32_out else 1) + (1 if p.head_dim == 128 else 0)
+
+
 def host(codes, scales):
     return oracle.Fp8Cache(codes.cpu().numpy().copy(), scales.cpu().numpy().copy())
 
@@ -88,13 +94,14 @@ def test_fp8_append_special_rows():
 LENS = [1, 63, 64, 65, 1000, 3001, 17, 4096]
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("bs", [8, 16, 32, 64, 128, 512])
-def test_fp8_decode_block_sizes(bs):
-    p = problem(lens=LENS, bs=bs, hq=4, hkv=4, dtype=W.F16, seed=bs)
+def test_fp8_decode_block_sizes(bs, d):
+    p = problem(lens=LENS, bs=bs, hq=4, hkv=4, d=d, dtype=W.F16, seed=bs)
     codes, scales = device_fp8(p)
     out, lse = decode(p, codes, scales)
     ref, ref_lse = oracle.attention_of(p, host(codes, scales))
-    check_close(out, ref, W.F16, roundings=1, what="fp8 bs=%d" % bs)
+    check_close(out, ref, W.F16, roundings=roundings(p), what="fp8 bs=%d d=%d" % (bs, d))
     np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-5, atol=1e-5)
 
 
@@ -106,18 +113,30 @@ def test_fp8_decode_groupings(dtype, hq, hkv, d):
     codes, scales = device_fp8(p)
     out, lse = decode(p, codes, scales)
     ref, ref_lse = oracle.attention_of(p, host(codes, scales))
-    check_close(out, ref, dtype, roundings=1, what="fp8 %s hq=%d hkv=%d d=%d" % (dtype, hq, hkv, d))
+    check_close(out, ref, dtype, roundings=roundings(p), what="fp8 %s hq=%d hkv=%d d=%d" % (dtype, hq, hkv, d))
     np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-5, atol=1e-5)
 
 
 @pytest.mark.parametrize("num_splits", [1, 3, 64])
 def test_fp8_decode_splits_fp32_output(num_splits):
-    """FP32 output: nothing on the path is rounded to 16 bits -> the literal bounds."""
+    """FP32 output: only P is rounded to 16 bits (f16) on the way."""
     p = problem(lens=[3000, 64, 1, 2500], hq=8, hkv=2, bs=16, dtype=W.BF16, mb=256)
     codes, scales = device_fp8(p)
     out, lse = decode(p, codes, scales, num_splits=num_splits, out_dtype=torch.float32)
     ref, ref_lse = oracle.attention_of(p, host(codes, scales))
-    check_close(out, ref, W.BF16, roundings=0, what="fp8 splits=%d fp32 out" % num_splits)
+    check_close(out, ref, W.BF16, roundings=roundings(p, fp32_out=True), what="fp8 splits=%d fp32 out" % num_splits)
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-5, atol=1e-5)
+
+
+@pytest.mark.parametrize("bs", [128, 512])
+def test_fp8_decode_splits_not_multiples_of_the_tile(bs):
+    """Splits of 448 tokens (7 splits over 3072) start tiles at 64 mod 128 inside large pages."""
+    p = problem(lens=[3000, 700, 129], hq=8, hkv=8, bs=bs, dtype=W.BF16, mb=3072 // bs)
+    assert pkv.decode_split_tokens(3, 8, 8, 128, bs, 3072 // bs, num_splits=7) % 128 == 64
+    codes, scales = device_fp8(p)
+    out, lse = decode(p, codes, scales, num_splits=7)
+    ref, ref_lse = oracle.attention_of(p, host(codes, scales))
+    check_close(out, ref, W.BF16, roundings=roundings(p), what="fp8 bs=%d 7 splits" % bs)
     np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-5, atol=1e-5)
 
 
@@ -140,7 +159,7 @@ def test_fp8_decode_step_append_then_decode():
     torch.cuda.synchronize()
     ref, _ = oracle.paged_attention_fp8(p.dtype, got, p.q, p.num_q_heads, p.cu_q_lens, lens, step["block_tables"],
                                         p.scale, False)
-    check_close(out, ref, W.BF16, roundings=1, what="fp8 decode step")
+    check_close(out, ref, W.BF16, roundings=roundings(p), what="fp8 decode step")
 
 
 def test_fp8_prefill_is_refused():
@@ -167,4 +186,4 @@ def test_fp8_decode_full_7b_size_sampled():
     assert pkv.get_device_error() == 0
     p.q = p.q.cpu()
     ref, _ = oracle.attention_of(p, host(codes, scales))
-    check_close(out, ref, W.F16, roundings=1, what="fp8 7B decode")
+    check_close(out, ref, W.F16, roundings=roundings(p), what="fp8 7B decode")

@@ -45,7 +45,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", default="", help="comma list of extra workloads (bs_sweep,mixed,prefix,fp8,prefill)")
+    ap.add_argument("--only", default="", help="comma list of extra workloads (bs_sweep,mixed,prefix,fp8,mqa,prefill)")
     ap.add_argument("--profile", choices=["decode", "append", "prefill", "decode_mixed", "decode_prefix", "decode_fp8"],
                     default=None,
                     help="small case for ncu captures: W + K launches of one kernel, nothing else timed")
@@ -542,6 +542,36 @@ def bench_fp8(torch, steps, warmup, fp16_ms=None):
     return r
 
 
+def bench_mqa(torch, steps, warmup):
+    """Multi-query decode: 128 sequences, 32 query heads sharing one KV head."""
+    import paged_kv_flash_cache_gb300 as pkv
+    from paged_kv_flash_cache_gb300 import workloads as W
+    gen = torch.Generator().manual_seed(1241)
+    lens = torch.randint(1024, 8193, (128,), generator=gen).tolist()
+    nb = sum((L + 15) // 16 for L in lens)
+    order = torch.randperm(nb, generator=gen).tolist()
+    p = W.make_problem("mqa", batch=128, num_q_heads=32, num_kv_heads=1, head_dim=128, block_size=16,
+                       context_lens=lens, q_lens=[1] * 128, dtype=W.BF16, causal=False, seed=1242, num_blocks=nb,
+                       free_order=order, pool_init="none", device="cuda")
+    cache = device_problem(p, torch)
+    q, bt, ctx = p.q.cuda(), p.block_tables.cuda(), p.context_lens.cuda()
+    ws = torch.empty(max(16, pkv.decode_workspace_size(p.batch, 32, 1, 128, 16, bt.shape[1])), dtype=torch.uint8,
+                     device="cuda")
+    o = torch.empty((p.batch, 32, 128), dtype=q.dtype, device="cuda")
+    fn = lambda i: pkv.paged_attn_decode(cache, q, bt, ctx, scale=p.scale, workspace=ws, out=o)
+    for i in range(warmup):
+        fn(i)
+    ms = time_loop(torch, fn, steps, torch.cuda.current_stream()) / steps
+    b = decode_bytes(p)
+    del cache
+    torch.cuda.empty_cache()
+    return {"workload": "MQA decode: 128 seqs, contexts U[1024, 8192], 32 query heads / 1 KV head x 128, bf16, "
+                        "bs 16 (each group of 8 query heads is one tensor-core unit over the shared pages)",
+            "ms": round(ms, 4), "kv_gbs": round(b["kv"] / ms / 1e6, 1),
+            "frac_of_hbm": round(b["total"] / ms / 1e6 / peaks()["hbm_gbs"], 3),
+            "tokens_per_s": round(p.batch / ms * 1e3, 1)}
+
+
 def bench_prefill(torch, steps, warmup):
     import paged_kv_flash_cache_gb300 as pkv
     from paged_kv_flash_cache_gb300 import workloads as W
@@ -684,7 +714,8 @@ def main():
         extra = {}
         only = set(filter(None, args.only.split(",")))
         for name, fn in (("bs_sweep", bench_bs_sweep), ("mixed", bench_mixed), ("prefix", bench_prefix),
-                         ("fp8", lambda t, k, w: bench_fp8(t, k, w, r["decode_ms"])), ("prefill", bench_prefill)):
+                         ("fp8", lambda t, k, w: bench_fp8(t, k, w, r["decode_ms"])), ("mqa", bench_mqa),
+                         ("prefill", bench_prefill)):
             if only and name not in only:
                 continue
             try:

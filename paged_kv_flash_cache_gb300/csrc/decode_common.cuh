@@ -109,7 +109,7 @@ __device__ __forceinline__ bool merge_warp_loop(const DecodeArgs &a, const UnitT
                                                 size_t buf_floats, uint64_t *mfull, uint64_t *mempty,
                                                 const int *merge_unit, volatile int *abort_flag, int lane) {
     static_assert(W <= 32, "one lane per consumer warp");
-    const int hkv = a.cache.num_kv_heads, chunk = a.chunk;
+    const int hkv = a.cache.num_kv_heads * a.head_groups, chunk = a.chunk;  // unit heads
     int mbuf = 0;
     uint32_t mphase = 0;
     for (;;) {
@@ -225,7 +225,7 @@ __device__ __forceinline__ int decode_scan_units(const DecodeArgs &a, const Unit
         }
     }
     __syncthreads();
-    return t.first[S] * a.cache.num_kv_heads;
+    return t.first[S] * a.cache.num_kv_heads * a.head_groups;
 }
 
 }  // namespace pkv

@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int hkv = a.cache.num_kv_heads, bs = a.cache.block_size, chunk = a.chunk;
+    const int hu = hkv * a.head_groups;  // unit heads (KV heads, or groups of 8 query heads)
     // a tile is copied in slices of br = min(bs, 64) rows: tiles start at multiples of 64 tokens,
     // so every slice lies inside one page whatever the page size
     const int br = bs < 64 ? bs : 64;
@@ -157,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         UnitCursor c = {};
         PageWindow win = {};
         if ((int)blockIdx.x < num_units) {
-            c = unit_of(blockIdx.x, ut, a.s_max, hkv, chunk);
+            c = unit_of(blockIdx.x, ut, a.s_max, hu, chunk);
             win = unit_pages(a, c, lane);
         }
         for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
@@ -165,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             UnitCursor cn = c;
             PageWindow wn = win;
             if (u + (int)gridDim.x < num_units) {
-                cn = unit_of(u + gridDim.x, ut, a.s_max, hkv, chunk);
+                cn = unit_of(u + gridDim.x, ut, a.s_max, hu, chunk);
                 wn = unit_pages(a, cn, lane);
             }
             const int *bt = a.block_tables + (size_t)c.b * a.max_blocks_per_seq;
@@ -205,8 +206,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane < nslices) {
                     // one box: the slice's K rows then its V rows (page pb, head c.kvh, rows off..)
-                    tc::tma_load_5d(st + (size_t)lane * 2 * br * kD, &tm_codes, 0, off, c.kvh, 0, pb, &full[stage]);
-                    tc::tma_load_4d(st + L::kSOffset + (size_t)lane * spitch, &tm_scales, off, c.kvh, 0, pb,
+                    const int kvr = c.kvh / a.head_groups;  // the KV head of this unit
+                    tc::tma_load_5d(st + (size_t)lane * 2 * br * kD, &tm_codes, 0, off, kvr, 0, pb, &full[stage]);
+                    tc::tma_load_4d(st + L::kSOffset + (size_t)lane * spitch, &tm_scales, off, kvr, 0, pb,
                                     &full[stage]);
                 }
                 if (first_tile && lane == 0) {
@@ -250,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&full[stage], phase, abort_flag, a.err)) return;
         const int u = stage_unit[stage];
         if (u < 0) break;
-        const UnitCursor c = unit_of(u, ut, a.s_max, hkv, chunk);
+        const UnitCursor c = unit_of(u, ut, a.s_max, hu, chunk);
         float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
         float o[kChunks][4];
 #pragma unroll
@@ -463,7 +465,7 @@ cudaError_t launch_fp8_g(const DecodeArgs &a, int grid, cudaStream_t s) {
 cudaError_t launch_decode_fp8(const DecodeArgs &a, int grid, cudaStream_t s) {
     if (a.batch == 0) return cudaSuccess;
     if (a.cache.head_dim != kD || a.batch > kMaxBatch8) return cudaErrorInvalidValue;
-    switch (a.num_q_heads / a.cache.num_kv_heads) {
+    switch (a.num_q_heads / (a.cache.num_kv_heads * a.head_groups)) {  // query heads per unit
         case 1: return launch_fp8_g<1>(a, grid, s);
         case 2: return launch_fp8_g<2>(a, grid, s);
         case 4: return launch_fp8_g<4>(a, grid, s);

@@ -88,6 +88,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int hkv = a.cache.num_kv_heads, bs = a.cache.block_size, chunk = a.chunk;
+    const int hu = hkv * a.head_groups;  // unit heads (KV heads, or groups of 8 query heads)
 
     if (tid == 0) {
         for (int i = 0; i < kStagesG; ++i) {
@@ -116,7 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         UnitCursor c = {};
         PageWindow win = {};
         if ((int)blockIdx.x < num_units) {
-            c = unit_of(blockIdx.x, ut, a.s_max, hkv, chunk);
+            c = unit_of(blockIdx.x, ut, a.s_max, hu, chunk);
             win = unit_pages(a, c, lane);
         }
         for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
@@ -124,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             UnitCursor cn = c;
             PageWindow wn = win;
             if (u + (int)gridDim.x < num_units) {
-                cn = unit_of(u + gridDim.x, ut, a.s_max, hkv, chunk);
+                cn = unit_of(u + gridDim.x, ut, a.s_max, hu, chunk);
                 wn = unit_pages(a, cn, lane);
             }
             const int *bt = a.block_tables + (size_t)c.b * a.max_blocks_per_seq;
@@ -161,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
                 if (lane < npages) {
-                    const int rowK = ((pb * 2 + 0) * hkv + c.kvh) * bs + off;
+                    const int rowK = ((pb * 2 + 0) * hkv + c.kvh / a.head_groups) * bs + off;
                     const int rowV = rowK + hkv * bs;
                     const uint32_t dst = (uint32_t)lane * box_rows * 128u;
 #pragma unroll
@@ -212,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&full[stage], phase, abort_flag, a.err)) return;
         const int u = stage_unit[stage];
         if (u < 0) break;
-        const UnitCursor c = unit_of(u, ut, a.s_max, hkv, chunk);
+        const UnitCursor c = unit_of(u, ut, a.s_max, hu, chunk);
         float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
         float o[kKSteps][4];
 #pragma unroll
@@ -387,7 +388,7 @@ cudaError_t launch_gqa_t(const DecodeArgs &a, int grid, cudaStream_t s) {
 
 cudaError_t launch_decode_gqa(const DecodeArgs &a, int grid, cudaStream_t s) {
     if (a.batch == 0) return cudaSuccess;
-    const int group = a.num_q_heads / a.cache.num_kv_heads;
+    const int group = a.num_q_heads / (a.cache.num_kv_heads * a.head_groups);  // query heads per unit
     const bool bf16 = a.cache.dtype == 1;
     if (a.cache.head_dim == 128) {
         if (group == 4) return bf16 ? launch_gqa_t<128, 4, true>(a, grid, s) : launch_gqa_t<128, 4, false>(a, grid, s);

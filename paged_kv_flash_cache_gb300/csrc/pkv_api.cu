@@ -196,7 +196,9 @@ pkv_status pkv_paged_attn_decode(pkv_cache cache, const void *q, int num_q_heads
     if (batch < 0 || max_blocks_per_seq <= 0 || num_q_heads <= 0 || num_splits < 0) return PKV_ERR_INVALID_ARG;
     if (num_q_heads % cache.num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
     const int group = num_q_heads / cache.num_kv_heads;
-    if (group != 1 && group != 2 && group != 4 && group != 8) return PKV_ERR_UNSUPPORTED;
+    // 1, 2, 4, or any multiple of 8 (taken 8 query heads at a time) query heads per KV head
+    if (group != 1 && group != 2 && group != 4 && group % 8 != 0) return PKV_ERR_UNSUPPORTED;
+    if (group > 8 && cache.format == PKV_KV_FP8_E4M3 && cache.head_dim != 128) return PKV_ERR_UNSUPPORTED;
     if (batch > decode_max_batch()) return PKV_ERR_UNSUPPORTED;
     if (batch == 0) return PKV_OK;
     if (!q || !block_tables || !context_lens || !out) return PKV_ERR_INVALID_ARG;
@@ -220,6 +222,7 @@ pkv_status pkv_paged_attn_decode(pkv_cache cache, const void *q, int num_q_heads
     a.scale = scale;
     a.chunk = chunk;
     a.s_max = s_max;
+    a.head_groups = group > 8 ? group / 8 : 1;
     a.part_o = static_cast<float *>(workspace);
     a.part_lse = need > 0 ? a.part_o + (size_t)batch * num_q_heads * s_max * cache.head_dim : nullptr;
     a.out = out;

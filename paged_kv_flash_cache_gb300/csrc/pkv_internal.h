@@ -39,6 +39,10 @@ struct DecodeArgs {
     int batch, max_blocks_per_seq;
     float scale;
     int chunk;   // tokens per split (multiple of the decode tile)
+    // Groups of 8 query heads per KV head when a KV head serves more than 8 (MQA, wide groups),
+    // else 1: the tensor-core kernels then take each group as a "virtual" KV head -- unit head v
+    // reads KV head v / head_groups and serves query heads 8v .. 8v + 7.
+    int head_groups;
     int s_max;   // splits a full-capacity context uses: ceil(max_blocks_per_seq * block_size / chunk)
     float *part_o;    // [batch, Hq, s_max, D]
     float *part_lse;  // [batch, Hq, s_max]

@@ -70,6 +70,11 @@ def test_host_validation_without_gpu(lib):
                                  None)
     assert lib.pkv_paged_attn_decode(*args(3)) == 1
     assert lib.pkv_paged_attn_decode(*args(6)) == 2      # group 3
+    assert lib.pkv_paged_attn_decode(*args(20)) == 2     # group 10: not a multiple of 8
+    # FP8 cache with head_dim 64: groups above 8 are not supported
+    fp8_64 = (_cache(fmt=1, scales=4096, d=64), good, 32, good, good, 2, 4, F(0.1), 0, good, 1 << 20, good, 0, None,
+              None)
+    assert lib.pkv_paged_attn_decode(*fp8_64) == 2
     assert lib.pkv_paged_attn_decode(*args(2, out_dt=1)) == 2   # bf16 out for an fp16 cache
     # prefill: negative total_q
     assert lib.pkv_paged_attn_prefill(_cache(), good, 2, good, good, good, 1, 4, -1, 4, F(0.1), 1, good, 0, None,

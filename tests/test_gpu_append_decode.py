@@ -223,6 +223,19 @@ def test_decode_large_batch_many_equal_lengths(hq, hkv):
         np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-5, atol=1e-5)
 
 
+@pytest.mark.parametrize("dtype", [W.F16, W.BF16])
+@pytest.mark.parametrize("hq,hkv,d", [(32, 1, 128), (16, 1, 64), (64, 4, 128), (24, 1, 128)])
+def test_decode_mqa_and_wide_groups(dtype, hq, hkv, d):
+    """One KV head for many query heads (MQA) and groups above 8: the tensor-core kernel takes
+    each 8 query heads of a KV head as one unit, all reading that KV head's pages."""
+    p = problem(lens=[5, 700, 129, 2000], hq=hq, hkv=hkv, d=d, dtype=dtype, bs=32, seed=hq * 3 + d)
+    cache = device_cache(p)
+    out, lse = run_decode(p, cache)
+    ref, ref_lse = oracle.attention_of(p, cache_bits(cache))
+    check_close(out, ref, dtype, roundings=2, what="%s hq=%d hkv=%d d=%d" % (dtype, hq, hkv, d))
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-5, atol=1e-5)
+
+
 def test_decode_bad_page_flags_error():
     p = problem(lens=[200, 50], hq=4, hkv=4, bs=16)
     cache = device_cache(p)

@@ -140,6 +140,16 @@ def test_fp8_decode_splits_not_multiples_of_the_tile(bs):
     np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-5, atol=1e-5)
 
 
+@pytest.mark.parametrize("hq,hkv", [(32, 1), (64, 4)])
+def test_fp8_decode_mqa_and_wide_groups(hq, hkv):
+    p = problem(lens=[5, 700, 129, 2000], hq=hq, hkv=hkv, d=128, dtype=W.BF16, bs=16, seed=hq)
+    codes, scales = device_fp8(p)
+    out, lse = decode(p, codes, scales)
+    ref, ref_lse = oracle.attention_of(p, host(codes, scales))
+    check_close(out, ref, W.BF16, roundings=roundings(p), what="fp8 hq=%d hkv=%d" % (hq, hkv))
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-5, atol=1e-5)
+
+
 def test_fp8_decode_step_append_then_decode():
     """A decode step: one new token per sequence quantised into its page, then attention over it."""
     p = problem(lens=[100, 31, 512, 7], hq=8, hkv=2, bs=16, dtype=W.BF16, extra=12, mb=40)

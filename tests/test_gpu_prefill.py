@@ -101,6 +101,13 @@ def test_prefill_inputs_written_by_the_previous_kernel():
         check_close(out, ref, p.dtype, roundings=2, what="prefill inputs from kernels")
 
 
+def test_prefill_mqa():
+    p = problem(lens=[520, 77], q_lens=[200, 77], hq=32, hkv=1, d=128, dtype=W.BF16, causal=True, bs=16, seed=31)
+    cache = device_cache(p)
+    out, lse = run_prefill(p, cache)
+    check(p, cache, out, lse, roundings=2, what="prefill mqa")
+
+
 def test_prefill_fp32_output_single_rounding():
     p = problem(lens=[640, 333], q_lens=[512, 333], hq=4, hkv=4, dtype=W.BF16, bs=32, seed=3)
     cache = device_cache(p)

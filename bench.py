@@ -45,7 +45,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", default="", help="comma list of extra workloads (bs_sweep,mixed,prefix,fp8,mqa,prefill)")
+    ap.add_argument("--only", default="", help="comma list of extra workloads (bs_sweep,mixed,prefix,fp8,mqa,prefill,prefill_fp8)")
     ap.add_argument("--profile", choices=["decode", "append", "prefill", "decode_mixed", "decode_prefix", "decode_fp8"],
                     default=None,
                     help="small case for ncu captures: W + K launches of one kernel, nothing else timed")
@@ -572,12 +572,17 @@ def bench_mqa(torch, steps, warmup):
             "tokens_per_s": round(p.batch / ms * 1e3, 1)}
 
 
-def bench_prefill(torch, steps, warmup):
+def bench_prefill(torch, steps, warmup, fp8=False):
     import paged_kv_flash_cache_gb300 as pkv
     from paged_kv_flash_cache_gb300 import workloads as W
     p = W.prefill_long(device="cuda")
     shape = (p.num_blocks, 2, p.num_kv_heads, p.block_size, p.head_dim)
-    cache = torch.zeros(shape, dtype=p.q.dtype, device="cuda")
+    if fp8:  # the same prompt tokens quantised into an FP8 cache (codes + one FP32 scale per row)
+        cache = torch.zeros(shape, dtype=torch.uint8, device="cuda")
+        scales = torch.zeros(shape[:4], dtype=torch.float32, device="cuda")
+    else:
+        cache = torch.zeros(shape, dtype=p.q.dtype, device="cuda")
+        scales = None
     bt = p.block_tables.cuda()
     chunks = []
     for c in range(8192 // p.meta["chunk"]):
@@ -595,11 +600,11 @@ def bench_prefill(torch, steps, warmup):
         for c, ch in enumerate(chunks):
             if timed:
                 ev[c][0].record(stream)
-            pkv.kv_cache_append(cache, ch["k"], ch["v"], ch["cu"], ch["before"], bt)
+            pkv.kv_cache_append(cache, ch["k"], ch["v"], ch["cu"], ch["before"], bt, scales=scales)
             if timed:
                 ev[c][1].record(stream)
             pkv.paged_attn_prefill(cache, ch["q"], ch["cu"], ch["ctx"], bt, max_q_len=ch["ql"], scale=p.scale,
-                                   causal=True, out=ch["out"])
+                                   causal=True, out=ch["out"], scales=scales)
             if timed:
                 ev[c][2].record(stream)
 
@@ -617,13 +622,15 @@ def bench_prefill(torch, steps, warmup):
         attn_ms += sum(e[1].elapsed_time(e[2]) for e in ev)
     app_ms, attn_ms = app_ms / steps, attn_ms / steps
     flops = p.causal_flops()
-    # append moves every prompt token's K and V row-set once in, once out
-    app_bytes = 2 * 2 * p.batch * 8192 * p.num_kv_heads * p.head_dim * 2
+    # append moves every prompt token's K and V row-set once in, once out (FP8: out as codes + scales)
+    rows_kv = 2 * p.batch * 8192 * p.num_kv_heads
+    app_bytes = rows_kv * p.head_dim * 2 + (rows_kv * (p.head_dim + 4) if fp8 else rows_kv * p.head_dim * 2)
     pk = peaks()
-    del cache
+    del cache, scales
     torch.cuda.empty_cache()
     return {"workload": "4 x 8192 causal prefill, 32 heads x 128, bf16, bs 16 pages, 16 chunks of 512 "
-                        "(append chunk, then attend)", "ms_per_pass": round(ms, 3),
+                        "(append chunk, then attend)" + ("; FP8 E4M3 cache, products in f16" if fp8 else ""),
+            "ms_per_pass": round(ms, 3),
             "tflops": round(flops / ms / 1e9, 1), "frac_of_dense_bf16": round(flops / ms / 1e9 / pk["bf16_tflops"], 3),
             "attention_only": {"ms": round(attn_ms, 3), "tflops": round(flops / attn_ms / 1e9, 1),
                                "frac_of_dense_bf16": round(flops / attn_ms / 1e9 / pk["bf16_tflops"], 3),
@@ -715,7 +722,8 @@ def main():
         only = set(filter(None, args.only.split(",")))
         for name, fn in (("bs_sweep", bench_bs_sweep), ("mixed", bench_mixed), ("prefix", bench_prefix),
                          ("fp8", lambda t, k, w: bench_fp8(t, k, w, r["decode_ms"])), ("mqa", bench_mqa),
-                         ("prefill", bench_prefill)):
+                         ("prefill", bench_prefill),
+                         ("prefill_fp8", lambda t, k, w: bench_prefill(t, k, w, fp8=True))):
             if only and name not in only:
                 continue
             try:

@@ -284,7 +284,7 @@ pkv_status pkv_paged_attn_prefill(pkv_cache cache, const void *q, int num_q_head
                                   void *out, pkv_dtype out_dtype, float *lse, void *stream) {
     pkv_status st = check_cache(cache);
     if (st != PKV_OK) return st;
-    if (cache.format != PKV_KV_NATIVE) return PKV_ERR_UNSUPPORTED;
+    if (cache.format == PKV_KV_FP8_E4M3 && cache.head_dim != 128) return PKV_ERR_UNSUPPORTED;
     if ((st = check_out_dtype(out_dtype, cache.dtype)) != PKV_OK) return st;
     if (batch < 0 || max_blocks_per_seq <= 0 || num_q_heads <= 0 || total_q < 0 || max_q_len < 0)
         return PKV_ERR_INVALID_ARG;

@@ -10,7 +10,9 @@
 // O(n²)", prefill / decode section): Q K^T and P V are dense contractions and run as tcgen05.mma.
 //
 // CTA = one query head x 256 query rows of one sequence, as two 128-row tiles A and B that share
-// every K/V tile (384 threads, three warpgroups):
+// every K/V tile (384 threads, three warpgroups). Over an FP8 cache (head_dim 128) warps 2-3
+// convert each K/V tile in place from E4M3 codes to f16 (V times its row scales), the products run
+// in f16 and the softmax multiplies each score column by its K row scale; otherwise as below:
 //   warp 0     TMA producer: both Q tiles once (3-D tensor map over [total_q, Hq, D]); then for
 //              each 128-key tile j the K tile and the V tile, each into one slot of a 4-slot ring:
 //              the pages a tile covers are looked up in the block table by the warp's lanes and each
@@ -48,7 +50,7 @@ constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by mo
 // O_A [256,384), O_B [384,512).
 constexpr uint32_t kColS = 0, kColO = 256;
 
-template <int D>
+template <int D, bool FP8 = false>
 struct PrefillLayout {
     static constexpr int kHalves = D / 64;                      // 128-byte swizzle atoms along D
     static constexpr uint32_t kTileHalf = 128 * 128;            // 128 rows x 128 bytes
@@ -57,7 +59,11 @@ struct PrefillLayout {
     static constexpr uint32_t kQOff = 0;
     static constexpr uint32_t kRingOff = 2 * kQBytes;
     static constexpr uint32_t kBarOff = kRingOff + kRing * kKVBytes;
-    static constexpr uint32_t kSmemBytes = kBarOff + 256 + 1024;  // barriers + alignment slack
+    // FP8 cache: the codes of a ring item land in its slot's upper half (128 rows x 128 bytes,
+    // where the f16 tile's second 64-column half goes) and its row scales in a scale slot
+    static constexpr uint32_t kCodeOff = kTileHalf;             // within a ring slot
+    static constexpr uint32_t kScaleOff = kBarOff + 256;        // [kRing][128] FP32
+    static constexpr uint32_t kSmemBytes = kBarOff + 256 + (FP8 ? kRing * 128 * 4 : 0) + 1024;  // + alignment slack
     static constexpr uint32_t kTmemCols = 512;
 };
 
@@ -66,6 +72,7 @@ struct PrefillParams {
     int batch, mb, num_q_heads, num_kv_heads, group, bs, log2_bs, num_blocks;
     float scale_log2;
     int causal;
+    const float *scales;  // FP8 cache: FP32 row scales [NB, 2, Hkv, bs]
     void *out;
     int out_dtype;
     float *lse;
@@ -119,11 +126,14 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, bool bf16) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-template <int D, bool BF16>
+// BF16: type of q and the default output. FP8: the cache holds E4M3 codes with one FP32 scale per
+// row; the tensor-core products then run in f16 (MMA below), which holds every code exactly.
+template <int D, bool BF16, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
                    PrefillParams p) {
-    using Lay = PrefillLayout<D>;
+    using Lay = PrefillLayout<D, FP8>;
+    constexpr bool MMA_BF16 = BF16 && !FP8;  // operand type of the tcgen05 products and of P
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment: the 128-byte swizzle pattern is a function of address bits 4-9.
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -139,6 +149,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *drain = bars + 17;         // every MMA issued has completed
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 18);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 19);
+    uint64_t *kv_code = bars + 20;       // [kRing] FP8: codes and scales of a ring item have landed
+    uint64_t *q_ready = bars + 24;       // FP8: Q converted to f16 (or left as it is for f16 q)
+    const float *sScale = reinterpret_cast<const float *>(smem + Lay::kScaleOff);  // FP8: [kRing][128]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int mt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -160,10 +173,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kRing; ++s) {
-            mbar_init(&kv_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
+            // FP8: a slot is full once both converter warps have written it; a K slot (even: items
+            // alternate K, V) is free once its QK MMAs are done and the 8 softmax warps have read
+            // its row scales
+            mbar_init(&kv_full[s], FP8 ? 2 : 1);
+            mbar_init(&kv_empty[s], (FP8 && (s & 1) == 0) ? 9 : 1);
+            if (FP8) mbar_init(&kv_code[s], 1);
         }
         mbar_init(q_full, 1);
+        if (FP8) mbar_init(q_ready, 2);
         for (int x = 0; x < 2; ++x) {
             mbar_init(&s_full[x], 1);
             mbar_init(&p_full[x], 4);
@@ -219,15 +237,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t u = 2u * j + kv, slot = u % kRing, ph = (u / kRing) & 1u;
                     if (!mbar_wait(&kv_empty[slot], ph ^ 1u, abort_flag, p.err)) { ok = false; break; }
                     uint8_t *dst0 = sRing + slot * Lay::kKVBytes;
-                    if (lane == 0)
-                        mbar_arrive_expect_tx(&kv_full[slot], (uint32_t)npages * box_rows * 128u * Lay::kHalves);
-                    __syncwarp();
-                    if (lane < npages) {
-                        const int row = ((pb * 2 + kv) * p.num_kv_heads + g) * p.bs + off;
-                        const uint32_t dst = (uint32_t)lane * box_rows * 128u;
+                    if constexpr (FP8) {
+                        // codes (one 128-byte box row per token) and row scales of each page slice
+                        if (lane == 0) mbar_arrive_expect_tx(&kv_code[slot], (uint32_t)npages * box_rows * (128u + 4u));
+                        __syncwarp();
+                        if (lane < npages) {
+                            const int row = ((pb * 2 + kv) * p.num_kv_heads + g) * p.bs + off;
+                            const uint32_t dst = (uint32_t)lane * box_rows;
+                            tc::tma_load_2d(dst0 + Lay::kCodeOff + dst * 128u, &tm_kv, 0, row, &kv_code[slot]);
+                            bulk_g2s(smem + Lay::kScaleOff + (slot * 128u + dst) * 4u, p.scales + row,
+                                     (uint32_t)box_rows * 4u, &kv_code[slot], l2_policy_evict_first());
+                        }
+                    } else {
+                        if (lane == 0)
+                            mbar_arrive_expect_tx(&kv_full[slot], (uint32_t)npages * box_rows * 128u * Lay::kHalves);
+                        __syncwarp();
+                        if (lane < npages) {
+                            const int row = ((pb * 2 + kv) * p.num_kv_heads + g) * p.bs + off;
+                            const uint32_t dst = (uint32_t)lane * box_rows * 128u;
 #pragma unroll
-                        for (int hf = 0; hf < Lay::kHalves; ++hf)
-                            tc::tma_load_2d(dst0 + hf * Lay::kTileHalf + dst, &tm_kv, hf * 64, row, &kv_full[slot]);
+                            for (int hf = 0; hf < Lay::kHalves; ++hf)
+                                tc::tma_load_2d(dst0 + hf * Lay::kTileHalf + dst, &tm_kv, hf * 64, row, &kv_full[slot]);
+                        }
                     }
                     ++issued;
                 }
@@ -237,14 +268,81 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t first = issued > (uint32_t)kRing ? issued - kRing : 0u;
                 for (uint32_t u = first; u < issued; ++u) {
                     volatile int no_abort = 0;
-                    mbar_wait(&kv_full[u % kRing], (u / kRing) & 1u, &no_abort, nullptr);
+                    mbar_wait(FP8 ? &kv_code[u % kRing] : &kv_full[u % kRing], (u / kRing) & 1u, &no_abort, nullptr);
                 }
+            }
+        } else if (FP8 && warp >= 2) {
+            // ================================ FP8 converter warps ================================
+            // In place, per ring item: the codes of row r (upper half of the slot) become the f16 row
+            // of the layout TMA writes for a 16-bit cache (two 64-column halves, 128-byte swizzle):
+            // K exactly, V as f16(code * row scale) (one rounding). 8 lanes per row, 4 rows per pass:
+            // a row is read entirely before any of it is written. V rows beyond the context are zeroed.
+            const int cw = warp - 2, c = lane & 7;
+            bool cok = mbar_wait(q_full, 0, abort_flag, p.err);
+            if (BF16 && cok) {
+                // q to f16 in place (exact for |q| within f16's range)
+                uint4 *q4 = reinterpret_cast<uint4 *>(sQ);
+                for (int i = cw * 32 + lane; i < 2 * (int)Lay::kQBytes / 16; i += 64) {
+                    const uint4 v = q4[i];
+                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                    uint32_t o[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) o[k] = pack2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xffff0000u), false);
+                    q4[i] = make_uint4(o[0], o[1], o[2], o[3]);
+                }
+                tc::fence_proxy_async_smem();
+            }
+            __syncwarp();
+            if (lane == 0 && cok) mbar_arrive(q_ready);
+            for (int u = 0; cok && u < 2 * n_tiles; ++u) {
+                const int slot = u % kRing, kv = u & 1;
+                if (!(cok = mbar_wait(&kv_code[slot], (uint32_t)(u / kRing) & 1u, abort_flag, p.err))) break;
+                const int n_valid = L - (u >> 1) * kBN;
+                uint8_t *base = sRing + slot * Lay::kKVBytes;
+                const float *sc = sScale + slot * 128;
+                for (int r = cw * 64 + (lane >> 3); r < cw * 64 + 64; r += 4) {
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(base + Lay::kCodeOff + r * 128 + ((c ^ (r & 7)) << 4));
+                    __syncwarp();
+                    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+                    uint32_t h16[8];  // f16 pairs of dims 16c .. 16c+15
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        uint32_t lo, hi;
+                        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(lo) : "h"((unsigned short)(w[k] & 0xffffu)));
+                        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hi) : "h"((unsigned short)(w[k] >> 16)));
+                        h16[2 * k] = lo;
+                        h16[2 * k + 1] = hi;
+                    }
+                    if (kv == 1) {
+                        if (r >= n_valid) {
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) h16[k] = 0u;
+                        } else {
+                            const float sv = sc[r];
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) {
+                                __half2 hh;
+                                memcpy(&hh, &h16[k], 4);
+                                const float2 f = __half22float2(hh);
+                                h16[k] = pack2(f.x * sv, f.y * sv, false);
+                            }
+                        }
+                    }
+                    const int hf = c >> 2, k0 = 2 * (c & 3);
+                    uint8_t *rowp = base + hf * Lay::kTileHalf + r * 128;
+                    *reinterpret_cast<uint4 *>(rowp + ((k0 ^ (r & 7)) << 4)) = make_uint4(h16[0], h16[1], h16[2], h16[3]);
+                    *reinterpret_cast<uint4 *>(rowp + (((k0 + 1) ^ (r & 7)) << 4)) =
+                        make_uint4(h16[4], h16[5], h16[6], h16[7]);
+                }
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&kv_full[slot]);
             }
         } else if (warp == 1) {
             // ===================================== MMA issuer =====================================
             if (lane == 0) {
-                const uint32_t id_qk = tc::idesc_f16(BF16, kBM, kBN, false);
-                const uint32_t id_pv = tc::idesc_f16(BF16, kBM, D, true);
+                const uint32_t id_qk = tc::idesc_f16(MMA_BF16, kBM, kBN, false);
+                const uint32_t id_pv = tc::idesc_f16(MMA_BF16, kBM, D, true);
                 const uint32_t aQ = smem_addr(sQ), aRing = smem_addr(sRing);
                 auto ring_wait = [&](uint32_t u) {
                     return mbar_wait(&kv_full[u % kRing], (u / kRing) & 1u, abort_flag, p.err);
@@ -270,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc::mma_commit(&o_done[x]);
                 };
-                bool ok = mbar_wait(q_full, 0, abort_flag, p.err) && ring_wait(0);
+                bool ok = mbar_wait(FP8 ? q_ready : q_full, 0, abort_flag, p.err) && ring_wait(0);
                 if (ok) {
                     tc::fence_after_sync();
                     qk(0, aRing);  // S_A = Q_A K_0^T
@@ -333,6 +431,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int cc = 0; cc < kBN / 32; ++cc)
                 tc::tmem_ld32(tS + cc * 32, *reinterpret_cast<float(*)[32]>(&s[cc * 32]));
             tc::tmem_wait_ld();
+            if constexpr (FP8) {
+                // K row scales multiply the score columns (FP32); the K slot is freed for the next
+                // copy only after all 8 softmax warps have read them
+                const uint32_t uK = 2u * j, slot = uK % kRing;
+                // the scales came by bulk copy (completion on kv_code); the slot cannot move on to
+                // its next item before these warps arrive on kv_empty below
+                if (!(ok = mbar_wait(&kv_code[slot], (uK / kRing) & 1u, abort_flag, p.err))) break;
+                const float4 *ks4 = reinterpret_cast<const float4 *>(sScale + slot * 128);
+#pragma unroll
+                for (int i = 0; i < kBN / 4; ++i) {
+                    const float4 k4 = ks4[i];
+                    s[4 * i] *= k4.x;
+                    s[4 * i + 1] *= k4.y;
+                    s[4 * i + 2] *= k4.z;
+                    s[4 * i + 3] *= k4.w;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&kv_empty[slot]);
+            }
             // last key index this row may see in this tile (-1: none)
             int lim = L - 1 - kv_start;
             if (p.causal) lim = min(lim, qpos - kv_start);
@@ -371,16 +488,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float2 xq = ffma2(make_float2(s[2 * q], s[2 * q + 1]), c2, nm2);
                     const float2 e = make_float2(fast_exp2(xq.x), fast_exp2(xq.y));
                     l4[q & 3] = fadd2(l4[q & 3], e);
-                    pk[q] = pack2(e.x, e.y, BF16);
+                    pk[q] = pack2(e.x, e.y, MMA_BF16);
                 }
             } else {
 #pragma unroll
                 for (int q = 0; q < kBN / 2; ++q) {
                     const float2 xq = ffma2(make_float2(s[2 * q], s[2 * q + 1]), c2, nm2);
-                    const float2 e = ((q & 7) < kEmuPerEight) ? exp2_fma2<BF16>(xq)
+                    const float2 e = ((q & 7) < kEmuPerEight) ? exp2_fma2<MMA_BF16>(xq)
                                                               : make_float2(fast_exp2(xq.x), fast_exp2(xq.y));
                     l4[q & 3] = fadd2(l4[q & 3], e);
-                    pk[q] = pack2(e.x, e.y, BF16);
+                    pk[q] = pack2(e.x, e.y, MMA_BF16);
                 }
             }
             const float2 l2 = fadd2(fadd2(l4[0], l4[1]), fadd2(l4[2], l4[3]));
@@ -408,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::tmem_wait_st();
             // keys at or beyond the context end may hold unwritten cache bytes: tile A zeroes those V rows
             const int n_valid = L - kv_start;
-            if (x == 0 && n_valid < kBN) {
+            if (!FP8 && x == 0 && n_valid < kBN) {  // (an FP8 cache's converter writes zeros there)
                 const uint32_t uV = 2u * j + 1;
                 if (!(ok = mbar_wait(&kv_full[uV % kRing], (uV / kRing) & 1u, abort_flag, p.err))) break;
                 if (r >= n_valid) {
@@ -551,9 +668,9 @@ cudaError_t encode_fp8_maps(const CacheView &c, int box_rows, CUtensorMap *codes
 
 namespace {
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool FP8>
 cudaError_t launch_t(const PrefillArgs &a, cudaStream_t stream) {
-    using Lay = PrefillLayout<D>;
+    using Lay = PrefillLayout<D, FP8>;
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     const CUtensorMapDataType dt = BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -587,11 +704,12 @@ cudaError_t launch_t(const PrefillArgs &a, cudaStream_t stream) {
     p.num_blocks = a.cache.num_blocks;
     p.scale_log2 = a.scale * kLog2e;
     p.causal = a.causal;
+    p.scales = a.cache.scales;
     p.out = a.out;
     p.out_dtype = a.out_dtype;
     p.lse = a.lse;
     p.err = a.err;
-    auto kern = prefill_kernel<D, BF16>;
+    auto kern = prefill_kernel<D, BF16, FP8>;
     static bool configured[64] = {};
     const int dev = device_info().device;
     if (dev >= 64 || !configured[dev]) {
@@ -608,8 +726,12 @@ cudaError_t launch_t(const PrefillArgs &a, cudaStream_t stream) {
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t s) {
     if (a.max_q_len == 0) return cudaSuccess;
     const bool bf16 = a.cache.dtype == 1;
-    if (a.cache.head_dim == 128) return bf16 ? launch_t<128, true>(a, s) : launch_t<128, false>(a, s);
-    return bf16 ? launch_t<64, true>(a, s) : launch_t<64, false>(a, s);
+    if (a.cache.fp8) {
+        if (a.cache.head_dim != 128) return cudaErrorNotSupported;
+        return bf16 ? launch_t<128, true, true>(a, s) : launch_t<128, false, true>(a, s);
+    }
+    if (a.cache.head_dim == 128) return bf16 ? launch_t<128, true, false>(a, s) : launch_t<128, false, false>(a, s);
+    return bf16 ? launch_t<64, true, false>(a, s) : launch_t<64, false, false>(a, s);
 }
 
 }  // namespace pkv

@@ -172,12 +172,79 @@ def test_fp8_decode_step_append_then_decode():
     check_close(out, ref, W.BF16, roundings=roundings(p), what="fp8 decode step")
 
 
-def test_fp8_prefill_is_refused():
-    p = problem(lens=[40], hq=4, hkv=4, bs=16)
+def prefill_problem(*, lens, q_lens, hq=8, hkv=8, d=128, bs=16, dtype=W.BF16, causal=True, seed=11, extra=5):
+    nb = sum((L + bs - 1) // bs for L in lens) + extra
+    order = torch.randperm(nb, generator=torch.Generator().manual_seed(seed + 3)).tolist()
+    return W.make_problem("fp", batch=len(lens), num_q_heads=hq, num_kv_heads=hkv, head_dim=d, block_size=bs,
+                          context_lens=lens, q_lens=q_lens, dtype=dtype, causal=causal, seed=seed,
+                          num_blocks=nb, free_order=order, kv_format="fp8")
+
+
+def run_prefill_fp8(p, codes, scales, out_dtype=None):
+    lse = torch.empty((p.total_q, p.num_q_heads), dtype=torch.float32, device="cuda")
+    out = pkv.paged_attn_prefill(codes, to_dev(p.q), to_dev(p.cu_q_lens), to_dev(p.context_lens),
+                                 to_dev(p.block_tables), max_q_len=int(p.q_lens.max()), scale=p.scale,
+                                 causal=p.causal, out_dtype=out_dtype, lse=lse, scales=scales)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    return out, lse
+
+
+# Roundings on the FP8 prefill path: the output, P (f16) and V (f16(code * scale)).
+PREFILL_ROUNDINGS = 3
+
+
+@pytest.mark.parametrize("bs", [8, 16, 128, 512])
+def test_fp8_prefill_block_sizes(bs):
+    p = prefill_problem(lens=[300, 129, 700], q_lens=[300, 1, 257], bs=bs, hq=4, hkv=4, seed=bs)
+    codes, scales = device_fp8(p)
+    out, lse = run_prefill_fp8(p, codes, scales)
+    ref, ref_lse = oracle.attention_of(p, host(codes, scales))
+    check_close(out, ref, p.dtype, roundings=PREFILL_ROUNDINGS, what="fp8 prefill bs=%d" % bs)
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-4, atol=1e-4)
+
+
+@pytest.mark.parametrize("dtype", [W.F16, W.BF16])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 4), (32, 1)])
+def test_fp8_prefill_dtypes_gqa_causality(dtype, causal, hq, hkv):
+    p = prefill_problem(lens=[520, 77, 1000], q_lens=[200, 77, 384], hq=hq, hkv=hkv, dtype=dtype, causal=causal,
+                        seed=hq * 7 + hkv)
+    codes, scales = device_fp8(p)
+    out, lse = run_prefill_fp8(p, codes, scales)
+    ref, ref_lse = oracle.attention_of(p, host(codes, scales))
+    check_close(out, ref, dtype, roundings=PREFILL_ROUNDINGS,
+                what="fp8 prefill %s causal=%s hq=%d hkv=%d" % (dtype, causal, hq, hkv))
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-4, atol=1e-4)
+
+
+def test_fp8_prefill_fp32_output():
+    p = prefill_problem(lens=[640, 333], q_lens=[512, 333], hq=4, hkv=4, dtype=W.BF16, bs=32, seed=3)
+    codes, scales = device_fp8(p)
+    out, lse = run_prefill_fp8(p, codes, scales, out_dtype=torch.float32)
+    ref, _ = oracle.attention_of(p, host(codes, scales))
+    check_close(out, ref, W.BF16, roundings=PREFILL_ROUNDINGS - 1, what="fp8 prefill fp32 out")
+
+
+def test_fp8_prefill_chunks_match_decode():
+    """The last row of a causal chunk over the FP8 cache and a decode of that row's query over the
+    same context compute the same attention."""
+    p = prefill_problem(lens=[900, 300], q_lens=[128, 300], hq=8, hkv=2, dtype=W.BF16, seed=21)
+    codes, scales = device_fp8(p)
+    out, _ = run_prefill_fp8(p, codes, scales, out_dtype=torch.float32)
+    last = (p.cu_q_lens[1:] - 1).long()
+    qd = p.q[last].contiguous()
+    dec = pkv.paged_attn_decode(codes, to_dev(qd), to_dev(p.block_tables), to_dev(p.context_lens), scale=p.scale,
+                                out_dtype=torch.float32, scales=scales)
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(out[last.cuda()].cpu().numpy(), dec.cpu().numpy(), atol=2e-2, rtol=0)
+
+
+def test_fp8_prefill_head_dim_64_is_refused():
+    p = prefill_problem(lens=[40], q_lens=[8], hq=4, hkv=4, d=64, bs=16)
     codes, scales = device_fp8(p)
     with pytest.raises(pkv.PkvError) as e:
-        pkv.paged_attn_prefill(codes, to_dev(p.q), to_dev(p.cu_q_lens), to_dev(p.context_lens),
-                               to_dev(p.block_tables), max_q_len=1, scale=p.scale, scales=scales)
+        run_prefill_fp8(p, codes, scales)
     assert e.value.status == 2
 
 

@@ -46,7 +46,8 @@ def parse():
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="", help="comma list of extra workloads (bs_sweep,mixed,prefix,fp8,mqa,prefill,prefill_fp8)")
-    ap.add_argument("--profile", choices=["decode", "append", "prefill", "decode_mixed", "decode_prefix", "decode_fp8"],
+    ap.add_argument("--profile", choices=["decode", "append", "prefill", "decode_mixed", "decode_prefix", "decode_fp8",
+                                          "prefill_fp8"],
                     default=None,
                     help="small case for ncu captures: W + K launches of one kernel, nothing else timed")
     return ap.parse_args()
@@ -117,17 +118,23 @@ def profile_case(args):
         torch.cuda.synchronize()
         assert pkv.get_device_error() == 0
     else:
+        fp8 = args.profile == "prefill_fp8"
         p = W.prefill_long(batch=1, device="cuda")
         shape = (p.num_blocks, 2, p.num_kv_heads, p.block_size, p.head_dim)
-        cache = torch.zeros(shape, dtype=p.q.dtype, device="cuda")
+        if fp8:
+            cache = torch.zeros(shape, dtype=torch.uint8, device="cuda")
+            scales = torch.zeros(shape[:4], dtype=torch.float32, device="cuda")
+        else:
+            cache = torch.zeros(shape, dtype=p.q.dtype, device="cuda")
+            scales = None
         bt = p.block_tables.cuda()
         pkv.kv_cache_append(cache, p.k_ctx.cuda(), p.v_ctx.cuda(), p.cu_ctx_lens.cuda(),
-                            torch.zeros(1, dtype=torch.int32, device="cuda"), bt)
+                            torch.zeros(1, dtype=torch.int32, device="cuda"), bt, scales=scales)
         v = W.prefill_chunk_view(p, 15)
         q = p.q[v["rows"]].cuda()
         cu, ctx = v["cu_q_lens"].cuda(), v["context_lens"].cuda()
         for _ in range(args.warmup + args.steps):
-            pkv.paged_attn_prefill(cache, q, cu, ctx, bt, max_q_len=512, scale=p.scale, causal=True)
+            pkv.paged_attn_prefill(cache, q, cu, ctx, bt, max_q_len=512, scale=p.scale, causal=True, scales=scales)
         torch.cuda.synchronize()
         assert pkv.get_device_error() == 0
     print("profile case done:", args.profile)

@@ -11,7 +11,7 @@
 //
 // CTA = one query head x 256 query rows of one sequence, as two 128-row tiles A and B that share
 // every K/V tile (384 threads, three warpgroups). Over an FP8 cache (head_dim 128) warps 2-3
-// convert each K/V tile in place from E4M3 codes to f16 (V times its row scales), the products run
+// convert each K/V tile in place from E4M3 codes to f16 (V times its row scale), the products run
 // in f16 and the softmax multiplies each score column by its K row scale; otherwise as below:
 //   warp 0     TMA producer: both Q tiles once (3-D tensor map over [total_q, Hq, D]); then for
 //              each 128-key tile j the K tile and the V tile, each into one slot of a 4-slot ring:
@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ================================ FP8 converter warps ================================
             // In place, per ring item: the codes of row r (upper half of the slot) become the f16 row
             // of the layout TMA writes for a 16-bit cache (two 64-column halves, 128-byte swizzle):
-            // K exactly, V as f16(code * row scale) (one rounding). 8 lanes per row, 4 rows per pass:
+            // K exactly, V as f16(code) * f16(row scale) in f16. 8 lanes per row, 4 rows per pass:
             // a row is read entirely before any of it is written. V rows beyond the context are zeroed.
             const int cw = warp - 2, c = lane & 7;
             bool cok = mbar_wait(q_full, 0, abort_flag, p.err);
@@ -304,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint4 raw = *reinterpret_cast<const uint4 *>(base + Lay::kCodeOff + r * 128 + ((c ^ (r & 7)) << 4));
                     __syncwarp();
                     const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-                    uint32_t h16[8];  // f16 pairs of dims 16c .. 16c+15
+                    uint32_t h16[8];  // f16 pairs of dims 16c .. 16c+15 (exact)
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         uint32_t lo, hi;
@@ -318,21 +318,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int k = 0; k < 8; ++k) h16[k] = 0u;
                         } else {
-                            const float sv = sc[r];
+                            // f16 products: the scale rounded to f16, then the product (two roundings,
+                            // each within half an f16 ulp)
+                            const __half2 sv = __float2half2_rn(sc[r]);
 #pragma unroll
                             for (int k = 0; k < 8; ++k) {
                                 __half2 hh;
                                 memcpy(&hh, &h16[k], 4);
-                                const float2 f = __half22float2(hh);
-                                h16[k] = pack2(f.x * sv, f.y * sv, false);
+                                hh = __hmul2(hh, sv);
+                                memcpy(&h16[k], &hh, 4);
                             }
                         }
                     }
                     const int hf = c >> 2, k0 = 2 * (c & 3);
                     uint8_t *rowp = base + hf * Lay::kTileHalf + r * 128;
-                    *reinterpret_cast<uint4 *>(rowp + ((k0 ^ (r & 7)) << 4)) = make_uint4(h16[0], h16[1], h16[2], h16[3]);
-                    *reinterpret_cast<uint4 *>(rowp + (((k0 + 1) ^ (r & 7)) << 4)) =
-                        make_uint4(h16[4], h16[5], h16[6], h16[7]);
+                    // the two halves' lanes store opposite chunks first: the row's 8 stores of each
+                    // instruction then fill all 32 banks once
+                    const uint4 v0 = make_uint4(h16[0], h16[1], h16[2], h16[3]);
+                    const uint4 v1 = make_uint4(h16[4], h16[5], h16[6], h16[7]);
+                    const int ka = hf ? k0 + 1 : k0, kb = hf ? k0 : k0 + 1;
+                    *reinterpret_cast<uint4 *>(rowp + ((ka ^ (r & 7)) << 4)) = hf ? v1 : v0;
+                    *reinterpret_cast<uint4 *>(rowp + ((kb ^ (r & 7)) << 4)) = hf ? v0 : v1;
                 }
                 tc::fence_proxy_async_smem();
                 __syncwarp();

@@ -45,7 +45,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", default="", help="comma list of extra workloads (bs_sweep,mixed,prefix,fp8,mqa,prefill,prefill_fp8)")
+    ap.add_argument("--only", default="", help="comma list of extra workloads (bs_sweep,mixed,prefix,fp8,mqa,mixed_call,prefill,prefill_fp8)")
     ap.add_argument("--profile", choices=["decode", "append", "prefill", "decode_mixed", "decode_prefix", "decode_fp8",
                                           "prefill_fp8"],
                     default=None,
@@ -579,6 +579,55 @@ def bench_mqa(torch, steps, warmup):
             "tokens_per_s": round(p.batch / ms * 1e3, 1)}
 
 
+def bench_mixed_call(torch, steps, warmup):
+    """One paged_attn_mixed call over 64 decode sequences and 4 prefill chunks, against the same
+    work as a decode call plus a prefill call."""
+    import paged_kv_flash_cache_gb300 as pkv
+    from paged_kv_flash_cache_gb300 import workloads as W
+    gen = torch.Generator().manual_seed(1243)
+    dec_lens = torch.randint(1024, 8193, (64,), generator=gen).tolist()
+    chunk_lens = [2048, 4096, 6144, 8192]
+    lens = dec_lens + chunk_lens
+    q_lens = [1] * 64 + [512] * 4
+    nb = sum((L + 15) // 16 for L in lens)
+    order = torch.randperm(nb, generator=gen).tolist()
+    p = W.make_problem("mixed_call", batch=len(lens), num_q_heads=32, num_kv_heads=32, head_dim=128, block_size=16,
+                       context_lens=lens, q_lens=q_lens, dtype=W.BF16, causal=True, seed=1244, num_blocks=nb,
+                       free_order=order, pool_init="none", device="cuda")
+    cache = device_problem(p, torch)
+    q, bt, ctx, cu = p.q.cuda(), p.block_tables.cuda(), p.context_lens.cuda(), p.cu_q_lens.cuda()
+    ws = torch.empty(max(16, pkv.decode_workspace_size(p.batch, 32, 32, 128, 16, bt.shape[1])), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.empty_like(q)
+    mixed = lambda i: pkv.paged_attn_mixed(cache, q, cu, ctx, bt, max_q_len=512, scale=p.scale, workspace=ws, out=out)
+    qd, qp = q[:64].contiguous(), q[64:].contiguous()
+    bt_d, bt_p = bt[:64].contiguous(), bt[64:].contiguous()
+    ctx_d, ctx_p = ctx[:64].contiguous(), ctx[64:].contiguous()
+    cu_p = torch.tensor([0, 512, 1024, 1536, 2048], dtype=torch.int32, device="cuda")
+    od, op = torch.empty_like(qd), torch.empty_like(qp)
+    ws_d = torch.empty(max(16, pkv.decode_workspace_size(64, 32, 32, 128, 16, bt.shape[1])), dtype=torch.uint8,
+                       device="cuda")
+
+    def separate(i):
+        pkv.paged_attn_decode(cache, qd, bt_d, ctx_d, scale=p.scale, workspace=ws_d, out=od)
+        pkv.paged_attn_prefill(cache, qp, cu_p, ctx_p, bt_p, max_q_len=512, scale=p.scale, causal=True, out=op)
+
+    res = {}
+    for name, fn in (("mixed", mixed), ("separate", separate)):
+        for i in range(warmup):
+            fn(i)
+        res[name] = time_loop(torch, fn, steps, torch.cuda.current_stream()) / steps
+    kv_dec = sum(dec_lens) * 32 * 128 * 2 * 2
+    flops = 4 * 128 * 32 * (sum(dec_lens) + sum(512 * (L - 512) + 512 * 513 // 2 for L in chunk_lens))
+    del cache
+    torch.cuda.empty_cache()
+    return {"workload": "one call: 64 decode sequences (contexts U[1024, 8192]) + 4 prefill chunks of 512 "
+                        "(contexts 2k-8k), 32 heads x 128, bf16, bs 16",
+            "ms": round(res["mixed"], 4), "separate_calls_ms": round(res["separate"], 4),
+            "decode_kv_bytes": kv_dec, "flops": flops, "tflops": round(flops / res["mixed"] / 1e9, 1),
+            "rows_per_s": round((64 + 2048) / res["mixed"] * 1e3, 1)}
+
+
 def bench_prefill(torch, steps, warmup, fp8=False):
     import paged_kv_flash_cache_gb300 as pkv
     from paged_kv_flash_cache_gb300 import workloads as W
@@ -729,7 +778,7 @@ def main():
         only = set(filter(None, args.only.split(",")))
         for name, fn in (("bs_sweep", bench_bs_sweep), ("mixed", bench_mixed), ("prefix", bench_prefix),
                          ("fp8", lambda t, k, w: bench_fp8(t, k, w, r["decode_ms"])), ("mqa", bench_mqa),
-                         ("prefill", bench_prefill),
+                         ("mixed_call", bench_mixed_call), ("prefill", bench_prefill),
                          ("prefill_fp8", lambda t, k, w: bench_prefill(t, k, w, fp8=True))):
             if only and name not in only:
                 continue

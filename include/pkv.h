@@ -177,6 +177,23 @@ PKV_API pkv_status pkv_paged_attn_prefill(pkv_cache cache, const void *q, int nu
                                   int total_q, int max_q_len, float scale, int causal,
                                   void *out, pkv_dtype out_dtype, float *lse, void *stream);
 
+/* paged_attn_mixed -- one call over a batch that mixes decode sequences (exactly one query
+ * row) and prefill chunks (several query rows, their K/V already appended): prefill and
+ * decode in one step, as a continuously batched serving loop issues them ([ON2] continuous
+ * batching; "Prefill/Decode mixed execution"). Arguments as pkv_paged_attn_prefill (q, out,
+ * lse indexed by the rows of cu_q_lens; causal applies to the chunks, a single row sees its
+ * whole context either way) plus num_splits / workspace as pkv_paged_attn_decode, sized by
+ * pkv_decode_workspace_size(batch, ...). The single-row sequences run on the decode kernels
+ * (split-KV, one unit per KV head's query group), the others on the prefill kernel; each
+ * kernel leaves the other kind's rows untouched. The decode constraints (head grouping,
+ * batch <= 2048) apply to the whole call. */
+PKV_API pkv_status pkv_paged_attn_mixed(pkv_cache cache, const void *q, int num_q_heads,
+                                const int *cu_q_lens, const int *context_lens,
+                                const int *block_tables, int batch, int max_blocks_per_seq,
+                                int total_q, int max_q_len, float scale, int causal,
+                                int num_splits, void *workspace, size_t workspace_bytes,
+                                void *out, pkv_dtype out_dtype, float *lse, void *stream);
+
 /* attn_combine -- log-sum-exp merge of split-KV partial results ([FAPA] s2: the
  * same rescale-by-exp(m_old - m_new) identity applied to whole splits).
  *   partial_o     FP32 [n_rows, num_splits, head_dim]: each split's output,

@@ -7,7 +7,7 @@ caller does not pass them, and forwards raw device pointers and the current CUDA
 stream. There is no CPU fallback: if the library is missing every call raises.
 
 Entry points (same names as the C ABI without the ``pkv_`` prefix):
-  kv_cache_append, paged_attn_decode, paged_attn_prefill, attn_combine,
+  kv_cache_append, paged_attn_decode, paged_attn_prefill, paged_attn_mixed, attn_combine,
   decode_workspace_size, decode_split_tokens, get_device_error.
 Cache tensors have shape [num_blocks, 2, num_kv_heads, block_size, head_dim]
 (K at index 0, V at index 1) in float16 or bfloat16, or hold FP8 E4M3 codes
@@ -26,7 +26,7 @@ from typing import Optional
 __all__ = [
     "PkvError", "library_path", "load_library", "kv_cache_append", "paged_attn_decode", "paged_attn_prefill",
     "attn_combine", "decode_workspace_size", "decode_split_tokens", "get_device_error", "STATUS",
-    "paged_attn_decode_noalloc",
+    "paged_attn_decode_noalloc", "paged_attn_mixed",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -41,8 +41,8 @@ KV_NATIVE, KV_FP8_E4M3 = 0, 1
 
 # Every symbol include/pkv.h declares.
 EXPORTS = ("pkv_kv_cache_append", "pkv_decode_workspace_size", "pkv_decode_split_tokens", "pkv_paged_attn_decode",
-           "pkv_paged_attn_decode_noalloc", "pkv_paged_attn_prefill", "pkv_attn_combine", "pkv_get_device_error",
-           "pkv_status_string", "pkv_version")
+           "pkv_paged_attn_decode_noalloc", "pkv_paged_attn_prefill", "pkv_paged_attn_mixed", "pkv_attn_combine",
+           "pkv_get_device_error", "pkv_status_string", "pkv_version")
 DECODE_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024   # PKV_DECODE_NOALLOC_SCRATCH_BYTES in include/pkv.h
 
 
@@ -85,6 +85,8 @@ def load_library():
         lib.pkv_paged_attn_decode_noalloc.restype = I
         lib.pkv_paged_attn_prefill.argtypes = [_Cache, P, I, P, P, P, I, I, I, I, F, I, P, I, P, P]
         lib.pkv_paged_attn_prefill.restype = I
+        lib.pkv_paged_attn_mixed.argtypes = [_Cache, P, I, P, P, P, I, I, I, I, F, I, I, P, Z, P, I, P, P]
+        lib.pkv_paged_attn_mixed.restype = I
         lib.pkv_attn_combine.argtypes = [P, P, I, I, I, P, I, P, P]
         lib.pkv_attn_combine.restype = I
         lib.pkv_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
@@ -262,6 +264,31 @@ def paged_attn_prefill(cache, q, cu_q_lens, context_lens, block_tables, max_q_le
                                       mb, total_q, int(max_q_len), scale, 1 if causal else 0, _dev(out, "out"),
                                       _dtype_code(out.dtype), _dev(lse, "lse"), _stream(stream)),
            "pkv_paged_attn_prefill")
+    return out
+
+
+def paged_attn_mixed(cache, q, cu_q_lens, context_lens, block_tables, max_q_len: int,
+                     scale: Optional[float] = None, causal: bool = True, num_splits: int = 0, workspace=None,
+                     out=None, out_dtype=None, lse=None, stream=None, scales=None):
+    """One call over a batch mixing decode rows (q_len 1) and prefill chunks (q_len > 1):
+    q [sum q_len, Hq, D], rows by cu_q_lens. Returns `out`."""
+    torch = _torch()
+    lib = load_library()
+    c = _cache_struct(cache, q.dtype, scales)
+    total_q, hq, d = q.shape
+    batch, mb = block_tables.shape
+    if out is None:
+        out = torch.empty((total_q, hq, d), dtype=out_dtype or q.dtype, device=q.device)
+    need = decode_workspace_size(batch, hq, cache.shape[2], d, cache.shape[3], mb, num_splits)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    scale = (1.0 / math.sqrt(d)) if scale is None else float(scale)
+    _check(lib.pkv_paged_attn_mixed(c, _dev(q, "q"), hq, _i32(cu_q_lens, "cu_q_lens"), _i32(context_lens, "context_lens"),
+                                    _i32(block_tables, "block_tables"), batch, mb, total_q, int(max_q_len), scale,
+                                    1 if causal else 0, int(num_splits), _dev(workspace, "workspace"), ws_bytes,
+                                    _dev(out, "out"), _dtype_code(out.dtype), _dev(lse, "lse"), _stream(stream)),
+           "pkv_paged_attn_mixed")
     return out
 
 

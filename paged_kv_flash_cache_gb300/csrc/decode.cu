@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
                     }
                 }
                 if (first_tile && lane == 0) {
-                    const uint16_t *qsrc = qg + ((size_t)c.b * a.num_q_heads + (size_t)c.kvh * G) * D;
+                    const uint16_t *qsrc = qg + ((size_t)ut.qrow[c.b] * a.num_q_heads + (size_t)c.kvh * G) * D;
                     bulk_g2s(st + 2 * L::kKBytes, qsrc, (uint32_t)L::kQBytes, &full[stage], pol);
                 }
                 issued_mask |= 1u << stage;
@@ -542,13 +542,19 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
     const int lane = threadIdx.x & 31;
     int S = a.num_splits;
     bool done_by_split = false;
+    size_t out_row = (size_t)row;
     if (row < a.n_rows && a.context_lens) {
         const int b = row / a.rows_per_seq;
         int len = __ldg(a.context_lens + b);
         len = len < 0 ? 0 : len;
+        if (a.cu_q_lens) {  // mixed batch: rows of prefill chunks are not this kernel's
+            const int q0 = __ldg(a.cu_q_lens + b);
+            if (__ldg(a.cu_q_lens + b + 1) - q0 != 1) done_by_split = true;
+            out_row = (size_t)q0 * a.rows_per_seq + (row - b * a.rows_per_seq);
+        }
         S = (len + a.chunk - 1) / a.chunk;
         if (S > a.num_splits) S = a.num_splits;
-        done_by_split = (S == 1);  // finished by the split kernel
+        done_by_split = done_by_split || (S == 1);  // (or finished by the split kernel)
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (row >= a.n_rows || done_by_split) return;
@@ -584,8 +590,8 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) store_out(a.out, (size_t)row * D + lane * kPer + j, o_acc[j] * inv, a.out_dtype);
-    if (lane == 0 && a.lse) a.lse[row] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
+    for (int j = 0; j < kPer; ++j) store_out(a.out, out_row * D + lane * kPer + j, o_acc[j] * inv, a.out_dtype);
+    if (lane == 0 && a.lse) a.lse[out_row] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
 }
 
 template <typename Tag, int D, int G, bool FP8>

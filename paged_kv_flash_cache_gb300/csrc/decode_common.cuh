@@ -26,12 +26,13 @@ struct UnitCursor {
 //   first [s_max + 1]  first[s] = sum over sequences of min(splits, s); split s's units start at
 //                      first[s] * hkv and number n_s * hkv, n_s = first[s + 1] - first[s]
 //   hist  [s_max + 1]  prologue scratch: sequences per split count, then a fill count
+//   qrow  [batch]      the sequence's query / output row (b, or cu_q_lens[b] in a mixed batch)
 struct UnitTable {
-    int *lens, *ord, *first, *hist;
+    int *lens, *ord, *first, *hist, *qrow;
 };
 
 __host__ __device__ constexpr size_t unit_table_ints(int batch, int s_max) {
-    return 2 * (size_t)batch + 2 * ((size_t)s_max + 1);
+    return 3 * (size_t)batch + 2 * ((size_t)s_max + 1);
 }
 
 __device__ __forceinline__ UnitTable unit_table(int *ints, int batch, int s_max) {
@@ -40,6 +41,7 @@ __device__ __forceinline__ UnitTable unit_table(int *ints, int batch, int s_max)
     t.ord = ints + batch;
     t.first = ints + 2 * batch;
     t.hist = t.first + s_max + 1;
+    t.qrow = t.hist + s_max + 1;
     return t;
 }
 
@@ -135,20 +137,22 @@ __device__ __forceinline__ bool merge_warp_loop(const DecodeArgs &a, const UnitT
 #pragma unroll
             for (int w = 0; w < W; ++w) wv[w] = __shfl_sync(0xffffffffu, wgt, w);
             const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-            const size_t row_id = (size_t)c.b * a.num_q_heads + (size_t)c.kvh * G + g;
+            const size_t head = (size_t)c.kvh * G + g;
+            const size_t row_id = (size_t)c.b * a.num_q_heads + head;                 // partials
+            const size_t out_row = (size_t)ut.qrow[c.b] * a.num_q_heads + head;       // output
 #pragma unroll
             for (int d = lane; d < D; d += 32) {
                 float o = 0.f;
 #pragma unroll
                 for (int w = 0; w < W; ++w) o += rg[(size_t)w * G * (D + 2) + d] * wv[w];
                 const float res = o * inv;
-                if (splits == 1) store_out(a.out, row_id * D + d, res, a.out_dtype);
+                if (splits == 1) store_out(a.out, out_row * D + d, res, a.out_dtype);
                 else a.part_o[(row_id * a.s_max + c.split) * D + d] = res;
             }
             if (lane == 0) {
                 const float lse_v = lsum > 0.f ? (M + log2f(lsum)) * kLn2 : -INFINITY;
                 if (splits == 1) {
-                    if (a.lse) a.lse[row_id] = lse_v;
+                    if (a.lse) a.lse[out_row] = lse_v;
                 } else {
                     a.part_lse[row_id * a.s_max + c.split] = lse_v;
                 }
@@ -178,7 +182,14 @@ __device__ __forceinline__ int decode_scan_units(const DecodeArgs &a, const Unit
             set_error(a.err, kErrDeviceRange);
             len = len < 0 ? 0 : cap;
         }
+        int qrow = i;
+        if (a.cu_q_lens) {  // mixed batch: only single-row sequences are decoded here
+            const int q0 = __ldg(a.cu_q_lens + i), q1 = __ldg(a.cu_q_lens + i + 1);
+            qrow = q0;
+            if (q1 - q0 != 1) len = 0;
+        }
         t.lens[i] = len;
+        t.qrow[i] = qrow;
         atomicAdd(&t.hist[(len + chunk - 1) / chunk], 1);  // split count <= S since len <= cap
     }
     __syncthreads();

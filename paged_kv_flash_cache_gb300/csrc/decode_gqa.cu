@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (first_tile && lane == 0) {
-                    const uint16_t *qsrc = qg + ((size_t)c.b * a.num_q_heads + (size_t)c.kvh * G) * D;
+                    const uint16_t *qsrc = qg + ((size_t)ut.qrow[c.b] * a.num_q_heads + (size_t)c.kvh * G) * D;
                     bulk_g2s(st + 2 * L::kKBytes, qsrc, L::kQBytes, &full[stage], pol);
                 }
                 issued_mask |= 1u << stage;

@@ -186,10 +186,17 @@ size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads, i
     return (size_t)batch * num_q_heads * s_max * (head_dim + 1) * sizeof(float);
 }
 
-pkv_status pkv_paged_attn_decode(pkv_cache cache, const void *q, int num_q_heads, const int *block_tables,
-                                 const int *context_lens, int batch, int max_blocks_per_seq, float scale,
-                                 int num_splits, void *workspace, size_t workspace_bytes, void *out,
-                                 pkv_dtype out_dtype, float *lse, void *stream) {
+}  // extern "C"
+
+namespace pkv {
+namespace {
+
+// The decode call; cu_q_lens != nullptr decodes only the single-row sequences of a mixed batch
+// (their rows cu_q_lens[b]) and leaves the other rows untouched.
+pkv_status decode_impl(const pkv_cache &cache, const void *q, int num_q_heads, const int *block_tables,
+                       const int *context_lens, const int *cu_q_lens, int batch, int max_blocks_per_seq,
+                       float scale, int num_splits, void *workspace, size_t workspace_bytes, void *out,
+                       pkv_dtype out_dtype, float *lse, void *stream) {
     pkv_status st = check_cache(cache);
     if (st != PKV_OK) return st;
     if ((st = check_out_dtype(out_dtype, cache.dtype)) != PKV_OK) return st;
@@ -223,6 +230,7 @@ pkv_status pkv_paged_attn_decode(pkv_cache cache, const void *q, int num_q_heads
     a.chunk = chunk;
     a.s_max = s_max;
     a.head_groups = group > 8 ? group / 8 : 1;
+    a.cu_q_lens = cu_q_lens;
     a.part_o = static_cast<float *>(workspace);
     a.part_lse = need > 0 ? a.part_o + (size_t)batch * num_q_heads * s_max * cache.head_dim : nullptr;
     a.out = out;
@@ -247,11 +255,25 @@ pkv_status pkv_paged_attn_decode(pkv_cache cache, const void *q, int num_q_heads
     c.context_lens = context_lens;
     c.rows_per_seq = num_q_heads;
     c.chunk = chunk;
+    c.cu_q_lens = cu_q_lens;
     c.out = out;
     c.out_dtype = (int)out_dtype;
     c.lse = lse;
     if (launch_combine(c, cs) != cudaSuccess) return PKV_ERR_CUDA;
     return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" {
+
+pkv_status pkv_paged_attn_decode(pkv_cache cache, const void *q, int num_q_heads, const int *block_tables,
+                                 const int *context_lens, int batch, int max_blocks_per_seq, float scale,
+                                 int num_splits, void *workspace, size_t workspace_bytes, void *out,
+                                 pkv_dtype out_dtype, float *lse, void *stream) {
+    return decode_impl(cache, q, num_q_heads, block_tables, context_lens, nullptr, batch, max_blocks_per_seq, scale,
+                       num_splits, workspace, workspace_bytes, out, out_dtype, lse, stream);
 }
 
 pkv_status pkv_attn_combine(const float *partial_o, const float *partial_lse, int n_rows, int num_splits,
@@ -270,6 +292,7 @@ pkv_status pkv_attn_combine(const float *partial_o, const float *partial_lse, in
     c.num_splits = num_splits;
     c.head_dim = head_dim;
     c.context_lens = nullptr;
+    c.cu_q_lens = nullptr;
     c.rows_per_seq = 1;
     c.chunk = 1;
     c.out = out;
@@ -278,10 +301,16 @@ pkv_status pkv_attn_combine(const float *partial_o, const float *partial_lse, in
     return launch_combine(c, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-pkv_status pkv_paged_attn_prefill(pkv_cache cache, const void *q, int num_q_heads, const int *cu_q_lens,
-                                  const int *context_lens, const int *block_tables, int batch,
-                                  int max_blocks_per_seq, int total_q, int max_q_len, float scale, int causal,
-                                  void *out, pkv_dtype out_dtype, float *lse, void *stream) {
+}  // extern "C"
+
+namespace pkv {
+namespace {
+
+// The prefill call; skip_single leaves the single-row sequences of a mixed batch to the decode.
+pkv_status prefill_impl(const pkv_cache &cache, const void *q, int num_q_heads, const int *cu_q_lens,
+                        const int *context_lens, const int *block_tables, int batch, int max_blocks_per_seq,
+                        int total_q, int max_q_len, float scale, int causal, void *out, pkv_dtype out_dtype,
+                        float *lse, void *stream, int skip_single) {
     pkv_status st = check_cache(cache);
     if (st != PKV_OK) return st;
     if (cache.format == PKV_KV_FP8_E4M3 && cache.head_dim != 128) return PKV_ERR_UNSUPPORTED;
@@ -308,6 +337,7 @@ pkv_status pkv_paged_attn_prefill(pkv_cache cache, const void *q, int num_q_head
     a.max_q_len = max_q_len;
     a.scale = scale;
     a.causal = causal ? 1 : 0;
+    a.skip_single = skip_single;
     a.out = out;
     a.out_dtype = (int)out_dtype;
     a.lse = lse;
@@ -315,6 +345,34 @@ pkv_status pkv_paged_attn_prefill(pkv_cache cache, const void *q, int num_q_head
     cudaError_t e = launch_prefill(a, static_cast<cudaStream_t>(stream));
     if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" {
+
+pkv_status pkv_paged_attn_prefill(pkv_cache cache, const void *q, int num_q_heads, const int *cu_q_lens,
+                                  const int *context_lens, const int *block_tables, int batch,
+                                  int max_blocks_per_seq, int total_q, int max_q_len, float scale, int causal,
+                                  void *out, pkv_dtype out_dtype, float *lse, void *stream) {
+    return prefill_impl(cache, q, num_q_heads, cu_q_lens, context_lens, block_tables, batch, max_blocks_per_seq,
+                        total_q, max_q_len, scale, causal, out, out_dtype, lse, stream, 0);
+}
+
+pkv_status pkv_paged_attn_mixed(pkv_cache cache, const void *q, int num_q_heads, const int *cu_q_lens,
+                                const int *context_lens, const int *block_tables, int batch, int max_blocks_per_seq,
+                                int total_q, int max_q_len, float scale, int causal, int num_splits, void *workspace,
+                                size_t workspace_bytes, void *out, pkv_dtype out_dtype, float *lse, void *stream) {
+    if (!cu_q_lens && batch > 0) return PKV_ERR_INVALID_ARG;
+    // decode rows first (split kernel + merge), then the prefill chunks; each kernel leaves the
+    // other kind's rows alone
+    pkv_status st = decode_impl(cache, q, num_q_heads, block_tables, context_lens, cu_q_lens, batch,
+                                max_blocks_per_seq, scale, num_splits, workspace, workspace_bytes, out, out_dtype,
+                                lse, stream);
+    if (st != PKV_OK) return st;
+    return prefill_impl(cache, q, num_q_heads, cu_q_lens, context_lens, block_tables, batch, max_blocks_per_seq,
+                        total_q, max_q_len, scale, causal, out, out_dtype, lse, stream, 1);
 }
 
 pkv_status pkv_get_device_error(void *stream, int *code) {

@@ -43,6 +43,10 @@ struct DecodeArgs {
     // else 1: the tensor-core kernels then take each group as a "virtual" KV head -- unit head v
     // reads KV head v / head_groups and serves query heads 8v .. 8v + 7.
     int head_groups;
+    // Mixed batch (prefill chunks and decode rows in one call): cu_q_lens [batch + 1] of the call's
+    // q / out rows; only sequences with exactly one query row are decoded here, their row being
+    // cu_q_lens[b]. nullptr: every sequence has one query row, row b.
+    const int *cu_q_lens;
     int s_max;   // splits a full-capacity context uses: ceil(max_blocks_per_seq * block_size / chunk)
     float *part_o;    // [batch, Hq, s_max, D]
     float *part_lse;  // [batch, Hq, s_max]
@@ -59,6 +63,9 @@ struct CombineArgs {
     // splits; rows with exactly one split were finished by the decode kernel.
     const int *context_lens;
     int rows_per_seq, chunk;
+    // mixed batch: row r = b * rows_per_seq + h goes to output row cu_q_lens[b] * rows_per_seq + h,
+    // and only for sequences with exactly one query row (nullptr: output row r)
+    const int *cu_q_lens;
     void *out;
     int out_dtype;
     float *lse;
@@ -72,6 +79,7 @@ struct PrefillArgs {
     int batch, max_blocks_per_seq, total_q, max_q_len;
     float scale;
     int causal;
+    int skip_single;  // mixed batch: sequences with one query row are the decode's
     void *out;
     int out_dtype;
     float *lse;

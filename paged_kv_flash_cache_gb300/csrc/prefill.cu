@@ -72,6 +72,7 @@ struct PrefillParams {
     int batch, mb, num_q_heads, num_kv_heads, group, bs, log2_bs, num_blocks;
     float scale_log2;
     int causal;
+    int skip_single;      // mixed batch: leave sequences with one query row to the decode kernels
     const float *scales;  // FP8 cache: FP32 row scales [NB, 2, Hkv, bs]
     void *out;
     int out_dtype;
@@ -159,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q0 = __ldg(p.cu_q_lens + b);
     const int q_len = __ldg(p.cu_q_lens + b + 1) - q0;
     const int m_start = mt * kRows;
-    if (m_start >= q_len) return;  // uniform: nothing allocated yet
+    if (m_start >= q_len || (p.skip_single && q_len == 1)) return;  // uniform: nothing allocated yet
     const int L = __ldg(p.context_lens + b);
     if (L > p.mb * p.bs || q_len > L || L < 0) {
         if (threadIdx.x == 0) set_error(p.err, kErrDeviceRange);
@@ -710,6 +711,7 @@ cudaError_t launch_t(const PrefillArgs &a, cudaStream_t stream) {
     p.num_blocks = a.cache.num_blocks;
     p.scale_log2 = a.scale * kLog2e;
     p.causal = a.causal;
+    p.skip_single = a.skip_single;
     p.scales = a.cache.scales;
     p.out = a.out;
     p.out_dtype = a.out_dtype;

@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp < 4) {
-        tc::regs_dec<56>();
+        tc::regs_dec<72>();
         if (warp == 0) {
             // ==================================== TMA producer ====================================
             const int box_rows = p.bs < kBN ? p.bs : kBN;
@@ -414,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
         }
     } else {
-        tc::regs_inc<224>();
+        tc::regs_inc<208>();
         // ================================= softmax + epilogue =================================
         const int x = (warp >> 2) - 1;                 // 0: tile A, 1: tile B
         const int quarter = warp & 3;                  // TMEM lanes 32*quarter .. +31

@@ -42,21 +42,22 @@ constexpr int kProducerWarp = kWarps;
 constexpr int kMergeWarp = kWarps + 1;
 constexpr int kThreads = (kWarps + 2) * 32;
 constexpr int kTile = 64;                         // tokens per stage
-constexpr int kStagesG = 4;
+constexpr int kStagesMax = 4;
 constexpr int kMaxBatchG = 2048;
 constexpr float kRescale = 8.0f;                  // lazy rescale threshold (log2 units)
 
 template <int D, int G>
 struct GqaLayout {
+    static constexpr int kStages = G > 8 ? 3 : kStagesMax;  // 16 heads: the merge buffers need a stage's room
     static constexpr int kHalves = D / 64;                          // 128-byte swizzle atoms along D
     static constexpr uint32_t kHalfBytes = kTile * 128;             // 64 rows x 128 bytes
     static constexpr uint32_t kKBytes = kHalves * kHalfBytes;       // one K (or V) tile
     static constexpr uint32_t kQBytes = G * D * 2;
     static constexpr uint32_t kStageBytes = (2 * kKBytes + kQBytes + 1023) / 1024 * 1024;
-    static constexpr uint32_t kBarOffset = kStagesG * kStageBytes;
+    static constexpr uint32_t kBarOffset = kStages * kStageBytes;
     // barriers: full / empty per stage, merge full / empty per merge buffer; then the abort flag
     // (padded to 16 bytes), the unit of each stage and the unit of each merge buffer
-    static constexpr uint32_t kMergeOffset = kBarOffset + (2 * kStagesG + 4) * 8 + 64;
+    static constexpr uint32_t kMergeOffset = kBarOffset + (2 * kStages + 4) * 8 + 64;
     static constexpr uint32_t kMergeFloats = kWarps * G * (D + 2);  // one of two merge buffers
     static constexpr uint32_t kIntsOffset = kMergeOffset + 2 * kMergeFloats * 4;
     __host__ __device__ static size_t smem_bytes(int batch, int s_max) {
@@ -74,6 +75,7 @@ template <int D, int G, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_gqa_kernel(const __grid_constant__ CUtensorMap tm_kv, DecodeArgs a) {
     using L = GqaLayout<D, G>;
+    constexpr int kStagesG = L::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kBarOffset);
@@ -200,11 +202,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ===================================== consumer warps =====================================
+    // The group's heads fill NT n-tiles of 8 head slots (NT = 2 for 16 heads; padding slots zero).
     constexpr int kKSteps = D / 16;         // k-steps of q.K^T, m-tiles of O^T
+    constexpr int NT = (G + 7) / 8;
     const int gid = lane >> 2, tig = lane & 3;
-    const int g_lo = 2 * tig;               // this lane's two head slots (columns of S^T / O^T)
+    const int g_lo = 2 * tig;               // this lane's two head slots of each n-tile
     const float sl = a.scale * kLog2e;
-    uint32_t bq[kKSteps][2];                // q as B fragments (n = head slot, k = dims)
+    uint32_t bq[kKSteps][NT][2];            // q as B fragments (n = head slot, k = dims)
     int stage = 0;
     uint32_t phase = 0;
     int mbuf = 0;  // merge buffer of the next unit
@@ -214,10 +218,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int u = stage_unit[stage];
         if (u < 0) break;
         const UnitCursor c = unit_of(u, ut, a.s_max, hu, chunk);
-        float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-        float o[kKSteps][4];
+        float m[NT][2], l[NT][2];
+        float o[kKSteps][NT][4];
 #pragma unroll
-        for (int mt = 0; mt < kKSteps; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+        for (int nt = 0; nt < NT; ++nt) {
+            m[nt][0] = m[nt][1] = -INFINITY;
+            l[nt][0] = l[nt][1] = 0.f;
+#pragma unroll
+            for (int mt = 0; mt < kKSteps; ++mt) o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
+        }
         for (int ts = c.t0; ts < c.t1; ts += kTile) {
             const int n = min(kTile, c.t1 - ts);
             if (ts != c.t0 && !mbar_wait(&full[stage], phase, abort_flag, a.err)) return;
@@ -226,12 +235,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ts == c.t0) {
                 const uint16_t *sq = reinterpret_cast<const uint16_t *>(st + 2 * L::kKBytes);
 #pragma unroll
-                for (int kk = 0; kk < kKSteps; ++kk) {
-                    if (gid < G) {
-                        bq[kk][0] = *reinterpret_cast<const uint32_t *>(sq + gid * D + kk * 16 + 2 * tig);
-                        bq[kk][1] = *reinterpret_cast<const uint32_t *>(sq + gid * D + kk * 16 + 8 + 2 * tig);
-                    } else {
-                        bq[kk][0] = bq[kk][1] = 0u;
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int hs = nt * 8 + gid;  // head slot
+#pragma unroll
+                    for (int kk = 0; kk < kKSteps; ++kk) {
+                        if (hs < G) {
+                            bq[kk][nt][0] = *reinterpret_cast<const uint32_t *>(sq + hs * D + kk * 16 + 2 * tig);
+                            bq[kk][nt][1] = *reinterpret_cast<const uint32_t *>(sq + hs * D + kk * 16 + 8 + 2 * tig);
+                        } else {
+                            bq[kk][nt][0] = bq[kk][nt][1] = 0u;
+                        }
                     }
                 }
             }
@@ -248,8 +261,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
             }
-            // ---- S^T = K_w q^T: 16 tokens x 8 head slots ----
-            float s[4] = {0.f, 0.f, 0.f, 0.f};
+            // ---- S^T = K_w q^T: 16 tokens x 8 head slots per n-tile (one K fragment for all) ----
+            float s[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
             {
                 const int mi = lane >> 3;
                 const int t = t0w + (lane & 7) + 8 * (mi & 1);
@@ -258,54 +273,59 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t af[4];
                     const int cc = 2 * (kk & 3) + (mi >> 1);
                     ldsm_x4(swz(aK + (kk >> 2) * L::kHalfBytes, t, cc), af);
-                    mma16816<BF16>(s, af, bq[kk][0], bq[kk][1]);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) mma16816<BF16>(s[nt], af, bq[kk][nt][0], bq[kk][nt][1]);
                 }
             }
             const bool v0 = t0w + gid < n, v1 = t0w + gid + 8 < n;
-            s[0] = v0 ? s[0] : -INFINITY;
-            s[1] = v0 ? s[1] : -INFINITY;
-            s[2] = v1 ? s[2] : -INFINITY;
-            s[3] = v1 ? s[3] : -INFINITY;
-            // column max over the 16 tokens (lanes with the same tig)
-            float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+            uint32_t pb[NT][2];
 #pragma unroll
-            for (int ofs = 4; ofs < 32; ofs <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, ofs));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, ofs));
-            }
-            mx0 *= sl;
-            mx1 *= sl;
-            // lazy rescale: the running max of a head moves only when a score exceeds it by > 2^8
-            if (mx0 > m[0] + kRescale) {
-                const float al = ex2f(m[0] - mx0);  // 0 when m = -inf
-                l[0] *= al;
+            for (int nt = 0; nt < NT; ++nt) {
+                s[nt][0] = v0 ? s[nt][0] : -INFINITY;
+                s[nt][1] = v0 ? s[nt][1] : -INFINITY;
+                s[nt][2] = v1 ? s[nt][2] : -INFINITY;
+                s[nt][3] = v1 ? s[nt][3] : -INFINITY;
+                // column max over the 16 tokens (lanes with the same tig)
+                float mx0 = fmaxf(s[nt][0], s[nt][2]), mx1 = fmaxf(s[nt][1], s[nt][3]);
 #pragma unroll
-                for (int mt = 0; mt < kKSteps; ++mt) {
-                    o[mt][0] *= al;
-                    o[mt][2] *= al;
+                for (int ofs = 4; ofs < 32; ofs <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, ofs));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, ofs));
                 }
-                m[0] = mx0;
-            }
-            if (mx1 > m[1] + kRescale) {
-                const float al = ex2f(m[1] - mx1);
-                l[1] *= al;
+                mx0 *= sl;
+                mx1 *= sl;
+                // lazy rescale: a head's running max moves only when a score exceeds it by > 2^8
+                if (mx0 > m[nt][0] + kRescale) {
+                    const float al = ex2f(m[nt][0] - mx0);  // 0 when m = -inf
+                    l[nt][0] *= al;
 #pragma unroll
-                for (int mt = 0; mt < kKSteps; ++mt) {
-                    o[mt][1] *= al;
-                    o[mt][3] *= al;
+                    for (int mt = 0; mt < kKSteps; ++mt) {
+                        o[mt][nt][0] *= al;
+                        o[mt][nt][2] *= al;
+                    }
+                    m[nt][0] = mx0;
                 }
-                m[1] = mx1;
+                if (mx1 > m[nt][1] + kRescale) {
+                    const float al = ex2f(m[nt][1] - mx1);
+                    l[nt][1] *= al;
+#pragma unroll
+                    for (int mt = 0; mt < kKSteps; ++mt) {
+                        o[mt][nt][1] *= al;
+                        o[mt][nt][3] *= al;
+                    }
+                    m[nt][1] = mx1;
+                }
+                const float p0 = v0 ? ex2f(fmaf(s[nt][0], sl, -m[nt][0])) : 0.f;
+                const float p1 = v0 ? ex2f(fmaf(s[nt][1], sl, -m[nt][1])) : 0.f;
+                const float p2 = v1 ? ex2f(fmaf(s[nt][2], sl, -m[nt][0])) : 0.f;
+                const float p3 = v1 ? ex2f(fmaf(s[nt][3], sl, -m[nt][1])) : 0.f;
+                l[nt][0] += p0 + p2;
+                l[nt][1] += p1 + p3;
+                // P^T (tokens x head slots) in accumulator layout -> P as B fragments (k = tokens)
+                pb[nt][0] = movmatrix_t(pack_pair<BF16>(p0, p1));
+                pb[nt][1] = movmatrix_t(pack_pair<BF16>(p2, p3));
             }
-            const float p0 = v0 ? ex2f(fmaf(s[0], sl, -m[0])) : 0.f;
-            const float p1 = v0 ? ex2f(fmaf(s[1], sl, -m[1])) : 0.f;
-            const float p2 = v1 ? ex2f(fmaf(s[2], sl, -m[0])) : 0.f;
-            const float p3 = v1 ? ex2f(fmaf(s[3], sl, -m[1])) : 0.f;
-            l[0] += p0 + p2;
-            l[1] += p1 + p3;
-            // P^T (tokens x head slots) in accumulator layout -> P as B fragments (k = tokens)
-            const uint32_t pb0 = movmatrix_t(pack_pair<BF16>(p0, p1));
-            const uint32_t pb1 = movmatrix_t(pack_pair<BF16>(p2, p3));
-            // ---- O^T += V_w^T P^T: D x 8 head slots ----
+            // ---- O^T += V_w^T P^T: D x 8 head slots per n-tile (one V fragment for all) ----
             {
                 const int mi = lane >> 3;
                 const int t = t0w + (lane & 7) + 8 * (mi >> 1);
@@ -314,7 +334,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t af[4];
                     const int cc = 2 * (mt & 3) + (mi & 1);
                     ldsm_x4_t(swz(aV + (mt >> 2) * L::kHalfBytes, t, cc), af);
-                    mma16816<BF16>(o[mt], af, pb0, pb1);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) mma16816<BF16>(o[mt][nt], af, pb[nt][0], pb[nt][1]);
                 }
             }
             __syncwarp();
@@ -326,29 +347,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // ---- merge: sum l over the lanes of each head slot, then across the warps ----
 #pragma unroll
-        for (int ofs = 4; ofs < 32; ofs <<= 1) {
-            l[0] += __shfl_xor_sync(0xffffffffu, l[0], ofs);
-            l[1] += __shfl_xor_sync(0xffffffffu, l[1], ofs);
-        }
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int ofs = 4; ofs < 32; ofs <<= 1) {
+                l[nt][0] += __shfl_xor_sync(0xffffffffu, l[nt][0], ofs);
+                l[nt][1] += __shfl_xor_sync(0xffffffffu, l[nt][1], ofs);
+            }
         // ---- hand this warp's rows to the merge warp ----
         if (!mbar_wait(&mempty[mbuf], mphase ^ 1u, abort_flag, a.err)) return;
         float *rows = merge + (size_t)mbuf * L::kMergeFloats;
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int g = g_lo + j;
-            if (g < G) {
-                float *row = rows + ((size_t)warp * G + g) * (D + 2);
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int mt = 0; mt < kKSteps; ++mt) {
-                    row[mt * 16 + gid] = o[mt][j];
-                    row[mt * 16 + gid + 8] = o[mt][j + 2];
-                }
-                if (gid == 0) {
-                    row[D] = m[j];
-                    row[D + 1] = l[j];
+            for (int j = 0; j < 2; ++j) {
+                const int g = nt * 8 + g_lo + j;
+                if (g < G) {
+                    float *row = rows + ((size_t)warp * G + g) * (D + 2);
+#pragma unroll
+                    for (int mt = 0; mt < kKSteps; ++mt) {
+                        row[mt * 16 + gid] = o[mt][nt][j];
+                        row[mt * 16 + gid + 8] = o[mt][nt][j + 2];
+                    }
+                    if (gid == 0) {
+                        row[D] = m[nt][j];
+                        row[D + 1] = l[nt][j];
+                    }
                 }
             }
-        }
         if (warp == 0 && lane == 0) merge_unit[mbuf] = u;
         __syncwarp();
         if (lane == 0) mbar_arrive(&mfull[mbuf]);
@@ -393,9 +418,11 @@ cudaError_t launch_decode_gqa(const DecodeArgs &a, int grid, cudaStream_t s) {
     if (a.cache.head_dim == 128) {
         if (group == 4) return bf16 ? launch_gqa_t<128, 4, true>(a, grid, s) : launch_gqa_t<128, 4, false>(a, grid, s);
         if (group == 8) return bf16 ? launch_gqa_t<128, 8, true>(a, grid, s) : launch_gqa_t<128, 8, false>(a, grid, s);
+        if (group == 16) return bf16 ? launch_gqa_t<128, 16, true>(a, grid, s) : launch_gqa_t<128, 16, false>(a, grid, s);
     } else {
         if (group == 4) return bf16 ? launch_gqa_t<64, 4, true>(a, grid, s) : launch_gqa_t<64, 4, false>(a, grid, s);
         if (group == 8) return bf16 ? launch_gqa_t<64, 8, true>(a, grid, s) : launch_gqa_t<64, 8, false>(a, grid, s);
+        if (group == 16) return bf16 ? launch_gqa_t<64, 16, true>(a, grid, s) : launch_gqa_t<64, 16, false>(a, grid, s);
     }
     return cudaErrorInvalidValue;
 }

@@ -229,7 +229,9 @@ pkv_status decode_impl(const pkv_cache &cache, const void *q, int num_q_heads, c
     a.scale = scale;
     a.chunk = chunk;
     a.s_max = s_max;
-    a.head_groups = group > 8 ? group / 8 : 1;
+    // query heads per unit: the FP8 kernel holds 8 head slots, the native group kernel 16
+    const int per_unit = (cache.format == PKV_KV_FP8_E4M3) ? 8 : (group % 16 == 0 ? 16 : 8);
+    a.head_groups = group > per_unit ? group / per_unit : 1;
     a.cu_q_lens = cu_q_lens;
     a.part_o = static_cast<float *>(workspace);
     a.part_lse = need > 0 ? a.part_o + (size_t)batch * num_q_heads * s_max * cache.head_dim : nullptr;

@@ -39,9 +39,9 @@ struct DecodeArgs {
     int batch, max_blocks_per_seq;
     float scale;
     int chunk;   // tokens per split (multiple of the decode tile)
-    // Groups of 8 query heads per KV head when a KV head serves more than 8 (MQA, wide groups),
-    // else 1: the tensor-core kernels then take each group as a "virtual" KV head -- unit head v
-    // reads KV head v / head_groups and serves query heads 8v .. 8v + 7.
+    // Units per KV head when a KV head serves more query heads than one unit holds (16 for the
+    // native group kernel when the group is a multiple of 16, else 8; MQA, wide groups), else 1:
+    // unit head v reads KV head v / head_groups and serves query heads n*v .. n*v + n-1.
     int head_groups;
     // Mixed batch (prefill chunks and decode rows in one call): cu_q_lens [batch + 1] of the call's
     // q / out rows; only sequences with exactly one query row are decoded here, their row being

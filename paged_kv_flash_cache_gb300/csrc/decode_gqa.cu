@@ -52,6 +52,8 @@ struct GqaLayout {
     static constexpr int kHalves = D / 64;                          // 128-byte swizzle atoms along D
     static constexpr uint32_t kHalfBytes = kTile * 128;             // 64 rows x 128 bytes
     static constexpr uint32_t kKBytes = kHalves * kHalfBytes;       // one K (or V) tile
+    // per 64-column half: page slices of br rows, each its br K rows then its br V rows
+    static constexpr uint32_t kHalfRegion = 2 * kHalfBytes;
     static constexpr uint32_t kQBytes = G * D * 2;
     static constexpr uint32_t kStageBytes = (2 * kKBytes + kQBytes + 1023) / 1024 * 1024;
     static constexpr uint32_t kBarOffset = kStages * kStageBytes;
@@ -90,7 +92,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int hkv = a.cache.num_kv_heads, bs = a.cache.block_size, chunk = a.chunk;
-    const int hu = hkv * a.head_groups;  // unit heads (KV heads, or groups of 8 query heads)
+    const int hu = hkv * a.head_groups;  // unit heads (KV heads, or groups of query heads)
+    const int br = bs < kTile ? bs : kTile;  // rows per page slice (tiles start at multiples of 64)
 
     if (tid == 0) {
         for (int i = 0; i < kStagesG; ++i) {
@@ -111,7 +114,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ===================================== producer warp =====================================
         const uint64_t pol = l2_policy_evict_first();
         const uint16_t *qg = static_cast<const uint16_t *>(a.q);
-        const int box_rows = bs < kTile ? bs : kTile;
         if (lane == 0) tc::prefetch_tensormap(&tm_kv);
         int stage = 0;
         uint32_t phase = 0;
@@ -134,13 +136,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int unit_last_page = (c.t1 - 1) >> a.cache.log2_block_size;
             for (int ts = c.t0; ts < c.t1; ts += kTile) {
                 const int n = min(kTile, c.t1 - ts);
+                const int nslices = (n + br - 1) / br;  // <= 8
                 const int page0 = ts >> a.cache.log2_block_size;
-                const int npages = bs < kTile ? (n + bs - 1) / bs : 1;
-                const int off = bs < kTile ? 0 : (ts & (bs - 1));
-                if (page0 + npages > win.first + win.count)  // units of more than 64 pages
+                const int page_last = (ts + n - 1) >> a.cache.log2_block_size;
+                if (page_last >= win.first + win.count)  // units of more than 64 pages
                     win = load_pages(bt, page0, unit_last_page - page0 + 1, lane);
-                int pb = window_page(win, page0 + lane);
-                if (lane < npages) {
+                const int tok0 = ts + lane * br;  // this lane's slice
+                const int off = tok0 & (bs - 1);
+                int pb = window_page(win, tok0 >> a.cache.log2_block_size);
+                if (lane < nslices) {
                     if (pb < 0 || pb >= a.cache.num_blocks) {
                         set_error(a.err, kErrDeviceRange);
                         pb = 0;
@@ -158,20 +162,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool first_tile = (ts == c.t0);
                 if (lane == 0) {
                     stage_unit[stage] = u;
-                    const uint32_t bytes = (uint32_t)npages * box_rows * 128u * L::kHalves * 2u +
+                    const uint32_t bytes = (uint32_t)nslices * br * 128u * L::kHalves * 2u +
                                            (first_tile ? L::kQBytes : 0u);
                     mbar_arrive_expect_tx(&full[stage], bytes);
                 }
                 __syncwarp();
-                if (lane < npages) {
-                    const int rowK = ((pb * 2 + 0) * hkv + c.kvh / a.head_groups) * bs + off;
-                    const int rowV = rowK + hkv * bs;
-                    const uint32_t dst = (uint32_t)lane * box_rows * 128u;
+                if (lane < nslices) {
+                    // one box per 64-column half: the slice's K rows, then its V rows
+                    const int kvr = c.kvh / a.head_groups;
+                    const uint32_t dst = (uint32_t)lane * 2u * br * 128u;
 #pragma unroll
-                    for (int hf = 0; hf < L::kHalves; ++hf) {
-                        tc::tma_load_2d(st + hf * L::kHalfBytes + dst, &tm_kv, hf * 64, rowK, &full[stage]);
-                        tc::tma_load_2d(st + L::kKBytes + hf * L::kHalfBytes + dst, &tm_kv, hf * 64, rowV, &full[stage]);
-                    }
+                    for (int hf = 0; hf < L::kHalves; ++hf)
+                        tc::tma_load_5d(st + hf * L::kHalfRegion + dst, &tm_kv, hf * 64, off, kvr, 0, pb, &full[stage]);
                 }
                 if (first_tile && lane == 0) {
                     const uint16_t *qsrc = qg + ((size_t)ut.qrow[c.b] * a.num_q_heads + (size_t)c.kvh * G) * D;
@@ -231,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int n = min(kTile, c.t1 - ts);
             if (ts != c.t0 && !mbar_wait(&full[stage], phase, abort_flag, a.err)) return;
             uint8_t *st = smem + (size_t)stage * L::kStageBytes;
-            const uint32_t aK = smem_addr(st), aV = aK + L::kKBytes;
+            const uint32_t aK = smem_addr(st), aV = aK + br * 128u;  // + slice row tp: K; + tp: V
             if (ts == c.t0) {
                 const uint16_t *sq = reinterpret_cast<const uint16_t *>(st + 2 * L::kKBytes);
 #pragma unroll
@@ -254,9 +256,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // tile data): zero this warp's V rows there so that 0 * garbage cannot reach O
                 for (int t = t0w + (lane >> 3); t < t0w + 16; t += 4) {
                     if (t < n) continue;
+                    const int tp = t + (t & -br);  // tile row t in the slice layout
 #pragma unroll
                     for (int hf = 0; hf < L::kHalves; ++hf)
-                        *reinterpret_cast<uint4 *>(st + L::kKBytes + hf * L::kHalfBytes + t * 128 + (lane & 7) * 16) =
+                        *reinterpret_cast<uint4 *>(st + hf * L::kHalfRegion + (tp + br) * 128 + (lane & 7) * 16) =
                             make_uint4(0, 0, 0, 0);
                 }
                 __syncwarp();
@@ -268,11 +271,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             {
                 const int mi = lane >> 3;
                 const int t = t0w + (lane & 7) + 8 * (mi & 1);
+                const int tp = t + (t & -br);  // slice j starts at row 2 * j * br of its half
 #pragma unroll
                 for (int kk = 0; kk < kKSteps; ++kk) {
                     uint32_t af[4];
                     const int cc = 2 * (kk & 3) + (mi >> 1);
-                    ldsm_x4(swz(aK + (kk >> 2) * L::kHalfBytes, t, cc), af);
+                    ldsm_x4(swz(aK + (kk >> 2) * L::kHalfRegion, tp, cc), af);
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) mma16816<BF16>(s[nt], af, bq[kk][nt][0], bq[kk][nt][1]);
                 }
@@ -329,11 +333,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             {
                 const int mi = lane >> 3;
                 const int t = t0w + (lane & 7) + 8 * (mi >> 1);
+                const int tp = t + (t & -br);
 #pragma unroll
                 for (int mt = 0; mt < kKSteps; ++mt) {
                     uint32_t af[4];
                     const int cc = 2 * (mt & 3) + (mi & 1);
-                    ldsm_x4_t(swz(aV + (mt >> 2) * L::kHalfBytes, t, cc), af);
+                    ldsm_x4_t(swz(aV + (mt >> 2) * L::kHalfRegion, tp, cc), af);
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) mma16816<BF16>(o[mt][nt], af, pb[nt][0], pb[nt][1]);
                 }
@@ -395,7 +400,7 @@ template <int D, int G, bool BF16>
 cudaError_t launch_gqa_t(const DecodeArgs &a, int grid, cudaStream_t s) {
     CUtensorMap tm;
     const int box_rows = a.cache.block_size < kTile ? a.cache.block_size : kTile;
-    cudaError_t e = encode_cache_map(a.cache, box_rows, &tm);
+    cudaError_t e = encode_kv5_map(a.cache, box_rows, &tm);
     if (e != cudaSuccess) return e;
     auto kern = decode_gqa_kernel<D, G, BF16>;
     static bool configured[64] = {};

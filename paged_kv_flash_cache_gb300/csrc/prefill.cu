@@ -639,26 +639,40 @@ cudaError_t encode_cache_map(const CacheView &c, int box_rows, CUtensorMap *map)
     return cudaSuccess;
 }
 
-// An FP8 cache viewed so that one box holds a page slice of K and of V: codes as the 5-D tensor
-// [NB][2][Hkv][bs][D] (box D x box_rows x 1 head x 2 (K, V) x 1 page, 128-byte swizzle; shared
-// memory receives the K rows, then the V rows) and scales as the 4-D tensor [NB][2][Hkv][bs]
+// The cache viewed as the 5-D tensor [NB][2][Hkv][bs][D] so that one box holds a page slice of K
+// and of V: box = 128 bytes of columns (64 16-bit elements, or 128 FP8 codes) x box_rows x 1 head
+// x 2 (K, V) x 1 page, 128-byte swizzle; shared memory receives the K rows, then the V rows.
+cudaError_t encode_kv5_map(const CacheView &c, int box_rows, CUtensorMap *map) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t D = (cuuint64_t)c.head_dim, bs = (cuuint64_t)c.block_size, h = (cuuint64_t)c.num_kv_heads;
+    const cuuint64_t nb = (cuuint64_t)c.num_blocks, es_bytes = c.fp8 ? 1 : 2;
+    if (nb == 0 || nb > 0x7fffffffull) return cudaErrorNotSupported;
+    if (c.fp8 && D != 128) return cudaErrorNotSupported;
+    const CUtensorMapDataType dt = c.fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : c.dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    cuuint64_t dims[5] = {D, bs, h, 2, nb};
+    cuuint64_t strides[4] = {D * es_bytes, D * bs * es_bytes, D * bs * h * es_bytes, D * bs * h * 2 * es_bytes};
+    cuuint32_t box[5] = {(cuuint32_t)(128 / es_bytes), (cuuint32_t)box_rows, 1, 2, 1};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    if (enc(map, dt, 5, const_cast<void *>(c.ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+        CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    return cudaSuccess;
+}
+
+// An FP8 cache: the codes as encode_kv5_map, the scales as the 4-D tensor [NB][2][Hkv][bs]
 // (box box_rows x 1 x 2 x 1: K scales, then V scales).
 cudaError_t encode_fp8_maps(const CacheView &c, int box_rows, CUtensorMap *codes, CUtensorMap *scales) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     if (!c.fp8 || c.head_dim != 128) return cudaErrorNotSupported;
-    const cuuint64_t D = 128, bs = (cuuint64_t)c.block_size, h = (cuuint64_t)c.num_kv_heads;
+    const cuuint64_t bs = (cuuint64_t)c.block_size, h = (cuuint64_t)c.num_kv_heads;
     const cuuint64_t nb = (cuuint64_t)c.num_blocks;
-    if (nb == 0 || nb > 0x7fffffffull) return cudaErrorNotSupported;
     {
-        cuuint64_t dims[5] = {D, bs, h, 2, nb};
-        cuuint64_t strides[4] = {D, D * bs, D * bs * h, D * bs * h * 2};
-        cuuint32_t box[5] = {128, (cuuint32_t)box_rows, 1, 2, 1};
-        cuuint32_t es[5] = {1, 1, 1, 1, 1};
-        if (enc(codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void *>(c.ptr), dims, strides, box, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
+        const cudaError_t e = encode_kv5_map(c, box_rows, codes);
+        if (e != cudaSuccess) return e;
     }
     {
         cuuint64_t dims[4] = {bs, h, 2, nb};

@@ -143,17 +143,27 @@ __global__ void __launch_bounds__(kAppendThreads) append_fp8_kernel(AppendArgs a
             continue;
         }
         const int off = (int)(pos & (a.block_size - 1));
-        for (int r0 = 0; r0 < 2 * nh; r0 += kRows) {
-            const int r = r0 + sub;  // row r: K (r < nh) or V of head h0 + r % nh
+        // all of this lane's loads first (one memory round trip per item), then the rows
+        constexpr int kPasses = 2 * kHeadsPerItem / kRows;
+        uint4 raws[kPasses];
+#pragma unroll
+        for (int ps = 0; ps < kPasses; ++ps) {
+            const int r = ps * kRows + sub;
+            raws[ps] = make_uint4(0u, 0u, 0u, 0u);
+            if (r < 2 * nh) {
+                const int kv = r >= nh ? 1 : 0;
+                const int h = h0 + r - kv * nh;
+                raws[ps] = ld_stream((kv ? vn : kn) + ((size_t)t * hkv + h) * kLanesPerRow + chk);
+            }
+        }
+#pragma unroll
+        for (int ps = 0; ps < kPasses; ++ps) {
+            const int r = ps * kRows + sub;  // row r: K (r < nh) or V of head h0 + r % nh
             const bool active = r < 2 * nh;
             const int kv = active && r >= nh ? 1 : 0;
             const int h = h0 + (active ? r - kv * nh : 0);
-            float2 f[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                           make_float2(0.f, 0.f)};
-            if (active) {
-                const uint4 raw = ld_stream((kv ? vn : kn) + ((size_t)t * hkv + h) * kLanesPerRow + chk);
-                unpack8x2(raw, f, Tag());
-            }
+            float2 f[4];
+            unpack8x2(raws[ps], f, Tag());
             float amax = 0.f;
 #pragma unroll
             for (int j = 0; j < 4; ++j) amax = fmaxf(amax, fmaxf(fabsf(f[j].x), fabsf(f[j].y)));

@@ -231,6 +231,14 @@ PKV_API pkv_status pkv_paged_attn_decode_noalloc(pkv_cache cache, const void *q,
                                          int max_blocks_per_seq, float scale, int num_splits,
                                          void *out, pkv_dtype out_dtype, float *lse, void *stream);
 
+/* selftest_wait_timeout -- failure-detection check. Every wait inside the kernels is bounded:
+ * after its limit it records PKV_ERR_TIMEOUT in the device error word and the kernel winds
+ * down instead of hanging. This launches one warp that waits, the same way, on an mbarrier
+ * nothing will complete, with a limit of timeout_us microseconds (1..1000000); read the
+ * result with pkv_get_device_error (PKV_ERR_TIMEOUT expected). The pages have no
+ * counterpart; it exists to test the failure path without faulting the GPU. */
+PKV_API pkv_status pkv_selftest_wait_timeout(unsigned int timeout_us, void *stream);
+
 /* Synchronise `stream`, then read and clear the sticky device error word of the
  * current device.  *code receives PKV_OK, PKV_ERR_DEVICE_RANGE or PKV_ERR_TIMEOUT.
  * Returns PKV_ERR_CUDA if the synchronisation or the read fails. */

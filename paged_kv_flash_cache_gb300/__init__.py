@@ -26,7 +26,7 @@ from typing import Optional
 __all__ = [
     "PkvError", "library_path", "load_library", "kv_cache_append", "paged_attn_decode", "paged_attn_prefill",
     "attn_combine", "decode_workspace_size", "decode_split_tokens", "get_device_error", "STATUS",
-    "paged_attn_decode_noalloc", "paged_attn_mixed",
+    "paged_attn_decode_noalloc", "paged_attn_mixed", "selftest_wait_timeout",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -42,7 +42,7 @@ KV_NATIVE, KV_FP8_E4M3 = 0, 1
 # Every symbol include/pkv.h declares.
 EXPORTS = ("pkv_kv_cache_append", "pkv_decode_workspace_size", "pkv_decode_split_tokens", "pkv_paged_attn_decode",
            "pkv_paged_attn_decode_noalloc", "pkv_paged_attn_prefill", "pkv_paged_attn_mixed", "pkv_attn_combine",
-           "pkv_get_device_error", "pkv_status_string", "pkv_version")
+           "pkv_get_device_error", "pkv_selftest_wait_timeout", "pkv_status_string", "pkv_version")
 DECODE_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024   # PKV_DECODE_NOALLOC_SCRATCH_BYTES in include/pkv.h
 
 
@@ -89,6 +89,8 @@ def load_library():
         lib.pkv_paged_attn_mixed.restype = I
         lib.pkv_attn_combine.argtypes = [P, P, I, I, I, P, I, P, P]
         lib.pkv_attn_combine.restype = I
+        lib.pkv_selftest_wait_timeout.argtypes = [ctypes.c_uint, P]
+        lib.pkv_selftest_wait_timeout.restype = I
         lib.pkv_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
         lib.pkv_get_device_error.restype = I
         lib.pkv_status_string.argtypes = [I]
@@ -303,6 +305,12 @@ def attn_combine(partial_o, partial_lse, out=None, out_dtype=None, lse=None, str
                                 _dev(out, "out"), _dtype_code(out.dtype), _dev(lse, "lse"), _stream(stream)),
            "pkv_attn_combine")
     return out
+
+
+def selftest_wait_timeout(timeout_us: int = 20000, stream=None) -> None:
+    """Launch one warp that waits on a barrier nothing completes, bounded by timeout_us; the
+    device error word then holds PKV_ERR_TIMEOUT (read it with get_device_error)."""
+    _check(load_library().pkv_selftest_wait_timeout(int(timeout_us), _stream(stream)), "pkv_selftest_wait_timeout")
 
 
 def get_device_error(stream=None) -> int:

@@ -112,6 +112,7 @@ int split_tokens(int batch, int num_kv_heads, int block_size, int max_blocks_per
 }  // namespace
 
 const DeviceInfo &device_info() { return slot().info; }
+int *device_error_word() { return slot().err_ptr; }
 
 }  // namespace pkv
 

@@ -62,16 +62,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Wait for phase `parity` of `bar` to complete.  Gives up (returns false) when
-// *abort becomes non-zero or after kWaitTimeoutNs, in which case it records
-// kErrTimeout and raises *abort so the CTA's other roles stop too.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort, int *err) {
+// *abort becomes non-zero or after timeout_ns (default kWaitTimeoutNs), in which case it
+// records kErrTimeout and raises *abort so the CTA's other roles stop too.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort, int *err,
+                                          unsigned long long timeout_ns = kWaitTimeoutNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_timer_ns();
     for (uint32_t n = 1;; ++n) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((n & 63u) == 0) {
             if (*abort) return false;
-            if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+            if (global_timer_ns() - t0 > timeout_ns) {
                 set_error(err, kErrTimeout);
                 *abort = 1;
                 return false;

@@ -111,6 +111,7 @@ struct DeviceInfo {
     int decode_ctas_per_sm;
 };
 const DeviceInfo &device_info();
+int *device_error_word();  // the current device's sticky error word (device address)
 
 constexpr int kDecodeTile = 64;         // tokens per decode pipeline stage
 constexpr int kDecodeMaxSplits = 2048;  // splits of one context (bounds the split size from below)

@@ -102,6 +102,11 @@ def test_fp8_cache_validation_without_gpu(lib):
     assert lib.pkv_paged_attn_decode(*args) == 2
 
 
+def test_selftest_rejects_bad_limits_without_gpu(lib):
+    assert lib.pkv_selftest_wait_timeout(0, None) == 1
+    assert lib.pkv_selftest_wait_timeout(2000000, None) == 1
+
+
 def test_workspace_sizing_with_explicit_splits(lib):
     # capacity 4 * 16 = 64 tokens in 1 split: no workspace
     assert pkv.decode_workspace_size(2, 4, 4, 128, 16, 4, num_splits=1) == 0

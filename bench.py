@@ -764,6 +764,7 @@ def main():
                 "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / pk["hbm_gbs"], 3), "peak_source": pk["source"],
                 "traffic": ncu_traffic("decode_split_7b_ncu.txt", files),
+                "traffic_of": "decode_split_kernel (ncu, scaled from a batch-4 capture by cached tokens)",
                 "algorithmic_bytes_per_launch": r["bytes"]["total"], "avg_launch_ms": round(r["decode_ms"], 4)}
     line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",

@@ -47,7 +47,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="", help="comma list of extra workloads (bs_sweep,mixed,prefix,fp8,mqa,mixed_call,prefill,prefill_fp8)")
     ap.add_argument("--profile", choices=["decode", "append", "prefill", "decode_mixed", "decode_prefix", "decode_fp8",
-                                          "prefill_fp8"],
+                                          "prefill_fp8", "decode_mqa"],
                     default=None,
                     help="small case for ncu captures: W + K launches of one kernel, nothing else timed")
     return ap.parse_args()
@@ -102,6 +102,16 @@ def profile_case(args):
         out = torch.empty((p.batch, 32, 128), dtype=torch.float16, device="cuda")
         for _ in range(args.warmup + args.steps):
             pkv.paged_attn_decode(codes, q, bt, ctx, scale=p.scale, out=out, scales=scales)
+        torch.cuda.synchronize()
+        assert pkv.get_device_error() == 0
+    elif args.profile == "decode_mqa":
+        # the MQA batch itself: 0.30 GB of K/V (above L2)
+        p = mqa_problem(torch)
+        cache = device_problem(p, torch)
+        q, bt, ctx = p.q.cuda(), p.block_tables.cuda(), p.context_lens.cuda()
+        out = torch.empty((p.batch, 32, 128), dtype=torch.bfloat16, device="cuda")
+        for _ in range(args.warmup + args.steps):
+            pkv.paged_attn_decode(cache, q, bt, ctx, scale=p.scale, out=out)
         torch.cuda.synchronize()
         assert pkv.get_device_error() == 0
     elif args.profile == "decode_prefix":
@@ -549,17 +559,24 @@ def bench_fp8(torch, steps, warmup, fp16_ms=None):
     return r
 
 
-def bench_mqa(torch, steps, warmup):
-    """Multi-query decode: 128 sequences, 32 query heads sharing one KV head."""
-    import paged_kv_flash_cache_gb300 as pkv
+def mqa_problem(torch):
+    """128 sequences, contexts U[1024, 8192], 32 query heads sharing one KV head of 128, bf16, bs 16:
+    0.30 GB of K/V in a pool of exactly the pages needed, shuffled."""
     from paged_kv_flash_cache_gb300 import workloads as W
     gen = torch.Generator().manual_seed(1241)
     lens = torch.randint(1024, 8193, (128,), generator=gen).tolist()
     nb = sum((L + 15) // 16 for L in lens)
     order = torch.randperm(nb, generator=gen).tolist()
-    p = W.make_problem("mqa", batch=128, num_q_heads=32, num_kv_heads=1, head_dim=128, block_size=16,
-                       context_lens=lens, q_lens=[1] * 128, dtype=W.BF16, causal=False, seed=1242, num_blocks=nb,
-                       free_order=order, pool_init="none", device="cuda")
+    return W.make_problem("mqa", batch=128, num_q_heads=32, num_kv_heads=1, head_dim=128, block_size=16,
+                          context_lens=lens, q_lens=[1] * 128, dtype=W.BF16, causal=False, seed=1242, num_blocks=nb,
+                          free_order=order, pool_init="none", device="cuda")
+
+
+def bench_mqa(torch, steps, warmup):
+    """Multi-query decode: 128 sequences, 32 query heads sharing one KV head."""
+    import paged_kv_flash_cache_gb300 as pkv
+    from paged_kv_flash_cache_gb300 import workloads as W
+    p = mqa_problem(torch)
     cache = device_problem(p, torch)
     q, bt, ctx = p.q.cuda(), p.block_tables.cuda(), p.context_lens.cuda()
     ws = torch.empty(max(16, pkv.decode_workspace_size(p.batch, 32, 1, 128, 16, bt.shape[1])), dtype=torch.uint8,

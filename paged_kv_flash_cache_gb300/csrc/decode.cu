@@ -62,7 +62,7 @@ struct DecodeLayout {
     static constexpr size_t kQBytes = (size_t)G * D * 2;
     static constexpr size_t kSOffset = 2 * kKBytes + kQBytes;  // FP8: K row scales [kTile], V row scales [kTile]
     static constexpr size_t kStageBytes = ((kSOffset + (FP8 ? 2 * kTile * 4 : 0)) + 127) / 128 * 128;
-    static constexpr size_t kMergeFloats = (size_t)kConsumerWarps * G * (D + 2);
+    static constexpr size_t kMergeFloats = (size_t)kConsumerWarps * G * kMergeRow<D>;
     static constexpr size_t kBarOffset = kStages * kStageBytes;
     // barriers: full / empty per stage, merge full / empty per merge buffer; then the abort flag
     // (padded to 16 bytes), the unit of each stage and the unit of each merge buffer
@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
     volatile int *abort_flag = reinterpret_cast<volatile int *>(mempty + 2);
     int *stage_unit = reinterpret_cast<int *>(mempty + 2) + 4;  // [kStages] unit of each filled stage, -1: end
     int *merge_unit = stage_unit + kStages;                     // [2] unit of each merge buffer, -1: end
-    float *merge = reinterpret_cast<float *>(smem + L::kMergeOffset);  // [2][kConsumerWarps][G][D + 2]
+    float *merge = reinterpret_cast<float *>(smem + L::kMergeOffset);  // [2][kConsumerWarps][G][kMergeRow<D>]
     const UnitTable ut = unit_table(reinterpret_cast<int *>(smem + L::kIntsOffset), a.batch, a.s_max);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -503,7 +503,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
         if (slot == 0) {
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                float *row = rows + ((size_t)warp * G + g) * (D + 2);
+                float *row = rows + ((size_t)warp * G + g) * kMergeRow<D>;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     row[chk * 8 + 2 * j] = acc[g][j].x;

@@ -99,18 +99,44 @@ __device__ __forceinline__ int window_page(const PageWindow &w, int page) {
     return rel < 32 ? lo : hi;
 }
 
-// The merge warp of a decode CTA. At the end of a unit each of the W consumer warps leaves its
-// (acc[D], m, l) row per query head of the unit in merge buffer i ([W][G][D + 2] floats; m in
-// log2 units, acc and l relative to 2^m), writes the unit id (warp 0) and arrives on mfull[i]; this
-// loop combines the rows -- M = max m, weights 2^(m_w - M), out = sum w acc / sum w l, lse =
+// Merge rows: a consumer warp's D partial sums of one query head, then its m and l, padded to
+// a multiple of four floats so that every row starts on a 16-byte boundary (vector reads below)
+// and the rows of neighbouring heads start in different banks.
+template <int D>
+constexpr int kMergeRow = D + 4;
+
+// Sum of x[0..N) in the order of a butterfly reduction over N lanes (pairs i, i + N/2 first), so
+// that a lane-parallel sum and a per-lane sum round alike.
+template <int N>
+__device__ __forceinline__ float tree_sum(const float (&x)[N]) {
+    if constexpr (N == 1) {
+        return x[0];
+    } else {
+        float y[N / 2];
+#pragma unroll
+        for (int i = 0; i < N / 2; ++i) y[i] = x[i] + x[i + N / 2];
+        return tree_sum<N / 2>(y);
+    }
+}
+
+// The merge warp of a decode CTA. At the end of a unit each of the W token slices leaves its
+// (acc[D], m, l) row per query head of the unit in merge buffer i ([W][G][kMergeRow<D>] floats; m
+// in log2 units, acc and l relative to 2^m), the unit id is written (warp 0) and mfull[i] completes;
+// this loop combines the rows -- M = max m, weights 2^(m_w - M), out = sum w acc / sum w l, lse =
 // (M + log2 sum w l) ln 2 -- writes the final output of a single-split context or the split's
-// partial, and frees the buffer on mempty[i]. Buffers alternate; unit id -1 ends the loop.
-// Returns false if a wait gave up (the error word is set).
+// partial, and frees the buffer on mempty[i]. Buffers alternate; unit id -1 ends the loop. Lane g
+// finds the weights of head g (all heads at once); then each head's output is D / 32 consecutive
+// dims per lane, read and written as vectors. Returns false if a wait gave up (the error word is
+// set).
 template <int D, int G, int W>
 __device__ __forceinline__ bool merge_warp_loop(const DecodeArgs &a, const UnitTable &ut, const float *merge,
                                                 size_t buf_floats, uint64_t *mfull, uint64_t *mempty,
                                                 const int *merge_unit, volatile int *abort_flag, int lane) {
-    static_assert(W <= 32, "one lane per consumer warp");
+    static_assert(G <= 32, "one lane per query head of a unit");
+    static_assert(W == 1 || W == 2 || W == 4 || W == 8 || W == 16 || W == 32, "token slices: a power of two");
+    constexpr int RS = kMergeRow<D>;
+    constexpr int V = D / 32;  // consecutive dims per lane
+    static_assert(V == 2 || V == 4, "head_dim 64 or 128");
     const int hkv = a.cache.num_kv_heads * a.head_groups, chunk = a.chunk;  // unit heads
     int mbuf = 0;
     uint32_t mphase = 0;
@@ -121,42 +147,65 @@ __device__ __forceinline__ bool merge_warp_loop(const DecodeArgs &a, const UnitT
         const UnitCursor c = unit_of(u, ut, a.s_max, hkv, chunk);
         const float *rows = merge + (size_t)mbuf * buf_floats;
         const int splits = (ut.lens[c.b] + chunk - 1) / chunk;
-#pragma unroll 1
+        const size_t prow0 = (size_t)c.b * a.num_q_heads + (size_t)c.kvh * G;          // partial rows
+        const size_t orow0 = (size_t)ut.qrow[c.b] * a.num_q_heads + (size_t)c.kvh * G;  // output rows
+        float wl[W];
+        float inv_l = 0.f;
+#pragma unroll
+        for (int w = 0; w < W; ++w) wl[w] = 0.f;
+        if (lane < G) {
+            float mw[W], lw[W];
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < W; ++w) {
+                const float *r = rows + ((size_t)w * G + lane) * RS;
+                mw[w] = r[D];
+                lw[w] = r[D + 1];
+                M = fmaxf(M, mw[w]);
+            }
+            float lt[W];
+#pragma unroll
+            for (int w = 0; w < W; ++w) {
+                wl[w] = (mw[w] == -INFINITY) ? 0.f : exp2f(mw[w] - M);
+                lt[w] = lw[w] * wl[w];
+            }
+            const float lsum = tree_sum<W>(lt);
+            inv_l = lsum > 0.f ? 1.f / lsum : 0.f;
+            const float lse_v = lsum > 0.f ? (M + log2f(lsum)) * kLn2 : -INFINITY;
+            if (splits == 1) {
+                if (a.lse) a.lse[orow0 + lane] = lse_v;
+            } else {
+                a.part_lse[(prow0 + lane) * a.s_max + c.split] = lse_v;
+            }
+        }
+#pragma unroll(G < 4 ? G : 4)
         for (int g = 0; g < G; ++g) {
-            const float *rg = rows + (size_t)g * (D + 2);  // warp w's row: rg + w * G * (D + 2)
-            const float mw = lane < W ? rg[(size_t)lane * G * (D + 2) + D] : -INFINITY;
-            const float lw = lane < W ? rg[(size_t)lane * G * (D + 2) + D + 1] : 0.f;
-            float M = mw;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-            const float wgt = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
-            float lsum = lw * wgt;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
             float wv[W];
 #pragma unroll
-            for (int w = 0; w < W; ++w) wv[w] = __shfl_sync(0xffffffffu, wgt, w);
-            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-            const size_t head = (size_t)c.kvh * G + g;
-            const size_t row_id = (size_t)c.b * a.num_q_heads + head;                 // partials
-            const size_t out_row = (size_t)ut.qrow[c.b] * a.num_q_heads + head;       // output
+            for (int w = 0; w < W; ++w) wv[w] = __shfl_sync(0xffffffffu, wl[w], g);
+            const float inv = __shfl_sync(0xffffffffu, inv_l, g);
+            float acc[V];
 #pragma unroll
-            for (int d = lane; d < D; d += 32) {
-                float o = 0.f;
+            for (int v = 0; v < V; ++v) acc[v] = 0.f;
 #pragma unroll
-                for (int w = 0; w < W; ++w) o += rg[(size_t)w * G * (D + 2) + d] * wv[w];
-                const float res = o * inv;
-                if (splits == 1) store_out(a.out, out_row * D + d, res, a.out_dtype);
-                else a.part_o[(row_id * a.s_max + c.split) * D + d] = res;
-            }
-            if (lane == 0) {
-                const float lse_v = lsum > 0.f ? (M + log2f(lsum)) * kLn2 : -INFINITY;
-                if (splits == 1) {
-                    if (a.lse) a.lse[out_row] = lse_v;
+            for (int w = 0; w < W; ++w) {
+                const float *r = rows + ((size_t)w * G + g) * RS + V * lane;
+                if constexpr (V == 4) {
+                    const float4 x = *reinterpret_cast<const float4 *>(r);
+                    acc[0] += x.x * wv[w];
+                    acc[1] += x.y * wv[w];
+                    acc[2] += x.z * wv[w];
+                    acc[3] += x.w * wv[w];
                 } else {
-                    a.part_lse[row_id * a.s_max + c.split] = lse_v;
+                    const float2 x = *reinterpret_cast<const float2 *>(r);
+                    acc[0] += x.x * wv[w];
+                    acc[1] += x.y * wv[w];
                 }
             }
+#pragma unroll
+            for (int v = 0; v < V; ++v) acc[v] *= inv;
+            if (splits == 1) store_out_vec<V>(a.out, (orow0 + g) * D + V * lane, acc, a.out_dtype);
+            else store_out_vec<V>(a.part_o, ((prow0 + g) * a.s_max + c.split) * D + V * lane, acc, 2);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&mempty[mbuf]);

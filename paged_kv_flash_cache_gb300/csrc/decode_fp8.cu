@@ -69,7 +69,7 @@ struct Fp8Layout {
     // barriers: full / empty per stage, merge full / empty per merge buffer; then the abort flag
     // (padded to 16 bytes), the unit of each stage and the unit of each merge buffer
     static constexpr uint32_t kMergeOffset = kBarOffset + (2 * kStages8 + 4) * 8 + 64;
-    static constexpr uint32_t kMergeFloats = kWarps * G * (kD + 2);  // one of two merge buffers
+    static constexpr uint32_t kMergeFloats = kWarps * G * kMergeRow<kD>;  // one of two merge buffers
     static constexpr uint32_t kIntsOffset = kMergeOffset + 2 * kMergeFloats * 4;
     static size_t smem_bytes(int batch, int s_max) {
         return kIntsOffset + unit_table_ints(batch, s_max) * 4 + 1024;  // + 1024-byte alignment slack
@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(mempty + 2);
     int *stage_unit = reinterpret_cast<int *>(mempty + 2) + 4;
     int *merge_unit = stage_unit + kStages8;  // [2] unit of each merge buffer, -1: end
-    float *merge = reinterpret_cast<float *>(smem + L::kMergeOffset);  // [2][kWarps][G][kD + 2]
+    float *merge = reinterpret_cast<float *>(smem + L::kMergeOffset);  // [2][kWarps][G][kMergeRow<kD>]
     const UnitTable ut = unit_table(reinterpret_cast<int *>(smem + L::kIntsOffset), a.batch, a.s_max);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 2; ++j) {
             const int g = g_lo + j;
             if (g < G) {
-                float *row = rows + ((size_t)warp * G + g) * (kD + 2);
+                float *row = rows + ((size_t)warp * G + g) * kMergeRow<kD>;
 #pragma unroll
                 for (int mt = 0; mt < kChunks; ++mt) {
                     row[mt * 16 + 2 * gid] = o[mt][j];          // M slot gid: dim 2gid of the chunk

@@ -11,21 +11,23 @@
 // conversions and cross-lane sums; here one mma.sync m16n8k16 covers 16 tokens x 8 head slots x
 // 16 dims.
 //
-// Kernel structure (persistent, one CTA per SM, 6 warps):
+// Kernel structure (persistent, one CTA per SM, 6 warps; 10 for units of 16 query heads):
 //   * units (sequence, KV head, split) are numbered from the context lengths and dealt
 //     round-robin to the CTAs, as in decode.cu;
 //   * warp 4 streams each unit's 64-token tiles with TMA: the page ids of a unit are read one
 //     unit ahead, and each lane issues its page's K and V boxes (64 columns x rows, 128-byte
 //     swizzle, through a 2-D tensor map over the cache), into a 4-stage ring; q comes in with the
 //     unit's first tile;
-//   * warps 0-3 each own 16 tokens of a tile: ldmatrix from the swizzled tile gives the A fragments
+//   * warps 0-3 each own 16 tokens of a tile (units of 16 query heads: warps 0-7, two per 16 tokens,
+//     each with one 8-head n-tile, so that each dependent chain is half as long and every scheduler
+//     has two of them): ldmatrix from the swizzled tile gives the A fragments
 //     of K (row) and of V (transposed); q, held as B fragments for the whole unit, has the group's
 //     heads in the N slots (padding slots are zero); the scores stay in the accumulator fragments:
 //     column max by shuffles, lazy rescale (threshold 2^8), exp2, and P moved into B-fragment
 //     layout with movmatrix; O^T accumulates in registers; at the end of a unit each warp leaves
 //     its rows in one of two shared-memory merge buffers and goes on with the next unit;
-//   * warp 5 merges the four warps' rows and writes the output (single split) or the split
-//     partials.
+//   * the last warp merges the four token slices' rows and writes the output (single split) or
+//     the split partials.
 #include <cuda.h>
 
 #include "decode_common.cuh"
@@ -37,10 +39,7 @@
 namespace pkv {
 namespace {
 
-constexpr int kWarps = 4;                         // consumer warps, 16 tokens each
-constexpr int kProducerWarp = kWarps;
-constexpr int kMergeWarp = kWarps + 1;
-constexpr int kThreads = (kWarps + 2) * 32;
+constexpr int kWarps = 4;                         // token slices of a tile, 16 tokens each
 constexpr int kTile = 64;                         // tokens per stage
 constexpr int kStagesMax = 4;
 constexpr int kMaxBatchG = 2048;
@@ -60,11 +59,22 @@ struct GqaLayout {
     // barriers: full / empty per stage, merge full / empty per merge buffer; then the abort flag
     // (padded to 16 bytes), the unit of each stage and the unit of each merge buffer
     static constexpr uint32_t kMergeOffset = kBarOffset + (2 * kStages + 4) * 8 + 64;
-    static constexpr uint32_t kMergeFloats = kWarps * G * (D + 2);  // one of two merge buffers
+    static constexpr uint32_t kMergeFloats = kWarps * G * kMergeRow<D>;  // one of two merge buffers
     static constexpr uint32_t kIntsOffset = kMergeOffset + 2 * kMergeFloats * 4;
     __host__ __device__ static size_t smem_bytes(int batch, int s_max) {
         return kIntsOffset + unit_table_ints(batch, s_max) * 4 + 1024;  // + 1024-byte alignment slack
     }
+};
+
+// Warp roles: kHS consumer warps per token slice, each with NT / kHS of the unit's n-tiles of 8
+// head slots; then the producer and the merge warp.
+template <int G>
+struct GqaWarps {
+    static constexpr int kHS = G >= 16 ? 2 : 1;
+    static constexpr int kConsumers = kWarps * kHS;
+    static constexpr int kProducer = kConsumers;
+    static constexpr int kMerge = kConsumers + 1;
+    static constexpr int kThreads = (kConsumers + 2) * 32;
 };
 
 // Shared-memory address of token row t, 16-byte chunk cc (0..7) of a 64-column half in the
@@ -74,9 +84,10 @@ __device__ __forceinline__ uint32_t swz(uint32_t half_base, int t, int cc) {
 }
 
 template <int D, int G, bool BF16>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(GqaWarps<G>::kThreads, 1)
     decode_gqa_kernel(const __grid_constant__ CUtensorMap tm_kv, DecodeArgs a) {
     using L = GqaLayout<D, G>;
+    using W = GqaWarps<G>;
     constexpr int kStagesG = L::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -87,7 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(mempty + 2);
     int *stage_unit = reinterpret_cast<int *>(mempty + 2) + 4;
     int *merge_unit = stage_unit + kStagesG;  // [2] unit of each merge buffer, -1: end
-    float *merge = reinterpret_cast<float *>(smem + L::kMergeOffset);  // [2][kWarps][G][D + 2]
+    float *merge = reinterpret_cast<float *>(smem + L::kMergeOffset);  // [2][kWarps][G][kMergeRow<D>]
     const UnitTable ut = unit_table(reinterpret_cast<int *>(smem + L::kIntsOffset), a.batch, a.s_max);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -98,19 +109,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int i = 0; i < kStagesG; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kWarps);
+            mbar_init(&empty[i], W::kConsumers);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&mfull[i], kWarps);
+            mbar_init(&mfull[i], W::kConsumers);
             mbar_init(&mempty[i], 1);
         }
         *abort_flag = 0;
         fence_barrier_init();
     }
     pdl_wait();  // lengths, tables, q and the cache may come from the previous kernel
-    const int num_units = decode_scan_units<kThreads>(a, ut);
+    const int num_units = decode_scan_units<W::kThreads>(a, ut);
 
-    if (warp == kProducerWarp) {
+    if (warp == W::kProducer) {
         // ===================================== producer warp =====================================
         const uint64_t pol = l2_policy_evict_first();
         const uint16_t *qg = static_cast<const uint16_t *>(a.q);
@@ -196,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return;
     }
 
-    if (warp == kMergeWarp) {
+    if (warp == W::kMerge) {
         // ====================================== merge warp ======================================
         merge_warp_loop<D, G, kWarps>(a, ut, merge, L::kMergeFloats, mfull, mempty, merge_unit, abort_flag, lane);
         pdl_launch_dependents();
@@ -204,9 +215,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ===================================== consumer warps =====================================
-    // The group's heads fill NT n-tiles of 8 head slots (NT = 2 for 16 heads; padding slots zero).
+    // The group's heads fill n-tiles of 8 head slots (padding slots zero); this warp holds NT of
+    // them, from n-tile nt0, for the 16 tokens of its slice.
     constexpr int kKSteps = D / 16;         // k-steps of q.K^T, m-tiles of O^T
-    constexpr int NT = (G + 7) / 8;
+    constexpr int NT = (G + 7) / 8 / W::kHS;
+    static_assert(NT * W::kHS * 8 >= G, "n-tiles must cover the group");
+    const int slice = warp % kWarps, nt0 = (warp / kWarps) * NT;
     const int gid = lane >> 2, tig = lane & 3;
     const int g_lo = 2 * tig;               // this lane's two head slots of each n-tile
     const float sl = a.scale * kLog2e;
@@ -238,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint16_t *sq = reinterpret_cast<const uint16_t *>(st + 2 * L::kKBytes);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    const int hs = nt * 8 + gid;  // head slot
+                    const int hs = (nt0 + nt) * 8 + gid;  // head slot
 #pragma unroll
                     for (int kk = 0; kk < kKSteps; ++kk) {
                         if (hs < G) {
@@ -250,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            const int t0w = warp * 16;      // this warp's tokens in the tile
+            const int t0w = slice * 16;     // this warp's tokens in the tile
             if (t0w + 16 > n) {
                 // tokens at or beyond the context end may hold unwritten cache bytes (or stale
                 // tile data): zero this warp's V rows there so that 0 * garbage cannot reach O
@@ -365,9 +379,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-                const int g = nt * 8 + g_lo + j;
+                const int g = (nt0 + nt) * 8 + g_lo + j;
                 if (g < G) {
-                    float *row = rows + ((size_t)warp * G + g) * (D + 2);
+                    float *row = rows + ((size_t)slice * G + g) * kMergeRow<D>;
 #pragma unroll
                     for (int mt = 0; mt < kKSteps; ++mt) {
                         row[mt * 16 + gid] = o[mt][nt][j];
@@ -411,7 +425,8 @@ cudaError_t launch_gqa_t(const DecodeArgs &a, int grid, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         if (dev < 64) configured[dev] = true;
     }
-    return launch_pdl(kern, dim3(grid), dim3(kThreads), GqaLayout<D, G>::smem_bytes(a.batch, a.s_max), s, tm, a);
+    return launch_pdl(kern, dim3(grid), dim3(GqaWarps<G>::kThreads), GqaLayout<D, G>::smem_bytes(a.batch, a.s_max), s, tm,
+                      a);
 }
 
 }  // namespace

@@ -7,6 +7,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
+#include <string.h>
 
 namespace pkv {
 
@@ -249,6 +250,33 @@ __device__ __forceinline__ void store_out(void *out, size_t idx, float v, int ou
     } else {
         static_cast<__half *>(out)[idx] = __float2half_rn(v);
     }
+}
+
+// V (2 or 4) consecutive outputs from element idx on (idx a multiple of V, the base 16-byte
+// aligned): one vector store, rounded as store_out rounds each value.
+template <int V>
+__device__ __forceinline__ void store_out_vec(void *out, size_t idx, const float (&v)[V], int out_dtype) {
+    static_assert(V == 2 || V == 4, "vectors of 2 or 4");
+    if (out_dtype == 2) {
+        float *o = static_cast<float *>(out) + idx;
+        if constexpr (V == 4) *reinterpret_cast<float4 *>(o) = make_float4(v[0], v[1], v[2], v[3]);
+        else *reinterpret_cast<float2 *>(o) = make_float2(v[0], v[1]);
+        return;
+    }
+    uint32_t w[V / 2];
+#pragma unroll
+    for (int i = 0; i < V / 2; ++i) {
+        if (out_dtype == 1) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+            memcpy(&w[i], &h, 4);
+        } else {
+            const __half2 h = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+            memcpy(&w[i], &h, 4);
+        }
+    }
+    uint16_t *o = static_cast<uint16_t *>(out) + idx;
+    if constexpr (V == 4) *reinterpret_cast<uint2 *>(o) = make_uint2(w[0], w[1]);
+    else *reinterpret_cast<uint32_t *>(o) = w[0];
 }
 
 constexpr float kLog2e = 1.4426950408889634f;

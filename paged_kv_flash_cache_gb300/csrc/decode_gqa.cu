@@ -16,8 +16,9 @@
 //     round-robin to the CTAs, as in decode.cu;
 //   * warp 4 streams each unit's 64-token tiles with TMA: the page ids of a unit are read one
 //     unit ahead, and each lane issues its page's K and V boxes (64 columns x rows, 128-byte
-//     swizzle, through a 2-D tensor map over the cache), into a 4-stage ring; q comes in with the
-//     unit's first tile;
+//     swizzle, through a 5-D tensor map over the cache), into a ring of as many stages (up to 6)
+//     as the shared memory left by the merge buffers and the unit tables holds; q comes in with
+//     the unit's first tile;
 //   * warps 0-3 each own 16 tokens of a tile (units of 16 query heads: warps 0-7, two per 16 tokens,
 //     each with one 8-head n-tile, so that each dependent chain is half as long and every scheduler
 //     has two of them): ldmatrix from the swizzled tile gives the A fragments
@@ -41,13 +42,13 @@ namespace {
 
 constexpr int kWarps = 4;                         // token slices of a tile, 16 tokens each
 constexpr int kTile = 64;                         // tokens per stage
-constexpr int kStagesMax = 4;
-constexpr int kMaxBatchG = 2048;
+constexpr int kStagesMax = 6;
 constexpr float kRescale = 8.0f;                  // lazy rescale threshold (log2 units)
 
+// Shared memory: the two merge buffers, the barriers and unit ids (fixed sizes), then from the
+// next 1024-byte boundary the ring of stages, then the unit tables (sized by batch and splits).
 template <int D, int G>
 struct GqaLayout {
-    static constexpr int kStages = G > 8 ? 3 : kStagesMax;  // 16 heads: the merge buffers need a stage's room
     static constexpr int kHalves = D / 64;                          // 128-byte swizzle atoms along D
     static constexpr uint32_t kHalfBytes = kTile * 128;             // 64 rows x 128 bytes
     static constexpr uint32_t kKBytes = kHalves * kHalfBytes;       // one K (or V) tile
@@ -55,14 +56,21 @@ struct GqaLayout {
     static constexpr uint32_t kHalfRegion = 2 * kHalfBytes;
     static constexpr uint32_t kQBytes = G * D * 2;
     static constexpr uint32_t kStageBytes = (2 * kKBytes + kQBytes + 1023) / 1024 * 1024;
-    static constexpr uint32_t kBarOffset = kStages * kStageBytes;
-    // barriers: full / empty per stage, merge full / empty per merge buffer; then the abort flag
-    // (padded to 16 bytes), the unit of each stage and the unit of each merge buffer
-    static constexpr uint32_t kMergeOffset = kBarOffset + (2 * kStages + 4) * 8 + 64;
     static constexpr uint32_t kMergeFloats = kWarps * G * kMergeRow<D>;  // one of two merge buffers
-    static constexpr uint32_t kIntsOffset = kMergeOffset + 2 * kMergeFloats * 4;
-    __host__ __device__ static size_t smem_bytes(int batch, int s_max) {
-        return kIntsOffset + unit_table_ints(batch, s_max) * 4 + 1024;  // + 1024-byte alignment slack
+    // barriers: full / empty per stage slot, merge full / empty per merge buffer; then the abort
+    // flag (padded to 16 bytes), the unit of each stage slot and the unit of each merge buffer
+    static constexpr uint32_t kBarOffset = 2 * kMergeFloats * 4;
+    static constexpr uint32_t kFixedBytes = kBarOffset + (2 * kStagesMax + 4) * 8 + 16 + (kStagesMax + 2) * 4;
+    static constexpr uint32_t kStagesOffset = (kFixedBytes + 1023) / 1024 * 1024;
+    __host__ __device__ static size_t ints_offset(int stages) { return kStagesOffset + (size_t)stages * kStageBytes; }
+    __host__ __device__ static size_t smem_bytes(int batch, int s_max, int stages) {
+        return ints_offset(stages) + unit_table_ints(batch, s_max) * 4 + 1024;  // + 1024-byte alignment slack
+    }
+    // the most stages (2 .. kStagesMax) that fit in max_smem; 0 if not even 2 do
+    static int stages_for(int batch, int s_max, size_t max_smem) {
+        for (int st = kStagesMax; st >= 2; --st)
+            if (smem_bytes(batch, s_max, st) <= max_smem) return st;
+        return 0;
     }
 };
 
@@ -88,18 +96,19 @@ __global__ void __launch_bounds__(GqaWarps<G>::kThreads, 1)
     decode_gqa_kernel(const __grid_constant__ CUtensorMap tm_kv, DecodeArgs a) {
     using L = GqaLayout<D, G>;
     using W = GqaWarps<G>;
-    constexpr int kStagesG = L::kStages;
+    const int nst = a.stages;  // stages of the ring: 2 .. kStagesMax, chosen at launch
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kBarOffset);
-    uint64_t *empty = full + kStagesG;
-    uint64_t *mfull = empty + kStagesG;  // [2] the consumer warps' rows of a unit are in buffer i
-    uint64_t *mempty = mfull + 2;        // [2] the merge warp has read buffer i
+    uint8_t *base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    float *merge = reinterpret_cast<float *>(base);  // [2][kWarps][G][kMergeRow<D>]
+    uint64_t *full = reinterpret_cast<uint64_t *>(base + L::kBarOffset);
+    uint64_t *empty = full + kStagesMax;
+    uint64_t *mfull = empty + kStagesMax;  // [2] the consumer warps' rows of a unit are in buffer i
+    uint64_t *mempty = mfull + 2;          // [2] the merge warp has read buffer i
     volatile int *abort_flag = reinterpret_cast<volatile int *>(mempty + 2);
     int *stage_unit = reinterpret_cast<int *>(mempty + 2) + 4;
-    int *merge_unit = stage_unit + kStagesG;  // [2] unit of each merge buffer, -1: end
-    float *merge = reinterpret_cast<float *>(smem + L::kMergeOffset);  // [2][kWarps][G][kMergeRow<D>]
-    const UnitTable ut = unit_table(reinterpret_cast<int *>(smem + L::kIntsOffset), a.batch, a.s_max);
+    int *merge_unit = stage_unit + kStagesMax;  // [2] unit of each merge buffer, -1: end
+    uint8_t *smem = base + L::kStagesOffset;    // stage i at i * kStageBytes
+    const UnitTable ut = unit_table(reinterpret_cast<int *>(base + L::ints_offset(nst)), a.batch, a.s_max);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int hkv = a.cache.num_kv_heads, bs = a.cache.block_size, chunk = a.chunk;
@@ -107,7 +116,7 @@ __global__ void __launch_bounds__(GqaWarps<G>::kThreads, 1)
     const int br = bs < kTile ? bs : kTile;  // rows per page slice (tiles start at multiples of 64)
 
     if (tid == 0) {
-        for (int i = 0; i < kStagesG; ++i) {
+        for (int i = 0; i < nst; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], W::kConsumers);
         }
@@ -162,7 +171,7 @@ __global__ void __launch_bounds__(GqaWarps<G>::kThreads, 1)
                     }
                 }
                 if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.err)) {
-                    for (int i = 0; i < kStagesG; ++i)
+                    for (int i = 0; i < nst; ++i)
                         if (issued_mask & (1u << i)) {
                             volatile int no_abort = 0;
                             mbar_wait(&full[i], (issued_parity >> i) & 1u, &no_abort, nullptr);
@@ -192,7 +201,7 @@ __global__ void __launch_bounds__(GqaWarps<G>::kThreads, 1)
                 }
                 issued_mask |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-                if (++stage == kStagesG) {
+                if (++stage == nst) {
                     stage = 0;
                     phase ^= 1u;
                 }
@@ -359,7 +368,7 @@ __global__ void __launch_bounds__(GqaWarps<G>::kThreads, 1)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
-            if (++stage == kStagesG) {
+            if (++stage == nst) {
                 stage = 0;
                 phase ^= 1u;
             }
@@ -412,21 +421,24 @@ __global__ void __launch_bounds__(GqaWarps<G>::kThreads, 1)
 
 template <int D, int G, bool BF16>
 cudaError_t launch_gqa_t(const DecodeArgs &a, int grid, cudaStream_t s) {
+    using L = GqaLayout<D, G>;
     CUtensorMap tm;
     const int box_rows = a.cache.block_size < kTile ? a.cache.block_size : kTile;
     cudaError_t e = encode_kv5_map(a.cache, box_rows, &tm);
     if (e != cudaSuccess) return e;
+    const DeviceInfo &info = device_info();
+    DecodeArgs args = a;
+    args.stages = L::stages_for(a.batch, a.s_max, (size_t)info.max_smem);
+    if (args.stages == 0) return cudaErrorInvalidValue;  // tables of this batch and split count do not fit
     auto kern = decode_gqa_kernel<D, G, BF16>;
     static bool configured[64] = {};
-    const int dev = device_info().device;
-    if (dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)GqaLayout<D, G>::smem_bytes(kMaxBatchG, kDecodeMaxSplits));
+    if (info.device >= 64 || !configured[info.device]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, info.max_smem);
         if (e != cudaSuccess) return e;
-        if (dev < 64) configured[dev] = true;
+        if (info.device < 64) configured[info.device] = true;
     }
-    return launch_pdl(kern, dim3(grid), dim3(GqaWarps<G>::kThreads), GqaLayout<D, G>::smem_bytes(a.batch, a.s_max), s, tm,
-                      a);
+    return launch_pdl(kern, dim3(grid), dim3(GqaWarps<G>::kThreads), L::smem_bytes(a.batch, a.s_max, args.stages), s,
+                      tm, args);
 }
 
 }  // namespace

@@ -48,6 +48,9 @@ DeviceSlot &slot() {
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
             s.info.num_sms = sms > 0 ? sms : 1;
             s.info.decode_ctas_per_sm = 1;
+            int smem = 0;
+            cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+            s.info.max_smem = smem > 0 ? smem : 48 * 1024;
             void *p = nullptr;
             if (cudaGetSymbolAddress(&p, g_device_error) == cudaSuccess) s.err_ptr = static_cast<int *>(p);
             s.ready = true;
@@ -230,6 +233,7 @@ pkv_status decode_impl(const pkv_cache &cache, const void *q, int num_q_heads, c
     a.scale = scale;
     a.chunk = chunk;
     a.s_max = s_max;
+    a.stages = 0;  // set by the group kernel's launcher
     // query heads per unit: the FP8 kernel holds 8 head slots, the native group kernel 16
     const int per_unit = (cache.format == PKV_KV_FP8_E4M3) ? 8 : (group % 16 == 0 ? 16 : 8);
     a.head_groups = group > per_unit ? group / per_unit : 1;

@@ -48,6 +48,7 @@ struct DecodeArgs {
     // cu_q_lens[b]. nullptr: every sequence has one query row, row b.
     const int *cu_q_lens;
     int s_max;   // splits a full-capacity context uses: ceil(max_blocks_per_seq * block_size / chunk)
+    int stages;  // pipeline stages of the group kernel (chosen at launch from the shared memory left)
     float *part_o;    // [batch, Hq, s_max, D]
     float *part_lse;  // [batch, Hq, s_max]
     void *out;
@@ -109,6 +110,7 @@ struct DeviceInfo {
     int device;
     int num_sms;
     int decode_ctas_per_sm;
+    int max_smem;  // dynamic shared memory a CTA may opt in to (bytes)
 };
 const DeviceInfo &device_info();
 int *device_error_word();  // the current device's sticky error word (device address)

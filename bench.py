@@ -590,7 +590,7 @@ def bench_mqa(torch, steps, warmup):
     del cache
     torch.cuda.empty_cache()
     return {"workload": "MQA decode: 128 seqs, contexts U[1024, 8192], 32 query heads / 1 KV head x 128, bf16, "
-                        "bs 16 (each group of 16 query heads is one tensor-core unit over the shared pages)",
+                        "bs 16 (the 32 query heads are one tensor-core unit over the shared pages)",
             "ms": round(ms, 4), "kv_gbs": round(b["kv"] / ms / 1e6, 1),
             "frac_of_hbm": round(b["total"] / ms / 1e6 / peaks()["hbm_gbs"], 3),
             "tokens_per_s": round(p.batch / ms * 1e3, 1)}

@@ -124,11 +124,11 @@ __device__ __forceinline__ float tree_sum(const float (&x)[N]) {
 // in log2 units, acc and l relative to 2^m), the unit id is written (warp 0) and mfull[i] completes;
 // this loop combines the rows -- M = max m, weights 2^(m_w - M), out = sum w acc / sum w l, lse =
 // (M + log2 sum w l) ln 2 -- writes the final output of a single-split context or the split's
-// partial, and frees the buffer on mempty[i]. Buffers alternate; unit id -1 ends the loop. Lane g
+// partial, and frees the buffer on mempty[i]. NB buffers (1 or 2) take turns; unit id -1 ends the loop. Lane g
 // finds the weights of head g (all heads at once); then each head's output is D / 32 consecutive
 // dims per lane, read and written as vectors. Returns false if a wait gave up (the error word is
 // set).
-template <int D, int G, int W>
+template <int D, int G, int W, int NB = 2>
 __device__ __forceinline__ bool merge_warp_loop(const DecodeArgs &a, const UnitTable &ut, const float *merge,
                                                 size_t buf_floats, uint64_t *mfull, uint64_t *mempty,
                                                 const int *merge_unit, volatile int *abort_flag, int lane) {
@@ -209,7 +209,7 @@ __device__ __forceinline__ bool merge_warp_loop(const DecodeArgs &a, const UnitT
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&mempty[mbuf]);
-        if (++mbuf == 2) {
+        if (++mbuf == NB) {
             mbuf = 0;
             mphase ^= 1u;
         }

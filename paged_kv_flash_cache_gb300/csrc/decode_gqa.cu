@@ -26,7 +26,8 @@
 //     heads in the N slots (padding slots are zero); the scores stay in the accumulator fragments:
 //     column max by shuffles, lazy rescale (threshold 2^8), exp2, and P moved into B-fragment
 //     layout with movmatrix; O^T accumulates in registers; at the end of a unit each warp leaves
-//     its rows in one of two shared-memory merge buffers and goes on with the next unit;
+//     its rows in a shared-memory merge buffer (two taking turns; one for 16-head units) and goes
+//     on with the next unit;
 //   * the last warp merges the four token slices' rows and writes the output (single split) or
 //     the split partials.
 #include <cuda.h>
@@ -45,7 +46,7 @@ constexpr int kTile = 64;                         // tokens per stage
 constexpr int kStagesMax = 6;
 constexpr float kRescale = 8.0f;                  // lazy rescale threshold (log2 units)
 
-// Shared memory: the two merge buffers, the barriers and unit ids (fixed sizes), then from the
+// Shared memory: the merge buffers, the barriers and unit ids (fixed sizes), then from the
 // next 1024-byte boundary the ring of stages, then the unit tables (sized by batch and splits).
 template <int D, int G>
 struct GqaLayout {
@@ -56,10 +57,13 @@ struct GqaLayout {
     static constexpr uint32_t kHalfRegion = 2 * kHalfBytes;
     static constexpr uint32_t kQBytes = G * D * 2;
     static constexpr uint32_t kStageBytes = (2 * kKBytes + kQBytes + 1023) / 1024 * 1024;
-    static constexpr uint32_t kMergeFloats = kWarps * G * kMergeRow<D>;  // one of two merge buffers
+    static constexpr uint32_t kMergeFloats = kWarps * G * kMergeRow<D>;  // one merge buffer
+    // 16 heads: one merge buffer (the consumers wait for the merge of the previous unit), which
+    // leaves room for a fifth stage; fewer heads: two, taking turns
+    static constexpr int kMergeBufs = G >= 16 ? 1 : 2;
     // barriers: full / empty per stage slot, merge full / empty per merge buffer; then the abort
     // flag (padded to 16 bytes), the unit of each stage slot and the unit of each merge buffer
-    static constexpr uint32_t kBarOffset = 2 * kMergeFloats * 4;
+    static constexpr uint32_t kBarOffset = kMergeBufs * kMergeFloats * 4;
     static constexpr uint32_t kFixedBytes = kBarOffset + (2 * kStagesMax + 4) * 8 + 16 + (kStagesMax + 2) * 4;
     static constexpr uint32_t kStagesOffset = (kFixedBytes + 1023) / 1024 * 1024;
     __host__ __device__ static size_t ints_offset(int stages) { return kStagesOffset + (size_t)stages * kStageBytes; }
@@ -99,7 +103,7 @@ __global__ void __launch_bounds__(GqaWarps<G>::kThreads, 1)
     const int nst = a.stages;  // stages of the ring: 2 .. kStagesMax, chosen at launch
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-    float *merge = reinterpret_cast<float *>(base);  // [2][kWarps][G][kMergeRow<D>]
+    float *merge = reinterpret_cast<float *>(base);  // [kMergeBufs][kWarps][G][kMergeRow<D>]
     uint64_t *full = reinterpret_cast<uint64_t *>(base + L::kBarOffset);
     uint64_t *empty = full + kStagesMax;
     uint64_t *mfull = empty + kStagesMax;  // [2] the consumer warps' rows of a unit are in buffer i
@@ -218,7 +222,8 @@ __global__ void __launch_bounds__(GqaWarps<G>::kThreads, 1)
 
     if (warp == W::kMerge) {
         // ====================================== merge warp ======================================
-        merge_warp_loop<D, G, kWarps>(a, ut, merge, L::kMergeFloats, mfull, mempty, merge_unit, abort_flag, lane);
+        merge_warp_loop<D, G, kWarps, L::kMergeBufs>(a, ut, merge, L::kMergeFloats, mfull, mempty, merge_unit, abort_flag,
+                                                    lane);
         pdl_launch_dependents();
         return;
     }
@@ -405,7 +410,7 @@ __global__ void __launch_bounds__(GqaWarps<G>::kThreads, 1)
         if (warp == 0 && lane == 0) merge_unit[mbuf] = u;
         __syncwarp();
         if (lane == 0) mbar_arrive(&mfull[mbuf]);
-        if (++mbuf == 2) {
+        if (++mbuf == L::kMergeBufs) {
             mbuf = 0;
             mphase ^= 1u;
         }
@@ -451,6 +456,7 @@ cudaError_t launch_decode_gqa(const DecodeArgs &a, int grid, cudaStream_t s) {
         if (group == 4) return bf16 ? launch_gqa_t<128, 4, true>(a, grid, s) : launch_gqa_t<128, 4, false>(a, grid, s);
         if (group == 8) return bf16 ? launch_gqa_t<128, 8, true>(a, grid, s) : launch_gqa_t<128, 8, false>(a, grid, s);
         if (group == 16) return bf16 ? launch_gqa_t<128, 16, true>(a, grid, s) : launch_gqa_t<128, 16, false>(a, grid, s);
+        if (group == 32) return bf16 ? launch_gqa_t<128, 32, true>(a, grid, s) : launch_gqa_t<128, 32, false>(a, grid, s);
     } else {
         if (group == 4) return bf16 ? launch_gqa_t<64, 4, true>(a, grid, s) : launch_gqa_t<64, 4, false>(a, grid, s);
         if (group == 8) return bf16 ? launch_gqa_t<64, 8, true>(a, grid, s) : launch_gqa_t<64, 8, false>(a, grid, s);

@@ -234,8 +234,11 @@ pkv_status decode_impl(const pkv_cache &cache, const void *q, int num_q_heads, c
     a.chunk = chunk;
     a.s_max = s_max;
     a.stages = 0;  // set by the group kernel's launcher
-    // query heads per unit: the FP8 kernel holds 8 head slots, the native group kernel 16
-    const int per_unit = (cache.format == PKV_KV_FP8_E4M3) ? 8 : (group % 16 == 0 ? 16 : 8);
+    // query heads per unit: the FP8 kernel holds 8 head slots, the native group kernel 32 (head_dim
+    // 128), 16 or 8
+    const int per_unit = (cache.format == PKV_KV_FP8_E4M3) ? 8
+                         : (group % 32 == 0 && cache.head_dim == 128) ? 32
+                         : (group % 16 == 0) ? 16 : 8;
     a.head_groups = group > per_unit ? group / per_unit : 1;
     a.cu_q_lens = cu_q_lens;
     a.part_o = static_cast<float *>(workspace);

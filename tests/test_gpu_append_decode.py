@@ -224,10 +224,12 @@ def test_decode_large_batch_many_equal_lengths(hq, hkv):
 
 
 @pytest.mark.parametrize("dtype", [W.F16, W.BF16])
-@pytest.mark.parametrize("hq,hkv,d", [(32, 1, 128), (16, 1, 64), (64, 4, 128), (24, 1, 128)])
+@pytest.mark.parametrize("hq,hkv,d", [(32, 1, 128), (16, 1, 64), (64, 4, 128), (24, 1, 128), (64, 1, 128),
+                                     (32, 1, 64)])
 def test_decode_mqa_and_wide_groups(dtype, hq, hkv, d):
     """One KV head for many query heads (MQA) and groups above 8: the tensor-core kernel takes
-    each 8 query heads of a KV head as one unit, all reading that KV head's pages."""
+    the query heads of a KV head in units of 32 (head_dim 128), 16 or 8, all units reading that
+    KV head's pages (64 heads: two units of 32; 24: three of 8; head_dim 64 at 32: two of 16)."""
     p = problem(lens=[5, 700, 129, 2000], hq=hq, hkv=hkv, d=d, dtype=dtype, bs=32, seed=hq * 3 + d)
     cache = device_cache(p)
     out, lse = run_decode(p, cache)

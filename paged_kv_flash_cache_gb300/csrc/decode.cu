@@ -532,6 +532,22 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
     pdl_launch_dependents();
 }
 
+// V (2 or 4) consecutive floats from a 4V-byte aligned address, as one vector load.
+template <int V>
+__device__ __forceinline__ void load_vec(const float *src, float (&x)[V]) {
+    if constexpr (V == 4) {
+        const float4 v = *reinterpret_cast<const float4 *>(src);
+        x[0] = v.x;
+        x[1] = v.y;
+        x[2] = v.z;
+        x[3] = v.w;
+    } else {
+        const float2 v = *reinterpret_cast<const float2 *>(src);
+        x[0] = v.x;
+        x[1] = v.y;
+    }
+}
+
 // ---- split merge: one warp per output row --------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
@@ -559,7 +575,7 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (row >= a.n_rows || done_by_split) return;
     const float *pl = a.part_lse + (size_t)row * a.num_splits;
-    const float *po = a.part_o + (size_t)row * a.num_splits * D;
+    const float *po = a.part_o + (size_t)row * a.num_splits * D + kPer * lane;
     float M = -INFINITY;
     for (int s = lane; s < S; s += 32) M = fmaxf(M, pl[s]);
 #pragma unroll
@@ -569,20 +585,32 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
     for (int j = 0; j < kPer; ++j) o_acc[j] = 0.f;
     float wsum = 0.f;
     if (M != -INFINITY) {
-        // 32 splits at a time: lane s holds split s's weight; partial rows are read with the
-        // loads of four splits in flight
+        // 32 splits at a time: lane s holds split s's weight; each lane reads its kPer consecutive
+        // dims of a partial row as one vector, eight splits' loads in flight before their sums
         for (int s0 = 0; s0 < S; s0 += 32) {
             const int s_l = s0 + lane;
             const float ls = s_l < S ? pl[s_l] : -INFINITY;
             const float w_l = ls == -INFINITY ? 0.f : exp2f((ls - M) * kLog2e);
             wsum += w_l;
             const int n = min(32, S - s0);
-#pragma unroll 4
-            for (int k = 0; k < n; ++k) {
-                const float w = __shfl_sync(0xffffffffu, w_l, k);
-                const float *src = po + (size_t)(s0 + k) * D + lane * kPer;
+            int k = 0;
+            for (; k + 8 <= n; k += 8) {
+                float x[8][kPer];
 #pragma unroll
-                for (int j = 0; j < kPer; ++j) o_acc[j] = fmaf(w, src[j], o_acc[j]);
+                for (int i = 0; i < 8; ++i) load_vec<kPer>(po + (size_t)(s0 + k + i) * D, x[i]);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float w = __shfl_sync(0xffffffffu, w_l, k + i);
+#pragma unroll
+                    for (int j = 0; j < kPer; ++j) o_acc[j] = fmaf(w, x[i][j], o_acc[j]);
+                }
+            }
+            for (; k < n; ++k) {
+                float x[kPer];
+                load_vec<kPer>(po + (size_t)(s0 + k) * D, x);
+                const float w = __shfl_sync(0xffffffffu, w_l, k);
+#pragma unroll
+                for (int j = 0; j < kPer; ++j) o_acc[j] = fmaf(w, x[j], o_acc[j]);
             }
         }
 #pragma unroll
@@ -590,7 +618,8 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) store_out(a.out, out_row * D + lane * kPer + j, o_acc[j] * inv, a.out_dtype);
+    for (int j = 0; j < kPer; ++j) o_acc[j] *= inv;
+    store_out_vec<kPer>(a.out, out_row * D + lane * kPer, o_acc, a.out_dtype);
     if (lane == 0 && a.lse) a.lse[out_row] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
 }
 

@@ -169,7 +169,8 @@ PKV_API pkv_status pkv_paged_attn_decode(pkv_cache cache, const void *q, int num
  *   causal        non-zero: query r of sequence b sits at absolute position
  *                 context_lens[b] - q_len_b + r and sees keys 0 .. that position
  *                 (bottom-right alignment); zero: every query sees the whole context.
- *   max_q_len     an upper bound of q_len_b over the batch (sizes the grid).
+ *   max_q_len     an upper bound of q_len_b over the batch (sizes the grid; batch and
+ *                 ceil(max_q_len / 256) at most 65535 each, else PKV_ERR_UNSUPPORTED).
  *   out           [total_q, Hq, D] in out_dtype; lse FP32 [total_q, Hq] or NULL. */
 PKV_API pkv_status pkv_paged_attn_prefill(pkv_cache cache, const void *q, int num_q_heads,
                                   const int *cu_q_lens, const int *context_lens,

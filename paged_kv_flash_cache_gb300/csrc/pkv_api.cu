@@ -333,6 +333,8 @@ pkv_status prefill_impl(const pkv_cache &cache, const void *q, int num_q_heads, 
     if (!aligned16(q) || !aligned16(out) || (lse && !aligned16(lse))) return PKV_ERR_INVALID_ARG;
     const long long cap = (long long)max_blocks_per_seq * cache.block_size;
     if (cap > (1ll << 30)) return PKV_ERR_UNSUPPORTED;
+    // grid (heads, sequences, 256-row blocks): the last two dimensions hold at most 65535
+    if (batch > 65535 || (max_q_len + 255) / 256 > 65535) return PKV_ERR_UNSUPPORTED;
     DeviceSlot &s = slot();
     PrefillArgs a;
     a.cache = view_of(cache);

@@ -155,7 +155,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float *sScale = reinterpret_cast<const float *>(smem + Lay::kScaleOff);  // FP8: [kRing][128]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int mt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    // grid (heads, batch, row blocks) with the row blocks last-first: CTAs start in linear order, so
+    // the row blocks that see the most keys (causal) start in the first wave and the short ones
+    // fill in behind them
+    const int mt = (int)gridDim.z - 1 - (int)blockIdx.z, h = blockIdx.x, b = blockIdx.y;
     pdl_wait();  // lengths, tables, q and the chunk's own K/V may come from the previous kernel
     const int q0 = __ldg(p.cu_q_lens + b);
     const int q_len = __ldg(p.cu_q_lens + b + 1) - q0;
@@ -739,7 +742,7 @@ cudaError_t launch_t(const PrefillArgs &a, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         if (dev < 64) configured[dev] = true;
     }
-    dim3 grid((a.max_q_len + kRows - 1) / kRows, a.num_q_heads, a.batch);
+    dim3 grid(a.num_q_heads, a.batch, (a.max_q_len + kRows - 1) / kRows);
     return launch_pdl(kern, grid, dim3(kThreads), Lay::kSmemBytes, stream, tm_q, tm_kv, p);
 }
 

@@ -79,6 +79,11 @@ def test_host_validation_without_gpu(lib):
     # prefill: negative total_q
     assert lib.pkv_paged_attn_prefill(_cache(), good, 2, good, good, good, 1, 4, -1, 4, F(0.1), 1, good, 0, None,
                                       None) == 1
+    # prefill grid (heads, sequences, 256-row blocks): more than 65535 sequences or row blocks
+    assert lib.pkv_paged_attn_prefill(_cache(), good, 2, good, good, good, 65536, 4, 65536, 1, F(0.1), 1, good, 0,
+                                      None, None) == 2
+    assert lib.pkv_paged_attn_prefill(_cache(), good, 2, good, good, good, 1, 4, 1 << 25, 1 << 25, F(0.1), 1, good,
+                                      0, None, None) == 2
     # combine: bad head_dim, bad split count
     assert lib.pkv_attn_combine(good, good, 4, 2, 96, good, 2, None, None) == 2
     assert lib.pkv_attn_combine(good, good, 4, 0, 128, good, 2, None, None) == 1

@@ -14,9 +14,12 @@
 //     context lengths (decode_common.cuh: split-major, all KV heads of a sequence together)
 //     and dealt round-robin to the CTAs;
 //   * warp 8 (producer) streams each unit's tokens in 64-token tiles into a ring of
-//     shared-memory stages with bulk copies (TMA engine, one copy per page slice of K and of
-//     V -- pages are contiguous [block_size, D] rows), completion on an mbarrier; page ids
-//     are read one unit ahead;
+//     shared-memory stages, completion on an mbarrier; page ids are read one unit ahead. A
+//     16-bit cache comes by TMA, one box per page slice of min(block_size, 64) tokens holding
+//     the slice's K rows and then its V rows (the cache viewed as [NB][2][Hkv][bs][D]); an FP8
+//     cache by bulk copies, one per page slice of K, of V and of their row scales. Every read
+//     carries an L2 evict-first policy: the stream is read once, and without the hint it
+//     pushed the lines still in use out of L2;
 //   * warps 0-7 (consumers) each take 8 tokens of a tile: lanes split D into 16-byte
 //     chunks, q.k partial sums are reduced with xor shuffles, and every lane keeps running
 //     (m, l, acc) for the query heads of its KV head, so each K/V byte is read from HBM once
@@ -31,6 +34,7 @@
 #include "decode_common.cuh"
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
+#include "tcgen05.cuh"
 
 namespace pkv {
 namespace {
@@ -94,8 +98,23 @@ __device__ __forceinline__ float row_scale(const float *scales, int t) {
     else return 1.f;
 }
 
+// Tile row of token t. A native cache arrives by one TMA box per page slice of br = min(bs, 64)
+// tokens holding the slice's K rows and then its V rows, so slice j starts at row 2 j br; an
+// FP8 cache arrives by bulk copies, all K rows first and the V rows from row kTile on.
+template <bool FP8>
+__device__ __forceinline__ int k_row(int t, int br) {
+    if constexpr (FP8) return t;
+    else return t + (t & -br);
+}
+template <bool FP8>
+__device__ __forceinline__ int v_row(int t, int br, int tile) {
+    if constexpr (FP8) return t + tile;
+    else return t + (t & -br) + br;
+}
+
 template <typename Tag, int D, int G, bool FP8>
-__global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kDecodeThreads, 1)
+    decode_split_kernel(const __grid_constant__ CUtensorMap tm_kv, DecodeArgs a) {
     using L = DecodeLayout<D, G, FP8>;
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kBarOffset);
@@ -185,7 +204,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
                 const bool first_tile = (ts == c.t0);
                 if (lane == 0) {
                     stage_unit[stage] = u;
-                    uint32_t bytes = (uint32_t)n * D * L::kKB * 2 + (first_tile ? (uint32_t)L::kQBytes : 0u);
+                    // native: whole page slices (rows past the context come too; the consumers
+                    // mask their scores and skip their V rows); FP8: the valid rows
+                    uint32_t bytes = (FP8 ? (uint32_t)n : (uint32_t)npages * (uint32_t)(bs < L::kTile ? bs : L::kTile)) *
+                                         D * L::kKB * 2 +
+                                     (first_tile ? (uint32_t)L::kQBytes : 0u);
                     if constexpr (FP8) {
                         // row scales, each page slice's copy rounded up to 4 rows (16 bytes)
                         for (int lp = first_page; lp <= last_page; ++lp) {
@@ -196,7 +219,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
                     mbar_arrive_expect_tx(&full[stage], bytes);
                 }
                 __syncwarp();
-                if (lane < npages) {
+                if constexpr (!FP8) {
+                    if (lane < npages) {
+                        // one box: the slice's K rows, then its V rows (page pb, head c.kvh, rows off..)
+                        const int lp = first_page + lane;
+                        const int off = max(ts, lp * bs) - lp * bs;
+                        const int br = bs < L::kTile ? bs : L::kTile;
+                        tc::tma_load_5d_hint(st + (size_t)lane * 2 * br * D * L::kKB, &tm_kv, 0, off, c.kvh, 0, pb,
+                                             &full[stage], pol);
+                    }
+                } else if (lane < npages) {
                     const int lp = first_page + lane;
                     const int tok_lo = max(ts, lp * bs);
                     const int tok_hi = min(ts + n, (lp + 1) * bs);
@@ -207,7 +239,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
                     uint8_t *dk = st + (size_t)(tok_lo - ts) * D * L::kKB;
                     bulk_g2s(dk, cache + kbase, bytes, &full[stage], pol);
                     bulk_g2s(dk + L::kKBytes, cache + vbase, bytes, &full[stage], pol);
-                    if constexpr (FP8) {
+                    {
                         // off and tok_lo - ts are multiples of 4 rows, and a page holds a multiple
                         // of 4 rows, so the rounded-up copy stays inside the page's scale row
                         const float *ksrc = a.cache.scales + (((size_t)pb * 2) * hkv + c.kvh) * bs + off;
@@ -248,6 +280,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
     }
 
     // ================================ consumer warps ================================
+    const int br = bs < L::kTile ? bs : L::kTile;  // rows per page slice (native cache)
     const int slot = lane / L::kLanesPerTok;   // token slot within a step
     const int chk = lane % L::kLanesPerTok;    // this lane's 8-element chunk of D
     const float qscale = a.scale * kLog2e;     // scores in log2 units
@@ -298,8 +331,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
                 }
             }
             if constexpr (G == 1) {
-            const uint8_t *sk = st;
-            const uint8_t *sv = st + L::kKBytes;
             const float *ksc = reinterpret_cast<const float *>(st + L::kSOffset);  // FP8 row scales
             const float *vsc = ksc + L::kTile;
             (void)ksc; (void)vsc;
@@ -312,7 +343,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
                     const int t = warp * L::kTokPerWarp + (b0 + i) * L::kTokPerStep + slot;
                     valid[i] = t < n;
                     float2 kf[4];
-                    load_row8<Tag, D, FP8>(sk, t, chk, kf);
+                    load_row8<Tag, D, FP8>(st, k_row<FP8>(t, br), chk, kf);
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
                         float2 pp = fmul2(qf[g][0], kf[0]);
@@ -351,7 +382,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
                     if (!valid[i]) continue;
                     const int t = warp * L::kTokPerWarp + (b0 + i) * L::kTokPerStep + slot;
                     float2 vf[4];
-                    load_row8<Tag, D, FP8>(sv, t, chk, vf);
+                    load_row8<Tag, D, FP8>(st, v_row<FP8>(t, br, L::kTile), chk, vf);
                     const float vs = row_scale<FP8>(vsc, t);
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
@@ -363,8 +394,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
                 }
             }
             } else {
-            const uint8_t *sk = st;
-            const uint8_t *sv = st + L::kKBytes;
             const float *ksc = reinterpret_cast<const float *>(st + L::kSOffset);  // FP8 row scales
             const float *vsc = ksc + L::kTile;
             (void)ksc; (void)vsc;
@@ -377,7 +406,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
                 for (int i = 0; i < S; ++i) {
                     const int t = warp * L::kTokPerWarp + (b0 + i) * L::kTokPerStep + slot;
                     float2 kf[4];
-                    load_row8<Tag, D, FP8>(sk, t, chk, kf);
+                    load_row8<Tag, D, FP8>(st, k_row<FP8>(t, br), chk, kf);
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
                         float2 pp = fmul2(qf[g][0], kf[0]);
@@ -442,7 +471,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_split_kernel(DecodeA
                     const int t = warp * L::kTokPerWarp + (b0 + i) * L::kTokPerStep + slot;
                     if (t >= n) continue;
                     float2 vf[4];
-                    load_row8<Tag, D, FP8>(sv, t, chk, vf);
+                    load_row8<Tag, D, FP8>(st, v_row<FP8>(t, br, L::kTile), chk, vf);
                     const float vs = row_scale<FP8>(vsc, t);
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
@@ -639,7 +668,13 @@ cudaError_t launch_decode_t(const DecodeArgs &a, int grid, cudaStream_t s) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    return launch_pdl(kern, dim3(grid), dim3(kDecodeThreads), smem, s, a);
+    CUtensorMap tm = {};  // native cache: K and V rows of a page slice per box; FP8: unused
+    if constexpr (!FP8) {
+        const int br = a.cache.block_size < kDecodeTile ? a.cache.block_size : kDecodeTile;
+        const cudaError_t e = encode_kv5_rows_map(a.cache, br, &tm);
+        if (e != cudaSuccess) return e;
+    }
+    return launch_pdl(kern, dim3(grid), dim3(kDecodeThreads), smem, s, tm, a);
 }
 
 template <typename Tag, int D>

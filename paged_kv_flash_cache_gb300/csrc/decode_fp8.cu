@@ -207,9 +207,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane < nslices) {
                     // one box: the slice's K rows then its V rows (page pb, head c.kvh, rows off..)
                     const int kvr = c.kvh / a.head_groups;  // the KV head of this unit
-                    tc::tma_load_5d(st + (size_t)lane * 2 * br * kD, &tm_codes, 0, off, kvr, 0, pb, &full[stage]);
-                    tc::tma_load_4d(st + L::kSOffset + (size_t)lane * spitch, &tm_scales, off, kvr, 0, pb,
-                                    &full[stage]);
+                    tc::tma_load_5d_hint(st + (size_t)lane * 2 * br * kD, &tm_codes, 0, off, kvr, 0, pb, &full[stage],
+                                         pol);
+                    tc::tma_load_4d_hint(st + L::kSOffset + (size_t)lane * spitch, &tm_scales, off, kvr, 0, pb,
+                                         &full[stage], pol);
                 }
                 if (first_tile && lane == 0) {
                     const uint16_t *qsrc = qg + ((size_t)ut.qrow[c.b] * a.num_q_heads + (size_t)c.kvh * G) * kD;

@@ -197,7 +197,8 @@ __global__ void __launch_bounds__(GqaWarps<G>::kThreads, 1)
                     const uint32_t dst = (uint32_t)lane * 2u * br * 128u;
 #pragma unroll
                     for (int hf = 0; hf < L::kHalves; ++hf)
-                        tc::tma_load_5d(st + hf * L::kHalfRegion + dst, &tm_kv, hf * 64, off, kvr, 0, pb, &full[stage]);
+                        tc::tma_load_5d_hint(st + hf * L::kHalfRegion + dst, &tm_kv, hf * 64, off, kvr, 0, pb,
+                                             &full[stage], pol);
                 }
                 if (first_tile && lane == 0) {
                     const uint16_t *qsrc = qg + ((size_t)ut.qrow[c.b] * a.num_q_heads + (size_t)c.kvh * G) * D;

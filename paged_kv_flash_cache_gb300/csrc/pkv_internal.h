@@ -120,6 +120,9 @@ constexpr int kDecodeMaxSplits = 2048;  // splits of one context (bounds the spl
 
 cudaError_t launch_append(const AppendArgs &a, cudaStream_t s);
 cudaError_t encode_cache_map(const CacheView &c, int box_rows, CUtensorMap *map);
+// As encode_kv5_map with whole rows of D elements per box row and no swizzle (the CUDA-core
+// decode reads plain rows).
+cudaError_t encode_kv5_rows_map(const CacheView &c, int box_rows, CUtensorMap *map);
 cudaError_t encode_kv5_map(const CacheView &c, int box_rows, CUtensorMap *map);
 cudaError_t encode_fp8_maps(const CacheView &c, int box_rows, CUtensorMap *codes, CUtensorMap *scales);
 cudaError_t launch_decode_gqa(const DecodeArgs &a, int grid, cudaStream_t s);

@@ -665,6 +665,25 @@ cudaError_t encode_kv5_map(const CacheView &c, int box_rows, CUtensorMap *map) {
     return cudaSuccess;
 }
 
+cudaError_t encode_kv5_rows_map(const CacheView &c, int box_rows, CUtensorMap *map) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    if (c.fp8) return cudaErrorNotSupported;
+    const cuuint64_t D = (cuuint64_t)c.head_dim, bs = (cuuint64_t)c.block_size, h = (cuuint64_t)c.num_kv_heads;
+    const cuuint64_t nb = (cuuint64_t)c.num_blocks;
+    if (nb == 0 || nb > 0x7fffffffull || D > 256) return cudaErrorNotSupported;
+    const CUtensorMapDataType dt = c.dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    cuuint64_t dims[5] = {D, bs, h, 2, nb};
+    cuuint64_t strides[4] = {D * 2, D * bs * 2, D * bs * h * 2, D * bs * h * 2 * 2};
+    cuuint32_t box[5] = {(cuuint32_t)D, (cuuint32_t)box_rows, 1, 2, 1};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    if (enc(map, dt, 5, const_cast<void *>(c.ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+        CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    return cudaSuccess;
+}
+
 // An FP8 cache: the codes as encode_kv5_map, the scales as the 4-D tensor [NB][2][Hkv][bs]
 // (box box_rows x 1 x 2 x 1: K scales, then V scales).
 cudaError_t encode_fp8_maps(const CacheView &c, int box_rows, CUtensorMap *codes, CUtensorMap *scales) {

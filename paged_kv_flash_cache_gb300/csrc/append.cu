@@ -12,6 +12,8 @@
 // every SM busy even when a call appends a few thousand tokens.
 // Pure bandwidth: 2 reads + 2 writes of Hkv * D * 2 bytes per token (an FP8 cache: writes of
 // Hkv * (D + 4) bytes for each of K and V).
+#include <climits>
+
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
@@ -31,9 +33,47 @@ __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
 
 constexpr int kHeadsPerItem = 8;  // a work item is one token's K and V rows of up to 8 heads
 
+// Page and in-page row of new token t (all lanes of the warp, same t). The sequence is the last b
+// with cu_new_lens[b] <= t, i.e. the count of b in [1, batch) with cu_new_lens[b] <= t (lengths
+// are non-negative): up to 32 sequences, one load per lane and a ballot, ctx_before read in the
+// same round trip; more, a binary search. Returns false (error word set) for a position outside
+// the table or a page id outside the pool.
+__device__ __forceinline__ bool token_slot(const AppendArgs &a, int t, int lane, int &pb, int &off) {
+    int b;
+    long long pos;
+    if (a.batch <= 32) {
+        const int cu_j = (lane >= 1 && lane < a.batch) ? __ldg(a.cu_new_lens + lane) : INT_MAX;
+        const int ctx_j = lane < a.batch ? __ldg(a.ctx_before + lane) : 0;
+        const int cu_b_j = lane < a.batch ? __ldg(a.cu_new_lens + lane) : 0;
+        b = __popc(__ballot_sync(0xffffffffu, cu_j <= t));
+        pos = (long long)__shfl_sync(0xffffffffu, ctx_j, b) + (t - __shfl_sync(0xffffffffu, cu_b_j, b));
+    } else {
+        int lo = 0, hi = a.batch;  // answer in [lo, hi)
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (__ldg(a.cu_new_lens + mid) <= t) lo = mid; else hi = mid;
+        }
+        b = lo;
+        pos = (long long)__ldg(a.ctx_before + b) + (t - __ldg(a.cu_new_lens + b));
+    }
+    const long long logical = pos >> a.log2_block_size;
+    if (pos < 0 || logical >= a.max_blocks_per_seq) {
+        if (lane == 0) set_error(a.err, kErrDeviceRange);
+        return false;
+    }
+    pb = __ldg(a.block_tables + (size_t)b * a.max_blocks_per_seq + logical);
+    if (pb < 0 || pb >= a.num_blocks) {
+        if (lane == 0) set_error(a.err, kErrDeviceRange);
+        return false;
+    }
+    off = (int)(pos & (a.block_size - 1));
+    return true;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kAppendThreads) append_kernel(AppendArgs a) {
     constexpr int kVecPerRow = D / 8;  // 16-byte vectors per head row
+    static_assert(kHeadsPerItem * kVecPerRow <= 32 * kUnroll, "one pass of the warp per item");
     const int lane = threadIdx.x & 31;
     const int warps_total = gridDim.x * (kAppendThreads / 32);
     const int hkv = a.num_kv_heads;
@@ -53,48 +93,31 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(AppendArgs a) {
         const int t = (int)(it / chunks);
         const int h0 = (int)(it - (long long)t * chunks) * kHeadsPerItem;
         const int nvec = min(kHeadsPerItem, hkv - h0) * kVecPerRow;
-        // sequence of token t: last b with cu_new_lens[b] <= t
-        int lo = 0, hi = a.batch;  // answer in [lo, hi)
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (__ldg(a.cu_new_lens + mid) <= t) lo = mid; else hi = mid;
-        }
-        const int b = lo;
-        const long long pos = (long long)__ldg(a.ctx_before + b) + (t - __ldg(a.cu_new_lens + b));
-        const long long logical = pos >> a.log2_block_size;
-        if (pos < 0 || logical >= a.max_blocks_per_seq) {
-            if (lane == 0) set_error(a.err, kErrDeviceRange);
-            continue;
-        }
-        const int pb = __ldg(a.block_tables + (size_t)b * a.max_blocks_per_seq + logical);
-        if (pb < 0 || pb >= a.num_blocks) {
-            if (lane == 0) set_error(a.err, kErrDeviceRange);
-            continue;
-        }
-        const int off = (int)(pos & (a.block_size - 1));
-        const size_t page_base = (size_t)pb * 2 * kv_stride + (size_t)off * kVecPerRow;
+        // the item's K and V vectors first: they depend only on the token, so their loads overlap
+        // the lookup of its page
         const uint4 *ks = kn + (size_t)t * vec_per_token + (size_t)h0 * kVecPerRow;
         const uint4 *vs = vn + (size_t)t * vec_per_token + (size_t)h0 * kVecPerRow;
-        for (int c0 = lane; c0 < nvec; c0 += 32 * kUnroll) {
-            uint4 kv[kUnroll], vv[kUnroll];
+        uint4 kv[kUnroll], vv[kUnroll];
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int c = c0 + u * 32;
-                if (c < nvec) {
-                    kv[u] = ld_stream(ks + c);
-                    vv[u] = ld_stream(vs + c);
-                }
+        for (int u = 0; u < kUnroll; ++u) {
+            const int c = lane + u * 32;
+            if (c < nvec) {
+                kv[u] = ld_stream(ks + c);
+                vv[u] = ld_stream(vs + c);
             }
+        }
+        int pb, off;
+        if (!token_slot(a, t, lane, pb, off)) continue;
+        const size_t page_base = (size_t)pb * 2 * kv_stride + (size_t)off * kVecPerRow;
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int c = c0 + u * 32;
-                if (c < nvec) {
-                    const int h = h0 + c / kVecPerRow;
-                    const int e = c % kVecPerRow;
-                    const size_t dst = page_base + (size_t)h * head_stride + e;
-                    cache[dst] = kv[u];
-                    cache[dst + kv_stride] = vv[u];
-                }
+        for (int u = 0; u < kUnroll; ++u) {
+            const int c = lane + u * 32;
+            if (c < nvec) {
+                const int h = h0 + c / kVecPerRow;
+                const int e = c % kVecPerRow;
+                const size_t dst = page_base + (size_t)h * head_stride + e;
+                cache[dst] = kv[u];
+                cache[dst + kv_stride] = vv[u];
             }
         }
     }
@@ -125,25 +148,8 @@ __global__ void __launch_bounds__(kAppendThreads) append_fp8_kernel(AppendArgs a
         const int t = (int)(it / chunks);
         const int h0 = (int)(it - (long long)t * chunks) * kHeadsPerItem;
         const int nh = min(kHeadsPerItem, hkv - h0);
-        int lo = 0, hi = a.batch;  // sequence of token t: last b with cu_new_lens[b] <= t
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (__ldg(a.cu_new_lens + mid) <= t) lo = mid; else hi = mid;
-        }
-        const int b = lo;
-        const long long pos = (long long)__ldg(a.ctx_before + b) + (t - __ldg(a.cu_new_lens + b));
-        const long long logical = pos >> a.log2_block_size;
-        if (pos < 0 || logical >= a.max_blocks_per_seq) {
-            if (lane == 0) set_error(a.err, kErrDeviceRange);
-            continue;
-        }
-        const int pb = __ldg(a.block_tables + (size_t)b * a.max_blocks_per_seq + logical);
-        if (pb < 0 || pb >= a.num_blocks) {
-            if (lane == 0) set_error(a.err, kErrDeviceRange);
-            continue;
-        }
-        const int off = (int)(pos & (a.block_size - 1));
-        // all of this lane's loads first (one memory round trip per item), then the rows
+        // all of this lane's loads first (one memory round trip per item, overlapping the lookup
+        // of the token's page), then the rows
         constexpr int kPasses = 2 * kHeadsPerItem / kRows;
         uint4 raws[kPasses];
 #pragma unroll
@@ -156,6 +162,8 @@ __global__ void __launch_bounds__(kAppendThreads) append_fp8_kernel(AppendArgs a
                 raws[ps] = ld_stream((kv ? vn : kn) + ((size_t)t * hkv + h) * kLanesPerRow + chk);
             }
         }
+        int pb, off;
+        if (!token_slot(a, t, lane, pb, off)) continue;
 #pragma unroll
         for (int ps = 0; ps < kPasses; ++ps) {
             const int r = ps * kRows + sub;  // row r: K (r < nh) or V of head h0 + r % nh

@@ -11,23 +11,23 @@
 // conversions and cross-lane sums; here one mma.sync m16n8k16 covers 16 tokens x 8 head slots x
 // 16 dims.
 //
-// Kernel structure (persistent, one CTA per SM, 6 warps; 10 for units of 16 query heads):
+// Kernel structure (persistent, one CTA per SM, 6 warps; 10 for units of 16 or 32 query heads):
 //   * units (sequence, KV head, split) are numbered from the context lengths and dealt
 //     round-robin to the CTAs, as in decode.cu;
-//   * warp 4 streams each unit's 64-token tiles with TMA: the page ids of a unit are read one
-//     unit ahead, and each lane issues its page's K and V boxes (64 columns x rows, 128-byte
-//     swizzle, through a 5-D tensor map over the cache), into a ring of as many stages (up to 6)
-//     as the shared memory left by the merge buffers and the unit tables holds; q comes in with
-//     the unit's first tile;
-//   * warps 0-3 each own 16 tokens of a tile (units of 16 query heads: warps 0-7, two per 16 tokens,
-//     each with one 8-head n-tile, so that each dependent chain is half as long and every scheduler
-//     has two of them): ldmatrix from the swizzled tile gives the A fragments
+//   * the producer warp streams each unit's 64-token tiles with TMA: the page ids of a unit are
+//     read one unit ahead, and each lane issues its page slice's boxes (K rows then V rows, 64
+//     columns, 128-byte swizzle, through a 5-D tensor map over the cache; evict-first in L2, since
+//     each line is read once), into a ring of as many stages (up to 6) as the shared memory left
+//     by the merge buffers and the unit tables holds; q comes in with the unit's first tile;
+//   * warps 0-3 each own 16 tokens of a tile (units of 16 or 32 query heads: warps 0-7, two per 16
+//     tokens, each with half the unit's 8-head n-tiles, so that each dependent chain is half as
+//     long and every scheduler has two of them): ldmatrix from the swizzled tile gives the A fragments
 //     of K (row) and of V (transposed); q, held as B fragments for the whole unit, has the group's
 //     heads in the N slots (padding slots are zero); the scores stay in the accumulator fragments:
 //     column max by shuffles, lazy rescale (threshold 2^8), exp2, and P moved into B-fragment
 //     layout with movmatrix; O^T accumulates in registers; at the end of a unit each warp leaves
-//     its rows in a shared-memory merge buffer (two taking turns; one for 16-head units) and goes
-//     on with the next unit;
+//     its rows in a shared-memory merge buffer (two taking turns; one for 16- and 32-head units)
+//     and goes on with the next unit;
 //   * the last warp merges the four token slices' rows and writes the output (single split) or
 //     the split partials.
 #include <cuda.h>
@@ -58,8 +58,8 @@ struct GqaLayout {
     static constexpr uint32_t kQBytes = G * D * 2;
     static constexpr uint32_t kStageBytes = (2 * kKBytes + kQBytes + 1023) / 1024 * 1024;
     static constexpr uint32_t kMergeFloats = kWarps * G * kMergeRow<D>;  // one merge buffer
-    // 16 heads: one merge buffer (the consumers wait for the merge of the previous unit), which
-    // leaves room for a fifth stage; fewer heads: two, taking turns
+    // 16 or 32 heads: one merge buffer (the consumers wait for the merge of the previous unit),
+    // which leaves room for another stage; fewer heads: two, taking turns
     static constexpr int kMergeBufs = G >= 16 ? 1 : 2;
     // barriers: full / empty per stage slot, merge full / empty per merge buffer; then the abort
     // flag (padded to 16 bytes), the unit of each stage slot and the unit of each merge buffer

@@ -116,6 +116,8 @@ __device__ __forceinline__ float2 exp2_fma2(float2 x) {
 }
 
 // Pairs q of a 128-key row with (q % 8) < kEmuPerEight take exp2_fma2, the others MUFU ex2.
+// 0: every exponential on MUFU. Moving a quarter of them to the FMA pipe timed slower on this
+// kernel, whose bound is the hand-off between the MMA thread and the softmax warps, not ex2.
 constexpr int kEmuPerEight = 0;
 
 __device__ __forceinline__ uint32_t pack2(float a, float b, bool bf16) {

@@ -251,8 +251,8 @@ def paged_attn_prefill(cache, q, cu_q_lens, context_lens, block_tables, max_q_le
                        scale: Optional[float] = None, causal: bool = True, out=None, out_dtype=None, lse=None,
                        stream=None, scales=None):
     """A chunk of queries per sequence ([sum q_len, Hq, D]) against its paged context
-    (the chunk's own K/V already appended). Returns `out`. An FP8 cache raises PkvError
-    (PKV_ERR_UNSUPPORTED)."""
+    (the chunk's own K/V already appended). Returns `out`. An FP8 cache (pass `scales`) needs
+    head_dim 128; with head_dim 64 it raises PkvError (PKV_ERR_UNSUPPORTED)."""
     torch = _torch()
     lib = load_library()
     c = _cache_struct(cache, q.dtype, scales)

@@ -1,0 +1,173 @@
+"""GPU parity on seeded random configurations: head_dim, page size, head grouping, dtype, output
+type, split count, context and chunk lengths (0, 1, page multiples and ragged values mixed), for
+the decode, prefill and mixed calls over 16-bit and FP8 caches. Each configuration is drawn from
+its index alone, so a failure names a reproducible case; every output is checked against the
+oracle (prefill: every row of small chunks, else the first, last and 12 seeded rows of each)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_flash_cache_gb300 as pkv
+from paged_kv_flash_cache_gb300 import workloads as W
+from tests.helpers import cache_bits, check_close, device_cache, to_dev
+
+pytestmark = pytest.mark.gpu
+
+BLOCK_SIZES = [8, 16, 32, 64, 128, 256, 512]
+# (Hq, Hkv): MHA, GQA groups 2..32, MQA, and groups taken as several tensor-core units
+GROUPS_DECODE = [(4, 4), (8, 4), (16, 4), (32, 8), (16, 2), (32, 2), (16, 1), (32, 1), (64, 2), (48, 1), (24, 3)]
+GROUPS_FP8_D64 = [(4, 4), (8, 4), (16, 4), (8, 1)]  # the CUDA-core FP8 kernel: groups 1, 2, 4, 8
+GROUPS_PREFILL = [(4, 4), (8, 2), (6, 3), (12, 4), (16, 1), (9, 3)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from paged_kv_flash_cache_gb300 import build
+    build.build()
+    oracle.build()
+    assert torch.cuda.is_available()
+
+
+def draw_lengths(rng, n, hi, bs):
+    out = []
+    for _ in range(n):
+        kind = rng.integers(0, 5)
+        if kind == 0:
+            out.append(int(rng.integers(0, 2)))                     # empty or one token
+        elif kind == 1:
+            out.append(int(bs * rng.integers(1, max(2, hi // bs))))  # a page multiple
+        else:
+            out.append(int(rng.integers(2, hi)))
+    return out
+
+
+def make(rng, *, lens, q_lens, hq, hkv, d, bs, dtype, causal, kv_format, seed):
+    nb = sum((L + bs - 1) // bs for L in lens) + int(rng.integers(0, 9))
+    order = torch.randperm(max(nb, 1), generator=torch.Generator().manual_seed(seed)).tolist()
+    return W.make_problem("rand", batch=len(lens), num_q_heads=hq, num_kv_heads=hkv, head_dim=d, block_size=bs,
+                          context_lens=lens, q_lens=q_lens, dtype=dtype, causal=causal, seed=seed,
+                          num_blocks=max(nb, 1), free_order=order, kv_format=kv_format)
+
+
+def on_device(p):
+    """(cache, scales, oracle's view of the cache) with the context appended by the library."""
+    if p.kv_format == "native":
+        cache = device_cache(p)
+        torch.cuda.synchronize()
+        return cache, None, cache_bits(cache)
+    codes, scales = p.pool_init
+    codes, scales = codes.cuda().contiguous(), scales.cuda().contiguous()
+    if p.k_ctx.shape[0]:
+        pkv.kv_cache_append(codes, to_dev(p.k_ctx), to_dev(p.v_ctx), to_dev(p.cu_ctx_lens),
+                            torch.zeros(p.batch, dtype=torch.int32, device="cuda"), to_dev(p.block_tables),
+                            scales=scales)
+    torch.cuda.synchronize()
+    return codes, scales, oracle.Fp8Cache(codes.cpu().numpy().copy(), scales.cpu().numpy().copy())
+
+
+def compare(p, out, lse, host, roundings, what, rows=None):
+    assert pkv.get_device_error() == 0, what
+    ref, ref_lse = oracle.attention_of(p, host, rows=rows)
+    sel = None if rows is None else torch.as_tensor(rows, device=out.device)
+    got = out if sel is None else out[sel]
+    check_close(got, ref, p.dtype, roundings=roundings, what=what)
+    got_lse = (lse if sel is None else lse[sel]).cpu().numpy()
+    assert np.array_equal(np.isneginf(got_lse), np.isneginf(ref_lse)), what
+    fin = np.isfinite(ref_lse)
+    np.testing.assert_allclose(got_lse[fin], ref_lse[fin], rtol=1e-4, atol=1e-4, err_msg=what)
+
+
+def sample_rows(p, rng, full_below=64):
+    cu = p.cu_q_lens.tolist()
+    rows = []
+    for b in range(p.batch):
+        n = cu[b + 1] - cu[b]
+        if n <= full_below:
+            rows += list(range(cu[b], cu[b + 1]))
+        else:
+            rows += [cu[b], cu[b + 1] - 1] + [cu[b] + int(x) for x in rng.choice(np.arange(1, n - 1), 12, replace=False)]
+    return rows
+
+
+@pytest.mark.parametrize("fmt", ["native", "fp8"])
+@pytest.mark.parametrize("i", range(12))
+def test_random_decode(fmt, i):
+    rng = np.random.default_rng(1000 + i + (500 if fmt == "fp8" else 0))
+    d = int(rng.choice([64, 128]))
+    bs = int(rng.choice(BLOCK_SIZES))
+    groups = GROUPS_FP8_D64 if (fmt == "fp8" and d == 64) else GROUPS_DECODE
+    hq, hkv = groups[int(rng.integers(0, len(groups)))]
+    dtype = W.F16 if rng.integers(0, 2) else W.BF16
+    lens = draw_lengths(rng, int(rng.integers(1, 7)), 2500, bs)
+    splits = int(rng.choice([0, 0, 1, 3, 7]))
+    fp32 = bool(rng.integers(0, 4) == 0)
+    what = "decode %s d=%d bs=%d %d/%d %s splits=%d fp32=%s lens=%s" % (fmt, d, bs, hq, hkv, dtype, splits, fp32, lens)
+    p = make(rng, lens=lens, q_lens=[1] * len(lens), hq=hq, hkv=hkv, d=d, bs=bs, dtype=dtype, causal=False,
+             kv_format=fmt, seed=2000 + i)
+    cache, scales, host = on_device(p)
+    lse = torch.empty((p.batch, hq), dtype=torch.float32, device="cuda")
+    out = pkv.paged_attn_decode(cache, to_dev(p.q), to_dev(p.block_tables), to_dev(p.context_lens), scale=p.scale,
+                                num_splits=splits, out_dtype=torch.float32 if fp32 else None, lse=lse, scales=scales)
+    torch.cuda.synchronize()
+    # roundings to 16 bits: the output unless FP32; P before a tensor-core P.V (groups of 4+ on a
+    # 16-bit cache, head_dim 128 on an FP8 cache)
+    tensor_pv = (hq // hkv >= 4) if fmt == "native" else (d == 128)
+    compare(p, out, lse, host, (0 if fp32 else 1) + (1 if tensor_pv else 0), what)
+
+
+@pytest.mark.parametrize("fmt", ["native", "fp8"])
+@pytest.mark.parametrize("i", range(8))
+def test_random_prefill(fmt, i):
+    rng = np.random.default_rng(3000 + i + (500 if fmt == "fp8" else 0))
+    d = 128 if fmt == "fp8" else int(rng.choice([64, 128]))
+    bs = int(rng.choice(BLOCK_SIZES))
+    hq, hkv = GROUPS_PREFILL[int(rng.integers(0, len(GROUPS_PREFILL)))]
+    dtype = W.F16 if rng.integers(0, 2) else W.BF16
+    n = int(rng.integers(1, 4))
+    lens = [int(rng.integers(1, 1300)) for _ in range(n)]
+    q_lens = [int(min(L, rng.choice([1, L, rng.integers(1, 300)]))) for L in lens]
+    causal = bool(rng.integers(0, 3) > 0)
+    fp32 = bool(rng.integers(0, 4) == 0)
+    what = "prefill %s d=%d bs=%d %d/%d %s causal=%s fp32=%s lens=%s q=%s" % (fmt, d, bs, hq, hkv, dtype, causal,
+                                                                               fp32, lens, q_lens)
+    p = make(rng, lens=lens, q_lens=q_lens, hq=hq, hkv=hkv, d=d, bs=bs, dtype=dtype, causal=causal, kv_format=fmt,
+             seed=4000 + i)
+    cache, scales, host = on_device(p)
+    lse = torch.empty((p.total_q, hq), dtype=torch.float32, device="cuda")
+    out = pkv.paged_attn_prefill(cache, to_dev(p.q), to_dev(p.cu_q_lens), to_dev(p.context_lens),
+                                 to_dev(p.block_tables), max_q_len=max(q_lens), scale=p.scale, causal=causal,
+                                 out_dtype=torch.float32 if fp32 else None, lse=lse, scales=scales)
+    torch.cuda.synchronize()
+    # roundings: output (unless FP32) and P; an FP8 cache adds V = f16(code) * f16(scale) (two)
+    r = (0 if fp32 else 1) + 1 + (2 if fmt == "fp8" else 0)
+    compare(p, out, lse, host, r, what, rows=sample_rows(p, rng))
+
+
+@pytest.mark.parametrize("i", range(6))
+def test_random_mixed(i):
+    rng = np.random.default_rng(5000 + i)
+    fmt = "fp8" if i % 3 == 2 else "native"
+    d = 128 if fmt == "fp8" else int(rng.choice([64, 128]))
+    bs = int(rng.choice(BLOCK_SIZES))
+    hq, hkv = [(8, 8), (8, 4), (16, 4), (32, 1), (16, 2)][int(rng.integers(0, 5))]
+    dtype = W.F16 if rng.integers(0, 2) else W.BF16
+    n = int(rng.integers(2, 8))
+    lens = [int(rng.integers(1, 1500)) for _ in range(n)]
+    q_lens = [int(min(L, rng.choice([1, 1, 0, rng.integers(2, 200)]))) for L in lens]
+    if all(q == 0 for q in q_lens):
+        q_lens[0] = 1
+    splits = int(rng.choice([0, 0, 2, 5]))
+    what = "mixed %s d=%d bs=%d %d/%d %s splits=%d lens=%s q=%s" % (fmt, d, bs, hq, hkv, dtype, splits, lens, q_lens)
+    p = make(rng, lens=lens, q_lens=q_lens, hq=hq, hkv=hkv, d=d, bs=bs, dtype=dtype, causal=True, kv_format=fmt,
+             seed=6000 + i)
+    cache, scales, host = on_device(p)
+    out = torch.full((p.total_q, hq, d), float("nan"), dtype=p.q.dtype, device="cuda")
+    lse = torch.full((p.total_q, hq), float("nan"), dtype=torch.float32, device="cuda")
+    pkv.paged_attn_mixed(cache, to_dev(p.q), to_dev(p.cu_q_lens), to_dev(p.context_lens), to_dev(p.block_tables),
+                         max_q_len=max(q_lens), scale=p.scale, causal=True, num_splits=splits, out=out, lse=lse,
+                         scales=scales)
+    torch.cuda.synchronize()
+    assert not torch.isnan(out).any() and not torch.isnan(lse).any(), what
+    # the chunks' bound (output, P; FP8: and V's two f16 roundings) covers the decode rows too
+    compare(p, out, lse, host, 2 + (2 if fmt == "fp8" else 0), what, rows=sample_rows(p, rng))

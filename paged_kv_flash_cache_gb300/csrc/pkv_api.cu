@@ -207,7 +207,7 @@ pkv_status decode_impl(const pkv_cache &cache, const void *q, int num_q_heads, c
     if (batch < 0 || max_blocks_per_seq <= 0 || num_q_heads <= 0 || num_splits < 0) return PKV_ERR_INVALID_ARG;
     if (num_q_heads % cache.num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
     const int group = num_q_heads / cache.num_kv_heads;
-    // 1, 2, 4, or any multiple of 8 (taken 8 query heads at a time) query heads per KV head
+    // 1, 2, 4, or any multiple of 8 query heads per KV head (wide groups as several units)
     if (group != 1 && group != 2 && group != 4 && group % 8 != 0) return PKV_ERR_UNSUPPORTED;
     if (group > 8 && cache.format == PKV_KV_FP8_E4M3 && cache.head_dim != 128) return PKV_ERR_UNSUPPORTED;
     if (batch > decode_max_batch()) return PKV_ERR_UNSUPPORTED;

@@ -39,8 +39,9 @@ struct DecodeArgs {
     int batch, max_blocks_per_seq;
     float scale;
     int chunk;   // tokens per split (multiple of the decode tile)
-    // Units per KV head when a KV head serves more query heads than one unit holds (16 for the
-    // native group kernel when the group is a multiple of 16, else 8; MQA, wide groups), else 1:
+    // Units per KV head when a KV head serves more query heads than one unit holds (the native
+    // group kernel holds 32 (head_dim 128), 16 or 8, the largest that divides the group; the FP8
+    // kernel 8; MQA, wide groups), else 1:
     // unit head v reads KV head v / head_groups and serves query heads n*v .. n*v + n-1.
     int head_groups;
     // Mixed batch (prefill chunks and decode rows in one call): cu_q_lens [batch + 1] of the call's

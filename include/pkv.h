@@ -221,7 +221,8 @@ PKV_API pkv_status pkv_attn_combine(const float *partial_o, const float *partial
  *     rejected with PKV_ERR_WORKSPACE before anything is launched.
  *   - The first call on each device (that device current) looks up the array's device
  *     address with cudaGetSymbolAddress; make that first call before any stream
- *     capture.
+ *     capture.  A lookup that fails returns PKV_ERR_CUDA and is not remembered: the
+ *     next call looks again.
  *   - All calls share the one array, which keeps the last call's contents.  Nothing
  *     in it has to start at zero: each call writes every partial it later reads.
  *     Calls that overlap on the GPU (concurrent streams, or several host threads)

@@ -657,14 +657,14 @@ cudaError_t launch_decode_t(const DecodeArgs &a, int grid, cudaStream_t s) {
     const size_t smem = DecodeLayout<D, G, FP8>::smem_bytes(a.batch, a.s_max);
     auto kern = decode_split_kernel<Tag, D, G, FP8>;
     // opt in to the largest size this kernel can ask for, once per device
-    static unsigned int configured = 0;
+    static DeviceFlags configured;
     const int dev = device_info().device;
-    if (dev < 32 && !(configured & (1u << dev))) {
+    if (dev < 64 && !configured.test(dev)) {
         const int max_smem = (int)DecodeLayout<D, G, FP8>::smem_bytes(kMaxBatch, kDecodeMaxSplits);
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
         if (e != cudaSuccess) return e;
-        configured |= 1u << dev;
-    } else if (dev >= 32) {
+        configured.set(dev);
+    } else if (dev >= 64) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }

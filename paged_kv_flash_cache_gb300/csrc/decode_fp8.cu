@@ -360,9 +360,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int ofs = 4; ofs < 32; ofs <<= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, ofs));
             const float rw = wmax > 0.f ? 1.f / wmax : 0.f;
             const float r0 = w0 * rw, r1 = w1 * rw;
-            // P^T (tokens x head slots) in accumulator layout -> P as B fragments (k = tokens)
-            const uint32_t pb0 = movmatrix_t(pack_pair<false>(p0 * r0, p1 * r0));
-            const uint32_t pb1 = movmatrix_t(pack_pair<false>(p2 * r1, p3 * r1));
+            // P^T (tokens x head slots) in accumulator layout -> P as B fragments (k = tokens), as
+            // an f16 part and its f16 remainder, each its own MMA into the same FP32 accumulator:
+            // P.V sees P almost unrounded, so the output's is the only 16-bit rounding on the path
+            uint32_t h01, e01, h23, e23;
+            split_pair<false>(p0 * r0, p1 * r0, h01, e01);
+            split_pair<false>(p2 * r1, p3 * r1, h23, e23);
+            const uint32_t pb0 = movmatrix_t(h01), pb1 = movmatrix_t(h23);
+            const uint32_t pe0 = movmatrix_t(e01), pe1 = movmatrix_t(e23);
             // ---- O^T += w_max V_w^T P^T: 128 dims (permuted within each 16-dim chunk) x 8 slots ----
             float ot[kChunks][4];
 #pragma unroll
@@ -382,6 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t hi = __byte_perm(r[2 * h + 1], 0, 0x3120);
                         const uint32_t af[4] = {e4m3x2_to_f16x2(lo), e4m3x2_to_f16x2(lo >> 16), e4m3x2_to_f16x2(hi),
                                                 e4m3x2_to_f16x2(hi >> 16)};
+                        mma16816<false>(ot[cp + h], af, pe0, pe1);
                         mma16816<false>(ot[cp + h], af, pb0, pb1);
                     }
                 }
@@ -445,13 +451,13 @@ cudaError_t launch_fp8_t(const DecodeArgs &a, int grid, cudaStream_t s) {
     cudaError_t e = encode_fp8_maps(a.cache, box_rows, &tm, &tm_s);
     if (e != cudaSuccess) return e;
     auto kern = decode_fp8_kernel<G, BF16>;
-    static bool configured[64] = {};
+    static DeviceFlags configured;
     const int dev = device_info().device;
-    if (dev >= 64 || !configured[dev]) {
+    if (!configured.test(dev)) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)Fp8Layout<G>::smem_bytes(kMaxBatch8, kDecodeMaxSplits));
         if (e != cudaSuccess) return e;
-        if (dev < 64) configured[dev] = true;
+        configured.set(dev);
     }
     return launch_pdl(kern, dim3(grid), dim3(kThreads), Fp8Layout<G>::smem_bytes(a.batch, a.s_max), s, tm, tm_s, a);
 }

@@ -24,8 +24,9 @@
 //     long and every scheduler has two of them): ldmatrix from the swizzled tile gives the A fragments
 //     of K (row) and of V (transposed); q, held as B fragments for the whole unit, has the group's
 //     heads in the N slots (padding slots are zero); the scores stay in the accumulator fragments:
-//     column max by shuffles, lazy rescale (threshold 2^8), exp2, and P moved into B-fragment
-//     layout with movmatrix; O^T accumulates in registers; at the end of a unit each warp leaves
+//     column max by shuffles, lazy rescale (threshold 2^8), exp2, and P, as a part rounded to the
+//     input type plus its rounded remainder, moved into B-fragment layout with movmatrix; O^T
+//     accumulates both parts' products in FP32 registers; at the end of a unit each warp leaves
 //     its rows in a shared-memory merge buffer (two taking turns; one for 16- and 32-head units)
 //     and goes on with the next unit;
 //   * the last warp merges the four token slices' rows and writes the output (single split) or
@@ -311,7 +312,7 @@ __global__ void __launch_bounds__(GqaWarps<G>::kThreads, 1)
                 }
             }
             const bool v0 = t0w + gid < n, v1 = t0w + gid + 8 < n;
-            uint32_t pb[NT][2];
+            uint32_t pb[NT][2], pr[NT][2];  // P in the input type, and its remainders
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 s[nt][0] = v0 ? s[nt][0] : -INFINITY;
@@ -354,9 +355,17 @@ __global__ void __launch_bounds__(GqaWarps<G>::kThreads, 1)
                 const float p3 = v1 ? ex2f(fmaf(s[nt][3], sl, -m[nt][1])) : 0.f;
                 l[nt][0] += p0 + p2;
                 l[nt][1] += p1 + p3;
-                // P^T (tokens x head slots) in accumulator layout -> P as B fragments (k = tokens)
-                pb[nt][0] = movmatrix_t(pack_pair<BF16>(p0, p1));
-                pb[nt][1] = movmatrix_t(pack_pair<BF16>(p2, p3));
+                // P^T (tokens x head slots) in accumulator layout -> P as B fragments (k = tokens).
+                // P goes in as a rounded part and a remainder, each its own MMA into the same FP32
+                // accumulator, so P.V sees P almost unrounded: the only rounding to the input type
+                // on the decode path stays the output's
+                uint32_t h01, r01, h23, r23;
+                split_pair<BF16>(p0, p1, h01, r01);
+                split_pair<BF16>(p2, p3, h23, r23);
+                pb[nt][0] = movmatrix_t(h01);
+                pb[nt][1] = movmatrix_t(h23);
+                pr[nt][0] = movmatrix_t(r01);
+                pr[nt][1] = movmatrix_t(r23);
             }
             // ---- O^T += V_w^T P^T: D x 8 head slots per n-tile (one V fragment for all) ----
             {
@@ -369,7 +378,10 @@ __global__ void __launch_bounds__(GqaWarps<G>::kThreads, 1)
                     const int cc = 2 * (mt & 3) + (mi & 1);
                     ldsm_x4_t(swz(aV + (mt >> 2) * L::kHalfRegion, tp, cc), af);
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) mma16816<BF16>(o[mt][nt], af, pb[nt][0], pb[nt][1]);
+                    for (int nt = 0; nt < NT; ++nt) {
+                        mma16816<BF16>(o[mt][nt], af, pr[nt][0], pr[nt][1]);
+                        mma16816<BF16>(o[mt][nt], af, pb[nt][0], pb[nt][1]);
+                    }
                 }
             }
             __syncwarp();
@@ -437,11 +449,11 @@ cudaError_t launch_gqa_t(const DecodeArgs &a, int grid, cudaStream_t s) {
     args.stages = L::stages_for(a.batch, a.s_max, (size_t)info.max_smem);
     if (args.stages == 0) return cudaErrorInvalidValue;  // tables of this batch and split count do not fit
     auto kern = decode_gqa_kernel<D, G, BF16>;
-    static bool configured[64] = {};
-    if (info.device >= 64 || !configured[info.device]) {
+    static DeviceFlags configured;
+    if (!configured.test(info.device)) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, info.max_smem);
         if (e != cudaSuccess) return e;
-        if (info.device < 64) configured[info.device] = true;
+        configured.set(info.device);
     }
     return launch_pdl(kern, dim3(grid), dim3(GqaWarps<G>::kThreads), L::smem_bytes(a.batch, a.s_max, args.stages), s,
                       tm, args);

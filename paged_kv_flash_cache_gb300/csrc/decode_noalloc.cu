@@ -12,10 +12,12 @@
 // library reserves it (once its module is loaded) until the process exits. Host code cannot
 // use the array's name as a device address -- on the host that name is only a stand-in -- so on
 // the first call on each device (with that device current) cudaGetSymbolAddress fetches the
-// real address, which is cached per device and passed to the kernels. The rest is the regular
-// decode path (pkv_paged_attn_decode) unchanged, with this array as its workspace.
+// real address, which is kept per device once the lookup succeeds and passed to the kernels.
+// The rest is the regular decode path (pkv_paged_attn_decode) unchanged, with this array as its
+// workspace.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "pkv_internal.h"
@@ -25,31 +27,35 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_decode_scratch[PKV_DECODE_NOALLOC_SCRATCH_BYTES];
 
-struct ScratchSlot {
-    bool ready = false;
-    cudaError_t status = cudaSuccess;
-    void *ptr = nullptr;
-};
+// The array's device address on each device, once looked up (nullptr: not yet). Only a
+// successful lookup is kept; a failed one (made during a stream capture, say) is retried by the
+// next call.
 constexpr int kMaxDevices = 64;
-ScratchSlot g_scratch[kMaxDevices];
+std::atomic<void *> g_scratch[kMaxDevices];
 std::mutex g_scratch_lock;
 
-// Device address of g_decode_scratch on the current device (looked up once per device).
+// Device address of g_decode_scratch on the current device.
 cudaError_t scratch_address(void **out) {
+    *out = nullptr;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> g(g_scratch_lock);
-    ScratchSlot &s = g_scratch[dev];
-    if (!s.ready) {
-        void *p = nullptr;
-        s.status = cudaGetSymbolAddress(&p, g_decode_scratch);
-        s.ptr = (s.status == cudaSuccess) ? p : nullptr;
-        s.ready = true;
+    void *p = g_scratch[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+        std::lock_guard<std::mutex> g(g_scratch_lock);
+        p = g_scratch[dev].load(std::memory_order_relaxed);
+        if (p == nullptr) {
+            e = cudaGetSymbolAddress(&p, g_decode_scratch);
+            if (e != cudaSuccess || p == nullptr) {
+                (void)cudaGetLastError();  // leave no error behind for the caller's next check
+                return e != cudaSuccess ? e : cudaErrorInvalidSymbol;
+            }
+            g_scratch[dev].store(p, std::memory_order_release);
+        }
     }
-    *out = s.ptr;
-    return s.status;
+    *out = p;
+    return cudaSuccess;
 }
 
 }  // namespace

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "pkv_internal.h"
@@ -15,8 +16,11 @@ __device__ int g_device_error;
 
 namespace {
 
+// Per-device launch facts and the address of the device error word, filled once per device by
+// the first call that finds the device usable. `ready` is stored with release order after the
+// fields and loaded with acquire order, so a thread that sees it set also sees the fields.
 struct DeviceSlot {
-    bool ready = false;
+    std::atomic<bool> ready{false};
     DeviceInfo info{};
     int *err_ptr = nullptr;
 };
@@ -35,29 +39,39 @@ int ilog2(int x) {
     return r;
 }
 
-DeviceSlot &slot() {
+// The current device's slot, or nullptr when the device, its attributes or the address of its
+// error word cannot be read. A failure is not cached: the next call tries again.
+DeviceSlot *slot() {
     int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= kMaxDevices) dev = 0;
-    DeviceSlot &s = g_slots[dev];
-    if (!s.ready) {
-        std::lock_guard<std::mutex> g(g_slot_lock);
-        if (!s.ready) {
-            s.info.device = dev;
-            int sms = 0;
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-            s.info.num_sms = sms > 0 ? sms : 1;
-            s.info.decode_ctas_per_sm = 1;
-            int smem = 0;
-            cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-            s.info.max_smem = smem > 0 ? smem : 48 * 1024;
-            void *p = nullptr;
-            if (cudaGetSymbolAddress(&p, g_device_error) == cudaSuccess) s.err_ptr = static_cast<int *>(p);
-            s.ready = true;
-        }
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        (void)cudaGetLastError();
+        return nullptr;
     }
-    return s;
+    DeviceSlot &s = g_slots[dev];
+    if (s.ready.load(std::memory_order_acquire)) return &s;
+    std::lock_guard<std::mutex> g(g_slot_lock);
+    if (!s.ready.load(std::memory_order_relaxed)) {
+        int sms = 0, smem = 0;
+        void *p = nullptr;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+            cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess || p == nullptr || sms <= 0 || smem <= 0) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
+        s.info.device = dev;
+        s.info.num_sms = sms;
+        s.info.decode_ctas_per_sm = 1;
+        s.info.max_smem = smem;
+        s.err_ptr = static_cast<int *>(p);
+        s.ready.store(true, std::memory_order_release);
+    }
+    return &s;
 }
+
+// Launch facts of a device that could not be queried: used only to size workspaces before any
+// device is usable (the smallest split chunk, so the size is never too small).
+const DeviceInfo kNoDevice = {-1, 1, 1, 48 * 1024};
 
 pkv_status check_cache(const pkv_cache &c) {
     if (!c.ptr || !aligned16(c.ptr)) return PKV_ERR_INVALID_ARG;
@@ -100,7 +114,8 @@ int split_tokens(int batch, int num_kv_heads, int block_size, int max_blocks_per
     if (num_splits > 0) {
         c = (cap + num_splits - 1) / num_splits;
     } else {
-        const DeviceInfo &d = slot().info;
+        const DeviceSlot *s = slot();
+        const DeviceInfo &d = s ? s->info : kNoDevice;
         const long long ctas = (long long)d.num_sms * d.decode_ctas_per_sm;
         const long long want = (long long)batch * num_kv_heads * cap / (ctas * 8 > 0 ? ctas * 8 : 1);
         c = 512;
@@ -114,8 +129,14 @@ int split_tokens(int batch, int num_kv_heads, int block_size, int max_blocks_per
 
 }  // namespace
 
-const DeviceInfo &device_info() { return slot().info; }
-int *device_error_word() { return slot().err_ptr; }
+const DeviceInfo &device_info() {
+    const DeviceSlot *s = slot();
+    return s ? s->info : kNoDevice;
+}
+int *device_error_word() {
+    DeviceSlot *s = slot();
+    return s ? s->err_ptr : nullptr;
+}
 
 }  // namespace pkv
 
@@ -147,7 +168,8 @@ pkv_status pkv_kv_cache_append(pkv_cache cache, const void *k_new, const void *v
     if (batch == 0 || num_new_tokens == 0) return PKV_OK;
     if (!k_new || !v_new || !cu_new_lens || !ctx_before || !block_tables) return PKV_ERR_INVALID_ARG;
     if (!aligned16(k_new) || !aligned16(v_new)) return PKV_ERR_INVALID_ARG;
-    DeviceSlot &s = slot();
+    DeviceSlot *s = slot();
+    if (!s) return PKV_ERR_CUDA;
     AppendArgs a;
     a.cache = cache.ptr;
     a.num_blocks = cache.num_blocks;
@@ -166,7 +188,7 @@ pkv_status pkv_kv_cache_append(pkv_cache cache, const void *k_new, const void *v
     a.batch = batch;
     a.max_blocks_per_seq = max_blocks_per_seq;
     a.num_new_tokens = num_new_tokens;
-    a.err = s.err_ptr;
+    a.err = s->err_ptr;
     return launch_append(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
@@ -216,7 +238,8 @@ pkv_status decode_impl(const pkv_cache &cache, const void *q, int num_q_heads, c
     if (!aligned16(q) || !aligned16(out) || (lse && !aligned16(lse))) return PKV_ERR_INVALID_ARG;
     const long long cap = (long long)max_blocks_per_seq * cache.block_size;
     if (cap > (1ll << 30)) return PKV_ERR_UNSUPPORTED;
-    DeviceSlot &s = slot();
+    DeviceSlot *s = slot();
+    if (!s) return PKV_ERR_CUDA;
     const int chunk = split_tokens(batch, cache.num_kv_heads, cache.block_size, max_blocks_per_seq, num_splits);
     const int s_max = (int)((cap + chunk - 1) / chunk);
     const size_t need = pkv_decode_workspace_size(batch, num_q_heads, cache.num_kv_heads, cache.head_dim,
@@ -246,9 +269,9 @@ pkv_status decode_impl(const pkv_cache &cache, const void *q, int num_q_heads, c
     a.out = out;
     a.out_dtype = (int)out_dtype;
     a.lse = lse;
-    a.err = s.err_ptr;
+    a.err = s->err_ptr;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    const int grid = s.info.num_sms * s.info.decode_ctas_per_sm;
+    const int grid = s->info.num_sms * s->info.decode_ctas_per_sm;
     // tensor cores: four or more query heads per KV head of a native cache (the group kernel),
     // and every grouping of an FP8 cache with head_dim 128; CUDA cores for the rest
     cudaError_t le;
@@ -294,7 +317,7 @@ pkv_status pkv_attn_combine(const float *partial_o, const float *partial_lse, in
     if (n_rows == 0) return PKV_OK;
     if (!partial_o || !partial_lse || !out) return PKV_ERR_INVALID_ARG;
     if (!aligned16(partial_o) || !aligned16(out)) return PKV_ERR_INVALID_ARG;
-    slot();
+    if (!slot()) return PKV_ERR_CUDA;
     CombineArgs c;
     c.part_o = partial_o;
     c.part_lse = partial_lse;
@@ -335,7 +358,8 @@ pkv_status prefill_impl(const pkv_cache &cache, const void *q, int num_q_heads, 
     if (cap > (1ll << 30)) return PKV_ERR_UNSUPPORTED;
     // grid (heads, sequences, 256-row blocks): the last two dimensions hold at most 65535
     if (batch > 65535 || (max_q_len + 255) / 256 > 65535) return PKV_ERR_UNSUPPORTED;
-    DeviceSlot &s = slot();
+    DeviceSlot *s = slot();
+    if (!s) return PKV_ERR_CUDA;
     PrefillArgs a;
     a.cache = view_of(cache);
     a.q = q;
@@ -353,7 +377,7 @@ pkv_status prefill_impl(const pkv_cache &cache, const void *q, int num_q_heads, 
     a.out = out;
     a.out_dtype = (int)out_dtype;
     a.lse = lse;
-    a.err = s.err_ptr;
+    a.err = s->err_ptr;
     cudaError_t e = launch_prefill(a, static_cast<cudaStream_t>(stream));
     if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
@@ -391,13 +415,13 @@ pkv_status pkv_get_device_error(void *stream, int *code) {
     if (!code) return PKV_ERR_INVALID_ARG;
     *code = PKV_OK;
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return PKV_ERR_CUDA;
-    DeviceSlot &s = slot();
-    if (!s.err_ptr) return PKV_ERR_CUDA;
+    DeviceSlot *s = slot();
+    if (!s) return PKV_ERR_CUDA;
     int v = 0;
-    if (cudaMemcpy(&v, s.err_ptr, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return PKV_ERR_CUDA;
+    if (cudaMemcpy(&v, s->err_ptr, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return PKV_ERR_CUDA;
     if (v != 0) {
         const int zero = 0;
-        if (cudaMemcpy(s.err_ptr, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return PKV_ERR_CUDA;
+        if (cudaMemcpy(s->err_ptr, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return PKV_ERR_CUDA;
     }
     *code = v;
     return PKV_OK;

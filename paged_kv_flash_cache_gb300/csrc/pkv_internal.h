@@ -2,6 +2,7 @@
 // and the kernel translation units.  Arguments arrive here already validated.
 #pragma once
 
+#include <atomic>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -114,6 +115,19 @@ struct DeviceInfo {
     int max_smem;  // dynamic shared memory a CTA may opt in to (bytes)
 };
 const DeviceInfo &device_info();
+
+// Once-per-device flags (devices 0..63) for a launcher's one-time cudaFuncSetAttribute opt-in.
+// Setting the attribute twice is harmless, so threads that race on a first launch may both set
+// it; the flags are atomic so that the race is not a data race.
+struct DeviceFlags {
+    std::atomic<unsigned long long> bits{0};
+    bool test(int dev) const {
+        return dev >= 0 && dev < 64 && ((bits.load(std::memory_order_acquire) >> dev) & 1ull) != 0;
+    }
+    void set(int dev) {
+        if (dev >= 0 && dev < 64) bits.fetch_or(1ull << dev, std::memory_order_release);
+    }
+};
 int *device_error_word();  // the current device's sticky error word (device address)
 
 constexpr int kDecodeTile = 64;         // tokens per decode pipeline stage

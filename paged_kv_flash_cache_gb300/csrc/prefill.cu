@@ -756,12 +756,12 @@ cudaError_t launch_t(const PrefillArgs &a, cudaStream_t stream) {
     p.lse = a.lse;
     p.err = a.err;
     auto kern = prefill_kernel<D, BF16, FP8>;
-    static bool configured[64] = {};
+    static DeviceFlags configured;
     const int dev = device_info().device;
-    if (dev >= 64 || !configured[dev]) {
+    if (!configured.test(dev)) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Lay::kSmemBytes);
         if (e != cudaSuccess) return e;
-        if (dev < 64) configured[dev] = true;
+        configured.set(dev);
     }
     dim3 grid(a.num_q_heads, a.batch, (a.max_q_len + kRows - 1) / kRows);
     return launch_pdl(kern, grid, dim3(kThreads), Lay::kSmemBytes, stream, tm_q, tm_kv, p);

@@ -313,16 +313,19 @@ def decode_7b(seed: int = 1236, batch: int = 16, lo: int = 1024, hi: int = 8192,
 
 
 def prefill_long(seed: int = 1237, batch: int = 4, seq: int = 8192, chunk: int = 512, heads: int = 32,
-                 head_dim: int = 128, block_size: int = 16, dtype: str = BF16, device="cpu") -> PagedProblem:
+                 head_dim: int = 128, block_size: int = 16, dtype: str = BF16, device="cpu",
+                 kv_format: str = "native") -> PagedProblem:
     """Long causal prefill: `batch` sequences of `seq` tokens in bf16, pages of 16 tokens
     spread by a seeded permutation over a pool of exactly the pages needed. The whole
-    sequence is described once; `prefill_chunks` cuts it into `chunk`-token query calls."""
+    sequence is described once; `prefill_chunks` cuts it into `chunk`-token query calls
+    (kv_format "fp8": the same tokens into an FP8 cache)."""
     gen = torch.Generator().manual_seed(seed)
     pages = batch * ((seq + block_size - 1) // block_size)
     order = torch.randperm(pages, generator=gen).tolist()
     p = make_problem("prefill_long", batch=batch, num_q_heads=heads, num_kv_heads=heads, head_dim=head_dim,
                      block_size=block_size, context_lens=[seq] * batch, q_lens=[seq] * batch, dtype=dtype,
-                     causal=True, seed=seed + 1, num_blocks=pages, free_order=order, pool_init="none", device=device)
+                     causal=True, seed=seed + 1, num_blocks=pages, free_order=order, pool_init="none", device=device,
+                     kv_format=kv_format)
     p.meta["chunk"] = chunk
     return p
 

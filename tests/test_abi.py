@@ -120,3 +120,57 @@ def test_workspace_sizing_with_explicit_splits(lib):
     assert pkv.decode_workspace_size(16, 32, 32, 128, 16, 512, num_splits=4) == 16 * 32 * 4 * 129 * 4
     # split size is rounded up to the 64-token tile
     assert pkv.decode_split_tokens(1, 8, 8, 64, 16, 10, num_splits=3) == 64
+
+
+def test_device_slot_from_eight_threads(lib):
+    """The per-device state behind every entry point is set up by whichever call comes first;
+    eight threads calling at once (ctypes releases the GIL during each call) must all see the
+    same answers. Only calls that launch nothing are made while a device could be visible."""
+    import threading
+
+    import torch
+
+    n_threads, n_calls = 8, 300
+    start = threading.Barrier(n_threads)
+    results = [None] * n_threads
+
+    def worker(i):
+        code = ctypes.c_int(-1)
+        start.wait()
+        seen = set()
+        for _ in range(n_calls):
+            seen.add(("ws", lib.pkv_decode_workspace_size(16, 32, 8, 128, 16, 512, 0)))
+            seen.add(("split", lib.pkv_decode_split_tokens(16, 32, 8, 128, 16, 512, 0)))
+            seen.add(("err", lib.pkv_get_device_error(None, ctypes.byref(code)), code.value))
+        results[i] = seen
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(n_threads)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert all(r == results[0] for r in results), results
+    assert len(results[0]) == 3, results[0]   # one answer per call kind, the same in every thread
+    err = [x for x in results[0] if x[0] == "err"][0]
+    if torch.cuda.is_available() or err[1] != 4:
+        return
+    # no usable device: entry points that would launch must fail with PKV_ERR_CUDA after their
+    # argument checks, from every thread, and never cache the failed device lookup
+    P, F = ctypes.c_void_p, ctypes.c_float
+    good = P(4096)
+    codes = [None] * n_threads
+
+    def launcher(i):
+        start.wait()
+        codes[i] = {(lib.pkv_kv_cache_append(_cache(), good, good, good, good, good, 1, 4, 3, None),
+                     lib.pkv_attn_combine(good, good, 4, 2, 128, good, 2, None, None),
+                     lib.pkv_paged_attn_prefill(_cache(), good, 2, good, good, good, 1, 4, 8, 8, F(0.1), 1, good, 0,
+                                                None, None))
+                    for _ in range(50)}
+
+    threads = [threading.Thread(target=launcher, args=(i,)) for i in range(n_threads)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert all(c == {(4, 4, 4)} for c in codes), codes

@@ -37,4 +37,4 @@ def test_bounded_wait_reports_timeout_and_the_context_stays_usable():
     torch.cuda.synchronize()
     assert pkv.get_device_error() == 0
     ref, _ = oracle.attention_of(p, cache_bits(cache))
-    check_close(out, ref, W.BF16, roundings=2, what="decode after a timeout")
+    check_close(out, ref, W.BF16, roundings=1, what="decode after a timeout")

@@ -43,9 +43,10 @@ def device_fp8(p):
 
 
 def roundings(p, fp32_out=False):
-    """Roundings to 16 bits on the path: the output (unless FP32) and, on the tensor-core path
-    (head_dim 128), the probabilities P in f16 before the P.V product."""
-    return (0 if fp32_out else 1) + (1 if p.head_dim == 128 else 0)
+    """Roundings to 16 bits on the decode path: the output, unless FP32. The tensor-core path
+    (head_dim 128) takes P into the P.V product as an f16 part plus its f16 remainder, and the
+    CUDA-core path (head_dim 64) keeps P in FP32."""
+    return 0 if fp32_out else 1
 
 
 def host(codes, scales):

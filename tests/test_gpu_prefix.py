@@ -57,8 +57,7 @@ def test_prefix_decode_and_a_decode_step(heads, kv_heads, dtype):
     torch.cuda.synchronize()
     assert pkv.get_device_error() == 0
     ref, ref_lse = oracle.attention_of(p, before)
-    roundings = 1 + (1 if heads // kv_heads >= 4 else 0)
-    check_close(out, ref, dtype, roundings=roundings, what="prefix decode")
+    check_close(out, ref, dtype, roundings=1, what="prefix decode")
     np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-5, atol=1e-5)
     # one decode step's new tokens land in private pages only
     step = W.append_step(p, seed=3)

@@ -110,10 +110,9 @@ def test_random_decode(fmt, i):
     out = pkv.paged_attn_decode(cache, to_dev(p.q), to_dev(p.block_tables), to_dev(p.context_lens), scale=p.scale,
                                 num_splits=splits, out_dtype=torch.float32 if fp32 else None, lse=lse, scales=scales)
     torch.cuda.synchronize()
-    # roundings to 16 bits: the output unless FP32; P before a tensor-core P.V (groups of 4+ on a
-    # 16-bit cache, head_dim 128 on an FP8 cache)
-    tensor_pv = (hq // hkv >= 4) if fmt == "native" else (d == 128)
-    compare(p, out, lse, host, (0 if fp32 else 1) + (1 if tensor_pv else 0), what)
+    # roundings to 16 bits on the decode path: the output, unless FP32 (tensor-core P.V takes P as
+    # a rounded part plus its remainder)
+    compare(p, out, lse, host, 0 if fp32 else 1, what)
 
 
 @pytest.mark.parametrize("fmt", ["native", "fp8"])
@@ -169,5 +168,13 @@ def test_random_mixed(i):
                          scales=scales)
     torch.cuda.synchronize()
     assert not torch.isnan(out).any() and not torch.isnan(lse).any(), what
-    # the chunks' bound (output, P; FP8: and V's two f16 roundings) covers the decode rows too
-    compare(p, out, lse, host, 2 + (2 if fmt == "fp8" else 0), what, rows=sample_rows(p, rng))
+    # decode rows at the decode bound (the output); chunk rows at the prefill bound (output, P;
+    # FP8: and V's two f16 roundings)
+    rows = sample_rows(p, rng)
+    single = {p.cu_q_lens[b].item() for b in range(p.batch) if p.q_lens[b].item() == 1}
+    dec = [r for r in rows if r in single]
+    chunk = [r for r in rows if r not in single]
+    if dec:
+        compare(p, out, lse, host, 1, what + " (decode rows)", rows=dec)
+    if chunk:
+        compare(p, out, lse, host, 2 + (2 if fmt == "fp8" else 0), what + " (chunk rows)", rows=chunk)

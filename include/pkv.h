@@ -91,9 +91,9 @@ typedef enum { PKV_KV_NATIVE = 0, PKV_KV_FP8_E4M3 = 1 } pkv_kv_format;
  * [num_blocks, 2, num_kv_heads, block_size], 16-byte aligned; NULL for a native
  * cache).  An FP8 cache is supported by append, decode and (head_dim 128) prefill;
  * prefill over an FP8 cache with head_dim 64 returns PKV_ERR_UNSUPPORTED.  Over an
- * FP8 cache with head_dim 128 the tensor-core products run in f16: q (and, in
- * prefill, each V element times its scale) must lie within f16's range
- * (|x| < 65504; magnitudes below 2^-24 count as 0). */
+ * FP8 cache with head_dim 128 the tensor-core products run in f16 on the exact
+ * codes (the row scales are applied in FP32): q must lie within f16's range
+ * (|q| < 65504; magnitudes below 2^-24 count as 0). */
 typedef struct {
     void *ptr;
     int num_blocks;

@@ -11,8 +11,10 @@
 //
 // CTA = one query head x 256 query rows of one sequence, as two 128-row tiles A and B that share
 // every K/V tile (384 threads, three warpgroups). Over an FP8 cache (head_dim 128) warps 2-3
-// convert each K/V tile in place from E4M3 codes to f16 (V times its row scale), the products run
-// in f16 and the softmax multiplies each score column by its K row scale; otherwise as below:
+// convert each K/V tile in place from E4M3 codes to f16, exactly; the products run in f16; the
+// softmax multiplies each score column by its K row scale and each P column by its V row scale
+// over W (a power of two the converter keeps at or above every V scale so far; O carries the
+// factor W); otherwise as below:
 //   warp 0     TMA producer: both Q tiles once (3-D tensor map over [total_q, Hq, D]); then for
 //              each 128-key tile j the K tile and the V tile, each into one slot of a 4-slot ring:
 //              the pages a tile covers are looked up in the block table by the warp's lanes and each
@@ -129,6 +131,22 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, bool bf16) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// Four E4M3 codes (one 32-bit word, lowest byte first) to two f16x2 words, exactly.
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+}
+
+// Smallest power of two >= x, for finite x >= 0 (0 for 0; 2^-126 for subnormal x).
+__device__ __forceinline__ float pow2_ceil(float x) {
+    uint32_t b = __float_as_uint(x);
+    if (b == 0u) return 0.f;
+    if (b & 0x7fffffu) b = (b & 0x7f800000u) + 0x800000u;
+    return __uint_as_float(b);
+}
+
 // BF16: type of q and the default output. FP8: the cache holds E4M3 codes with one FP32 scale per
 // row; the tensor-core products then run in f16 (MMA below), which holds every code exactly.
 template <int D, bool BF16, bool FP8>
@@ -155,6 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *kv_code = bars + 20;       // [kRing] FP8: codes and scales of a ring item have landed
     uint64_t *q_ready = bars + 24;       // FP8: Q converted to f16 (or left as it is for f16 q)
     const float *sScale = reinterpret_cast<const float *>(smem + Lay::kScaleOff);  // FP8: [kRing][128]
+    float *sW = reinterpret_cast<float *>(bars + 25);  // FP8: [kRing] W of each V item (see the converter)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // grid (heads, batch, row blocks) with the row blocks last-first: CTAs start in linear order, so
@@ -280,10 +299,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (FP8 && warp >= 2) {
             // ================================ FP8 converter warps ================================
             // In place, per ring item: the codes of row r (upper half of the slot) become the f16 row
-            // of the layout TMA writes for a 16-bit cache (two 64-column halves, 128-byte swizzle):
-            // K exactly, V as f16(code) * f16(row scale) in f16. 8 lanes per row, 4 rows per pass:
-            // a row is read entirely before any of it is written. V rows beyond the context are zeroed.
-            const int cw = warp - 2, c = lane & 7;
+            // of the layout TMA writes for a 16-bit cache (two 64-column halves, 128-byte swizzle),
+            // exactly, K and V alike; V rows beyond the context are zeroed. Warp 2 (rows 0-63) and
+            // warp 3 (rows 64-127) take 8 consecutive rows per pass: lane -> rows rr and rr + 4 of the
+            // group (rr = lane / 8), 16-code chunk c = lane % 8, so every swizzled address is a lane
+            // constant plus 1 KB per pass. A row is read entirely before any of it is written (its
+            // codes sit where its second f16 half goes).
+            // Warp 2 also turns each V item's row scales w into r = w / W in place, W a power of two
+            // at or above every V scale seen so far in this CTA (kept in sW[slot]): the softmax
+            // folds r into P, and O carries the factor W (rescaled exactly when W grows).
+            const int cw = warp - 2, c = lane & 7, rr = lane >> 3;
             bool cok = mbar_wait(q_full, 0, abort_flag, p.err);
             if (BF16 && cok) {
                 // q to f16 in place (exact for |q| within f16's range)
@@ -300,51 +325,66 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
             if (lane == 0 && cok) mbar_arrive(q_ready);
+            // lane-constant byte offsets within an 8-row group: code chunk c of rows rr and rr + 4,
+            // and the two f16 chunks (half hf, chunks k0 and k0 + 1) each row's 16 codes become. The
+            // lanes of the two halves store opposite chunks first: the 8 stores of a row in one
+            // instruction then fill all 32 banks once.
+            const int hf = c >> 2, k0 = 2 * (c & 3);
+            const int ka = hf ? k0 + 1 : k0, kb = hf ? k0 : k0 + 1;
+            uint32_t ld[2], sta[2], stb[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int rw = rr + 4 * i;  // == row & 7
+                ld[i] = Lay::kCodeOff + rw * 128u + ((c ^ rw) << 4);
+                sta[i] = hf * Lay::kTileHalf + rw * 128u + ((ka ^ rw) << 4);
+                stb[i] = hf * Lay::kTileHalf + rw * 128u + ((kb ^ rw) << 4);
+            }
+            float w_run = 0.f;  // warp 2: W so far
             for (int u = 0; cok && u < 2 * n_tiles; ++u) {
                 const int slot = u % kRing, kv = u & 1;
                 if (!(cok = mbar_wait(&kv_code[slot], (uint32_t)(u / kRing) & 1u, abort_flag, p.err))) break;
                 const int n_valid = L - (u >> 1) * kBN;
                 uint8_t *base = sRing + slot * Lay::kKVBytes;
-                const float *sc = sScale + slot * 128;
-                for (int r = cw * 64 + (lane >> 3); r < cw * 64 + 64; r += 4) {
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(base + Lay::kCodeOff + r * 128 + ((c ^ (r & 7)) << 4));
-                    __syncwarp();
-                    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-                    uint32_t h16[8];  // f16 pairs of dims 16c .. 16c+15 (exact)
+                if (kv == 1 && cw == 0) {
+                    // r = w / W for this V item's rows (0 beyond the context), W = max(W so far,
+                    // 2^ceil(log2 max w)); each lane rewrites the 4 scales it read
+                    float *sc = const_cast<float *>(sScale) + slot * 128;
+                    float4 w4 = reinterpret_cast<const float4 *>(sc)[lane];
+                    const int r0 = 4 * lane;
+                    w4.x = r0 < n_valid ? w4.x : 0.f;
+                    w4.y = r0 + 1 < n_valid ? w4.y : 0.f;
+                    w4.z = r0 + 2 < n_valid ? w4.z : 0.f;
+                    w4.w = r0 + 3 < n_valid ? w4.w : 0.f;
+                    float vmax = fmaxf(fmaxf(w4.x, w4.y), fmaxf(w4.z, w4.w));
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        uint32_t lo, hi;
-                        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(lo) : "h"((unsigned short)(w[k] & 0xffffu)));
-                        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hi) : "h"((unsigned short)(w[k] >> 16)));
-                        h16[2 * k] = lo;
-                        h16[2 * k + 1] = hi;
-                    }
-                    if (kv == 1) {
-                        if (r >= n_valid) {
+                    for (int o = 16; o > 0; o >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
+                    w_run = fmaxf(w_run, pow2_ceil(vmax));
+                    const float inv_w = w_run > 0.f ? __frcp_rn(w_run) : 0.f;  // exact: W is a power of two
+                    reinterpret_cast<float4 *>(sc)[lane] = make_float4(w4.x * inv_w, w4.y * inv_w, w4.z * inv_w, w4.w * inv_w);
+                    if (lane == 0) sW[slot] = w_run;
+                }
+                for (int g = cw * 64; g < cw * 64 + 64; g += 8) {
+                    const uint32_t grp = (uint32_t)g * 128u;
+                    uint4 raw[2];
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) raw[i] = *reinterpret_cast<const uint4 *>(base + grp + ld[i]);
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        uint32_t h16[8];  // f16 pairs of dims 16c .. 16c+15
+                        e4m3x4_to_f16(raw[i].x, h16[0], h16[1]);
+                        e4m3x4_to_f16(raw[i].y, h16[2], h16[3]);
+                        e4m3x4_to_f16(raw[i].z, h16[4], h16[5]);
+                        e4m3x4_to_f16(raw[i].w, h16[6], h16[7]);
+                        if (kv == 1 && g + rr + 4 * i >= n_valid) {
 #pragma unroll
                             for (int k = 0; k < 8; ++k) h16[k] = 0u;
-                        } else {
-                            // f16 products: the scale rounded to f16, then the product (two roundings,
-                            // each within half an f16 ulp)
-                            const __half2 sv = __float2half2_rn(sc[r]);
-#pragma unroll
-                            for (int k = 0; k < 8; ++k) {
-                                __half2 hh;
-                                memcpy(&hh, &h16[k], 4);
-                                hh = __hmul2(hh, sv);
-                                memcpy(&h16[k], &hh, 4);
-                            }
                         }
+                        const uint4 v0 = make_uint4(h16[0], h16[1], h16[2], h16[3]);
+                        const uint4 v1 = make_uint4(h16[4], h16[5], h16[6], h16[7]);
+                        *reinterpret_cast<uint4 *>(base + grp + sta[i]) = hf ? v1 : v0;
+                        *reinterpret_cast<uint4 *>(base + grp + stb[i]) = hf ? v0 : v1;
                     }
-                    const int hf = c >> 2, k0 = 2 * (c & 3);
-                    uint8_t *rowp = base + hf * Lay::kTileHalf + r * 128;
-                    // the two halves' lanes store opposite chunks first: the row's 8 stores of each
-                    // instruction then fill all 32 banks once
-                    const uint4 v0 = make_uint4(h16[0], h16[1], h16[2], h16[3]);
-                    const uint4 v1 = make_uint4(h16[4], h16[5], h16[6], h16[7]);
-                    const int ka = hf ? k0 + 1 : k0, kb = hf ? k0 : k0 + 1;
-                    *reinterpret_cast<uint4 *>(rowp + ((ka ^ (r & 7)) << 4)) = hf ? v1 : v0;
-                    *reinterpret_cast<uint4 *>(rowp + ((kb ^ (r & 7)) << 4)) = hf ? v0 : v1;
                 }
                 tc::fence_proxy_async_smem();
                 __syncwarp();
@@ -432,6 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tO = tmem + kColO + 128u * x + lane_base;
         const float c = p.scale_log2;
         float m_use = -INFINITY, l = 0.f;
+        float w_cur = 0.f;  // FP8: the factor W that O carries (the converter's, as of the last V item)
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
             const int kv_start = j * kBN;
@@ -493,6 +534,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t pk[kBN / 2];
             float2 l4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
             const float2 c2 = make_float2(c, c), nm2 = make_float2(neg_m, neg_m);
+            // FP8: P' = p * r (r = V row scale / W, FP32) enters the P.V product, so the V tile
+            // holds the exact codes; l sums p. W is the converter's for this V item.
+            bool w_grow = false;
+            float w_ratio = 1.f;
+            const float4 *r4 = nullptr;
+            if constexpr (FP8) {
+                const uint32_t uV = 2u * j + 1, vslot = uV % kRing;
+                if (!(ok = mbar_wait(&kv_full[vslot], (uV / kRing) & 1u, abort_flag, p.err))) break;
+                const float w_j = sW[vslot];
+                w_grow = w_j > w_cur;  // the same for every thread of the CTA
+                if (w_grow) {
+                    w_ratio = w_cur / w_j;  // exact: powers of two (0 while O is still 0)
+                    w_cur = w_j;
+                }
+                r4 = reinterpret_cast<const float4 *>(sScale + vslot * 128);
+            }
             if (masked) {
                 // boundary tiles: -inf entries, MUFU only (ex2(-inf) = 0)
 #pragma unroll
@@ -500,7 +557,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float2 xq = ffma2(make_float2(s[2 * q], s[2 * q + 1]), c2, nm2);
                     const float2 e = make_float2(fast_exp2(xq.x), fast_exp2(xq.y));
                     l4[q & 3] = fadd2(l4[q & 3], e);
-                    pk[q] = pack2(e.x, e.y, MMA_BF16);
+                    if constexpr (FP8) {
+                        const float4 rv = r4[q >> 1];
+                        pk[q] = (q & 1) ? pack2(e.x * rv.z, e.y * rv.w, false) : pack2(e.x * rv.x, e.y * rv.y, false);
+                    } else {
+                        pk[q] = pack2(e.x, e.y, MMA_BF16);
+                    }
                 }
             } else {
 #pragma unroll
@@ -509,7 +571,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float2 e = ((q & 7) < kEmuPerEight) ? exp2_fma2<MMA_BF16>(xq)
                                                               : make_float2(fast_exp2(xq.x), fast_exp2(xq.y));
                     l4[q & 3] = fadd2(l4[q & 3], e);
-                    pk[q] = pack2(e.x, e.y, MMA_BF16);
+                    if constexpr (FP8) {
+                        const float4 rv = r4[q >> 1];
+                        pk[q] = (q & 1) ? pack2(e.x * rv.z, e.y * rv.w, false) : pack2(e.x * rv.x, e.y * rv.y, false);
+                    } else {
+                        pk[q] = pack2(e.x, e.y, MMA_BF16);
+                    }
                 }
             }
             const float2 l2 = fadd2(fadd2(l4[0], l4[1]), fadd2(l4[2], l4[3]));
@@ -519,14 +586,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (j > 0) {
                 if (!(ok = mbar_wait(&o_done[x], (uint32_t)(j - 1) & 1u, abort_flag, p.err))) break;
                 tc::fence_after_sync();
-                if (__any_sync(0xffffffffu, grow)) {
+                if (__any_sync(0xffffffffu, grow) || w_grow) {
+                    const float o_scale = alpha * w_ratio;
 #pragma unroll
                     for (int cc = 0; cc < D / 32; ++cc) {
                         float o[32];
                         tc::tmem_ld32(tO + cc * 32, o);
                         tc::tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                        for (int i = 0; i < 32; ++i) o[i] *= o_scale;
                         tc::tmem_st32(tO + cc * 32, o);
                     }
                 }
@@ -558,7 +626,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- epilogue: O / l ----
         if (ok && mbar_wait(&o_done[x], (uint32_t)(n_tiles - 1) & 1u, abort_flag, p.err)) {
             tc::fence_after_sync();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            // O / l; over an FP8 cache O carries the factor W (0 only when every V scale is 0)
+            const float inv = l > 0.f ? (FP8 ? w_cur : 1.f) / l : 0.f;
             const size_t row_g = (size_t)(q0 + m_start + row);
             const size_t obase = (row_g * p.num_q_heads + h) * D;
 #pragma unroll

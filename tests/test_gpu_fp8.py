@@ -191,9 +191,9 @@ def run_prefill_fp8(p, codes, scales, out_dtype=None):
     return out, lse
 
 
-# Roundings on the FP8 prefill path: the output, P (f16), and V = f16(code) * f16(scale) in f16
-# (the scale's rounding and the product's).
-PREFILL_ROUNDINGS = 4
+# Roundings on the FP8 prefill path: the output and P' = P * (V row scale / W) in f16. The codes
+# enter the products exactly, and the row scales only in FP32.
+PREFILL_ROUNDINGS = 2
 
 
 @pytest.mark.parametrize("bs", [8, 16, 128, 512])
@@ -266,3 +266,37 @@ def test_fp8_decode_full_7b_size_sampled():
     p.q = p.q.cpu()
     ref, _ = oracle.attention_of(p, host(codes, scales))
     check_close(out, ref, W.F16, roundings=roundings(p), what="fp8 7B decode")
+
+
+@pytest.mark.parametrize("dtype", [W.F16, W.BF16])
+def test_fp8_prefill_tiny_zero_and_growing_v_scales(dtype):
+    """V rows whose magnitudes rise from 2^-20 to 2^4 along each sequence (some rows all zero):
+    row scales far below f16's normal range, and a largest V scale that keeps growing from key
+    tile to key tile, so the factor W the kernel keeps on O grows several times mid-sequence
+    (each time O is rescaled by a power of two). Decode over the same cache is checked too."""
+    lens, q_lens = [900, 1300, 257], [300, 1300, 257]
+    gen = torch.Generator().manual_seed(41)
+    tot = sum(lens)
+    k = W.randn_t(gen, (tot, 4, 128), dtype)
+    v = W.randn_t(gen, (tot, 4, 128), dtype).float()
+    mag = torch.cat([torch.exp2(torch.linspace(-20.0, 4.0, L)) for L in lens])
+    v = v * mag[:, None, None]
+    v[torch.arange(0, tot, 97)] = 0.0                     # all-zero rows: scale 0
+    v = v.to(W.TORCH_DTYPE[dtype])
+    p = prefill_problem(lens=lens, q_lens=q_lens, hq=8, hkv=4, dtype=dtype, seed=43)
+    p = W.make_problem("fp", batch=3, num_q_heads=8, num_kv_heads=4, head_dim=128, block_size=16,
+                       context_lens=lens, q_lens=q_lens, dtype=dtype, causal=True, seed=43,
+                       num_blocks=p.num_blocks, kv_format="fp8", kv_data=(k, v))
+    codes, scales = device_fp8(p)
+    out, lse = run_prefill_fp8(p, codes, scales)
+    ref, ref_lse = oracle.attention_of(p, host(codes, scales))
+    check_close(out, ref, dtype, roundings=PREFILL_ROUNDINGS, what="fp8 prefill growing scales %s" % dtype)
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-4, atol=1e-4)
+    # decode of one query per sequence over the same cache
+    qd = W.randn_t(gen, (3, 8, 128), dtype)
+    dec = pkv.paged_attn_decode(codes, to_dev(qd), to_dev(p.block_tables), to_dev(p.context_lens), scale=p.scale,
+                                scales=scales)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    ref_d, _ = oracle.attention_of(p, host(codes, scales), q=qd, cu_q_lens=W.cu_lens([1, 1, 1]))
+    check_close(dec, ref_d, dtype, roundings=roundings(p), what="fp8 decode growing scales %s" % dtype)

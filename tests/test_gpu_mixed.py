@@ -43,7 +43,7 @@ def run(p, cache, scales=None, num_splits=0):
 
 def check_rows(p, out, ref, chunk_roundings, what):
     """Decode rows (q_len 1) at the decode path's bound (the output is its one rounding to 16
-    bits); chunk rows at the prefill path's (P and the output, plus what an FP8 cache adds)."""
+    bits); chunk rows at the prefill path's (P and the output)."""
     cu, ql = p.cu_q_lens.tolist(), p.q_lens.tolist()
     dec = [cu[b] for b in range(p.batch) if ql[b] == 1]
     chunk = [r for b in range(p.batch) if ql[b] > 1 for r in range(cu[b], cu[b + 1])]
@@ -92,5 +92,5 @@ def test_mixed_batch_fp8_cache():
     out, lse = run(p, codes, scales=scales)
     ref, ref_lse = oracle.attention_of(p, oracle.Fp8Cache(codes.cpu().numpy(), scales.cpu().numpy()))
     assert torch.isfinite(out).all()
-    check_rows(p, out, ref, 4, "mixed fp8")
+    check_rows(p, out, ref, 2, "mixed fp8")
     np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-4, atol=1e-4)

@@ -10,11 +10,12 @@
 // O(n²)", prefill / decode section): Q K^T and P V are dense contractions and run as tcgen05.mma.
 //
 // CTA = one query head x 256 query rows of one sequence, as two 128-row tiles A and B that share
-// every K/V tile (384 threads, three warpgroups). Over an FP8 cache (head_dim 128) warps 2-3
-// convert each K/V tile in place from E4M3 codes to f16, exactly; the products run in f16; the
+// every K/V tile (384 threads, three warpgroups). Over an FP8 cache (head_dim 128) the E4M3 codes
+// are converted in place to f16 (exactly, as code * 2^-8, on the integer pipe): K tiles by warps
+// 2-3, V tiles by the softmax warps between key tiles; the products run in f16; the
 // softmax multiplies each score column by its K row scale and each P column by its V row scale
-// over W (a power of two the converter keeps at or above every V scale so far; O carries the
-// factor W); otherwise as below:
+// over W (a power of two warp 2 keeps at or above every V scale so far; O carries the factor W);
+// otherwise as below:
 //   warp 0     TMA producer: both Q tiles once (3-D tensor map over [total_q, Hq, D]); then for
 //              each 128-key tile j the K tile and the V tile, each into one slot of a 4-slot ring:
 //              the pages a tile covers are looked up in the block table by the warp's lanes and each
@@ -65,7 +66,9 @@ struct PrefillLayout {
     // where the f16 tile's second 64-column half goes) and its row scales in a scale slot
     static constexpr uint32_t kCodeOff = kTileHalf;             // within a ring slot
     static constexpr uint32_t kScaleOff = kBarOff + 256;        // [kRing][128] FP32
-    static constexpr uint32_t kSmemBytes = kBarOff + 256 + (FP8 ? kRing * 128 * 4 : 0) + 1024;  // + alignment slack
+    // the K row scales of key tile j times the softmax's log2 scale, at [j % 4][128] FP32
+    static constexpr uint32_t kKScaleOff = kScaleOff + kRing * 128 * 4;
+    static constexpr uint32_t kSmemBytes = kBarOff + 256 + (FP8 ? 2 * kRing * 128 * 4 : 0) + 1024;  // + alignment slack
     static constexpr uint32_t kTmemCols = 512;
 };
 
@@ -131,13 +134,21 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, bool bf16) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// Four E4M3 codes (one 32-bit word, lowest byte first) to two f16x2 words, exactly.
+// Four E4M3 codes (one 32-bit word, lowest byte first) to two f16x2 words holding the codes'
+// values times 2^-8, exactly, on the integer pipe. An E4M3 code s.eeee.mmm (bias 7) placed as the
+// f16 bits s.0eeee.mmm0000000 (bias 15) is its value times 2^(7 - 15) = 2^-8: normal codes map to
+// normal f16 values and subnormal codes (eeee = 0, value m * 2^-9) to f16 subnormals m * 2^-17,
+// both exact. Per pair of codes: a byte permute, then (t + (t & sign bits)) << 7, where the
+// addition moves each sign bit from bit 7 to bit 8 of its 16-bit half. (The f16 conversion
+// instruction would do the same work on the pipe that also packs P, which the softmax keeps busy:
+// measured, the whole pass then took 3.38 ms against 3.18 ms.)
 __device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t &lo, uint32_t &hi) {
-    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
-        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
-        : "=r"(lo), "=r"(hi)
-        : "r"(w));
+    const uint32_t tl = __byte_perm(w, 0u, 0x4140), th = __byte_perm(w, 0u, 0x4342);
+    lo = (tl + (tl & 0x00800080u)) << 7;
+    hi = (th + (th & 0x00800080u)) << 7;
 }
+// The factor the converted codes carry (2^-8), undone in FP32 by the K scales and the epilogue.
+constexpr float kCodeFactorInv = 256.f;
 
 // Smallest power of two >= x, for finite x >= 0 (0 for 0; 2^-126 for subnormal x).
 __device__ __forceinline__ float pow2_ceil(float x) {
@@ -146,6 +157,57 @@ __device__ __forceinline__ float pow2_ceil(float x) {
     if (b & 0x7fffffu) b = (b & 0x7f800000u) + 0x800000u;
     return __uint_as_float(b);
 }
+
+// In place, over an FP8 cache: the E4M3 codes of row r of a ring item (the slot's upper half, 128
+// bytes a row) become the f16 row r (values times 2^-8, see e4m3x4_to_f16) of the layout TMA
+// writes for a 16-bit cache (two 64-column halves, 128-byte swizzle); rows at or beyond zero_from
+// become zero. A pass takes 8 rows g .. g + 7 (g a multiple of 8): lane -> rows rr and rr + 4
+// (rr = lane / 8), 16-code chunk c = lane % 8, so every swizzled address is a lane constant plus
+// 1 KB a pass. A row is read entirely before any of it is written (its codes sit where its
+// second f16 half goes). The lanes of the two halves store opposite chunks first: the 8 stores
+// of a row in one instruction then fill all 32 banks once.
+template <uint32_t kCodeOff, uint32_t kTileHalf>
+struct RowConverter {
+    uint32_t ld[2], sta[2], stb[2];
+    int rr, hf;
+    __device__ __forceinline__ explicit RowConverter(int lane) {
+        const int c = lane & 7;
+        rr = lane >> 3;
+        hf = c >> 2;
+        const int k0 = 2 * (c & 3);
+        const int ka = hf ? k0 + 1 : k0, kb = hf ? k0 : k0 + 1;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int rw = rr + 4 * i;  // == row & 7
+            ld[i] = kCodeOff + rw * 128u + ((c ^ rw) << 4);
+            sta[i] = hf * kTileHalf + rw * 128u + ((ka ^ rw) << 4);
+            stb[i] = hf * kTileHalf + rw * 128u + ((kb ^ rw) << 4);
+        }
+    }
+    __device__ __forceinline__ void pass(uint8_t *base, int g, int zero_from) const {
+        const uint32_t grp = (uint32_t)g * 128u;
+        uint4 raw[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) raw[i] = *reinterpret_cast<const uint4 *>(base + grp + ld[i]);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            uint32_t h16[8];  // f16 pairs of dims 16c .. 16c+15
+            e4m3x4_to_f16(raw[i].x, h16[0], h16[1]);
+            e4m3x4_to_f16(raw[i].y, h16[2], h16[3]);
+            e4m3x4_to_f16(raw[i].z, h16[4], h16[5]);
+            e4m3x4_to_f16(raw[i].w, h16[6], h16[7]);
+            if (g + rr + 4 * i >= zero_from) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) h16[k] = 0u;
+            }
+            const uint4 v0 = make_uint4(h16[0], h16[1], h16[2], h16[3]);
+            const uint4 v1 = make_uint4(h16[4], h16[5], h16[6], h16[7]);
+            *reinterpret_cast<uint4 *>(base + grp + sta[i]) = hf ? v1 : v0;
+            *reinterpret_cast<uint4 *>(base + grp + stb[i]) = hf ? v0 : v1;
+        }
+    }
+};
 
 // BF16: type of q and the default output. FP8: the cache holds E4M3 codes with one FP32 scale per
 // row; the tensor-core products then run in f16 (MMA below), which holds every code exactly.
@@ -174,6 +236,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *q_ready = bars + 24;       // FP8: Q converted to f16 (or left as it is for f16 q)
     const float *sScale = reinterpret_cast<const float *>(smem + Lay::kScaleOff);  // FP8: [kRing][128]
     float *sW = reinterpret_cast<float *>(bars + 25);  // FP8: [kRing] W of each V item (see the converter)
+    uint64_t *ks_ready = bars + 27;      // [4] FP8: K scales of key tile j in sKS[j % 4]
+    uint64_t *r_ready = bars + 11;       // [2] FP8: r and W of the V item in ring slot 2i + 1
+    float *sKS = reinterpret_cast<float *>(smem + Lay::kKScaleOff);  // FP8: [4][128]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // grid (heads, batch, row blocks) with the row blocks last-first: CTAs start in linear order, so
@@ -198,12 +263,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kRing; ++s) {
-            // FP8: a slot is full once both converter warps have written it; a K slot (even: items
-            // alternate K, V) is free once its QK MMAs are done and the 8 softmax warps have read
-            // its row scales
-            mbar_init(&kv_full[s], FP8 ? 2 : 1);
-            mbar_init(&kv_empty[s], (FP8 && (s & 1) == 0) ? 9 : 1);
-            if (FP8) mbar_init(&kv_code[s], 1);
+            // FP8: a K slot (even: items alternate K, V) is full once both converter warps have
+            // converted it, a V slot once the 8 softmax warps have; the K row scales leave the
+            // ring slot for sKS, so every slot is free once its MMAs are done
+            mbar_init(&kv_full[s], FP8 ? ((s & 1) ? 8 : 2) : 1);
+            mbar_init(&kv_empty[s], 1);
+            if (FP8) {
+                mbar_init(&kv_code[s], 1);
+                mbar_init(&ks_ready[s], 1);
+                if (s < 2) mbar_init(&r_ready[s], 1);
+            }
         }
         mbar_init(q_full, 1);
         if (FP8) mbar_init(q_ready, 2);
@@ -298,17 +367,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         } else if (FP8 && warp >= 2) {
             // ================================ FP8 converter warps ================================
-            // In place, per ring item: the codes of row r (upper half of the slot) become the f16 row
-            // of the layout TMA writes for a 16-bit cache (two 64-column halves, 128-byte swizzle),
-            // exactly, K and V alike; V rows beyond the context are zeroed. Warp 2 (rows 0-63) and
-            // warp 3 (rows 64-127) take 8 consecutive rows per pass: lane -> rows rr and rr + 4 of the
-            // group (rr = lane / 8), 16-code chunk c = lane % 8, so every swizzled address is a lane
-            // constant plus 1 KB per pass. A row is read entirely before any of it is written (its
-            // codes sit where its second f16 half goes).
-            // Warp 2 also turns each V item's row scales w into r = w / W in place, W a power of two
-            // at or above every V scale seen so far in this CTA (kept in sW[slot]): the softmax
-            // folds r into P, and O carries the factor W (rescaled exactly when W grows).
-            const int cw = warp - 2, c = lane & 7, rr = lane >> 3;
+            // Per K item: the codes become f16 in place (RowConverter), warp 2 rows 0-63 and warp 3
+            // rows 64-127; warp 3 also copies the K row scales, times the log2 scale and 2^8 (the
+            // converted codes' factor), to sKS. The V items' codes are converted by the 8 softmax
+            // warps, each after its previous key tile (V_j is needed only after the softmax of
+            // tile j); here warp 2 turns each V item's row scales w into r = w / W in place, W a
+            // power of two at or above every V scale seen so far in this CTA (kept in sW[slot]):
+            // the softmax folds r into P, and O carries the factor W (rescaled exactly when W
+            // grows).
+            const int cw = warp - 2;
+            const RowConverter<Lay::kCodeOff, Lay::kTileHalf> conv(lane);
             bool cok = mbar_wait(q_full, 0, abort_flag, p.err);
             if (BF16 && cok) {
                 // q to f16 in place (exact for |q| within f16's range)
@@ -325,29 +393,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
             if (lane == 0 && cok) mbar_arrive(q_ready);
-            // lane-constant byte offsets within an 8-row group: code chunk c of rows rr and rr + 4,
-            // and the two f16 chunks (half hf, chunks k0 and k0 + 1) each row's 16 codes become. The
-            // lanes of the two halves store opposite chunks first: the 8 stores of a row in one
-            // instruction then fill all 32 banks once.
-            const int hf = c >> 2, k0 = 2 * (c & 3);
-            const int ka = hf ? k0 + 1 : k0, kb = hf ? k0 : k0 + 1;
-            uint32_t ld[2], sta[2], stb[2];
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int rw = rr + 4 * i;  // == row & 7
-                ld[i] = Lay::kCodeOff + rw * 128u + ((c ^ rw) << 4);
-                sta[i] = hf * Lay::kTileHalf + rw * 128u + ((ka ^ rw) << 4);
-                stb[i] = hf * Lay::kTileHalf + rw * 128u + ((kb ^ rw) << 4);
-            }
             float w_run = 0.f;  // warp 2: W so far
             for (int u = 0; cok && u < 2 * n_tiles; ++u) {
                 const int slot = u % kRing, kv = u & 1;
+                if (kv == 1 && cw == 1) continue;  // V codes: converted by the softmax warps
                 if (!(cok = mbar_wait(&kv_code[slot], (uint32_t)(u / kRing) & 1u, abort_flag, p.err))) break;
                 const int n_valid = L - (u >> 1) * kBN;
-                uint8_t *base = sRing + slot * Lay::kKVBytes;
-                if (kv == 1 && cw == 0) {
-                    // r = w / W for this V item's rows (0 beyond the context), W = max(W so far,
-                    // 2^ceil(log2 max w)); each lane rewrites the 4 scales it read
+                if (kv == 0) {
+                    if (cw == 1) {
+                        // the K row scales of this key tile, times the softmax's log2 scale, to
+                        // sKS[tile % 4] (read there by the softmax warps, so that the ring slot is
+                        // free as soon as its QK MMAs are done)
+                        const float4 k4 = reinterpret_cast<const float4 *>(sScale + slot * 128)[lane];
+                        const float sl2 = p.scale_log2 * kCodeFactorInv;
+                        reinterpret_cast<float4 *>(sKS + ((u >> 1) & 3) * 128)[lane] =
+                            make_float4(k4.x * sl2, k4.y * sl2, k4.z * sl2, k4.w * sl2);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&ks_ready[(u >> 1) & 3]);
+                    }
+                    for (int g = cw * 64; g < cw * 64 + 64; g += 8)
+                        conv.pass(sRing + slot * Lay::kKVBytes, g, kBN);
+                    tc::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&kv_full[slot]);
+                } else {
+                    // warp 2: r = w / W for this V item's rows (0 beyond the context), W = max(W so
+                    // far, 2^ceil(log2 max w)); each lane rewrites the 4 scales it read
                     float *sc = const_cast<float *>(sScale) + slot * 128;
                     float4 w4 = reinterpret_cast<const float4 *>(sc)[lane];
                     const int r0 = 4 * lane;
@@ -362,33 +433,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float inv_w = w_run > 0.f ? __frcp_rn(w_run) : 0.f;  // exact: W is a power of two
                     reinterpret_cast<float4 *>(sc)[lane] = make_float4(w4.x * inv_w, w4.y * inv_w, w4.z * inv_w, w4.w * inv_w);
                     if (lane == 0) sW[slot] = w_run;
-                }
-                for (int g = cw * 64; g < cw * 64 + 64; g += 8) {
-                    const uint32_t grp = (uint32_t)g * 128u;
-                    uint4 raw[2];
-#pragma unroll
-                    for (int i = 0; i < 2; ++i) raw[i] = *reinterpret_cast<const uint4 *>(base + grp + ld[i]);
                     __syncwarp();
-#pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        uint32_t h16[8];  // f16 pairs of dims 16c .. 16c+15
-                        e4m3x4_to_f16(raw[i].x, h16[0], h16[1]);
-                        e4m3x4_to_f16(raw[i].y, h16[2], h16[3]);
-                        e4m3x4_to_f16(raw[i].z, h16[4], h16[5]);
-                        e4m3x4_to_f16(raw[i].w, h16[6], h16[7]);
-                        if (kv == 1 && g + rr + 4 * i >= n_valid) {
-#pragma unroll
-                            for (int k = 0; k < 8; ++k) h16[k] = 0u;
-                        }
-                        const uint4 v0 = make_uint4(h16[0], h16[1], h16[2], h16[3]);
-                        const uint4 v1 = make_uint4(h16[4], h16[5], h16[6], h16[7]);
-                        *reinterpret_cast<uint4 *>(base + grp + sta[i]) = hf ? v1 : v0;
-                        *reinterpret_cast<uint4 *>(base + grp + stb[i]) = hf ? v0 : v1;
-                    }
+                    if (lane == 0) mbar_arrive(&r_ready[slot >> 1]);
                 }
-                tc::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&kv_full[slot]);
             }
         } else if (warp == 1) {
             // ===================================== MMA issuer =====================================
@@ -470,11 +517,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         const uint32_t tS = tmem + kColS + 128u * x + lane_base;   // S_x, and P_x over its first 64 columns
         const uint32_t tO = tmem + kColO + 128u * x + lane_base;
-        const float c = p.scale_log2;
+        // over an FP8 cache the log2 scale is folded into the K row scales (sKS)
+        const float c = FP8 ? 1.f : p.scale_log2;
         float m_use = -INFINITY, l = 0.f;
         float w_cur = 0.f;  // FP8: the factor W that O carries (the converter's, as of the last V item)
         bool ok = true;
-        for (int j = 0; j < n_tiles; ++j) {
+        // FP8: the 8 softmax warps convert the codes of V item jv in place, 16 rows each (2 passes
+        // of 8 rows; rows beyond the context zeroed), V_0 before the first key tile and V_{j+1}
+        // right after tile j: V_{j+1}'s codes land while the softmax works on tile j, and the P
+        // V_{j+1} MMAs need it only after the softmax of tile j + 1
+        const RowConverter<Lay::kCodeOff, Lay::kTileHalf> vconv(lane);
+        auto convert_v = [&](int jv) -> bool {
+            const uint32_t uV = 2u * jv + 1, vslot = uV % kRing;
+            if (!mbar_wait(&kv_code[vslot], (uV / kRing) & 1u, abort_flag, p.err)) return false;
+            const int g = (x * 4 + quarter) * 16;
+            uint8_t *vb = sRing + vslot * Lay::kKVBytes;
+            vconv.pass(vb, g, L - jv * kBN);
+            vconv.pass(vb, g + 8, L - jv * kBN);
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&kv_full[vslot]);
+            return true;
+        };
+        if constexpr (FP8) ok = convert_v(0);
+        for (int j = 0; ok && j < n_tiles; ++j) {
             const int kv_start = j * kBN;
             const uint32_t ph = (uint32_t)j & 1u;
             if (!(ok = mbar_wait(&s_full[x], ph, abort_flag, p.err))) break;
@@ -485,23 +551,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::tmem_ld32(tS + cc * 32, *reinterpret_cast<float(*)[32]>(&s[cc * 32]));
             tc::tmem_wait_ld();
             if constexpr (FP8) {
-                // K row scales multiply the score columns (FP32); the K slot is freed for the next
-                // copy only after all 8 softmax warps have read them
-                const uint32_t uK = 2u * j, slot = uK % kRing;
-                // the scales came by bulk copy (completion on kv_code); the slot cannot move on to
-                // its next item before these warps arrive on kv_empty below
-                if (!(ok = mbar_wait(&kv_code[slot], (uK / kRing) & 1u, abort_flag, p.err))) break;
-                const float4 *ks4 = reinterpret_cast<const float4 *>(sScale + slot * 128);
+                // K row scales (times the log2 scale) multiply the score columns, in FP32. sKS[j % 4]
+                // is next written for tile j + 4, whose K item cannot arrive before both softmax
+                // warpgroups are done with tile j + 1
+                if (!(ok = mbar_wait(&ks_ready[j & 3], (uint32_t)(j >> 2) & 1u, abort_flag, p.err))) break;
+                const float4 *ks4 = reinterpret_cast<const float4 *>(sKS + (j & 3) * 128);
 #pragma unroll
                 for (int i = 0; i < kBN / 4; ++i) {
                     const float4 k4 = ks4[i];
-                    s[4 * i] *= k4.x;
-                    s[4 * i + 1] *= k4.y;
-                    s[4 * i + 2] *= k4.z;
-                    s[4 * i + 3] *= k4.w;
+                    const float2 a = fmul2(make_float2(s[4 * i], s[4 * i + 1]), make_float2(k4.x, k4.y));
+                    const float2 b = fmul2(make_float2(s[4 * i + 2], s[4 * i + 3]), make_float2(k4.z, k4.w));
+                    s[4 * i] = a.x;
+                    s[4 * i + 1] = a.y;
+                    s[4 * i + 2] = b.x;
+                    s[4 * i + 3] = b.y;
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&kv_empty[slot]);
             }
             // last key index this row may see in this tile (-1: none)
             int lim = L - 1 - kv_start;
@@ -541,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float4 *r4 = nullptr;
             if constexpr (FP8) {
                 const uint32_t uV = 2u * j + 1, vslot = uV % kRing;
-                if (!(ok = mbar_wait(&kv_full[vslot], (uV / kRing) & 1u, abort_flag, p.err))) break;
+                if (!(ok = mbar_wait(&r_ready[vslot >> 1], (uV / kRing) & 1u, abort_flag, p.err))) break;
                 const float w_j = sW[vslot];
                 w_grow = w_j > w_cur;  // the same for every thread of the CTA
                 if (w_grow) {
@@ -559,7 +623,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     l4[q & 3] = fadd2(l4[q & 3], e);
                     if constexpr (FP8) {
                         const float4 rv = r4[q >> 1];
-                        pk[q] = (q & 1) ? pack2(e.x * rv.z, e.y * rv.w, false) : pack2(e.x * rv.x, e.y * rv.y, false);
+                        const float2 er = fmul2(e, (q & 1) ? make_float2(rv.z, rv.w) : make_float2(rv.x, rv.y));
+                        pk[q] = pack2(er.x, er.y, false);
                     } else {
                         pk[q] = pack2(e.x, e.y, MMA_BF16);
                     }
@@ -573,7 +638,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     l4[q & 3] = fadd2(l4[q & 3], e);
                     if constexpr (FP8) {
                         const float4 rv = r4[q >> 1];
-                        pk[q] = (q & 1) ? pack2(e.x * rv.z, e.y * rv.w, false) : pack2(e.x * rv.x, e.y * rv.y, false);
+                        const float2 er = fmul2(e, (q & 1) ? make_float2(rv.z, rv.w) : make_float2(rv.x, rv.y));
+                        pk[q] = pack2(er.x, er.y, false);
                     } else {
                         pk[q] = pack2(e.x, e.y, MMA_BF16);
                     }
@@ -622,12 +688,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[x]);
+            if constexpr (FP8) {
+                if (j + 1 < n_tiles && !(ok = convert_v(j + 1))) break;
+            }
         }
         // ---- epilogue: O / l ----
         if (ok && mbar_wait(&o_done[x], (uint32_t)(n_tiles - 1) & 1u, abort_flag, p.err)) {
             tc::fence_after_sync();
-            // O / l; over an FP8 cache O carries the factor W (0 only when every V scale is 0)
-            const float inv = l > 0.f ? (FP8 ? w_cur : 1.f) / l : 0.f;
+            // O / l; over an FP8 cache O carries the factor W (0 only when every V scale is 0) and
+            // the converted codes' 2^-8
+            const float inv = l > 0.f ? (FP8 ? w_cur * kCodeFactorInv : 1.f) / l : 0.f;
             const size_t row_g = (size_t)(q0 + m_start + row);
             const size_t obase = (row_g * p.num_q_heads + h) * D;
 #pragma unroll

@@ -18,7 +18,8 @@
 //     read one unit ahead, and each lane issues its page slice's boxes (K rows then V rows, 64
 //     columns, 128-byte swizzle, through a 5-D tensor map over the cache; evict-first in L2, since
 //     each line is read once), into a ring of as many stages (up to 6) as the shared memory left
-//     by the merge buffers and the unit tables holds; q comes in with the unit's first tile;
+//     by the merge buffers, the two q buffers and the unit tables holds; each unit's q goes to one
+//     of two q buffers with barriers of their own (units can be shorter than the ring);
 //   * warps 0-3 each own 16 tokens of a tile (units of 16 or 32 query heads: warps 0-7, two per 16
 //     tokens, each with half the unit's 8-head n-tiles, so that each dependent chain is half as
 //     long and every scheduler has two of them): ldmatrix from the swizzled tile gives the A fragments
@@ -57,15 +58,18 @@ struct GqaLayout {
     // per 64-column half: page slices of br rows, each its br K rows then its br V rows
     static constexpr uint32_t kHalfRegion = 2 * kHalfBytes;
     static constexpr uint32_t kQBytes = G * D * 2;
-    static constexpr uint32_t kStageBytes = (2 * kKBytes + kQBytes + 1023) / 1024 * 1024;
+    static constexpr uint32_t kStageBytes = 2 * kKBytes;  // K and V of a tile (q has its own buffers)
     static constexpr uint32_t kMergeFloats = kWarps * G * kMergeRow<D>;  // one merge buffer
     // 16 or 32 heads: one merge buffer (the consumers wait for the merge of the previous unit),
     // which leaves room for another stage; fewer heads: two, taking turns
     static constexpr int kMergeBufs = G >= 16 ? 1 : 2;
-    // barriers: full / empty per stage slot, merge full / empty per merge buffer; then the abort
-    // flag (padded to 16 bytes), the unit of each stage slot and the unit of each merge buffer
-    static constexpr uint32_t kBarOffset = kMergeBufs * kMergeFloats * 4;
-    static constexpr uint32_t kFixedBytes = kBarOffset + (2 * kStagesMax + 4) * 8 + 16 + (kStagesMax + 2) * 4;
+    // q of two units, taking turns (a unit's q is read at its first tile)
+    static constexpr uint32_t kQOffset = kMergeBufs * kMergeFloats * 4;
+    // barriers: full / empty per stage slot, merge full / empty per merge buffer, q full / empty
+    // per q buffer; then the abort flag (padded to 16 bytes), the unit of each stage slot and the
+    // unit of each merge buffer
+    static constexpr uint32_t kBarOffset = kQOffset + 2 * kQBytes;
+    static constexpr uint32_t kFixedBytes = kBarOffset + (2 * kStagesMax + 8) * 8 + 16 + (kStagesMax + 2) * 4;
     static constexpr uint32_t kStagesOffset = (kFixedBytes + 1023) / 1024 * 1024;
     __host__ __device__ static size_t ints_offset(int stages) { return kStagesOffset + (size_t)stages * kStageBytes; }
     __host__ __device__ static size_t smem_bytes(int batch, int s_max, int stages) {
@@ -109,8 +113,11 @@ __global__ void __launch_bounds__(GqaWarps<G>::kThreads, 1)
     uint64_t *empty = full + kStagesMax;
     uint64_t *mfull = empty + kStagesMax;  // [2] the consumer warps' rows of a unit are in buffer i
     uint64_t *mempty = mfull + 2;          // [2] the merge warp has read buffer i
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(mempty + 2);
-    int *stage_unit = reinterpret_cast<int *>(mempty + 2) + 4;
+    uint64_t *qfull = mempty + 2;          // [2] q of a unit has landed in q buffer i
+    uint64_t *qempty = qfull + 2;          // [2] the consumer warps have read q buffer i
+    uint8_t *qbuf = base + L::kQOffset;    // [2][G][D]
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(qempty + 2);
+    int *stage_unit = reinterpret_cast<int *>(qempty + 2) + 4;
     int *merge_unit = stage_unit + kStagesMax;  // [2] unit of each merge buffer, -1: end
     uint8_t *smem = base + L::kStagesOffset;    // stage i at i * kStageBytes
     const UnitTable ut = unit_table(reinterpret_cast<int *>(base + L::ints_offset(nst)), a.batch, a.s_max);
@@ -128,6 +135,8 @@ __global__ void __launch_bounds__(GqaWarps<G>::kThreads, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&mfull[i], W::kConsumers);
             mbar_init(&mempty[i], 1);
+            mbar_init(&qfull[i], 1);
+            mbar_init(&qempty[i], W::kConsumers);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -143,12 +152,23 @@ __global__ void __launch_bounds__(GqaWarps<G>::kThreads, 1)
         int stage = 0;
         uint32_t phase = 0;
         uint32_t issued_mask = 0, issued_parity = 0;
+        int qb = 0;                      // q buffer of the next unit
+        uint32_t qphase = 0;
+        uint32_t q_issued = 0, q_parity = 0;  // q copies issued per buffer (for the abort drain)
         UnitCursor c = {};
         PageWindow win = {};
         if ((int)blockIdx.x < num_units) {
             c = unit_of(blockIdx.x, ut, a.s_max, hu, chunk);
             win = unit_pages(a, c, lane);
         }
+        // on a wait that gave up: let every copy in flight land before the warp exits (bounded)
+        auto drain = [&]() {
+            volatile int no_abort = 0;
+            for (int i = 0; i < nst; ++i)
+                if (issued_mask & (1u << i)) mbar_wait(&full[i], (issued_parity >> i) & 1u, &no_abort, nullptr);
+            for (int i = 0; i < 2; ++i)
+                if (q_issued & (1u << i)) mbar_wait(&qfull[i], (q_parity >> i) & 1u, &no_abort, nullptr);
+        };
         for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
             // the next unit's cursor and page ids, loading while this unit's copies go out
             UnitCursor cn = c;
@@ -159,6 +179,22 @@ __global__ void __launch_bounds__(GqaWarps<G>::kThreads, 1)
             }
             const int *bt = a.block_tables + (size_t)c.b * a.max_blocks_per_seq;
             const int unit_last_page = (c.t1 - 1) >> a.cache.log2_block_size;
+            // the unit's q into q buffer qb, once the consumers have read the unit two back from it
+            if (!mbar_wait(&qempty[qb], qphase ^ 1u, abort_flag, a.err)) {
+                drain();
+                return;
+            }
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&qfull[qb], L::kQBytes);
+                const uint16_t *qsrc = qg + ((size_t)ut.qrow[c.b] * a.num_q_heads + (size_t)c.kvh * G) * D;
+                bulk_g2s(qbuf + qb * L::kQBytes, qsrc, L::kQBytes, &qfull[qb], pol);
+            }
+            q_issued |= 1u << qb;
+            q_parity = (q_parity & ~(1u << qb)) | (qphase << qb);
+            if (++qb == 2) {
+                qb = 0;
+                qphase ^= 1u;
+            }
             for (int ts = c.t0; ts < c.t1; ts += kTile) {
                 const int n = min(kTile, c.t1 - ts);
                 const int nslices = (n + br - 1) / br;  // <= 8
@@ -176,20 +212,13 @@ __global__ void __launch_bounds__(GqaWarps<G>::kThreads, 1)
                     }
                 }
                 if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.err)) {
-                    for (int i = 0; i < nst; ++i)
-                        if (issued_mask & (1u << i)) {
-                            volatile int no_abort = 0;
-                            mbar_wait(&full[i], (issued_parity >> i) & 1u, &no_abort, nullptr);
-                        }
+                    drain();
                     return;
                 }
                 uint8_t *st = smem + (size_t)stage * L::kStageBytes;
-                const bool first_tile = (ts == c.t0);
                 if (lane == 0) {
                     stage_unit[stage] = u;
-                    const uint32_t bytes = (uint32_t)nslices * br * 128u * L::kHalves * 2u +
-                                           (first_tile ? L::kQBytes : 0u);
-                    mbar_arrive_expect_tx(&full[stage], bytes);
+                    mbar_arrive_expect_tx(&full[stage], (uint32_t)nslices * br * 128u * L::kHalves * 2u);
                 }
                 __syncwarp();
                 if (lane < nslices) {
@@ -200,10 +229,6 @@ __global__ void __launch_bounds__(GqaWarps<G>::kThreads, 1)
                     for (int hf = 0; hf < L::kHalves; ++hf)
                         tc::tma_load_5d_hint(st + hf * L::kHalfRegion + dst, &tm_kv, hf * 64, off, kvr, 0, pb,
                                              &full[stage], pol);
-                }
-                if (first_tile && lane == 0) {
-                    const uint16_t *qsrc = qg + ((size_t)ut.qrow[c.b] * a.num_q_heads + (size_t)c.kvh * G) * D;
-                    bulk_g2s(st + 2 * L::kKBytes, qsrc, L::kQBytes, &full[stage], pol);
                 }
                 issued_mask |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -245,11 +270,37 @@ __global__ void __launch_bounds__(GqaWarps<G>::kThreads, 1)
     uint32_t phase = 0;
     int mbuf = 0;  // merge buffer of the next unit
     uint32_t mphase = 0;
+    int qb = 0;    // q buffer of the next unit
+    uint32_t qphase = 0;
     for (;;) {
         if (!mbar_wait(&full[stage], phase, abort_flag, a.err)) return;
         const int u = stage_unit[stage];
         if (u < 0) break;
         const UnitCursor c = unit_of(u, ut, a.s_max, hu, chunk);
+        {
+            // the unit's q as B fragments, then q buffer qb is free for the unit after next
+            if (!mbar_wait(&qfull[qb], qphase, abort_flag, a.err)) return;
+            const uint16_t *sq = reinterpret_cast<const uint16_t *>(qbuf + qb * L::kQBytes);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int hs = (nt0 + nt) * 8 + gid;  // head slot
+#pragma unroll
+                for (int kk = 0; kk < kKSteps; ++kk) {
+                    if (hs < G) {
+                        bq[kk][nt][0] = *reinterpret_cast<const uint32_t *>(sq + hs * D + kk * 16 + 2 * tig);
+                        bq[kk][nt][1] = *reinterpret_cast<const uint32_t *>(sq + hs * D + kk * 16 + 8 + 2 * tig);
+                    } else {
+                        bq[kk][nt][0] = bq[kk][nt][1] = 0u;
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&qempty[qb]);
+            if (++qb == 2) {
+                qb = 0;
+                qphase ^= 1u;
+            }
+        }
         float m[NT][2], l[NT][2];
         float o[kKSteps][NT][4];
 #pragma unroll
@@ -264,22 +315,6 @@ __global__ void __launch_bounds__(GqaWarps<G>::kThreads, 1)
             if (ts != c.t0 && !mbar_wait(&full[stage], phase, abort_flag, a.err)) return;
             uint8_t *st = smem + (size_t)stage * L::kStageBytes;
             const uint32_t aK = smem_addr(st), aV = aK + br * 128u;  // + slice row tp: K; + tp: V
-            if (ts == c.t0) {
-                const uint16_t *sq = reinterpret_cast<const uint16_t *>(st + 2 * L::kKBytes);
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const int hs = (nt0 + nt) * 8 + gid;  // head slot
-#pragma unroll
-                    for (int kk = 0; kk < kKSteps; ++kk) {
-                        if (hs < G) {
-                            bq[kk][nt][0] = *reinterpret_cast<const uint32_t *>(sq + hs * D + kk * 16 + 2 * tig);
-                            bq[kk][nt][1] = *reinterpret_cast<const uint32_t *>(sq + hs * D + kk * 16 + 8 + 2 * tig);
-                        } else {
-                            bq[kk][nt][0] = bq[kk][nt][1] = 0u;
-                        }
-                    }
-                }
-            }
             const int t0w = slice * 16;     // this warp's tokens in the tile
             if (t0w + 16 > n) {
                 // tokens at or beyond the context end may hold unwritten cache bytes (or stale

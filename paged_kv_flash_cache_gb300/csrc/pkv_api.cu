@@ -105,11 +105,12 @@ CacheView view_of(const pkv_cache &c) {
 
 // Tokens per decode split.  Automatic: enough (sequence, KV head, split) units for about
 // eight per CTA at full capacity, in [128, 512] tokens; explicit: capacity / num_splits
-// rounded up to the tile.  Either way at least capacity / kDecodeMaxSplits, rounded up to the
-// tile, so that a full context has at most kDecodeMaxSplits splits.
+// rounded up to kSplitAlign (128, the tensor-core decode's key tile).  Either way at least
+// capacity / kDecodeMaxSplits, rounded up, so that a full context has at most kDecodeMaxSplits
+// splits.
 int split_tokens(int batch, int num_kv_heads, int block_size, int max_blocks_per_seq, int num_splits) {
     const long long cap = (long long)max_blocks_per_seq * block_size;
-    const long long tile = kDecodeTile;
+    const long long tile = kSplitAlign;
     long long c;
     if (num_splits > 0) {
         c = (cap + num_splits - 1) / num_splits;
@@ -196,7 +197,7 @@ int pkv_decode_split_tokens(int batch, int num_q_heads, int num_kv_heads, int he
                             int max_blocks_per_seq, int num_splits) {
     (void)num_q_heads;
     (void)head_dim;
-    if (batch <= 0 || num_kv_heads <= 0 || block_size <= 0 || max_blocks_per_seq <= 0) return kDecodeTile;
+    if (batch <= 0 || num_kv_heads <= 0 || block_size <= 0 || max_blocks_per_seq <= 0) return kSplitAlign;
     return split_tokens(batch, num_kv_heads, block_size, max_blocks_per_seq, num_splits);
 }
 
@@ -220,7 +221,7 @@ namespace {
 // The decode call; cu_q_lens != nullptr decodes only the single-row sequences of a mixed batch
 // (their rows cu_q_lens[b]) and leaves the other rows untouched.
 pkv_status decode_impl(const pkv_cache &cache, const void *q, int num_q_heads, const int *block_tables,
-                       const int *context_lens, const int *cu_q_lens, int batch, int max_blocks_per_seq,
+                       const int *context_lens, const int *cu_q_lens, int batch, int q_rows, int max_blocks_per_seq,
                        float scale, int num_splits, void *workspace, size_t workspace_bytes, void *out,
                        pkv_dtype out_dtype, float *lse, void *stream) {
     pkv_status st = check_cache(cache);
@@ -229,9 +230,11 @@ pkv_status decode_impl(const pkv_cache &cache, const void *q, int num_q_heads, c
     if (batch < 0 || max_blocks_per_seq <= 0 || num_q_heads <= 0 || num_splits < 0) return PKV_ERR_INVALID_ARG;
     if (num_q_heads % cache.num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
     const int group = num_q_heads / cache.num_kv_heads;
-    // 1, 2, 4, or any multiple of 8 query heads per KV head (wide groups as several units)
-    if (group != 1 && group != 2 && group != 4 && group % 8 != 0) return PKV_ERR_UNSUPPORTED;
-    if (group > 8 && cache.format == PKV_KV_FP8_E4M3 && cache.head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    const bool fp8 = cache.format == PKV_KV_FP8_E4M3;
+    // an FP8 cache: 1, 2, 4, or any multiple of 8 query heads per KV head (8 per unit; head_dim 64:
+    // at most 8); a native cache: any group
+    if (fp8 && group != 1 && group != 2 && group != 4 && group % 8 != 0) return PKV_ERR_UNSUPPORTED;
+    if (fp8 && group > 8 && cache.head_dim != 128) return PKV_ERR_UNSUPPORTED;
     if (batch > decode_max_batch()) return PKV_ERR_UNSUPPORTED;
     if (batch == 0) return PKV_OK;
     if (!q || !block_tables || !context_lens || !out) return PKV_ERR_INVALID_ARG;
@@ -255,14 +258,33 @@ pkv_status decode_impl(const pkv_cache &cache, const void *q, int num_q_heads, c
     a.max_blocks_per_seq = max_blocks_per_seq;
     a.scale = scale;
     a.chunk = chunk;
+    a.q_rows = q_rows;
     a.s_max = s_max;
     a.stages = 0;  // set by the group kernel's launcher
-    // query heads per unit: the FP8 kernel holds 8 head slots, the native group kernel 32 (head_dim
-    // 128), 16 or 8
-    const int per_unit = (cache.format == PKV_KV_FP8_E4M3) ? 8
-                         : (group % 32 == 0 && cache.head_dim == 128) ? 32
-                         : (group % 16 == 0) ? 16 : 8;
-    a.head_groups = group > per_unit ? group / per_unit : 1;
+    // The kernel and the query heads of a unit (a KV head's group, or an equal share of it):
+    //   FP8 cache: the FP8 kernels, at most 8 per unit;
+    //   native cache, 1 or 2 heads per KV head: CUDA cores (decode.cu), the group as one unit;
+    //   4 or 8: mma.sync units of the whole group (decode_gqa.cu);
+    //   any other group: tcgen05 units (decode_tc.cu) of the group, or, above 128 heads, of its
+    //   largest divisor up to 128.
+    enum { kCudaCores, kMmaSync, kTcgen05, kFp8Tensor } path;
+    int per_unit;
+    if (fp8) {
+        path = cache.head_dim == 128 ? kFp8Tensor : kCudaCores;
+        per_unit = group < 8 ? group : 8;
+    } else if (group <= 2) {
+        path = kCudaCores;
+        per_unit = group;
+    } else if (group == 4 || group == 8) {
+        path = kMmaSync;
+        per_unit = group;
+    } else {
+        path = kTcgen05;
+        per_unit = group;
+        for (int d = 128; per_unit > 128; --d)
+            if (group % d == 0) per_unit = d;
+    }
+    a.head_groups = group / per_unit;
     a.cu_q_lens = cu_q_lens;
     a.part_o = static_cast<float *>(workspace);
     a.part_lse = need > 0 ? a.part_o + (size_t)batch * num_q_heads * s_max * cache.head_dim : nullptr;
@@ -272,11 +294,13 @@ pkv_status decode_impl(const pkv_cache &cache, const void *q, int num_q_heads, c
     a.err = s->err_ptr;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const int grid = s->info.num_sms * s->info.decode_ctas_per_sm;
-    // tensor cores: four or more query heads per KV head of a native cache (the group kernel),
-    // and every grouping of an FP8 cache with head_dim 128; CUDA cores for the rest
     cudaError_t le;
-    if (a.cache.fp8) le = cache.head_dim == 128 ? launch_decode_fp8(a, grid, cs) : launch_decode(a, grid, cs);
-    else le = group >= 4 ? launch_decode_gqa(a, grid, cs) : launch_decode(a, grid, cs);
+    switch (path) {
+        case kFp8Tensor: le = launch_decode_fp8(a, grid, cs); break;
+        case kMmaSync: le = launch_decode_gqa(a, grid, cs); break;
+        case kTcgen05: le = launch_decode_tc(a, grid, cs); break;
+        default: le = launch_decode(a, grid, cs); break;
+    }
     if (le != cudaSuccess) return PKV_ERR_CUDA;
     // Rows that span several splits (and empty rows) are finished by the merge.
     CombineArgs c;
@@ -305,8 +329,8 @@ pkv_status pkv_paged_attn_decode(pkv_cache cache, const void *q, int num_q_heads
                                  const int *context_lens, int batch, int max_blocks_per_seq, float scale,
                                  int num_splits, void *workspace, size_t workspace_bytes, void *out,
                                  pkv_dtype out_dtype, float *lse, void *stream) {
-    return decode_impl(cache, q, num_q_heads, block_tables, context_lens, nullptr, batch, max_blocks_per_seq, scale,
-                       num_splits, workspace, workspace_bytes, out, out_dtype, lse, stream);
+    return decode_impl(cache, q, num_q_heads, block_tables, context_lens, nullptr, batch, batch, max_blocks_per_seq,
+                       scale, num_splits, workspace, workspace_bytes, out, out_dtype, lse, stream);
 }
 
 pkv_status pkv_attn_combine(const float *partial_o, const float *partial_lse, int n_rows, int num_splits,
@@ -403,7 +427,8 @@ pkv_status pkv_paged_attn_mixed(pkv_cache cache, const void *q, int num_q_heads,
     if (!cu_q_lens && batch > 0) return PKV_ERR_INVALID_ARG;
     // decode rows first (split kernel + merge), then the prefill chunks; each kernel leaves the
     // other kind's rows alone
-    pkv_status st = decode_impl(cache, q, num_q_heads, block_tables, context_lens, cu_q_lens, batch,
+    if (total_q < 0) return PKV_ERR_INVALID_ARG;
+    pkv_status st = decode_impl(cache, q, num_q_heads, block_tables, context_lens, cu_q_lens, batch, total_q,
                                 max_blocks_per_seq, scale, num_splits, workspace, workspace_bytes, out, out_dtype,
                                 lse, stream);
     if (st != PKV_OK) return st;

@@ -49,6 +49,7 @@ struct DecodeArgs {
     // q / out rows; only sequences with exactly one query row are decoded here, their row being
     // cu_q_lens[b]. nullptr: every sequence has one query row, row b.
     const int *cu_q_lens;
+    int q_rows;  // rows of q (and of out): batch, or the mixed call's total query rows
     int s_max;   // splits a full-capacity context uses: ceil(max_blocks_per_seq * block_size / chunk)
     int stages;  // pipeline stages of the group kernel (chosen at launch from the shared memory left)
     float *part_o;    // [batch, Hq, s_max, D]
@@ -131,6 +132,7 @@ struct DeviceFlags {
 int *device_error_word();  // the current device's sticky error word (device address)
 
 constexpr int kDecodeTile = 64;         // tokens per decode pipeline stage
+constexpr int kSplitAlign = 128;        // decode splits start at multiples of this many tokens
 constexpr int kDecodeMaxSplits = 2048;  // splits of one context (bounds the split size from below)
 
 cudaError_t launch_append(const AppendArgs &a, cudaStream_t s);
@@ -140,7 +142,13 @@ cudaError_t encode_cache_map(const CacheView &c, int box_rows, CUtensorMap *map)
 cudaError_t encode_kv5_rows_map(const CacheView &c, int box_rows, CUtensorMap *map);
 cudaError_t encode_kv5_map(const CacheView &c, int box_rows, CUtensorMap *map);
 cudaError_t encode_fp8_maps(const CacheView &c, int box_rows, CUtensorMap *codes, CUtensorMap *scales);
+// 2-D tensor map over `rows` rows of `cols` 16-bit elements (bf16 if bf16 != 0, else f16), rows
+// contiguous; boxes of box_cols x box_rows, 128-byte swizzle (box_cols * 2 = 128).
+cudaError_t encode_rows_map(const void *ptr, int bf16, long long rows, int cols, int box_cols, int box_rows,
+                            CUtensorMap *map);
 cudaError_t launch_decode_gqa(const DecodeArgs &a, int grid, cudaStream_t s);
+// Tensor-core (tcgen05) decode for a unit of up to 128 query heads of one KV head.
+cudaError_t launch_decode_tc(const DecodeArgs &a, int grid, cudaStream_t s);
 cudaError_t launch_decode_fp8(const DecodeArgs &a, int grid, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs &a, int grid, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s);

@@ -783,6 +783,23 @@ cudaError_t encode_cache_map(const CacheView &c, int box_rows, CUtensorMap *map)
     return cudaSuccess;
 }
 
+cudaError_t encode_rows_map(const void *ptr, int bf16, long long rows, int cols, int box_cols, int box_rows,
+                            CUtensorMap *map) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    if (rows <= 0 || rows > 0x7fffffffll || box_rows <= 0 || box_rows > 256 || box_cols * 2 != 128)
+        return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr),
+            dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    return cudaSuccess;
+}
+
 // The cache viewed as the 5-D tensor [NB][2][Hkv][bs][D] so that one box holds a page slice of K
 // and of V: box = 128 bytes of columns (64 16-bit elements, or 128 FP8 codes) x box_rows x 1 head
 // x 2 (K, V) x 1 page, 128-byte swizzle; shared memory receives the K rows, then the V rows.

@@ -64,13 +64,16 @@ def test_host_validation_without_gpu(lib):
     assert lib.pkv_kv_cache_append(_cache(), good, good, good, good, good, -1, 4, 3, None) == 1
     # nothing to do is fine and launches nothing
     assert lib.pkv_kv_cache_append(_cache(), good, good, good, good, good, 1, 4, 0, None) == 0
-    # decode: Hq not a multiple of Hkv, unsupported group, out dtype
+    # decode: Hq not a multiple of Hkv, group unsupported over an FP8 cache, out dtype (a native
+    # cache takes any group; nothing here reaches a launch)
     F = ctypes.c_float
     args = lambda hq, out_dt=0: (_cache(), good, hq, good, good, 2, 4, F(0.1), 0, good, 1 << 20, good, out_dt, None,
                                  None)
+    fp8_args = lambda hq: (_cache(fmt=1, scales=4096), good, hq, good, good, 2, 4, F(0.1), 0, good, 1 << 20, good, 0,
+                           None, None)
     assert lib.pkv_paged_attn_decode(*args(3)) == 1
-    assert lib.pkv_paged_attn_decode(*args(6)) == 2      # group 3
-    assert lib.pkv_paged_attn_decode(*args(20)) == 2     # group 10: not a multiple of 8
+    assert lib.pkv_paged_attn_decode(*fp8_args(6)) == 2      # group 3
+    assert lib.pkv_paged_attn_decode(*fp8_args(20)) == 2     # group 10: not a multiple of 8
     # FP8 cache with head_dim 64: groups above 8 are not supported
     fp8_64 = (_cache(fmt=1, scales=4096, d=64), good, 32, good, good, 2, 4, F(0.1), 0, good, 1 << 20, good, 0, None,
               None)
@@ -118,8 +121,8 @@ def test_workspace_sizing_with_explicit_splits(lib):
     # capacity 512 * 16 = 8192 tokens in 4 splits of 2048: B * Hq * 4 * (D + 1) floats
     assert pkv.decode_split_tokens(16, 32, 32, 128, 16, 512, num_splits=4) == 2048
     assert pkv.decode_workspace_size(16, 32, 32, 128, 16, 512, num_splits=4) == 16 * 32 * 4 * 129 * 4
-    # split size is rounded up to the 64-token tile
-    assert pkv.decode_split_tokens(1, 8, 8, 64, 16, 10, num_splits=3) == 64
+    # split size is rounded up to 128 tokens (splits start at multiples of 128)
+    assert pkv.decode_split_tokens(1, 8, 8, 64, 16, 10, num_splits=3) == 128
 
 
 def test_device_slot_from_eight_threads(lib):

@@ -130,10 +130,12 @@ def test_fp8_decode_splits_fp32_output(num_splits):
 
 
 @pytest.mark.parametrize("bs", [128, 512])
-def test_fp8_decode_splits_not_multiples_of_the_tile(bs):
-    """Splits of 448 tokens (7 splits over 3072) start tiles at 64 mod 128 inside large pages."""
+def test_fp8_decode_seven_splits_in_large_pages(bs):
+    """7 requested splits over a 3072-token capacity: splits are rounded up to a multiple of 128
+    tokens (512 here, 6 splits), and inside 128- and 512-token pages a split's tiles start at
+    offsets 0 and 128..384 of a page."""
     p = problem(lens=[3000, 700, 129], hq=8, hkv=8, bs=bs, dtype=W.BF16, mb=3072 // bs)
-    assert pkv.decode_split_tokens(3, 8, 8, 128, bs, 3072 // bs, num_splits=7) % 128 == 64
+    assert pkv.decode_split_tokens(3, 8, 8, 128, bs, 3072 // bs, num_splits=7) == 512
     codes, scales = device_fp8(p)
     out, lse = decode(p, codes, scales, num_splits=7)
     ref, ref_lse = oracle.attention_of(p, host(codes, scales))

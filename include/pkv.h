@@ -131,8 +131,8 @@ PKV_API size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_
                                  int block_size, int max_blocks_per_seq, int num_splits);
 
 /* Tokens per split that pkv_paged_attn_decode uses for these sizes (a multiple of
- * its 64-token tile, and at least capacity / 2048 so that a context has at most 2048
- * splits); a context of L tokens is cut into ceil(L / chunk) splits. */
+ * 128, and at least capacity / 2048 so that a context has at most 2048 splits); a
+ * context of L tokens is cut into ceil(L / chunk) splits. */
 PKV_API int pkv_decode_split_tokens(int batch, int num_q_heads, int num_kv_heads, int head_dim,
                             int block_size, int max_blocks_per_seq, int num_splits);
 
@@ -150,8 +150,12 @@ PKV_API int pkv_decode_split_tokens(int batch, int num_q_heads, int num_kv_heads
  *                 (FP32 partial outputs and their lse); contents need no init.
  *   out           [batch, Hq, D] in out_dtype (the cache dtype or PKV_F32).
  *   lse           FP32 [batch, Hq] or NULL.
+ *   num_q_heads   any multiple of the cache's num_kv_heads (any group size); over an
+ *                 FP8 cache the group must be 1, 2, 4 or a multiple of 8 (head_dim 64:
+ *                 at most 8), else PKV_ERR_UNSUPPORTED.
+ *   batch         any size: batches run in slices of up to 2048 sequences.
  * Launches the split kernel and, when some context spans several splits, the
- * merge of pkv_attn_combine on the same stream. */
+ * merge of pkv_attn_combine on the same stream (once per slice). */
 PKV_API pkv_status pkv_paged_attn_decode(pkv_cache cache, const void *q, int num_q_heads,
                                  const int *block_tables, const int *context_lens, int batch,
                                  int max_blocks_per_seq, float scale, int num_splits,

@@ -235,7 +235,6 @@ pkv_status decode_impl(const pkv_cache &cache, const void *q, int num_q_heads, c
     // at most 8); a native cache: any group
     if (fp8 && group != 1 && group != 2 && group != 4 && group % 8 != 0) return PKV_ERR_UNSUPPORTED;
     if (fp8 && group > 8 && cache.head_dim != 128) return PKV_ERR_UNSUPPORTED;
-    if (batch > decode_max_batch()) return PKV_ERR_UNSUPPORTED;
     if (batch == 0) return PKV_OK;
     if (!q || !block_tables || !context_lens || !out) return PKV_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(out) || (lse && !aligned16(lse))) return PKV_ERR_INVALID_ARG;
@@ -294,29 +293,57 @@ pkv_status decode_impl(const pkv_cache &cache, const void *q, int num_q_heads, c
     a.err = s->err_ptr;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const int grid = s->info.num_sms * s->info.decode_ctas_per_sm;
-    cudaError_t le;
-    switch (path) {
-        case kFp8Tensor: le = launch_decode_fp8(a, grid, cs); break;
-        case kMmaSync: le = launch_decode_gqa(a, grid, cs); break;
-        case kTcgen05: le = launch_decode_tc(a, grid, cs); break;
-        default: le = launch_decode(a, grid, cs); break;
+    // The kernels keep a launch's unit tables in shared memory, so a batch runs in slices of at
+    // most decode_max_batch() sequences, each a decode of its own (the split size and the
+    // workspace layout [batch, Hq, s_max, ...] are the whole batch's; a slice's partials start at
+    // its first sequence's). A mixed batch's rows are absolute (cu_q_lens), so only cu_q_lens moves.
+    const size_t qe = 2, oe = out_dtype == PKV_F32 ? 4 : 2;  // element sizes of q and out
+    // sequences a launch: at most decode_max_batch(), and unit tables (3 ints a sequence, 2 a split)
+    // of at most 24 KB, which every decode kernel's shared-memory layout leaves room for
+    int slice = (6144 - 2 * (s_max + 1)) / 3;
+    slice = slice < 1 ? 1 : (slice > decode_max_batch() ? decode_max_batch() : slice);
+    for (int b0 = 0; b0 < batch; b0 += slice) {
+        const int nb = batch - b0 < slice ? batch - b0 : slice;
+        DecodeArgs d = a;
+        d.batch = nb;
+        d.block_tables = block_tables + (size_t)b0 * max_blocks_per_seq;
+        d.context_lens = context_lens + b0;
+        if (cu_q_lens) {
+            d.cu_q_lens = cu_q_lens + b0;
+        } else {
+            d.q = static_cast<const uint8_t *>(q) + (size_t)b0 * num_q_heads * cache.head_dim * qe;
+            d.q_rows = nb;
+            d.out = static_cast<uint8_t *>(out) + (size_t)b0 * num_q_heads * cache.head_dim * oe;
+            d.lse = lse ? lse + (size_t)b0 * num_q_heads : nullptr;
+        }
+        if (need > 0) {
+            d.part_o = a.part_o + (size_t)b0 * num_q_heads * s_max * cache.head_dim;
+            d.part_lse = a.part_lse + (size_t)b0 * num_q_heads * s_max;
+        }
+        cudaError_t le;
+        switch (path) {
+            case kFp8Tensor: le = launch_decode_fp8(d, grid, cs); break;
+            case kMmaSync: le = launch_decode_gqa(d, grid, cs); break;
+            case kTcgen05: le = launch_decode_tc(d, grid, cs); break;
+            default: le = launch_decode(d, grid, cs); break;
+        }
+        if (le != cudaSuccess) return PKV_ERR_CUDA;
+        // Rows that span several splits (and empty rows) are finished by the merge.
+        CombineArgs c;
+        c.part_o = d.part_o;
+        c.part_lse = d.part_lse;
+        c.n_rows = nb * num_q_heads;
+        c.num_splits = s_max;
+        c.head_dim = cache.head_dim;
+        c.context_lens = d.context_lens;
+        c.rows_per_seq = num_q_heads;
+        c.chunk = chunk;
+        c.cu_q_lens = d.cu_q_lens;
+        c.out = d.out;
+        c.out_dtype = (int)out_dtype;
+        c.lse = d.lse;
+        if (launch_combine(c, cs) != cudaSuccess) return PKV_ERR_CUDA;
     }
-    if (le != cudaSuccess) return PKV_ERR_CUDA;
-    // Rows that span several splits (and empty rows) are finished by the merge.
-    CombineArgs c;
-    c.part_o = a.part_o;
-    c.part_lse = a.part_lse;
-    c.n_rows = batch * num_q_heads;
-    c.num_splits = s_max;
-    c.head_dim = cache.head_dim;
-    c.context_lens = context_lens;
-    c.rows_per_seq = num_q_heads;
-    c.chunk = chunk;
-    c.cu_q_lens = cu_q_lens;
-    c.out = out;
-    c.out_dtype = (int)out_dtype;
-    c.lse = lse;
-    if (launch_combine(c, cs) != cudaSuccess) return PKV_ERR_CUDA;
     return PKV_OK;
 }
 

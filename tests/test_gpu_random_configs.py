@@ -91,13 +91,18 @@ def sample_rows(p, rng, full_below=64):
 
 
 @pytest.mark.parametrize("fmt", ["native", "fp8"])
-@pytest.mark.parametrize("i", range(12))
+@pytest.mark.parametrize("i", range(16))
 def test_random_decode(fmt, i):
     rng = np.random.default_rng(1000 + i + (500 if fmt == "fp8" else 0))
     d = int(rng.choice([64, 128]))
     bs = int(rng.choice(BLOCK_SIZES))
-    groups = GROUPS_FP8_D64 if (fmt == "fp8" and d == 64) else GROUPS_DECODE
-    hq, hkv = groups[int(rng.integers(0, len(groups)))]
+    if fmt == "native":
+        # any group 1..48 (uneven ones included) over 1, 2, 3, 4 or 8 KV heads
+        hkv = int(rng.choice([1, 2, 3, 4, 8]))
+        hq = hkv * int(rng.integers(1, 49 if hkv <= 2 else 17))
+    else:
+        groups = GROUPS_FP8_D64 if d == 64 else GROUPS_DECODE
+        hq, hkv = groups[int(rng.integers(0, len(groups)))]
     dtype = W.F16 if rng.integers(0, 2) else W.BF16
     lens = draw_lengths(rng, int(rng.integers(1, 7)), 2500, bs)
     splits = int(rng.choice([0, 0, 1, 3, 7]))
@@ -177,3 +182,42 @@ def test_random_mixed(i):
         compare(p, out, lse, host, 1, what + " (decode rows)", rows=dec)
     if chunk:
         compare(p, out, lse, host, 2, what + " (chunk rows)", rows=chunk)
+
+
+@pytest.mark.parametrize("hq,hkv,fmt", [(4, 4, "native"), (8, 2, "native"), (12, 2, "native"), (8, 8, "fp8")])
+def test_decode_batches_above_2048(hq, hkv, fmt):
+    """Batches of more than 2048 sequences run in slices (the unit tables of a launch live in
+    shared memory): 4100 short contexts (0..300 tokens, one of them empty) through the MHA, the
+    mma.sync group, the tcgen05 and the FP8 kernels, with forced splits, every row checked."""
+    rng = np.random.default_rng(77 + hq)
+    lens = [int(x) for x in rng.integers(0, 301, 4100)]
+    lens[5] = 0
+    p = make(rng, lens=lens, q_lens=[1] * len(lens), hq=hq, hkv=hkv, d=64, bs=16, dtype=W.BF16, causal=False,
+             kv_format=fmt, seed=91 + hq)
+    cache, scales, host = on_device(p)
+    lse = torch.empty((p.batch, hq), dtype=torch.float32, device="cuda")
+    out = pkv.paged_attn_decode(cache, to_dev(p.q), to_dev(p.block_tables), to_dev(p.context_lens), scale=p.scale,
+                                num_splits=3, lse=lse, scales=scales)
+    torch.cuda.synchronize()
+    compare(p, out, lse, host, 1, "batch 4100 %d/%d %s" % (hq, hkv, fmt))
+
+
+def test_mixed_call_batch_above_2048():
+    """A mixed call of 2500 sequences (decode rows and short chunks): the decode rows run in
+    slices, their rows found through cu_q_lens."""
+    rng = np.random.default_rng(5)
+    lens = [int(x) for x in rng.integers(1, 200, 2500)]
+    q_lens = [1 if rng.integers(0, 4) else int(min(L, rng.integers(2, 20))) for L in lens]
+    p = make(rng, lens=lens, q_lens=q_lens, hq=6, hkv=2, d=64, bs=16, dtype=W.F16, causal=True, kv_format="native",
+             seed=17)
+    cache, scales, host = on_device(p)
+    out = torch.full((p.total_q, 6, 64), float("nan"), dtype=p.q.dtype, device="cuda")
+    lse = torch.full((p.total_q, 6), float("nan"), dtype=torch.float32, device="cuda")
+    pkv.paged_attn_mixed(cache, to_dev(p.q), to_dev(p.cu_q_lens), to_dev(p.context_lens), to_dev(p.block_tables),
+                         max_q_len=max(q_lens), scale=p.scale, causal=True, num_splits=2, out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert not torch.isnan(out).any()
+    single = {p.cu_q_lens[b].item() for b in range(p.batch) if q_lens[b] == 1}
+    rows = list(range(p.total_q))
+    compare(p, out, lse, host, 1, "mixed 2500 decode rows", rows=[r for r in rows if r in single])
+    compare(p, out, lse, host, 2, "mixed 2500 chunk rows", rows=[r for r in rows if r not in single])

@@ -256,6 +256,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::mma_commit(&kv_empty[t % ring]);  // the slot's K and V are both done
                 return true;
             };
+            // the tile whose P V is still to be issued: after the next tile's QK, also across units
+            bool pending = false, pend_first = false;
+            uint32_t pend_t = 0, pend_o = 0;
             for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x, ++U) {
                 const UnitCursor c = unit_of(u, ut, a.s_max, hu, chunk);
                 const int ntiles = (c.t1 - c.t0 + kBN - 1) / kBN;
@@ -282,10 +285,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::mma_commit(&s_full[T & 1u]);
                     if (k == ntiles - 1) tc::mma_commit(&q_empty[qb]);  // every QK of the unit issued
                     // the previous tile's P V (its softmax overlapped this QK)
-                    if (k > 0 && !(ok = pv(T - 1, tO, k == 1))) break;
+                    if (pending && !(ok = pv(pend_t, pend_o, pend_first))) break;
+                    pending = true;
+                    pend_t = T;
+                    pend_o = tO;
+                    pend_first = (k == 0);
                 }
-                if (ok) ok = pv(T - 1, tO, ntiles == 1);
             }
+            if (ok && pending) ok = pv(pend_t, pend_o, pend_first);
             tc::mma_commit(drain);
             volatile int no_abort = 0;
             mbar_wait(drain, 0, &no_abort, a.err);
@@ -298,6 +305,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float c2 = a.scale * kLog2e;
         uint32_t T = 0, U = 0;
         bool ok = true;
+        // a finished unit whose epilogue is still to run
+        struct Done {
+            UnitCursor c;
+            uint32_t U, t_last;
+            float m, l;
+        };
+        bool have_prev = false;
+        Done prev = {};
+        // O / l of unit d once its last P V is done: the output of a single-split context, or the
+        // split's partial and lse; then O_{d.U % 2} is free for the unit after next
+        auto epilogue = [&](const Done &d) -> bool {
+            if (!mbar_wait(&o_done[d.t_last & 1u], (d.t_last >> 1) & 1u, abort_flag, a.err)) return false;
+            tc::fence_after_sync();
+            const uint32_t tOd = tmem + kColO + 128u * (d.U & 1u) + lane_base;
+            const int splits = (ut.lens[d.c.b] + chunk - 1) / chunk;
+            const bool row_ok = r < gu;
+            const float inv = d.l > 0.f ? 1.f / d.l : 0.f;
+            const float lse_v = d.l > 0.f ? (d.m + __log2f(d.l)) * kLn2 : -INFINITY;
+            const size_t h = (size_t)d.c.kvh * gu + r;  // query head
+            const size_t orow = (size_t)ut.qrow[d.c.b] * a.num_q_heads + h;
+            const size_t prow = (size_t)d.c.b * a.num_q_heads + h;
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+                float o[32];
+                tc::tmem_ld32(tOd + cc * 32, o);
+                tc::tmem_wait_ld();
+                if (row_ok) {
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        const float x[4] = {o[4 * v] * inv, o[4 * v + 1] * inv, o[4 * v + 2] * inv,
+                                            o[4 * v + 3] * inv};
+                        if (splits == 1) store_out_vec<4>(a.out, orow * D + cc * 32 + 4 * v, x, a.out_dtype);
+                        else store_out_vec<4>(a.part_o, (prow * a.s_max + d.c.split) * D + cc * 32 + 4 * v, x, 2);
+                    }
+                }
+            }
+            if (row_ok) {
+                if (splits == 1) {
+                    if (a.lse) a.lse[orow] = lse_v;
+                } else {
+                    a.part_lse[prow * a.s_max + d.c.split] = lse_v;
+                }
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&o_empty[d.U & 1u]);
+            return true;
+        };
         for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x, ++U) {
             const UnitCursor c = unit_of(u, ut, a.s_max, hu, chunk);
             const int ntiles = (c.t1 - c.t0 + kBN - 1) / kBN;
@@ -385,43 +440,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[T & 1u]);
+                if (k == 0 && have_prev) {
+                    have_prev = false;
+                    if (!(ok = epilogue(prev))) break;
+                }
             }
             if (!ok) break;
-            // ---- epilogue: O / l of this unit, once its last P V is done ----
-            if (!(ok = mbar_wait(&o_done[(T - 1) & 1u], ((T - 1) >> 1) & 1u, abort_flag, a.err))) break;
-            tc::fence_after_sync();
-            const int splits = (ut.lens[c.b] + chunk - 1) / chunk;
-            const bool row_ok = r < gu;
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            const float lse_v = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
-            const size_t h = (size_t)c.kvh * gu + r;  // query head
-            const size_t orow = (size_t)ut.qrow[c.b] * a.num_q_heads + h;
-            const size_t prow = (size_t)c.b * a.num_q_heads + h;
-#pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
-                float o[32];
-                tc::tmem_ld32(tO + cc * 32, o);
-                tc::tmem_wait_ld();
-                if (row_ok) {
-#pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        const float x[4] = {o[4 * v] * inv, o[4 * v + 1] * inv, o[4 * v + 2] * inv, o[4 * v + 3] * inv};
-                        if (splits == 1) store_out_vec<4>(a.out, orow * D + cc * 32 + 4 * v, x, a.out_dtype);
-                        else store_out_vec<4>(a.part_o, (prow * a.s_max + c.split) * D + cc * 32 + 4 * v, x, 2);
-                    }
-                }
-            }
-            if (row_ok) {
-                if (splits == 1) {
-                    if (a.lse) a.lse[orow] = lse_v;
-                } else {
-                    a.part_lse[prow * a.s_max + c.split] = lse_v;
-                }
-            }
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&o_empty[U & 1u]);
+            // this unit's epilogue runs after the next unit's first tile (or at the end): its last
+            // P V is issued after that tile's QK, so by then it is done and nothing waits on it
+            have_prev = true;
+            prev = {c, U, T - 1, m, l};
         }
+        if (ok && have_prev) ok = epilogue(prev);
     }
     tc::fence_before_sync();
     __syncthreads();

@@ -45,6 +45,9 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-full", action="store_true",
+                    help="time the oracle on every workload in full (the long prefill: minutes), not on bounded "
+                         "samples")
     ap.add_argument("--only", default="", help="comma list of extra workloads (bs_sweep,mixed,prefix,fp8,mqa,mixed_call,prefill,prefill_fp8)")
     ap.add_argument("--profile", choices=["decode", "append", "prefill", "decode_mixed", "decode_prefix", "decode_fp8",
                                           "prefill_fp8", "decode_mqa"],
@@ -427,6 +430,95 @@ def cpu_baseline_decode(p, budget_s=8.0):
                       % (p.batch, p.num_q_heads, int(p.context_lens.sum()), reps, t, t_build)}
 
 
+def cpu_model() -> str:
+    """The host CPU's name as the OS reports it."""
+    try:
+        for line in open("/proc/cpuinfo"):
+            key = line.split(":", 1)[0].strip().lower()
+            if key in ("model name", "cpu model", "hardware"):
+                return line.split(":", 1)[1].strip()
+        # Arm: no model name line; the part number identifies the core
+        parts = {line.split(":", 1)[1].strip() for line in open("/proc/cpuinfo") if line.startswith("CPU part")}
+        impl = {line.split(":", 1)[1].strip() for line in open("/proc/cpuinfo") if line.startswith("CPU implementer")}
+        if parts:
+            names = {"0xd4f": "Neoverse V2", "0xd40": "Neoverse V1", "0xd0c": "Neoverse N1", "0xd49": "Neoverse N2",
+                     "0xd8e": "Neoverse N3", "0xd83": "Neoverse V3"}
+            known = ", ".join(sorted({names[p] for p in parts if p in names}))
+            return "Arm %s(implementer %s, part %s)" % (known + " " if known else "", ",".join(sorted(impl)),
+                                                         ",".join(sorted(parts)))
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def oracle_seconds(fn, budget_s):
+    """Seconds per call of fn: repeated until budget_s of wall time (at least once)."""
+    reps, t = 0, 0.0
+    while reps == 0 or (t < budget_s and reps < 20):
+        t0 = time.time()
+        fn()
+        t += time.time() - t0
+        reps += 1
+    return t / reps, reps
+
+
+def cpu_baseline_breadth(torch, p7b, full=False, budget_s=2.5):
+    """The oracle as it stands, at one thread and at all host cores, on the workloads of the GPU
+    lines (same generators and seeds). Decode workloads run in full; the long prefill (2.2 TFLOP in
+    fp64) on a seeded sample of its query rows: 1/16 at all cores and 1/256 at one thread, or with
+    full all rows and 1/16 (about a minute each on 16 cores). Returns {workload: {threads: {...}}};
+    values in the GPU line's unit."""
+    import numpy as np
+
+    import oracle
+    from paged_kv_flash_cache_gb300 import workloads as W
+    oracle.build()
+    cores = os.cpu_count() or 1
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    res = {}
+
+    def decode_case(name, p, note):
+        cache = oracle.build_cache(p)
+        ent = {}
+        for thr in (1, cores):
+            sec, reps = oracle_seconds(lambda: oracle.attention_of(p, cache, nthreads=thr), budget_s)
+            ent["%d_thread%s" % (thr, "" if thr == 1 else "s")] = {
+                "value": round(p.kv_bytes_read() / sec / 1e9, 3), "unit": "GB/s of K/V", "threads": thr,
+                "seconds_per_call": round(sec, 3), "calls": reps, "sample": "whole batch: " + note}
+        del cache
+        res[name] = ent
+
+    dec, pre = W.tiny()
+    decode_case("tiny_decode", dec, "2 sequences (37, 100 tokens), 4 heads x 64, fp16, bs 16")
+    decode_case("decode_7b", p7b, "16 sequences U[1024, 8192], 32 heads x 128, fp16, bs 16")
+    decode_case("bs_sweep_16", W.bs_sweep(16, kv_data=W.bs_sweep_kv(device=dev), pool_init="none", device=dev),
+                "32 x 4096 tokens, 32 heads x 128, fp16, bs 16 (one page size of the sweep)")
+    decode_case("mixed", W.mixed_serving(pool_init="none", device=dev),
+                "64 lognormal contexts, 32 q / 8 kv heads x 128, bf16, bs 32")
+    # long causal prefill: TFLOP/s over the sampled rows (4 D Hq per row and key it sees)
+    p = W.prefill_long(device=dev)
+    cache = oracle.build_cache(p)
+    total_rows = int(p.q_lens.sum())
+    gen = np.random.default_rng(3)
+    ent = {}
+    for thr, frac in ((cores, 1 if full else 16), (1, 16 if full else 256)):
+        rows = np.sort(gen.choice(total_rows, total_rows // frac, replace=False))
+        pos = rows % 8192                              # absolute position: row r sees keys 0 .. pos
+        flops = float(np.sum(pos + 1)) * 4 * p.head_dim * p.num_q_heads
+        sec, reps = oracle_seconds(
+            lambda: oracle.paged_attention(p.dtype, cache, p.q, p.num_q_heads, p.cu_q_lens, p.context_lens,
+                                           p.block_tables, p.scale, True, rows=rows, nthreads=thr), 0.0)
+        ent["%d_thread%s" % (thr, "" if thr == 1 else "s")] = {
+            "value": round(flops / sec / 1e12, 6), "unit": "TFLOP/s (causal)", "threads": thr,
+            "seconds_per_call": round(sec, 3), "calls": reps,
+            "sample": "%s of the 4 x 8192 query rows (%d rows, seeded), all 32 heads, bf16, bs 16 pages"
+                      % ("all" if frac == 1 else "1/%d" % frac, rows.size)}
+    del cache
+    res["prefill_long"] = ent
+    return res
+
+
 def bench_bs_sweep(torch, steps, warmup):
     import paged_kv_flash_cache_gb300 as pkv
     from paged_kv_flash_cache_gb300 import workloads as W
@@ -807,6 +899,16 @@ def main():
         line["extra"] = extra
     if dist.rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_decode(p)
+        line["cpu_baseline"]["cpu_model"] = cpu_model()
+        try:
+            breadth = cpu_baseline_breadth(torch, p, full=args.cpu_full)
+            line["cpu_baseline"]["by_workload"] = breadth
+            # beside each GPU line: the oracle on the same workload
+            for name, key in (("bs_sweep", "bs_sweep_16"), ("mixed", "mixed"), ("prefill", "prefill_long")):
+                if isinstance(line.get("extra", {}).get(name), dict) and key in breadth:
+                    line["extra"][name]["oracle"] = breadth[key]
+        except Exception as e:  # the baseline's breadth must not hide the headline line
+            line["cpu_baseline"]["by_workload"] = {"error": "%s: %s" % (type(e).__name__, str(e)[:200])}
     if dist.rank == 0:
         print(json.dumps(line))
     dist.close()

@@ -397,7 +397,6 @@ pkv_status prefill_impl(const pkv_cache &cache, const void *q, int num_q_heads, 
                         float *lse, void *stream, int skip_single) {
     pkv_status st = check_cache(cache);
     if (st != PKV_OK) return st;
-    if (cache.format == PKV_KV_FP8_E4M3 && cache.head_dim != 128) return PKV_ERR_UNSUPPORTED;
     if ((st = check_out_dtype(out_dtype, cache.dtype)) != PKV_OK) return st;
     if (batch < 0 || max_blocks_per_seq <= 0 || num_q_heads <= 0 || total_q < 0 || max_q_len < 0)
         return PKV_ERR_INVALID_ARG;

@@ -62,13 +62,21 @@ struct PrefillLayout {
     static constexpr uint32_t kQOff = 0;
     static constexpr uint32_t kRingOff = 2 * kQBytes;
     static constexpr uint32_t kBarOff = kRingOff + kRing * kKVBytes;
-    // FP8 cache: the codes of a ring item land in its slot's upper half (128 rows x 128 bytes,
-    // where the f16 tile's second 64-column half goes) and its row scales in a scale slot
-    static constexpr uint32_t kCodeOff = kTileHalf;             // within a ring slot
+    // FP8 cache: the codes of a ring item (128 rows of D bytes) land, for D = 128, in its slot's
+    // upper half (where the f16 tile's second 64-column half goes; converted in place), for D = 64
+    // in a code buffer of their own (64-byte rows, unswizzled); its row scales in a scale slot
+    static constexpr bool kCodesApart = FP8 && D == 64;
+    static constexpr uint32_t kCodeOff = kTileHalf;             // within a ring slot (D = 128)
     static constexpr uint32_t kScaleOff = kBarOff + 256;        // [kRing][128] FP32
     // the K row scales of key tile j times the softmax's log2 scale, at [j % 4][128] FP32
     static constexpr uint32_t kKScaleOff = kScaleOff + kRing * 128 * 4;
-    static constexpr uint32_t kSmemBytes = kBarOff + 256 + (FP8 ? 2 * kRing * 128 * 4 : 0) + 1024;  // + alignment slack
+    static constexpr uint32_t kCodeBufOff = kKScaleOff + kRing * 128 * 4;  // [kRing][128 x 64 B] (D = 64)
+    static constexpr uint32_t kSmemBytes = kBarOff + 256 + (FP8 ? 2 * kRing * 128 * 4 : 0) +
+                                           (kCodesApart ? kRing * 128 * 64 : 0) + 1024;  // + alignment slack
+    // the codes of ring slot `slot`
+    __device__ static uint8_t *codes(uint8_t *smem, uint8_t *ring, int slot) {
+        return kCodesApart ? smem + kCodeBufOff + slot * (128 * 64) : ring + slot * kKVBytes + kCodeOff;
+    }
     static constexpr uint32_t kTmemCols = 512;
 };
 
@@ -158,16 +166,22 @@ __device__ __forceinline__ float pow2_ceil(float x) {
     return __uint_as_float(b);
 }
 
-// In place, over an FP8 cache: the E4M3 codes of row r of a ring item (the slot's upper half, 128
-// bytes a row) become the f16 row r (values times 2^-8, see e4m3x4_to_f16) of the layout TMA
-// writes for a 16-bit cache (two 64-column halves, 128-byte swizzle); rows at or beyond zero_from
-// become zero. A pass takes 8 rows g .. g + 7 (g a multiple of 8): lane -> rows rr and rr + 4
-// (rr = lane / 8), 16-code chunk c = lane % 8, so every swizzled address is a lane constant plus
-// 1 KB a pass. A row is read entirely before any of it is written (its codes sit where its
-// second f16 half goes). The lanes of the two halves store opposite chunks first: the 8 stores
-// of a row in one instruction then fill all 32 banks once.
-template <uint32_t kCodeOff, uint32_t kTileHalf>
-struct RowConverter {
+// Over an FP8 cache: the E4M3 codes of row r of a ring item become the f16 row r (values times
+// 2^-8, see e4m3x4_to_f16) of the layout TMA writes for a 16-bit cache (64-column halves of
+// 128-byte rows, 128-byte swizzle); rows at or beyond zero_from become zero. A pass takes 8 rows
+// g .. g + 7 (g a multiple of 8), and every swizzled address is a lane constant plus 1 KB a pass.
+//   D = 128: the codes (128 bytes a row, swizzled like an f16 half by TMA) sit where the row's
+//   second f16 half goes, so the pass converts in place: lane -> rows rr and rr + 4 (rr = lane /
+//   8), 16-code chunk c = lane % 8; a row is read entirely before any of it is written. The lanes
+//   of the two halves store opposite chunks first: the 8 stores of a row in one instruction then
+//   fill all 32 banks once.
+//   D = 64: the codes come from a buffer of their own (64 bytes a row, unswizzled): lane -> row
+//   rr = lane / 4, 16-code chunk c = lane % 4, written as f16 chunks 2c and 2c + 1.
+template <int D, uint32_t kTileHalf>
+struct RowConverter;
+
+template <uint32_t kTileHalf>
+struct RowConverter<128, kTileHalf> {
     uint32_t ld[2], sta[2], stb[2];
     int rr, hf;
     __device__ __forceinline__ explicit RowConverter(int lane) {
@@ -179,16 +193,16 @@ struct RowConverter {
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             const int rw = rr + 4 * i;  // == row & 7
-            ld[i] = kCodeOff + rw * 128u + ((c ^ rw) << 4);
+            ld[i] = rw * 128u + ((c ^ rw) << 4);
             sta[i] = hf * kTileHalf + rw * 128u + ((ka ^ rw) << 4);
             stb[i] = hf * kTileHalf + rw * 128u + ((kb ^ rw) << 4);
         }
     }
-    __device__ __forceinline__ void pass(uint8_t *base, int g, int zero_from) const {
+    __device__ __forceinline__ void pass(const uint8_t *codes, uint8_t *f16, int g, int zero_from) const {
         const uint32_t grp = (uint32_t)g * 128u;
         uint4 raw[2];
 #pragma unroll
-        for (int i = 0; i < 2; ++i) raw[i] = *reinterpret_cast<const uint4 *>(base + grp + ld[i]);
+        for (int i = 0; i < 2; ++i) raw[i] = *reinterpret_cast<const uint4 *>(codes + grp + ld[i]);
         __syncwarp();
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
@@ -203,9 +217,37 @@ struct RowConverter {
             }
             const uint4 v0 = make_uint4(h16[0], h16[1], h16[2], h16[3]);
             const uint4 v1 = make_uint4(h16[4], h16[5], h16[6], h16[7]);
-            *reinterpret_cast<uint4 *>(base + grp + sta[i]) = hf ? v1 : v0;
-            *reinterpret_cast<uint4 *>(base + grp + stb[i]) = hf ? v0 : v1;
+            *reinterpret_cast<uint4 *>(f16 + grp + sta[i]) = hf ? v1 : v0;
+            *reinterpret_cast<uint4 *>(f16 + grp + stb[i]) = hf ? v0 : v1;
         }
+    }
+};
+
+template <uint32_t kTileHalf>
+struct RowConverter<64, kTileHalf> {
+    uint32_t ld, sta, stb;
+    int rr;
+    __device__ __forceinline__ explicit RowConverter(int lane) {
+        const int c = lane & 3;
+        rr = lane >> 2;  // == row & 7
+        ld = rr * 64u + c * 16u;
+        sta = rr * 128u + (((2 * c) ^ rr) << 4);
+        stb = rr * 128u + (((2 * c + 1) ^ rr) << 4);
+    }
+    __device__ __forceinline__ void pass(const uint8_t *codes, uint8_t *f16, int g, int zero_from) const {
+        const uint4 raw = *reinterpret_cast<const uint4 *>(codes + (uint32_t)g * 64u + ld);
+        uint32_t h16[8];
+        e4m3x4_to_f16(raw.x, h16[0], h16[1]);
+        e4m3x4_to_f16(raw.y, h16[2], h16[3]);
+        e4m3x4_to_f16(raw.z, h16[4], h16[5]);
+        e4m3x4_to_f16(raw.w, h16[6], h16[7]);
+        if (g + rr >= zero_from) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) h16[k] = 0u;
+        }
+        const uint32_t grp = (uint32_t)g * 128u;
+        *reinterpret_cast<uint4 *>(f16 + grp + sta) = make_uint4(h16[0], h16[1], h16[2], h16[3]);
+        *reinterpret_cast<uint4 *>(f16 + grp + stb) = make_uint4(h16[4], h16[5], h16[6], h16[7]);
     }
 };
 
@@ -333,12 +375,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t *dst0 = sRing + slot * Lay::kKVBytes;
                     if constexpr (FP8) {
                         // codes (one 128-byte box row per token) and row scales of each page slice
-                        if (lane == 0) mbar_arrive_expect_tx(&kv_code[slot], (uint32_t)npages * box_rows * (128u + 4u));
+                        if (lane == 0) mbar_arrive_expect_tx(&kv_code[slot], (uint32_t)npages * box_rows * (D + 4u));
                         __syncwarp();
                         if (lane < npages) {
                             const int row = ((pb * 2 + kv) * p.num_kv_heads + g) * p.bs + off;
                             const uint32_t dst = (uint32_t)lane * box_rows;
-                            tc::tma_load_2d(dst0 + Lay::kCodeOff + dst * 128u, &tm_kv, 0, row, &kv_code[slot]);
+                            tc::tma_load_2d(Lay::codes(smem, sRing, slot) + dst * D, &tm_kv, 0, row, &kv_code[slot]);
                             bulk_g2s(smem + Lay::kScaleOff + (slot * 128u + dst) * 4u, p.scales + row,
                                      (uint32_t)box_rows * 4u, &kv_code[slot], l2_policy_evict_first());
                         }
@@ -376,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the softmax folds r into P, and O carries the factor W (rescaled exactly when W
             // grows).
             const int cw = warp - 2;
-            const RowConverter<Lay::kCodeOff, Lay::kTileHalf> conv(lane);
+            const RowConverter<D, Lay::kTileHalf> conv(lane);
             bool cok = mbar_wait(q_full, 0, abort_flag, p.err);
             if (BF16 && cok) {
                 // q to f16 in place (exact for |q| within f16's range)
@@ -412,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (lane == 0) mbar_arrive(&ks_ready[(u >> 1) & 3]);
                     }
                     for (int g = cw * 64; g < cw * 64 + 64; g += 8)
-                        conv.pass(sRing + slot * Lay::kKVBytes, g, kBN);
+                        conv.pass(Lay::codes(smem, sRing, slot), sRing + slot * Lay::kKVBytes, g, kBN);
                     tc::fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&kv_full[slot]);
@@ -526,14 +568,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // of 8 rows; rows beyond the context zeroed), V_0 before the first key tile and V_{j+1}
         // right after tile j: V_{j+1}'s codes land while the softmax works on tile j, and the P
         // V_{j+1} MMAs need it only after the softmax of tile j + 1
-        const RowConverter<Lay::kCodeOff, Lay::kTileHalf> vconv(lane);
+        const RowConverter<D, Lay::kTileHalf> vconv(lane);
         auto convert_v = [&](int jv) -> bool {
             const uint32_t uV = 2u * jv + 1, vslot = uV % kRing;
             if (!mbar_wait(&kv_code[vslot], (uV / kRing) & 1u, abort_flag, p.err)) return false;
             const int g = (x * 4 + quarter) * 16;
             uint8_t *vb = sRing + vslot * Lay::kKVBytes;
-            vconv.pass(vb, g, L - jv * kBN);
-            vconv.pass(vb, g + 8, L - jv * kBN);
+            const uint8_t *vc = Lay::codes(smem, sRing, vslot);
+            vconv.pass(vc, vb, g, L - jv * kBN);
+            vconv.pass(vc, vb, g + 8, L - jv * kBN);
             tc::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&kv_full[vslot]);
@@ -765,20 +808,22 @@ EncodeTiledFn encode_fn() {
 cudaError_t encode_cache_map(const CacheView &c, int box_rows, CUtensorMap *map) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
-    // 16-bit elements: boxes of 64 columns (128 bytes); FP8 codes: boxes of 128 one-byte columns
-    // (head_dim 128), so every box row is one 128-byte swizzle atom either way
-    if (c.fp8 && c.head_dim != 128) return cudaErrorNotSupported;
+    // 16-bit elements: boxes of 64 columns (128 bytes); FP8 codes, head_dim 128: boxes of 128
+    // one-byte columns, so every box row is one 128-byte swizzle atom either way; FP8 codes,
+    // head_dim 64: boxes of 64-byte rows, unswizzled
+    const bool codes64 = c.fp8 && c.head_dim == 64;
+    if (c.fp8 && c.head_dim != 128 && !codes64) return cudaErrorNotSupported;
     const CUtensorMapDataType dt = c.fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                  : c.dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const cuuint64_t nrows = (cuuint64_t)c.num_blocks * 2 * c.num_kv_heads * c.block_size;
     if (nrows > 0x7fffffffull || nrows == 0) return cudaErrorNotSupported;  // TMA row coordinates are int32
     cuuint64_t dims[2] = {(cuuint64_t)c.head_dim, nrows};
     cuuint64_t strides[1] = {(cuuint64_t)c.head_dim * (c.fp8 ? 1 : 2)};
-    cuuint32_t box[2] = {c.fp8 ? 128u : 64u, (cuuint32_t)box_rows};
+    cuuint32_t box[2] = {c.fp8 ? (cuuint32_t)c.head_dim : 64u, (cuuint32_t)box_rows};
     cuuint32_t es[2] = {1, 1};
     if (enc(map, dt, 2, const_cast<void *>(c.ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
-        CUDA_SUCCESS)
+            codes64 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     return cudaSuccess;
 }
@@ -929,8 +974,8 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t s) {
     if (a.max_q_len == 0) return cudaSuccess;
     const bool bf16 = a.cache.dtype == 1;
     if (a.cache.fp8) {
-        if (a.cache.head_dim != 128) return cudaErrorNotSupported;
-        return bf16 ? launch_t<128, true, true>(a, s) : launch_t<128, false, true>(a, s);
+        if (a.cache.head_dim == 128) return bf16 ? launch_t<128, true, true>(a, s) : launch_t<128, false, true>(a, s);
+        return bf16 ? launch_t<64, true, true>(a, s) : launch_t<64, false, true>(a, s);
     }
     if (a.cache.head_dim == 128) return bf16 ? launch_t<128, true, false>(a, s) : launch_t<128, false, false>(a, s);
     return bf16 ? launch_t<64, true, false>(a, s) : launch_t<64, false, false>(a, s);

@@ -102,8 +102,8 @@ def test_fp8_cache_validation_without_gpu(lib):
     assert lib.pkv_kv_cache_append(_cache(fmt=7, scales=4096), good, good, good, good, good, 1, 4, 3, None) == 2
     # nothing to append: accepted, nothing launched
     assert lib.pkv_kv_cache_append(_cache(fmt=1, scales=4096), good, good, good, good, good, 1, 4, 0, None) == 0
-    # prefill over an FP8 cache with head_dim 64 is not supported
-    assert lib.pkv_paged_attn_prefill(_cache(fmt=1, scales=4096, d=64), good, 2, good, good, good, 1, 4, 8, 4,
+    # prefill over an FP8 cache with an unsupported head_dim
+    assert lib.pkv_paged_attn_prefill(_cache(fmt=1, scales=4096, d=96), good, 2, good, good, good, 1, 4, 8, 4,
                                       F(0.1), 1, good, 0, None, None) == 2
     # decode: the activation dtype must still be fp16 / bf16
     args = (_cache(fmt=1, scales=4096, dt=2), good, 2, good, good, 2, 4, F(0.1), 0, good, 1 << 20, good, 0, None, None)

@@ -244,12 +244,18 @@ def test_fp8_prefill_chunks_match_decode():
     np.testing.assert_allclose(out[last.cuda()].cpu().numpy(), dec.cpu().numpy(), atol=2e-2, rtol=0)
 
 
-def test_fp8_prefill_head_dim_64_is_refused():
-    p = prefill_problem(lens=[40], q_lens=[8], hq=4, hkv=4, d=64, bs=16)
+@pytest.mark.parametrize("dtype", [W.F16, W.BF16])
+@pytest.mark.parametrize("bs", [8, 16, 128])
+def test_fp8_prefill_head_dim_64(dtype, bs):
+    """head_dim 64: the codes (64-byte rows) land in buffers of their own and are converted into
+    the f16 tile; causal chunks, a one-token context, GQA, ragged lengths and page sizes."""
+    p = prefill_problem(lens=[40, 1, 700, 300], q_lens=[8, 1, 300, 300], hq=8, hkv=2, d=64, bs=bs, dtype=dtype,
+                        seed=bs + 1)
     codes, scales = device_fp8(p)
-    with pytest.raises(pkv.PkvError) as e:
-        run_prefill_fp8(p, codes, scales)
-    assert e.value.status == 2
+    out, lse = run_prefill_fp8(p, codes, scales)
+    ref, ref_lse = oracle.attention_of(p, host(codes, scales))
+    check_close(out, ref, dtype, roundings=PREFILL_ROUNDINGS, what="fp8 prefill d=64 %s bs=%d" % (dtype, bs))
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-4, atol=1e-4)
 
 
 def test_fp8_decode_full_7b_size_sampled():

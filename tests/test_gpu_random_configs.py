@@ -124,7 +124,7 @@ def test_random_decode(fmt, i):
 @pytest.mark.parametrize("i", range(8))
 def test_random_prefill(fmt, i):
     rng = np.random.default_rng(3000 + i + (500 if fmt == "fp8" else 0))
-    d = 128 if fmt == "fp8" else int(rng.choice([64, 128]))
+    d = int(rng.choice([64, 128]))
     bs = int(rng.choice(BLOCK_SIZES))
     hq, hkv = GROUPS_PREFILL[int(rng.integers(0, len(GROUPS_PREFILL)))]
     dtype = W.F16 if rng.integers(0, 2) else W.BF16
@@ -152,7 +152,7 @@ def test_random_prefill(fmt, i):
 def test_random_mixed(i):
     rng = np.random.default_rng(5000 + i)
     fmt = "fp8" if i % 3 == 2 else "native"
-    d = 128 if fmt == "fp8" else int(rng.choice([64, 128]))
+    d = int(rng.choice([64, 128]))
     bs = int(rng.choice(BLOCK_SIZES))
     hq, hkv = [(8, 8), (8, 4), (16, 4), (32, 1), (16, 2)][int(rng.integers(0, 5))]
     dtype = W.F16 if rng.integers(0, 2) else W.BF16

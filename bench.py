@@ -202,6 +202,54 @@ class Dist:
 # clocks: nvidia-smi sampled in the background, kept for the timed window
 # ------------------------------------------------------------------------------------------------
 
+class NvmlClocks:
+    """Read-only, in-process NVML (the driver's libnvidia-ml) reads of one GPU's SM clock and its
+    clock event reasons, cheap enough to take while timed work is executing. Nothing is set."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, gpu_index: int):
+        import ctypes
+        self.lib = None
+        self.samples = []
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            handle = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(gpu_index), ctypes.byref(handle)) != 0:
+                return
+            self.ct, self.lib, self.handle = ctypes, lib, handle
+            mx = ctypes.c_uint()
+            self.max_mhz = mx.value if lib.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx)) == 0 else None
+            name = "nvmlDeviceGetCurrentClocksEventReasons"
+            self.reasons_fn = getattr(lib, name, None) or getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        except (OSError, AttributeError):
+            self.lib = None
+
+    def probe(self):
+        if not self.lib:
+            return
+        ct = self.ct
+        mhz, reasons = ct.c_uint(), ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.handle, 1, ct.byref(mhz)) == 0 and \
+                self.reasons_fn(self.handle, ct.byref(reasons)) == 0:
+            self.samples.append((mhz.value, reasons.value))
+
+    def summary(self):
+        if not self.samples:
+            return None
+        return {"sm_mhz": statistics.median([m for m, _ in self.samples]), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted({n for _, r in self.samples for bit, n in self.REASONS.items() if r & bit}),
+                "samples": len(self.samples),
+                "window": "timed: in-process NVML reads while the timed steps execute (after half and after all "
+                          "of them are enqueued, before the closing synchronize)"}
+
+    def close(self):
+        if self.lib:
+            self.lib.nvmlShutdown()
+
+
 class ClockSampler:
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -356,12 +404,19 @@ def bench_decode(torch, p, steps, warmup, dist, want_clocks=True):
     torch.cuda.synchronize()
     assert pkv.get_device_error() == 0
     sampler = ClockSampler(torch.cuda.current_device()) if want_clocks else None
+    nvml = NvmlClocks(torch.cuda.current_device()) if want_clocks else None
     if sampler:
         time.sleep(0.3)
     dist.barrier()
     torch.cuda.synchronize()
     t0 = time.time()
-    ms = time_loop(torch, lambda i: step(i, True), steps, stream)
+
+    def timed_step(i):
+        step(i, True)
+        if nvml and (i == steps // 2 or i == steps - 1):
+            nvml.probe()  # the GPU is executing the steps enqueued before this one
+
+    ms = time_loop(torch, timed_step, steps, stream)
     torch.cuda.synchronize()
     t1 = time.time()
     dist.barrier()
@@ -371,6 +426,13 @@ def bench_decode(torch, p, steps, warmup, dist, want_clocks=True):
         time.sleep(0.25)
         sampler.stop()
         clocks = sampler.summary(t0, t1)
+        in_region = nvml.summary() if nvml else None
+        if in_region:
+            # the in-process reads are of the timed region itself; the sampled ones stay beside them
+            in_region["nvidia_smi"] = clocks
+            clocks = in_region
+    if nvml:
+        nvml.close()
     assert pkv.get_device_error() == 0
     res = {"ms_total": ms, "ms_per_step": ms / steps, "decode_ms": decode_ms, "clocks": clocks,
            "launches_per_step": 3, "bytes": decode_bytes(p)}

@@ -21,7 +21,6 @@ namespace pkv {
 namespace {
 
 constexpr int kAppendThreads = 256;
-constexpr int kUnroll = 4;
 
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
     uint4 v;
@@ -73,6 +72,7 @@ __device__ __forceinline__ bool token_slot(const AppendArgs &a, int t, int lane,
 template <int D>
 __global__ void __launch_bounds__(kAppendThreads) append_kernel(AppendArgs a) {
     constexpr int kVecPerRow = D / 8;  // 16-byte vectors per head row
+    constexpr int kUnroll = (kHeadsPerItem * kVecPerRow + 31) / 32;  // vectors per lane per item
     static_assert(kHeadsPerItem * kVecPerRow <= 32 * kUnroll, "one pass of the warp per item");
     const int lane = threadIdx.x & 31;
     const int warps_total = gridDim.x * (kAppendThreads / 32);
@@ -212,6 +212,7 @@ cudaError_t launch_append(const AppendArgs &a, cudaStream_t s) {
         if (a.head_dim == 128) return launch_pdl(append_fp8_kernel<128, F16Tag>, dim3(grid), dim3(kAppendThreads), 0, s, a);
         return launch_pdl(append_fp8_kernel<64, F16Tag>, dim3(grid), dim3(kAppendThreads), 0, s, a);
     }
+    if (a.head_dim == 256) return launch_pdl(append_kernel<256>, dim3(grid), dim3(kAppendThreads), 0, s, a);
     if (a.head_dim == 128) return launch_pdl(append_kernel<128>, dim3(grid), dim3(kAppendThreads), 0, s, a);
     return launch_pdl(append_kernel<64>, dim3(grid), dim3(kAppendThreads), 0, s, a);
 }

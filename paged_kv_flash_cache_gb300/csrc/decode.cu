@@ -561,10 +561,20 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     pdl_launch_dependents();
 }
 
-// V (2 or 4) consecutive floats from a 4V-byte aligned address, as one vector load.
+// V (2, 4 or 8) consecutive floats from a 16-byte (V = 2: 8-byte) aligned address, as vector loads.
 template <int V>
 __device__ __forceinline__ void load_vec(const float *src, float (&x)[V]) {
-    if constexpr (V == 4) {
+    if constexpr (V == 8) {
+        const float4 v = *reinterpret_cast<const float4 *>(src), w = *reinterpret_cast<const float4 *>(src + 4);
+        x[0] = v.x;
+        x[1] = v.y;
+        x[2] = v.z;
+        x[3] = v.w;
+        x[4] = w.x;
+        x[5] = w.y;
+        x[6] = w.z;
+        x[7] = w.w;
+    } else if constexpr (V == 4) {
         const float4 v = *reinterpret_cast<const float4 *>(src);
         x[0] = v.x;
         x[1] = v.y;
@@ -725,6 +735,7 @@ cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (a.head_dim == 256) return cudaLaunchKernelEx(&cfg, combine_kernel<256>, a);
     if (a.head_dim == 128) return cudaLaunchKernelEx(&cfg, combine_kernel<128>, a);
     return cudaLaunchKernelEx(&cfg, combine_kernel<64>, a);
 }

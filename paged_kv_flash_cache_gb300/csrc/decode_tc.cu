@@ -44,7 +44,6 @@ namespace pkv {
 namespace {
 
 constexpr int kBM = 128;      // MMA rows: the query heads of a unit (at most 128)
-constexpr int kBN = 128;      // tokens per K / V tile
 constexpr int kRingMax = 6;   // key tiles (K and V) in flight
 constexpr int kSoftmaxWarps = 4;
 constexpr int kProducerWarp = 4;
@@ -52,8 +51,8 @@ constexpr int kMmaWarp = 5;
 constexpr int kThreads = 6 * 32;
 constexpr float kRescale = 8.0f;  // lazy rescale threshold (log2 units)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;     // S_0 [0, 128), S_1 [128, 256)
-constexpr uint32_t kColO = 256;   // O_0 [256, 256 + D), O_1 [384, 384 + D)
+constexpr uint32_t kColS = 0;     // S_0 [0, BN), S_1 [BN, 2 BN)
+constexpr uint32_t kColO = 256;   // O_0 [256, 256 + D), O_1 [384, 384 + D) (head_dim 256: O_0 only)
 
 // Shared memory: the two q buffers, then the ring of key tiles (K then V), the barriers and the
 // unit tables. A q buffer holds only the unit's Gu rows (rounded up to 8) per 64-column half: the QK
@@ -62,8 +61,12 @@ constexpr uint32_t kColO = 256;   // O_0 [256, 256 + D), O_1 [384, 384 + D)
 // produce TMEM rows that no one reads.
 template <int D>
 struct TcLayout {
+    // tokens per key tile: 128, or 64 at head_dim 256 (a K or V tile stays 32 KB)
+    static constexpr int kBN = D > 128 ? 64 : 128;
+    // O buffers in TMEM: two (a unit's epilogue overlaps the next unit), one at head_dim 256
+    static constexpr int kNumO = D > 128 ? 1 : 2;
     static constexpr int kHalves = D / 64;                      // 128-byte swizzle atoms along D
-    static constexpr uint32_t kTileHalf = 128 * 128;            // 128 rows x 128 bytes
+    static constexpr uint32_t kTileHalf = kBN * 128;            // kBN rows x 128 bytes
     static constexpr uint32_t kTileBytes = kHalves * kTileHalf;  // a K or V tile
     static constexpr uint32_t kSlotBytes = 2 * kTileBytes;       // a ring slot: K, then V
     static constexpr uint32_t kBarBytes = 512;
@@ -89,6 +92,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
                      DecodeArgs a) {
     using L = TcLayout<D>;
+    constexpr int kBN = L::kBN;
     const int ring = a.stages;
     const int hu = a.cache.num_kv_heads * a.head_groups;  // unit heads
     const int gu = a.num_q_heads / hu;                    // query heads per unit (<= 128)
@@ -106,7 +110,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *s_full = q_empty + 2;          // [2] S_i computed
     uint64_t *p_full = s_full + 2;           // [2] P written over S_i (and O rescaled)
     uint64_t *o_done = p_full + 2;           // [2] the P V of the last tile t with t % 2 == i is done
-    uint64_t *o_empty = o_done + 2;          // [2] the epilogue has read O_i
+    uint64_t *o_empty = o_done + 2;          // [kNumO] the epilogue has read O_i
     uint64_t *drain = o_empty + 2;           // every MMA issued has completed
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -230,6 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ====================================== MMA issuer ======================================
         if (lane == 0) {
             const uint32_t id_qk = tc::idesc_f16(BF16, kBM, kBN, false);
+            const uint32_t sP = (uint32_t)kBN / 2;  // TMEM columns of one P part (kBN 16-bit values, 2 a column)
             const uint32_t id_pv = tc::idesc_f16(BF16, kBM, D, true);
             const uint32_t aQ = smem_addr(sQ), aRing = smem_addr(sRing);
             uint32_t T = 0, U = 0;  // key tiles and units consumed
@@ -240,16 +245,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             // O_ob (+)= P_t V_t: P's rounded part (columns 0-63 of S_{t%2}), then its remainder
             // (columns 64-127); V is [tokens x D], D contiguous: MN-major B, 8-token groups 1024 B
             // apart, 64-column halves kTileHalf apart; 16 tokens = 8 TMEM columns of P
-            auto pv = [&](uint32_t t, uint32_t tO, bool first) -> bool {
+            auto pv = [&](uint32_t t, uint32_t tO, bool first, uint32_t u_of_t) -> bool {
                 if (!mbar_wait(&p_full[t & 1u], (t >> 1) & 1u, abort_flag, a.err)) return false;
+                // the unit's first P V overwrites its O buffer: the epilogue of the unit that had
+                // it before (kNumO units back) must have read it
+                if (first && !mbar_wait(&o_empty[u_of_t % L::kNumO], ((u_of_t / L::kNumO) & 1u) ^ 1u, abort_flag, a.err))
+                    return false;
                 tc::fence_after_sync();
-                const uint32_t tP = tmem + kColS + 128u * (t & 1u);
+                const uint32_t tP = tmem + kColS + (uint32_t)kBN * (t & 1u);
                 const uint32_t aV = aRing + (t % ring) * L::kSlotBytes + L::kTileBytes;
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
                     for (int kk = 0; kk < kBN / 16; ++kk)
-                        tc::mma_f16_ts(tO, tP + 64u * part + 8u * kk,
+                        tc::mma_f16_ts(tO, tP + sP * part + 8u * kk,
                                        tc::smem_desc(aV + (uint32_t)kk * 2048u, L::kTileHalf, 1024), id_pv,
                                        (first && part == 0 && kk == 0) ? 0u : 1u);
                 tc::mma_commit(&o_done[t & 1u]);
@@ -258,15 +267,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             // the tile whose P V is still to be issued: after the next tile's QK, also across units
             bool pending = false, pend_first = false;
-            uint32_t pend_t = 0, pend_o = 0;
+            uint32_t pend_t = 0, pend_o = 0, pend_u = 0;
             for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x, ++U) {
                 const UnitCursor c = unit_of(u, ut, a.s_max, hu, chunk);
                 const int ntiles = (c.t1 - c.t0 + kBN - 1) / kBN;
-                const uint32_t qb = U & 1u, ob = U & 1u;
-                // q landed, and the epilogue of the unit two back has read O_ob
-                if (!(ok = mbar_wait(&q_full[qb], (U >> 1) & 1u, abort_flag, a.err) &&
-                           mbar_wait(&o_empty[ob], ((U >> 1) & 1u) ^ 1u, abort_flag, a.err)))
-                    break;
+                const uint32_t qb = U & 1u, ob = U % L::kNumO;
+                if (!(ok = mbar_wait(&q_full[qb], (U >> 1) & 1u, abort_flag, a.err))) break;
                 tc::fence_after_sync();
                 const uint32_t aQu = aQ + qb * q_bytes, tO = tmem + kColO + 128u * ob;
                 for (int k = 0; k < ntiles; ++k, ++T) {
@@ -274,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(ok = kv_wait(T))) break;
                     tc::fence_after_sync();
                     const uint32_t aK = aRing + (T % ring) * L::kSlotBytes;
-                    const uint32_t tS = tmem + kColS + 128u * (T & 1u);
+                    const uint32_t tS = tmem + kColS + (uint32_t)kBN * (T & 1u);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t oq = (uint32_t)(kk >> 2) * q_half + (uint32_t)(kk & 3) * 32u;
@@ -285,14 +291,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::mma_commit(&s_full[T & 1u]);
                     if (k == ntiles - 1) tc::mma_commit(&q_empty[qb]);  // every QK of the unit issued
                     // the previous tile's P V (its softmax overlapped this QK)
-                    if (pending && !(ok = pv(pend_t, pend_o, pend_first))) break;
+                    if (pending && !(ok = pv(pend_t, pend_o, pend_first, pend_u))) break;
                     pending = true;
                     pend_t = T;
                     pend_o = tO;
                     pend_first = (k == 0);
+                    pend_u = U;
                 }
             }
-            if (ok && pending) ok = pv(pend_t, pend_o, pend_first);
+            if (ok && pending) ok = pv(pend_t, pend_o, pend_first, pend_u);
             tc::mma_commit(drain);
             volatile int no_abort = 0;
             mbar_wait(drain, 0, &no_abort, a.err);
@@ -318,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto epilogue = [&](const Done &d) -> bool {
             if (!mbar_wait(&o_done[d.t_last & 1u], (d.t_last >> 1) & 1u, abort_flag, a.err)) return false;
             tc::fence_after_sync();
-            const uint32_t tOd = tmem + kColO + 128u * (d.U & 1u) + lane_base;
+            const uint32_t tOd = tmem + kColO + 128u * (d.U % L::kNumO) + lane_base;
             const int splits = (ut.lens[d.c.b] + chunk - 1) / chunk;
             const bool row_ok = r < gu;
             const float inv = d.l > 0.f ? 1.f / d.l : 0.f;
@@ -350,19 +357,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&o_empty[d.U & 1u]);
+            if (lane == 0) mbar_arrive(&o_empty[d.U % L::kNumO]);
             return true;
         };
         for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x, ++U) {
             const UnitCursor c = unit_of(u, ut, a.s_max, hu, chunk);
             const int ntiles = (c.t1 - c.t0 + kBN - 1) / kBN;
-            const uint32_t tO = tmem + kColO + 128u * (U & 1u) + lane_base;
+            const uint32_t tO = tmem + kColO + 128u * (U % L::kNumO) + lane_base;
             float m = -INFINITY, l = 0.f;
             for (int k = 0; k < ntiles; ++k, ++T) {
                 const int n_valid = min(kBN, c.t1 - (c.t0 + k * kBN));
                 if (!(ok = mbar_wait(&s_full[T & 1u], (T >> 1) & 1u, abort_flag, a.err))) break;
                 tc::fence_after_sync();
-                const uint32_t tS = tmem + kColS + 128u * (T & 1u) + lane_base;
+                const uint32_t tS = tmem + kColS + (uint32_t)kBN * (T & 1u) + lane_base;
                 float s[kBN];
 #pragma unroll
                 for (int cc = 0; cc < kBN / 32; ++cc)
@@ -432,9 +439,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::fence_proxy_async_smem();
                 }
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
+                for (int cc = 0; cc < kBN / 32; ++cc) {
                     tc::tmem_st16(tS + cc * 16, *reinterpret_cast<uint32_t(*)[16]>(&ph[cc * 16]));
-                    tc::tmem_st16(tS + 64 + cc * 16, *reinterpret_cast<uint32_t(*)[16]>(&pl[cc * 16]));
+                    tc::tmem_st16(tS + kBN / 2 + cc * 16, *reinterpret_cast<uint32_t(*)[16]>(&pl[cc * 16]));
                 }
                 tc::tmem_wait_st();
                 tc::fence_before_sync();
@@ -465,6 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, bool BF16>
 cudaError_t launch_tc_t(const DecodeArgs &a, int grid, cudaStream_t s) {
     using L = TcLayout<D>;
+    constexpr int kBN = L::kBN;
     const int gu = a.num_q_heads / (a.cache.num_kv_heads * a.head_groups);
     if (gu < 1 || gu > kBM) return cudaErrorInvalidValue;
     CUtensorMap tm_q, tm_kv;
@@ -491,8 +499,9 @@ cudaError_t launch_tc_t(const DecodeArgs &a, int grid, cudaStream_t s) {
 
 cudaError_t launch_decode_tc(const DecodeArgs &a, int grid, cudaStream_t s) {
     if (a.batch == 0) return cudaSuccess;
-    if (a.chunk % kBN != 0) return cudaErrorInvalidValue;  // splits start at multiples of 128 tokens
+    if (a.chunk % 128 != 0) return cudaErrorInvalidValue;  // splits start at multiples of 128 tokens
     const bool bf16 = a.cache.dtype == 1;
+    if (a.cache.head_dim == 256) return bf16 ? launch_tc_t<256, true>(a, grid, s) : launch_tc_t<256, false>(a, grid, s);
     if (a.cache.head_dim == 128) return bf16 ? launch_tc_t<128, true>(a, grid, s) : launch_tc_t<128, false>(a, grid, s);
     if (a.cache.head_dim == 64) return bf16 ? launch_tc_t<64, true>(a, grid, s) : launch_tc_t<64, false>(a, grid, s);
     return cudaErrorInvalidValue;

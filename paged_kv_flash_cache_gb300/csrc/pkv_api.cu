@@ -79,7 +79,8 @@ pkv_status check_cache(const pkv_cache &c) {
     if (c.format != PKV_KV_NATIVE && c.format != PKV_KV_FP8_E4M3) return PKV_ERR_UNSUPPORTED;
     if (c.format == PKV_KV_FP8_E4M3 && (!c.scales || !aligned16(c.scales))) return PKV_ERR_INVALID_ARG;
     if (c.dtype != PKV_F16 && c.dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
-    if (c.head_dim != 64 && c.head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (c.head_dim != 64 && c.head_dim != 128 && c.head_dim != 256) return PKV_ERR_UNSUPPORTED;
+    if (c.format == PKV_KV_FP8_E4M3 && c.head_dim == 256) return PKV_ERR_UNSUPPORTED;
     if (!is_pow2(c.block_size) || c.block_size < 8 || c.block_size > 512) return PKV_ERR_UNSUPPORTED;
     return PKV_OK;
 }
@@ -271,10 +272,10 @@ pkv_status decode_impl(const pkv_cache &cache, const void *q, int num_q_heads, c
     if (fp8) {
         path = cache.head_dim == 128 ? kFp8Tensor : kCudaCores;
         per_unit = group < 8 ? group : 8;
-    } else if (group <= 2) {
+    } else if (group <= 2 && cache.head_dim <= 128) {
         path = kCudaCores;
         per_unit = group;
-    } else if (group == 4 || group == 8) {
+    } else if ((group == 4 || group == 8) && cache.head_dim <= 128) {
         path = kMmaSync;
         per_unit = group;
     } else {
@@ -363,7 +364,7 @@ pkv_status pkv_paged_attn_decode(pkv_cache cache, const void *q, int num_q_heads
 pkv_status pkv_attn_combine(const float *partial_o, const float *partial_lse, int n_rows, int num_splits,
                             int head_dim, void *out, pkv_dtype out_dtype, float *lse, void *stream) {
     if (n_rows < 0 || num_splits <= 0) return PKV_ERR_INVALID_ARG;
-    if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PKV_ERR_UNSUPPORTED;
     if (out_dtype != PKV_F16 && out_dtype != PKV_BF16 && out_dtype != PKV_F32) return PKV_ERR_UNSUPPORTED;
     if (n_rows == 0) return PKV_OK;
     if (!partial_o || !partial_lse || !out) return PKV_ERR_INVALID_ARG;

@@ -252,11 +252,32 @@ __device__ __forceinline__ void store_out(void *out, size_t idx, float v, int ou
     }
 }
 
-// V (2 or 4) consecutive outputs from element idx on (idx a multiple of V, the base 16-byte
-// aligned): one vector store, rounded as store_out rounds each value.
+// V (2, 4 or 8) consecutive outputs from element idx on (idx a multiple of V, the base 16-byte
+// aligned): vector stores (one; two for 8 FP32 values), rounded as store_out rounds each value.
 template <int V>
 __device__ __forceinline__ void store_out_vec(void *out, size_t idx, const float (&v)[V], int out_dtype) {
-    static_assert(V == 2 || V == 4, "vectors of 2 or 4");
+    static_assert(V == 2 || V == 4 || V == 8, "vectors of 2, 4 or 8");
+    if constexpr (V == 8) {
+        if (out_dtype == 2) {
+            float *o = static_cast<float *>(out) + idx;
+            *reinterpret_cast<float4 *>(o) = make_float4(v[0], v[1], v[2], v[3]);
+            *reinterpret_cast<float4 *>(o + 4) = make_float4(v[4], v[5], v[6], v[7]);
+            return;
+        }
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (out_dtype == 1) {
+                const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+                memcpy(&w[i], &h, 4);
+            } else {
+                const __half2 h = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+                memcpy(&w[i], &h, 4);
+            }
+        }
+        *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + idx) = make_uint4(w[0], w[1], w[2], w[3]);
+        return;
+    } else {
     if (out_dtype == 2) {
         float *o = static_cast<float *>(out) + idx;
         if constexpr (V == 4) *reinterpret_cast<float4 *>(o) = make_float4(v[0], v[1], v[2], v[3]);
@@ -277,6 +298,7 @@ __device__ __forceinline__ void store_out_vec(void *out, size_t idx, const float
     uint16_t *o = static_cast<uint16_t *>(out) + idx;
     if constexpr (V == 4) *reinterpret_cast<uint2 *>(o) = make_uint2(w[0], w[1]);
     else *reinterpret_cast<uint32_t *>(o) = w[0];
+    }
 }
 
 constexpr float kLog2e = 1.4426950408889634f;

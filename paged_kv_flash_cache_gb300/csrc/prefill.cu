@@ -972,6 +972,7 @@ cudaError_t launch_t(const PrefillArgs &a, cudaStream_t stream) {
 
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t s) {
     if (a.max_q_len == 0) return cudaSuccess;
+    if (a.cache.head_dim != 64 && a.cache.head_dim != 128) return cudaErrorNotSupported;
     const bool bf16 = a.cache.dtype == 1;
     if (a.cache.fp8) {
         if (a.cache.head_dim == 128) return bf16 ? launch_t<128, true, true>(a, s) : launch_t<128, false, true>(a, s);

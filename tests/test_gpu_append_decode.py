@@ -247,9 +247,10 @@ def test_decode_bad_page_flags_error():
     assert pkv.get_device_error() == 0
 
 
-def test_attn_combine_entry_point():
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_attn_combine_entry_point(d):
     rng = np.random.default_rng(3)
-    po = rng.standard_normal((37, 5, 128))
+    po = rng.standard_normal((37, 5, d))
     pl = rng.standard_normal((37, 5)) * 3
     pl[0, :] = -np.inf
     pl[1, 2:] = -np.inf
@@ -262,3 +263,38 @@ def test_attn_combine_entry_point():
     got_lse = lse.cpu().numpy()
     assert np.isneginf(got_lse[0]) and np.all(out[0].cpu().numpy() == 0)
     np.testing.assert_allclose(got_lse[1:], ref_lse[1:], rtol=1e-6, atol=1e-6)
+
+
+# ------------------------------------------------------------------------------------------------
+# head_dim 256 (every grouping runs on the tcgen05 decode kernel, with 64-token key tiles)
+# ------------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("bs", [16, 64])
+def test_append_bit_exact_head_dim_256(bs):
+    p = problem(lens=[1, 37, 300, 513], bs=bs, d=256, dtype=W.BF16, hq=2, hkv=2)
+    dev = device_cache(p)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    assert np.array_equal(cache_bits(dev), oracle.build_cache(p))
+
+
+@pytest.mark.parametrize("dtype", [W.F16, W.BF16])
+@pytest.mark.parametrize("hq,hkv", [(2, 2), (4, 2), (6, 2), (8, 2), (16, 2), (32, 1)])
+def test_decode_head_dim_256(dtype, hq, hkv):
+    p = problem(lens=[5, 700, 129, 2000, 1], hq=hq, hkv=hkv, d=256, dtype=dtype, bs=32, seed=hq + 256)
+    cache = device_cache(p)
+    out, lse = run_decode(p, cache)
+    ref, ref_lse = oracle.attention_of(p, cache_bits(cache))
+    check_close(out, ref, dtype, roundings=1, what="d=256 %s hq=%d hkv=%d" % (dtype, hq, hkv))
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-5, atol=1e-5)
+
+
+@pytest.mark.parametrize("num_splits", [1, 3, 7])
+def test_decode_head_dim_256_splits_fp32_output(num_splits):
+    """head_dim 256 with forced splits and an FP32 output: the stated bounds as written."""
+    p = problem(lens=[3000, 64, 1, 2500], hq=8, hkv=8, d=256, bs=16, dtype=W.BF16, mb=256, seed=9)
+    cache = device_cache(p)
+    out, lse = run_decode(p, cache, num_splits=num_splits, out_dtype=torch.float32)
+    ref, ref_lse = oracle.attention_of(p, cache_bits(cache))
+    check_close(out, ref, "bf16", roundings=0, what="d=256 splits=%d fp32 out" % num_splits)
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-5, atol=1e-5)

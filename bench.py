@@ -405,6 +405,9 @@ def bench_decode(torch, p, steps, warmup, dist, want_clocks=True):
     assert pkv.get_device_error() == 0
     sampler = ClockSampler(torch.cuda.current_device()) if want_clocks else None
     nvml = NvmlClocks(torch.cuda.current_device()) if want_clocks else None
+    if nvml:
+        nvml.probe()  # the first read is slow (library set-up): take it before the timed region
+        nvml.samples.clear()
     if sampler:
         time.sleep(0.3)
     dist.barrier()

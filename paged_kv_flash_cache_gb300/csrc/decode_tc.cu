@@ -45,7 +45,6 @@ namespace {
 
 constexpr int kBM = 128;      // MMA rows: the query heads of a unit (at most 128)
 constexpr int kRingMax = 6;   // key tiles (K and V) in flight
-constexpr int kSoftmaxWarps = 4;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kThreads = 6 * 32;
@@ -87,7 +86,26 @@ struct TcLayout {
     }
 };
 
-template <int D, bool BF16>
+// TMEM accesses of a softmax thread's columns. M = 128: thread = lane = row, 32x32b. M = 64: the
+// .16x32bx2 shape, threads t and t + 16 sharing row t % 16 of the quarter, the second at OFF
+// columns further on.
+template <int kM, int OFF>
+__device__ __forceinline__ void ld_cols32(uint32_t taddr, float (&v)[32]) {
+    if constexpr (kM == 64) tc::tmem_ld16x2_32<OFF>(taddr, v);
+    else tc::tmem_ld32(taddr, v);
+}
+template <int kM, int OFF>
+__device__ __forceinline__ void st_cols32(uint32_t taddr, const float (&v)[32]) {
+    if constexpr (kM == 64) tc::tmem_st16x2_32<OFF>(taddr, v);
+    else tc::tmem_st32(taddr, v);
+}
+template <int kM, int OFF>
+__device__ __forceinline__ void st_cols16(uint32_t taddr, const uint32_t (&v)[16]) {
+    if constexpr (kM == 64) tc::tmem_st16x2_16<OFF>(taddr, v);
+    else tc::tmem_st16(taddr, v);
+}
+
+template <int D, bool BF16, int kM>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
                      DecodeArgs a) {
@@ -117,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const UnitTable ut = unit_table(reinterpret_cast<int *>(smem + L::ints_off(gu, ring)), a.batch, a.s_max);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_sm = (gu + 31) >> 5;                      // softmax warps with head rows
+    const int n_sm = kM == 64 ? (gu + 15) >> 4 : (gu + 31) >> 5;  // softmax warps with head rows
     const int chunk = a.chunk;
 
     if (threadIdx.x == 0) {
@@ -233,9 +251,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kMmaWarp) {
         // ====================================== MMA issuer ======================================
         if (lane == 0) {
-            const uint32_t id_qk = tc::idesc_f16(BF16, kBM, kBN, false);
+            const uint32_t id_qk = tc::idesc_f16(BF16, kM, kBN, false);
             const uint32_t sP = (uint32_t)kBN / 2;  // TMEM columns of one P part (kBN 16-bit values, 2 a column)
-            const uint32_t id_pv = tc::idesc_f16(BF16, kBM, D, true);
+            const uint32_t id_pv = tc::idesc_f16(BF16, kM, D, true);
             const uint32_t aQ = smem_addr(sQ), aRing = smem_addr(sRing);
             uint32_t T = 0, U = 0;  // key tiles and units consumed
             bool ok = true;
@@ -307,7 +325,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp < n_sm) {
         // ================================ softmax + epilogue warps ================================
-        const int r = warp * 32 + lane;  // the row: head r of the unit (rows >= gu are padding)
+        // M = 128: thread = TMEM lane = row 32 w + lane, with all kBN columns of S and D of O. M = 64:
+        // rows 16 w .. 16 w + 15 in lanes 0-15 of the warp's quarter; threads t and t + 16 share row
+        // 16 w + t % 16, thread t / 16 = h taking S columns (tokens) [h kBN / 2, (h + 1) kBN / 2) and O
+        // columns [h D / 2, (h + 1) D / 2): the row max and sum are combined by one shuffle.
+        constexpr int kSplit = kM == 64 ? 2 : 1;
+        constexpr int kCols = kBN / kSplit;  // S columns of this thread
+        constexpr int kDCols = D / kSplit;   // O columns of this thread
+        const int half = kM == 64 ? lane >> 4 : 0;
+        const int r = kM == 64 ? warp * 16 + (lane & 15) : warp * 32 + lane;  // head r of the unit
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         const float c2 = a.scale * kLog2e;
         uint32_t T = 0, U = 0;
@@ -328,27 +354,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t tOd = tmem + kColO + 128u * (d.U % L::kNumO) + lane_base;
             const int splits = (ut.lens[d.c.b] + chunk - 1) / chunk;
             const bool row_ok = r < gu;
-            const float inv = d.l > 0.f ? 1.f / d.l : 0.f;
-            const float lse_v = d.l > 0.f ? (d.m + __log2f(d.l)) * kLn2 : -INFINITY;
+            float lt = d.l;
+            if constexpr (kM == 64) lt += __shfl_xor_sync(0xffffffffu, lt, 16);  // the row's two halves
+            const float inv = lt > 0.f ? 1.f / lt : 0.f;
+            const float lse_v = lt > 0.f ? (d.m + __log2f(lt)) * kLn2 : -INFINITY;
             const size_t h = (size_t)d.c.kvh * gu + r;  // query head
             const size_t orow = (size_t)ut.qrow[d.c.b] * a.num_q_heads + h;
             const size_t prow = (size_t)d.c.b * a.num_q_heads + h;
 #pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
+            for (int cc = 0; cc < kDCols / 32; ++cc) {
                 float o[32];
-                tc::tmem_ld32(tOd + cc * 32, o);
+                ld_cols32<kM, kDCols>(tOd + cc * 32, o);
                 tc::tmem_wait_ld();
                 if (row_ok) {
+                    const int col = half * kDCols + cc * 32;
 #pragma unroll
                     for (int v = 0; v < 8; ++v) {
                         const float x[4] = {o[4 * v] * inv, o[4 * v + 1] * inv, o[4 * v + 2] * inv,
                                             o[4 * v + 3] * inv};
-                        if (splits == 1) store_out_vec<4>(a.out, orow * D + cc * 32 + 4 * v, x, a.out_dtype);
-                        else store_out_vec<4>(a.part_o, (prow * a.s_max + d.c.split) * D + cc * 32 + 4 * v, x, 2);
+                        if (splits == 1) store_out_vec<4>(a.out, orow * D + col + 4 * v, x, a.out_dtype);
+                        else store_out_vec<4>(a.part_o, (prow * a.s_max + d.c.split) * D + col + 4 * v, x, 2);
                     }
                 }
             }
-            if (row_ok) {
+            if (row_ok && half == 0) {
                 if (splits == 1) {
                     if (a.lse) a.lse[orow] = lse_v;
                 } else {
@@ -370,24 +399,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!(ok = mbar_wait(&s_full[T & 1u], (T >> 1) & 1u, abort_flag, a.err))) break;
                 tc::fence_after_sync();
                 const uint32_t tS = tmem + kColS + (uint32_t)kBN * (T & 1u) + lane_base;
-                float s[kBN];
+                float s[kCols];  // tokens half * kCols + i of the tile
 #pragma unroll
-                for (int cc = 0; cc < kBN / 32; ++cc)
-                    tc::tmem_ld32(tS + cc * 32, *reinterpret_cast<float(*)[32]>(&s[cc * 32]));
+                for (int cc = 0; cc < kCols / 32; ++cc)
+                    ld_cols32<kM, kCols>(tS + cc * 32, *reinterpret_cast<float(*)[32]>(&s[cc * 32]));
                 tc::tmem_wait_ld();
-                if (n_valid < kBN) {
+                const int nv = n_valid - half * kCols;  // visible tokens among this thread's columns
+                if (nv < kCols) {
 #pragma unroll
-                    for (int i = 0; i < kBN; ++i) s[i] = (i < n_valid) ? s[i] : -INFINITY;
+                    for (int i = 0; i < kCols; ++i) s[i] = (i < nv) ? s[i] : -INFINITY;
                 }
                 // row max as 8 independent chains
                 float m8[8];
 #pragma unroll
                 for (int q = 0; q < 8; ++q) m8[q] = fmax3(s[q], s[q + 8], s[q + 16]);
 #pragma unroll
-                for (int i = 24; i < kBN; i += 16)
+                for (int i = 24; i < kCols; i += 16)
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) m8[q] = fmax3(m8[q], s[i + q], (i + 8 + q < kBN) ? s[i + 8 + q] : -INFINITY);
-                const float mx = fmaxf(fmax3(m8[0], m8[1], m8[2]), fmax3(fmax3(m8[3], m8[4], m8[5]), m8[6], m8[7]));
+                    for (int q = 0; q < 8; ++q)
+                        m8[q] = fmax3(m8[q], s[i + q], (i + 8 + q < kCols) ? s[i + 8 + q] : -INFINITY);
+                float mx = fmaxf(fmax3(m8[0], m8[1], m8[2]), fmax3(fmax3(m8[3], m8[4], m8[5]), m8[6], m8[7]));
+                if constexpr (kM == 64) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
                 const float m_new = fmaxf(m, mx * c2);
                 const bool grow = m_new > m + kRescale;  // false when m_new = -inf
                 const float alpha = grow ? ex2f(m - m_new) : 1.f;  // 0 when m = -inf
@@ -397,11 +429,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // every row has a visible key (n_valid >= 1), so m is finite here
                 const float2 cc2 = make_float2(c2, c2), nm2 = make_float2(-m, -m);
-                uint32_t ph[kBN / 2], pl[kBN / 2];  // P's rounded part and remainder, pairs of tokens
+                uint32_t ph[kCols / 2], pl[kCols / 2];  // P's rounded part and remainder, pairs of tokens
                 float2 l4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                 make_float2(0.f, 0.f)};
 #pragma unroll
-                for (int q = 0; q < kBN / 2; ++q) {
+                for (int q = 0; q < kCols / 2; ++q) {
                     const float2 xq = ffma2(make_float2(s[2 * q], s[2 * q + 1]), cc2, nm2);
                     const float2 e = make_float2(ex2f(xq.x), ex2f(xq.y));  // ex2(-inf) = 0
                     l4[q & 3] = fadd2(l4[q & 3], e);
@@ -415,13 +447,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(ok = mbar_wait(&o_done[(T - 1) & 1u], ((T - 1) >> 1) & 1u, abort_flag, a.err))) break;
                     tc::fence_after_sync();
 #pragma unroll
-                    for (int cc = 0; cc < D / 32; ++cc) {
+                    for (int cc = 0; cc < kDCols / 32; ++cc) {
                         float o[32];
-                        tc::tmem_ld32(tO + cc * 32, o);
+                        ld_cols32<kM, kDCols>(tO + cc * 32, o);
                         tc::tmem_wait_ld();
 #pragma unroll
                         for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                        tc::tmem_st32(tO + cc * 32, o);
+                        st_cols32<kM, kDCols>(tO + cc * 32, o);
                     }
                 }
                 // tokens at or beyond the unit's end may hold unwritten cache bytes (or the next
@@ -439,9 +471,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::fence_proxy_async_smem();
                 }
 #pragma unroll
-                for (int cc = 0; cc < kBN / 32; ++cc) {
-                    tc::tmem_st16(tS + cc * 16, *reinterpret_cast<uint32_t(*)[16]>(&ph[cc * 16]));
-                    tc::tmem_st16(tS + kBN / 2 + cc * 16, *reinterpret_cast<uint32_t(*)[16]>(&pl[cc * 16]));
+                for (int cc = 0; cc < kCols / 32; ++cc) {
+                    st_cols16<kM, kCols / 2>(tS + cc * 16, *reinterpret_cast<uint32_t(*)[16]>(&ph[cc * 16]));
+                    st_cols16<kM, kCols / 2>(tS + kBN / 2 + cc * 16, *reinterpret_cast<uint32_t(*)[16]>(&pl[cc * 16]));
                 }
                 tc::tmem_wait_st();
                 tc::fence_before_sync();
@@ -469,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, int kM>
 cudaError_t launch_tc_t(const DecodeArgs &a, int grid, cudaStream_t s) {
     using L = TcLayout<D>;
     constexpr int kBN = L::kBN;
@@ -484,7 +516,7 @@ cudaError_t launch_tc_t(const DecodeArgs &a, int grid, cudaStream_t s) {
     DecodeArgs args = a;
     args.stages = L::ring_for(gu, a.batch, a.s_max, (size_t)info.max_smem);
     if (args.stages == 0) return cudaErrorInvalidValue;  // tables of this batch and split count do not fit
-    auto kern = decode_tc_kernel<D, BF16>;
+    auto kern = decode_tc_kernel<D, BF16, kM>;
     static DeviceFlags configured;
     if (!configured.test(info.device)) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, info.max_smem);
@@ -495,16 +527,26 @@ cudaError_t launch_tc_t(const DecodeArgs &a, int grid, cudaStream_t s) {
                       tm_kv, args);
 }
 
+template <int D, int kM>
+cudaError_t launch_tc_d(const DecodeArgs &a, bool bf16, int grid, cudaStream_t s) {
+    return bf16 ? launch_tc_t<D, true, kM>(a, grid, s) : launch_tc_t<D, false, kM>(a, grid, s);
+}
+
 }  // namespace
 
 cudaError_t launch_decode_tc(const DecodeArgs &a, int grid, cudaStream_t s) {
     if (a.batch == 0) return cudaSuccess;
     if (a.chunk % 128 != 0) return cudaErrorInvalidValue;  // splits start at multiples of 128 tokens
     const bool bf16 = a.cache.dtype == 1;
-    if (a.cache.head_dim == 256) return bf16 ? launch_tc_t<256, true>(a, grid, s) : launch_tc_t<256, false>(a, grid, s);
-    if (a.cache.head_dim == 128) return bf16 ? launch_tc_t<128, true>(a, grid, s) : launch_tc_t<128, false>(a, grid, s);
-    if (a.cache.head_dim == 64) return bf16 ? launch_tc_t<64, true>(a, grid, s) : launch_tc_t<64, false>(a, grid, s);
-    return cudaErrorInvalidValue;
+    // units of at most 64 query heads: M = 64 products (half the tensor time of M = 128, and their
+    // rows spread over twice the softmax warps)
+    const bool m64 = a.num_q_heads / (a.cache.num_kv_heads * a.head_groups) <= 64;
+    switch (a.cache.head_dim) {
+        case 256: return m64 ? launch_tc_d<256, 64>(a, bf16, grid, s) : launch_tc_d<256, 128>(a, bf16, grid, s);
+        case 128: return m64 ? launch_tc_d<128, 64>(a, bf16, grid, s) : launch_tc_d<128, 128>(a, bf16, grid, s);
+        case 64: return m64 ? launch_tc_d<64, 64>(a, bf16, grid, s) : launch_tc_d<64, 128>(a, bf16, grid, s);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace pkv

@@ -407,8 +407,10 @@ pkv_status prefill_impl(const pkv_cache &cache, const void *q, int num_q_heads, 
     if (!aligned16(q) || !aligned16(out) || (lse && !aligned16(lse))) return PKV_ERR_INVALID_ARG;
     const long long cap = (long long)max_blocks_per_seq * cache.block_size;
     if (cap > (1ll << 30)) return PKV_ERR_UNSUPPORTED;
-    // grid (heads, sequences, 256-row blocks): the last two dimensions hold at most 65535
-    if (batch > 65535 || (max_q_len + 255) / 256 > 65535) return PKV_ERR_UNSUPPORTED;
+    // grid (heads, sequences, row blocks of 256 rows, 128 at head_dim 256): the last two dimensions
+    // hold at most 65535
+    const int block_rows = cache.head_dim == 256 ? 128 : 256;
+    if (batch > 65535 || ((long long)max_q_len + block_rows - 1) / block_rows > 65535) return PKV_ERR_UNSUPPORTED;
     DeviceSlot *s = slot();
     if (!s) return PKV_ERR_CUDA;
     PrefillArgs a;

@@ -153,6 +153,12 @@ cudaError_t launch_decode_fp8(const DecodeArgs &a, int grid, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs &a, int grid, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t s);
+// head_dim 256 (prefill_wide.cu): one 128-row query tile a CTA, 64-key tiles
+cudaError_t launch_prefill_wide(const PrefillArgs &a, cudaStream_t s);
+// q [total_q, Hq, D] as a 3-D tensor map (d, head, token), boxes of 64 columns x 1 head x box_rows
+// tokens, 128-byte swizzle
+cudaError_t encode_q_heads_map(const void *q, int bf16, int total_q, int num_q_heads, int head_dim, int box_rows,
+                               CUtensorMap *map);
 int decode_ctas_per_sm(int head_dim, int group, int dtype);
 int decode_max_batch();
 

@@ -828,6 +828,23 @@ cudaError_t encode_cache_map(const CacheView &c, int box_rows, CUtensorMap *map)
     return cudaSuccess;
 }
 
+cudaError_t encode_q_heads_map(const void *q, int bf16, int total_q, int num_q_heads, int head_dim, int box_rows,
+                               CUtensorMap *map) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    if (total_q <= 0 || box_rows <= 0 || box_rows > 256) return cudaErrorNotSupported;
+    // q [total_q, Hq, D]: x = d, y = head, z = token; box 64 x 1 x box_rows
+    cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_q_heads, (cuuint64_t)total_q};
+    cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)num_q_heads * head_dim * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(q),
+            dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    return cudaSuccess;
+}
+
 cudaError_t encode_rows_map(const void *ptr, int bf16, long long rows, int cols, int box_cols, int box_rows,
                             CUtensorMap *map) {
     EncodeTiledFn enc = encode_fn();
@@ -917,20 +934,10 @@ namespace {
 template <int D, bool BF16, bool FP8>
 cudaError_t launch_t(const PrefillArgs &a, cudaStream_t stream) {
     using Lay = PrefillLayout<D, FP8>;
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return cudaErrorNotSupported;
-    const CUtensorMapDataType dt = BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUtensorMap tm_q, tm_kv;
     {
-        // q [total_q, Hq, D]: x = d, y = head, z = token; box 64 x 1 x 128
-        cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)a.num_q_heads, (cuuint64_t)a.total_q};
-        cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)a.num_q_heads * D * 2};
-        cuuint32_t box[3] = {64, 1, (cuuint32_t)kBM};
-        cuuint32_t es[3] = {1, 1, 1};
-        if (enc(&tm_q, dt, 3, const_cast<void *>(a.q), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
+        const cudaError_t e = encode_q_heads_map(a.q, BF16 ? 1 : 0, a.total_q, a.num_q_heads, D, kBM, &tm_q);
+        if (e != cudaSuccess) return e;
     }
     {
         const cudaError_t e = encode_cache_map(a.cache, a.cache.block_size < kBN ? a.cache.block_size : kBN, &tm_kv);
@@ -972,6 +979,7 @@ cudaError_t launch_t(const PrefillArgs &a, cudaStream_t stream) {
 
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t s) {
     if (a.max_q_len == 0) return cudaSuccess;
+    if (a.cache.head_dim == 256) return a.cache.fp8 ? cudaErrorNotSupported : launch_prefill_wide(a, s);
     if (a.cache.head_dim != 64 && a.cache.head_dim != 128) return cudaErrorNotSupported;
     const bool bf16 = a.cache.dtype == 1;
     if (a.cache.fp8) {

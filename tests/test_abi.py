@@ -87,6 +87,9 @@ def test_host_validation_without_gpu(lib):
                                       None, None) == 2
     assert lib.pkv_paged_attn_prefill(_cache(), good, 2, good, good, good, 1, 4, 1 << 25, 1 << 25, F(0.1), 1, good,
                                       0, None, None) == 2
+    # head_dim 256 runs 128-row blocks: 65537 of them are too many
+    assert lib.pkv_paged_attn_prefill(_cache(d=256), good, 2, good, good, good, 1, 4, (1 << 23) + 1, (1 << 23) + 1,
+                                      F(0.1), 1, good, 0, None, None) == 2
     # combine: bad head_dim, bad split count
     assert lib.pkv_attn_combine(good, good, 4, 2, 96, good, 2, None, None) == 2
     assert lib.pkv_attn_combine(good, good, 4, 0, 128, good, 2, None, None) == 1

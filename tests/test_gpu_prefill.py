@@ -220,3 +220,51 @@ def test_long_prefill_full_size_fp8_cache():
     ref, _ = oracle.attention_of(p, host, rows=sel)
     check_close(outs[torch.as_tensor(sel, device="cuda")], ref, "bf16", roundings=PREFILL_ROUNDINGS,
                 what="long prefill fp8")
+
+
+# ------------------------------------------------------------------------------------------------
+# head_dim 256 (prefill_wide.cu: one 128-row query tile a CTA, 64-key tiles)
+# ------------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", [W.F16, W.BF16])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 2), (6, 1)])
+def test_prefill_head_dim_256(dtype, causal, hq, hkv):
+    p = problem(lens=[520, 77, 1000, 64], q_lens=[200, 77, 384, 1], hq=hq, hkv=hkv, d=256, dtype=dtype,
+                causal=causal, bs=16, seed=hq * 5 + hkv)
+    cache = device_cache(p)
+    out, lse = run_prefill(p, cache)
+    check(p, cache, out, lse, roundings=2, what="d=256 %s causal=%s hq=%d hkv=%d" % (dtype, causal, hq, hkv))
+
+
+@pytest.mark.parametrize("bs", [8, 64, 256])
+def test_prefill_head_dim_256_block_sizes_fp32_output(bs):
+    """Block sizes below, at and above the 64-key tile; FP32 output leaves P's rounding alone."""
+    p = problem(lens=[300, 129, 700], q_lens=[300, 2, 257], bs=bs, hq=4, hkv=2, d=256, seed=bs + 256)
+    cache = device_cache(p)
+    out, lse = run_prefill(p, cache, out_dtype=torch.float32)
+    check(p, cache, out, lse, roundings=1, what="d=256 bs=%d fp32 out" % bs)
+
+
+def test_prefill_head_dim_256_first_row_is_v0():
+    p = problem(lens=[130], q_lens=[130], hq=2, hkv=2, d=256, dtype=W.F16, bs=16, seed=19)
+    cache = device_cache(p)
+    out, _ = run_prefill(p, cache, out_dtype=torch.float32)
+    assert torch.equal(out[0].cpu(), p.v_ctx[0].to(torch.float32))
+
+
+def test_mixed_call_head_dim_256():
+    """Decode rows and prefill chunks in one call at head_dim 256: the tcgen05 decode for the single
+    rows, the wide prefill kernel for the chunks."""
+    lens, q_lens = [700, 1, 300, 1500, 90], [1, 1, 200, 1, 90]
+    p = problem(lens=lens, q_lens=q_lens, hq=8, hkv=2, d=256, dtype=W.BF16, bs=16, seed=77)
+    cache = device_cache(p)
+    lse = torch.empty((p.total_q, p.num_q_heads), dtype=torch.float32, device="cuda")
+    out = pkv.paged_attn_mixed(cache, to_dev(p.q), to_dev(p.cu_q_lens), to_dev(p.context_lens),
+                               to_dev(p.block_tables), max_q_len=int(p.q_lens.max()), scale=p.scale, causal=True,
+                               lse=lse)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    ref, ref_lse = oracle.attention_of(p, cache_bits(cache))
+    check_close(out, ref, p.dtype, roundings=2, what="mixed d=256")
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-4, atol=1e-4)

@@ -50,7 +50,7 @@ def parse():
                          "samples")
     ap.add_argument("--only", default="", help="comma list of extra workloads (bs_sweep,mixed,prefix,fp8,mqa,mixed_call,prefill,prefill_fp8)")
     ap.add_argument("--profile", choices=["decode", "append", "prefill", "decode_mixed", "decode_prefix", "decode_fp8",
-                                          "prefill_fp8", "decode_mqa"],
+                                          "prefill_fp8", "decode_mqa", "prefill_d256"],
                     default=None,
                     help="small case for ncu captures: W + K launches of one kernel, nothing else timed")
     return ap.parse_args()
@@ -128,6 +128,21 @@ def profile_case(args):
         out = torch.empty((p.batch, 32, 128), dtype=torch.float16, device="cuda")
         for _ in range(args.warmup + args.steps):
             pkv.paged_attn_decode(cache, q, bt, ctx, scale=p.scale, out=out)
+        torch.cuda.synchronize()
+        assert pkv.get_device_error() == 0
+    elif args.profile == "prefill_d256":
+        # the head_dim 256 prefill of the bench line: 4 x 4096 tokens, 16 query / 8 KV heads, one
+        # causal call (0.13 GB of K/V)
+        gen = torch.Generator().manual_seed(1256)
+        nb = 4 * 4096 // 16
+        order = torch.randperm(nb, generator=gen).tolist()
+        p = W.make_problem("d256", batch=4, num_q_heads=16, num_kv_heads=8, head_dim=256, block_size=16,
+                           context_lens=[4096] * 4, q_lens=[4096] * 4, dtype=W.BF16, causal=True, seed=1257,
+                           num_blocks=nb, free_order=order, pool_init="none", device="cuda")
+        cache = device_problem(p, torch)
+        q, cu, ctx, bt = p.q.cuda(), p.cu_q_lens.cuda(), p.context_lens.cuda(), p.block_tables.cuda()
+        for _ in range(args.warmup + args.steps):
+            pkv.paged_attn_prefill(cache, q, cu, ctx, bt, max_q_len=4096, scale=p.scale, causal=True)
         torch.cuda.synchronize()
         assert pkv.get_device_error() == 0
     else:
@@ -753,6 +768,50 @@ def bench_mqa(torch, steps, warmup):
             "tokens_per_s": round(p.batch / ms * 1e3, 1)}
 
 
+def bench_head_dim_256(torch, steps, warmup):
+    """head_dim 256: a causal prefill of 4 prompts x 4096 tokens (16 query heads on 8 KV heads, bf16,
+    bs 16) as one call, and the decode of a token per sequence over the same 4 x 4096 context with
+    the same heads (the tcgen05 decode, units of 2 query heads)."""
+    import paged_kv_flash_cache_gb300 as pkv
+    from paged_kv_flash_cache_gb300 import workloads as W
+    gen = torch.Generator().manual_seed(1256)
+    lens = [4096] * 4
+    nb = sum((L + 15) // 16 for L in lens)
+    order = torch.randperm(nb, generator=gen).tolist()
+    p = W.make_problem("d256", batch=4, num_q_heads=16, num_kv_heads=8, head_dim=256, block_size=16,
+                       context_lens=lens, q_lens=lens, dtype=W.BF16, causal=True, seed=1257, num_blocks=nb,
+                       free_order=order, pool_init="none", device="cuda")
+    cache = device_problem(p, torch)
+    q, cu, ctx, bt = p.q.cuda(), p.cu_q_lens.cuda(), p.context_lens.cuda(), p.block_tables.cuda()
+    out = torch.empty_like(q)
+    fn = lambda i: pkv.paged_attn_prefill(cache, q, cu, ctx, bt, max_q_len=4096, scale=p.scale, causal=True,
+                                          out=out)
+    for i in range(warmup):
+        fn(i)
+    ms = time_loop(torch, fn, steps, torch.cuda.current_stream()) / steps
+    flops = p.causal_flops()
+    # decode: the last token of each prompt against its whole context
+    qd = q[cu[1:].long() - 1].contiguous()
+    od = torch.empty_like(qd)
+    ws = torch.empty(max(16, pkv.decode_workspace_size(4, 16, 8, 256, 16, bt.shape[1])), dtype=torch.uint8,
+                     device="cuda")
+    fd = lambda i: pkv.paged_attn_decode(cache, qd, bt, ctx, scale=p.scale, workspace=ws, out=od)
+    for i in range(warmup):
+        fd(i)
+    ms_d = time_loop(torch, fd, steps, torch.cuda.current_stream()) / steps
+    kv = 4 * 4096 * 8 * 256 * 2 * 2
+    pk = peaks()
+    del cache
+    torch.cuda.empty_cache()
+    return {"workload": "head_dim 256, bf16, bs 16, 16 query heads on 8 KV heads, 4 x 4096 tokens",
+            "prefill": {"ms": round(ms, 3), "tflops": round(flops / ms / 1e9, 1),
+                        "frac_of_dense_bf16": round(flops / ms / 1e9 / pk["bf16_tflops"], 3),
+                        "kernel": "prefill_wide_kernel (causal, one call)"},
+            "decode": {"ms": round(ms_d, 4), "kv_gbs": round(kv / ms_d / 1e6, 1),
+                       "frac_of_hbm": round(kv / ms_d / 1e6 / pk["hbm_gbs"], 3),
+                       "kernel": "decode_tc_kernel<256> + combine"}}
+
+
 def bench_mixed_call(torch, steps, warmup):
     """One paged_attn_mixed call over 64 decode sequences and 4 prefill chunks, against the same
     work as a decode call plus a prefill call."""
@@ -953,7 +1012,8 @@ def main():
         only = set(filter(None, args.only.split(",")))
         for name, fn in (("bs_sweep", bench_bs_sweep), ("mixed", bench_mixed), ("prefix", bench_prefix),
                          ("fp8", lambda t, k, w: bench_fp8(t, k, w, r["decode_ms"])), ("mqa", bench_mqa),
-                         ("mixed_call", bench_mixed_call), ("prefill", bench_prefill),
+                         ("mixed_call", bench_mixed_call), ("head_dim_256", bench_head_dim_256),
+                         ("prefill", bench_prefill),
                          ("prefill_fp8", lambda t, k, w: bench_prefill(t, k, w, fp8=True))):
             if only and name not in only:
                 continue

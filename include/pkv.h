@@ -86,14 +86,14 @@ typedef enum { PKV_KV_NATIVE = 0, PKV_KV_FP8_E4M3 = 1 } pkv_kv_format;
 
 /* The paged KV cache [num_blocks, 2, num_kv_heads, block_size, head_dim] ([FAPA] s3).
  * dtype (PKV_F16 or PKV_BF16) is the type of q, k_new and v_new, of the default
- * output, and of the elements of a native cache.  Supported: head_dim 64 or 128;
- * block_size a power of two in [8, 512].  format and scales are as above (scales
- * [num_blocks, 2, num_kv_heads, block_size], 16-byte aligned; NULL for a native
- * cache).  An FP8 cache is supported by append, decode and (head_dim 128) prefill;
- * prefill over an FP8 cache with head_dim 64 returns PKV_ERR_UNSUPPORTED.  Over an
- * FP8 cache with head_dim 128 the tensor-core products run in f16 on the exact
- * codes (the row scales are applied in FP32): q must lie within f16's range
- * (|q| < 65504; magnitudes below 2^-24 count as 0). */
+ * output, and of the elements of a native cache.  Supported: head_dim 64, 128 or
+ * 256 (256: a native cache only; an FP8 cache with head_dim 256 returns
+ * PKV_ERR_UNSUPPORTED); block_size a power of two in [8, 512].  format and scales
+ * are as above (scales [num_blocks, 2, num_kv_heads, block_size], 16-byte aligned;
+ * NULL for a native cache).  Every call accepts an FP8 cache.  Over an FP8 cache
+ * the tensor-core products run in f16 on the exact codes (the row scales are
+ * applied in FP32): q must lie within f16's range (|q| < 65504; magnitudes below
+ * 2^-24 count as 0). */
 typedef struct {
     void *ptr;
     int num_blocks;
@@ -174,7 +174,8 @@ PKV_API pkv_status pkv_paged_attn_decode(pkv_cache cache, const void *q, int num
  *                 context_lens[b] - q_len_b + r and sees keys 0 .. that position
  *                 (bottom-right alignment); zero: every query sees the whole context.
  *   max_q_len     an upper bound of q_len_b over the batch (sizes the grid; batch and
- *                 ceil(max_q_len / 256) at most 65535 each, else PKV_ERR_UNSUPPORTED).
+ *                 ceil(max_q_len / 256), or ceil(max_q_len / 128) at head_dim 256, at most
+ *                 65535 each, else PKV_ERR_UNSUPPORTED).
  *   out           [total_q, Hq, D] in out_dtype; lse FP32 [total_q, Hq] or NULL. */
 PKV_API pkv_status pkv_paged_attn_prefill(pkv_cache cache, const void *q, int num_q_heads,
                                   const int *cu_q_lens, const int *context_lens,
@@ -190,8 +191,8 @@ PKV_API pkv_status pkv_paged_attn_prefill(pkv_cache cache, const void *q, int nu
  * whole context either way) plus num_splits / workspace as pkv_paged_attn_decode, sized by
  * pkv_decode_workspace_size(batch, ...). The single-row sequences run on the decode kernels
  * (split-KV, one unit per KV head's query group), the others on the prefill kernel; each
- * kernel leaves the other kind's rows untouched. The decode constraints (head grouping,
- * batch <= 2048) apply to the whole call. */
+ * kernel leaves the other kind's rows untouched. The decode constraint on head grouping (an
+ * FP8 cache) applies to the whole call. */
 PKV_API pkv_status pkv_paged_attn_mixed(pkv_cache cache, const void *q, int num_q_heads,
                                 const int *cu_q_lens, const int *context_lens,
                                 const int *block_tables, int batch, int max_blocks_per_seq,

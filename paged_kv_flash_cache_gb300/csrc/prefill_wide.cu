@@ -91,9 +91,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // grid (heads, batch, row blocks), row blocks last-first: the blocks that see the most keys
-    // (causal) start in the first wave
-    const int mt = (int)gridDim.z - 1 - (int)blockIdx.z, h = blockIdx.x, b = blockIdx.y;
+    // grid (heads, row blocks, sequences), row blocks last-first: CTAs start in linear order, so the
+    // CTAs running together share one sequence's K/V (it stays in L2), and within it the blocks that
+    // see the most keys (causal) start first
+    const int mt = (int)gridDim.y - 1 - (int)blockIdx.y, h = blockIdx.x, b = blockIdx.z;
     pdl_wait();  // lengths, tables, q and the chunk's own K/V may come from the previous kernel
     const int q0 = __ldg(p.cu_q_lens + b);
     const int q_len = __ldg(p.cu_q_lens + b + 1) - q0;
@@ -408,7 +409,7 @@ cudaError_t launch_wide_t(const PrefillArgs &a, cudaStream_t stream) {
     }
     const long long row_blocks = ((long long)a.max_q_len + kBM - 1) / kBM;
     if (row_blocks > 65535) return cudaErrorNotSupported;
-    dim3 grid(a.num_q_heads, a.batch, (unsigned)row_blocks);
+    dim3 grid(a.num_q_heads, (unsigned)row_blocks, a.batch);
     return launch_pdl(kern, grid, dim3(kThreads), kSmemBytes, stream, tm_q, tm_kv, p);
 }
 

@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--profile-batch", type=int, default=1,
+                    help="prefill / prefill_fp8 profile cases: sequences of the 4 x 8192 prompt set (4 = the bench's occupancy)")
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-full", action="store_true",
@@ -147,7 +149,7 @@ def profile_case(args):
         assert pkv.get_device_error() == 0
     else:
         fp8 = args.profile == "prefill_fp8"
-        p = W.prefill_long(batch=1, device="cuda")
+        p = W.prefill_long(batch=args.profile_batch, device="cuda")
         shape = (p.num_blocks, 2, p.num_kv_heads, p.block_size, p.head_dim)
         if fp8:
             cache = torch.zeros(shape, dtype=torch.uint8, device="cuda")
@@ -157,7 +159,7 @@ def profile_case(args):
             scales = None
         bt = p.block_tables.cuda()
         pkv.kv_cache_append(cache, p.k_ctx.cuda(), p.v_ctx.cuda(), p.cu_ctx_lens.cuda(),
-                            torch.zeros(1, dtype=torch.int32, device="cuda"), bt, scales=scales)
+                            torch.zeros(p.batch, dtype=torch.int32, device="cuda"), bt, scales=scales)
         v = W.prefill_chunk_view(p, 15)
         q = p.q[v["rows"]].cuda()
         cu, ctx = v["cu_q_lens"].cuda(), v["context_lens"].cuda()

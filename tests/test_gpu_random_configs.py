@@ -29,6 +29,10 @@ def built():
     assert torch.cuda.is_available()
 
 
+# head_dim 256 on a native cache only (an FP8 cache with head_dim 256 is refused)
+HEAD_DIMS = {"native": [64, 128, 256], "fp8": [64, 128]}
+
+
 def draw_lengths(rng, n, hi, bs):
     out = []
     for _ in range(n):
@@ -94,7 +98,7 @@ def sample_rows(p, rng, full_below=64):
 @pytest.mark.parametrize("i", range(16))
 def test_random_decode(fmt, i):
     rng = np.random.default_rng(1000 + i + (500 if fmt == "fp8" else 0))
-    d = int(rng.choice([64, 128]))
+    d = int(rng.choice(HEAD_DIMS[fmt]))
     bs = int(rng.choice(BLOCK_SIZES))
     if fmt == "native":
         # any group 1..48 (uneven ones included) over 1, 2, 3, 4 or 8 KV heads
@@ -124,7 +128,7 @@ def test_random_decode(fmt, i):
 @pytest.mark.parametrize("i", range(8))
 def test_random_prefill(fmt, i):
     rng = np.random.default_rng(3000 + i + (500 if fmt == "fp8" else 0))
-    d = int(rng.choice([64, 128]))
+    d = int(rng.choice(HEAD_DIMS[fmt]))
     bs = int(rng.choice(BLOCK_SIZES))
     hq, hkv = GROUPS_PREFILL[int(rng.integers(0, len(GROUPS_PREFILL)))]
     dtype = W.F16 if rng.integers(0, 2) else W.BF16
@@ -152,7 +156,7 @@ def test_random_prefill(fmt, i):
 def test_random_mixed(i):
     rng = np.random.default_rng(5000 + i)
     fmt = "fp8" if i % 3 == 2 else "native"
-    d = int(rng.choice([64, 128]))
+    d = int(rng.choice(HEAD_DIMS[fmt]))
     bs = int(rng.choice(BLOCK_SIZES))
     hq, hkv = [(8, 8), (8, 4), (16, 4), (32, 1), (16, 2)][int(rng.integers(0, 5))]
     dtype = W.F16 if rng.integers(0, 2) else W.BF16

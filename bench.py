@@ -456,23 +456,30 @@ def bench_decode(torch, p, steps, warmup, dist, want_clocks=True):
     assert pkv.get_device_error() == 0
     res = {"ms_total": ms, "ms_per_step": ms / steps, "decode_ms": decode_ms, "clocks": clocks,
            "launches_per_step": 3, "bytes": decode_bytes(p)}
-    # end to end through the public API: inputs copied from pinned host memory every step,
-    # the step's output read back
-    h_q = p.q.cpu().pin_memory()
-    h_k, h_v = step_in["k_new"].pin_memory(), step_in["v_new"].pin_memory()
-    h_cu, h_before = step_in["cu_new_lens"].pin_memory(), step_in["ctx_before"].pin_memory()
-    h_bt, h_ctx = step_in["block_tables"].pin_memory(), p.context_lens.pin_memory()
+    # end to end through the public API: inputs copied from pinned host memory every step, the
+    # step's output read back. The step's inputs (q, the new K/V, their offsets and positions, the
+    # tables and lengths) sit in one pinned host buffer, 16-byte aligned pieces, and go to the
+    # device in one transfer a step; the calls take device views of its pieces.
+    host_parts = [p.q.cpu(), step_in["k_new"], step_in["v_new"], step_in["cu_new_lens"], step_in["ctx_before"],
+                  step_in["block_tables"], p.context_lens]
+    offs, total = [], 0
+    for t in host_parts:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 15) // 16 * 16
+    h_stage = torch.empty(total, dtype=torch.uint8).pin_memory()
+    d_stage = torch.empty(total, dtype=torch.uint8, device="cuda")
+    views = []
+    for t, o in zip(host_parts, offs):
+        nb = t.numel() * t.element_size()
+        h_stage[o:o + nb].copy_(t.contiguous().flatten().view(torch.uint8))
+        views.append(d_stage[o:o + nb].view(t.dtype).view(t.shape))
+    d_q, d_k, d_v, d_cu, d_before, d_bt, d_ctx = views
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new)
-    d_cu, d_before, d_bt, d_ctx = (torch.empty_like(cu_new), torch.empty_like(before), torch.empty_like(bt),
-                                   torch.empty_like(ctx))
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_cu, h_before, h_bt, h_ctx))
+    h2d = sum(t.numel() * t.element_size() for t in host_parts)
     d2h = h_out.numel() * h_out.element_size()
 
     def e2e_step(i):
-        for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_cu, h_cu), (d_before, h_before), (d_bt, h_bt),
-                     (d_ctx, h_ctx)):
-            d.copy_(h, non_blocking=True)
+        d_stage.copy_(h_stage, non_blocking=True)
         pkv.paged_attn_decode(cache, d_q, d_bt, d_ctx, scale=p.scale, workspace=ws, out=out)
         pkv.kv_cache_append(cache, d_k, d_v, d_cu, d_before, d_bt)
         h_out.copy_(out, non_blocking=True)

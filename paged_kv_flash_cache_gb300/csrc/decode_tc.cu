@@ -49,21 +49,27 @@ constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kThreads = 6 * 32;
 constexpr float kRescale = 8.0f;  // lazy rescale threshold (log2 units)
-constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;     // S_0 [0, BN), S_1 [BN, 2 BN)
-constexpr uint32_t kColO = 256;   // O_0 [256, 256 + D), O_1 [384, 384 + D) (head_dim 256: O_0 only)
 
-// Shared memory: the two q buffers, then the ring of key tiles (K then V), the barriers and the
-// unit tables. A q buffer holds only the unit's Gu rows (rounded up to 8) per 64-column half: the QK
+// Shared memory: the q buffers, then the ring of key tiles (K then V), the barriers and the unit
+// tables. A q buffer holds only the unit's Gu rows (rounded up to 8) per 64-column half: the QK
 // MMA reads 128 rows of A, and its reads past row Gu run on into the next half, buffer or ring
 // tile (always inside the CTA's shared memory, the ring coming after the q buffers) and only
 // produce TMEM rows that no one reads.
-template <int D>
+// kCtas = CTAs per SM: 1 (the SM's 512 TMEM columns and ~227 KB of shared memory), or 2 (each CTA
+// 256 columns and half the shared memory: 64-token key tiles, one O buffer, one q buffer; two
+// independent pipelines per SM, for units of at most 64 heads at head_dim up to 128).
+template <int D, int kCtas>
 struct TcLayout {
-    // tokens per key tile: 128, or 64 at head_dim 256 (a K or V tile stays 32 KB)
-    static constexpr int kBN = D > 128 ? 64 : 128;
-    // O buffers in TMEM: two (a unit's epilogue overlaps the next unit), one at head_dim 256
-    static constexpr int kNumO = D > 128 ? 1 : 2;
+    static_assert(kCtas == 1 || (kCtas == 2 && D <= 128), "two CTAs an SM: S_0, S_1 and O in 256 columns");
+    // tokens per key tile: 128, or 64 at head_dim 256 or two CTAs an SM (a K or V tile <= 32 KB)
+    static constexpr int kBN = (D > 128 || kCtas == 2) ? 64 : 128;
+    // O buffers in TMEM: two (a unit's epilogue overlaps the next unit), else one
+    static constexpr int kNumO = (D > 128 || kCtas == 2) ? 1 : 2;
+    static constexpr uint32_t kTmemCols = kCtas == 2 ? 256 : 512;
+    // O_0 [kColO, kColO + D), O_1 [kColO + 128, ...) (one O buffer: O_0 only)
+    static constexpr uint32_t kColO = kCtas == 2 ? 128 : 256;
+    static constexpr int kQBufs = kCtas == 2 ? 1 : 2;
     static constexpr int kHalves = D / 64;                      // 128-byte swizzle atoms along D
     static constexpr uint32_t kTileHalf = kBN * 128;            // kBN rows x 128 bytes
     static constexpr uint32_t kTileBytes = kHalves * kTileHalf;  // a K or V tile
@@ -72,7 +78,7 @@ struct TcLayout {
     // bytes between the 64-column halves of a q buffer (a multiple of 1024)
     __host__ __device__ static uint32_t q_half(int gu) { return (uint32_t)((gu + 7) / 8) * 8u * 128u; }
     __host__ __device__ static uint32_t q_bytes(int gu) { return kHalves * q_half(gu); }
-    __host__ __device__ static size_t ring_off(int gu) { return 2 * (size_t)q_bytes(gu); }
+    __host__ __device__ static size_t ring_off(int gu) { return kQBufs * (size_t)q_bytes(gu); }
     __host__ __device__ static size_t bar_off(int gu, int ring) { return ring_off(gu) + (size_t)ring * kSlotBytes; }
     __host__ __device__ static size_t ints_off(int gu, int ring) { return bar_off(gu, ring) + kBarBytes; }
     __host__ __device__ static size_t smem_bytes(int gu, int batch, int s_max, int ring) {
@@ -105,11 +111,11 @@ __device__ __forceinline__ void st_cols16(uint32_t taddr, const uint32_t (&v)[16
     else tc::tmem_st16(taddr, v);
 }
 
-template <int D, bool BF16, int kM>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, bool BF16, int kM, int kCtas>
+__global__ void __launch_bounds__(kThreads, kCtas)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
                      DecodeArgs a) {
-    using L = TcLayout<D>;
+    using L = TcLayout<D, kCtas>;
     constexpr int kBN = L::kBN;
     const int ring = a.stages;
     const int hu = a.cache.num_kv_heads * a.head_groups;  // unit heads
@@ -117,14 +123,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment: the 128-byte swizzle pattern is a function of address bits 4-9.
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-    uint8_t *sQ = smem;  // q[2]
+    uint8_t *sQ = smem;  // q[kQBufs]
     uint8_t *sRing = smem + L::ring_off(gu);
     const uint32_t q_half = L::q_half(gu), q_bytes = L::q_bytes(gu);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::bar_off(gu, ring));
     uint64_t *kv_full = bars;                // [kRingMax] a key tile's K and V have landed
     uint64_t *kv_empty = bars + kRingMax;    // [kRingMax] its MMAs are done
-    uint64_t *q_full = bars + 2 * kRingMax;  // [2] a unit's q has landed in q buffer i
-    uint64_t *q_empty = q_full + 2;          // [2] the unit's QK MMAs are done with q buffer i
+    uint64_t *q_full = bars + 2 * kRingMax;  // [kQBufs] a unit's q has landed in q buffer i
+    uint64_t *q_empty = q_full + 2;          // [kQBufs] the unit's QK MMAs are done with q buffer i
     uint64_t *s_full = q_empty + 2;          // [2] S_i computed
     uint64_t *p_full = s_full + 2;           // [2] P written over S_i (and O rescaled)
     uint64_t *o_done = p_full + 2;           // [2] the P V of the last tile t with t % 2 == i is done
@@ -156,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_barrier_init();
     }
     if (warp == kMmaWarp) {
-        tc::tmem_alloc(tmem_slot, kTmemCols);
+        tc::tmem_alloc(tmem_slot, L::kTmemCols);
         tc::tmem_relinquish();
     }
     tc::fence_before_sync();
@@ -192,8 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 wn = unit_pages(a, cn, lane);
             }
             // q of the unit: rows qrow * Hq + unit head * Gu .. + Gu - 1, one box per 64 columns
-            const uint32_t qb = qn & 1u;
-            if (!(ok = mbar_wait(&q_empty[qb], ((qn >> 1) & 1u) ^ 1u, abort_flag, a.err))) break;
+            const uint32_t qb = qn % L::kQBufs;
+            if (!(ok = mbar_wait(&q_empty[qb], ((qn / L::kQBufs) & 1u) ^ 1u, abort_flag, a.err))) break;
             if (lane == 0) {
                 mbar_arrive_expect_tx(&q_full[qb], (uint32_t)gu * D * 2u);
                 const int row0 = ut.qrow[c.b] * a.num_q_heads + c.kvh * gu;
@@ -245,8 +251,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t first = item > (uint32_t)ring ? item - (uint32_t)ring : 0u;
             for (uint32_t i = first; i < item; ++i)
                 mbar_wait(&kv_full[i % ring], (i / ring) & 1u, &no_abort, nullptr);
-            const uint32_t qfirst = qn > 2u ? qn - 2u : 0u;
-            for (uint32_t i = qfirst; i < qn; ++i) mbar_wait(&q_full[i & 1u], (i >> 1) & 1u, &no_abort, nullptr);
+            const uint32_t qfirst = qn > (uint32_t)L::kQBufs ? qn - L::kQBufs : 0u;
+            for (uint32_t i = qfirst; i < qn; ++i)
+                mbar_wait(&q_full[i % L::kQBufs], (i / L::kQBufs) & 1u, &no_abort, nullptr);
         }
     } else if (warp == kMmaWarp) {
         // ====================================== MMA issuer ======================================
@@ -289,10 +296,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x, ++U) {
                 const UnitCursor c = unit_of(u, ut, a.s_max, hu, chunk);
                 const int ntiles = (c.t1 - c.t0 + kBN - 1) / kBN;
-                const uint32_t qb = U & 1u, ob = U % L::kNumO;
-                if (!(ok = mbar_wait(&q_full[qb], (U >> 1) & 1u, abort_flag, a.err))) break;
+                const uint32_t qb = U % L::kQBufs, ob = U % L::kNumO;
+                if (!(ok = mbar_wait(&q_full[qb], (U / L::kQBufs) & 1u, abort_flag, a.err))) break;
                 tc::fence_after_sync();
-                const uint32_t aQu = aQ + qb * q_bytes, tO = tmem + kColO + 128u * ob;
+                const uint32_t aQu = aQ + qb * q_bytes, tO = tmem + L::kColO + 128u * ob;
                 for (int k = 0; k < ntiles; ++k, ++T) {
                     // S_{T%2} = Q K_k^T
                     if (!(ok = kv_wait(T))) break;
@@ -351,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto epilogue = [&](const Done &d) -> bool {
             if (!mbar_wait(&o_done[d.t_last & 1u], (d.t_last >> 1) & 1u, abort_flag, a.err)) return false;
             tc::fence_after_sync();
-            const uint32_t tOd = tmem + kColO + 128u * (d.U % L::kNumO) + lane_base;
+            const uint32_t tOd = tmem + L::kColO + 128u * (d.U % L::kNumO) + lane_base;
             const int splits = (ut.lens[d.c.b] + chunk - 1) / chunk;
             const bool row_ok = r < gu;
             float lt = d.l;
@@ -392,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x, ++U) {
             const UnitCursor c = unit_of(u, ut, a.s_max, hu, chunk);
             const int ntiles = (c.t1 - c.t0 + kBN - 1) / kBN;
-            const uint32_t tO = tmem + kColO + 128u * (U % L::kNumO) + lane_base;
+            const uint32_t tO = tmem + L::kColO + 128u * (U % L::kNumO) + lane_base;
             float m = -INFINITY, l = 0.f;
             for (int k = 0; k < ntiles; ++k, ++T) {
                 const int n_valid = min(kBN, c.t1 - (c.t0 + k * kBN));
@@ -497,39 +504,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_launch_dependents();
     if (warp == kMmaWarp) {
         tc::fence_after_sync();
-        tc::tmem_dealloc(tmem, kTmemCols);
+        tc::tmem_dealloc(tmem, L::kTmemCols);
     }
 }
 
-template <int D, bool BF16, int kM>
+template <int D, bool BF16, int kM, int kCtas>
 cudaError_t launch_tc_t(const DecodeArgs &a, int grid, cudaStream_t s) {
-    using L = TcLayout<D>;
+    using L = TcLayout<D, kCtas>;
     constexpr int kBN = L::kBN;
     const int gu = a.num_q_heads / (a.cache.num_kv_heads * a.head_groups);
-    if (gu < 1 || gu > kBM) return cudaErrorInvalidValue;
+    if (gu < 1 || gu > kM) return cudaErrorInvalidValue;
     CUtensorMap tm_q, tm_kv;
     cudaError_t e = encode_rows_map(a.q, BF16 ? 1 : 0, (long long)a.q_rows * a.num_q_heads, D, 64, gu, &tm_q);
     if (e != cudaSuccess) return e;
     e = encode_cache_map(a.cache, a.cache.block_size < kBN ? a.cache.block_size : kBN, &tm_kv);
     if (e != cudaSuccess) return e;
     const DeviceInfo &info = device_info();
+    // shared memory a CTA may take: what the SM gives one CTA, or with two CTAs an SM half of the
+    // SM's total (one CTA's maximum plus its 1 KB reserve) less the reserve
+    const size_t cta_smem = kCtas == 1 ? (size_t)info.max_smem : ((size_t)info.max_smem + 1024) / 2 - 1024;
     DecodeArgs args = a;
-    args.stages = L::ring_for(gu, a.batch, a.s_max, (size_t)info.max_smem);
+    args.stages = L::ring_for(gu, a.batch, a.s_max, cta_smem);
     if (args.stages == 0) return cudaErrorInvalidValue;  // tables of this batch and split count do not fit
-    auto kern = decode_tc_kernel<D, BF16, kM>;
+    auto kern = decode_tc_kernel<D, BF16, kM, kCtas>;
     static DeviceFlags configured;
     if (!configured.test(info.device)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, info.max_smem);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cta_smem);
         if (e != cudaSuccess) return e;
         configured.set(info.device);
     }
-    return launch_pdl(kern, dim3(grid), dim3(kThreads), L::smem_bytes(gu, a.batch, a.s_max, args.stages), s, tm_q,
-                      tm_kv, args);
+    return launch_pdl(kern, dim3(grid * kCtas), dim3(kThreads), L::smem_bytes(gu, a.batch, a.s_max, args.stages), s,
+                      tm_q, tm_kv, args);
 }
 
-template <int D, int kM>
+template <int D, int kM, int kCtas>
 cudaError_t launch_tc_d(const DecodeArgs &a, bool bf16, int grid, cudaStream_t s) {
-    return bf16 ? launch_tc_t<D, true, kM>(a, grid, s) : launch_tc_t<D, false, kM>(a, grid, s);
+    return bf16 ? launch_tc_t<D, true, kM, kCtas>(a, grid, s) : launch_tc_t<D, false, kM, kCtas>(a, grid, s);
 }
 
 }  // namespace
@@ -541,10 +551,12 @@ cudaError_t launch_decode_tc(const DecodeArgs &a, int grid, cudaStream_t s) {
     // units of at most 64 query heads: M = 64 products (half the tensor time of M = 128, and their
     // rows spread over twice the softmax warps)
     const bool m64 = a.num_q_heads / (a.cache.num_kv_heads * a.head_groups) <= 64;
+    // units of at most 64 heads at head_dim up to 128 run two CTAs an SM: two independent
+    // pipelines, each with 64-token key tiles in half the SM's TMEM and shared memory
     switch (a.cache.head_dim) {
-        case 256: return m64 ? launch_tc_d<256, 64>(a, bf16, grid, s) : launch_tc_d<256, 128>(a, bf16, grid, s);
-        case 128: return m64 ? launch_tc_d<128, 64>(a, bf16, grid, s) : launch_tc_d<128, 128>(a, bf16, grid, s);
-        case 64: return m64 ? launch_tc_d<64, 64>(a, bf16, grid, s) : launch_tc_d<64, 128>(a, bf16, grid, s);
+        case 256: return m64 ? launch_tc_d<256, 64, 1>(a, bf16, grid, s) : launch_tc_d<256, 128, 1>(a, bf16, grid, s);
+        case 128: return m64 ? launch_tc_d<128, 64, 2>(a, bf16, grid, s) : launch_tc_d<128, 128, 1>(a, bf16, grid, s);
+        case 64: return m64 ? launch_tc_d<64, 64, 2>(a, bf16, grid, s) : launch_tc_d<64, 128, 1>(a, bf16, grid, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -9,7 +9,8 @@
 // small batch still fills every SM (parallelism over key/value blocks, "从一次压测翻车说起",
 // sections 3.3 and 5.3); split results are merged by their log-sum-exp instead of atomics.
 //
-// Kernel structure (one persistent CTA per SM):
+// Kernel structure (persistent, two CTAs per SM: two independent pipelines of two stages each
+// keep the same bytes in flight as one of four, and each covers the other's waits):
 //   * work unit = (sequence, KV head, split); units are numbered in a prologue from the
 //     context lengths (decode_common.cuh: split-major, all KV heads of a sequence together)
 //     and dealt round-robin to the CTAs;
@@ -43,7 +44,6 @@ constexpr int kConsumerWarps = 8;
 constexpr int kProducerWarp = kConsumerWarps;
 constexpr int kMergeWarp = kConsumerWarps + 1;
 constexpr int kDecodeThreads = (kConsumerWarps + 2) * 32;
-constexpr int kStages = 4;
 constexpr int kMaxBatch = 2048;  // unit tables (lengths, order, split offsets) kept in shared memory
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (log2 units)
 
@@ -55,6 +55,11 @@ __device__ __forceinline__ float ex2_approx(float x) {
 
 template <int D, int G, bool FP8>
 struct DecodeLayout {
+    // resident CTAs per SM: two for a 16-bit cache (~75 KB of shared memory and 72 registers a
+    // thread each), with two stages each; one with four stages over an FP8 cache, whose 4- and
+    // 8-head units need more registers than two CTAs leave
+    static constexpr int kCtasPerSm = FP8 ? 1 : 2;
+    static constexpr int kStages = FP8 ? 4 : 2;
     static constexpr int kTile = kDecodeTile;
     static constexpr int kKB = FP8 ? 1 : 2;                        // bytes per cached element
     static constexpr int kTokPerWarp = kTile / kConsumerWarps;      // 8
@@ -113,17 +118,17 @@ __device__ __forceinline__ int v_row(int t, int br, int tile) {
 }
 
 template <typename Tag, int D, int G, bool FP8>
-__global__ void __launch_bounds__(kDecodeThreads, 1)
+__global__ void __launch_bounds__(kDecodeThreads, DecodeLayout<D, G, FP8>::kCtasPerSm)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_kv, DecodeArgs a) {
     using L = DecodeLayout<D, G, FP8>;
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kBarOffset);
-    uint64_t *empty = full + kStages;
-    uint64_t *mfull = empty + kStages;   // [2] the consumer warps' rows of a unit are in buffer i
+    uint64_t *empty = full + L::kStages;
+    uint64_t *mfull = empty + L::kStages;   // [2] the consumer warps' rows of a unit are in buffer i
     uint64_t *mempty = mfull + 2;        // [2] the merger has read buffer i
     volatile int *abort_flag = reinterpret_cast<volatile int *>(mempty + 2);
-    int *stage_unit = reinterpret_cast<int *>(mempty + 2) + 4;  // [kStages] unit of each filled stage, -1: end
-    int *merge_unit = stage_unit + kStages;                     // [2] unit of each merge buffer, -1: end
+    int *stage_unit = reinterpret_cast<int *>(mempty + 2) + 4;  // [L::kStages] unit of each filled stage, -1: end
+    int *merge_unit = stage_unit + L::kStages;                     // [2] unit of each merge buffer, -1: end
     float *merge = reinterpret_cast<float *>(smem + L::kMergeOffset);  // [2][kConsumerWarps][G][kMergeRow<D>]
     const UnitTable ut = unit_table(reinterpret_cast<int *>(smem + L::kIntsOffset), a.batch, a.s_max);
 
@@ -131,7 +136,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     const int hkv = a.cache.num_kv_heads, bs = a.cache.block_size, chunk = a.chunk;
 
     if (tid == 0) {
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < L::kStages; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kConsumerWarps);
         }
@@ -192,7 +197,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.err)) {
                     // Stop issuing; let copies already in flight land before the CTA exits
                     // (each wait is bounded again).
-                    for (int i = 0; i < kStages; ++i) {
+                    for (int i = 0; i < L::kStages; ++i) {
                         if (issued_mask & (1u << i)) {
                             volatile int no_abort = 0;
                             mbar_wait(&full[i], (issued_parity >> i) & 1u, &no_abort, nullptr);
@@ -255,7 +260,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 }
                 issued_mask |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-                if (++stage == kStages) {
+                if (++stage == L::kStages) {
                     stage = 0;
                     phase ^= 1u;
                 }
@@ -486,7 +491,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
-            if (++stage == kStages) {
+            if (++stage == L::kStages) {
                 stage = 0;
                 phase ^= 1u;
             }
@@ -684,7 +689,7 @@ cudaError_t launch_decode_t(const DecodeArgs &a, int grid, cudaStream_t s) {
         const cudaError_t e = encode_kv5_rows_map(a.cache, br, &tm);
         if (e != cudaSuccess) return e;
     }
-    return launch_pdl(kern, dim3(grid), dim3(kDecodeThreads), smem, s, tm, a);
+    return launch_pdl(kern, dim3(grid * DecodeLayout<D, G, FP8>::kCtasPerSm), dim3(kDecodeThreads), smem, s, tm, a);
 }
 
 template <typename Tag, int D>
@@ -711,7 +716,9 @@ int decode_max_batch() { return kMaxBatch; }
 
 int decode_ctas_per_sm(int head_dim, int group, int dtype) {
     (void)head_dim; (void)group; (void)dtype;
-    return 1;  // __launch_bounds__(.., 1) and ~130 KB of stages: one resident CTA per SM
+    // the split-size rule counts one CTA per SM for every decode kernel; this kernel launches
+    // DecodeLayout::kCtasPerSm CTAs per SM over the same units
+    return 1;
 }
 
 cudaError_t launch_decode(const DecodeArgs &a, int grid, cudaStream_t s) {

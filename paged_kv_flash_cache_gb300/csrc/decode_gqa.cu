@@ -13,7 +13,8 @@
 // conversions and cross-lane sums; here one mma.sync m16n8k16 covers 16 tokens x 8 head slots x
 // 16 dims.
 //
-// Kernel structure (persistent, one CTA per SM, 6 warps; 10 for units of 16 or 32 query heads):
+// Kernel structure (persistent, two CTAs per SM, each with half the SM's shared memory: two
+// independent pipelines whose waits overlap; 6 warps a CTA, 10 for units of 16 or 32 query heads):
 //   * units (sequence, KV head, split) are numbered from the context lengths and dealt
 //     round-robin to the CTAs, as in decode.cu;
 //   * the producer warp streams each unit's 64-token tiles with TMA: the page ids of a unit are
@@ -48,6 +49,7 @@ namespace {
 constexpr int kWarps = 4;                         // token slices of a tile, 16 tokens each
 constexpr int kTile = 64;                         // tokens per stage
 constexpr int kStagesMax = 6;
+constexpr int kCtasPerSm = 2;  // resident CTAs per SM (100 / 139 registers a thread for 4 / 8 heads)
 constexpr float kRescale = 8.0f;                  // lazy rescale threshold (log2 units)
 
 // Shared memory: the merge buffers, the barriers and unit ids (fixed sizes), then from the
@@ -103,7 +105,7 @@ __device__ __forceinline__ uint32_t swz(uint32_t half_base, int t, int cc) {
 }
 
 template <int D, int G, bool BF16>
-__global__ void __launch_bounds__(GqaWarps<G>::kThreads, 1)
+__global__ void __launch_bounds__(GqaWarps<G>::kThreads, kCtasPerSm)
     decode_gqa_kernel(const __grid_constant__ CUtensorMap tm_kv, DecodeArgs a) {
     using L = GqaLayout<D, G>;
     using W = GqaWarps<G>;
@@ -483,7 +485,15 @@ cudaError_t launch_gqa_t(const DecodeArgs &a, int grid, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const DeviceInfo &info = device_info();
     DecodeArgs args = a;
-    args.stages = L::stages_for(a.batch, a.s_max, (size_t)info.max_smem);
+    // each of the SM's kCtasPerSm CTAs takes its share of the SM's shared memory (one CTA's maximum
+    // plus its 1 KB reserve), less the reserve
+    const size_t cta_smem = ((size_t)info.max_smem + 1024) / kCtasPerSm - 1024;
+    int ctas = kCtasPerSm;
+    args.stages = L::stages_for(a.batch, a.s_max, cta_smem);
+    if (args.stages == 0) {  // large unit tables: one CTA an SM, with the SM's whole shared memory
+        ctas = 1;
+        args.stages = L::stages_for(a.batch, a.s_max, (size_t)info.max_smem);
+    }
     if (args.stages == 0) return cudaErrorInvalidValue;  // tables of this batch and split count do not fit
     auto kern = decode_gqa_kernel<D, G, BF16>;
     static DeviceFlags configured;
@@ -492,7 +502,7 @@ cudaError_t launch_gqa_t(const DecodeArgs &a, int grid, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         configured.set(info.device);
     }
-    return launch_pdl(kern, dim3(grid), dim3(GqaWarps<G>::kThreads), L::smem_bytes(a.batch, a.s_max, args.stages), s,
+    return launch_pdl(kern, dim3(grid * ctas), dim3(GqaWarps<G>::kThreads), L::smem_bytes(a.batch, a.s_max, args.stages), s,
                       tm, args);
 }
 

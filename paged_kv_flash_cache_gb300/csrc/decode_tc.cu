@@ -43,7 +43,6 @@
 namespace pkv {
 namespace {
 
-constexpr int kBM = 128;      // MMA rows: the query heads of a unit (at most 128)
 constexpr int kRingMax = 6;   // key tiles (K and V) in flight
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
@@ -524,16 +523,21 @@ cudaError_t launch_tc_t(const DecodeArgs &a, int grid, cudaStream_t s) {
     // SM's total (one CTA's maximum plus its 1 KB reserve) less the reserve
     const size_t cta_smem = kCtas == 1 ? (size_t)info.max_smem : ((size_t)info.max_smem + 1024) / 2 - 1024;
     DecodeArgs args = a;
+    int ctas = kCtas;
     args.stages = L::ring_for(gu, a.batch, a.s_max, cta_smem);
+    if (args.stages == 0 && kCtas > 1) {  // large unit tables: one CTA an SM, with all its shared memory
+        ctas = 1;
+        args.stages = L::ring_for(gu, a.batch, a.s_max, (size_t)info.max_smem);
+    }
     if (args.stages == 0) return cudaErrorInvalidValue;  // tables of this batch and split count do not fit
     auto kern = decode_tc_kernel<D, BF16, kM, kCtas>;
     static DeviceFlags configured;
     if (!configured.test(info.device)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cta_smem);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, info.max_smem);
         if (e != cudaSuccess) return e;
         configured.set(info.device);
     }
-    return launch_pdl(kern, dim3(grid * kCtas), dim3(kThreads), L::smem_bytes(gu, a.batch, a.s_max, args.stages), s,
+    return launch_pdl(kern, dim3(grid * ctas), dim3(kThreads), L::smem_bytes(gu, a.batch, a.s_max, args.stages), s,
                       tm_q, tm_kv, args);
 }
 

@@ -24,15 +24,16 @@
 // lane codes (token 2tig, dims 2gid and 2gid+1) and (token 2tig+1, same dims); one byte permute
 // regroups them per dim, so M slot gid of a 16-dim chunk holds dim 2gid and slot gid+8 dim 2gid+1.
 //
-// Kernel structure (persistent, one CTA per SM, 10 warps): as decode_gqa.cu -- warp 8 streams
-// each unit's 128-token tiles into a ring of 4
-// stages (3 for groups of 4 or 8 heads), warps 0-7 take 16 tokens each, warp 9 merges the warps'
-// rows and writes the output or the split partials. A tile arrives as page slices of
+// Kernel structure (persistent, two CTAs per SM, 6 warps each): as decode_gqa.cu -- warp 4
+// streams each unit's 64-token tiles into a ring of 4 stages (3 for groups of 4 or 8 heads),
+// warps 0-3 take 16 tokens each, warp 5 merges the warps' rows and writes the output or the split
+// partials. A tile arrives as page slices of
 // br = min(block_size, 64) tokens; one TMA box per slice holds its K and V code rows (a 5-D view
 // of the cache [NB][2][Hkv][bs][D]) and one its K and V row scales, so a page costs two copies.
-// Tiles of 128 tokens and two consumer warps
-// per scheduler: a 64-token tile of one-byte codes left each dependent ldmatrix / cvt / mma chain
-// with half the bytes of the 16-bit kernels and the consumers latency-bound.
+// Two CTAs per SM give every scheduler two consumer warps from two independent pipelines: the
+// consumers' dependent ldmatrix / cvt / mma chains are the bound, and one CTA with 8 consumer
+// warps and 128-token tiles (129 registers a thread, too many for two such CTAs) left them exposed
+// at every unit boundary and stage hand-off (0.151 ms against 0.122 ms for the 7B-like batch).
 #include <cuda.h>
 
 #include "decode_common.cuh"
@@ -45,11 +46,12 @@ namespace pkv {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kWarps = 8;  // consumer warps, 16 tokens each
+constexpr int kWarps = 4;  // consumer warps, 16 tokens each
 constexpr int kProducerWarp = kWarps;
 constexpr int kMergeWarp = kWarps + 1;
 constexpr int kThreads = (kWarps + 2) * 32;
-constexpr int kTile = 128;  // tokens per stage (32 KB of K and V codes)
+constexpr int kTile = 64;  // tokens per stage (16 KB of K and V codes)
+constexpr int kCtasPerSm = 2;
 constexpr int kMaxBatch8 = 2048;
 constexpr float kRescale = 8.0f;  // lazy rescale threshold (log2 units)
 constexpr int kChunks = kD / 16;  // 16-dim chunks: k-steps of q.K^T, m-tiles of O^T
@@ -63,7 +65,7 @@ struct Fp8Layout {
     static constexpr uint32_t kQBytes = G * kD * 2;
     static constexpr uint32_t kQOffset = kCodeBytes;
     static constexpr uint32_t kSOffset = kQOffset + kQBytes;
-    static constexpr uint32_t kSBytes = 2048;  // 16 slices x 128 bytes (br = 8), or kTile x 8 bytes
+    static constexpr uint32_t kSBytes = 1024;  // 8 slices x 128 bytes (br = 8), or kTile x 8 bytes
     static constexpr uint32_t kStageBytes = (kSOffset + kSBytes + 1023) / 1024 * 1024;
     static constexpr uint32_t kBarOffset = kStages8 * kStageBytes;
     // barriers: full / empty per stage, merge full / empty per merge buffer; then the abort flag
@@ -104,7 +106,7 @@ __device__ __forceinline__ void q4_to_f16(uint2 raw, uint32_t &lo, uint32_t &hi)
 }
 
 template <int G, bool BF16>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
     decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scales,
                       DecodeArgs a) {
     using L = Fp8Layout<G>;
@@ -173,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int unit_last_page = (c.t1 - 1) >> a.cache.log2_block_size;
             for (int ts = c.t0; ts < c.t1; ts += kTile) {
                 const int n = min(kTile, c.t1 - ts);
-                const int nslices = (n + br - 1) / br;  // <= 16
+                const int nslices = (n + br - 1) / br;  // <= 8
                 const int page0 = ts >> a.cache.log2_block_size;
                 const int page_last = (ts + n - 1) >> a.cache.log2_block_size;
                 if (page_last >= win.first + win.count)  // units of more than 64 pages
@@ -459,7 +461,12 @@ cudaError_t launch_fp8_t(const DecodeArgs &a, int grid, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         configured.set(dev);
     }
-    return launch_pdl(kern, dim3(grid), dim3(kThreads), Fp8Layout<G>::smem_bytes(a.batch, a.s_max), s, tm, tm_s, a);
+    // two CTAs an SM when both fit in its shared memory (one CTA's maximum plus its 1 KB reserve,
+    // each less the reserve); a batch with large unit tables runs one
+    const size_t smem = Fp8Layout<G>::smem_bytes(a.batch, a.s_max);
+    const size_t cta_smem = ((size_t)device_info().max_smem + 1024) / kCtasPerSm - 1024;
+    const int ctas = smem <= cta_smem ? kCtasPerSm : 1;
+    return launch_pdl(kern, dim3(grid * ctas), dim3(kThreads), smem, s, tm, tm_s, a);
 }
 
 template <int G>

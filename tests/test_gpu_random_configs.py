@@ -206,21 +206,21 @@ def test_decode_batches_above_2048(hq, hkv, fmt):
     compare(p, out, lse, host, 1, "batch 4100 %d/%d %s" % (hq, hkv, fmt))
 
 
-@pytest.mark.parametrize("hq,hkv", [(8, 1), (32, 1)])
-def test_decode_large_batch_head_dim_128(hq, hkv):
+@pytest.mark.parametrize("hq,hkv,fmt", [(8, 1, "native"), (32, 1, "native"), (8, 1, "fp8"), (2, 2, "fp8")])
+def test_decode_large_batch_head_dim_128(hq, hkv, fmt):
     """2100 sequences at head_dim 128: with 8-head units the unit tables of a 2048-sequence slice
-    leave no room for two CTAs an SM in the group kernel's shared memory, so that launch runs one
-    CTA an SM; the MQA unit keeps two."""
+    leave no room for two CTAs an SM in the group kernels' shared memory, so those launches run one
+    CTA an SM; the MQA unit and the FP8 MHA unit keep two."""
     rng = np.random.default_rng(99 + hq)
     lens = [int(x) for x in rng.integers(0, 200, 2100)]
     p = make(rng, lens=lens, q_lens=[1] * len(lens), hq=hq, hkv=hkv, d=128, bs=16, dtype=W.BF16, causal=False,
-             kv_format="native", seed=93 + hq)
+             kv_format=fmt, seed=93 + hq)
     cache, scales, host = on_device(p)
     lse = torch.empty((p.batch, hq), dtype=torch.float32, device="cuda")
     out = pkv.paged_attn_decode(cache, to_dev(p.q), to_dev(p.block_tables), to_dev(p.context_lens), scale=p.scale,
                                 num_splits=3, lse=lse, scales=scales)
     torch.cuda.synchronize()
-    compare(p, out, lse, host, 1, "batch 2100 d=128 %d/%d" % (hq, hkv))
+    compare(p, out, lse, host, 1, "batch 2100 d=128 %d/%d %s" % (hq, hkv, fmt))
 
 
 def test_mixed_call_batch_above_2048():

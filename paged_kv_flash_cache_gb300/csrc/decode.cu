@@ -676,11 +676,11 @@ cudaError_t launch_decode_t(const DecodeArgs &a, int grid, cudaStream_t s) {
     const int dev = device_info().device;
     if (dev < 64 && !configured.test(dev)) {
         const int max_smem = (int)DecodeLayout<D, G, FP8>::smem_bytes(kMaxBatch, kDecodeMaxSplits);
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+        cudaError_t e = set_smem_attributes(kern, max_smem);
         if (e != cudaSuccess) return e;
         configured.set(dev);
     } else if (dev >= 64) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = set_smem_attributes(kern, (int)smem);
         if (e != cudaSuccess) return e;
     }
     CUtensorMap tm = {};  // native cache: K and V rows of a page slice per box; FP8: unused

@@ -456,8 +456,7 @@ cudaError_t launch_fp8_t(const DecodeArgs &a, int grid, cudaStream_t s) {
     static DeviceFlags configured;
     const int dev = device_info().device;
     if (!configured.test(dev)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)Fp8Layout<G>::smem_bytes(kMaxBatch8, kDecodeMaxSplits));
+        e = set_smem_attributes(kern, (int)Fp8Layout<G>::smem_bytes(kMaxBatch8, kDecodeMaxSplits));
         if (e != cudaSuccess) return e;
         configured.set(dev);
     }

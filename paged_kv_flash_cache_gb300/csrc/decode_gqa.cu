@@ -498,7 +498,7 @@ cudaError_t launch_gqa_t(const DecodeArgs &a, int grid, cudaStream_t s) {
     auto kern = decode_gqa_kernel<D, G, BF16>;
     static DeviceFlags configured;
     if (!configured.test(info.device)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, info.max_smem);
+        e = set_smem_attributes(kern, info.max_smem);
         if (e != cudaSuccess) return e;
         configured.set(info.device);
     }

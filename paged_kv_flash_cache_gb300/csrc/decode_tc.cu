@@ -533,7 +533,7 @@ cudaError_t launch_tc_t(const DecodeArgs &a, int grid, cudaStream_t s) {
     auto kern = decode_tc_kernel<D, BF16, kM, kCtas>;
     static DeviceFlags configured;
     if (!configured.test(info.device)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, info.max_smem);
+        e = set_smem_attributes(kern, info.max_smem);
         if (e != cudaSuccess) return e;
         configured.set(info.device);
     }

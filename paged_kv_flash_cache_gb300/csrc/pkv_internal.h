@@ -108,6 +108,16 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
     return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
 }
 
+// Opt a kernel in to `max_dynamic_smem` bytes of dynamic shared memory and to the largest shared
+// memory carve-out of the L1 / shared array, so that as many of its CTAs as the shared memory allows
+// are resident on an SM (the decode kernels that run two CTAs an SM rely on it).
+template <typename K>
+inline cudaError_t set_smem_attributes(K *kern, int max_dynamic_smem) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dynamic_smem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+}
+
 // Per-device facts cached on first use.
 struct DeviceInfo {
     int device;

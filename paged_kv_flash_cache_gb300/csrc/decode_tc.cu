@@ -12,26 +12,27 @@
 // is computed and never read (a decode step is bound by the K/V bytes, and the 5th-generation
 // tensor cores have the throughput to spare; with mma.sync the same products bounded the call).
 //
-// Kernel structure (persistent, one CTA per SM, 6 warps):
+// Kernel structure (persistent, 6 warps a CTA; one CTA per SM, or two for units of at most 64
+// heads at head_dim up to 128, see TcLayout):
 //   * units (sequence, unit head, split) are numbered from the context lengths and dealt
 //     round-robin, as in decode.cu; splits start at multiples of 128 tokens;
 //   * warp 4 streams each unit's q (one TMA box per 64-column half: Gu rows, 128-byte swizzle,
-//     into one of two q buffers) and then its 128-token key tiles into a ring of 2..6 slots, a
-//     slot holding a tile's K and then its V: one lane per page issues the page's K boxes and
-//     then its V boxes (one 2-D box per 64-column half, as prefill.cu), with an evict-first L2
-//     policy (each line is read once);
-//   * warp 5 owns TMEM (512 columns: S_0, S_1 of 128 columns, O_0, O_1 of D columns) and one
-//     thread issues the MMAs: S_{t%2} = Q K_t^T for tile t, then O_{u%2} += P_t V_t once the
-//     softmax has written P_t over S_{t%2}, in the order QK(0), QK(1), PV(0), QK(2), PV(1), ... so
-//     that the softmax of tile t + 1 overlaps the P V of tile t;
-//   * warps 0..3: the softmax of TMEM lanes 32w .. 32w + 31 = the unit's heads (warps with no
-//     head rows idle): one row per thread, running max / sum with a lazy rescale (the max moves
-//     only when a score exceeds it by more than 2^8), P written to TMEM as its part rounded to
-//     the input type (columns 0-63) plus the rounded remainder (columns 64-127), the two P V
-//     products accumulating both in FP32, so P is not a rounding to the input type; the unit's
-//     epilogue reads O (double-buffered per unit, so the next unit's products run meanwhile)
-//     and writes the output of a single-split context, or the split's partial and lse for the
-//     merge kernel.
+//     into one of the q buffers) and then its key tiles (128 tokens; 64 at head_dim 256 or with two
+//     CTAs an SM) into a ring of 2..6 slots, a slot holding a tile's K and then its V: one lane per
+//     page issues the page's K boxes and then its V boxes (one 2-D box per 64-column half, as
+//     prefill.cu), with an evict-first L2 policy (each line is read once);
+//   * warp 5 owns the CTA's TMEM (S_0, S_1 of one key tile's columns, then one or two O buffers of
+//     D columns) and one thread issues the MMAs: S_{t%2} = Q K_t^T for tile t, then O += P_t V_t
+//     once the softmax has written P_t over S_{t%2}, in the order QK(0), QK(1), PV(0), QK(2),
+//     PV(1), ... so that the softmax of tile t + 1 overlaps the P V of tile t;
+//   * warps 0..3: the softmax of the unit's heads (M = 128 products: TMEM lanes 32w .. 32w + 31,
+//     one row per thread; M = 64: lanes 0-15 of each quarter, a row's columns split between
+//     threads t and t + 16; warps with no head rows idle): running max / sum with a lazy rescale
+//     (the max moves only when a score exceeds it by more than 2^8), P written to TMEM as its part
+//     rounded to the input type plus the rounded remainder, the two P V products accumulating both
+//     in FP32, so P is not a rounding to the input type; the unit's epilogue reads O (with two O
+//     buffers, while the next unit's products run) and writes the output of a single-split
+//     context, or the split's partial and lse for the merge kernel.
 #include <cuda.h>
 
 #include "decode_common.cuh"

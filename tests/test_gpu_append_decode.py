@@ -298,3 +298,35 @@ def test_decode_head_dim_256_splits_fp32_output(num_splits):
     ref, ref_lse = oracle.attention_of(p, cache_bits(cache))
     check_close(out, ref, "bf16", roundings=0, what="d=256 splits=%d fp32 out" % num_splits)
     np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-5, atol=1e-5)
+
+
+@pytest.mark.parametrize("hq,hkv,d,dtype", [(8, 8, 128, W.F16), (4, 2, 64, W.BF16), (16, 4, 128, W.BF16),
+                                            (16, 2, 64, W.F16), (24, 1, 128, W.BF16)])
+@pytest.mark.parametrize("num_splits", [0, 7])
+def test_decode_workspace_contents_and_repeated_calls(hq, hkv, d, dtype, num_splits):
+    """The workspace needs no initialisation and a call leaves nothing in it that the next call
+    depends on: a workspace full of random bytes, an output full of NaN (the rows of the empty
+    context must be written) and three calls on the same workspace give the same bits, within the
+    oracle's bounds, on every split-kernel path (CUDA cores, mma.sync groups, tcgen05)."""
+    p = problem(lens=[0, 700, 1, 2500, 129, 2048], hq=hq, hkv=hkv, d=d, dtype=dtype, bs=16, mb=160,
+                seed=hq + 3 * hkv + d)
+    cache = device_cache(p)
+    q, bt, ctx = to_dev(p.q), to_dev(p.block_tables), to_dev(p.context_lens)
+    need = pkv.decode_workspace_size(p.batch, hq, hkv, d, 16, bt.shape[1], num_splits)
+    assert need > 0
+    gen = torch.Generator(device="cuda").manual_seed(11)
+    ws = torch.randint(0, 256, (need,), dtype=torch.uint8, device="cuda", generator=gen)
+    ws[: need // 3].fill_(255)
+    runs = []
+    for _ in range(3):
+        out = torch.full((p.batch, hq, d), float("nan"), dtype=q.dtype, device="cuda")
+        lse = torch.full((p.batch, hq), float("nan"), dtype=torch.float32, device="cuda")
+        pkv.paged_attn_decode(cache, q, bt, ctx, scale=p.scale, num_splits=num_splits, workspace=ws, out=out, lse=lse)
+        torch.cuda.synchronize()
+        assert pkv.get_device_error() == 0
+        runs.append((out.cpu(), lse.cpu()))
+    for o, l in runs[1:]:
+        assert torch.equal(o, runs[0][0]) and torch.equal(l, runs[0][1])
+    ref, ref_lse = oracle.attention_of(p, cache_bits(cache))
+    check_close(runs[0][0], ref, dtype, roundings=1, what="hq=%d hkv=%d d=%d splits=%d" % (hq, hkv, d, num_splits))
+    np.testing.assert_allclose(runs[0][1].numpy(), ref_lse, rtol=1e-5, atol=1e-5)

@@ -308,3 +308,29 @@ def test_fp8_prefill_tiny_zero_and_growing_v_scales(dtype):
     assert pkv.get_device_error() == 0
     ref_d, _ = oracle.attention_of(p, host(codes, scales), q=qd, cu_q_lens=W.cu_lens([1, 1, 1]))
     check_close(dec, ref_d, dtype, roundings=roundings(p), what="fp8 decode growing scales %s" % dtype)
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(8, 8, 128), (32, 4, 128), (16, 2, 64)])
+def test_fp8_decode_workspace_contents_and_repeated_calls(hq, hkv, d):
+    """Over an FP8 cache too: a workspace of random bytes, an output full of NaN and three calls on
+    the same workspace give the same bits, within the oracle's bounds."""
+    p = problem(lens=[0, 700, 1, 2500, 129, 2048], hq=hq, hkv=hkv, d=d, dtype=W.BF16, bs=16, mb=160, seed=hq + d)
+    codes, scales = device_fp8(p)
+    q, bt, ctx = to_dev(p.q), to_dev(p.block_tables), to_dev(p.context_lens)
+    need = pkv.decode_workspace_size(p.batch, hq, hkv, d, 16, bt.shape[1], 7)
+    gen = torch.Generator(device="cuda").manual_seed(12)
+    ws = torch.randint(0, 256, (need,), dtype=torch.uint8, device="cuda", generator=gen)
+    runs = []
+    for _ in range(3):
+        out = torch.full((p.batch, hq, d), float("nan"), dtype=q.dtype, device="cuda")
+        lse = torch.full((p.batch, hq), float("nan"), dtype=torch.float32, device="cuda")
+        pkv.paged_attn_decode(codes, q, bt, ctx, scale=p.scale, num_splits=7, workspace=ws, out=out, lse=lse,
+                              scales=scales)
+        torch.cuda.synchronize()
+        assert pkv.get_device_error() == 0
+        runs.append((out.cpu(), lse.cpu()))
+    for o, l in runs[1:]:
+        assert torch.equal(o, runs[0][0]) and torch.equal(l, runs[0][1])
+    ref, ref_lse = oracle.attention_of(p, host(codes, scales))
+    check_close(runs[0][0], ref, W.BF16, roundings=roundings(p), what="fp8 hq=%d hkv=%d d=%d" % (hq, hkv, d))
+    np.testing.assert_allclose(runs[0][1].numpy(), ref_lse, rtol=1e-5, atol=1e-5)

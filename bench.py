@@ -74,9 +74,11 @@ def profile_case(args):
         pkv.kv_cache_append(cache, k, v, cu, zeros, bt)
         q, ctx = p.q.cuda(), p.context_lens.cuda()
         out = torch.empty((p.batch, 32, 128), dtype=torch.float16, device="cuda")
+        step = W.append_step(p, seed=7)  # the decode step's token, as the bench's step appends it
+        bt_step, k_step, v_step = step["block_tables"].cuda(), step["k_new"].cuda(), step["v_new"].cuda()
         for _ in range(args.warmup + args.steps):
             if args.profile == "decode":
-                pkv.paged_attn_decode(cache, q, bt, ctx, scale=p.scale, out=out)
+                pkv.paged_attn_decode_step(cache, q, bt_step, ctx, k_step, v_step, scale=p.scale, out=out)
             else:
                 pkv.kv_cache_append(cache, k, v, cu, zeros, bt)
         torch.cuda.synchronize()
@@ -369,14 +371,16 @@ def device_problem(p, torch):
     return cache
 
 
-def decode_bytes(p) -> dict:
+def decode_bytes(p, appended=False) -> dict:
     """Algorithmic bytes of one decode call: K/V of every cached token once per KV head, q in,
-    output out, the block-table entries and context lengths read."""
+    output out, the block-table entries and context lengths read; with `appended` (a decode step),
+    also the new token's K and V rows read and written."""
     kv = p.kv_bytes_read()
     qo = 2 * p.batch * p.num_q_heads * p.head_dim * 2
     pages = sum((int(L) + p.block_size - 1) // p.block_size for L in p.context_lens.tolist())
     table = pages * 4 + p.batch * 4
-    return {"kv": kv, "total": kv + qo + table}
+    app = 2 * 2 * p.batch * p.num_kv_heads * p.head_dim * 2 if appended else 0
+    return {"kv": kv, "append": app, "total": kv + qo + table + app}
 
 
 def time_loop(torch, fn, steps, stream, inner_events=None):
@@ -400,21 +404,19 @@ def bench_decode(torch, p, steps, warmup, dist, want_clocks=True):
     step_in = W.append_step(p, seed=7)
     bt = step_in["block_tables"].cuda()
     k_new, v_new = step_in["k_new"].cuda(), step_in["v_new"].cuda()
-    cu_new, before = step_in["cu_new_lens"].cuda(), step_in["ctx_before"].cuda()
     mb = bt.shape[1]
     ws_bytes = pkv.decode_workspace_size(p.batch, p.num_q_heads, p.num_kv_heads, p.head_dim, p.block_size, mb)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
     out = torch.empty((p.batch, p.num_q_heads, p.head_dim), dtype=q.dtype, device="cuda")
     stream = torch.cuda.current_stream()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
 
-    def step(i, timed=False):
-        if timed:
-            ev[i][0].record(stream)
-        pkv.paged_attn_decode(cache, q, bt, ctx, scale=p.scale, workspace=ws, out=out)
-        if timed:
-            ev[i][1].record(stream)
-        pkv.kv_cache_append(cache, k_new, v_new, cu_new, before, bt)
+    # one decode step: attend each sequence's context, append its new token at position
+    # context_lens[b] (one call: the split kernel writes the new rows, then the merge). The step is
+    # that one call, so the call's average duration is the timed loop's time per step; events
+    # around each call would also stop each step's first kernel from overlapping the previous
+    # step's tail (programmatic dependent launch), which a serving loop does not do.
+    def step(i):
+        pkv.paged_attn_decode_step(cache, q, bt, ctx, k_new, v_new, scale=p.scale, workspace=ws, out=out)
 
     for i in range(warmup):
         step(i)
@@ -432,7 +434,7 @@ def bench_decode(torch, p, steps, warmup, dist, want_clocks=True):
     t0 = time.time()
 
     def timed_step(i):
-        step(i, True)
+        step(i)
         if nvml and (i == steps // 2 or i == steps - 1):
             nvml.probe()  # the GPU is executing the steps enqueued before this one
 
@@ -440,7 +442,7 @@ def bench_decode(torch, p, steps, warmup, dist, want_clocks=True):
     torch.cuda.synchronize()
     t1 = time.time()
     dist.barrier()
-    decode_ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+    decode_ms = ms / steps  # the step is the one call
     clocks = None
     if sampler:
         time.sleep(0.25)
@@ -455,13 +457,12 @@ def bench_decode(torch, p, steps, warmup, dist, want_clocks=True):
         nvml.close()
     assert pkv.get_device_error() == 0
     res = {"ms_total": ms, "ms_per_step": ms / steps, "decode_ms": decode_ms, "clocks": clocks,
-           "launches_per_step": 3, "bytes": decode_bytes(p)}
+           "launches_per_step": 2, "bytes": decode_bytes(p, appended=True)}
     # end to end through the public API: inputs copied from pinned host memory every step, the
     # step's output read back. The step's inputs (q, the new K/V, their offsets and positions, the
     # tables and lengths) sit in one pinned host buffer, 16-byte aligned pieces, and go to the
     # device in one transfer a step; the calls take device views of its pieces.
-    host_parts = [p.q.cpu(), step_in["k_new"], step_in["v_new"], step_in["cu_new_lens"], step_in["ctx_before"],
-                  step_in["block_tables"], p.context_lens]
+    host_parts = [p.q.cpu(), step_in["k_new"], step_in["v_new"], step_in["block_tables"], p.context_lens]
     offs, total = [], 0
     for t in host_parts:
         offs.append(total)
@@ -473,15 +474,14 @@ def bench_decode(torch, p, steps, warmup, dist, want_clocks=True):
         nb = t.numel() * t.element_size()
         h_stage[o:o + nb].copy_(t.contiguous().flatten().view(torch.uint8))
         views.append(d_stage[o:o + nb].view(t.dtype).view(t.shape))
-    d_q, d_k, d_v, d_cu, d_before, d_bt, d_ctx = views
+    d_q, d_k, d_v, d_bt, d_ctx = views
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host_parts)
     d2h = h_out.numel() * h_out.element_size()
 
     def e2e_step(i):
         d_stage.copy_(h_stage, non_blocking=True)
-        pkv.paged_attn_decode(cache, d_q, d_bt, d_ctx, scale=p.scale, workspace=ws, out=out)
-        pkv.kv_cache_append(cache, d_k, d_v, d_cu, d_before, d_bt)
+        pkv.paged_attn_decode_step(cache, d_q, d_bt, d_ctx, d_k, d_v, scale=p.scale, workspace=ws, out=out)
         h_out.copy_(out, non_blocking=True)
 
     for i in range(warmup):
@@ -951,8 +951,9 @@ def main():
     workload_cfg = {"workload": "7B-like paged decode step: batch 16, 32 heads x head_dim 128, fp16, block_size 16, "
                                 "contexts uniform in [1024, 8192] (seeded), pages shuffled over a pool 1.2x the "
                                 "pages needed",
-                    "step": "paged_attn_decode (split-KV kernel + merge kernel) then kv_cache_append of the new "
-                            "token (16 tokens)",
+                    "step": "paged_attn_decode_step: attention over each context (split-KV kernel, whose merge "
+                            "warps also append the step's new token at position context_lens[b], 16 tokens) + "
+                            "merge kernel",
                     "l2": "inputs larger than L2: %.2f GB of K/V read per step vs 129 MB L2" % 0,
                     "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
     if args.impl == "reference":
@@ -1002,7 +1003,8 @@ def main():
     e2e_ms = dist.max(r["e2e_ms_per_step"])
     achieved = r["bytes"]["total"] / (r["decode_ms"] * 1e-3) / 1e9
     files = ["decode.cu", "decode_common.cuh", "pkv_device.cuh", "pkv_internal.h"]
-    roofline = {"bound": "hbm", "kernel": "paged_attn_decode call (decode_split_kernel + combine_kernel)",
+    roofline = {"bound": "hbm", "kernel": "paged_attn_decode_step call (decode_split_kernel, which also writes the "
+                "step's new K/V rows, + combine_kernel)",
                 "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / pk["hbm_gbs"], 3), "peak_source": pk["source"],
                 "traffic": ncu_traffic("decode_split_7b_ncu.txt", files),

@@ -162,6 +162,30 @@ PKV_API pkv_status pkv_paged_attn_decode(pkv_cache cache, const void *q, int num
                                  void *workspace, size_t workspace_bytes,
                                  void *out, pkv_dtype out_dtype, float *lse, void *stream);
 
+/* paged_attn_decode_step -- one decode step in one call: the attention of
+ * pkv_paged_attn_decode over each sequence's context_lens[b] cached tokens, and the
+ * append of the step's new token, whose K and V go to position context_lens[b] (attend,
+ * then append: [ON2] decode; position -> page and offset as pkv_kv_cache_append).
+ * Arguments as pkv_paged_attn_decode, plus
+ *   k_new, v_new  [batch, Hkv, D] in the cache's 16-bit type (over an FP8 cache: quantised
+ *                 to E4M3 codes + row scales as pkv_kv_cache_append does); device, 16-byte
+ *                 aligned, required when batch > 0 (else PKV_ERR_INVALID_ARG).
+ * The attention reads positions below context_lens[b] only, so the result is that of
+ * pkv_paged_attn_decode followed by pkv_kv_cache_append of one token per sequence, bit for
+ * bit (outputs, lse and every cache element). The caller advances context_lens by one for
+ * the next step. A position context_lens[b] outside the table (the table full) or a page id
+ * outside the pool is skipped and flags PKV_ERR_DEVICE_RANGE; the attention still runs.
+ * Launches: on a 16-bit cache with 1, 2, 4 or 8 query heads per KV head (head_dim 64 or
+ * 128) the split kernel writes the new rows itself (its merge warps, before their first
+ * unit), so the call is the split kernel and its merge; otherwise the append kernel
+ * follows the decode on the same stream. */
+PKV_API pkv_status pkv_paged_attn_decode_step(pkv_cache cache, const void *q, int num_q_heads,
+                                      const int *block_tables, const int *context_lens, int batch,
+                                      int max_blocks_per_seq, float scale, int num_splits,
+                                      void *workspace, size_t workspace_bytes,
+                                      void *out, pkv_dtype out_dtype, float *lse,
+                                      const void *k_new, const void *v_new, void *stream);
+
 /* paged_attn_prefill -- a chunk of queries per sequence against its paged context,
  * causal or not ([ON2] prefill; [FAPA] s2 causal flag; [BLK] s2.2 chunked queries).
  * "Append first, then attend": the chunk's own K/V must already be in the cache.

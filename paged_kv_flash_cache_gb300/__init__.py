@@ -7,8 +7,8 @@ caller does not pass them, and forwards raw device pointers and the current CUDA
 stream. There is no CPU fallback: if the library is missing every call raises.
 
 Entry points (same names as the C ABI without the ``pkv_`` prefix):
-  kv_cache_append, paged_attn_decode, paged_attn_prefill, paged_attn_mixed, attn_combine,
-  decode_workspace_size, decode_split_tokens, get_device_error.
+  kv_cache_append, paged_attn_decode, paged_attn_decode_step, paged_attn_prefill, paged_attn_mixed,
+  attn_combine, decode_workspace_size, decode_split_tokens, get_device_error.
 Cache tensors have shape [num_blocks, 2, num_kv_heads, block_size, head_dim]
 (K at index 0, V at index 1) in float16 or bfloat16, or hold FP8 E4M3 codes
 (torch.float8_e4m3fn or uint8) with a float32 `scales` tensor
@@ -26,7 +26,7 @@ from typing import Optional
 __all__ = [
     "PkvError", "library_path", "load_library", "kv_cache_append", "paged_attn_decode", "paged_attn_prefill",
     "attn_combine", "decode_workspace_size", "decode_split_tokens", "get_device_error", "STATUS",
-    "paged_attn_decode_noalloc", "paged_attn_mixed", "selftest_wait_timeout",
+    "paged_attn_decode_noalloc", "paged_attn_mixed", "selftest_wait_timeout", "paged_attn_decode_step",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -41,7 +41,7 @@ KV_NATIVE, KV_FP8_E4M3 = 0, 1
 
 # Every symbol include/pkv.h declares.
 EXPORTS = ("pkv_kv_cache_append", "pkv_decode_workspace_size", "pkv_decode_split_tokens", "pkv_paged_attn_decode",
-           "pkv_paged_attn_decode_noalloc", "pkv_paged_attn_prefill", "pkv_paged_attn_mixed", "pkv_attn_combine",
+           "pkv_paged_attn_decode_step", "pkv_paged_attn_decode_noalloc", "pkv_paged_attn_prefill", "pkv_paged_attn_mixed", "pkv_attn_combine",
            "pkv_get_device_error", "pkv_selftest_wait_timeout", "pkv_status_string", "pkv_version")
 DECODE_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024   # PKV_DECODE_NOALLOC_SCRATCH_BYTES in include/pkv.h
 
@@ -81,6 +81,8 @@ def load_library():
         lib.pkv_decode_split_tokens.restype = I
         lib.pkv_paged_attn_decode.argtypes = [_Cache, P, I, P, P, I, I, F, I, P, Z, P, I, P, P]
         lib.pkv_paged_attn_decode.restype = I
+        lib.pkv_paged_attn_decode_step.argtypes = [_Cache, P, I, P, P, I, I, F, I, P, Z, P, I, P, P, P, P]
+        lib.pkv_paged_attn_decode_step.restype = I
         lib.pkv_paged_attn_decode_noalloc.argtypes = [_Cache, P, I, P, P, I, I, F, I, P, I, P, P]
         lib.pkv_paged_attn_decode_noalloc.restype = I
         lib.pkv_paged_attn_prefill.argtypes = [_Cache, P, I, P, P, P, I, I, I, I, F, I, P, I, P, P]
@@ -222,6 +224,36 @@ def paged_attn_decode(cache, q, block_tables, context_lens, scale: Optional[floa
                                      _dev(workspace, "workspace"), ws_bytes, _dev(out, "out"),
                                      _dtype_code(out.dtype), _dev(lse, "lse"), _stream(stream)),
            "pkv_paged_attn_decode")
+    return out
+
+
+def paged_attn_decode_step(cache, q, block_tables, context_lens, k_new, v_new, scale: Optional[float] = None,
+                           num_splits: int = 0, workspace=None, out=None, out_dtype=None, lse=None, stream=None,
+                           scales=None):
+    """One decode step: paged_attn_decode over context_lens[b] cached tokens, and the step's new
+    token (k_new / v_new [B, Hkv, D]) written at position context_lens[b]. Returns `out`."""
+    torch = _torch()
+    lib = load_library()
+    if k_new.dtype != q.dtype or v_new.dtype != q.dtype or k_new.shape != v_new.shape:
+        raise TypeError("k_new / v_new must match each other and q's dtype")
+    c = _cache_struct(cache, q.dtype, scales)
+    batch, hq, d = q.shape
+    if tuple(k_new.shape) != (batch, cache.shape[2], d):
+        raise ValueError("k_new / v_new must be [batch, num_kv_heads, head_dim]")
+    mb = block_tables.shape[1]
+    if out is None:
+        out = torch.empty((batch, hq, d), dtype=out_dtype or q.dtype, device=q.device)
+    need = decode_workspace_size(batch, hq, cache.shape[2], d, cache.shape[3], mb, num_splits)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    scale = (1.0 / math.sqrt(d)) if scale is None else float(scale)
+    _check(lib.pkv_paged_attn_decode_step(c, _dev(q, "q"), hq, _i32(block_tables, "block_tables"),
+                                          _i32(context_lens, "context_lens"), batch, mb, scale, int(num_splits),
+                                          _dev(workspace, "workspace"), ws_bytes, _dev(out, "out"),
+                                          _dtype_code(out.dtype), _dev(lse, "lse"), _dev(k_new, "k_new"),
+                                          _dev(v_new, "v_new"), _stream(stream)),
+           "pkv_paged_attn_decode_step")
     return out
 
 

@@ -35,12 +35,15 @@ constexpr int kHeadsPerItem = 8;  // a work item is one token's K and V rows of 
 // Page and in-page row of new token t (all lanes of the warp, same t). The sequence is the last b
 // with cu_new_lens[b] <= t, i.e. the count of b in [1, batch) with cu_new_lens[b] <= t (lengths
 // are non-negative): up to 32 sequences, one load per lane and a ballot, ctx_before read in the
-// same round trip; more, a binary search. Returns false (error word set) for a position outside
+// same round trip; more, a binary search; no cu_new_lens (a decode step), sequence t. Returns false (error word set) for a position outside
 // the table or a page id outside the pool.
 __device__ __forceinline__ bool token_slot(const AppendArgs &a, int t, int lane, int &pb, int &off) {
     int b;
     long long pos;
-    if (a.batch <= 32) {
+    if (!a.cu_new_lens) {  // one new token per sequence
+        b = t;
+        pos = __ldg(a.ctx_before + t);
+    } else if (a.batch <= 32) {
         const int cu_j = (lane >= 1 && lane < a.batch) ? __ldg(a.cu_new_lens + lane) : INT_MAX;
         const int ctx_j = lane < a.batch ? __ldg(a.ctx_before + lane) : 0;
         const int cu_b_j = lane < a.batch ? __ldg(a.cu_new_lens + lane) : 0;

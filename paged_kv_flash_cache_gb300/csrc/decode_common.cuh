@@ -119,6 +119,44 @@ __device__ __forceinline__ float tree_sum(const float (&x)[N]) {
     }
 }
 
+// The decode step's append, by the merge warp of each CTA before its first unit (a native cache):
+// row r of the batch's 2 * batch * Hkv new rows -- sequence r / (2 Hkv), head (r / 2) % Hkv, K
+// (even r) or V (odd r) -- goes to position context_lens[b] of its sequence, page
+// block_table[b][pos / block_size], offset pos % block_size, as D / 8 16-byte vectors, one per
+// lane. The attention of the same call reads positions below context_lens[b] only, so the two
+// touch different rows (a page slice that a copy brings in whole holds the new row as one of the
+// rows past the context end, which every kernel masks). A position outside the table or a page
+// outside the pool is flagged (kErrDeviceRange) and skipped, as the append kernel does.
+template <int D>
+__device__ __forceinline__ void append_step_rows(const DecodeArgs &a, int lane) {
+    constexpr int kVec = D / 8;            // 16-byte vectors a row
+    constexpr int kRowsPerPass = 32 / kVec;
+    const int hkv = a.cache.num_kv_heads, bs = a.cache.block_size;
+    const int nrows = 2 * a.batch * hkv;
+    const int sub = lane / kVec, e = lane % kVec;
+    const long long cap = (long long)a.max_blocks_per_seq * bs;
+    uint4 *cache = static_cast<uint4 *>(const_cast<void *>(a.cache.ptr));
+    for (int r0 = blockIdx.x * kRowsPerPass; r0 < nrows; r0 += gridDim.x * kRowsPerPass) {
+        const int r = r0 + sub;
+        if (r >= nrows) continue;
+        const int kv = r & 1, bh = r >> 1;
+        const int b = bh / hkv, h = bh - b * hkv;
+        const uint4 v = __ldg(static_cast<const uint4 *>(kv ? a.v_new : a.k_new) + (size_t)bh * kVec + e);
+        const int pos = __ldg(a.context_lens + b);
+        if (pos < 0 || pos >= cap) {
+            if (e == 0) set_error(a.err, kErrDeviceRange);
+            continue;
+        }
+        const int pb = __ldg(a.block_tables + (size_t)b * a.max_blocks_per_seq + (pos >> a.cache.log2_block_size));
+        if (pb < 0 || pb >= a.cache.num_blocks) {
+            if (e == 0) set_error(a.err, kErrDeviceRange);
+            continue;
+        }
+        const size_t row = (((size_t)pb * 2 + kv) * hkv + h) * bs + (pos & (bs - 1));
+        cache[row * kVec + e] = v;
+    }
+}
+
 // The merge warp of a decode CTA. At the end of a unit each of the W token slices leaves its
 // (acc[D], m, l) row per query head of the unit in merge buffer i ([W][G][kMergeRow<D>] floats; m
 // in log2 units, acc and l relative to 2^m), the unit id is written (warp 0) and mfull[i] completes;
@@ -138,6 +176,7 @@ __device__ __forceinline__ bool merge_warp_loop(const DecodeArgs &a, const UnitT
     constexpr int V = D / 32;  // consecutive dims per lane
     static_assert(V == 2 || V == 4, "head_dim 64 or 128");
     const int hkv = a.cache.num_kv_heads * a.head_groups, chunk = a.chunk;  // unit heads
+    if (a.k_new && !a.cache.fp8) append_step_rows<D>(a, lane);
     int mbuf = 0;
     uint32_t mphase = 0;
     for (;;) {

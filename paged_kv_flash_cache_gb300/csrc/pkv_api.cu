@@ -224,7 +224,8 @@ namespace {
 pkv_status decode_impl(const pkv_cache &cache, const void *q, int num_q_heads, const int *block_tables,
                        const int *context_lens, const int *cu_q_lens, int batch, int q_rows, int max_blocks_per_seq,
                        float scale, int num_splits, void *workspace, size_t workspace_bytes, void *out,
-                       pkv_dtype out_dtype, float *lse, void *stream) {
+                       pkv_dtype out_dtype, float *lse, void *stream, const void *k_new = nullptr,
+                       const void *v_new = nullptr) {
     pkv_status st = check_cache(cache);
     if (st != PKV_OK) return st;
     if ((st = check_out_dtype(out_dtype, cache.dtype)) != PKV_OK) return st;
@@ -292,6 +293,11 @@ pkv_status decode_impl(const pkv_cache &cache, const void *q, int num_q_heads, c
     a.out_dtype = (int)out_dtype;
     a.lse = lse;
     a.err = s->err_ptr;
+    // a decode step's append goes with the kernels that have a merge warp (16-bit cache, CUDA-core
+    // and mma.sync paths); the others get the append kernel after the decode
+    const bool fused_append = k_new && !fp8 && path != kTcgen05;
+    a.k_new = fused_append ? k_new : nullptr;
+    a.v_new = fused_append ? v_new : nullptr;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const int grid = s->info.num_sms * s->info.decode_ctas_per_sm;
     // The kernels keep a launch's unit tables in shared memory, so a batch runs in slices of at
@@ -321,6 +327,11 @@ pkv_status decode_impl(const pkv_cache &cache, const void *q, int num_q_heads, c
             d.part_o = a.part_o + (size_t)b0 * num_q_heads * s_max * cache.head_dim;
             d.part_lse = a.part_lse + (size_t)b0 * num_q_heads * s_max;
         }
+        if (fused_append) {
+            const size_t row_bytes = (size_t)cache.num_kv_heads * cache.head_dim * 2;
+            d.k_new = static_cast<const uint8_t *>(k_new) + (size_t)b0 * row_bytes;
+            d.v_new = static_cast<const uint8_t *>(v_new) + (size_t)b0 * row_bytes;
+        }
         cudaError_t le;
         switch (path) {
             case kFp8Tensor: le = launch_decode_fp8(d, grid, cs); break;
@@ -345,6 +356,28 @@ pkv_status decode_impl(const pkv_cache &cache, const void *q, int num_q_heads, c
         c.lse = d.lse;
         if (launch_combine(c, cs) != cudaSuccess) return PKV_ERR_CUDA;
     }
+    if (k_new && !fused_append) {
+        AppendArgs ap;
+        ap.cache = const_cast<void *>(cache.ptr);
+        ap.num_blocks = cache.num_blocks;
+        ap.num_kv_heads = cache.num_kv_heads;
+        ap.block_size = cache.block_size;
+        ap.log2_block_size = ilog2(cache.block_size);
+        ap.head_dim = cache.head_dim;
+        ap.dtype = (int)cache.dtype;
+        ap.fp8 = fp8 ? 1 : 0;
+        ap.scales = fp8 ? cache.scales : nullptr;
+        ap.k_new = k_new;
+        ap.v_new = v_new;
+        ap.cu_new_lens = nullptr;  // one token per sequence, at position context_lens[b]
+        ap.ctx_before = context_lens;
+        ap.block_tables = block_tables;
+        ap.batch = batch;
+        ap.max_blocks_per_seq = max_blocks_per_seq;
+        ap.num_new_tokens = batch;
+        ap.err = s->err_ptr;
+        if (launch_append(ap, cs) != cudaSuccess) return PKV_ERR_CUDA;
+    }
     return PKV_OK;
 }
 
@@ -359,6 +392,16 @@ pkv_status pkv_paged_attn_decode(pkv_cache cache, const void *q, int num_q_heads
                                  pkv_dtype out_dtype, float *lse, void *stream) {
     return decode_impl(cache, q, num_q_heads, block_tables, context_lens, nullptr, batch, batch, max_blocks_per_seq,
                        scale, num_splits, workspace, workspace_bytes, out, out_dtype, lse, stream);
+}
+
+pkv_status pkv_paged_attn_decode_step(pkv_cache cache, const void *q, int num_q_heads, const int *block_tables,
+                                      const int *context_lens, int batch, int max_blocks_per_seq, float scale,
+                                      int num_splits, void *workspace, size_t workspace_bytes, void *out,
+                                      pkv_dtype out_dtype, float *lse, const void *k_new, const void *v_new,
+                                      void *stream) {
+    if (batch > 0 && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))) return PKV_ERR_INVALID_ARG;
+    return decode_impl(cache, q, num_q_heads, block_tables, context_lens, nullptr, batch, batch, max_blocks_per_seq,
+                       scale, num_splits, workspace, workspace_bytes, out, out_dtype, lse, stream, k_new, v_new);
 }
 
 pkv_status pkv_attn_combine(const float *partial_o, const float *partial_lse, int n_rows, int num_splits,

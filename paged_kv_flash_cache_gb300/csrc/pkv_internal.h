@@ -27,6 +27,7 @@ struct AppendArgs {
     int fp8;        // 1: quantise into E4M3 codes + per-row scales
     float *scales;
     const void *k_new, *v_new;
+    // cu_new_lens nullptr: one new token per sequence (a decode step), token t being sequence t's
     const int *cu_new_lens, *ctx_before, *block_tables;
     int batch, max_blocks_per_seq, num_new_tokens;
     int *err;
@@ -58,6 +59,10 @@ struct DecodeArgs {
     int out_dtype;
     float *lse;
     int *err;
+    // Decode step on the kernels with a merge warp (a native cache on the CUDA-core and mma.sync
+    // paths): the new token's K and V rows [batch, Hkv, D], which the merge warps write at
+    // position context_lens[b] of each sequence before their first unit. nullptr: no append.
+    const void *k_new, *v_new;
 };
 
 struct CombineArgs {

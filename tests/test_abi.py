@@ -79,6 +79,13 @@ def test_host_validation_without_gpu(lib):
               None)
     assert lib.pkv_paged_attn_decode(*fp8_64) == 2
     assert lib.pkv_paged_attn_decode(*args(2, out_dt=1)) == 2   # bf16 out for an fp16 cache
+    # decode step: the new token's K and V are required (and 16-byte aligned) when batch > 0; a
+    # step whose decode is refused is refused whole
+    step = lambda hq, k, v: args(hq)[:-1] + (k, v, None)
+    assert lib.pkv_paged_attn_decode_step(*step(2, None, good)) == 1
+    assert lib.pkv_paged_attn_decode_step(*step(2, good, P(4100))) == 1
+    assert lib.pkv_paged_attn_decode_step(*step(3, good, good)) == 1
+    assert lib.pkv_paged_attn_decode_step(*(fp8_args(6)[:-1] + (good, good, None))) == 2
     # prefill: negative total_q
     assert lib.pkv_paged_attn_prefill(_cache(), good, 2, good, good, good, 1, 4, -1, 4, F(0.1), 1, good, 0, None,
                                       None) == 1

@@ -330,3 +330,54 @@ def test_decode_workspace_contents_and_repeated_calls(hq, hkv, d, dtype, num_spl
     ref, ref_lse = oracle.attention_of(p, cache_bits(cache))
     check_close(runs[0][0], ref, dtype, roundings=1, what="hq=%d hkv=%d d=%d splits=%d" % (hq, hkv, d, num_splits))
     np.testing.assert_allclose(runs[0][1].numpy(), ref_lse, rtol=1e-5, atol=1e-5)
+
+
+@pytest.mark.parametrize("hq,hkv,d,dtype", [(8, 8, 128, W.F16), (4, 2, 64, W.BF16), (16, 4, 128, W.BF16),
+                                            (16, 2, 64, W.F16), (24, 1, 128, W.BF16), (4, 2, 256, W.BF16)])
+@pytest.mark.parametrize("bs", [16, 64])
+def test_decode_step_is_decode_then_append(hq, hkv, d, dtype, bs):
+    """paged_attn_decode_step: the same output and lse bits as paged_attn_decode over the context,
+    and the cache of the oracle's append of the step's token at position context_lens[b] (the
+    append written by the split kernel's merge warps for groups of 1, 2, 4, 8 at head_dim 64/128;
+    by the append kernel after the tcgen05 decode for 24 heads on one KV head and head_dim 256)."""
+    p = problem(lens=[0, 700, 1, 2500, 129, 2047, 64], hq=hq, hkv=hkv, d=d, dtype=dtype, bs=bs, mb=2560 // bs,
+                seed=hq + hkv + d + bs, extra=9)
+    step = W.append_step(p, seed=5)
+    cache = device_cache(p)
+    q, bt, ctx = to_dev(p.q), to_dev(step["block_tables"]), to_dev(p.context_lens)
+    ref_lse = torch.empty((p.batch, hq), dtype=torch.float32, device="cuda")
+    ref_out = pkv.paged_attn_decode(cache, q, bt, ctx, scale=p.scale, num_splits=3, lse=ref_lse)
+    torch.cuda.synchronize()
+    ref_bits = cache_bits(cache)
+    assert oracle.kv_cache_append(ref_bits, step["k_new"], step["v_new"], step["cu_new_lens"], step["ctx_before"],
+                                  step["block_tables"]) == 0
+    lse = torch.full((p.batch, hq), float("nan"), dtype=torch.float32, device="cuda")
+    out = pkv.paged_attn_decode_step(cache, q, bt, ctx, to_dev(step["k_new"]), to_dev(step["v_new"]), scale=p.scale,
+                                     num_splits=3, lse=lse)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
+    assert np.array_equal(cache_bits(cache), ref_bits)
+
+
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 2)])
+def test_decode_step_full_table_is_flagged_and_skipped(hq, hkv):
+    """A sequence whose table is full (context_lens[b] = capacity) has no position for the step's
+    token: that token is skipped and PKV_ERR_DEVICE_RANGE raised; the others are appended and the
+    attention is that of the whole contexts."""
+    bs, mb = 16, 8
+    p = problem(lens=[bs * mb, 40, bs * mb - 1], hq=hq, hkv=hkv, d=128, dtype=W.F16, bs=bs, mb=mb, extra=4)
+    cache = device_cache(p)
+    bt, ctx, q = to_dev(p.block_tables), to_dev(p.context_lens), to_dev(p.q)
+    gen = torch.Generator().manual_seed(8)
+    k_new = torch.randn(p.batch, hkv, 128, generator=gen).to(torch.float16)
+    v_new = torch.randn(p.batch, hkv, 128, generator=gen).to(torch.float16)
+    ref_out = pkv.paged_attn_decode(cache, q, bt, ctx, scale=p.scale)
+    torch.cuda.synchronize()
+    ref_bits = cache_bits(cache)
+    assert oracle.kv_cache_append(ref_bits, k_new, v_new, W.cu_lens([1] * p.batch), p.context_lens,
+                                  p.block_tables) == -1
+    out = pkv.paged_attn_decode_step(cache, q, bt, ctx, to_dev(k_new), to_dev(v_new), scale=p.scale)
+    assert pkv.get_device_error() == 5
+    assert torch.equal(out, ref_out)
+    assert np.array_equal(cache_bits(cache), ref_bits)

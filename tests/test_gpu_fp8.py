@@ -334,3 +334,24 @@ def test_fp8_decode_workspace_contents_and_repeated_calls(hq, hkv, d):
     ref, ref_lse = oracle.attention_of(p, host(codes, scales))
     check_close(runs[0][0], ref, W.BF16, roundings=roundings(p), what="fp8 hq=%d hkv=%d d=%d" % (hq, hkv, d))
     np.testing.assert_allclose(runs[0][1].numpy(), ref_lse, rtol=1e-5, atol=1e-5)
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(8, 2, 128), (4, 4, 64)])
+def test_fp8_decode_step_is_decode_then_append(hq, hkv, d):
+    """paged_attn_decode_step over an FP8 cache: the decode's output bits, and the oracle's
+    quantising append of the step's token (the append kernel runs after the decode)."""
+    p = problem(lens=[100, 31, 512, 7, 0], hq=hq, hkv=hkv, d=d, bs=16, dtype=W.BF16, extra=12, mb=40)
+    codes, scales = device_fp8(p)
+    step = W.append_step(p, seed=6)
+    q, bt, ctx = to_dev(p.q), to_dev(step["block_tables"]), to_dev(p.context_lens)
+    ref_out = pkv.paged_attn_decode(codes, q, bt, ctx, scale=p.scale, scales=scales)
+    torch.cuda.synchronize()
+    ref_cache = host(codes, scales)
+    assert oracle.kv_cache_append_fp8(ref_cache, p.dtype, **step) == 0
+    out = pkv.paged_attn_decode_step(codes, q, bt, ctx, to_dev(step["k_new"]), to_dev(step["v_new"]), scale=p.scale,
+                                     scales=scales)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    assert torch.equal(out, ref_out)
+    got = host(codes, scales)
+    assert np.array_equal(got.codes, ref_cache.codes) and np.array_equal(got.scales, ref_cache.scales)

@@ -459,38 +459,74 @@ def bench_decode(torch, p, steps, warmup, dist, want_clocks=True):
     res = {"ms_total": ms, "ms_per_step": ms / steps, "decode_ms": decode_ms, "clocks": clocks,
            "launches_per_step": 2, "bytes": decode_bytes(p, appended=True)}
     # end to end through the public API: inputs copied from pinned host memory every step, the
-    # step's output read back. The step's inputs (q, the new K/V, their offsets and positions, the
-    # tables and lengths) sit in one pinned host buffer, 16-byte aligned pieces, and go to the
-    # device in one transfer a step; the calls take device views of its pieces.
+    # step's output read back. The step's inputs (q, the new K/V, the tables and lengths) sit in one
+    # pinned host buffer, 16-byte aligned pieces, and go to the device in one transfer a step; the
+    # call takes device views of its pieces. Copies run on streams of their own (the copy engines),
+    # two slots deep: step i's inputs upload while step i - 1 computes, and step i's output is read
+    # back while step i + 1 computes. Every step's transfers lie inside the timed region, which
+    # ends when the last read-back has landed.
     host_parts = [p.q.cpu(), step_in["k_new"], step_in["v_new"], step_in["block_tables"], p.context_lens]
     offs, total = [], 0
     for t in host_parts:
         offs.append(total)
         total += (t.numel() * t.element_size() + 15) // 16 * 16
     h_stage = torch.empty(total, dtype=torch.uint8).pin_memory()
-    d_stage = torch.empty(total, dtype=torch.uint8, device="cuda")
-    views = []
     for t, o in zip(host_parts, offs):
         nb = t.numel() * t.element_size()
         h_stage[o:o + nb].copy_(t.contiguous().flatten().view(torch.uint8))
-        views.append(d_stage[o:o + nb].view(t.dtype).view(t.shape))
-    d_q, d_k, d_v, d_bt, d_ctx = views
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    d_stage, views = [], []
+    for _ in range(2):
+        d = torch.empty(total, dtype=torch.uint8, device="cuda")
+        d_stage.append(d)
+        views.append([d[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+                      for t, o in zip(host_parts, offs)])
+    outs = [torch.empty_like(out) for _ in range(2)]
+    h_outs = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host_parts)
-    d2h = h_out.numel() * h_out.element_size()
+    d2h = h_outs[0].numel() * h_outs[0].element_size()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]     # slot's inputs on the device
+    ev_done = [torch.cuda.Event() for _ in range(2)]   # slot's step computed
+    ev_back = [torch.cuda.Event() for _ in range(2)]   # slot's output read back
 
     def e2e_step(i):
-        d_stage.copy_(h_stage, non_blocking=True)
-        pkv.paged_attn_decode_step(cache, d_q, d_bt, d_ctx, d_k, d_v, scale=p.scale, workspace=ws, out=out)
-        h_out.copy_(out, non_blocking=True)
+        j = i & 1
+        up.wait_event(ev_done[j])       # the slot's previous step has read its inputs
+        with torch.cuda.stream(up):
+            d_stage[j].copy_(h_stage, non_blocking=True)
+        ev_in[j].record(up)
+        stream.wait_event(ev_in[j])
+        stream.wait_event(ev_back[j])   # the slot's previous output has been read back
+        d_q, d_k, d_v, d_bt, d_ctx = views[j]
+        pkv.paged_attn_decode_step(cache, d_q, d_bt, d_ctx, d_k, d_v, scale=p.scale, workspace=ws, out=outs[j])
+        ev_done[j].record(stream)
+        down.wait_event(ev_done[j])
+        with torch.cuda.stream(down):
+            h_outs[j].copy_(outs[j], non_blocking=True)
+        ev_back[j].record(down)
 
-    for i in range(warmup):
-        e2e_step(i)
+    def e2e_loop(n):
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        up.wait_stream(stream)
+        down.wait_stream(stream)
+        for i in range(n):
+            e2e_step(i)
+        stream.wait_stream(down)
+        stream.wait_stream(up)
+        end.record(stream)
+        end.synchronize()
+        return start.elapsed_time(end)
+
+    e2e_loop(max(warmup, 1))
+    torch.cuda.synchronize()
+    # the same inputs as the device-resident steps: the read-back output is theirs, bit for bit
+    assert torch.equal(h_outs[(max(warmup, 1) - 1) & 1], out.cpu()), "end-to-end step output differs"
+    dist.barrier()
+    e2e_ms = e2e_loop(steps)
     torch.cuda.synchronize()
     dist.barrier()
-    e2e_ms = time_loop(torch, e2e_step, steps, stream)
-    torch.cuda.synchronize()
-    dist.barrier()
+    assert pkv.get_device_error() == 0
     res.update(e2e_ms_per_step=e2e_ms / steps, h2d=h2d, d2h=d2h)
     del cache
     torch.cuda.empty_cache()

@@ -125,14 +125,17 @@ PKV_API pkv_status pkv_kv_cache_append(pkv_cache cache, const void *k_new, const
                                int num_new_tokens, void *stream);
 
 /* Bytes of workspace pkv_paged_attn_decode needs for these sizes: the FP32 split
- * partials, or 0 when no context can span several splits.  num_splits as passed to
- * pkv_paged_attn_decode (0 = automatic). */
+ * partials (padded to 16 bytes) and a 16-byte slot, or 0 when no context can span several
+ * splits.  num_splits as passed to pkv_paged_attn_decode (0 = automatic). */
 PKV_API size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim,
                                  int block_size, int max_blocks_per_seq, int num_splits);
 
 /* Tokens per split that pkv_paged_attn_decode uses for these sizes (a multiple of
  * 128, and at least capacity / 2048 so that a context has at most 2048 splits); a
- * context of L tokens is cut into ceil(L / chunk) splits. */
+ * context of L tokens is cut into ceil(L / chunk) splits.  With num_splits = 0 this is the
+ * smallest split: the split kernel, which sees the context lengths, may take 1.5, 2, 3 or
+ * 4 times it (rounded up to a multiple of 128) where its model of the launch's time says
+ * the work divides better over its CTAs; the workspace size holds for every choice. */
 PKV_API int pkv_decode_split_tokens(int batch, int num_q_heads, int num_kv_heads, int head_dim,
                             int block_size, int max_blocks_per_seq, int num_splits);
 

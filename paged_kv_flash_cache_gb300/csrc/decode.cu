@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeLayout<D, G, FP8>::kCtas
     const UnitTable ut = unit_table(reinterpret_cast<int *>(smem + L::kIntsOffset), a.batch, a.s_max);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int hkv = a.cache.num_kv_heads, bs = a.cache.block_size, chunk = a.chunk;
+    const int hkv = a.cache.num_kv_heads, bs = a.cache.block_size;
 
     if (tid == 0) {
         for (int i = 0; i < L::kStages; ++i) {
@@ -152,6 +152,7 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeLayout<D, G, FP8>::kCtas
     pdl_wait();
     // ---- prologue: clamp lengths, units per sequence, exclusive scan (all threads) ----
     const int num_units = decode_scan_units<kDecodeThreads>(a, ut);
+    const int chunk = ut.misc[0];  // the launch's split size
 
     if (warp == kProducerWarp) {
         // ================================ producer warp ================================
@@ -603,21 +604,31 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
     int S = a.num_splits;
     bool done_by_split = false;
     size_t out_row = (size_t)row;
+    int len = 0;
     if (row < a.n_rows && a.context_lens) {
         const int b = row / a.rows_per_seq;
-        int len = __ldg(a.context_lens + b);
+        len = __ldg(a.context_lens + b);
         len = len < 0 ? 0 : len;
         if (a.cu_q_lens) {  // mixed batch: rows of prefill chunks are not this kernel's
             const int q0 = __ldg(a.cu_q_lens + b);
             if (__ldg(a.cu_q_lens + b + 1) - q0 != 1) done_by_split = true;
             out_row = (size_t)q0 * a.rows_per_seq + (row - b * a.rows_per_seq);
         }
-        S = (len + a.chunk - 1) / a.chunk;
-        if (S > a.num_splits) S = a.num_splits;
-        done_by_split = done_by_split || (S == 1);  // (or finished by the split kernel)
+        if (!a.chunk_dev) {
+            S = len > 0 ? (len - 1) / a.chunk + 1 : 0;
+            if (S > a.num_splits) S = a.num_splits;
+            done_by_split = done_by_split || (S == 1);  // (or finished by the split kernel)
+        }
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (row >= a.n_rows || done_by_split) return;
+    if (a.chunk_dev && a.context_lens) {
+        // the split size the split kernel chose (written by it; visible after the wait)
+        const int chunk = *a.chunk_dev;
+        S = len > 0 ? (len - 1) / chunk + 1 : 0;
+        if (S > a.num_splits) S = a.num_splits;
+        if (S == 1) return;  // finished by the split kernel
+    }
     const float *pl = a.part_lse + (size_t)row * a.num_splits;
     const float *po = a.part_o + (size_t)row * a.num_splits * D + kPer * lane;
     float M = -INFINITY;

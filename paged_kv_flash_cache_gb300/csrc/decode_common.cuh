@@ -27,12 +27,14 @@ struct UnitCursor {
 //                      first[s] * hkv and number n_s * hkv, n_s = first[s + 1] - first[s]
 //   hist  [s_max + 1]  prologue scratch: sequences per split count, then a fill count
 //   qrow  [batch]      the sequence's query / output row (b, or cu_q_lens[b] in a mixed batch)
+//   misc  [kUnitMisc]  misc[0] the split size of the launch (see decode_scan_units); misc[1..]
+//                      prologue scratch (unit counts of the candidate split sizes)
 struct UnitTable {
-    int *lens, *ord, *first, *hist, *qrow;
+    int *lens, *ord, *first, *hist, *qrow, *misc;
 };
 
 __host__ __device__ constexpr size_t unit_table_ints(int batch, int s_max) {
-    return 3 * (size_t)batch + 2 * ((size_t)s_max + 1);
+    return 3 * (size_t)batch + 2 * ((size_t)s_max + 1) + kUnitMisc;
 }
 
 __device__ __forceinline__ UnitTable unit_table(int *ints, int batch, int s_max) {
@@ -42,6 +44,7 @@ __device__ __forceinline__ UnitTable unit_table(int *ints, int batch, int s_max)
     t.first = ints + 2 * batch;
     t.hist = t.first + s_max + 1;
     t.qrow = t.hist + s_max + 1;
+    t.misc = t.qrow + batch;
     return t;
 }
 
@@ -175,7 +178,7 @@ __device__ __forceinline__ bool merge_warp_loop(const DecodeArgs &a, const UnitT
     constexpr int RS = kMergeRow<D>;
     constexpr int V = D / 32;  // consecutive dims per lane
     static_assert(V == 2 || V == 4, "head_dim 64 or 128");
-    const int hkv = a.cache.num_kv_heads * a.head_groups, chunk = a.chunk;  // unit heads
+    const int hkv = a.cache.num_kv_heads * a.head_groups, chunk = ut.misc[0];  // unit heads; split size
     if (a.k_new && !a.cache.fp8) append_step_rows<D>(a, lane);
     int mbuf = 0;
     uint32_t mphase = 0;
@@ -255,15 +258,37 @@ __device__ __forceinline__ bool merge_warp_loop(const DecodeArgs &a, const UnitT
     }
 }
 
-// Prologue run by all kThreads threads of a CTA: clamp the lengths (flagging out-of-range ones)
-// and build the tables above. Returns the number of units; ends with __syncthreads.
+// Split size of an automatic split (DecodeArgs::auto_chunk): the host's chunk c0 (which sizes the
+// workspace: s_max splits of c0 at full capacity) or 1.5, 2, 3 or 4 times it, rounded up to the
+// 128-token split alignment, whichever minimises the modelled time of the launch: units are dealt
+// round-robin to the grid's CTAs, so a CTA runs about ceil(U / grid) units of up to c tokens, each
+// costing its tokens plus a fixed kUnitCostTokens (the unit's set-up, pipeline refill and partial
+// row). A larger split never needs more than s_max splits, so the workspace layout still holds.
+// Every CTA computes the same choice from the same lengths.
+constexpr int kSplitCandidates = 5;
+constexpr int kUnitCostTokens = 150;
+
+__device__ __forceinline__ int split_candidate(int c0, int k, int cap) {
+    const int m = k == 0 ? 2 : k == 1 ? 3 : k == 2 ? 4 : k == 3 ? 6 : 8;  // halves of c0
+    const long long c = ((long long)c0 * m / 2 + 127) / 128 * 128, top = ((long long)cap + 127) / 128 * 128;
+    return (int)(c < top ? c : top);  // at most the capacity (one split a context), rounded
+}
+
+// Prologue run by all kThreads threads of a CTA: clamp the lengths (flagging out-of-range ones),
+// choose the split size (automatic splits; misc[0], and *chunk_out from CTA 0 for the merge
+// kernel) and build the tables above. Returns the number of units; ends with __syncthreads.
 template <int kThreads>
 __device__ __forceinline__ int decode_scan_units(const DecodeArgs &a, const UnitTable &t) {
     const int tid = threadIdx.x, lane = tid & 31;
-    const int chunk = a.chunk, S = a.s_max;
+    const int S = a.s_max;
     const int cap = a.max_blocks_per_seq * a.cache.block_size;
+    const bool choose = a.auto_chunk && S > 1;
     for (int s = tid; s <= S; s += kThreads) t.hist[s] = 0;
+    if (tid < kUnitMisc) t.misc[tid] = 0;
     __syncthreads();
+    int cnt[kSplitCandidates];
+#pragma unroll
+    for (int k = 0; k < kSplitCandidates; ++k) cnt[k] = 0;
     for (int i = tid; i < a.batch; i += kThreads) {
         int len = __ldg(a.context_lens + i);
         if (len < 0 || len > cap) {
@@ -278,8 +303,46 @@ __device__ __forceinline__ int decode_scan_units(const DecodeArgs &a, const Unit
         }
         t.lens[i] = len;
         t.qrow[i] = qrow;
-        atomicAdd(&t.hist[(len + chunk - 1) / chunk], 1);  // split count <= S since len <= cap
+        if (choose) {
+#pragma unroll
+            for (int k = 0; k < kSplitCandidates; ++k) {
+                const int c = split_candidate(a.chunk, k, cap);
+                cnt[k] += len > 0 ? (len - 1) / c + 1 : 0;
+            }
+        }
     }
+    int chunk = a.chunk;
+    if (choose) {
+#pragma unroll
+        for (int k = 0; k < kSplitCandidates; ++k) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) cnt[k] += __shfl_xor_sync(0xffffffffu, cnt[k], o);
+            if (lane == 0 && cnt[k]) atomicAdd(&t.misc[1 + k], cnt[k]);
+        }
+        __syncthreads();
+        if (tid < 32) {
+            // lane k prices candidate k; the cheapest wins, the smaller split on a tie
+            const long long hu = (long long)a.cache.num_kv_heads * a.head_groups, grid = gridDim.x;
+            const int k = lane < kSplitCandidates ? lane : 0;
+            const int c = split_candidate(a.chunk, k, cap);
+            const long long units = (long long)t.misc[1 + k] * hu;
+            long long key = ((units + grid - 1) / grid * (long long)(min(c, cap) + kUnitCostTokens)) * 8 + k;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) key = min(key, __shfl_xor_sync(0xffffffffu, key, o));
+            if (lane == 0) {
+                const int best = split_candidate(a.chunk, (int)(key & 7), cap);
+                t.misc[0] = best;
+                if (blockIdx.x == 0 && a.chunk_out) *a.chunk_out = best;
+            }
+        }
+        __syncthreads();
+        chunk = t.misc[0];
+    } else if (tid == 0) {
+        t.misc[0] = chunk;
+        if (blockIdx.x == 0 && a.chunk_out) *a.chunk_out = chunk;
+    }
+    for (int i = tid; i < a.batch; i += kThreads)
+        atomicAdd(&t.hist[(t.lens[i] + chunk - 1) / chunk], 1);  // split count <= S since len <= cap
     __syncthreads();
     if (tid < 32) {
         // n_s = batch - (sequences with at most s splits); first[s + 1] = first[s] + n_s

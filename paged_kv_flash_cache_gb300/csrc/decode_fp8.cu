@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const UnitTable ut = unit_table(reinterpret_cast<int *>(smem + L::kIntsOffset), a.batch, a.s_max);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int hkv = a.cache.num_kv_heads, bs = a.cache.block_size, chunk = a.chunk;
+    const int hkv = a.cache.num_kv_heads, bs = a.cache.block_size;
     const int hu = hkv * a.head_groups;  // unit heads (KV heads, or groups of 8 query heads)
     // a tile is copied in slices of br = min(bs, 64) rows: tiles start at multiples of 64 tokens,
     // so every slice lies inside one page whatever the page size
@@ -145,6 +145,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
     pdl_wait();  // lengths, tables, q and the cache may come from the previous kernel
     const int num_units = decode_scan_units<kThreads>(a, ut);
+    const int chunk = ut.misc[0];  // the launch's split size
 
     if (warp == kProducerWarp) {
         // ===================================== producer warp =====================================

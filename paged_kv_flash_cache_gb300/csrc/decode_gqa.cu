@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(GqaWarps<G>::kThreads, kCtasPerSm)
     const UnitTable ut = unit_table(reinterpret_cast<int *>(base + L::ints_offset(nst)), a.batch, a.s_max);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int hkv = a.cache.num_kv_heads, bs = a.cache.block_size, chunk = a.chunk;
+    const int hkv = a.cache.num_kv_heads, bs = a.cache.block_size;
     const int hu = hkv * a.head_groups;  // unit heads (KV heads, or groups of query heads)
     const int br = bs < kTile ? bs : kTile;  // rows per page slice (tiles start at multiples of 64)
 
@@ -147,6 +147,7 @@ __global__ void __launch_bounds__(GqaWarps<G>::kThreads, kCtasPerSm)
     }
     pdl_wait();  // lengths, tables, q and the cache may come from the previous kernel
     const int num_units = decode_scan_units<W::kThreads>(a, ut);
+    const int chunk = ut.misc[0];  // the launch's split size
 
     if (warp == W::kProducer) {
         // ===================================== producer warp =====================================

@@ -142,7 +142,6 @@ __global__ void __launch_bounds__(kThreads, kCtas)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_sm = kM == 64 ? (gu + 15) >> 4 : (gu + 31) >> 5;  // softmax warps with head rows
-    const int chunk = a.chunk;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < ring; ++i) {
@@ -168,6 +167,7 @@ __global__ void __launch_bounds__(kThreads, kCtas)
     tc::fence_before_sync();
     pdl_wait();  // lengths, tables, q and the cache may come from the previous kernel
     const int num_units = decode_scan_units<kThreads>(a, ut);  // ends with __syncthreads
+    const int chunk = ut.misc[0];  // the launch's split size
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 

@@ -202,6 +202,11 @@ int pkv_decode_split_tokens(int batch, int num_q_heads, int num_kv_heads, int he
     return split_tokens(batch, num_kv_heads, block_size, max_blocks_per_seq, num_splits);
 }
 
+static size_t partial_bytes(int batch, int num_q_heads, long long s_max, int head_dim) {
+    const size_t b = (size_t)batch * num_q_heads * s_max * (head_dim + 1) * sizeof(float);
+    return (b + 15) & ~(size_t)15;
+}
+
 size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                                  int max_blocks_per_seq, int num_splits) {
     if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
@@ -211,7 +216,9 @@ size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads, i
     const int chunk = split_tokens(batch, num_kv_heads, block_size, max_blocks_per_seq, num_splits);
     const long long s_max = (cap + chunk - 1) / chunk;
     if (s_max <= 1) return 0;
-    return (size_t)batch * num_q_heads * s_max * (head_dim + 1) * sizeof(float);
+    // FP32 partials [batch, Hq, s_max, D] and their lse [batch, Hq, s_max], padded to 16 bytes, then
+    // one 16-byte slot: the split size the split kernel took (read by the merge kernel)
+    return partial_bytes(batch, num_q_heads, s_max, head_dim) + 16;
 }
 
 }  // extern "C"
@@ -259,6 +266,9 @@ pkv_status decode_impl(const pkv_cache &cache, const void *q, int num_q_heads, c
     a.max_blocks_per_seq = max_blocks_per_seq;
     a.scale = scale;
     a.chunk = chunk;
+    a.chunk_out = need > 0 ? reinterpret_cast<int *>(static_cast<uint8_t *>(workspace) +
+                                                     partial_bytes(batch, num_q_heads, s_max, cache.head_dim))
+                           : nullptr;
     a.q_rows = q_rows;
     a.s_max = s_max;
     a.stages = 0;  // set by the group kernel's launcher
@@ -286,6 +296,11 @@ pkv_status decode_impl(const pkv_cache &cache, const void *q, int num_q_heads, c
             if (group % d == 0) per_unit = d;
     }
     a.head_groups = group / per_unit;
+    // The tcgen05 units (many query heads each) run below the memory roofline, so how evenly the
+    // units divide over the CTAs sets their time: with an automatic split the kernel picks the split
+    // size from the lengths (decode_scan_units). The other paths stream at the copy rate, where the
+    // host's split measured best; a requested split count is kept as given.
+    a.auto_chunk = (num_splits == 0 && path == kTcgen05) ? 1 : 0;
     a.cu_q_lens = cu_q_lens;
     a.part_o = static_cast<float *>(workspace);
     a.part_lse = need > 0 ? a.part_o + (size_t)batch * num_q_heads * s_max * cache.head_dim : nullptr;
@@ -305,9 +320,9 @@ pkv_status decode_impl(const pkv_cache &cache, const void *q, int num_q_heads, c
     // workspace layout [batch, Hq, s_max, ...] are the whole batch's; a slice's partials start at
     // its first sequence's). A mixed batch's rows are absolute (cu_q_lens), so only cu_q_lens moves.
     const size_t qe = 2, oe = out_dtype == PKV_F32 ? 4 : 2;  // element sizes of q and out
-    // sequences a launch: at most decode_max_batch(), and unit tables (3 ints a sequence, 2 a split)
+    // sequences a launch: at most decode_max_batch(), and unit tables (3 ints a sequence, 2 a split, 8 more)
     // of at most 24 KB, which every decode kernel's shared-memory layout leaves room for
-    int slice = (6144 - 2 * (s_max + 1)) / 3;
+    int slice = (6144 - 2 * (s_max + 1) - kUnitMisc) / 3;
     slice = slice < 1 ? 1 : (slice > decode_max_batch() ? decode_max_batch() : slice);
     for (int b0 = 0; b0 < batch; b0 += slice) {
         const int nb = batch - b0 < slice ? batch - b0 : slice;
@@ -350,6 +365,7 @@ pkv_status decode_impl(const pkv_cache &cache, const void *q, int num_q_heads, c
         c.context_lens = d.context_lens;
         c.rows_per_seq = num_q_heads;
         c.chunk = chunk;
+        c.chunk_dev = a.auto_chunk ? a.chunk_out : nullptr;  // the kernel's own choice, else chunk
         c.cu_q_lens = d.cu_q_lens;
         c.out = d.out;
         c.out_dtype = (int)out_dtype;
@@ -423,6 +439,7 @@ pkv_status pkv_attn_combine(const float *partial_o, const float *partial_lse, in
     c.cu_q_lens = nullptr;
     c.rows_per_seq = 1;
     c.chunk = 1;
+    c.chunk_dev = nullptr;
     c.out = out;
     c.out_dtype = (int)out_dtype;
     c.lse = lse;

@@ -40,7 +40,9 @@ struct DecodeArgs {
     const int *block_tables, *context_lens;
     int batch, max_blocks_per_seq;
     float scale;
-    int chunk;   // tokens per split (multiple of the decode tile)
+    int chunk;   // tokens per split (multiple of the decode tile); with auto_chunk the smallest
+    int auto_chunk;  // 1: the kernel may take 1.5 - 4 times chunk (decode_scan_units), 0: chunk
+    int *chunk_out;  // where CTA 0 stores the split size it took (for the merge kernel), or nullptr
     // Units per KV head when a KV head serves more query heads than one unit holds (the native
     // group kernel holds 32 (head_dim 128), 16 or 8, the largest that divides the group; the FP8
     // kernel 8; MQA, wide groups), else 1:
@@ -72,6 +74,7 @@ struct CombineArgs {
     // splits; rows with exactly one split were finished by the decode kernel.
     const int *context_lens;
     int rows_per_seq, chunk;
+    const int *chunk_dev;  // the split size the split kernel chose (read after it completes), or nullptr: chunk
     // mixed batch: row r = b * rows_per_seq + h goes to output row cu_q_lens[b] * rows_per_seq + h,
     // and only for sequences with exactly one query row (nullptr: output row r)
     const int *cu_q_lens;
@@ -149,6 +152,7 @@ int *device_error_word();  // the current device's sticky error word (device add
 constexpr int kDecodeTile = 64;         // tokens per decode pipeline stage
 constexpr int kSplitAlign = 128;        // decode splits start at multiples of this many tokens
 constexpr int kDecodeMaxSplits = 2048;  // splits of one context (bounds the split size from below)
+constexpr int kUnitMisc = 8;           // ints of a decode CTA's unit table beyond its per-sequence and per-split parts
 
 cudaError_t launch_append(const AppendArgs &a, cudaStream_t s);
 cudaError_t encode_cache_map(const CacheView &c, int box_rows, CUtensorMap *map);

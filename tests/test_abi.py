@@ -128,9 +128,13 @@ def test_selftest_rejects_bad_limits_without_gpu(lib):
 def test_workspace_sizing_with_explicit_splits(lib):
     # capacity 4 * 16 = 64 tokens in 1 split: no workspace
     assert pkv.decode_workspace_size(2, 4, 4, 128, 16, 4, num_splits=1) == 0
-    # capacity 512 * 16 = 8192 tokens in 4 splits of 2048: B * Hq * 4 * (D + 1) floats
+    # capacity 512 * 16 = 8192 tokens in 4 splits of 2048: B * Hq * 4 * (D + 1) floats, then a
+    # 16-byte slot (the split size the split kernel took)
     assert pkv.decode_split_tokens(16, 32, 32, 128, 16, 512, num_splits=4) == 2048
-    assert pkv.decode_workspace_size(16, 32, 32, 128, 16, 512, num_splits=4) == 16 * 32 * 4 * 129 * 4
+    assert pkv.decode_workspace_size(16, 32, 32, 128, 16, 512, num_splits=4) == 16 * 32 * 4 * 129 * 4 + 16
+    # the partials are padded to 16 bytes before the slot: 1 * 1 * 2 * 65 floats = 520 -> 528
+    assert pkv.decode_split_tokens(1, 1, 1, 64, 16, 16, num_splits=2) == 128
+    assert pkv.decode_workspace_size(1, 1, 1, 64, 16, 16, num_splits=2) == 528 + 16
     # split size is rounded up to 128 tokens (splits start at multiples of 128)
     assert pkv.decode_split_tokens(1, 8, 8, 64, 16, 10, num_splits=3) == 128
 

@@ -120,8 +120,12 @@ int split_tokens(int batch, int num_kv_heads, int block_size, int max_blocks_per
         const DeviceInfo &d = s ? s->info : kNoDevice;
         const long long ctas = (long long)d.num_sms * d.decode_ctas_per_sm;
         const long long want = (long long)batch * num_kv_heads * cap / (ctas * 8 > 0 ? ctas * 8 : 1);
-        c = 512;
-        while (c > 128 && c > want) c >>= 1;
+        // the largest of these at or below want (at least 128): 768-token splits measured best on
+        // the streaming paths (7B-like, FP8 and mixed batches against 512, 640 and 1024)
+        static const int kSizes[] = {768, 512, 384, 256, 128};
+        int i = 0;
+        while (kSizes[i] > 128 && kSizes[i] > want) ++i;
+        c = kSizes[i];
     }
     const long long floor_c = (cap + kDecodeMaxSplits - 1) / kDecodeMaxSplits;
     if (c < floor_c) c = floor_c;

@@ -282,7 +282,8 @@ __device__ __forceinline__ int decode_scan_units(const DecodeArgs &a, const Unit
     const int tid = threadIdx.x, lane = tid & 31;
     const int S = a.s_max;
     const int cap = a.max_blocks_per_seq * a.cache.block_size;
-    const bool choose = a.auto_chunk && S > 1;
+    // (the largest candidate, the capacity rounded up to 128, keeps len + chunk - 1 within int)
+    const bool choose = a.auto_chunk && S > 1 && cap <= (1 << 30) - 128;
     for (int s = tid; s <= S; s += kThreads) t.hist[s] = 0;
     if (tid < kUnitMisc) t.misc[tid] = 0;
     __syncthreads();

@@ -381,3 +381,62 @@ def test_decode_step_full_table_is_flagged_and_skipped(hq, hkv):
     assert pkv.get_device_error() == 5
     assert torch.equal(out, ref_out)
     assert np.array_equal(cache_bits(cache), ref_bits)
+
+
+def _chosen_split(ws, need):
+    # the split kernel leaves the split size it took in the workspace's last 16-byte slot
+    return int(ws[need - 16:need - 12].view(torch.int32).item())
+
+
+def _model_split(lens, c0, cap, unit_heads, grid):
+    """The device's choice restated: the host split c0 or 1.5, 2, 3, 4 times it (rounded up to 128,
+    at most the capacity rounded up), whichever minimises ceil(units / grid) * (split + 150)."""
+    top = (cap + 127) // 128 * 128
+    best = None
+    for k, m in enumerate((2, 3, 4, 6, 8)):
+        c = min((c0 * m // 2 + 127) // 128 * 128, top)
+        units = sum((L - 1) // c + 1 for L in lens if L > 0) * unit_heads
+        key = (-(-units // grid) * (min(c, cap) + 150), k)
+        if best is None or key < best[0]:
+            best = (key, c)
+    return best[1]
+
+
+@pytest.mark.parametrize("batch,lo,hi,seed", [(128, 1024, 8192, 1241), (64, 2048, 16384, 3), (256, 512, 4096, 4)])
+def test_decode_split_chosen_on_device(batch, lo, hi, seed):
+    """Multi-query decode (32 query heads on one KV head, the tcgen05 path with two CTAs an SM)
+    with an automatic split: the split kernel picks the split size from the lengths. The choice
+    matches the model restated here, and the result is bit for bit the decode with that split
+    requested explicitly."""
+    gen = torch.Generator().manual_seed(seed)
+    lens = torch.randint(lo, hi + 1, (batch,), generator=gen).tolist()
+    bs = 16
+    nb = sum((L + bs - 1) // bs for L in lens)
+    p = W.make_problem("m", batch=batch, num_q_heads=32, num_kv_heads=1, head_dim=128, block_size=bs,
+                       context_lens=lens, q_lens=[1] * batch, dtype=W.BF16, causal=False, seed=seed + 1,
+                       num_blocks=nb, free_order=torch.randperm(nb, generator=gen).tolist())
+    cache = device_cache(p)
+    q, bt, ctx = to_dev(p.q), to_dev(p.block_tables), to_dev(p.context_lens)
+    mb = bt.shape[1]
+    cap = mb * bs
+    need = pkv.decode_workspace_size(batch, 32, 1, 128, bs, mb)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    lse = torch.empty((batch, 32), dtype=torch.float32, device="cuda")
+    out = pkv.paged_attn_decode(cache, q, bt, ctx, scale=p.scale, workspace=ws, lse=lse)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    chosen = _chosen_split(ws, need)
+    c0 = pkv.decode_split_tokens(batch, 32, 1, 128, bs, mb)
+    grid = 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    assert chosen == _model_split(lens, c0, cap, 1, grid), (chosen, c0)
+    assert chosen >= c0 and chosen % 128 == 0
+    # the same split requested (a split count whose split size is the chosen one, where one exists)
+    ns = next((n for n in range(1, 2049) if pkv.decode_split_tokens(batch, 32, 1, 128, bs, mb, n) == chosen), None)
+    if ns is not None:
+        lse2 = torch.empty_like(lse)
+        out2 = pkv.paged_attn_decode(cache, q, bt, ctx, scale=p.scale, num_splits=ns, lse=lse2)
+        torch.cuda.synchronize()
+        assert torch.equal(out, out2) and torch.equal(lse, lse2)
+    ref, ref_lse = oracle.attention_of(p, cache_bits(cache))
+    check_close(out, ref, W.BF16, roundings=1, what="split chosen on the device (%d tokens)" % chosen)
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-5, atol=1e-5)

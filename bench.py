@@ -52,7 +52,7 @@ def parse():
                          "samples")
     ap.add_argument("--only", default="", help="comma list of extra workloads (bs_sweep,mixed,prefix,fp8,mqa,mixed_call,prefill,prefill_fp8)")
     ap.add_argument("--profile", choices=["decode", "append", "prefill", "decode_mixed", "decode_prefix", "decode_fp8",
-                                          "prefill_fp8", "decode_mqa", "prefill_d256"],
+                                          "prefill_fp8", "decode_mqa", "prefill_d256", "append_chunk"],
                     default=None,
                     help="small case for ncu captures: W + K launches of one kernel, nothing else timed")
     return ap.parse_args()
@@ -132,6 +132,21 @@ def profile_case(args):
         out = torch.empty((p.batch, 32, 128), dtype=torch.float16, device="cuda")
         for _ in range(args.warmup + args.steps):
             pkv.paged_attn_decode(cache, q, bt, ctx, scale=p.scale, out=out)
+        torch.cuda.synchronize()
+        assert pkv.get_device_error() == 0
+    elif args.profile == "append_chunk":
+        # one chunk's append of the long prefill pass: 4 sequences x 512 new tokens, 32 KV heads x 128,
+        # bf16 (33.5 MB of K/V in, the same out into their pages)
+        p = W.prefill_long(device="cuda")
+        shape = (p.num_blocks, 2, p.num_kv_heads, p.block_size, p.head_dim)
+        cache = torch.zeros(shape, dtype=p.q.dtype, device="cuda")
+        bt = p.block_tables.cuda()
+        v = W.prefill_chunk_view(p, 15)
+        rows = v["rows"].cuda()
+        k, vv = p.k_ctx[rows].contiguous(), p.v_ctx[rows].contiguous()
+        cu, before = v["cu_q_lens"].cuda(), v["ctx_before"].cuda()
+        for _ in range(args.warmup + args.steps):
+            pkv.kv_cache_append(cache, k, vv, cu, before, bt)
         torch.cuda.synchronize()
         assert pkv.get_device_error() == 0
     elif args.profile == "prefill_d256":

@@ -440,3 +440,25 @@ def test_decode_split_chosen_on_device(batch, lo, hi, seed):
     ref, ref_lse = oracle.attention_of(p, cache_bits(cache))
     check_close(out, ref, W.BF16, roundings=1, what="split chosen on the device (%d tokens)" % chosen)
     np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-5, atol=1e-5)
+
+
+@pytest.mark.parametrize("hq,hkv", [(2, 2), (8, 2)])
+def test_decode_step_batch_slices(hq, hkv):
+    """A decode step over more sequences than one launch's unit tables hold (the call runs in
+    slices): every slice's split kernel appends its own sequences' new rows."""
+    gen = torch.Generator().manual_seed(21)
+    lens = torch.randint(0, 70, (2500,), generator=gen).tolist()
+    p = problem(lens=lens, hq=hq, hkv=hkv, d=64, dtype=W.F16, bs=16, mb=8, seed=22, extra=2600)
+    step = W.append_step(p, seed=23)
+    cache = device_cache(p)
+    q, bt, ctx = to_dev(p.q), to_dev(step["block_tables"]), to_dev(p.context_lens)
+    ref_out = pkv.paged_attn_decode(cache, q, bt, ctx, scale=p.scale)
+    torch.cuda.synchronize()
+    ref_bits = cache_bits(cache)
+    assert oracle.kv_cache_append(ref_bits, step["k_new"], step["v_new"], step["cu_new_lens"], step["ctx_before"],
+                                  step["block_tables"]) == 0
+    out = pkv.paged_attn_decode_step(cache, q, bt, ctx, to_dev(step["k_new"]), to_dev(step["v_new"]), scale=p.scale)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    assert torch.equal(out, ref_out)
+    assert np.array_equal(cache_bits(cache), ref_bits)

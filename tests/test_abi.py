@@ -139,6 +139,22 @@ def test_workspace_sizing_with_explicit_splits(lib):
     assert pkv.decode_split_tokens(1, 8, 8, 64, 16, 10, num_splits=3) == 128
 
 
+def test_automatic_split_size_without_gpu(lib):
+    # The automatic split is the largest of 768, 512, 384, 256, 128 tokens at or below
+    # B * Hkv * capacity / (8 * CTAs); with no device in this process the CTA count is 0, so the
+    # rule gives its largest size. A context has at most 2048 splits: a 4M-token capacity needs
+    # splits of at least 2048 tokens.
+    if not hasattr(lib, "pkv_decode_split_tokens"):
+        pytest.skip("library without the split query")
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("the no-device rule; on a GPU the SM count enters")
+    assert pkv.decode_split_tokens(16, 32, 32, 128, 16, 512) == 768
+    assert pkv.decode_split_tokens(1, 1, 1, 128, 16, 1 << 18) == 2048
+    # and the workspace follows the split: B * Hq * ceil(8192 / 768) * (D + 1) floats, then the slot
+    assert pkv.decode_workspace_size(16, 32, 32, 128, 16, 512) == 16 * 32 * 11 * 129 * 4 + 16
+
+
 def test_device_slot_from_eight_threads(lib):
     """The per-device state behind every entry point is set up by whichever call comes first;
     eight threads calling at once (ctypes releases the GIL during each call) must all see the

@@ -59,6 +59,35 @@ def test_decode_7b_full_size_every_row():
     check_workload(W.decode_7b(), "7B decode")
 
 
+def test_decode_7b_step_full_size_every_row():
+    """The step the benchmark times: paged_attn_decode_step over the same 7B-like batch (attention
+    over every context, the step's token appended at position context_lens[b] by the split kernel),
+    with the benchmark's workspace and output: every output row against the oracle, and the whole
+    pool bit for bit against the oracle's append of the step's tokens."""
+    p = W.decode_7b()
+    cache = device_cache(p)
+    torch.cuda.synchronize()
+    bits = cache_bits(cache)
+    assert np.array_equal(bits, oracle.build_cache(p))
+    step = W.append_step(p, seed=7)
+    bt, ctx, q = step["block_tables"].cuda(), p.context_lens.cuda(), p.q.cuda()
+    ws_bytes = pkv.decode_workspace_size(p.batch, p.num_q_heads, p.num_kv_heads, p.head_dim, p.block_size,
+                                         bt.shape[1])
+    ws = torch.empty(max(16, ws_bytes), dtype=torch.uint8, device="cuda")
+    out = torch.empty((p.batch, p.num_q_heads, p.head_dim), dtype=q.dtype, device="cuda")
+    lse = torch.empty((p.batch, p.num_q_heads), dtype=torch.float32, device="cuda")
+    pkv.paged_attn_decode_step(cache, q, bt, ctx, step["k_new"].cuda(), step["v_new"].cuda(), scale=p.scale,
+                               workspace=ws, out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    ref, ref_lse = oracle.attention_of(p, bits)
+    check_close(out, ref, p.dtype, roundings=1, what="7B decode step")
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-5, atol=1e-5)
+    assert oracle.kv_cache_append(bits, step["k_new"], step["v_new"], step["cu_new_lens"], step["ctx_before"],
+                                  step["block_tables"]) == 0
+    assert np.array_equal(cache_bits(cache), bits), "7B decode step: cache differs from the oracle's append"
+
+
 @pytest.mark.parametrize("bs", [8, 16, 32, 64, 128, 512])
 def test_block_size_sweep_full_size_every_row(bs):
     """32 sequences x 4096 tokens, 32 heads x 128, fp16: the same token data through every page size."""

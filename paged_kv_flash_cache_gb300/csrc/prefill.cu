@@ -38,6 +38,7 @@
 
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
+#include "prefill_common.cuh"
 #include "tcgen05.cuh"
 
 namespace pkv {
@@ -285,9 +286,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // grid (heads, batch, row blocks) with the row blocks last-first: CTAs start in linear order, so
     // the row blocks that see the most keys (causal) start in the first wave and the short ones
-    // fill in behind them
-    const int mt = (int)gridDim.z - 1 - (int)blockIdx.z, h = blockIdx.x, b = blockIdx.y;
+    // fill in behind them. A mixed batch: (heads, row blocks last-first, sequences by their rank
+    // among those with several query rows), so that no CTA without work precedes one with work.
+    const int h = blockIdx.x;
+    const int mt = p.skip_single ? (int)gridDim.y - 1 - (int)blockIdx.y : (int)gridDim.z - 1 - (int)blockIdx.z;
     pdl_wait();  // lengths, tables, q and the chunk's own K/V may come from the previous kernel
+    const int b = p.skip_single ? nth_multi_row_sequence(p.cu_q_lens, p.batch, blockIdx.z) : (int)blockIdx.y;
+    if (b < 0) return;  // uniform: past the mixed batch's last chunk
     const int q0 = __ldg(p.cu_q_lens + b);
     const int q_len = __ldg(p.cu_q_lens + b + 1) - q0;
     const int m_start = mt * kRows;
@@ -971,7 +976,8 @@ cudaError_t launch_t(const PrefillArgs &a, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         configured.set(dev);
     }
-    dim3 grid(a.num_q_heads, a.batch, (a.max_q_len + kRows - 1) / kRows);
+    const unsigned row_blocks = (unsigned)((a.max_q_len + kRows - 1) / kRows);
+    const dim3 grid = a.skip_single ? dim3(a.num_q_heads, row_blocks, a.batch) : dim3(a.num_q_heads, a.batch, row_blocks);
     return launch_pdl(kern, grid, dim3(kThreads), Lay::kSmemBytes, stream, tm_q, tm_kv, p);
 }
 

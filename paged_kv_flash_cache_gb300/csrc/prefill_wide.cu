@@ -25,6 +25,7 @@
 
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
+#include "prefill_common.cuh"
 #include "tcgen05.cuh"
 #include "warp_mma.cuh"
 
@@ -52,7 +53,7 @@ constexpr uint32_t kSmemBytes = kBarOff + 256 + 1024;  // + 1024-byte alignment 
 
 struct WideParams {
     const int *cu_q_lens, *context_lens, *block_tables;
-    int mb, num_q_heads, num_kv_heads, group, bs, log2_bs, num_blocks;
+    int batch, mb, num_q_heads, num_kv_heads, group, bs, log2_bs, num_blocks;
     float scale_log2;
     int causal, skip_single;
     void *out;
@@ -94,8 +95,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // grid (heads, row blocks, sequences), row blocks last-first: CTAs start in linear order, so the
     // CTAs running together share one sequence's K/V (it stays in L2), and within it the blocks that
     // see the most keys (causal) start first
-    const int mt = (int)gridDim.y - 1 - (int)blockIdx.y, h = blockIdx.x, b = blockIdx.z;
+    // (a mixed batch: sequences by their rank among those with several query rows, so that no CTA
+    // without work precedes one with work)
+    const int mt = (int)gridDim.y - 1 - (int)blockIdx.y, h = blockIdx.x;
     pdl_wait();  // lengths, tables, q and the chunk's own K/V may come from the previous kernel
+    const int b = p.skip_single ? nth_multi_row_sequence(p.cu_q_lens, p.batch, blockIdx.z) : (int)blockIdx.z;
+    if (b < 0) return;  // uniform: past the mixed batch's last chunk
     const int q0 = __ldg(p.cu_q_lens + b);
     const int q_len = __ldg(p.cu_q_lens + b + 1) - q0;
     const int m_start = mt * kBM;
@@ -385,6 +390,7 @@ cudaError_t launch_wide_t(const PrefillArgs &a, cudaStream_t stream) {
     p.cu_q_lens = a.cu_q_lens;
     p.context_lens = a.context_lens;
     p.block_tables = a.block_tables;
+    p.batch = a.batch;
     p.mb = a.max_blocks_per_seq;
     p.num_q_heads = a.num_q_heads;
     p.num_kv_heads = a.cache.num_kv_heads;
